@@ -1,0 +1,59 @@
+// conv_b200_internal.h -- declarations shared by the library's translation
+// units (never installed; the public ABI is include/conv_b200.h).
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/conv_b200.h"
+
+namespace cb200 {
+
+// Bits of the device error word.
+constexpr int kDevErrTimeout = 1;
+
+// The device error word lives in device memory (one per device, file scope in
+// api.cu); kernels receive its address.
+int* device_error_word();
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+inline cudaStream_t as_cuda(conv_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------------------
+// Launchers implemented in the .cu files (return cudaError_t of the launch).
+
+struct ConvDims {
+    int N, C, H, W, K, R, S, P, Q;   // K = outC, R = kH, S = stride, P/Q = outH/outW
+    int pad;
+};
+
+cudaError_t launch_conv_fwd(const ConvDims& d, const float* x, const float* w, const float* b, float* y,
+                            void* ws, cudaStream_t st);
+size_t conv_fwd_ws(const ConvDims& d);
+
+cudaError_t launch_conv_dgrad(const ConvDims& d, const float* w, const float* dy, float* dx, void* ws,
+                              cudaStream_t st);
+size_t conv_dgrad_ws(const ConvDims& d);
+
+cudaError_t launch_conv_wgrad(const ConvDims& d, const float* x, const float* dy, float* dw, void* ws,
+                              cudaStream_t st);
+size_t conv_wgrad_ws(const ConvDims& d);
+
+cudaError_t launch_matmul(int M, int K, int N, unsigned flags, const float* A, const float* B, float* C,
+                          cudaStream_t st);
+
+cudaError_t launch_bias_grad(const ConvDims& d, const float* dy, float* db, cudaStream_t st);
+cudaError_t launch_im2col(const ConvDims& d, const float* x, float* col, cudaStream_t st);
+cudaError_t launch_col2im(const ConvDims& d, const float* col, float* dx, cudaStream_t st);
+cudaError_t launch_maxpool_fwd(int N, int C, int H, int W, int k, int s, int P, int Q, const float* x, float* y,
+                               int32_t* idx, cudaStream_t st);
+cudaError_t launch_maxpool_bwd(int N, int C, int H, int W, int k, int s, int P, int Q, const float* dy,
+                               const int32_t* idx, float* dx, cudaStream_t st);
+cudaError_t launch_sgd(int64_t count, float lr, float clip, float* p, const float* g, cudaStream_t st);
+
+}  // namespace cb200

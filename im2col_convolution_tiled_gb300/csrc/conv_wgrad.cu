@@ -1,0 +1,251 @@
+// conv_wgrad.cu -- filter gradient of the page "DirectCompute Neural Network
+// Engine", section "Convolution: The im2col Approach" (backward: grad_reshaped
+// x im2col_matrix^T), as an implicit GEMM on the tcgen05 tensor cores:
+//
+//   dW[k, crs] = sum_j G[k, j] * col[crs, j],   j = (n, oh, ow)
+//
+// Rows of the accumulator are filter taps crs (A = the column matrix,
+// regathered from x), columns are filters k (B = G, read straight from dy in
+// NCHW: conv_grad_reshape is only an index map).  The reduction over j is long
+// (batch*outH*outW) and the output small, so j is split into contiguous ranges
+// spread over the SMs; each range writes its own partial tile and a second
+// kernel adds the partials in range order -- a fixed summation order, so the
+// result is deterministic.  Each range's tensor-core accumulation chain is
+// bounded by its length.
+//
+// Both operands are gathered ChunkFast: a thread holds 4 consecutive j of 8
+// rows, so 8 lanes read 32 consecutive pixels of one row.
+#include "conv_common.cuh"
+
+namespace cb200 {
+
+template <int BN>
+struct ConvWgradProb {
+    static constexpr bool kBBulk = false;
+    static constexpr Map kAMap = Map::ChunkFast;
+    static constexpr Map kBMap = Map::ChunkFast;
+
+    const float* x;
+    const float* dy;
+    float* out;   // dW (splits == 1) or partials [split][K][CRS]
+    int C, H, W, K, R, S, pad, P, Q;
+    int PQ, NPQ, CRS, HW, CHW;
+    FastDiv f_pq, f_q, f_rr, f_r;
+    int m_tiles, n_tiles, k_stages, splits, ks_per_split;
+
+    __device__ int num_tiles() const { return m_tiles * n_tiles * splits; }
+    __device__ Tile tile(int t) const
+    {
+        const int mn = m_tiles * n_tiles;
+        const int split = t / mn;
+        const int rem = t % mn;
+        Tile r;
+        r.n0 = (rem % n_tiles) * BN;
+        r.m0 = (rem / n_tiles) * kBM;
+        r.ks0 = split * ks_per_split;
+        r.ks1 = min(r.ks0 + ks_per_split, k_stages);
+        r.grp = split;
+        return r;
+    }
+
+    // Rows (taps) of this thread: (tid / 8) + 16 p.
+    struct AState {
+        int rowoff[8];   // c*H*W + r*W + q
+        int rq[8];       // (r << 16) | q, or a sentinel that is never inside
+    };
+    __device__ AState a_setup(const Tile& tl, int tid) const
+    {
+        AState s;
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            const int crs = tl.m0 + (tid >> 3) + 16 * p;
+            if (crs < CRS) {
+                uint32_t c, rem, r, q;
+                f_rr.divmod(uint32_t(crs), c, rem);
+                f_r.divmod(rem, r, q);
+                s.rowoff[p] = int(c) * HW + int(r) * W + int(q);
+                s.rq[p] = int((r << 16) | q);
+            } else {
+                s.rowoff[p] = 0;
+                s.rq[p] = 0x7FFF0000;
+            }
+        }
+        return s;
+    }
+
+    __device__ void load_a(const AState& s, const Tile&, int ks, int tid, float (&v)[32]) const
+    {
+        // Pixels j0..j0+3 of this thread's chunk.
+        const int j0 = ks * kBK + 4 * (tid & 7);
+        int jbase[4], jh[4], jw[4];
+        {
+            uint32_t n, pq, oh, ow;
+            f_pq.divmod(uint32_t(j0 < NPQ ? j0 : 0), n, pq);
+            f_q.divmod(pq, oh, ow);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (j0 + e < NPQ) {
+                    jh[e] = int(oh) * S - pad;
+                    jw[e] = int(ow) * S - pad;
+                    jbase[e] = int(n) * CHW + jh[e] * W + jw[e];
+                } else {
+                    jh[e] = -(1 << 24);
+                    jw[e] = 0;
+                    jbase[e] = 0;
+                }
+                if (++ow == uint32_t(Q)) {
+                    ow = 0;
+                    if (++oh == uint32_t(P)) { oh = 0; ++n; }
+                }
+            }
+        }
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int h = jh[e] + (s.rq[p] >> 16);
+                const int w = jw[e] + (s.rq[p] & 0xFFFF);
+                v[4 * p + e] =
+                    (unsigned(h) < unsigned(H) && unsigned(w) < unsigned(W)) ? __ldg(x + (jbase[e] + s.rowoff[p])) : 0.f;
+            }
+        }
+    }
+
+    struct BState {};
+    __device__ BState b_setup(const Tile&, int) const { return {}; }
+
+    __device__ void load_b(const BState&, const Tile& tl, int ks, int pass, int tid, float (&v)[32]) const
+    {
+        const int j0 = ks * kBK + 4 * (tid & 7);
+        int dbase[4];
+        bool jv[4];
+        {
+            uint32_t n, pq;
+            f_pq.divmod(uint32_t(j0 < NPQ ? j0 : 0), n, pq);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                jv[e] = j0 + e < NPQ;
+                dbase[e] = int(n) * K * PQ + int(pq);
+                if (++pq == uint32_t(PQ)) { pq = 0; ++n; }
+            }
+        }
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            const int k = tl.n0 + 128 * pass + (tid >> 3) + 16 * p;
+            const bool kv = k < K;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[4 * p + e] = (kv && jv[e]) ? __ldg(dy + (dbase[e] + k * PQ)) : 0.f;
+        }
+    }
+
+    __device__ const float* b_image(const Tile&, int) const { return nullptr; }
+
+    struct EState {
+        float* o;   // out + crs, filter stride CRS
+        bool valid;
+    };
+    __device__ EState e_setup(const Tile& tl, int row) const
+    {
+        EState e;
+        const int crs = tl.m0 + row;
+        e.valid = crs < CRS;
+        e.o = out + size_t(tl.grp) * K * CRS + (e.valid ? crs : 0);
+        return e;
+    }
+
+    __device__ void store(const EState& e, const Tile& tl, int, int c, const uint32_t (&r)[32]) const
+    {
+        if (!e.valid) return;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int k = tl.n0 + c + i;
+            if (k < K) e.o[size_t(k) * CRS] = __uint_as_float(r[i]);
+        }
+    }
+};
+
+// dW[i] = sum over split s (ascending) of part[s][i].
+__global__ void wgrad_reduce_kernel(const float* __restrict__ part, int splits, long long count, float* __restrict__ dw)
+{
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < count;
+         i += (long long)gridDim.x * blockDim.x) {
+        float acc = 0.f;
+        for (int s = 0; s < splits; ++s) acc += __ldg(part + s * count + i);
+        dw[i] = acc;
+    }
+}
+
+struct WgradPlan {
+    int bn, m_tiles, n_tiles, k_stages, splits, ks_per_split;
+};
+
+static WgradPlan plan_wgrad(const ConvDims& d)
+{
+    WgradPlan pl;
+    pl.bn = pick_conv_bn(d.K, &pl.n_tiles);
+    const int CRS = d.C * d.R * d.R;
+    const long long NPQ = (long long)d.N * d.P * d.Q;
+    pl.m_tiles = (CRS + kBM - 1) / kBM;
+    pl.k_stages = int((NPQ + kBK - 1) / kBK);
+    const int mn = pl.m_tiles * pl.n_tiles;
+    int splits = (sm_count() + mn / 2) / mn;       // about one tile per SM
+    const int min_stages = 16;                     // keep each range worth a tile
+    if (splits > pl.k_stages / min_stages) splits = pl.k_stages / min_stages;
+    if (splits < 1) splits = 1;
+    pl.ks_per_split = (pl.k_stages + splits - 1) / splits;
+    pl.splits = (pl.k_stages + pl.ks_per_split - 1) / pl.ks_per_split;   // no empty range
+    return pl;
+}
+
+size_t conv_wgrad_ws(const ConvDims& d)
+{
+    WgradPlan pl = plan_wgrad(d);
+    return pl.splits > 1 ? size_t(pl.splits) * d.K * d.C * d.R * d.R * sizeof(float) : 0;
+}
+
+template <int BN>
+static cudaError_t run_wgrad(const ConvDims& d, const WgradPlan& pl, const float* x, const float* dy, float* dw,
+                             void* ws, cudaStream_t st)
+{
+    ConvWgradProb<BN> p;
+    p.x = x;
+    p.dy = dy;
+    p.out = pl.splits > 1 ? static_cast<float*>(ws) : dw;
+    p.C = d.C; p.H = d.H; p.W = d.W; p.K = d.K; p.R = d.R; p.S = d.S; p.pad = d.pad; p.P = d.P; p.Q = d.Q;
+    p.PQ = d.P * d.Q;
+    p.NPQ = d.N * p.PQ;
+    p.CRS = d.C * d.R * d.R;
+    p.HW = d.H * d.W;
+    p.CHW = d.C * p.HW;
+    p.f_pq = FastDiv(p.PQ);
+    p.f_q = FastDiv(d.Q);
+    p.f_rr = FastDiv(d.R * d.R);
+    p.f_r = FastDiv(d.R);
+    p.m_tiles = pl.m_tiles;
+    p.n_tiles = pl.n_tiles;
+    p.k_stages = pl.k_stages;
+    p.splits = pl.splits;
+    p.ks_per_split = pl.ks_per_split;
+    cudaError_t e = launch_tc_gemm<ConvWgradProb<BN>, BN>(p, p.m_tiles * p.n_tiles * p.splits, device_error_word(), st);
+    if (e != cudaSuccess || pl.splits == 1) return e;
+    const long long count = (long long)d.K * p.CRS;
+    long long blocks = (count + 255) / 256;
+    if (blocks > 8LL * sm_count()) blocks = 8LL * sm_count();
+    wgrad_reduce_kernel<<<int(blocks), 256, 0, st>>>(static_cast<const float*>(ws), pl.splits, count, dw);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_conv_wgrad(const ConvDims& d, const float* x, const float* dy, float* dw, void* ws,
+                              cudaStream_t st)
+{
+    WgradPlan pl = plan_wgrad(d);
+    switch (pl.bn) {
+    case 32: return run_wgrad<32>(d, pl, x, dy, dw, ws, st);
+    case 64: return run_wgrad<64>(d, pl, x, dy, dw, ws, st);
+    case 128: return run_wgrad<128>(d, pl, x, dy, dw, ws, st);
+    case 192: return run_wgrad<192>(d, pl, x, dy, dw, ws, st);
+    default: return run_wgrad<256>(d, pl, x, dy, dw, ws, st);
+    }
+}
+
+}  // namespace cb200

@@ -1,0 +1,340 @@
+// gemm_tc.cuh -- persistent, warp-specialised tcgen05 GEMM in fp32-faithful
+// 3xTF32 mode, shared by the flagged matmul and the three convolution GEMMs.
+//
+// D (128 x BN tile, fp32, in tensor memory) = sum over K of A (rows x K) * B (cols x K)^T
+//
+// Each operand value a is split in registers into hi = tf32(a) and
+// lo = tf32(a - hi); every 8-deep K step issues three tcgen05.mma.kind::tf32:
+// hi*hi, hi*lo and lo*hi (the lo*lo term is below fp32 resolution).  The
+// tensor core accumulates in fp32.
+//
+// Warp roles (416 threads, one CTA per SM, persistent over output tiles):
+//   warps 0-3   A producers: gather a 128 x 32 slice of A, split, store it
+//               into the stage's hi/lo tiles (128-byte swizzled, K-major)
+//   warps 4-7   B producers: gather a BN x 32 slice of B the same way, or
+//               (bulk problems) warp 4 lane 0 copies a pre-split hi/lo image
+//               of the slice with one cp.async.bulk
+//   warp 8      allocates tensor memory; lane 0 issues the MMAs
+//   warps 9-12  epilogue: tcgen05.ld the accumulator, hand rows to the
+//               problem's store (bias, NCHW reshape, split-K partials ...)
+// Two accumulators (2 x BN TMEM columns) let the epilogue of tile i overlap
+// the main loop of tile i+1.
+//
+// Every wait is bounded (ptx.cuh); on give-up the kernel raises its abort
+// flag, records kDevErrTimeout in the device error word, waits for what it
+// already launched asynchronously, frees its tensor memory and returns.
+#pragma once
+#include "ptx.cuh"
+
+namespace cb200 {
+
+constexpr int kBM = 128;       // UMMA M: rows of a tile (TMEM lanes)
+constexpr int kBK = 32;        // K depth of one pipeline stage (one 128-byte swizzle row)
+constexpr int kThreads = 416;
+constexpr int kWarpMma = 8;
+constexpr int kWarpEpi0 = 9;
+constexpr size_t kSmemBudget = 200 * 1024;
+
+struct Tile {
+    int m0, n0;     // first row of A / of B (output row / column)
+    int ks0, ks1;   // K stages [ks0, ks1)
+    int grp;        // problem-defined: sub-problem (stride phase) or split index
+};
+
+template <int BN>
+struct TileCfg {
+    static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN must be a multiple of 32 in [32, 256]");
+    static constexpr uint32_t kATile = kBM * kBK * 4;   // bytes of one hi (or lo) A tile
+    static constexpr uint32_t kBTile = BN * kBK * 4;
+    static constexpr uint32_t kStage = 2 * kATile + 2 * kBTile;
+    static constexpr int kStages = (kSmemBudget / kStage) > 6 ? 6 : int(kSmemBudget / kStage);
+    static constexpr uint32_t kTmemCols = (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
+    static constexpr size_t kSmemBytes = size_t(kStages) * kStage + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr uint32_t kIdesc = idesc_tf32(kBM, BN);
+};
+
+// Producer-side layout of a gathered 32-value slice (per thread):
+//   RowFast:   thread t owns row t of a 128-row block; v[i] is k = ks*32 + i.
+//   ChunkFast: thread t owns 16-byte chunk (t % 8) of rows (t / 8) + 16 p,
+//              p = 0..7; v[4p + e] is k = ks*32 + 4 (t % 8) + e.
+enum class Map { RowFast, ChunkFast };
+
+template <Map M>
+__device__ __forceinline__ void store_slice(uint32_t hi_tile, uint32_t lo_tile, int row_base, int rows, int tid,
+                                            const float (&v)[32])
+{
+    if constexpr (M == Map::RowFast) {
+        int row = row_base + tid;
+        if (row - row_base < rows) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                store_split_chunk(hi_tile, lo_tile, row, c, v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+        }
+    } else {
+        int chunk = tid & 7;
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            int r = (tid >> 3) + 16 * p;
+            if (r < rows)
+                store_split_chunk(hi_tile, lo_tile, row_base + r, chunk, v[4 * p], v[4 * p + 1], v[4 * p + 2],
+                                  v[4 * p + 3]);
+        }
+    }
+}
+
+struct SharedCtl {
+    uint64_t full[8];
+    uint64_t empty[8];
+    uint64_t accf[2];
+    uint64_t acce[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+template <class Prob, int BN>
+__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ Prob prob, int* err_word)
+{
+    using Cfg = TileCfg<BN>;
+    constexpr int S = Cfg::kStages;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + size_t(S) * Cfg::kStage);
+    volatile int* abort_flag = &ctl->abort_flag;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t smem_base = smem_u32(smem);
+    auto a_hi = [&](int s) { return smem_base + uint32_t(s) * Cfg::kStage; };
+    auto a_lo = [&](int s) { return a_hi(s) + Cfg::kATile; };
+    auto b_hi = [&](int s) { return a_hi(s) + 2 * Cfg::kATile; };
+    auto b_lo = [&](int s) { return b_hi(s) + Cfg::kBTile; };
+
+    if (threadIdx.x == 0) {
+        const uint32_t full_count = 4 + (Prob::kBBulk ? 1 : 4);
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&ctl->full[s], full_count);
+            mbar_init(&ctl->empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&ctl->accf[b], 1);
+            mbar_init(&ctl->acce[b], 4);
+        }
+        mbar_init(&ctl->drain, 1);
+        ctl->abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == kWarpMma) tmem_alloc(&ctl->tmem_base, Cfg::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = ctl->tmem_base;
+
+    const int num_tiles = prob.num_tiles();
+    auto fail = [&]() {
+        ctl->abort_flag = 1;
+        atomicOr(err_word, kDevErrTimeout);
+    };
+
+    if (warp < 4) {
+        // ---------------- A producers ----------------
+        const int tid = threadIdx.x;   // 0..127
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            const Tile tile = prob.tile(t);
+            typename Prob::AState st = prob.a_setup(tile, tid);
+            for (int ks = tile.ks0; ks < tile.ks1; ++ks) {
+                float v[32];
+                prob.load_a(st, tile, ks, tid, v);
+                if (!mbar_wait_warp(&ctl->empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
+                store_slice<Prob::kAMap>(a_hi(stage), a_lo(stage), 0, kBM, tid, v);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->full[stage]);
+                if (++stage == S) { stage = 0; phase ^= 1; }
+            }
+        }
+        if (!ok) fail();
+    } else if (warp < 8) {
+        // ---------------- B producers ----------------
+        const int tid = threadIdx.x - 128;   // 0..127
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        if constexpr (Prob::kBBulk) {
+            if (tid == 0) {
+                int issued = 0;
+                for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                    const Tile tile = prob.tile(t);
+                    for (int ks = tile.ks0; ks < tile.ks1; ++ks) {
+                        if (!mbar_wait(&ctl->empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
+                        mbar_arrive_expect_tx(&ctl->full[stage], 2 * Cfg::kBTile);
+                        bulk_g2s(smem + (b_hi(stage) - smem_base), prob.b_image(tile, ks), 2 * Cfg::kBTile,
+                                 &ctl->full[stage]);
+                        ++issued;
+                        if (++stage == S) { stage = 0; phase ^= 1; }
+                    }
+                }
+                if (!ok) {
+                    fail();
+                    // Copies already issued land in stages the MMA never
+                    // consumed; wait (bounded) for each of them before exit.
+                    int s = stage, ph = phase;
+                    for (int i = 0; i < (issued < S ? issued : S); ++i) {
+                        if (--s < 0) { s = S - 1; ph ^= 1; }
+                        uint64_t t0 = globaltimer_ns();
+                        while (!mbar_try_wait(&ctl->full[s], ph) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+                    }
+                }
+            }
+            __syncwarp();
+        } else {
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                const Tile tile = prob.tile(t);
+                typename Prob::BState st = prob.b_setup(tile, tid);
+                for (int ks = tile.ks0; ks < tile.ks1; ++ks) {
+                    float v[BN > 128 ? 2 : 1][32];
+#pragma unroll
+                    for (int pass = 0; pass < (BN > 128 ? 2 : 1); ++pass) prob.load_b(st, tile, ks, pass, tid, v[pass]);
+                    if (!mbar_wait_warp(&ctl->empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
+#pragma unroll
+                    for (int pass = 0; pass < (BN > 128 ? 2 : 1); ++pass) {
+                        const int rows = BN - 128 * pass < 128 ? BN - 128 * pass : 128;
+                        store_slice<Prob::kBMap>(b_hi(stage), b_lo(stage), 128 * pass, rows, tid, v[pass]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctl->full[stage]);
+                    if (++stage == S) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (!ok) fail();
+        }
+    } else if (warp == kWarpMma) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int local = 0;
+            bool ok = true;
+            bool issued_any = false;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
+                const Tile tile = prob.tile(t);
+                const int acc = local & 1;
+                const uint32_t acc_phase = (local >> 1) & 1;
+                if (!mbar_wait(&ctl->acce[acc], acc_phase ^ 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
+                uint32_t accumulate = 0;
+                for (int ks = tile.ks0; ks < tile.ks1; ++ks) {
+                    if (!mbar_wait(&ctl->full[stage], phase, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 8; ++kk) {
+                        const uint64_t ah = sdesc_k_sw128(a_hi(stage) + kk * 32);
+                        const uint64_t al = sdesc_k_sw128(a_lo(stage) + kk * 32);
+                        const uint64_t bh = sdesc_k_sw128(b_hi(stage) + kk * 32);
+                        const uint64_t bl = sdesc_k_sw128(b_lo(stage) + kk * 32);
+                        mma_tf32_ss(d_tmem, al, bh, Cfg::kIdesc, accumulate);
+                        accumulate = 1;
+                        mma_tf32_ss(d_tmem, ah, bl, Cfg::kIdesc, 1);
+                        mma_tf32_ss(d_tmem, ah, bh, Cfg::kIdesc, 1);
+                    }
+                    issued_any = true;
+                    mma_commit(&ctl->empty[stage]);
+                    if (++stage == S) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                mma_commit(&ctl->accf[acc]);
+            }
+            if (!ok) {
+                fail();
+                if (issued_any) {
+                    // Let the MMAs in flight finish before the memory goes away.
+                    mma_commit(&ctl->drain);
+                    uint64_t t0 = globaltimer_ns();
+                    while (!mbar_try_wait(&ctl->drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue ----------------
+        const int q = warp & 3;               // TMEM lane quarter this warp may access
+        const int row = q * 32 + lane;        // accumulator row of this thread
+        int local = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
+            const Tile tile = prob.tile(t);
+            const int acc = local & 1;
+            const uint32_t acc_phase = (local >> 1) & 1;
+            if (!mbar_wait_warp(&ctl->accf[acc], acc_phase, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            typename Prob::EState es = prob.e_setup(tile, row);
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t r[32];
+                tmem_ld32(tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * BN + c), r);
+                prob.store(es, tile, row, c, r);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->acce[acc]);
+        }
+        if (!ok) fail();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    }
+}
+
+// Host-side launch: persistent grid of min(tiles, SMs) CTAs.
+template <class Prob, int BN>
+cudaError_t launch_tc_gemm(const Prob& prob, int num_tiles, int* err_word, cudaStream_t stream)
+{
+    using Cfg = TileCfg<BN>;
+    static bool attr_set = false;   // per process; the attribute is per function
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<Prob, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             int(Cfg::kSmemBytes));
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    if (num_tiles <= 0) return cudaSuccess;
+    int grid = num_tiles < sm_count() ? num_tiles : sm_count();
+    tc_gemm_kernel<Prob, BN><<<grid, kThreads, Cfg::kSmemBytes, stream>>>(prob, err_word);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Fast unsigned division by a runtime constant (Granlund-Montgomery):
+// q = floor(n / d) for 0 <= n < 2^31, d >= 1.
+struct FastDiv {
+    uint32_t d, m, s;
+    FastDiv() = default;
+    __host__ explicit FastDiv(uint32_t divisor) : d(divisor)
+    {
+        uint32_t l = 0;
+        while ((uint64_t(1) << l) < divisor) ++l;
+        s = l;
+        m = uint32_t(((uint64_t(1) << 32) * ((uint64_t(1) << l) - divisor)) / divisor + 1);
+    }
+    __device__ __forceinline__ uint32_t div(uint32_t n) const
+    {
+        uint32_t t = __umulhi(n, m);
+        return (t + n) >> s;   // exact for n < 2^31: t + n < 2^32
+    }
+    __device__ __forceinline__ void divmod(uint32_t n, uint32_t& q, uint32_t& r) const
+    {
+        q = div(n);
+        r = n - q * d;
+    }
+};
+
+}  // namespace cb200

@@ -1,0 +1,192 @@
+// matmul.cu -- the flagged matmul of the page "DirectCompute Neural Network
+// Engine", section "Optimizations" -> "Transpose via Flags": C = op(A) op(B),
+// row-major, flags bit 0 = A stored K x M, bit 1 = B stored N x K.
+//
+// Mapped onto the tcgen05 GEMM with A rows = rows of C and B rows = columns of
+// C.  The gathers read each operand in the order that keeps a warp's loads
+// contiguous: a K-contiguous operand is read 16 bytes per thread along K
+// (ChunkFast), an M/N-contiguous one 4 bytes per thread along M/N (RowFast).
+// Either way the producer writes K-major swizzled hi/lo tiles, so all four flag
+// combinations feed the same MMA.
+#include "gemm_tc.cuh"
+
+namespace cb200 {
+
+template <unsigned FLAGS, int BN>
+struct MatmulProb {
+    static constexpr bool kBBulk = false;
+    static constexpr Map kAMap = (FLAGS & 1u) ? Map::RowFast : Map::ChunkFast;
+    static constexpr Map kBMap = (FLAGS & 2u) ? Map::ChunkFast : Map::RowFast;
+
+    const float* A;
+    const float* B;
+    float* C;
+    int M, K, N;
+    int m_tiles, n_tiles, k_stages;
+    int vec_a, vec_b, vec_c;   // 16-byte accesses allowed along K (A, B) / along N (C)
+
+    __device__ int num_tiles() const { return m_tiles * n_tiles; }
+
+    __device__ Tile tile(int t) const
+    {
+        Tile r;
+        r.n0 = (t % n_tiles) * BN;
+        r.m0 = (t / n_tiles) * kBM;
+        r.ks0 = 0;
+        r.ks1 = k_stages;
+        r.grp = 0;
+        return r;
+    }
+
+    // Four consecutive-k values of a K-contiguous row (zero past K).
+    __device__ __forceinline__ static void load4_k(const float* row, int k, int K, bool vec, float* v)
+    {
+        if (vec && k + 3 < K) {
+            float4 f = __ldg(reinterpret_cast<const float4*>(row + k));
+            v[0] = f.x; v[1] = f.y; v[2] = f.z; v[3] = f.w;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[e] = (k + e < K) ? __ldg(row + k + e) : 0.f;
+        }
+    }
+
+    struct AState {};
+    __device__ AState a_setup(const Tile&, int) const { return {}; }
+
+    __device__ void load_a(const AState&, const Tile& tl, int ks, int tid, float (&v)[32]) const
+    {
+        const int k0 = ks * kBK;
+        if constexpr (FLAGS & 1u) {   // A stored K x M: (m, k) at k*M + m
+            const int m = tl.m0 + tid;
+            const bool mv = m < M;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int k = k0 + i;
+                v[i] = (mv && k < K) ? __ldg(A + size_t(k) * M + m) : 0.f;
+            }
+        } else {                      // A stored M x K: (m, k) at m*K + k
+            const int kc = k0 + 4 * (tid & 7);
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+                const int m = tl.m0 + (tid >> 3) + 16 * p;
+                if (m < M) {
+                    load4_k(A + size_t(m) * K, kc, K, vec_a, &v[4 * p]);
+                } else {
+                    v[4 * p] = v[4 * p + 1] = v[4 * p + 2] = v[4 * p + 3] = 0.f;
+                }
+            }
+        }
+    }
+
+    struct BState {};
+    __device__ BState b_setup(const Tile&, int) const { return {}; }
+
+    __device__ void load_b(const BState&, const Tile& tl, int ks, int pass, int tid, float (&v)[32]) const
+    {
+        const int k0 = ks * kBK;
+        if constexpr (FLAGS & 2u) {   // B stored N x K: (n, k) at n*K + k
+            const int kc = k0 + 4 * (tid & 7);
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+                const int n = tl.n0 + 128 * pass + (tid >> 3) + 16 * p;
+                if (n < N) {
+                    load4_k(B + size_t(n) * K, kc, K, vec_b, &v[4 * p]);
+                } else {
+                    v[4 * p] = v[4 * p + 1] = v[4 * p + 2] = v[4 * p + 3] = 0.f;
+                }
+            }
+        } else {                      // B stored K x N: (n, k) at k*N + n
+            const int n = tl.n0 + 128 * pass + tid;
+            const bool nv = n < N;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int k = k0 + i;
+                v[i] = (nv && k < K) ? __ldg(B + size_t(k) * N + n) : 0.f;
+            }
+        }
+    }
+
+    struct EState {
+        float* crow;
+        bool valid;
+    };
+    __device__ EState e_setup(const Tile& tl, int row) const
+    {
+        const int m = tl.m0 + row;
+        EState e;
+        e.valid = m < M;
+        e.crow = C + size_t(e.valid ? m : 0) * N;
+        return e;
+    }
+
+    __device__ void store(const EState& e, const Tile& tl, int, int c, const uint32_t (&r)[32]) const
+    {
+        if (!e.valid) return;
+        const int n0 = tl.n0 + c;
+        if (vec_c && n0 + 32 <= N) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+                *reinterpret_cast<float4*>(e.crow + n0 + i) =
+                    make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]), __uint_as_float(r[i + 2]),
+                                __uint_as_float(r[i + 3]));
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (n0 + i < N) e.crow[n0 + i] = __uint_as_float(r[i]);
+        }
+    }
+};
+
+template <unsigned FLAGS, int BN>
+static cudaError_t run_matmul(int M, int K, int N, const float* A, const float* B, float* C, cudaStream_t st)
+{
+    MatmulProb<FLAGS, BN> p;
+    p.A = A;
+    p.B = B;
+    p.C = C;
+    p.M = M;
+    p.K = K;
+    p.N = N;
+    p.m_tiles = (M + kBM - 1) / kBM;
+    p.n_tiles = (N + BN - 1) / BN;
+    p.k_stages = (K + kBK - 1) / kBK;
+    p.vec_a = (K % 4 == 0) && aligned16(A);
+    p.vec_b = (K % 4 == 0) && aligned16(B);
+    p.vec_c = (N % 4 == 0) && aligned16(C);
+    return launch_tc_gemm<MatmulProb<FLAGS, BN>, BN>(p, p.m_tiles * p.n_tiles, device_error_word(), st);
+}
+
+// Tile width: the widest of {256, 128, 64, 32} that still gives every SM a
+// tile; narrower C only when there are too few tiles to go round.
+static int pick_bn(int M, int N)
+{
+    const int m_tiles = (M + kBM - 1) / kBM;
+    const int bn_max = N <= 32 ? 32 : N <= 64 ? 64 : N <= 128 ? 128 : 256;
+    for (int bn = bn_max; bn > 64; bn /= 2)
+        if (m_tiles * ((N + bn - 1) / bn) >= sm_count()) return bn;
+    return bn_max < 64 ? bn_max : 64;
+}
+
+template <unsigned FLAGS>
+static cudaError_t run_flags(int M, int K, int N, const float* A, const float* B, float* C, cudaStream_t st)
+{
+    switch (pick_bn(M, N)) {
+    case 256: return run_matmul<FLAGS, 256>(M, K, N, A, B, C, st);
+    case 128: return run_matmul<FLAGS, 128>(M, K, N, A, B, C, st);
+    case 64: return run_matmul<FLAGS, 64>(M, K, N, A, B, C, st);
+    default: return run_matmul<FLAGS, 32>(M, K, N, A, B, C, st);
+    }
+}
+
+cudaError_t launch_matmul(int M, int K, int N, unsigned flags, const float* A, const float* B, float* C,
+                          cudaStream_t st)
+{
+    switch (flags) {
+    case 0: return run_flags<0>(M, K, N, A, B, C, st);
+    case 1: return run_flags<1>(M, K, N, A, B, C, st);
+    case 2: return run_flags<2>(M, K, N, A, B, C, st);
+    default: return run_flags<3>(M, K, N, A, B, C, st);
+    }
+}
+
+}  // namespace cb200

@@ -1,0 +1,167 @@
+/*
+ * conv_b200.h -- C ABI of libconv_b200: the im2col convolution pipeline of the
+ * page "DirectCompute Neural Network Engine" (directcompute-nn 0.1.0), forward
+ * and backward, with its flagged matmul, max pooling and SGD, as hand-written
+ * sm_103a CUDA kernels.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Tensors are fp32, row-major, NCHW (the page keeps every buffer as a float
+ *    StructuredBuffer, section "Buffer Layout"); max-pool indices are int32.
+ *  - Every pointer argument is a DEVICE pointer owned by the caller; the
+ *    library never frees, keeps or reallocates it.  Outputs are fully
+ *    OVERWRITTEN, never accumulated into (the page adds gradients with a
+ *    separate grad_accum shader and clears scatter targets first).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream).  The library never synchronises the host.  Argument errors are
+ *    reported before anything is launched.  A device-side failure (a bounded
+ *    wait that gave up) is latched in a device error word and reported by the
+ *    next conv_b200_check().
+ *  - Operands must not alias outputs.  Pointers must be 16-byte aligned
+ *    (CONV_ERR_ALIGN otherwise); element counts of every tensor must stay
+ *    below 2^31 (CONV_ERR_OVERFLOW otherwise).
+ *  - Convolution shape (section "Constant Buffer Convention", the im2col
+ *    parameter set batch/inC/inH/inW/kH/stride/padding/outH/outW): square
+ *    kH x kH filters, the same stride and zero padding on both axes,
+ *    outH = (inH + 2*padding - kH) / stride + 1 (floor) and likewise outW;
+ *    inconsistent outH/outW are rejected.
+ *  - Contractions (conv_fwd, conv_bwd_data, conv_bwd_filter, matmul) run on
+ *    the tcgen05 tensor cores in an fp32-faithful 3xTF32 mode with fp32
+ *    accumulation: each result is within 1e-4 * sum_k |a_k b_k| + 1e-6 of the
+ *    exact sum.
+ */
+#ifndef CONV_B200_H
+#define CONV_B200_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream (cudaStream_t). */
+typedef struct CUstream_st *conv_stream_t;
+
+typedef struct {
+    int32_t batch, inC, inH, inW; /* input x: batch x inC x inH x inW            */
+    int32_t outC;                 /* number of filters                           */
+    int32_t kH;                   /* filter extent (kW == kH)                    */
+    int32_t stride, padding;      /* same on both axes; padding reads zero       */
+    int32_t outH, outW;           /* output extent, must match the floor formula */
+} conv_shape_t;
+
+/* Return codes. */
+#define CONV_OK 0
+#define CONV_ERR_NULL (-1)           /* a required pointer is NULL                  */
+#define CONV_ERR_SHAPE (-2)          /* non-positive or inconsistent sizes, flags>3 */
+#define CONV_ERR_ALIGN (-3)          /* a pointer is not 16-byte aligned            */
+#define CONV_ERR_OVERFLOW (-4)       /* a tensor has 2^31 elements or more          */
+#define CONV_ERR_WORKSPACE (-5)      /* workspace missing or smaller than required  */
+#define CONV_ERR_CUDA (-6)           /* a CUDA runtime call or launch failed        */
+#define CONV_ERR_DEVICE_TIMEOUT (-7) /* a kernel's bounded wait gave up             */
+#define CONV_ERR_DEVICE (-8)         /* no usable sm_103 device                     */
+
+/* Operation ids for conv_b200_workspace_bytes. */
+#define CONV_OP_FWD 0
+#define CONV_OP_BWD_DATA 1
+#define CONV_OP_BWD_FILTER 2
+
+/* Forward convolution.  Page section "Convolution: The im2col Approach",
+ * forward: im2col -> filters (outC x inC*kH*kW) times the column matrix ->
+ * conv_reshape (+ bias) to (batch, outC, outH, outW).  Computed as one
+ * implicit GEMM: the column matrix is gathered tile by tile and never stored.
+ *   x  [batch][inC][inH][inW]   w [outC][inC][kH][kH]   b [outC] or NULL (no bias)
+ *   y  [batch][outC][outH][outW]                              (overwritten)
+ *   workspace: device scratch of conv_b200_workspace_bytes(CONV_OP_FWD, s)
+ *   bytes (the filters split into tensor-core tiles), owned by the caller,
+ *   reused freely after the stream passes the call. */
+int conv_fwd(const conv_shape_t *s, const float *x, const float *w, const float *b, float *y, void *workspace,
+             size_t workspace_bytes, conv_stream_t stream);
+
+/* Input gradient.  Page section "Convolution: The im2col Approach", backward:
+ * filters^T x grad_reshaped -> col2im -> grad_input.  Computed as one implicit
+ * GEMM per stride phase that gathers grad_output directly, so the col2im sum
+ * happens inside the accumulator and the column-matrix gradient is never
+ * stored.
+ *   w  [outC][inC][kH][kH]   dy [batch][outC][outH][outW]
+ *   dx [batch][inC][inH][inW] (overwritten; pixels no window reads get 0)
+ *   workspace: conv_b200_workspace_bytes(CONV_OP_BWD_DATA, s) bytes. */
+int conv_bwd_data(const conv_shape_t *s, const float *w, const float *dy, float *dx, void *workspace,
+                  size_t workspace_bytes, conv_stream_t stream);
+
+/* Filter gradient.  Page section "Convolution: The im2col Approach", backward:
+ * grad_reshaped x im2col_matrix^T.  The column matrix is regathered from x
+ * (not read from a saved copy); the batch*outH*outW reduction is split across
+ * the GPU and summed in a fixed order (deterministic).
+ *   x  [batch][inC][inH][inW]   dy [batch][outC][outH][outW]
+ *   dw [outC][inC][kH][kH] (overwritten)
+ *   workspace: conv_b200_workspace_bytes(CONV_OP_BWD_FILTER, s) bytes. */
+int conv_bwd_filter(const conv_shape_t *s, const float *x, const float *dy, float *dw, void *workspace,
+                    size_t workspace_bytes, conv_stream_t stream);
+
+/* Bias gradient.  Page section "Convolution: The im2col Approach", backward:
+ * the sum of grad_reshaped over its columns, i.e. over batch, outH and outW.
+ * Fixed-order reduction (deterministic).
+ *   dy [batch][outC][outH][outW]   db [outC] (overwritten) */
+int conv_bwd_bias(const conv_shape_t *s, const float *dy, float *db, conv_stream_t stream);
+
+/* Scratch bytes the given operation needs for shape s (0 if none).  op is one
+ * of CONV_OP_*; returns 0 for an invalid shape or op. */
+size_t conv_b200_workspace_bytes(int op, const conv_shape_t *s);
+
+/* Standalone im2col (the nn_im2col shader of section "Convolution Shaders"):
+ *   col[(c*kH + r)*kH + q][(n*outH + oh)*outW + ow] = x[n][c][oh*stride + r - padding][ow*stride + q - padding]
+ * or 0 where that position lies in the padding.
+ *   x [batch][inC][inH][inW]   col [inC*kH*kH][batch*outH*outW] (overwritten) */
+int im2col(const conv_shape_t *s, const float *x, float *col, conv_stream_t stream);
+
+/* Standalone col2im (the nn_col2im shader): the adjoint of im2col.  Every
+ * column-matrix entry is added to the input position im2col read it from;
+ * entries that came from padding are dropped.  Each dx element is summed in a
+ * fixed order (ascending r, then q), so the result is deterministic.
+ *   col [inC*kH*kH][batch*outH*outW]   dx [batch][inC][inH][inW] (overwritten) */
+int col2im(const conv_shape_t *s, const float *col, float *dx, conv_stream_t stream);
+
+/* Flagged matmul.  Page section "Optimizations" -> "Transpose via Flags" and
+ * the matmul shader table: C (M x N) = op(A) * op(B), row-major, where
+ * flags bit 0 reads A as column-major (A stored K x M) and flags bit 1 reads B
+ * as column-major (B stored N x K).  C is overwritten (no alpha/beta).
+ * Any M, K, N >= 1 (ragged edges are handled); flags in 0..3. */
+int matmul(int32_t M, int32_t K, int32_t N, uint32_t flags, const float *A, const float *B, float *C,
+           conv_stream_t stream);
+
+/* Max pooling forward (nn_maxpool_forward, section "Pooling Shaders"):
+ * k x k windows, stride `stride`, no padding, outH = (H - k) / stride + 1.
+ * y = window maximum; idx = flat offset into the whole NCHW x of the FIRST
+ * maximum in row-major window order.
+ *   x [batch][C][H][W]   y, idx [batch][C][outH][outW] (overwritten) */
+int maxpool2d_fwd(int32_t batch, int32_t C, int32_t H, int32_t W, int32_t k, int32_t stride, int32_t outH,
+                  int32_t outW, const float *x, float *y, int32_t *idx, conv_stream_t stream);
+
+/* Max pooling backward (nn_maxpool_backward): dx[i] = sum of dy[o] over the
+ * windows o whose saved index is i, in ascending window order (bit-exact and
+ * deterministic); 0 where no window routed a gradient.  idx must come from
+ * maxpool2d_fwd with the same sizes (every entry must lie inside the window of
+ * its own output; others are ignored).
+ *   dy, idx [batch][C][outH][outW]   dx [batch][C][H][W] (overwritten) */
+int maxpool2d_bwd(int32_t batch, int32_t C, int32_t H, int32_t W, int32_t k, int32_t stride, int32_t outH,
+                  int32_t outW, const float *dy, const int32_t *idx, float *dx, conv_stream_t stream);
+
+/* SGD step (nn_sgd, section "Utility Shaders"), in place:
+ *   param[i] = param[i] - lr * min(max(grad[i], -clip), clip)
+ * each operation rounded to fp32, no fused multiply-add.  count >= 0. */
+int sgd_step(int64_t count, float lr, float clip, float *param, const float *grad, conv_stream_t stream);
+
+/* Text for a return code. */
+const char *conv_b200_strerror(int code);
+
+/* Synchronise `stream`, then read and clear the device error word: returns
+ * CONV_OK, CONV_ERR_DEVICE_TIMEOUT, or CONV_ERR_CUDA. */
+int conv_b200_check(conv_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CONV_B200_H */
