@@ -1,0 +1,398 @@
+"""Benchmark: the im2col convolution pipeline (page "DirectCompute Neural Network
+Engine", section "Convolution: The im2col Approach"), forward + backward, on the
+AlexNet-shaped conv1-5 layers at batch 128, one GB300.
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+for every layer conv_fwd, (max-pool forward + backward after conv1 and conv2),
+conv_bwd_data, conv_bwd_filter, conv_bwd_bias and an SGD step on the filters
+and bias.  The metric is algorithmic TFLOP/s of the three convolution GEMMs
+(2 * outC * inC*k*k * batch*outH*outW each) over the whole step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead (host cores only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic  # noqa: E402
+
+METRIC = "conv fwd+bwd TFLOP/s per layer at batch 128 and % of tensor roofline"
+UNIT = "TFLOP/s"
+WORKLOAD = "AlexNet conv1-5 fwd+bwd (fwd, input grad, filter grad, bias grad, pools, SGD), batch 128, fp32 NCHW"
+LAYERS = synthetic.ALEXNET
+L2_BYTES = 126 * 1024 * 1024
+TF32_OVER_BF16 = 1.1 / 2.25      # nominal dense TF32 : BF16 tensor rate on GB300
+SPLIT_PRODUCTS = 3               # 3xTF32: three tensor-core products per fp32 product
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            m = json.load(f)
+        return float(m["bf16_tflops"]), float(m["hbm_gbs"]), "measured"
+    return 1900.0, 6800.0, "fallback"
+
+
+def step_flops(layers) -> int:
+    return sum(3 * L.gemm_flops for L in layers)
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle on a bounded sample
+
+def oracle_sample_run(layers, batch):
+    import oracle
+    orc = oracle.get()
+    flops = 0
+    t0 = time.perf_counter()
+    for L in layers:
+        l = L.with_batch(batch)
+        x, w, b, dy = l.make()
+        orc.conv_fwd(x, w, b, l.stride, l.pad)
+        orc.conv_bwd_data(w, dy, x.shape, l.stride, l.pad)
+        orc.conv_bwd_filter(x, dy, w.shape, l.stride, l.pad)
+        orc.conv_bwd_bias(dy)
+        flops += 3 * l.gemm_flops
+    dt = time.perf_counter() - t0
+    return flops / dt / 1e12, dt, orc.threads()
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    batch = args.ref_batch
+    for _ in range(args.warmup):
+        oracle_sample_run(LAYERS, batch)
+    vals, times = [], []
+    cores = 1
+    for _ in range(args.steps):
+        v, dt, cores = oracle_sample_run(LAYERS, batch)
+        vals.append(v)
+        times.append(dt)
+    value = len(vals) * step_flops([L.with_batch(batch) for L in LAYERS]) / sum(times) / 1e12
+    sample = "AlexNet conv1-5 fwd + input/filter/bias grads at batch %d (of 128) per step" % batch
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample_batch": batch},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            rows = [r.split(",") for r in open(self.path).read().strip().splitlines() if r.strip()]
+        except OSError:
+            rows = []
+        for r in rows:
+            try:
+                sm.append(float(r[0]))
+                mx = max(mx, float(r[1]))
+            except (ValueError, IndexError):
+                continue
+            for name, v in zip(names, r[4:8]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        if self.path:
+            os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+
+class LayerBufs:
+    def __init__(self, L, torch, cb):
+        self.L = L
+        x, w, b, dy = L.make()
+        self.host = {"x": x, "w": w, "b": b, "dy": dy}
+        dev = lambda a: torch.from_numpy(a).cuda()
+        self.x, self.w, self.b, self.dy = dev(x), dev(w), dev(b), dev(dy)
+        self.y = torch.empty(L.y_shape, device="cuda")
+        self.dx = torch.empty(L.x_shape, device="cuda")
+        self.dw = torch.empty(L.w_shape, device="cuda")
+        self.db = torch.empty((L.outC,), device="cuda")
+        self.pool = None
+        if L.pool:
+            k, s = L.pool
+            P = (L.outH - k) // s + 1
+            self.pool = (k, s)
+            self.yp = torch.empty((L.batch, L.outC, P, P), device="cuda")
+            self.idx = torch.empty((L.batch, L.outC, P, P), dtype=torch.int32, device="cuda")
+            self.host["dyp"] = synthetic.pool_grad((L.batch, L.outC, P, P), L.seed_base + 20)
+            self.dyp = dev(self.host["dyp"])
+            self.dxp = torch.empty(L.y_shape, device="cuda")
+        s = cb.shape_of(L.x_shape, L.w_shape, L.stride, L.pad)
+        self.ws_bytes = max(cb.workspace_bytes(op, s) for op in range(3))
+
+    def bytes_in(self):
+        return sum(a.nbytes for a in self.host.values())
+
+    def bytes_out(self):
+        n = self.y.numel() + self.dx.numel() + self.dw.numel() + self.db.numel()
+        if self.pool:
+            n += self.dxp.numel()
+        return 4 * n
+
+
+def run_ours(args):
+    import torch
+    import im2col_convolution_tiled_gb300 as cb
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+
+    if not os.path.exists(cb.LIB_PATH):
+        from im2col_convolution_tiled_gb300 import build
+        build.build()
+    cb.load()
+
+    bufs = [LayerBufs(L, torch, cb) for L in LAYERS]
+    ws = torch.empty(max(b.ws_bytes for b in bufs) + 16, dtype=torch.uint8, device="cuda")
+    lr, clip = synthetic.SGD_LR_CLIP
+    stream = torch.cuda.current_stream()
+    ops = ["fwd", "pool", "dgrad", "wgrad", "bias", "sgd"]
+    rec = {}   # (layer, op) -> list of (start_event, end_event)
+
+    def timed(key, fn):
+        if key is None:
+            fn()
+            return
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        rec.setdefault(key, []).append((e0, e1))
+
+    def step(record):
+        for b in bufs:
+            L = b.L
+            key = (lambda op: (L.name, op)) if record else (lambda op: None)
+            timed(key("fwd"), lambda: cb.conv_fwd(b.x, b.w, b.b, L.stride, L.pad, y=b.y, workspace=ws))
+            if b.pool:
+                k, s = b.pool
+                timed(key("pool"), lambda: (cb.maxpool2d_fwd(b.y, k, s, y=b.yp, idx=b.idx),
+                                            cb.maxpool2d_bwd(b.dyp, b.idx, L.y_shape, k, s, dx=b.dxp)))
+            timed(key("dgrad"), lambda: cb.conv_bwd_data(b.w, b.dy, L.x_shape, L.stride, L.pad, dx=b.dx,
+                                                         workspace=ws))
+            timed(key("wgrad"), lambda: cb.conv_bwd_filter(b.x, b.dy, L.w_shape, L.stride, L.pad, dw=b.dw,
+                                                           workspace=ws))
+            timed(key("bias"), lambda: cb.conv_bwd_bias(b.dy, db=b.db))
+            timed(key("sgd"), lambda: (cb.sgd_step(b.w, b.dw, lr, clip), cb.sgd_step(b.b, b.db, lr, clip)))
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step(False)
+    cb.check()
+
+    # --- device-resident timed region -------------------------------------
+    barrier()
+    n0 = cb.launch_count()
+    with ClockSampler(local) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for _ in range(args.steps):
+            step(True)
+        t_end.record(stream)
+        barrier()
+    launches = cb.launch_count() - n0
+    cb.check()
+    ms_total = t_start.elapsed_time(t_end)
+    if dist is not None:
+        t = torch.tensor([ms_total], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    flops = step_flops(LAYERS)
+    value = world * flops / (ms_step * 1e-3) / 1e12
+
+    avg = {k: sum(a.elapsed_time(b) for a, b in v) / len(v) for k, v in rec.items()}
+    per_layer = []
+    gemm_ms = 0.0
+    for b in bufs:
+        L = b.L
+        g = L.gemm_flops
+        d = {"layer": L.name}
+        for op in ops:
+            if (L.name, op) in avg:
+                d[op + "_ms"] = round(avg[(L.name, op)], 4)
+        for op in ("fwd", "dgrad", "wgrad"):
+            d[op + "_tflops"] = round(g / (avg[(L.name, op)] * 1e-3) / 1e12, 2)
+            gemm_ms += avg[(L.name, op)]
+        d["fwd_bwd_tflops"] = round(3 * g / ((avg[(L.name, "fwd")] + avg[(L.name, "dgrad")] +
+                                              avg[(L.name, "wgrad")]) * 1e-3) / 1e12, 2)
+        per_layer.append(d)
+
+    bf16, hbm, peak_kind = peaks()
+    peak = bf16 * TF32_OVER_BF16 / SPLIT_PRODUCTS
+    achieved = flops / (gemm_ms * 1e-3) / 1e12
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof):
+        with open(prof) as f:
+            traffic = json.load(f).get("conv_gemm_bytes_per_step")
+
+    # --- end to end through the public API with host buffers ---------------
+    pin = lambda a: torch.from_numpy(a).pin_memory()
+    host_in = [{k: pin(v) for k, v in b.host.items()} for b in bufs]
+    host_out = [{"y": torch.empty(b.L.y_shape).pin_memory(), "dx": torch.empty(b.L.x_shape).pin_memory(),
+                 "dw": torch.empty(b.L.w_shape).pin_memory(), "db": torch.empty((b.L.outC,)).pin_memory(),
+                 "dxp": torch.empty(b.L.y_shape).pin_memory() if b.pool else None} for b in bufs]
+    h2d = sum(b.bytes_in() for b in bufs)
+    d2h = sum(b.bytes_out() for b in bufs)
+
+    def e2e_step():
+        for b, hi in zip(bufs, host_in):
+            b.x.copy_(hi["x"], non_blocking=True)
+            b.w.copy_(hi["w"], non_blocking=True)
+            b.b.copy_(hi["b"], non_blocking=True)
+            b.dy.copy_(hi["dy"], non_blocking=True)
+            if b.pool:
+                b.dyp.copy_(hi["dyp"], non_blocking=True)
+        step(False)
+        for b, ho in zip(bufs, host_out):
+            ho["y"].copy_(b.y, non_blocking=True)
+            ho["dx"].copy_(b.dx, non_blocking=True)
+            ho["dw"].copy_(b.dw, non_blocking=True)
+            ho["db"].copy_(b.db, non_blocking=True)
+            if b.pool:
+                ho["dxp"].copy_(b.dxp, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    e2e_steps = max(3, args.steps // 4)
+    e2e_step()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    barrier()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    cb.check()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, dt, cores = oracle_sample_run(LAYERS, args.cpu_batch)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": "AlexNet conv1-5 fwd + input/filter/bias grads at batch %d (of 128), %.1f s"
+                         % (args.cpu_batch, dt)}
+
+    working_set = sum(b.bytes_in() + b.bytes_out() for b in bufs)
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": 128, "layers": [L.name for L in LAYERS],
+                   "precision": "fp32-faithful 3xTF32 on tcgen05, fp32 accumulation",
+                   "step_gflop": round(flops / 1e9, 2),
+                   "l2": "no flush: one step streams %.2f GB of distinct tensors (> %d MB L2)"
+                         % (working_set / 1e9, L2_BYTES >> 20),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": UNIT,
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "conv GEMMs (conv_fwd + conv_bwd_data + conv_bwd_filter, all layers)",
+                     "peak_basis": "%s bf16 %.1f TFLOP/s x %.3f (TF32/BF16) / 3 (3xTF32)"
+                                   % (peak_kind, bf16, TF32_OVER_BF16)},
+        "per_layer": per_layer,
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-batch", type=int, default=12)
+    ap.add_argument("--ref-batch", type=int, default=1)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps, always
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

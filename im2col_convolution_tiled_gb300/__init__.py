@@ -21,7 +21,7 @@ import os
 __all__ = [
     "ConvShape", "lib", "load", "conv_fwd", "conv_bwd_data", "conv_bwd_filter", "conv_bwd_bias",
     "im2col", "col2im", "matmul", "maxpool2d_fwd", "maxpool2d_bwd", "sgd_step", "workspace_bytes",
-    "check", "ConvError", "out_size", "LIB_PATH",
+    "check", "ConvError", "out_size", "LIB_PATH", "launch_count",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libconv_b200.so")
@@ -59,6 +59,7 @@ _SIGS = {
     "sgd_step": ([ctypes.c_int64, ctypes.c_float, ctypes.c_float, _P, _P, _P], ctypes.c_int),
     "conv_b200_strerror": ([ctypes.c_int], ctypes.c_char_p),
     "conv_b200_check": ([_P], ctypes.c_int),
+    "conv_b200_launch_count": ([], ctypes.c_uint64),
 }
 
 
@@ -282,6 +283,11 @@ def sgd_step(param, grad, lr, clip, stream=None):
         raise ValueError("param and grad sizes differ")
     _call("sgd_step", param.numel(), lr, clip, _ptr(param), _ptr(grad), _stream(stream))
     return param
+
+
+def launch_count() -> int:
+    """Kernels launched by the library so far (see conv_b200_launch_count)."""
+    return int(lib().conv_b200_launch_count())
 
 
 def check(stream=None):

@@ -1,6 +1,7 @@
 // api.cu -- the extern "C" entry points of libconv_b200 (include/conv_b200.h):
 // argument validation, then one or two asynchronous launches on the caller's
 // stream.  Nothing here synchronises the host except conv_b200_check().
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -35,6 +36,9 @@ void init_device(int dev)
     g_sms[dev] = sms;
 }
 }  // namespace
+
+static std::atomic<unsigned long long> g_launches{0};
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 int* device_error_word()
 {
@@ -263,6 +267,8 @@ int sgd_step(int64_t count, float lr, float clip, float* param, const float* gra
     if (!device_ok()) return CONV_ERR_DEVICE;
     return status_of(launch_sgd(count, lr, clip, param, grad, as_cuda(stream)));
 }
+
+uint64_t conv_b200_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char* conv_b200_strerror(int code)
 {

@@ -20,6 +20,10 @@ int* device_error_word();
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Count of kernels this library has launched since it was loaded (every
+// <<<>>> launch calls note_launch()); exported as conv_b200_launch_count().
+void note_launch();
+
 inline cudaStream_t as_cuda(conv_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -61,6 +61,7 @@ cudaError_t build_bimage(const Gen& gen, int n_rows, int k_total, int bn, float*
     long long blocks = (total + 255) / 256;
     if (blocks > 4LL * sm_count() * 8) blocks = 4LL * sm_count() * 8;
     build_bimage_kernel<Gen><<<int(blocks), 256, 0, st>>>(gen, n_rows, k_total, bn, img);
+    note_launch();
     return cudaGetLastError();
 }
 

@@ -232,6 +232,7 @@ static cudaError_t run_wgrad(const ConvDims& d, const WgradPlan& pl, const float
     long long blocks = (count + 255) / 256;
     if (blocks > 8LL * sm_count()) blocks = 8LL * sm_count();
     wgrad_reduce_kernel<<<int(blocks), 256, 0, st>>>(static_cast<const float*>(ws), pl.splits, count, dw);
+    note_launch();
     return cudaGetLastError();
 }
 

@@ -309,6 +309,7 @@ cudaError_t launch_tc_gemm(const Prob& prob, int num_tiles, int* err_word, cudaS
     if (num_tiles <= 0) return cudaSuccess;
     int grid = num_tiles < sm_count() ? num_tiles : sm_count();
     tc_gemm_kernel<Prob, BN><<<grid, kThreads, Cfg::kSmemBytes, stream>>>(prob, err_word);
+    note_launch();
     return cudaGetLastError();
 }
 

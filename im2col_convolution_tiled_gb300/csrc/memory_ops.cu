@@ -93,10 +93,12 @@ cudaError_t launch_im2col(const ConvDims& d, const float* x, float* col, cudaStr
         const long long total4 = (long long)CRS * (NPQ / 4);
         im2col_kernel<<<grid_for(total4, 256), 256, 0, st>>>(x, col, d.C, d.H, d.W, d.S, d.pad, d.P, d.Q, f_pq,
                                                              f_q, f_rr, f_r, FastDiv(NPQ / 4), int(total4));
+    note_launch();
     } else {
         const long long total = (long long)CRS * NPQ;
         im2col_scalar_kernel<<<grid_for(total, 256), 256, 0, st>>>(x, col, d.C, d.H, d.W, d.S, d.pad, FastDiv(NPQ),
                                                                     f_pq, f_q, f_rr, f_r, int(total));
+    note_launch();
     }
     return cudaGetLastError();
 }
@@ -135,6 +137,7 @@ cudaError_t launch_col2im(const ConvDims& d, const float* col, float* dx, cudaSt
     const long long total = (long long)d.N * d.C * d.H * d.W;
     col2im_kernel<<<grid_for(total, 256), 256, 0, st>>>(col, dx, d.R, d.S, d.pad, d.P, d.Q, d.N * d.P * d.Q,
                                                         FastDiv(d.W), FastDiv(d.H), FastDiv(d.C), int(total));
+    note_launch();
     return cudaGetLastError();
 }
 
@@ -171,6 +174,7 @@ cudaError_t launch_maxpool_fwd(int N, int C, int H, int W, int k, int s, int P, 
     const long long total = (long long)N * C * P * Q;
     maxpool_fwd_kernel<<<grid_for(total, 256), 256, 0, st>>>(x, y, idx, H, W, k, s, FastDiv(Q), FastDiv(P),
                                                              int(total));
+    note_launch();
     return cudaGetLastError();
 }
 
@@ -206,6 +210,7 @@ cudaError_t launch_maxpool_bwd(int N, int C, int H, int W, int k, int s, int P, 
     const long long total = (long long)N * C * H * W;
     maxpool_bwd_kernel<<<grid_for(total, 256), 256, 0, st>>>(dy, idx, dx, k, s, P, Q, FastDiv(W), FastDiv(H),
                                                              int(total));
+    note_launch();
     return cudaGetLastError();
 }
 
@@ -240,6 +245,7 @@ cudaError_t launch_sgd(int64_t count, float lr, float clip, float* p, const floa
     if (count == 0) return cudaSuccess;
     const long long n4 = count / 4;
     sgd_kernel<<<grid_for(n4 > 0 ? n4 : 1, 256), 256, 0, st>>>(p, g, n4, count, lr, clip);
+    note_launch();
     return cudaGetLastError();
 }
 
@@ -286,6 +292,7 @@ __global__ void __cluster_dims__(kBiasCluster, 1, 1) __launch_bounds__(kBiasThre
 cudaError_t launch_bias_grad(const ConvDims& d, const float* dy, float* db, cudaStream_t st)
 {
     bias_grad_kernel<<<d.K * kBiasCluster, kBiasThreads, 0, st>>>(dy, db, d.N, d.K, d.P * d.Q);
+    note_launch();
     return cudaGetLastError();
 }
 

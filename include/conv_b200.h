@@ -153,6 +153,11 @@ int maxpool2d_bwd(int32_t batch, int32_t C, int32_t H, int32_t W, int32_t k, int
  * each operation rounded to fp32, no fused multiply-add.  count >= 0. */
 int sgd_step(int64_t count, float lr, float clip, float *param, const float *grad, conv_stream_t stream);
 
+/* Number of kernels the library has launched since it was loaded (all
+ * devices, all streams).  A diagnostic: callers difference two readings to
+ * count the launches of a region of their own code. */
+uint64_t conv_b200_launch_count(void);
+
 /* Text for a return code. */
 const char *conv_b200_strerror(int code);
 
