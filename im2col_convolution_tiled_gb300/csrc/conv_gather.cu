@@ -1,0 +1,375 @@
+// conv_gather.cu -- the forward convolution and the input gradient of the page
+// "DirectCompute Neural Network Engine", section "Convolution: The im2col
+// Approach", both as one implicit GEMM on the tcgen05 tensor cores whose A
+// operand is a convolution-window gather.
+//
+// Forward (steps 1-3: im2col, filters x columns, conv_reshape + bias):
+//   D[(n, oh, ow), k] = sum_(r, q, c) x[n, c, oh*s + r - pad, ow*s + q - pad] * W[k, c, r, q]
+//   y[n, k, oh, ow]   = D + b[k]
+// The column matrix is the A operand, gathered straight from x (zero in the
+// padding) and never stored; the filters are the B operand.
+//
+// Input gradient (filters^T x grad_reshaped, then col2im): col2im adds, for an
+// input pixel h, the contributions of every tap r with oh*s + r - pad = h.
+// Write h = a + s*hh with phase a = h mod s; then oh = hh + d with
+// d = (a + pad - r) / s, so each dx pixel is
+//   dx[n, c, a + s*hh, b + s*ww] = sum_(d, e, k) dy[n, k, hh + d, ww + e] * W[k, c, a + pad - s*d, b + pad - s*e]
+// (terms whose tap falls outside 0..kH-1 are zero).  Taking (c, a, b) as the
+// GEMM column and (n, hh, ww) as the row makes this a single GEMM for any
+// stride: its A operand is again a window gather, now over dy with stride 1
+// and the window d in [d_lo, d_lo + T), and the phases widen N (C * s * s
+// columns) instead of splitting the problem.  Each dx element is produced by
+// exactly one accumulator: col2im needs no scatter, no atomics and no column
+// buffer.
+//
+// K order of both: tap-major, channel-fastest -- k = (tap_r * T + tap_q) * Ci + ci --
+// when Ci (channels of the gathered tensor) is a multiple of 32: a pipeline
+// stage then holds 32 channels of ONE tap, so its bounds test is done once
+// per stage and every element is one add and one load.  Otherwise
+// k = (ci * T + tap_r) * T + tap_q with a per-element decode shared across the
+// warp.  The B operand (filters, rearranged and zero-padded to the same K
+// order) is laid out once per call as pre-split hi/lo tiles and fed by bulk
+// copies.
+#include "conv_common.cuh"
+
+namespace cb200 {
+
+struct GatherGeom {
+    const float* in;         // gathered tensor [Nb][Ci][Hi][Wi]
+    int Ci, Hi, Wi, HiWi, CiHiWi;
+    int Gp, Gq, M;           // row grid per image and rows in all (Nb * Gp * Gq)
+    int sp;                  // window stride on the input
+    int o;                   // window origin offset: h = p*sp + o + tap_r
+    int T;                   // taps per axis
+    int K;                   // reduction length (T*T*Ci)
+    int chan_fast;           // 1: tap-major / channel-fastest K order (Ci % 32 == 0)
+    FastDiv f_gpq, f_gq;     // row decode
+    FastDiv f_cchunks;       // Ci / 32 (channel-fastest)
+    FastDiv f_tt, f_t;       // T*T and T (generic order)
+};
+
+struct OutGeom {
+    float* out;              // [Nb][Co][Ho][Wo]
+    const float* bias;       // [Co] or null
+    int Co, Ho, Wo, HoWo;
+    int so;                  // output phase stride (1: plain NCHW)
+    int ncols;               // Co * so * so
+};
+
+template <int BN>
+struct ConvGatherProb {
+    static constexpr bool kBBulk = true;
+    static constexpr int kGroups = 3;
+    static constexpr Map kAMap = Map::RowFast;
+    static constexpr Map kBMap = Map::RowFast;   // unused (bulk)
+
+    GatherGeom g;
+    OutGeom o;
+    const float* bimg;
+    int m_tiles, n_tiles, k_stages;
+
+    __device__ int num_tiles() const { return m_tiles * n_tiles; }
+    __device__ Tile tile(int t) const
+    {
+        Tile r;
+        r.n0 = (t % n_tiles) * BN;
+        r.m0 = (t / n_tiles) * kBM;
+        r.ks0 = 0;
+        r.ks1 = k_stages;
+        r.grp = t % n_tiles;
+        return r;
+    }
+
+    struct AState {
+        int base;      // offset of in[n][0][h0][w0]
+        int h0, w0;    // window origin of this row
+    };
+    __device__ AState a_setup(const Tile& tl, int tid) const
+    {
+        AState s;
+        const int m = tl.m0 + tid;
+        if (m < g.M) {
+            uint32_t n, pq, p, q;
+            g.f_gpq.divmod(uint32_t(m), n, pq);
+            g.f_gq.divmod(pq, p, q);
+            s.h0 = int(p) * g.sp + g.o;
+            s.w0 = int(q) * g.sp + g.o;
+            s.base = int(n) * g.CiHiWi + s.h0 * g.Wi + s.w0;
+        } else {
+            s.h0 = -(1 << 24);   // no window position is ever inside
+            s.w0 = 0;
+            s.base = 0;
+        }
+        return s;
+    }
+
+    __device__ void load_a(const AState& s, const Tile&, int ks, int tid, float (&v)[32]) const
+    {
+        if (g.chan_fast) {
+            // One tap, 32 consecutive channels.
+            uint32_t tap, chunk, tr, tq;
+            g.f_cchunks.divmod(uint32_t(ks), tap, chunk);
+            g.f_t.divmod(tap, tr, tq);
+            const int h = s.h0 + int(tr);
+            const int w = s.w0 + int(tq);
+            if (unsigned(h) < unsigned(g.Hi) && unsigned(w) < unsigned(g.Wi)) {
+                const float* p = g.in + (s.base + int(chunk) * 32 * g.HiWi + int(tr) * g.Wi + int(tq));
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = __ldg(p + i * g.HiWi);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = 0.f;
+            }
+        } else {
+            // Generic order: lane l decodes k = ks*32 + l, the warp shares it.
+            const int k = ks * kBK + (tid & 31);
+            int koff = 0, krs = 0x7FFF0000;   // past K: the tap lands far outside
+            if (k < g.K) {
+                uint32_t c, rem, r, q;
+                g.f_tt.divmod(uint32_t(k), c, rem);
+                g.f_t.divmod(rem, r, q);
+                koff = int(c) * g.HiWi + int(r) * g.Wi + int(q);
+                krs = int((r << 16) | q);
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int off = __shfl_sync(0xffffffffu, koff, i);
+                const int rs = __shfl_sync(0xffffffffu, krs, i);
+                const int h = s.h0 + (rs >> 16);
+                const int w = s.w0 + (rs & 0xFFFF);
+                v[i] = (unsigned(h) < unsigned(g.Hi) && unsigned(w) < unsigned(g.Wi)) ? __ldg(g.in + (s.base + off))
+                                                                                        : 0.f;
+            }
+        }
+    }
+
+    struct BState {};
+    __device__ BState b_setup(const Tile&, int) const { return {}; }
+    __device__ void load_b(const BState&, const Tile&, int, int, int, float (&)[32]) const {}
+    __device__ const float* b_image(const Tile& tl, int ks) const
+    {
+        return bimg + (size_t(tl.grp) * k_stages + ks) * 2 * size_t(BN) * kBK;
+    }
+
+    struct EState {
+        float* opix;   // out[n][0][p*so][q*so]
+        bool valid;
+        int hrem, wrem;   // rows/cols of the output left below/right of this pixel's phase block
+    };
+    __device__ EState e_setup(const Tile& tl, int row) const
+    {
+        EState e;
+        const int m = tl.m0 + row;
+        e.valid = m < g.M;
+        uint32_t n = 0, pq = 0, p = 0, q = 0;
+        if (e.valid) {
+            g.f_gpq.divmod(uint32_t(m), n, pq);
+            g.f_gq.divmod(pq, p, q);
+        }
+        const int h = int(p) * o.so, w = int(q) * o.so;
+        e.hrem = o.Ho - h;
+        e.wrem = o.Wo - w;
+        e.opix = o.out + size_t(n) * o.Co * o.HoWo + size_t(h) * o.Wo + w;
+        return e;
+    }
+
+    __device__ void store(const EState& e, const Tile& tl, int, int c0, const uint32_t (&r)[32]) const
+    {
+        if (!e.valid) return;
+        if (o.so == 1) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int ch = tl.n0 + c0 + i;
+                if (ch < o.Co)
+                    e.opix[size_t(ch) * o.HoWo] = __uint_as_float(r[i]) + (o.bias ? __ldg(o.bias + ch) : 0.f);
+            }
+        } else {
+            const int ss = o.so * o.so;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int col = tl.n0 + c0 + i;
+                const int ch = col / ss, ab = col - ch * ss;
+                const int a = ab / o.so, b = ab - a * o.so;
+                if (ch < o.Co && a < e.hrem && b < e.wrem)
+                    e.opix[size_t(ch) * o.HoWo + a * o.Wo + b] = __uint_as_float(r[i]);
+            }
+        }
+    }
+};
+
+// ---------------------------------------------------------------------------
+// B operands (filters in the GEMM's K order)
+
+struct FwdFilterGen {   // B[k, kk] = W[k, c, r, q]
+    const float* w;
+    int C, R, chan_fast;
+    FastDiv f_c, f_r, f_rr;
+    __device__ float operator()(int k, int kk) const
+    {
+        uint32_t c, r, q;
+        if (chan_fast) {
+            uint32_t tap;
+            f_c.divmod(uint32_t(kk), tap, c);
+            f_r.divmod(tap, r, q);
+        } else {
+            uint32_t rem;
+            f_rr.divmod(uint32_t(kk), c, rem);
+            f_r.divmod(rem, r, q);
+        }
+        return __ldg(w + ((size_t(k) * C + c) * R + r) * R + q);
+    }
+};
+
+struct DgradFilterGen {   // B[(c, a, b), (d, e, k)] = W[k, c, a + pad - s*d, b + pad - s*e]
+    const float* w;
+    int C, K, R, S, pad, d_lo, chan_fast;
+    FastDiv f_k, f_t, f_tt, f_ss, f_s;
+    __device__ float operator()(int col, int kk) const
+    {
+        uint32_t c, ab, a, b, k, td, te;
+        f_ss.divmod(uint32_t(col), c, ab);
+        f_s.divmod(ab, a, b);
+        if (chan_fast) {
+            uint32_t tap;
+            f_k.divmod(uint32_t(kk), tap, k);
+            f_t.divmod(tap, td, te);
+        } else {
+            uint32_t rem;
+            f_tt.divmod(uint32_t(kk), k, rem);
+            f_t.divmod(rem, td, te);
+        }
+        const int r = int(a) + pad - S * (d_lo + int(td));
+        const int q = int(b) + pad - S * (d_lo + int(te));
+        if (r < 0 || r >= R || q < 0 || q >= R) return 0.f;
+        return __ldg(w + ((size_t(k) * C + c) * R + r) * R + q);
+    }
+};
+
+// Window of dy rows a phase can reach: d = (a + pad - r) / s over taps r and
+// phases a, i.e. d in [ceil((pad - R + 1) / s), floor((s - 1 + pad) / s)].
+static void dgrad_window(const ConvDims& d, int* d_lo, int* T)
+{
+    const int lo_num = d.pad - d.R + 1;   // may be negative
+    const int lo = lo_num >= 0 ? (lo_num + d.S - 1) / d.S : -((-lo_num) / d.S);
+    const int hi = (d.S - 1 + d.pad) / d.S;
+    *d_lo = lo;
+    *T = hi - lo + 1;
+}
+
+static GatherGeom make_gather(const float* in, int Nb, int Ci, int Hi, int Wi, int Gp, int Gq, int sp, int o, int T)
+{
+    GatherGeom g{};
+    g.in = in;
+    g.Ci = Ci;
+    g.Hi = Hi;
+    g.Wi = Wi;
+    g.HiWi = Hi * Wi;
+    g.CiHiWi = Ci * Hi * Wi;
+    g.Gp = Gp;
+    g.Gq = Gq;
+    g.M = Nb * Gp * Gq;
+    g.sp = sp;
+    g.o = o;
+    g.T = T;
+    g.K = T * T * Ci;
+    g.chan_fast = (Ci % 32 == 0) ? 1 : 0;
+    g.f_gpq = FastDiv(uint32_t(Gp * Gq));
+    g.f_gq = FastDiv(uint32_t(Gq));
+    g.f_cchunks = FastDiv(uint32_t(Ci % 32 == 0 ? Ci / 32 : 1));
+    g.f_tt = FastDiv(uint32_t(T * T));
+    g.f_t = FastDiv(uint32_t(T));
+    return g;
+}
+
+size_t conv_fwd_ws(const ConvDims& d)
+{
+    int n_tiles;
+    const int bn = pick_conv_bn(d.K, &n_tiles);
+    return bimage_floats(d.K, d.C * d.R * d.R, bn) * sizeof(float);
+}
+
+static int dgrad_cols(const ConvDims& d) { return d.C * d.S * d.S; }
+
+size_t conv_dgrad_ws(const ConvDims& d)
+{
+    int d_lo, T, n_tiles;
+    dgrad_window(d, &d_lo, &T);
+    const int bn = pick_conv_bn(dgrad_cols(d), &n_tiles);
+    return bimage_floats(dgrad_cols(d), T * T * d.K, bn) * sizeof(float);
+}
+
+template <int BN>
+static cudaError_t run_gather(const GatherGeom& g, const OutGeom& o, float* img, cudaStream_t st)
+{
+    ConvGatherProb<BN> p;
+    p.g = g;
+    p.o = o;
+    p.bimg = img;
+    p.m_tiles = (g.M + kBM - 1) / kBM;
+    p.n_tiles = (o.ncols + BN - 1) / BN;
+    p.k_stages = (g.K + kBK - 1) / kBK;
+    return launch_tc_gemm<ConvGatherProb<BN>, BN>(p, p.m_tiles * p.n_tiles, device_error_word(), st);
+}
+
+static cudaError_t dispatch_gather(int bn, const GatherGeom& g, const OutGeom& o, float* img, cudaStream_t st)
+{
+    switch (bn) {
+    case 32: return run_gather<32>(g, o, img, st);
+    case 64: return run_gather<64>(g, o, img, st);
+    case 128: return run_gather<128>(g, o, img, st);
+    case 192: return run_gather<192>(g, o, img, st);
+    default: return run_gather<256>(g, o, img, st);
+    }
+}
+
+cudaError_t launch_conv_fwd(const ConvDims& d, const float* x, const float* w, const float* b, float* y, void* ws,
+                            cudaStream_t st)
+{
+    int n_tiles;
+    const int bn = pick_conv_bn(d.K, &n_tiles);
+    const GatherGeom g = make_gather(x, d.N, d.C, d.H, d.W, d.P, d.Q, d.S, -d.pad, d.R);
+    OutGeom o{};
+    o.out = y;
+    o.bias = b;
+    o.Co = d.K;
+    o.Ho = d.P;
+    o.Wo = d.Q;
+    o.HoWo = d.P * d.Q;
+    o.so = 1;
+    o.ncols = d.K;
+    float* img = static_cast<float*>(ws);
+    FwdFilterGen gen{w, d.C, d.R, g.chan_fast, FastDiv(uint32_t(d.C)), FastDiv(uint32_t(d.R)),
+                     FastDiv(uint32_t(d.R * d.R))};
+    cudaError_t e = build_bimage(gen, d.K, g.K, bn, img, st);
+    if (e != cudaSuccess) return e;
+    return dispatch_gather(bn, g, o, img, st);
+}
+
+cudaError_t launch_conv_dgrad(const ConvDims& d, const float* w, const float* dy, float* dx, void* ws,
+                              cudaStream_t st)
+{
+    int d_lo, T, n_tiles;
+    dgrad_window(d, &d_lo, &T);
+    const int ncols = dgrad_cols(d);
+    const int bn = pick_conv_bn(ncols, &n_tiles);
+    const int Hs = (d.H + d.S - 1) / d.S, Ws = (d.W + d.S - 1) / d.S;
+    const GatherGeom g = make_gather(dy, d.N, d.K, d.P, d.Q, Hs, Ws, 1, d_lo, T);
+    OutGeom o{};
+    o.out = dx;
+    o.bias = nullptr;
+    o.Co = d.C;
+    o.Ho = d.H;
+    o.Wo = d.W;
+    o.HoWo = d.H * d.W;
+    o.so = d.S;
+    o.ncols = ncols;
+    float* img = static_cast<float*>(ws);
+    DgradFilterGen gen{w, d.C, d.K, d.R, d.S, d.pad, d_lo, g.chan_fast, FastDiv(uint32_t(d.K)),
+                       FastDiv(uint32_t(T)), FastDiv(uint32_t(T * T)), FastDiv(uint32_t(d.S * d.S)),
+                       FastDiv(uint32_t(d.S))};
+    cudaError_t e = build_bimage(gen, ncols, g.K, bn, img, st);
+    if (e != cudaSuccess) return e;
+    return dispatch_gather(bn, g, o, img, st);
+}
+
+}  // namespace cb200

@@ -22,6 +22,7 @@ namespace cb200 {
 template <int BN>
 struct ConvWgradProb {
     static constexpr bool kBBulk = false;
+    static constexpr int kGroups = 2;
     static constexpr Map kAMap = Map::ChunkFast;
     static constexpr Map kBMap = Map::ChunkFast;
 

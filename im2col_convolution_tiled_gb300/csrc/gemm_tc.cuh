@@ -8,15 +8,18 @@
 // hi*hi, hi*lo and lo*hi (the lo*lo term is below fp32 resolution).  The
 // tensor core accumulates in fp32.
 //
-// Warp roles (416 threads, one CTA per SM, persistent over output tiles):
-//   warps 0-3   A producers: gather a 128 x 32 slice of A, split, store it
-//               into the stage's hi/lo tiles (128-byte swizzled, K-major)
-//   warps 4-7   B producers: gather a BN x 32 slice of B the same way, or
-//               (bulk problems) warp 4 lane 0 copies a pre-split hi/lo image
-//               of the slice with one cp.async.bulk
-//   warp 8      allocates tensor memory; lane 0 issues the MMAs
-//   warps 9-12  epilogue: tcgen05.ld the accumulator, hand rows to the
-//               problem's store (bias, NCHW reshape, split-K partials ...)
+// Warp roles (one CTA per SM, persistent over output tiles):
+//   warps 0 .. 4G-1   G producer groups of 4 warps.  Pipeline stages are dealt
+//                     round-robin to the groups, so G stages' worth of global
+//                     loads are in flight at once.  For its stage a group
+//                     gathers the 128 x 32 slice of A and -- unless the problem
+//                     ships B as a pre-split image (one cp.async.bulk by the
+//                     group's first thread) -- the BN x 32 slice of B, splits
+//                     every value into hi/lo and stores both into the stage's
+//                     tiles (128-byte swizzled, K-major)
+//   warp 4G           allocates tensor memory; lane 0 issues the MMAs
+//   warps 4G+1..4G+4  epilogue: tcgen05.ld the accumulator, hand rows to the
+//                     problem's store (bias, NCHW reshape, split-K partials ...)
 // Two accumulators (2 x BN TMEM columns) let the epilogue of tile i overlap
 // the main loop of tile i+1.
 //
@@ -30,10 +33,14 @@ namespace cb200 {
 
 constexpr int kBM = 128;       // UMMA M: rows of a tile (TMEM lanes)
 constexpr int kBK = 32;        // K depth of one pipeline stage (one 128-byte swizzle row)
-constexpr int kThreads = 416;
-constexpr int kWarpMma = 8;
-constexpr int kWarpEpi0 = 9;
 constexpr size_t kSmemBudget = 200 * 1024;
+
+template <int G>
+struct Roles {
+    static constexpr int kWarpMma = 4 * G;
+    static constexpr int kThreads = (4 * G + 5) * 32;
+};
+
 
 struct Tile {
     int m0, n0;     // first row of A / of B (output row / column)
@@ -51,6 +58,16 @@ struct TileCfg {
     static constexpr uint32_t kTmemCols = (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
     static constexpr size_t kSmemBytes = size_t(kStages) * kStage + 1024 /*align*/ + 256 /*barriers*/;
     static constexpr uint32_t kIdesc = idesc_tf32(kBM, BN);
+};
+
+// Producer groups actually used: never more than the pipeline has stages.
+// A group waits on a slot's "empty" barrier by phase parity, which is only
+// sound while no waiter runs more than one phase ahead of the barrier; with
+// G <= S the stage a group fills next is at most S ahead of one it already
+// saw consumed.
+template <class Prob, int BN>
+struct Groups {
+    static constexpr int value = Prob::kGroups < TileCfg<BN>::kStages ? Prob::kGroups : TileCfg<BN>::kStages;
 };
 
 // Producer-side layout of a gathered 32-value slice (per thread):
@@ -93,10 +110,15 @@ struct SharedCtl {
 };
 
 template <class Prob, int BN>
-__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ Prob prob, int* err_word)
+__global__ void __launch_bounds__(Roles<Groups<Prob, BN>::value>::kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ Prob prob, int* err_word)
 {
     using Cfg = TileCfg<BN>;
     constexpr int S = Cfg::kStages;
+    constexpr int G = Groups<Prob, BN>::value;
+    static_assert(G >= 1 && G <= S, "producer groups must not outnumber pipeline stages");
+    constexpr int kWarpMma = Roles<G>::kWarpMma;
+    constexpr int kBPasses = BN > 128 ? 2 : 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + size_t(S) * Cfg::kStage);
@@ -111,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     auto b_lo = [&](int s) { return b_hi(s) + Cfg::kBTile; };
 
     if (threadIdx.x == 0) {
-        const uint32_t full_count = 4 + (Prob::kBBulk ? 1 : 4);
+        const uint32_t full_count = 4 + (Prob::kBBulk ? 1 : 0);
         for (int s = 0; s < S; ++s) {
             mbar_init(&ctl->full[s], full_count);
             mbar_init(&ctl->empty[s], 1);
@@ -136,81 +158,68 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         atomicOr(err_word, kDevErrTimeout);
     };
 
-    if (warp < 4) {
-        // ---------------- A producers ----------------
-        const int tid = threadIdx.x;   // 0..127
-        int stage = 0;
-        uint32_t phase = 0;
+    if (warp < 4 * G) {
+        // ---------------- producer groups ----------------
+        const int g = warp >> 2;
+        const int tid = threadIdx.x - 128 * g;   // 0..127 inside the group
+        uint32_t cnt = 0;                        // stages of this CTA so far (all groups agree)
+        int last_issued = -1;                    // last stage this group bulk-copied
         bool ok = true;
         for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
             const Tile tile = prob.tile(t);
-            typename Prob::AState st = prob.a_setup(tile, tid);
-            for (int ks = tile.ks0; ks < tile.ks1; ++ks) {
-                float v[32];
-                prob.load_a(st, tile, ks, tid, v);
-                if (!mbar_wait_warp(&ctl->empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
-                store_slice<Prob::kAMap>(a_hi(stage), a_lo(stage), 0, kBM, tid, v);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ctl->full[stage]);
-                if (++stage == S) { stage = 0; phase ^= 1; }
-            }
-        }
-        if (!ok) fail();
-    } else if (warp < 8) {
-        // ---------------- B producers ----------------
-        const int tid = threadIdx.x - 128;   // 0..127
-        int stage = 0;
-        uint32_t phase = 0;
-        bool ok = true;
-        if constexpr (Prob::kBBulk) {
-            if (tid == 0) {
-                int issued = 0;
-                for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                    const Tile tile = prob.tile(t);
-                    for (int ks = tile.ks0; ks < tile.ks1; ++ks) {
-                        if (!mbar_wait(&ctl->empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
-                        mbar_arrive_expect_tx(&ctl->full[stage], 2 * Cfg::kBTile);
-                        bulk_g2s(smem + (b_hi(stage) - smem_base), prob.b_image(tile, ks), 2 * Cfg::kBTile,
-                                 &ctl->full[stage]);
-                        ++issued;
-                        if (++stage == S) { stage = 0; phase ^= 1; }
-                    }
-                }
-                if (!ok) {
-                    fail();
-                    // Copies already issued land in stages the MMA never
-                    // consumed; wait (bounded) for each of them before exit.
-                    int s = stage, ph = phase;
-                    for (int i = 0; i < (issued < S ? issued : S); ++i) {
-                        if (--s < 0) { s = S - 1; ph ^= 1; }
-                        uint64_t t0 = globaltimer_ns();
-                        while (!mbar_try_wait(&ctl->full[s], ph) && globaltimer_ns() - t0 < kWaitLimitNs) {}
-                    }
-                }
-            }
-            __syncwarp();
-        } else {
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                const Tile tile = prob.tile(t);
-                typename Prob::BState st = prob.b_setup(tile, tid);
-                for (int ks = tile.ks0; ks < tile.ks1; ++ks) {
-                    float v[BN > 128 ? 2 : 1][32];
+            const int nks = tile.ks1 - tile.ks0;
+            const int first = int((uint32_t(g) + uint32_t(G) - cnt % uint32_t(G)) % uint32_t(G));
+            if (first < nks) {
+                typename Prob::AState ast = prob.a_setup(tile, tid);
+                typename Prob::BState bst = prob.b_setup(tile, tid);
+                for (int i = first; i < nks; i += G) {
+                    const uint32_t c = cnt + uint32_t(i);
+                    const int slot = int(c % uint32_t(S));
+                    const uint32_t phase = (c / uint32_t(S)) & 1u;
+                    const int ks = tile.ks0 + i;
+                    float va[32];
+                    prob.load_a(ast, tile, ks, tid, va);
+                    float vb[kBPasses][32];
+                    if constexpr (!Prob::kBBulk) {
 #pragma unroll
-                    for (int pass = 0; pass < (BN > 128 ? 2 : 1); ++pass) prob.load_b(st, tile, ks, pass, tid, v[pass]);
-                    if (!mbar_wait_warp(&ctl->empty[stage], phase ^ 1, abort_flag)) { ok = false; break; }
+                        for (int pass = 0; pass < kBPasses; ++pass) prob.load_b(bst, tile, ks, pass, tid, vb[pass]);
+                    }
+                    if (!mbar_wait_warp(&ctl->empty[slot], phase ^ 1u, abort_flag)) { ok = false; break; }
+                    if constexpr (Prob::kBBulk) {
+                        if (tid == 0) {
+                            mbar_arrive_expect_tx(&ctl->full[slot], 2 * Cfg::kBTile);
+                            bulk_g2s(smem + (b_hi(slot) - smem_base), prob.b_image(tile, ks), 2 * Cfg::kBTile,
+                                     &ctl->full[slot]);
+                            last_issued = int(c);
+                        }
+                    }
+                    store_slice<Prob::kAMap>(a_hi(slot), a_lo(slot), 0, kBM, tid, va);
+                    if constexpr (!Prob::kBBulk) {
 #pragma unroll
-                    for (int pass = 0; pass < (BN > 128 ? 2 : 1); ++pass) {
-                        const int rows = BN - 128 * pass < 128 ? BN - 128 * pass : 128;
-                        store_slice<Prob::kBMap>(b_hi(stage), b_lo(stage), 128 * pass, rows, tid, v[pass]);
+                        for (int pass = 0; pass < kBPasses; ++pass) {
+                            const int rows = BN - 128 * pass < 128 ? BN - 128 * pass : 128;
+                            store_slice<Prob::kBMap>(b_hi(slot), b_lo(slot), 128 * pass, rows, tid, vb[pass]);
+                        }
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&ctl->full[stage]);
-                    if (++stage == S) { stage = 0; phase ^= 1; }
+                    if (lane == 0) mbar_arrive(&ctl->full[slot]);
                 }
             }
-            if (!ok) fail();
+            cnt += uint32_t(nks);
+        }
+        if (!ok) {
+            fail();
+            if (Prob::kBBulk && tid == 0 && last_issued >= 0) {
+                // Bulk copies already issued may still be landing in stages the
+                // MMA will not consume; wait (bounded) for each before exit.
+                for (int c = last_issued; c >= 0 && c > last_issued - S; c -= G) {
+                    uint64_t t0 = globaltimer_ns();
+                    while (!mbar_try_wait(&ctl->full[c % S], uint32_t(c / S) & 1u) &&
+                           globaltimer_ns() - t0 < kWaitLimitNs) {
+                    }
+                }
+            }
         }
     } else if (warp == kWarpMma) {
         // ---------------- MMA issuer ----------------
@@ -308,7 +317,8 @@ cudaError_t launch_tc_gemm(const Prob& prob, int num_tiles, int* err_word, cudaS
     }
     if (num_tiles <= 0) return cudaSuccess;
     int grid = num_tiles < sm_count() ? num_tiles : sm_count();
-    tc_gemm_kernel<Prob, BN><<<grid, kThreads, Cfg::kSmemBytes, stream>>>(prob, err_word);
+    tc_gemm_kernel<Prob, BN><<<grid, Roles<Groups<Prob, BN>::value>::kThreads, Cfg::kSmemBytes, stream>>>(prob,
+                                                                                                    err_word);
     note_launch();
     return cudaGetLastError();
 }

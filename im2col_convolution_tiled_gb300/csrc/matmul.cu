@@ -15,6 +15,7 @@ namespace cb200 {
 template <unsigned FLAGS, int BN>
 struct MatmulProb {
     static constexpr bool kBBulk = false;
+    static constexpr int kGroups = 2;
     static constexpr Map kAMap = (FLAGS & 1u) ? Map::RowFast : Map::ChunkFast;
     static constexpr Map kBMap = (FLAGS & 2u) ? Map::ChunkFast : Map::RowFast;
 

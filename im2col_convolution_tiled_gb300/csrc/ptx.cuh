@@ -206,20 +206,16 @@ __host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t
 }
 
 // ---------------------------------------------------------------------------
-// 3xTF32 split: a = hi + lo with hi = tf32(a) (round to nearest, ties away)
-// and lo = tf32(a - hi); a*b ~= hi_a*hi_b + hi_a*lo_b + lo_a*hi_b.
-
-__device__ __forceinline__ uint32_t to_tf32(float a)
-{
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(a));
-    return r;
-}
+// 3xTF32 split: a = hi + lo with hi = a truncated to tf32 (low 13 mantissa
+// bits cleared: exactly representable, so the tensor core takes it as is) and
+// lo = a - hi (exact in fp32; the tensor core keeps its top 11 significant
+// bits).  a*b ~= hi_a*hi_b + hi_a*lo_b + lo_a*hi_b with a relative error of a
+// few 2^-21 per product; lo_a*lo_b (< 2^-20 |ab|) is dropped.
 
 __device__ __forceinline__ void split_tf32(float a, uint32_t& hi, uint32_t& lo)
 {
-    hi = to_tf32(a);
-    lo = to_tf32(a - __uint_as_float(hi));
+    hi = __float_as_uint(a) & 0xFFFFE000u;
+    lo = __float_as_uint(a - __uint_as_float(hi));
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
