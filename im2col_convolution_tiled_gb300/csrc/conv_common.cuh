@@ -32,35 +32,41 @@ inline size_t bimage_floats(int n_rows, int k_total, int bn)
 // of one pipeline stage's B tiles, so one bulk copy moves it.  Rows past
 // n_rows and columns past k_total are zero.
 //
-// Gen(row, k) returns the (unsplit) B element.
+// Gen(row, k) returns the (unsplit) B element.  One thread builds one 16-byte
+// chunk (4 consecutive k of one row) of the hi and of the lo tile; blockIdx.y
+// is the row, so consecutive threads read consecutive k.
 template <class Gen>
-__global__ void build_bimage_kernel(Gen gen, int n_rows, int k_total, int bn, float* img)
+__global__ void build_bimage_kernel(Gen gen, int n_rows, int k_total, int bn, int k_stages, float* img)
 {
-    const int k_stages = (k_total + kBK - 1) / kBK;
-    const int n_tiles = (n_rows + bn - 1) / bn;
-    const long long total = (long long)n_tiles * bn * k_stages * kBK;
-    for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
-         e += (long long)gridDim.x * blockDim.x) {
-        const int k = int(e % (k_stages * kBK));
-        const int row = int(e / (k_stages * kBK));
-        float v = (row < n_rows && k < k_total) ? gen(row, k) : 0.f;
-        uint32_t hi, lo;
-        split_tf32(v, hi, lo);
-        const int nt = row / bn, r = row % bn, ks = k / kBK, kk = k % kBK;
+    const int row = blockIdx.y;
+    const int chunks = k_stages * (kBK / 4);
+    const int nt = row / bn, r = row % bn;
+    for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < chunks; t += gridDim.x * blockDim.x) {
+        const int k0 = t * 4;
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float v = (row < n_rows && k0 + e < k_total) ? gen(row, k0 + e) : 0.f;
+            split_tf32(v, hi[e], lo[e]);
+        }
+        const int ks = t / (kBK / 4), c = t % (kBK / 4);
         float* blk = img + ((size_t(nt) * k_stages + ks) * 2) * size_t(bn) * kBK;
-        const uint32_t off = sw128_offset(uint32_t(r), uint32_t(kk >> 2)) / 4 + (kk & 3);
-        reinterpret_cast<uint32_t*>(blk)[off] = hi;
-        reinterpret_cast<uint32_t*>(blk)[size_t(bn) * kBK + off] = lo;
+        const uint32_t off = sw128_offset(uint32_t(r), uint32_t(c)) / 4;
+        *reinterpret_cast<uint4*>(blk + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(blk + size_t(bn) * kBK + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
 }
 
 template <class Gen>
 cudaError_t build_bimage(const Gen& gen, int n_rows, int k_total, int bn, float* img, cudaStream_t st)
 {
-    const long long total = (long long)((n_rows + bn - 1) / bn) * bn * ((k_total + kBK - 1) / kBK) * kBK;
-    long long blocks = (total + 255) / 256;
-    if (blocks > 4LL * sm_count() * 8) blocks = 4LL * sm_count() * 8;
-    build_bimage_kernel<Gen><<<int(blocks), 256, 0, st>>>(gen, n_rows, k_total, bn, img);
+    const int n_tiles = (n_rows + bn - 1) / bn;
+    const int k_stages = (k_total + kBK - 1) / kBK;
+    const int chunks = k_stages * (kBK / 4);
+    int bx = (chunks + 255) / 256;
+    if (bx > 1024) bx = 1024;
+    dim3 grid(bx, n_tiles * bn);
+    build_bimage_kernel<Gen><<<grid, 256, 0, st>>>(gen, n_rows, k_total, bn, k_stages, img);
     note_launch();
     return cudaGetLastError();
 }

@@ -59,7 +59,7 @@ struct OutGeom {
 template <int BN>
 struct ConvGatherProb {
     static constexpr bool kBBulk = true;
-    static constexpr int kGroups = 3;
+    static constexpr int kGroups = 2;
     static constexpr Map kAMap = Map::RowFast;
     static constexpr Map kBMap = Map::RowFast;   // unused (bulk)
 

@@ -13,22 +13,25 @@
 // result is deterministic.  Each range's tensor-core accumulation chain is
 // bounded by its length.
 //
-// Both operands are gathered ChunkFast: a thread holds 4 consecutive j of 8
-// rows, so 8 lanes read 32 consecutive pixels of one row.
+// The A operand (column matrix) is gathered ChunkFast: a thread holds 4
+// consecutive j of 8 rows, so 8 lanes read 32 consecutive pixels of one row.
+// The B operand G is dy itself, re-laid once per call as pre-split hi/lo
+// tiles (one streaming pass over dy) and fed by bulk copies, so the producers
+// spend their issue slots on the gather that needs them.
 #include "conv_common.cuh"
 
 namespace cb200 {
 
 template <int BN>
 struct ConvWgradProb {
-    static constexpr bool kBBulk = false;
+    static constexpr bool kBBulk = true;
     static constexpr int kGroups = 2;
     static constexpr Map kAMap = Map::ChunkFast;
-    static constexpr Map kBMap = Map::ChunkFast;
+    static constexpr Map kBMap = Map::ChunkFast;   // unused (bulk)
 
     const float* x;
-    const float* dy;
-    float* out;   // dW (splits == 1) or partials [split][K][CRS]
+    const float* bimg;   // G as pre-split tiles
+    float* out;          // dW (splits == 1) or partials [split][K][CRS]
     int C, H, W, K, R, S, pad, P, Q;
     int PQ, NPQ, CRS, HW, CHW;
     FastDiv f_pq, f_q, f_rr, f_r;
@@ -114,32 +117,11 @@ struct ConvWgradProb {
 
     struct BState {};
     __device__ BState b_setup(const Tile&, int) const { return {}; }
-
-    __device__ void load_b(const BState&, const Tile& tl, int ks, int pass, int tid, float (&v)[32]) const
+    __device__ void load_b(const BState&, const Tile&, int, int, int, float (&)[32]) const {}
+    __device__ const float* b_image(const Tile& tl, int ks) const
     {
-        const int j0 = ks * kBK + 4 * (tid & 7);
-        int dbase[4];
-        bool jv[4];
-        {
-            uint32_t n, pq;
-            f_pq.divmod(uint32_t(j0 < NPQ ? j0 : 0), n, pq);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                jv[e] = j0 + e < NPQ;
-                dbase[e] = int(n) * K * PQ + int(pq);
-                if (++pq == uint32_t(PQ)) { pq = 0; ++n; }
-            }
-        }
-#pragma unroll
-        for (int p = 0; p < 8; ++p) {
-            const int k = tl.n0 + 128 * pass + (tid >> 3) + 16 * p;
-            const bool kv = k < K;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) v[4 * p + e] = (kv && jv[e]) ? __ldg(dy + (dbase[e] + k * PQ)) : 0.f;
-        }
+        return bimg + (size_t(tl.n0 / BN) * k_stages + ks) * 2 * size_t(BN) * kBK;
     }
-
-    __device__ const float* b_image(const Tile&, int) const { return nullptr; }
 
     struct EState {
         float* o;   // out + crs, filter stride CRS
@@ -162,6 +144,19 @@ struct ConvWgradProb {
             const int k = tl.n0 + c + i;
             if (k < K) e.o[size_t(k) * CRS] = __uint_as_float(r[i]);
         }
+    }
+};
+
+// B[k, j] = G[k, j] = dy[n, k, pq] with j = n*PQ + pq (conv_grad_reshape).
+struct GradGen {
+    const float* dy;
+    int K, PQ;
+    FastDiv f_pq;
+    __device__ float operator()(int k, int j) const
+    {
+        uint32_t n, pq;
+        f_pq.divmod(uint32_t(j), n, pq);
+        return __ldg(dy + (size_t(n) * K + k) * PQ + pq);
     }
 };
 
@@ -198,10 +193,17 @@ static WgradPlan plan_wgrad(const ConvDims& d)
     return pl;
 }
 
+// Workspace: the G image, then (split-K only) the partial tiles.
+static size_t wgrad_image_floats(const ConvDims& d, const WgradPlan& pl)
+{
+    return bimage_floats(d.K, d.N * d.P * d.Q, pl.bn);
+}
+
 size_t conv_wgrad_ws(const ConvDims& d)
 {
     WgradPlan pl = plan_wgrad(d);
-    return pl.splits > 1 ? size_t(pl.splits) * d.K * d.C * d.R * d.R * sizeof(float) : 0;
+    const size_t part = pl.splits > 1 ? size_t(pl.splits) * d.K * d.C * d.R * d.R : 0;
+    return (wgrad_image_floats(d, pl) + part) * sizeof(float);
 }
 
 template <int BN>
@@ -209,9 +211,11 @@ static cudaError_t run_wgrad(const ConvDims& d, const WgradPlan& pl, const float
                              void* ws, cudaStream_t st)
 {
     ConvWgradProb<BN> p;
+    float* img = static_cast<float*>(ws);
+    float* part = img + wgrad_image_floats(d, pl);
     p.x = x;
-    p.dy = dy;
-    p.out = pl.splits > 1 ? static_cast<float*>(ws) : dw;
+    p.bimg = img;
+    p.out = pl.splits > 1 ? part : dw;
     p.C = d.C; p.H = d.H; p.W = d.W; p.K = d.K; p.R = d.R; p.S = d.S; p.pad = d.pad; p.P = d.P; p.Q = d.Q;
     p.PQ = d.P * d.Q;
     p.NPQ = d.N * p.PQ;
@@ -227,12 +231,14 @@ static cudaError_t run_wgrad(const ConvDims& d, const WgradPlan& pl, const float
     p.k_stages = pl.k_stages;
     p.splits = pl.splits;
     p.ks_per_split = pl.ks_per_split;
-    cudaError_t e = launch_tc_gemm<ConvWgradProb<BN>, BN>(p, p.m_tiles * p.n_tiles * p.splits, device_error_word(), st);
+    cudaError_t e = build_bimage(GradGen{dy, d.K, p.PQ, FastDiv(uint32_t(p.PQ))}, d.K, p.NPQ, BN, img, st);
+    if (e != cudaSuccess) return e;
+    e = launch_tc_gemm<ConvWgradProb<BN>, BN>(p, p.m_tiles * p.n_tiles * p.splits, device_error_word(), st);
     if (e != cudaSuccess || pl.splits == 1) return e;
     const long long count = (long long)d.K * p.CRS;
     long long blocks = (count + 255) / 256;
     if (blocks > 8LL * sm_count()) blocks = 8LL * sm_count();
-    wgrad_reduce_kernel<<<int(blocks), 256, 0, st>>>(static_cast<const float*>(ws), pl.splits, count, dw);
+    wgrad_reduce_kernel<<<int(blocks), 256, 0, st>>>(part, pl.splits, count, dw);
     note_launch();
     return cudaGetLastError();
 }

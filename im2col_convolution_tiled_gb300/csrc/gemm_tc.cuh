@@ -172,19 +172,18 @@ __global__ void __launch_bounds__(Roles<Groups<Prob, BN>::value>::kThreads, 1)
             if (first < nks) {
                 typename Prob::AState ast = prob.a_setup(tile, tid);
                 typename Prob::BState bst = prob.b_setup(tile, tid);
-                for (int i = first; i < nks; i += G) {
+                // Everything for stage i except the A gather (already in va).
+                auto produce = [&](int i, const float (&va)[32]) -> bool {
                     const uint32_t c = cnt + uint32_t(i);
                     const int slot = int(c % uint32_t(S));
                     const uint32_t phase = (c / uint32_t(S)) & 1u;
                     const int ks = tile.ks0 + i;
-                    float va[32];
-                    prob.load_a(ast, tile, ks, tid, va);
                     float vb[kBPasses][32];
                     if constexpr (!Prob::kBBulk) {
 #pragma unroll
                         for (int pass = 0; pass < kBPasses; ++pass) prob.load_b(bst, tile, ks, pass, tid, vb[pass]);
                     }
-                    if (!mbar_wait_warp(&ctl->empty[slot], phase ^ 1u, abort_flag)) { ok = false; break; }
+                    if (!mbar_wait_warp(&ctl->empty[slot], phase ^ 1u, abort_flag)) return false;
                     if constexpr (Prob::kBBulk) {
                         if (tid == 0) {
                             mbar_arrive_expect_tx(&ctl->full[slot], 2 * Cfg::kBTile);
@@ -204,6 +203,27 @@ __global__ void __launch_bounds__(Roles<Groups<Prob, BN>::value>::kThreads, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&ctl->full[slot]);
+                    return true;
+                };
+                if constexpr (Prob::kBBulk) {
+                    // A gathers run one owned stage ahead: while stage i is
+                    // split and stored, the loads of stage i + G are in flight
+                    // (two register buffers, used in turn).
+                    float v0[32], v1[32];
+                    prob.load_a(ast, tile, tile.ks0 + first, tid, v0);
+                    for (int i = first; i < nks; i += 2 * G) {
+                        if (i + G < nks) prob.load_a(ast, tile, tile.ks0 + i + G, tid, v1);
+                        if (!produce(i, v0)) { ok = false; break; }
+                        if (i + G >= nks) break;
+                        if (i + 2 * G < nks) prob.load_a(ast, tile, tile.ks0 + i + 2 * G, tid, v0);
+                        if (!produce(i + G, v1)) { ok = false; break; }
+                    }
+                } else {
+                    for (int i = first; i < nks; i += G) {
+                        float va[32];
+                        prob.load_a(ast, tile, tile.ks0 + i, tid, va);
+                        if (!produce(i, va)) { ok = false; break; }
+                    }
                 }
             }
             cnt += uint32_t(nks);

@@ -168,9 +168,115 @@ __global__ void maxpool_fwd_kernel(const float* __restrict__ x, float* __restric
     }
 }
 
+// Plane-staged variant: a block copies whole (n, c) planes of x into shared
+// memory with coalesced loads, then each thread scans its windows there and
+// writes y / idx coalesced.  x is read from HBM exactly once.
+constexpr int kPoolThreads = 256;
+constexpr int kPoolSmemFloats = 8192;   // 32 KB of staged planes per block
+
+__global__ void __launch_bounds__(kPoolThreads) maxpool_fwd_plane_kernel(
+    const float* __restrict__ x, float* __restrict__ y, int32_t* __restrict__ idx, int NC, int H, int W, int k, int S,
+    int P, int Q, int ppb, FastDiv f_pq, FastDiv f_q)
+{
+    extern __shared__ float sx[];
+    const int HW = H * W, PQ = P * Q;
+    for (int nc0 = blockIdx.x * ppb; nc0 < NC; nc0 += gridDim.x * ppb) {
+        const int np = min(ppb, NC - nc0);
+        const float* src = x + size_t(nc0) * HW;
+        const int total = np * HW;
+#pragma unroll 4
+        for (int i = threadIdx.x; i < total; i += kPoolThreads) sx[i] = __ldg(src + i);
+        __syncthreads();
+        const int nout = np * PQ;
+        for (int o = threadIdx.x; o < nout; o += kPoolThreads) {
+            uint32_t pl, pq, oh, ow;
+            f_pq.divmod(uint32_t(o), pl, pq);
+            f_q.divmod(pq, oh, ow);
+            const int corner = int(pl) * HW + int(oh) * S * W + int(ow) * S;
+            int best = corner;
+            float m = sx[corner];
+            for (int r = 0; r < k; ++r)
+                for (int q = 0; q < k; ++q) {
+                    const int at = corner + r * W + q;
+                    const float v = sx[at];
+                    if (v > m) {
+                        m = v;
+                        best = at;
+                    }
+                }
+            y[size_t(nc0) * PQ + o] = m;
+            idx[size_t(nc0) * PQ + o] = nc0 * HW + best;
+        }
+        __syncthreads();
+    }
+}
+
+// Plane-staged backward: a block stages the windows' gradients and indices of
+// whole planes, then each thread gathers, in ascending window order, the
+// gradients routed to its input pixel and writes dx coalesced.  The window
+// rows covering input row h (and columns covering w) come from small tables
+// built once per block, so the per-pixel work is table lookups and compares.
+__global__ void __launch_bounds__(kPoolThreads) maxpool_bwd_plane_kernel(
+    const float* __restrict__ dy, const int32_t* __restrict__ idx, float* __restrict__ dx, int NC, int H, int W,
+    int k, int S, int P, int Q, int ppb, FastDiv f_hw, FastDiv f_w)
+{
+    extern __shared__ float sm[];
+    const int HW = H * W, PQ = P * Q;
+    float* sdy = sm;
+    int* sidx = reinterpret_cast<int*>(sm + ppb * PQ);
+    int* hrange = sidx + ppb * PQ;   // (first window row << 16) | last window row, per input row
+    int* wrange = hrange + H;        // same per input column
+    for (int i = threadIdx.x; i < H + W; i += kPoolThreads) {
+        const int v = i < H ? i : i - H;
+        const int lim = i < H ? P - 1 : Q - 1;
+        const int lo = v - k + 1 <= 0 ? 0 : (v - k + S) / S;
+        const int hi = min(v / S, lim);
+        (i < H ? hrange[i] : wrange[i - H]) = (lo << 16) | (hi & 0xFFFF);
+    }
+    for (int nc0 = blockIdx.x * ppb; nc0 < NC; nc0 += gridDim.x * ppb) {
+        const int np = min(ppb, NC - nc0);
+        const int nwin = np * PQ;
+#pragma unroll 4
+        for (int i = threadIdx.x; i < nwin; i += kPoolThreads) {
+            sdy[i] = __ldg(dy + size_t(nc0) * PQ + i);
+            sidx[i] = __ldg(idx + size_t(nc0) * PQ + i);
+        }
+        __syncthreads();
+        const int total = np * HW;
+        for (int i = threadIdx.x; i < total; i += kPoolThreads) {
+            uint32_t pl, hw, h, w;
+            f_hw.divmod(uint32_t(i), pl, hw);
+            f_w.divmod(hw, h, w);
+            const int flat = nc0 * HW + i;
+            const int hr = hrange[h], wr = wrange[w];
+            const int oh_lo = hr >> 16, oh_hi = hr & 0xFFFF;   // oh_hi < oh_lo: no window
+            const int ow_lo = wr >> 16, ow_hi = wr & 0xFFFF;
+            const int* irow = sidx + int(pl) * PQ;
+            const float* drow = sdy + int(pl) * PQ;
+            float acc = 0.f;
+            for (int oh = oh_lo; oh <= oh_hi; ++oh)
+                for (int ow = ow_lo; ow <= ow_hi; ++ow) {
+                    const int o = oh * Q + ow;
+                    if (irow[o] == flat) acc += drow[o];
+                }
+            dx[size_t(nc0) * HW + i] = acc;
+        }
+        __syncthreads();
+    }
+}
+
 cudaError_t launch_maxpool_fwd(int N, int C, int H, int W, int k, int s, int P, int Q, const float* x, float* y,
                                int32_t* idx, cudaStream_t st)
 {
+    const int NC = N * C;
+    if (H * W <= kPoolSmemFloats) {
+        const int ppb = kPoolSmemFloats / (H * W) < 8 ? kPoolSmemFloats / (H * W) : 8;
+        const int blocks = (NC + ppb - 1) / ppb;
+        maxpool_fwd_plane_kernel<<<blocks, kPoolThreads, size_t(ppb) * H * W * sizeof(float), st>>>(
+            x, y, idx, NC, H, W, k, s, P, Q, ppb, FastDiv(P * Q), FastDiv(Q));
+        note_launch();
+        return cudaGetLastError();
+    }
     const long long total = (long long)N * C * P * Q;
     maxpool_fwd_kernel<<<grid_for(total, 256), 256, 0, st>>>(x, y, idx, H, W, k, s, FastDiv(Q), FastDiv(P),
                                                              int(total));
@@ -207,6 +313,16 @@ __global__ void maxpool_bwd_kernel(const float* __restrict__ dy, const int32_t* 
 cudaError_t launch_maxpool_bwd(int N, int C, int H, int W, int k, int s, int P, int Q, const float* dy,
                                const int32_t* idx, float* dx, cudaStream_t st)
 {
+    const int NC = N * C;
+    if (P * Q * 2 + H + W <= kPoolSmemFloats) {
+        int ppb = (kPoolSmemFloats - H - W) / (2 * P * Q);
+        if (ppb > 8) ppb = 8;
+        const int blocks = (NC + ppb - 1) / ppb;
+        maxpool_bwd_plane_kernel<<<blocks, kPoolThreads, (size_t(ppb) * P * Q * 2 + H + W) * sizeof(float), st>>>(
+            dy, idx, dx, NC, H, W, k, s, P, Q, ppb, FastDiv(H * W), FastDiv(W));
+        note_launch();
+        return cudaGetLastError();
+    }
     const long long total = (long long)N * C * H * W;
     maxpool_bwd_kernel<<<grid_for(total, 256), 256, 0, st>>>(dy, idx, dx, k, s, P, Q, FastDiv(W), FastDiv(H),
                                                              int(total));
@@ -259,39 +375,55 @@ constexpr int kBiasCluster = 8;
 constexpr int kBiasThreads = 512;
 
 __global__ void __cluster_dims__(kBiasCluster, 1, 1) __launch_bounds__(kBiasThreads)
-    bias_grad_kernel(const float* __restrict__ dy, float* __restrict__ db, int N, int K, int PQ)
+    bias_grad_kernel(const float* __restrict__ dy, float* __restrict__ db, int N, int K, int PQ, FastDiv f_pq)
 {
     cg::cluster_group cluster = cg::this_cluster();
     __shared__ float warp_part[kBiasThreads / 32];
     __shared__ float cta_part;
     const int k = blockIdx.x / kBiasCluster;
     const int rank = int(cluster.block_rank());
-    float acc = 0.f;
-    for (int n = rank; n < N; n += kBiasCluster) {
-        const float* plane = dy + ((size_t)n * K + k) * PQ;
-        for (int i = threadIdx.x; i < PQ; i += kBiasThreads) acc += __ldg(plane + i);
+    // This CTA sums images n = rank, rank + 8, ...: element e of that list is
+    // (image rank + 8 * (e / PQ), pixel e % PQ).  Eight independent partial
+    // sums per thread keep eight loads in flight; they are combined in a
+    // fixed order, so the result is deterministic.
+    const int images = (N - rank + kBiasCluster - 1) / kBiasCluster;
+    const int total = images * PQ;
+    float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int e0 = threadIdx.x; e0 < total; e0 += 8 * kBiasThreads) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int e = e0 + u * kBiasThreads;
+            if (e < total) {
+                uint32_t nl, pq;
+                f_pq.divmod(uint32_t(e), nl, pq);
+                const int n = rank + kBiasCluster * int(nl);
+                part[u] += __ldg(dy + (size_t(n) * K + k) * PQ + pq);
+            }
+        }
     }
+    float acc = ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if ((threadIdx.x & 31) == 0) warp_part[threadIdx.x >> 5] = acc;
     __syncthreads();
     if (threadIdx.x == 0) {
-        float s = 0.f;
-        for (int i = 0; i < kBiasThreads / 32; ++i) s += warp_part[i];
-        cta_part = s;
+        float t = 0.f;
+        for (int i = 0; i < kBiasThreads / 32; ++i) t += warp_part[i];
+        cta_part = t;
     }
     cluster.sync();
     if (rank == 0 && threadIdx.x == 0) {
-        float s = 0.f;
-        for (int r = 0; r < kBiasCluster; ++r) s += *cluster.map_shared_rank(&cta_part, r);
-        db[k] = s;
+        float t = 0.f;
+        for (int r = 0; r < kBiasCluster; ++r) t += *cluster.map_shared_rank(&cta_part, r);
+        db[k] = t;
     }
     cluster.sync();   // keep every CTA's shared memory alive until rank 0 has read it
 }
 
 cudaError_t launch_bias_grad(const ConvDims& d, const float* dy, float* db, cudaStream_t st)
 {
-    bias_grad_kernel<<<d.K * kBiasCluster, kBiasThreads, 0, st>>>(dy, db, d.N, d.K, d.P * d.Q);
+    bias_grad_kernel<<<d.K * kBiasCluster, kBiasThreads, 0, st>>>(dy, db, d.N, d.K, d.P * d.Q,
+                                                                  FastDiv(d.P * d.Q));
     note_launch();
     return cudaGetLastError();
 }
