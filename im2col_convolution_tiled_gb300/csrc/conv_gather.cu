@@ -22,14 +22,16 @@
 // exactly one accumulator: col2im needs no scatter, no atomics and no column
 // buffer.
 //
-// K order of both: tap-major, channel-fastest -- k = (tap_r * T + tap_q) * Ci + ci --
-// when Ci (channels of the gathered tensor) is a multiple of 32: a pipeline
-// stage then holds 32 channels of ONE tap, so its bounds test is done once
-// per stage and every element is one add and one load.  Otherwise
-// k = (ci * T + tap_r) * T + tap_q with a per-element decode shared across the
-// warp.  The B operand (filters, rearranged and zero-padded to the same K
-// order) is laid out once per call as pre-split hi/lo tiles and fed by bulk
-// copies.
+// K order of both: tap-major, channel-fastest -- k = (tap_r * T + tap_q) * Cp + ci,
+// with the channels of the gathered tensor padded to Cp: Cp = Ci when Ci is
+// a multiple of 32 (a pipeline stage then holds 32 channels of ONE tap; also
+// 32 when 16 < Ci < 32), and the next power of two when Ci <= 16 (a stage
+// holds 32 / Cp whole taps).  The
+// bounds test is then done once per tap and every element is one add and one
+// load.  Any other Ci uses k = (ci * T + tap_r) * T + tap_q with a per-element
+// decode shared across the warp.  The B operand (filters, rearranged and
+// zero-padded to the same K order) is laid out once per call as pre-split
+// hi/lo tiles and fed by bulk copies.
 #include "conv_common.cuh"
 
 namespace cb200 {
@@ -41,12 +43,33 @@ struct GatherGeom {
     int sp;                  // window stride on the input
     int o;                   // window origin offset: h = p*sp + o + tap_r
     int T;                   // taps per axis
-    int K;                   // reduction length (T*T*Ci)
-    int chan_fast;           // 1: tap-major / channel-fastest K order (Ci % 32 == 0)
+    int mode;                // K order: 0 chunk of one tap, 1 tap group (Ci <= 16), 2 generic
+    int Cp, lcp;             // padded channels (modes 0/1) and log2 Cp (mode 1)
+    int K;                   // reduction length: T*T*Cp (modes 0/1), T*T*Ci (mode 2)
     FastDiv f_gpq, f_gq;     // row decode
-    FastDiv f_cchunks;       // Ci / 32 (channel-fastest)
-    FastDiv f_tt, f_t;       // T*T and T (generic order)
+    FastDiv f_cchunks;       // Cp / 32 (mode 0)
+    FastDiv f_tt, f_t;       // T*T and T
 };
+
+// K order of a gather over a tensor with `ci` channels (see top of file).
+static inline void k_order(int ci, int* mode, int* cp, int* lcp)
+{
+    if (ci % 32 == 0 || (ci > 16 && ci < 32)) {
+        *mode = 0;
+        *cp = (ci + 31) / 32 * 32;
+        *lcp = 0;
+    } else if (ci < 32) {
+        int l = 0;
+        while ((1 << l) < ci) ++l;
+        *mode = 1;
+        *cp = 1 << l;
+        *lcp = l;
+    } else {
+        *mode = 2;
+        *cp = ci;
+        *lcp = 0;
+    }
+}
 
 struct OutGeom {
     float* out;              // [Nb][Co][Ho][Wo]
@@ -103,22 +126,47 @@ struct ConvGatherProb {
         return s;
     }
 
+    // Mode 1: 32 / CP taps per stage, CP channels each.
+    template <int LCP>
+    __device__ __forceinline__ void load_taps(const AState& s, int ks, float (&v)[32]) const
+    {
+        constexpr int CP = 1 << LCP, TPS = 32 >> LCP;
+        const int TT = g.T * g.T;
+#pragma unroll
+        for (int t = 0; t < TPS; ++t) {
+            const int tap = ks * TPS + t;
+            uint32_t tr, tq;
+            g.f_t.divmod(uint32_t(tap), tr, tq);
+            const int h = s.h0 + int(tr);
+            const int w = s.w0 + int(tq);
+            const bool ok = tap < TT && unsigned(h) < unsigned(g.Hi) && unsigned(w) < unsigned(g.Wi);
+            const float* p = g.in + (s.base + int(tr) * g.Wi + int(tq));
+#pragma unroll
+            for (int c = 0; c < CP; ++c) v[t * CP + c] = ldg_keep_if(p + c * g.HiWi, ok && c < g.Ci);
+        }
+    }
+
     __device__ void load_a(const AState& s, const Tile&, int ks, int tid, float (&v)[32]) const
     {
-        if (g.chan_fast) {
+        if (g.mode == 0) {
             // One tap, 32 consecutive channels.
             uint32_t tap, chunk, tr, tq;
             g.f_cchunks.divmod(uint32_t(ks), tap, chunk);
             g.f_t.divmod(tap, tr, tq);
             const int h = s.h0 + int(tr);
             const int w = s.w0 + int(tq);
-            if (unsigned(h) < unsigned(g.Hi) && unsigned(w) < unsigned(g.Wi)) {
-                const float* p = g.in + (s.base + int(chunk) * 32 * g.HiWi + int(tr) * g.Wi + int(tq));
+            const bool ok = unsigned(h) < unsigned(g.Hi) && unsigned(w) < unsigned(g.Wi);
+            const int cleft = g.Ci - int(chunk) * 32;   // channels of this chunk that exist
+            const float* p = g.in + (s.base + int(chunk) * 32 * g.HiWi + int(tr) * g.Wi + int(tq));
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = __ldg(p + i * g.HiWi);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = 0.f;
+            for (int i = 0; i < 32; ++i) v[i] = ldg_keep_if(p + i * g.HiWi, ok && i < cleft);
+        } else if (g.mode == 1) {
+            switch (g.lcp) {
+            case 0: load_taps<0>(s, ks, v); break;
+            case 1: load_taps<1>(s, ks, v); break;
+            case 2: load_taps<2>(s, ks, v); break;
+            case 3: load_taps<3>(s, ks, v); break;
+            default: load_taps<4>(s, ks, v); break;
             }
         } else {
             // Generic order: lane l decodes k = ks*32 + l, the warp shares it.
@@ -137,8 +185,7 @@ struct ConvGatherProb {
                 const int rs = __shfl_sync(0xffffffffu, krs, i);
                 const int h = s.h0 + (rs >> 16);
                 const int w = s.w0 + (rs & 0xFFFF);
-                v[i] = (unsigned(h) < unsigned(g.Hi) && unsigned(w) < unsigned(g.Wi)) ? __ldg(g.in + (s.base + off))
-                                                                                        : 0.f;
+                v[i] = ldg_keep_if(g.in + (s.base + off), unsigned(h) < unsigned(g.Hi) && unsigned(w) < unsigned(g.Wi));
             }
         }
     }
@@ -200,17 +247,18 @@ struct ConvGatherProb {
 // ---------------------------------------------------------------------------
 // B operands (filters in the GEMM's K order)
 
-struct FwdFilterGen {   // B[k, kk] = W[k, c, r, q]
+struct FwdFilterGen {   // B[k, kk] = W[k, c, r, q] (0 for padded channels)
     const float* w;
-    int C, R, chan_fast;
-    FastDiv f_c, f_r, f_rr;
+    int C, R, generic;
+    FastDiv f_cp, f_r, f_rr;
     __device__ float operator()(int k, int kk) const
     {
         uint32_t c, r, q;
-        if (chan_fast) {
+        if (!generic) {
             uint32_t tap;
-            f_c.divmod(uint32_t(kk), tap, c);
+            f_cp.divmod(uint32_t(kk), tap, c);
             f_r.divmod(tap, r, q);
+            if (int(c) >= C) return 0.f;
         } else {
             uint32_t rem;
             f_rr.divmod(uint32_t(kk), c, rem);
@@ -222,17 +270,18 @@ struct FwdFilterGen {   // B[k, kk] = W[k, c, r, q]
 
 struct DgradFilterGen {   // B[(c, a, b), (d, e, k)] = W[k, c, a + pad - s*d, b + pad - s*e]
     const float* w;
-    int C, K, R, S, pad, d_lo, chan_fast;
-    FastDiv f_k, f_t, f_tt, f_ss, f_s;
+    int C, K, R, S, pad, d_lo, generic;
+    FastDiv f_kp, f_t, f_tt, f_ss, f_s;
     __device__ float operator()(int col, int kk) const
     {
         uint32_t c, ab, a, b, k, td, te;
         f_ss.divmod(uint32_t(col), c, ab);
         f_s.divmod(ab, a, b);
-        if (chan_fast) {
+        if (!generic) {
             uint32_t tap;
-            f_k.divmod(uint32_t(kk), tap, k);
+            f_kp.divmod(uint32_t(kk), tap, k);
             f_t.divmod(tap, td, te);
+            if (int(k) >= K) return 0.f;
         } else {
             uint32_t rem;
             f_tt.divmod(uint32_t(kk), k, rem);
@@ -271,21 +320,28 @@ static GatherGeom make_gather(const float* in, int Nb, int Ci, int Hi, int Wi, i
     g.sp = sp;
     g.o = o;
     g.T = T;
-    g.K = T * T * Ci;
-    g.chan_fast = (Ci % 32 == 0) ? 1 : 0;
+    k_order(Ci, &g.mode, &g.Cp, &g.lcp);
+    g.K = T * T * g.Cp;
     g.f_gpq = FastDiv(uint32_t(Gp * Gq));
     g.f_gq = FastDiv(uint32_t(Gq));
-    g.f_cchunks = FastDiv(uint32_t(Ci % 32 == 0 ? Ci / 32 : 1));
+    g.f_cchunks = FastDiv(uint32_t(g.mode == 0 ? g.Cp / 32 : 1));
     g.f_tt = FastDiv(uint32_t(T * T));
     g.f_t = FastDiv(uint32_t(T));
     return g;
+}
+
+static int padded(int ci)
+{
+    int mode, cp, lcp;
+    k_order(ci, &mode, &cp, &lcp);
+    return cp;
 }
 
 size_t conv_fwd_ws(const ConvDims& d)
 {
     int n_tiles;
     const int bn = pick_conv_bn(d.K, &n_tiles);
-    return bimage_floats(d.K, d.C * d.R * d.R, bn) * sizeof(float);
+    return bimage_floats(d.K, d.R * d.R * padded(d.C), bn) * sizeof(float);
 }
 
 static int dgrad_cols(const ConvDims& d) { return d.C * d.S * d.S; }
@@ -295,7 +351,7 @@ size_t conv_dgrad_ws(const ConvDims& d)
     int d_lo, T, n_tiles;
     dgrad_window(d, &d_lo, &T);
     const int bn = pick_conv_bn(dgrad_cols(d), &n_tiles);
-    return bimage_floats(dgrad_cols(d), T * T * d.K, bn) * sizeof(float);
+    return bimage_floats(dgrad_cols(d), T * T * padded(d.K), bn) * sizeof(float);
 }
 
 template <int BN>
@@ -338,7 +394,7 @@ cudaError_t launch_conv_fwd(const ConvDims& d, const float* x, const float* w, c
     o.so = 1;
     o.ncols = d.K;
     float* img = static_cast<float*>(ws);
-    FwdFilterGen gen{w, d.C, d.R, g.chan_fast, FastDiv(uint32_t(d.C)), FastDiv(uint32_t(d.R)),
+    FwdFilterGen gen{w, d.C, d.R, g.mode == 2, FastDiv(uint32_t(g.Cp)), FastDiv(uint32_t(d.R)),
                      FastDiv(uint32_t(d.R * d.R))};
     cudaError_t e = build_bimage(gen, d.K, g.K, bn, img, st);
     if (e != cudaSuccess) return e;
@@ -364,7 +420,7 @@ cudaError_t launch_conv_dgrad(const ConvDims& d, const float* w, const float* dy
     o.so = d.S;
     o.ncols = ncols;
     float* img = static_cast<float*>(ws);
-    DgradFilterGen gen{w, d.C, d.K, d.R, d.S, d.pad, d_lo, g.chan_fast, FastDiv(uint32_t(d.K)),
+    DgradFilterGen gen{w, d.C, d.K, d.R, d.S, d.pad, d_lo, g.mode == 2, FastDiv(uint32_t(g.Cp)),
                        FastDiv(uint32_t(T)), FastDiv(uint32_t(T * T)), FastDiv(uint32_t(d.S * d.S)),
                        FastDiv(uint32_t(d.S))};
     cudaError_t e = build_bimage(gen, ncols, g.K, bn, img, st);

@@ -109,8 +109,7 @@ struct ConvWgradProb {
             for (int e = 0; e < 4; ++e) {
                 const int h = jh[e] + (s.rq[p] >> 16);
                 const int w = jw[e] + (s.rq[p] & 0xFFFF);
-                v[4 * p + e] =
-                    (unsigned(h) < unsigned(H) && unsigned(w) < unsigned(W)) ? __ldg(x + (jbase[e] + s.rowoff[p])) : 0.f;
+                v[4 * p + e] = ldg_keep_if(x + (jbase[e] + s.rowoff[p]), unsigned(h) < unsigned(H) && unsigned(w) < unsigned(W));
             }
         }
     }

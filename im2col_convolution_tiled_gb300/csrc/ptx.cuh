@@ -85,6 +85,24 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, v
 }
 
 // ---------------------------------------------------------------------------
+// Gather loads.  Volatile so that the compiler keeps them where they are
+// written: a producer issues the next stage's loads before it blocks on a
+// barrier, and they must not be sunk past that wait.  The predicated form
+// leaves 0 where the position is outside the tensor (no access is made).
+
+__device__ __forceinline__ float ldg_keep(const float* p)
+{
+    float v;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float ldg_keep_if(const float* p, bool pred)
+{
+    return pred ? __ldg(p) : 0.f;
+}
+
+// ---------------------------------------------------------------------------
 // bulk (non-tensor) async copy global -> shared, completion on an mbarrier.
 // Source, destination and size must be multiples of 16 bytes.
 

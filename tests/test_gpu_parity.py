@@ -83,6 +83,9 @@ CONV_SHAPES = [
     (2, 4, 12, 12, 7, 3, 4, 0),        # stride > filter: phases with no tap
     (2, 3, 7, 7, 33, 2, 3, 1),
     (1, 20, 6, 6, 300, 3, 1, 1),       # 300 filters: two 192-wide tiles, ragged
+    (2, 16, 9, 9, 40, 3, 2, 1),        # 16 channels (one 16-wide tap group), 40 filters
+    (1, 48, 7, 7, 24, 3, 1, 1),        # 48 channels (per-element order), 24 filters
+    (1, 96, 8, 8, 17, 2, 2, 0),        # three 32-channel chunks, 17 filters
 ]
 
 
