@@ -282,6 +282,7 @@ const char* conv_b200_strerror(int code)
     case CONV_ERR_CUDA: return "a CUDA call or kernel launch failed";
     case CONV_ERR_DEVICE_TIMEOUT: return "a kernel gave up on a bounded wait";
     case CONV_ERR_DEVICE: return "no usable sm_103 device";
+    case CONV_ERR_SCRATCH_LIMIT: return "shape needs more scratch than the built-in array holds";
     default: return "unknown error";
     }
 }

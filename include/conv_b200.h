@@ -61,6 +61,7 @@ typedef struct {
 #define CONV_ERR_CUDA (-6)           /* a CUDA runtime call or launch failed        */
 #define CONV_ERR_DEVICE_TIMEOUT (-7) /* a kernel's bounded wait gave up             */
 #define CONV_ERR_DEVICE (-8)         /* no usable sm_103 device                     */
+#define CONV_ERR_SCRATCH_LIMIT (-9)  /* shape needs more than the built-in scratch  */
 
 /* Operation ids for conv_b200_workspace_bytes. */
 #define CONV_OP_FWD 0
@@ -157,6 +158,30 @@ int sgd_step(int64_t count, float lr, float clip, float *param, const float *gra
  * devices, all streams).  A diagnostic: callers difference two readings to
  * count the launches of a region of their own code. */
 uint64_t conv_b200_launch_count(void);
+
+/* conv_fwd without a workspace argument.  The page has no counterpart: this
+ * entry point exists for callers that cannot allocate device memory -- code
+ * running under a memory manager that owns the whole device heap, or a
+ * latency-critical loop that cannot afford an allocation's implicit device
+ * synchronisation.  Such callers pass x, w, b and y exactly as for conv_fwd;
+ * the scratch conv_fwd would take from `workspace` comes from a fixed array
+ * of CONV_FWD_NOALLOC_SCRATCH_BYTES inside the library instead.  The library
+ * allocates nothing for it: the array is part of the loaded module, and every
+ * device that loads the library keeps one until the process exits.
+ *  - Shapes with conv_b200_workspace_bytes(CONV_OP_FWD, s) larger than the
+ *    array (filters with more than about a million entries) are rejected
+ *    with CONV_ERR_SCRATCH_LIMIT before anything is launched.  Every other
+ *    argument is validated exactly as by conv_fwd, with the same codes.
+ *  - The first call on each device resolves the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before capturing a stream.
+ *  - All calls share the one array and each rewrites it in full.  Two calls
+ *    whose kernels may overlap on the GPU (different streams with no ordering
+ *    between them) race on it and can both return garbage: order them.
+ *  - The result is identical to conv_fwd's for the same inputs. */
+#define CONV_FWD_NOALLOC_SCRATCH_BYTES (8u << 20)
+int conv_fwd_noalloc(const conv_shape_t *s, const float *x, const float *w, const float *b, float *y,
+                     conv_stream_t stream);
 
 /* Text for a return code. */
 const char *conv_b200_strerror(int code);
