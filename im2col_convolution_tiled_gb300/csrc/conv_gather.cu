@@ -33,6 +33,7 @@
 // zero-padded to the same K order) is laid out once per call as pre-split
 // hi/lo tiles and fed by bulk copies.
 #include "conv_common.cuh"
+#include "gemm_patch.cuh"
 
 namespace cb200 {
 
@@ -82,6 +83,7 @@ struct OutGeom {
 template <int BN>
 struct ConvGatherProb {
     static constexpr bool kBBulk = true;
+    static constexpr bool kATmem = BN <= 128;     // A stages in tensor memory (keeps 2 accumulators)
     static constexpr int kGroups = 2;
     static constexpr Map kAMap = Map::RowFast;
     static constexpr Map kBMap = Map::RowFast;   // unused (bulk)
@@ -244,53 +246,130 @@ struct ConvGatherProb {
     }
 };
 
+// The same GEMMs on the patch-staged kernel (gemm_patch.cuh): tiles never
+// straddle images, and the K order is chunk-major in 32-channel chunks (or tap
+// groups when the gathered tensor has at most 16 channels).
+template <int BN>
+struct ConvPatchProb {
+    PatchGeom pg;
+    OutGeom o;
+    const float* bimg;
+    int n_tiles, k_stages;
+
+    __device__ int num_tiles() const { return pg.Nb * pg.tpi * n_tiles; }
+    __device__ Tile tile_t(int t) const
+    {
+        Tile r;
+        r.n0 = (t % n_tiles) * BN;
+        r.m0 = 0;
+        r.ks0 = 0;
+        r.ks1 = k_stages;
+        r.grp = t % n_tiles;
+        return r;
+    }
+    __device__ const float* b_image_t(int t, int ks) const
+    {
+        return bimg + (size_t(t % n_tiles) * k_stages + ks) * 2 * size_t(BN) * kBK;
+    }
+
+    using EState = typename ConvGatherProb<BN>::EState;
+    __device__ EState e_setup_t(int t, int row) const
+    {
+        const int mt = t / n_tiles;
+        const int n = mt / pg.tpi, ti = mt % pg.tpi;
+        const int pix = ti * kBM + row;
+        EState e;
+        e.valid = pix < pg.GpGq;
+        uint32_t p = 0, q = 0;
+        if (e.valid) pg.f_gq.divmod(uint32_t(pix), p, q);
+        const int h = int(p) * o.so, w = int(q) * o.so;
+        e.hrem = o.Ho - h;
+        e.wrem = o.Wo - w;
+        e.opix = o.out + size_t(n) * o.Co * o.HoWo + size_t(h) * o.Wo + w;
+        return e;
+    }
+    __device__ void store(const EState& e, const Tile& tl, int row, int c0, const uint32_t (&r)[32]) const
+    {
+        ConvGatherProb<BN> helper;
+        helper.o = o;
+        helper.store(e, tl, row, c0, r);
+    }
+};
+
 // ---------------------------------------------------------------------------
 // B operands (filters in the GEMM's K order)
 
+// K index -> (channel of the gathered tensor, tap index) in one of the three
+// orders the gathers use.
+struct KDecode {
+    int order;         // 0: tap-major, channels padded to Cp fastest; 1: 32-channel chunk, tap, channel; 2: channel, tap
+    FastDiv f_cp;      // order 0: Cp
+    FastDiv f_chunk;   // order 1: T*T*32
+    FastDiv f_tt;      // order 2: T*T
+    __device__ __forceinline__ void operator()(int kk, int& c, int& tap) const
+    {
+        uint32_t a, b;
+        if (order == 0) {
+            f_cp.divmod(uint32_t(kk), a, b);
+            tap = int(a);
+            c = int(b);
+        } else if (order == 1) {
+            f_chunk.divmod(uint32_t(kk), a, b);
+            tap = int(b) >> 5;
+            c = int(a) * 32 + (int(b) & 31);
+        } else {
+            f_tt.divmod(uint32_t(kk), a, b);
+            c = int(a);
+            tap = int(b);
+        }
+    }
+};
+
+static KDecode make_kdecode(int order, int cp, int T)
+{
+    KDecode d{};
+    d.order = order;
+    d.f_cp = FastDiv(uint32_t(cp > 0 ? cp : 1));
+    d.f_chunk = FastDiv(uint32_t(T * T * 32));
+    d.f_tt = FastDiv(uint32_t(T * T));
+    return d;
+}
+
 struct FwdFilterGen {   // B[k, kk] = W[k, c, r, q] (0 for padded channels)
     const float* w;
-    int C, R, generic;
-    FastDiv f_cp, f_r, f_rr;
+    int C, R;
+    KDecode dec;
+    FastDiv f_r;
     __device__ float operator()(int k, int kk) const
     {
-        uint32_t c, r, q;
-        if (!generic) {
-            uint32_t tap;
-            f_cp.divmod(uint32_t(kk), tap, c);
-            f_r.divmod(tap, r, q);
-            if (int(c) >= C) return 0.f;
-        } else {
-            uint32_t rem;
-            f_rr.divmod(uint32_t(kk), c, rem);
-            f_r.divmod(rem, r, q);
-        }
+        int c, tap;
+        dec(kk, c, tap);
+        if (c >= C || tap >= R * R) return 0.f;
+        uint32_t r, q;
+        f_r.divmod(uint32_t(tap), r, q);
         return __ldg(w + ((size_t(k) * C + c) * R + r) * R + q);
     }
 };
 
-struct DgradFilterGen {   // B[(c, a, b), (d, e, k)] = W[k, c, a + pad - s*d, b + pad - s*e]
+struct DgradFilterGen {   // B[(c, a, b), (d, e, kc)] = W[kc, c, a + pad - s*d, b + pad - s*e]
     const float* w;
-    int C, K, R, S, pad, d_lo, generic;
-    FastDiv f_kp, f_t, f_tt, f_ss, f_s;
+    int C, K, R, S, pad, d_lo;
+    KDecode dec;
+    FastDiv f_t, f_ss, f_s;
     __device__ float operator()(int col, int kk) const
     {
-        uint32_t c, ab, a, b, k, td, te;
+        uint32_t c, ab, a, b, td, te;
         f_ss.divmod(uint32_t(col), c, ab);
         f_s.divmod(ab, a, b);
-        if (!generic) {
-            uint32_t tap;
-            f_kp.divmod(uint32_t(kk), tap, k);
-            f_t.divmod(tap, td, te);
-            if (int(k) >= K) return 0.f;
-        } else {
-            uint32_t rem;
-            f_tt.divmod(uint32_t(kk), k, rem);
-            f_t.divmod(rem, td, te);
-        }
+        int kc, tap;
+        dec(kk, kc, tap);
+        if (kc >= K) return 0.f;
+        f_t.divmod(uint32_t(tap), td, te);
+        if (int(td) >= int(f_t.d)) return 0.f;   // tap past the window
         const int r = int(a) + pad - S * (d_lo + int(td));
         const int q = int(b) + pad - S * (d_lo + int(te));
         if (r < 0 || r >= R || q < 0 || q >= R) return 0.f;
-        return __ldg(w + ((size_t(k) * C + c) * R + r) * R + q);
+        return __ldg(w + ((size_t(kc) * C + c) * R + r) * R + q);
     }
 };
 
@@ -330,18 +409,24 @@ static GatherGeom make_gather(const float* in, int Nb, int Ci, int Hi, int Wi, i
     return g;
 }
 
-static int padded(int ci)
+// K extent of the B image for a gather over `ci` channels: chunks of 32
+// channels (patch kernel) cover every order the register-gather kernel uses
+// when ci > 16; tap groups of 2^ceil(log2 ci) channels otherwise.
+static int k_extent(int ci, int T)
 {
-    int mode, cp, lcp;
-    k_order(ci, &mode, &cp, &lcp);
-    return cp;
+    if (ci <= 16) {
+        int l = 0;
+        while ((1 << l) < ci) ++l;
+        return T * T * (1 << l);
+    }
+    return T * T * ((ci + 31) / 32 * 32);
 }
 
 size_t conv_fwd_ws(const ConvDims& d)
 {
     int n_tiles;
     const int bn = pick_conv_bn(d.K, &n_tiles);
-    return bimage_floats(d.K, d.R * d.R * padded(d.C), bn) * sizeof(float);
+    return bimage_floats(d.K, k_extent(d.C, d.R), bn) * sizeof(float);
 }
 
 static int dgrad_cols(const ConvDims& d) { return d.C * d.S * d.S; }
@@ -351,7 +436,7 @@ size_t conv_dgrad_ws(const ConvDims& d)
     int d_lo, T, n_tiles;
     dgrad_window(d, &d_lo, &T);
     const int bn = pick_conv_bn(dgrad_cols(d), &n_tiles);
-    return bimage_floats(dgrad_cols(d), T * T * padded(d.K), bn) * sizeof(float);
+    return bimage_floats(dgrad_cols(d), k_extent(d.K, T), bn) * sizeof(float);
 }
 
 template <int BN>
@@ -378,12 +463,104 @@ static cudaError_t dispatch_gather(int bn, const GatherGeom& g, const OutGeom& o
     }
 }
 
+static PatchGeom make_patch(const float* in, int Nb, int Ci, int Hi, int Wi, int Gp, int Gq, int sp, int o, int T)
+{
+    PatchGeom pg{};
+    pg.in = in;
+    pg.Nb = Nb;
+    pg.Ci = Ci;
+    pg.Hi = Hi;
+    pg.Wi = Wi;
+    pg.HiWi = Hi * Wi;
+    pg.CiHiWi = Ci * Hi * Wi;
+    pg.total = (long long)Nb * Ci * Hi * Wi;
+    pg.Gp = Gp;
+    pg.Gq = Gq;
+    pg.GpGq = Gp * Gq;
+    pg.tpi = (pg.GpGq + kBM - 1) / kBM;
+    pg.sp = sp;
+    pg.o = o;
+    pg.T = T;
+    if (Ci <= 16) {
+        int l = 0;
+        while ((1 << l) < Ci) ++l;
+        pg.mode = 1;
+        pg.lcp = l;
+        pg.Cp = 1 << l;
+        pg.nch = 1;
+        pg.spc = (T * T * pg.Cp + kBK - 1) / kBK;
+        pg.pc = Ci;
+    } else {
+        pg.mode = 0;
+        pg.lcp = 0;
+        pg.Cp = (Ci + 31) / 32 * 32;
+        pg.nch = pg.Cp / 32;
+        pg.spc = T * T;
+        pg.pc = 32;
+    }
+    pg.f_gq = FastDiv(uint32_t(Gq));
+    pg.f_t = FastDiv(uint32_t(T));
+    return pg;
+}
+
+static int patch_capacity(int bn)
+{
+    switch (bn) {
+    case 32: return PatchCfg<32>::kPatchFloats;
+    case 64: return PatchCfg<64>::kPatchFloats;
+    case 128: return PatchCfg<128>::kPatchFloats;
+    default: return 0;
+    }
+}
+
+template <int BN>
+static cudaError_t run_patch(const PatchGeom& pg, const OutGeom& o, float* img, cudaStream_t st)
+{
+    ConvPatchProb<BN> p;
+    p.pg = pg;
+    p.o = o;
+    p.bimg = img;
+    p.n_tiles = (o.ncols + BN - 1) / BN;
+    p.k_stages = pg.nch * pg.spc;
+    return launch_tc_patch<ConvPatchProb<BN>, BN>(p, pg.Nb * pg.tpi * p.n_tiles, device_error_word(), st);
+}
+
+// One convolution-window GEMM over the gathered tensor `in` [Nb][Ci][Hi][Wi]:
+// rows = the (Gp x Gq) grid of each image, window h = p*sp + o + tap.  The
+// patch-staged kernel is used when the output tile is at most 128 wide and
+// every tile's patch fits its shared-memory buffer; otherwise the
+// register-gather kernel.  MakeGen(KDecode) builds the B-operand generator in
+// the matching K order.
+template <class MakeGen>
+static cudaError_t run_window_gemm(const float* in, int Nb, int Ci, int Hi, int Wi, int Gp, int Gq, int sp, int o,
+                                   int T, const OutGeom& og, float* img, MakeGen make_gen, cudaStream_t st)
+{
+    int n_tiles;
+    const int bn = pick_conv_bn(og.ncols, &n_tiles);
+    if (bn <= 128) {
+        const PatchGeom pg = make_patch(in, Nb, Ci, Hi, Wi, Gp, Gq, sp, o, T);
+        if (max_patch_floats(pg) <= patch_capacity(bn)) {
+            const KDecode dec = make_kdecode(pg.mode == 0 ? 1 : 0, pg.Cp, T);
+            const int k_total = pg.mode == 0 ? pg.nch * T * T * kBK : T * T * pg.Cp;   // padded taps excluded
+            cudaError_t e = build_bimage(make_gen(dec), og.ncols, k_total, bn, img, st);
+            if (e != cudaSuccess) return e;
+            switch (bn) {
+            case 32: return run_patch<32>(pg, og, img, st);
+            case 64: return run_patch<64>(pg, og, img, st);
+            default: return run_patch<128>(pg, og, img, st);
+            }
+        }
+    }
+    const GatherGeom g = make_gather(in, Nb, Ci, Hi, Wi, Gp, Gq, sp, o, T);
+    const KDecode dec = make_kdecode(g.mode == 2 ? 2 : 0, g.Cp, T);
+    cudaError_t e = build_bimage(make_gen(dec), og.ncols, g.K, bn, img, st);
+    if (e != cudaSuccess) return e;
+    return dispatch_gather(bn, g, og, img, st);
+}
+
 cudaError_t launch_conv_fwd(const ConvDims& d, const float* x, const float* w, const float* b, float* y, void* ws,
                             cudaStream_t st)
 {
-    int n_tiles;
-    const int bn = pick_conv_bn(d.K, &n_tiles);
-    const GatherGeom g = make_gather(x, d.N, d.C, d.H, d.W, d.P, d.Q, d.S, -d.pad, d.R);
     OutGeom o{};
     o.out = y;
     o.bias = b;
@@ -393,23 +570,17 @@ cudaError_t launch_conv_fwd(const ConvDims& d, const float* x, const float* w, c
     o.HoWo = d.P * d.Q;
     o.so = 1;
     o.ncols = d.K;
-    float* img = static_cast<float*>(ws);
-    FwdFilterGen gen{w, d.C, d.R, g.mode == 2, FastDiv(uint32_t(g.Cp)), FastDiv(uint32_t(d.R)),
-                     FastDiv(uint32_t(d.R * d.R))};
-    cudaError_t e = build_bimage(gen, d.K, g.K, bn, img, st);
-    if (e != cudaSuccess) return e;
-    return dispatch_gather(bn, g, o, img, st);
+    auto make_gen = [&](const KDecode& dec) { return FwdFilterGen{w, d.C, d.R, dec, FastDiv(uint32_t(d.R))}; };
+    return run_window_gemm(x, d.N, d.C, d.H, d.W, d.P, d.Q, d.S, -d.pad, d.R, o, static_cast<float*>(ws), make_gen,
+                           st);
 }
 
 cudaError_t launch_conv_dgrad(const ConvDims& d, const float* w, const float* dy, float* dx, void* ws,
                               cudaStream_t st)
 {
-    int d_lo, T, n_tiles;
+    int d_lo, T;
     dgrad_window(d, &d_lo, &T);
-    const int ncols = dgrad_cols(d);
-    const int bn = pick_conv_bn(ncols, &n_tiles);
     const int Hs = (d.H + d.S - 1) / d.S, Ws = (d.W + d.S - 1) / d.S;
-    const GatherGeom g = make_gather(dy, d.N, d.K, d.P, d.Q, Hs, Ws, 1, d_lo, T);
     OutGeom o{};
     o.out = dx;
     o.bias = nullptr;
@@ -418,14 +589,12 @@ cudaError_t launch_conv_dgrad(const ConvDims& d, const float* w, const float* dy
     o.Wo = d.W;
     o.HoWo = d.H * d.W;
     o.so = d.S;
-    o.ncols = ncols;
-    float* img = static_cast<float*>(ws);
-    DgradFilterGen gen{w, d.C, d.K, d.R, d.S, d.pad, d_lo, g.mode == 2, FastDiv(uint32_t(g.Cp)),
-                       FastDiv(uint32_t(T)), FastDiv(uint32_t(T * T)), FastDiv(uint32_t(d.S * d.S)),
-                       FastDiv(uint32_t(d.S))};
-    cudaError_t e = build_bimage(gen, ncols, g.K, bn, img, st);
-    if (e != cudaSuccess) return e;
-    return dispatch_gather(bn, g, o, img, st);
+    o.ncols = dgrad_cols(d);
+    auto make_gen = [&](const KDecode& dec) {
+        return DgradFilterGen{w,   d.C, d.K, d.R, d.S, d.pad, d_lo, dec, FastDiv(uint32_t(T)),
+                              FastDiv(uint32_t(d.S * d.S)), FastDiv(uint32_t(d.S))};
+    };
+    return run_window_gemm(dy, d.N, d.K, d.P, d.Q, Hs, Ws, 1, d_lo, T, o, static_cast<float*>(ws), make_gen, st);
 }
 
 }  // namespace cb200

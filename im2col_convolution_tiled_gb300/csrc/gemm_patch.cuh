@@ -1,0 +1,434 @@
+// gemm_patch.cuh -- implicit-GEMM convolution whose A operand (the column
+// matrix of the page's im2col step) is built from input patches staged in
+// shared memory.
+//
+// A tile is 128 consecutive output positions of ONE image (tiles never straddle
+// images; the last tile of an image is partial).  For each chunk of channels
+// the tile reads, from the gathered tensor, every input row any tap of the tile
+// touches -- full-width rows, one contiguous run per channel -- into shared
+// memory with coalesced loads.  The taps of that chunk are then gathered from
+// shared memory: per element one shared load instead of one global load, and a
+// global request count lower by about the number of taps.
+//
+// Roles (448 threads, one CTA per SM, persistent over tiles):
+//   warps 0-3, 4-7   two converter groups; pipeline stages are dealt to them in
+//                    turn.  A converter thread owns one output position (one A
+//                    row): per stage it reads its 32 K values from the patch,
+//                    splits them into 3xTF32 hi/lo and writes both into the
+//                    stage's tensor-memory columns; the group's first thread
+//                    bulk-copies the stage's pre-split B tiles.
+//   warp 8           patch loader: fills a ring of two patch buffers one
+//                    chunk ahead, one bulk copy per channel run.
+//   warp 9           tensor-memory allocation; lane 0 issues tcgen05.mma with
+//                    A from tensor memory and B from shared memory.
+//   warps 10-13      epilogue (as in gemm_tc.cuh).
+//
+// Every converter warp waits on every chunk's "patch loaded" barrier and
+// signals every chunk's "patch read" barrier, and the two groups take
+// alternating stages with fewer groups than stages, so each parity wait is at
+// most one phase ahead of its barrier.  All waits are bounded (ptx.cuh).
+#pragma once
+#include "gemm_tc.cuh"
+
+namespace cb200 {
+
+struct PatchGeom {
+    const float* in;   // gathered tensor [Nb][Ci][Hi][Wi]
+    int Nb, Ci, Hi, Wi, HiWi, CiHiWi;
+    long long total;   // Nb*Ci*Hi*Wi (copies never read past it)
+    int Gp, Gq, GpGq;  // output grid of one image
+    int tpi;           // tiles per image
+    int sp, o, T;      // window: h = p*sp + o + tap_r
+    int mode;          // 0: 32-channel chunks, stage = one tap; 1: Ci <= 16, stage = 32/Cp taps
+    int Cp, lcp;       // mode 1: channels padded to Cp = 2^lcp
+    int nch;           // channel chunks per tile (mode 1: 1)
+    int spc;           // stages per chunk
+    int pc;            // channels one patch holds (mode 0: 32, mode 1: Ci)
+    FastDiv f_gq, f_t;
+};
+
+// Floats between consecutive channels of a staged patch holding `run`
+// floats per channel: at least run + 6 (room for a 16-byte-aligned copy of
+// the run, rounded out on both sides) and congruent to Hi*Wi modulo 4, so
+// every channel's run starts at the same offset (0..3) within its block.
+__host__ __device__ inline int patch_cstride(int run, int HiWi)
+{
+    int cps = run + 6;
+    cps += ((HiWi - cps) % 4 + 4) % 4;
+    return cps;
+}
+
+// Largest patch (floats) any tile of this geometry stages.
+inline int max_patch_floats(const PatchGeom& g)
+{
+    int best = 0;
+    for (int ti = 0; ti < g.tpi; ++ti) {
+        const int first = ti * kBM;
+        const int last = (first + kBM < g.GpGq ? first + kBM : g.GpGq) - 1;
+        const int p_lo = first / g.Gq, p_hi = last / g.Gq;
+        int h_lo = p_lo * g.sp + g.o, h_hi = p_hi * g.sp + g.o + g.T - 1;
+        if (h_lo < 0) h_lo = 0;
+        if (h_hi > g.Hi - 1) h_hi = g.Hi - 1;
+        const int rows = h_hi >= h_lo ? h_hi - h_lo + 1 : 0;
+        const int f = patch_cstride(rows * g.Wi, g.HiWi) * g.pc;
+        if (f > best) best = f;
+    }
+    return best;
+}
+
+// Mode 1 (Ci <= 16): 32 / CP whole taps per stage, CP (padded) channels each.
+template <int LCP>
+__device__ __forceinline__ void patch_taps(const PatchGeom& g, const float* pbuf, int j, int hp0, int wp0, bool pvalid,
+                                           int h_lo, int cstride, float (&v)[32])
+{
+    constexpr int CP = 1 << LCP, TPS = 32 >> LCP;
+    const int TT = g.T * g.T;
+#pragma unroll
+    for (int t = 0; t < TPS; ++t) {
+        const int tap = j * TPS + t;
+        uint32_t tr, tq;
+        g.f_t.divmod(uint32_t(tap), tr, tq);
+        const int h = hp0 + int(tr), w = wp0 + int(tq);
+        const bool ok = pvalid && tap < TT && unsigned(h) < unsigned(g.Hi) && unsigned(w) < unsigned(g.Wi);
+        const float* p = pbuf + ((h - h_lo) * g.Wi + w);
+#pragma unroll
+        for (int c = 0; c < CP; ++c) v[t * CP + c] = (ok && c < g.Ci) ? p[c * cstride] : 0.f;
+    }
+}
+
+template <int BN>
+struct PatchCfg {
+    static_assert(BN <= 128, "the patch kernel keeps two accumulators and up to six A stages in tensor memory");
+    static constexpr int kDBuf = 2;
+    static constexpr int kTmemStages0 = (512 - kDBuf * BN) / 64;
+    static constexpr int kStages = kTmemStages0 > 6 ? 6 : kTmemStages0;
+    static constexpr uint32_t kBTile = BN * kBK * 4;
+    static constexpr uint32_t kStage = 2 * kBTile;
+    static constexpr uint32_t kACol = uint32_t(kDBuf * BN);
+    static constexpr size_t kCtlBytes = 512;
+    static constexpr size_t kMaxSmem = 227 * 1024;
+    // two patch buffers share what the B stages leave
+    static constexpr size_t kPatchBytes =
+        ((kMaxSmem - 1024 - kCtlBytes - size_t(kStages) * kStage) / 2) & ~size_t(15);
+    static constexpr int kPatchFloats = int(kPatchBytes / 4);
+    static constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStage + 2 * kPatchBytes + kCtlBytes;
+    static constexpr uint32_t kIdesc = idesc_tf32(kBM, BN);
+};
+
+struct PatchCtl {
+    uint64_t full[8];
+    uint64_t empty[8];
+    uint64_t accf[2];
+    uint64_t acce[2];
+    uint64_t pfull[2];     // patch buffer holds its chunk (loader arrival)
+    uint64_t pempty[2];    // every converter warp is done with the buffer (8 arrivals)
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+// The problem supplies the B image location and the epilogue (same interface
+// as ConvGatherProb: b_image, EState, e_setup, store).  Tile decode is fixed:
+// t -> (n_tile = t % n_tiles, image, tile in image).
+template <class Prob, int BN>
+__global__ void __launch_bounds__(448, 1) tc_patch_kernel(const __grid_constant__ Prob prob, int* err_word)
+{
+    using Cfg = PatchCfg<BN>;
+    constexpr int S = Cfg::kStages;
+    constexpr int DB = Cfg::kDBuf;
+    const PatchGeom& g = prob.pg;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* patch[2] = {reinterpret_cast<float*>(smem + size_t(S) * Cfg::kStage),
+                       reinterpret_cast<float*>(smem + size_t(S) * Cfg::kStage + Cfg::kPatchBytes)};
+    PatchCtl* ctl = reinterpret_cast<PatchCtl*>(smem + size_t(S) * Cfg::kStage + 2 * Cfg::kPatchBytes);
+    volatile int* abort_flag = &ctl->abort_flag;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t smem_base = smem_u32(smem);
+    auto b_hi = [&](int s) { return smem_base + uint32_t(s) * Cfg::kStage; };
+    auto b_lo = [&](int s) { return b_hi(s) + Cfg::kBTile; };
+    auto a_col = [&](int s) { return Cfg::kACol + uint32_t(s) * 64u; };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&ctl->full[s], 5);   // 4 converter warps + the B bulk copy
+            mbar_init(&ctl->empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&ctl->accf[b], 1);
+            mbar_init(&ctl->acce[b], 4);
+            mbar_init(&ctl->pfull[b], 1);
+            mbar_init(&ctl->pempty[b], 8);
+        }
+        mbar_init(&ctl->drain, 1);
+        ctl->abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 9) tmem_alloc(&ctl->tmem_base, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = ctl->tmem_base;
+
+    const int num_tiles = prob.num_tiles();
+    auto fail = [&]() {
+        ctl->abort_flag = 1;
+        atomicOr(err_word, kDevErrTimeout);
+    };
+
+    // Patch geometry of tile t: image, tile in image, first/last output
+    // position, and the clamped input-row range every tap of the tile touches.
+    struct TileGeo {
+        int n, first, last, h_lo, rows;
+    };
+    auto tile_geo = [&](int t) {
+        TileGeo q;
+        const int mt = t / prob.n_tiles;
+        q.n = mt / g.tpi;
+        q.first = (mt % g.tpi) * kBM;
+        q.last = (q.first + kBM < g.GpGq ? q.first + kBM : g.GpGq) - 1;
+        int h_lo = (q.first / g.Gq) * g.sp + g.o;
+        int h_hi = (q.last / g.Gq) * g.sp + g.o + g.T - 1;
+        if (h_lo < 0) h_lo = 0;
+        if (h_hi > g.Hi - 1) h_hi = g.Hi - 1;
+        q.h_lo = h_lo;
+        q.rows = h_hi >= h_lo ? h_hi - h_lo + 1 : 0;
+        return q;
+    };
+
+    if (warp < 8) {
+        // ---------------- converter groups ----------------
+        const int grp = warp >> 2;
+        const int tid = threadIdx.x - 128 * grp;   // 0..127: the A row this thread owns
+        uint32_t u = 0;                            // chunk counter of this CTA
+        int last_issued = -1;
+        bool ok = true;
+        const uint32_t tbase = tmem_base + (uint32_t((warp & 3) * 32) << 16);
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            const TileGeo q = tile_geo(t);
+            const int cstride = patch_cstride(q.rows * g.Wi, g.HiWi);   // floats per channel in the patch
+            const int pix = q.first + tid;
+            const bool pvalid = pix <= q.last;
+            uint32_t pp = 0, pq = 0;
+            if (pvalid) g.f_gq.divmod(uint32_t(pix), pp, pq);
+            const int hp0 = int(pp) * g.sp + g.o;  // input row of tap 0
+            const int wp0 = int(pq) * g.sp + g.o;  // input column of tap 0
+            for (int cc = 0; cc < g.nch && ok; ++cc, ++u) {
+                const int pb = int(u & 1u);
+                // every channel run of this chunk starts s0 floats into its block
+                const long long x0 = (long long)q.n * g.CiHiWi + (long long)(cc * 32) * g.HiWi + (long long)q.h_lo * g.Wi;
+                const float* pbuf = patch[pb] + int(x0 & 3);
+                if (!mbar_wait_warp(&ctl->pfull[pb], (u >> 1) & 1u, abort_flag)) { ok = false; break; }
+                const uint32_t c_first = u * uint32_t(g.spc);
+                const int j0 = int((uint32_t(grp) + 2u - (c_first & 1u)) & 1u);   // first stage of this group
+                for (int j = j0; j < g.spc; j += 2) {
+                    const uint32_t c = c_first + uint32_t(j);
+                    const int slot = int(c % uint32_t(S));
+                    const uint32_t phase = (c / uint32_t(S)) & 1u;
+                    const int ks = cc * g.spc + j;
+                    float va[32];
+                    if (g.mode == 0) {
+                        uint32_t tr, tq;
+                        g.f_t.divmod(uint32_t(j), tr, tq);
+                        const int h = hp0 + int(tr), w = wp0 + int(tq);
+                        const bool okp = pvalid && unsigned(h) < unsigned(g.Hi) && unsigned(w) < unsigned(g.Wi);
+                        const int climit = okp ? g.Ci - cc * 32 : 0;
+                        const float* pp0 = pbuf + ((h - q.h_lo) * g.Wi + w);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) va[i] = i < climit ? pp0[i * cstride] : 0.f;
+                    } else {
+                        switch (g.lcp) {
+                        case 0: patch_taps<0>(g, pbuf, j, hp0, wp0, pvalid, q.h_lo, cstride, va); break;
+                        case 1: patch_taps<1>(g, pbuf, j, hp0, wp0, pvalid, q.h_lo, cstride, va); break;
+                        case 2: patch_taps<2>(g, pbuf, j, hp0, wp0, pvalid, q.h_lo, cstride, va); break;
+                        case 3: patch_taps<3>(g, pbuf, j, hp0, wp0, pvalid, q.h_lo, cstride, va); break;
+                        default: patch_taps<4>(g, pbuf, j, hp0, wp0, pvalid, q.h_lo, cstride, va); break;
+                        }
+                    }
+                    if (!mbar_wait_warp(&ctl->empty[slot], phase ^ 1u, abort_flag)) { ok = false; break; }
+                    if (tid == 0) {
+                        mbar_arrive_expect_tx(&ctl->full[slot], 2 * Cfg::kBTile);
+                        bulk_g2s(smem + (b_hi(slot) - smem_base), prob.b_image_t(t, ks), 2 * Cfg::kBTile,
+                                 &ctl->full[slot]);
+                        last_issued = int(c);
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int h4 = 0; h4 < 4; ++h4) {
+                        uint32_t hi[8], lo[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) split_tf32(va[8 * h4 + i], hi[i], lo[i]);
+                        tmem_st8(tbase + a_col(slot) + 8 * h4, hi);
+                        tmem_st8(tbase + a_col(slot) + 32 + 8 * h4, lo);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctl->full[slot]);
+                }
+                if (!ok) break;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->pempty[pb]);   // this warp is done reading the buffer
+            }
+        }
+        if (!ok) {
+            fail();
+            if (tid == 0 && last_issued >= 0) {
+                for (int c = last_issued; c >= 0 && c > last_issued - S; c -= 2) {
+                    uint64_t t0 = globaltimer_ns();
+                    while (!mbar_try_wait(&ctl->full[c % S], uint32_t(c / S) & 1u) &&
+                           globaltimer_ns() - t0 < kWaitLimitNs) {
+                    }
+                }
+            }
+        }
+    } else if (warp == 8) {
+        // ---------------- patch loader ----------------
+        uint32_t u = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            const TileGeo q = tile_geo(t);
+            const int cstride = patch_cstride(q.rows * g.Wi, g.HiWi);
+            for (int cc = 0; cc < g.nch && ok; ++cc, ++u) {
+                const int pb = int(u & 1u);
+                // chunk u - 2 (same buffer) must be fully read
+                if (u >= 2 && !mbar_wait_warp(&ctl->pempty[pb], ((u >> 1) - 1) & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                // lane c copies channel cc*32 + c: its run of rows*Wi floats, widened
+                // to 16-byte boundaries, with one bulk copy into block c of the buffer;
+                // a tail that would reach past the tensor's last 16-byte boundary
+                // (at most 3 floats) is copied with plain loads instead
+                const int c = lane;
+                const int run = q.rows * g.Wi;
+                const bool has = c < g.pc && cc * 32 + c < g.Ci && run > 0;
+                const long long x = (long long)q.n * g.CiHiWi + (long long)(cc * 32 + c) * g.HiWi +
+                                    (long long)q.h_lo * g.Wi;   // run start (floats into the tensor)
+                const long long x0 = x - (long long)c * g.HiWi;   // start of channel cc*32's run
+                const int sh = int(x0 & 3);                        // common offset of every run in its block
+                const long long a0 = x & ~3LL;                     // 16-byte-aligned copy start
+                long long a1 = (x + run + 3) & ~3LL;               // 16-byte-aligned copy end
+                const long long lim = g.total & ~3LL;
+                if (a1 > lim) a1 = lim;
+                const uint32_t bytes = has && a1 > a0 ? uint32_t((a1 - a0) * 4) : 0u;
+                // destination: element x of the run lands at block c + sh
+                const int dst_f = c * cstride + sh - int(x - a0);
+                uint32_t total_bytes = bytes;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) total_bytes += __shfl_xor_sync(0xffffffffu, total_bytes, o);
+                if (has) {
+                    // tail past the last aligned boundary of the tensor
+                    for (long long e = (a1 > x ? a1 : x); e < x + run; ++e)
+                        patch[pb][dst_f + int(e - a0)] = __ldg(g.in + e);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive_expect_tx(&ctl->pfull[pb], total_bytes);
+                __syncwarp();
+                if (bytes) bulk_g2s(patch[pb] + dst_f, g.in + a0, bytes, &ctl->pfull[pb]);
+
+            }
+        }
+        if (!ok) fail();
+    } else if (warp == 9) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int local = 0;
+            bool ok = true;
+            bool issued_any = false;
+            const int k_stages = g.nch * g.spc;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
+                const int acc = local % DB;
+                const uint32_t acc_phase = uint32_t(local / DB) & 1u;
+                if (!mbar_wait(&ctl->acce[acc], acc_phase ^ 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
+                uint32_t accumulate = 0;
+                for (int ks = 0; ks < k_stages; ++ks) {
+                    if (!mbar_wait(&ctl->full[stage], phase, abort_flag)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 8; ++kk) {
+                        const uint64_t bh = sdesc_k_sw128(b_hi(stage) + kk * 32);
+                        const uint64_t bl = sdesc_k_sw128(b_lo(stage) + kk * 32);
+                        const uint32_t ah = tmem_base + a_col(stage) + uint32_t(kk * 8);
+                        const uint32_t al = ah + 32;
+                        mma_tf32_ts(d_tmem, al, bh, Cfg::kIdesc, accumulate);
+                        accumulate = 1;
+                        mma_tf32_ts(d_tmem, ah, bl, Cfg::kIdesc, 1);
+                        mma_tf32_ts(d_tmem, ah, bh, Cfg::kIdesc, 1);
+                    }
+                    issued_any = true;
+                    mma_commit(&ctl->empty[stage]);
+                    if (++stage == S) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                mma_commit(&ctl->accf[acc]);
+            }
+            if (!ok) {
+                fail();
+                if (issued_any) {
+                    mma_commit(&ctl->drain);
+                    uint64_t t0 = globaltimer_ns();
+                    while (!mbar_try_wait(&ctl->drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue ----------------
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        int local = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
+            const int acc = local % DB;
+            const uint32_t acc_phase = uint32_t(local / DB) & 1u;
+            if (!mbar_wait_warp(&ctl->accf[acc], acc_phase, abort_flag)) { ok = false; break; }
+            tc_fence_after();
+            const Tile tile = prob.tile_t(t);
+            typename Prob::EState es = prob.e_setup_t(t, row);
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t r[32];
+                tmem_ld32(tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * BN + c), r);
+                prob.store(es, tile, row, c, r);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->acce[acc]);
+        }
+        if (!ok) fail();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+template <class Prob, int BN>
+cudaError_t launch_tc_patch(const Prob& prob, int num_tiles, int* err_word, cudaStream_t stream)
+{
+    using Cfg = PatchCfg<BN>;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(tc_patch_kernel<Prob, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             int(Cfg::kSmemBytes));
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    if (num_tiles <= 0) return cudaSuccess;
+    int grid = num_tiles < sm_count() ? num_tiles : sm_count();
+    tc_patch_kernel<Prob, BN><<<grid, 448, Cfg::kSmemBytes, stream>>>(prob, err_word);
+    note_launch();
+    return cudaGetLastError();
+}
+
+}  // namespace cb200

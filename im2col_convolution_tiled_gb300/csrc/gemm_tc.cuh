@@ -48,16 +48,36 @@ struct Tile {
     int grp;        // problem-defined: sub-problem (stride phase) or split index
 };
 
-template <int BN>
+// Tile configuration.  With ATMEM the A operand does not use shared memory:
+// producers write its hi/lo halves into tensor memory (64 columns per stage)
+// and the MMA reads A from there; shared memory then holds only B stages.
+template <int BN, bool ATMEM = false>
 struct TileCfg {
     static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN must be a multiple of 32 in [32, 256]");
-    static constexpr uint32_t kATile = kBM * kBK * 4;   // bytes of one hi (or lo) A tile
+    static constexpr uint32_t kATile = ATMEM ? 0 : kBM * kBK * 4;   // smem bytes of one hi (or lo) A tile
     static constexpr uint32_t kBTile = BN * kBK * 4;
     static constexpr uint32_t kStage = 2 * kATile + 2 * kBTile;
-    static constexpr int kStages = (kSmemBudget / kStage) > 6 ? 6 : int(kSmemBudget / kStage);
-    static constexpr uint32_t kTmemCols = (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
+    // accumulators: two (epilogue of tile i overlaps tile i+1) unless tensor
+    // memory is needed for A stages
+    static constexpr int kDBuf = (ATMEM && BN > 128) ? 1 : 2;
+    static constexpr int kSmemStages = int(kSmemBudget / kStage);
+    static constexpr int kTmemStages = ATMEM ? (512 - kDBuf * BN) / 64 : 8;
+    static constexpr int kStages0 = kSmemStages < kTmemStages ? kSmemStages : kTmemStages;
+    static constexpr int kStages = kStages0 > (ATMEM ? 8 : 6) ? (ATMEM ? 8 : 6) : kStages0;
+    static constexpr uint32_t kACol = uint32_t(kDBuf * BN);   // first TMEM column of the A stages
+    static constexpr uint32_t kTmemCols =
+        ATMEM ? 512 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
     static constexpr size_t kSmemBytes = size_t(kStages) * kStage + 1024 /*align*/ + 256 /*barriers*/;
     static constexpr uint32_t kIdesc = idesc_tf32(kBM, BN);
+};
+
+template <class Prob>
+struct UsesTmemA {
+    template <class P>
+    static constexpr bool test(decltype(P::kATmem)*) { return P::kATmem; }
+    template <class P>
+    static constexpr bool test(...) { return false; }
+    static constexpr bool value = test<Prob>(nullptr);
 };
 
 // Producer groups actually used: never more than the pipeline has stages.
@@ -67,7 +87,8 @@ struct TileCfg {
 // saw consumed.
 template <class Prob, int BN>
 struct Groups {
-    static constexpr int value = Prob::kGroups < TileCfg<BN>::kStages ? Prob::kGroups : TileCfg<BN>::kStages;
+    static constexpr int kS = TileCfg<BN, UsesTmemA<Prob>::value>::kStages;
+    static constexpr int value = Prob::kGroups < kS ? Prob::kGroups : kS;
 };
 
 // Producer-side layout of a gathered 32-value slice (per thread):
@@ -113,9 +134,11 @@ template <class Prob, int BN>
 __global__ void __launch_bounds__(Roles<Groups<Prob, BN>::value>::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ Prob prob, int* err_word)
 {
-    using Cfg = TileCfg<BN>;
+    constexpr bool ATMEM = UsesTmemA<Prob>::value;
+    using Cfg = TileCfg<BN, ATMEM>;
     constexpr int S = Cfg::kStages;
     constexpr int G = Groups<Prob, BN>::value;
+    constexpr int DB = Cfg::kDBuf;
     static_assert(G >= 1 && G <= S, "producer groups must not outnumber pipeline stages");
     constexpr int kWarpMma = Roles<G>::kWarpMma;
     constexpr int kBPasses = BN > 128 ? 2 : 1;
@@ -131,6 +154,7 @@ __global__ void __launch_bounds__(Roles<Groups<Prob, BN>::value>::kThreads, 1)
     auto a_lo = [&](int s) { return a_hi(s) + Cfg::kATile; };
     auto b_hi = [&](int s) { return a_hi(s) + 2 * Cfg::kATile; };
     auto b_lo = [&](int s) { return b_hi(s) + Cfg::kBTile; };
+    auto a_col = [&](int s) { return Cfg::kACol + uint32_t(s) * 64u; };   // ATMEM: hi at +0, lo at +32
 
     if (threadIdx.x == 0) {
         const uint32_t full_count = 4 + (Prob::kBBulk ? 1 : 0);
@@ -138,7 +162,7 @@ __global__ void __launch_bounds__(Roles<Groups<Prob, BN>::value>::kThreads, 1)
             mbar_init(&ctl->full[s], full_count);
             mbar_init(&ctl->empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < DB; ++b) {
             mbar_init(&ctl->accf[b], 1);
             mbar_init(&ctl->acce[b], 4);
         }
@@ -192,7 +216,25 @@ __global__ void __launch_bounds__(Roles<Groups<Prob, BN>::value>::kThreads, 1)
                             last_issued = int(c);
                         }
                     }
-                    store_slice<Prob::kAMap>(a_hi(slot), a_lo(slot), 0, kBM, tid, va);
+                    if constexpr (ATMEM) {
+                        // Thread = row 32 * (warp % 4) + lane = tid: write its split
+                        // row into the stage's hi and lo column blocks.
+                        static_assert(Prob::kAMap == Map::RowFast, "tensor-memory A needs one row per thread");
+                        tc_fence_after();
+                        const uint32_t tbase = tmem_base + (uint32_t((warp & 3) * 32) << 16) + a_col(slot);
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            uint32_t hi[8], lo[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) split_tf32(va[8 * h + i], hi[i], lo[i]);
+                            tmem_st8(tbase + 8 * h, hi);
+                            tmem_st8(tbase + 32 + 8 * h, lo);
+                        }
+                        tmem_wait_st();
+                        tc_fence_before();
+                    } else {
+                        store_slice<Prob::kAMap>(a_hi(slot), a_lo(slot), 0, kBM, tid, va);
+                    }
                     if constexpr (!Prob::kBBulk) {
 #pragma unroll
                         for (int pass = 0; pass < kBPasses; ++pass) {
@@ -251,8 +293,8 @@ __global__ void __launch_bounds__(Roles<Groups<Prob, BN>::value>::kThreads, 1)
             bool issued_any = false;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
                 const Tile tile = prob.tile(t);
-                const int acc = local & 1;
-                const uint32_t acc_phase = (local >> 1) & 1;
+                const int acc = local % DB;
+                const uint32_t acc_phase = uint32_t(local / DB) & 1u;
                 if (!mbar_wait(&ctl->acce[acc], acc_phase ^ 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
@@ -262,14 +304,23 @@ __global__ void __launch_bounds__(Roles<Groups<Prob, BN>::value>::kThreads, 1)
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < kBK / 8; ++kk) {
-                        const uint64_t ah = sdesc_k_sw128(a_hi(stage) + kk * 32);
-                        const uint64_t al = sdesc_k_sw128(a_lo(stage) + kk * 32);
                         const uint64_t bh = sdesc_k_sw128(b_hi(stage) + kk * 32);
                         const uint64_t bl = sdesc_k_sw128(b_lo(stage) + kk * 32);
-                        mma_tf32_ss(d_tmem, al, bh, Cfg::kIdesc, accumulate);
-                        accumulate = 1;
-                        mma_tf32_ss(d_tmem, ah, bl, Cfg::kIdesc, 1);
-                        mma_tf32_ss(d_tmem, ah, bh, Cfg::kIdesc, 1);
+                        if constexpr (ATMEM) {
+                            const uint32_t ah = tmem_base + a_col(stage) + uint32_t(kk * 8);
+                            const uint32_t al = ah + 32;
+                            mma_tf32_ts(d_tmem, al, bh, Cfg::kIdesc, accumulate);
+                            accumulate = 1;
+                            mma_tf32_ts(d_tmem, ah, bl, Cfg::kIdesc, 1);
+                            mma_tf32_ts(d_tmem, ah, bh, Cfg::kIdesc, 1);
+                        } else {
+                            const uint64_t ah = sdesc_k_sw128(a_hi(stage) + kk * 32);
+                            const uint64_t al = sdesc_k_sw128(a_lo(stage) + kk * 32);
+                            mma_tf32_ss(d_tmem, al, bh, Cfg::kIdesc, accumulate);
+                            accumulate = 1;
+                            mma_tf32_ss(d_tmem, ah, bl, Cfg::kIdesc, 1);
+                            mma_tf32_ss(d_tmem, ah, bh, Cfg::kIdesc, 1);
+                        }
                     }
                     issued_any = true;
                     mma_commit(&ctl->empty[stage]);
@@ -297,8 +348,8 @@ __global__ void __launch_bounds__(Roles<Groups<Prob, BN>::value>::kThreads, 1)
         bool ok = true;
         for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
             const Tile tile = prob.tile(t);
-            const int acc = local & 1;
-            const uint32_t acc_phase = (local >> 1) & 1;
+            const int acc = local % DB;
+            const uint32_t acc_phase = uint32_t(local / DB) & 1u;
             if (!mbar_wait_warp(&ctl->accf[acc], acc_phase, abort_flag)) { ok = false; break; }
             tc_fence_after();
             typename Prob::EState es = prob.e_setup(tile, row);
@@ -327,7 +378,7 @@ __global__ void __launch_bounds__(Roles<Groups<Prob, BN>::value>::kThreads, 1)
 template <class Prob, int BN>
 cudaError_t launch_tc_gemm(const Prob& prob, int num_tiles, int* err_word, cudaStream_t stream)
 {
-    using Cfg = TileCfg<BN>;
+    using Cfg = TileCfg<BN, UsesTmemA<Prob>::value>;
     static bool attr_set = false;   // per process; the attribute is per function
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<Prob, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
