@@ -10,23 +10,36 @@
 // shared memory: per element one shared load instead of one global load, and a
 // global request count lower by about the number of taps.
 //
-// Roles (448 threads, one CTA per SM, persistent over tiles):
-//   warps 0-3, 4-7   two converter groups; pipeline stages are dealt to them in
-//                    turn.  A converter thread owns one output position (one A
-//                    row): per stage it reads its 32 K values from the patch,
-//                    splits them into 3xTF32 hi/lo and writes both into the
-//                    stage's tensor-memory columns; the group's first thread
-//                    bulk-copies the stage's pre-split B tiles.
+// Roles (480 threads, one CTA per SM, persistent over tiles):
+//   warps 0-3, 4-7   two converter groups.  A converter thread owns one output
+//                    position (one A row): per stage it reads its 32 K values
+//                    from the patch, splits them into 3xTF32 hi/lo and writes
+//                    both into the stage's tensor-memory columns; the group's
+//                    first thread bulk-copies the stage's pre-split B tiles.
 //   warp 8           patch loader: fills a ring of two patch buffers one
 //                    chunk ahead, one bulk copy per channel run.
-//   warp 9           tensor-memory allocation; lane 0 issues tcgen05.mma with
-//                    A from tensor memory and B from shared memory.
-//   warps 10-13      epilogue (as in gemm_tc.cuh).
+//   warps 9, 10      MMA issuers (lane 0 of each; warp 9 also allocates tensor
+//                    memory): tcgen05.mma with A from tensor memory and B from
+//                    shared memory.
+//   warps 11-14      epilogue: adds the two issuers' accumulators and hands
+//                    the rows to the problem's store.
 //
-// Every converter warp waits on every chunk's "patch loaded" barrier and
-// signals every chunk's "patch read" barrier, and the two groups take
-// alternating stages with fewer groups than stages, so each parity wait is at
-// most one phase ahead of its barrier.  All waits are bounded (ptx.cuh).
+// Two issuers, because one thread cannot issue tcgen05.mma fast enough to keep
+// the tensor core busy on tiles this narrow (N <= 128): measured on GB300, a
+// single thread issues about one MMA per 25 ns whatever N is, while an
+// M=128, N=64, K=8 tf32 MMA takes the pipe about 16 ns, and every stage
+// handshake (barrier wait + commit) stalls the issuing thread further.  With
+// two threads feeding separate accumulators the pipe stays near its peak.
+//
+// The K stages of a tile are split by parity of the CTA-wide stage counter c:
+// stage c is filled by converter group c % 2 into slot c % S (S even, so the
+// slot has the same parity) and consumed by issuer c % 2 into that issuer's
+// accumulator; the epilogue adds accumulator 0 and accumulator 1 (always in
+// that order, so results do not depend on timing).  Each slot therefore has
+// exactly one filler group and one consumer, each visiting it in stage order,
+// so every parity wait is at most one phase ahead of its barrier.  Every
+// converter warp waits on every chunk's "patch loaded" barrier and signals its
+// "patch read" barrier.  All waits are bounded (ptx.cuh).
 #pragma once
 #include "gemm_tc.cuh"
 
@@ -98,13 +111,18 @@ __device__ __forceinline__ void patch_taps(const PatchGeom& g, const float* pbuf
 
 template <int BN>
 struct PatchCfg {
-    static_assert(BN <= 128, "the patch kernel keeps two accumulators and up to six A stages in tensor memory");
-    static constexpr int kDBuf = 2;
-    static constexpr int kTmemStages0 = (512 - kDBuf * BN) / 64;
-    static constexpr int kStages = kTmemStages0 > 6 ? 6 : kTmemStages0;
+    static_assert(BN <= 128, "the patch kernel keeps an accumulator per issuer and at least four A stages in "
+                             "tensor memory");
+    static constexpr int kThreads = 480;
+    // accumulator buffers per issuer: two (the epilogue of tile i overlaps the
+    // main loop of tile i+1) when six A stages still fit beside them, else one
+    static constexpr int kDBuf = (512 - 4 * BN) / 64 >= 6 ? 2 : 1;
+    static constexpr int kTmemStages0 = (512 - 2 * kDBuf * BN) / 64;
+    static constexpr int kStages = (kTmemStages0 > 6 ? 6 : kTmemStages0) & ~1;   // even: slot parity = issuer
+    static_assert(kStages >= 4, "too few A stages fit in tensor memory");
     static constexpr uint32_t kBTile = BN * kBK * 4;
     static constexpr uint32_t kStage = 2 * kBTile;
-    static constexpr uint32_t kACol = uint32_t(kDBuf * BN);
+    static constexpr uint32_t kACol = uint32_t(2 * kDBuf * BN);   // accumulators: [buffer][issuer]
     static constexpr size_t kCtlBytes = 512;
     static constexpr size_t kMaxSmem = 227 * 1024;
     // two patch buffers share what the B stages leave
@@ -122,7 +140,7 @@ struct PatchCtl {
     uint64_t acce[2];
     uint64_t pfull[2];     // patch buffer holds its chunk (loader arrival)
     uint64_t pempty[2];    // every converter warp is done with the buffer (8 arrivals)
-    uint64_t drain;
+    uint64_t drain[2];
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -131,7 +149,7 @@ struct PatchCtl {
 // as ConvGatherProb: b_image, EState, e_setup, store).  Tile decode is fixed:
 // t -> (n_tile = t % n_tiles, image, tile in image).
 template <class Prob, int BN>
-__global__ void __launch_bounds__(448, 1) tc_patch_kernel(const __grid_constant__ Prob prob, int* err_word)
+__global__ void __launch_bounds__(PatchCfg<BN>::kThreads, 1) tc_patch_kernel(const __grid_constant__ Prob prob, int* err_word)
 {
     using Cfg = PatchCfg<BN>;
     constexpr int S = Cfg::kStages;
@@ -157,12 +175,12 @@ __global__ void __launch_bounds__(448, 1) tc_patch_kernel(const __grid_constant_
             mbar_init(&ctl->empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&ctl->accf[b], 1);
+            mbar_init(&ctl->accf[b], 2);   // one commit per issuer
             mbar_init(&ctl->acce[b], 4);
             mbar_init(&ctl->pfull[b], 1);
             mbar_init(&ctl->pempty[b], 8);
+            mbar_init(&ctl->drain[b], 1);
         }
-        mbar_init(&ctl->drain, 1);
         ctl->abort_flag = 0;
         mbar_fence_init();
     }
@@ -332,30 +350,32 @@ __global__ void __launch_bounds__(448, 1) tc_patch_kernel(const __grid_constant_
             }
         }
         if (!ok) fail();
-    } else if (warp == 9) {
-        // ---------------- MMA issuer ----------------
+    } else if (warp == 9 || warp == 10) {
+        // ---------------- MMA issuers ----------------
+        const uint32_t me = uint32_t(warp - 9);
         if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
             int local = 0;
             bool ok = true;
             bool issued_any = false;
-            const int k_stages = g.nch * g.spc;
+            const uint32_t k_stages = uint32_t(g.nch * g.spc);
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
-                const int acc = local % DB;
+                const int buf = local % DB;
                 const uint32_t acc_phase = uint32_t(local / DB) & 1u;
-                if (!mbar_wait(&ctl->acce[acc], acc_phase ^ 1, abort_flag)) { ok = false; break; }
+                if (!mbar_wait(&ctl->acce[buf], acc_phase ^ 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
+                const uint32_t d_tmem = tmem_base + uint32_t((2 * buf + int(me)) * BN);
+                const uint32_t c0 = uint32_t(local) * k_stages;   // CTA-wide counter of the tile's first stage
                 uint32_t accumulate = 0;
-                for (int ks = 0; ks < k_stages; ++ks) {
-                    if (!mbar_wait(&ctl->full[stage], phase, abort_flag)) { ok = false; break; }
+                for (uint32_t ks = me ^ (c0 & 1u); ks < k_stages; ks += 2) {
+                    const uint32_t c = c0 + ks;
+                    const int slot = int(c % uint32_t(S));
+                    if (!mbar_wait(&ctl->full[slot], (c / uint32_t(S)) & 1u, abort_flag)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < kBK / 8; ++kk) {
-                        const uint64_t bh = sdesc_k_sw128(b_hi(stage) + kk * 32);
-                        const uint64_t bl = sdesc_k_sw128(b_lo(stage) + kk * 32);
-                        const uint32_t ah = tmem_base + a_col(stage) + uint32_t(kk * 8);
+                        const uint64_t bh = sdesc_k_sw128(b_hi(slot) + kk * 32);
+                        const uint64_t bl = sdesc_k_sw128(b_lo(slot) + kk * 32);
+                        const uint32_t ah = tmem_base + a_col(slot) + uint32_t(kk * 8);
                         const uint32_t al = ah + 32;
                         mma_tf32_ts(d_tmem, al, bh, Cfg::kIdesc, accumulate);
                         accumulate = 1;
@@ -363,18 +383,19 @@ __global__ void __launch_bounds__(448, 1) tc_patch_kernel(const __grid_constant_
                         mma_tf32_ts(d_tmem, ah, bh, Cfg::kIdesc, 1);
                     }
                     issued_any = true;
-                    mma_commit(&ctl->empty[stage]);
-                    if (++stage == S) { stage = 0; phase ^= 1; }
+                    mma_commit(&ctl->empty[slot]);
                 }
                 if (!ok) break;
-                mma_commit(&ctl->accf[acc]);
+                // arrives once this issuer's MMAs of the tile are done (at once
+                // if it had none: a one-stage tile)
+                mma_commit(&ctl->accf[buf]);
             }
             if (!ok) {
                 fail();
                 if (issued_any) {
-                    mma_commit(&ctl->drain);
+                    mma_commit(&ctl->drain[me]);
                     uint64_t t0 = globaltimer_ns();
-                    while (!mbar_try_wait(&ctl->drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+                    while (!mbar_try_wait(&ctl->drain[me], 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
                 }
             }
         }
@@ -383,24 +404,37 @@ __global__ void __launch_bounds__(448, 1) tc_patch_kernel(const __grid_constant_
         // ---------------- epilogue ----------------
         const int q = warp & 3;
         const int row = q * 32 + lane;
+        const uint32_t k_stages = uint32_t(g.nch * g.spc);
         int local = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
-            const int acc = local % DB;
+            const int buf = local % DB;
             const uint32_t acc_phase = uint32_t(local / DB) & 1u;
-            if (!mbar_wait_warp(&ctl->accf[acc], acc_phase, abort_flag)) { ok = false; break; }
+            if (!mbar_wait_warp(&ctl->accf[buf], acc_phase, abort_flag)) { ok = false; break; }
             tc_fence_after();
+            // a one-stage tile leaves the other issuer's accumulator untouched
+            const uint32_t c0 = uint32_t(local) * k_stages;
+            const bool use0 = k_stages >= 2 || (c0 & 1u) == 0;
+            const bool use1 = k_stages >= 2 || (c0 & 1u) == 1;
             const Tile tile = prob.tile_t(t);
             typename Prob::EState es = prob.e_setup_t(t, row);
+            const uint32_t lane_base = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(2 * buf * BN);
 #pragma unroll 1
             for (int c = 0; c < BN; c += 32) {
-                uint32_t r[32];
-                tmem_ld32(tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * BN + c), r);
-                prob.store(es, tile, row, c, r);
+                uint32_t r0[32], r1[32];
+                tmem_ld32x2(lane_base + uint32_t(c), lane_base + uint32_t(BN + c), r0, r1);
+                if (c + 32 >= BN) {
+                    // the accumulators are free once the last columns are in registers
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctl->acce[buf]);
+                }
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    r0[i] = __float_as_uint((use0 ? __uint_as_float(r0[i]) : 0.f) +
+                                            (use1 ? __uint_as_float(r1[i]) : 0.f));
+                prob.store(es, tile, row, c, r0);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctl->acce[acc]);
         }
         if (!ok) fail();
     }
@@ -426,7 +460,7 @@ cudaError_t launch_tc_patch(const Prob& prob, int num_tiles, int* err_word, cuda
     }
     if (num_tiles <= 0) return cudaSuccess;
     int grid = num_tiles < sm_count() ? num_tiles : sm_count();
-    tc_patch_kernel<Prob, BN><<<grid, 448, Cfg::kSmemBytes, stream>>>(prob, err_word);
+    tc_patch_kernel<Prob, BN><<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(prob, err_word);
     note_launch();
     return cudaGetLastError();
 }
