@@ -168,25 +168,85 @@ __global__ void maxpool_fwd_kernel(const float* __restrict__ x, float* __restric
     }
 }
 
-// Plane-staged variant: a block copies whole (n, c) planes of x into shared
-// memory with coalesced loads, then each thread scans its windows there and
-// writes y / idx coalesced.  x is read from HBM exactly once.
-constexpr int kPoolThreads = 256;
-constexpr int kPoolSmemFloats = 8192;   // 32 KB of staged planes per block
+// Staged variants.  Consecutive (n, c) planes are contiguous, so a group of
+// `ppb` planes is one contiguous range: a block stages it into shared memory
+// with one bulk copy (the tensor engine moves the bytes; no thread issues
+// loads) and scans the windows there.  Two stage buffers per block: while
+// group i is scanned, group i + 1 is in flight.  Blocks are persistent (a
+// few per SM) and take groups blockIdx.x, blockIdx.x + gridDim.x, ...
+constexpr int kPoolThreads = 512;
+constexpr int kPoolStageFloats = 6144;   // 24 KB per staged range
 
-__global__ void __launch_bounds__(kPoolThreads) maxpool_fwd_plane_kernel(
-    const float* __restrict__ x, float* __restrict__ y, int32_t* __restrict__ idx, int NC, int H, int W, int k, int S,
-    int P, int Q, int ppb, FastDiv f_pq, FastDiv f_q)
+// Thread 0: copy elements [start, start + count) of a tensor of `total`
+// elements into dst so that element start + i lands at dst[(start & 3) + i].
+// The tensor base is 16-byte aligned, so the bulk copy covers whole 16-byte
+// blocks; up to 3 elements past the tensor's last 16-byte boundary are
+// loaded with plain loads.  Returns the bulk-copied bytes.
+__device__ __forceinline__ uint32_t stage_range_bytes(long long start, int count, long long total)
 {
-    extern __shared__ float sx[];
+    const long long a0 = start & ~3LL;
+    long long a1 = (start + count + 3) & ~3LL;
+    const long long lim = total & ~3LL;
+    if (a1 > lim) a1 = lim;
+    return a1 > a0 ? uint32_t((a1 - a0) * 4) : 0u;
+}
+
+__device__ __forceinline__ void stage_range(float* dst, const float* base, long long start, int count, long long total,
+                                            uint64_t* bar)
+{
+    const long long a0 = start & ~3LL;
+    const uint32_t bytes = stage_range_bytes(start, count, total);
+    const long long a1 = a0 + bytes / 4;
+    for (long long e = a1 > start ? a1 : start; e < start + count; ++e) dst[e - a0] = __ldg(base + e);
+    if (bytes) bulk_g2s(dst, base + a0, bytes, bar);
+}
+
+// Bounded wait by every thread of the block on a staging barrier.  The
+// outcome is agreed block-wide (a barrier every thread reaches), so either all
+// threads go on or all leave the loop together; on give-up the device error
+// word is set.
+__device__ __forceinline__ bool stage_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err)
+{
+    const bool got = mbar_wait(bar, parity, abort_flag);
+    if (__syncthreads_and(got ? 1 : 0)) return true;
+    if (threadIdx.x == 0) {
+        *abort_flag = 1;
+        atomicOr(err, kDevErrTimeout);
+    }
+    return false;
+}
+
+__global__ void __launch_bounds__(kPoolThreads, 4) maxpool_fwd_staged_kernel(
+    const float* __restrict__ x, float* __restrict__ y, int32_t* __restrict__ idx, int NC, int H, int W, int k, int S,
+    int P, int Q, int ppb, int stage_floats, FastDiv f_pq, FastDiv f_q, int* err)
+{
+    extern __shared__ __align__(16) float pool_smem[];
+    __shared__ uint64_t bar[2];
+    __shared__ int abort_flag;
     const int HW = H * W, PQ = P * Q;
-    for (int nc0 = blockIdx.x * ppb; nc0 < NC; nc0 += gridDim.x * ppb) {
-        const int np = min(ppb, NC - nc0);
-        const float* src = x + size_t(nc0) * HW;
-        const int total = np * HW;
-#pragma unroll 4
-        for (int i = threadIdx.x; i < total; i += kPoolThreads) sx[i] = __ldg(src + i);
-        __syncthreads();
+    const long long total = (long long)NC * HW;
+    const int groups = (NC + ppb - 1) / ppb;
+    auto issue = [&](int g, int b) {
+        const int nc0 = g * ppb, np = min(ppb, NC - nc0);
+        const long long start = (long long)nc0 * HW;
+        mbar_arrive_expect_tx(&bar[b], stage_range_bytes(start, np * HW, total));
+        stage_range(pool_smem + b * stage_floats, x, start, np * HW, total, &bar[b]);
+    };
+    if (threadIdx.x == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        abort_flag = 0;
+        mbar_fence_init();
+        for (int i = 0; i < 2; ++i)
+            if (int(blockIdx.x) + i * int(gridDim.x) < groups) issue(blockIdx.x + i * gridDim.x, i);
+    }
+    __syncthreads();
+    int i = 0, g = blockIdx.x;
+    for (; g < groups; g += gridDim.x, ++i) {
+        const int b = i & 1;
+        if (!stage_wait(&bar[b], uint32_t(i >> 1) & 1u, &abort_flag, err)) break;
+        const int nc0 = g * ppb, np = min(ppb, NC - nc0);
+        const float* sx = pool_smem + b * stage_floats + ((long long)nc0 * HW & 3);
         const int nout = np * PQ;
         for (int o = threadIdx.x; o < nout; o += kPoolThreads) {
             uint32_t pl, pq, oh, ow;
@@ -207,73 +267,151 @@ __global__ void __launch_bounds__(kPoolThreads) maxpool_fwd_plane_kernel(
             y[size_t(nc0) * PQ + o] = m;
             idx[size_t(nc0) * PQ + o] = nc0 * HW + best;
         }
-        __syncthreads();
+        __syncthreads();   // buffer b fully read
+        if (threadIdx.x == 0 && g + 2 * int(gridDim.x) < groups) {
+            fence_proxy_async_smem();
+            issue(g + 2 * gridDim.x, b);
+        }
+    }
+    if (abort_flag && threadIdx.x == 0) {
+        // let copies still in flight (groups g and g + gridDim.x) land before
+        // the block's memory goes away
+        for (int j = 0; j < 2 && g + j * int(gridDim.x) < groups; ++j) {
+            uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(&bar[(i + j) & 1], uint32_t((i + j) >> 1) & 1u) &&
+                   globaltimer_ns() - t0 < kWaitLimitNs) {
+            }
+        }
     }
 }
 
-// Plane-staged backward: a block stages the windows' gradients and indices of
-// whole planes, then each thread gathers, in ascending window order, the
-// gradients routed to its input pixel and writes dx coalesced.  The window
-// rows covering input row h (and columns covering w) come from small tables
-// built once per block, so the per-pixel work is table lookups and compares.
-__global__ void __launch_bounds__(kPoolThreads) maxpool_bwd_plane_kernel(
+// Staged backward: a group's window gradients and saved indices (two
+// contiguous ranges) are staged per buffer.  Each thread owns an S x S block
+// of input pixels (rows S*i .., columns S*j ..).  It visits, in ascending
+// (oh, ow) order, the windows that can reach its block -- oh from
+// ceil((S*i - k + 1) / S) to i, the same for ow -- and adds each window's
+// gradient to the pixel of the block its saved index names, if any.  Every
+// pixel therefore sums its contributions in ascending window order (the
+// oracle's order) with a handful of compares per window and no per-pixel
+// division; the S*S results are written with coalesced stores.
+template <int S>
+__global__ void __launch_bounds__(kPoolThreads, 4) maxpool_bwd_staged_kernel(
     const float* __restrict__ dy, const int32_t* __restrict__ idx, float* __restrict__ dx, int NC, int H, int W,
-    int k, int S, int P, int Q, int ppb, FastDiv f_hw, FastDiv f_w)
+    int k, int P, int Q, int ppb, int stage_floats, int BH, int BW, FastDiv f_blk, FastDiv f_bw, int* err)
 {
-    extern __shared__ float sm[];
+    extern __shared__ __align__(16) float pool_smem[];
+    __shared__ uint64_t bar[2];
+    __shared__ int abort_flag;
     const int HW = H * W, PQ = P * Q;
-    float* sdy = sm;
-    int* sidx = reinterpret_cast<int*>(sm + ppb * PQ);
-    int* hrange = sidx + ppb * PQ;   // (first window row << 16) | last window row, per input row
-    int* wrange = hrange + H;        // same per input column
-    for (int i = threadIdx.x; i < H + W; i += kPoolThreads) {
-        const int v = i < H ? i : i - H;
-        const int lim = i < H ? P - 1 : Q - 1;
-        const int lo = v - k + 1 <= 0 ? 0 : (v - k + S) / S;
-        const int hi = min(v / S, lim);
-        (i < H ? hrange[i] : wrange[i - H]) = (lo << 16) | (hi & 0xFFFF);
+    // per buffer (2 * stage_floats): [gradients (stage_floats)][indices (stage_floats)]
+    const long long total = (long long)NC * PQ;
+    const int groups = (NC + ppb - 1) / ppb;
+    auto issue = [&](int g, int b) {
+        const int nc0 = g * ppb, np = min(ppb, NC - nc0);
+        const long long start = (long long)nc0 * PQ;
+        mbar_arrive_expect_tx(&bar[b], 2 * stage_range_bytes(start, np * PQ, total));
+        float* sb = pool_smem + 2 * b * stage_floats;
+        stage_range(sb, dy, start, np * PQ, total, &bar[b]);
+        stage_range(sb + stage_floats, reinterpret_cast<const float*>(idx), start, np * PQ, total, &bar[b]);
+    };
+    if (threadIdx.x == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        abort_flag = 0;
+        mbar_fence_init();
+        for (int i = 0; i < 2; ++i)
+            if (int(blockIdx.x) + i * int(gridDim.x) < groups) issue(blockIdx.x + i * gridDim.x, i);
     }
-    for (int nc0 = blockIdx.x * ppb; nc0 < NC; nc0 += gridDim.x * ppb) {
-        const int np = min(ppb, NC - nc0);
-        const int nwin = np * PQ;
-#pragma unroll 4
-        for (int i = threadIdx.x; i < nwin; i += kPoolThreads) {
-            sdy[i] = __ldg(dy + size_t(nc0) * PQ + i);
-            sidx[i] = __ldg(idx + size_t(nc0) * PQ + i);
-        }
-        __syncthreads();
-        const int total = np * HW;
-        for (int i = threadIdx.x; i < total; i += kPoolThreads) {
-            uint32_t pl, hw, h, w;
-            f_hw.divmod(uint32_t(i), pl, hw);
-            f_w.divmod(hw, h, w);
-            const int flat = nc0 * HW + i;
-            const int hr = hrange[h], wr = wrange[w];
-            const int oh_lo = hr >> 16, oh_hi = hr & 0xFFFF;   // oh_hi < oh_lo: no window
-            const int ow_lo = wr >> 16, ow_hi = wr & 0xFFFF;
+    __syncthreads();
+    const int nblk_plane = BH * BW;
+    int it = 0, g = blockIdx.x;
+    for (; g < groups; g += gridDim.x, ++it) {
+        const int b = it & 1;
+        if (!stage_wait(&bar[b], uint32_t(it >> 1) & 1u, &abort_flag, err)) break;
+        const int nc0 = g * ppb, np = min(ppb, NC - nc0);
+        const int sh = int((long long)nc0 * PQ & 3);
+        const float* sdy = pool_smem + 2 * b * stage_floats + sh;
+        const int* sidx = reinterpret_cast<const int*>(sdy + stage_floats);
+        const int nblk = np * nblk_plane;
+        for (int t = threadIdx.x; t < nblk; t += kPoolThreads) {
+            uint32_t pl, ij, bi, bj;
+            f_blk.divmod(uint32_t(t), pl, ij);
+            f_bw.divmod(ij, bi, bj);
+            const int h0 = S * int(bi), w0 = S * int(bj);
+            const int base = (nc0 + int(pl)) * HW + h0 * W + w0;   // flat index of the block's first pixel
+            const int oh_lo = h0 - k + 1 <= 0 ? 0 : (h0 - k + S) / S;
+            const int oh_hi = min(int(bi), P - 1);
+            const int ow_lo = w0 - k + 1 <= 0 ? 0 : (w0 - k + S) / S;
+            const int ow_hi = min(int(bj), Q - 1);
+            float acc[S * S];
+#pragma unroll
+            for (int a = 0; a < S * S; ++a) acc[a] = 0.f;
             const int* irow = sidx + int(pl) * PQ;
             const float* drow = sdy + int(pl) * PQ;
-            float acc = 0.f;
             for (int oh = oh_lo; oh <= oh_hi; ++oh)
                 for (int ow = ow_lo; ow <= ow_hi; ++ow) {
                     const int o = oh * Q + ow;
-                    if (irow[o] == flat) acc += drow[o];
+                    const int d = irow[o] - base;
+                    const float v = drow[o];
+#pragma unroll
+                    for (int dh = 0; dh < S; ++dh)
+#pragma unroll
+                        for (int dw = 0; dw < S; ++dw)
+                            if (w0 + dw < W && d == dh * W + dw) acc[dh * S + dw] += v;   // no wrap into the next row
                 }
-            dx[size_t(nc0) * HW + i] = acc;
+            float* out = dx + base;
+#pragma unroll
+            for (int dh = 0; dh < S; ++dh)
+#pragma unroll
+                for (int dw = 0; dw < S; ++dw)
+                    if (h0 + dh < H && w0 + dw < W) out[dh * W + dw] = acc[dh * S + dw];
         }
         __syncthreads();
+        if (threadIdx.x == 0 && g + 2 * int(gridDim.x) < groups) {
+            fence_proxy_async_smem();
+            issue(g + 2 * gridDim.x, b);
+        }
     }
+    if (abort_flag && threadIdx.x == 0) {
+        for (int j = 0; j < 2 && g + j * int(gridDim.x) < groups; ++j) {
+            uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(&bar[(it + j) & 1], uint32_t((it + j) >> 1) & 1u) &&
+                   globaltimer_ns() - t0 < kWaitLimitNs) {
+            }
+        }
+    }
+}
+
+// Blocks per SM for a staged kernel using `smem` bytes of dynamic shared memory.
+static int staged_grid(int groups, size_t smem)
+{
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaFuncSetAttribute(maxpool_fwd_staged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+        cudaFuncSetAttribute(maxpool_bwd_staged_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+        cudaFuncSetAttribute(maxpool_bwd_staged_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+        cudaFuncSetAttribute(maxpool_bwd_staged_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+        attr_set = true;
+    }
+    int per_sm = int((200 * 1024) / (smem + 1024));
+    if (per_sm > 4) per_sm = 4;
+    if (per_sm < 1) per_sm = 1;
+    const int cap = per_sm * sm_count();
+    return groups < cap ? groups : cap;
 }
 
 cudaError_t launch_maxpool_fwd(int N, int C, int H, int W, int k, int s, int P, int Q, const float* x, float* y,
                                int32_t* idx, cudaStream_t st)
 {
     const int NC = N * C;
-    if (H * W <= kPoolSmemFloats) {
-        const int ppb = kPoolSmemFloats / (H * W) < 8 ? kPoolSmemFloats / (H * W) : 8;
-        const int blocks = (NC + ppb - 1) / ppb;
-        maxpool_fwd_plane_kernel<<<blocks, kPoolThreads, size_t(ppb) * H * W * sizeof(float), st>>>(
-            x, y, idx, NC, H, W, k, s, P, Q, ppb, FastDiv(P * Q), FastDiv(Q));
+    const int HW = H * W;
+    if (HW + 4 <= kPoolStageFloats) {
+        const int ppb = (kPoolStageFloats - 4) / HW < 64 ? (kPoolStageFloats - 4) / HW : 64;
+        const int stage = (ppb * HW + 4 + 3) & ~3;   // floats per buffer (room for the 16-byte shift)
+        const size_t smem = 2 * size_t(stage) * sizeof(float);
+        const int groups = (NC + ppb - 1) / ppb;
+        maxpool_fwd_staged_kernel<<<staged_grid(groups, smem), kPoolThreads, smem, st>>>(
+            x, y, idx, NC, H, W, k, s, P, Q, ppb, stage, FastDiv(P * Q), FastDiv(Q), device_error_word());
         note_launch();
         return cudaGetLastError();
     }
@@ -314,12 +452,29 @@ cudaError_t launch_maxpool_bwd(int N, int C, int H, int W, int k, int s, int P, 
                                const int32_t* idx, float* dx, cudaStream_t st)
 {
     const int NC = N * C;
-    if (P * Q * 2 + H + W <= kPoolSmemFloats) {
-        int ppb = (kPoolSmemFloats - H - W) / (2 * P * Q);
-        if (ppb > 8) ppb = 8;
-        const int blocks = (NC + ppb - 1) / ppb;
-        maxpool_bwd_plane_kernel<<<blocks, kPoolThreads, (size_t(ppb) * P * Q * 2 + H + W) * sizeof(float), st>>>(
-            dy, idx, dx, NC, H, W, k, s, P, Q, ppb, FastDiv(H * W), FastDiv(W));
+    const int PQ = P * Q;
+    if (PQ + 4 <= kPoolStageFloats / 2 && s >= 1 && s <= 3) {
+        const int ppb = (kPoolStageFloats / 2 - 4) / PQ < 64 ? (kPoolStageFloats / 2 - 4) / PQ : 64;
+        const int stage = (ppb * PQ + 4 + 3) & ~3;
+        const size_t smem = 4 * size_t(stage) * sizeof(float);
+        const int groups = (NC + ppb - 1) / ppb;
+        const int BH = (H + s - 1) / s, BW = (W + s - 1) / s;
+        const int grid = staged_grid(groups, smem);
+        const FastDiv f_blk{uint32_t(BH * BW)}, f_bw{uint32_t(BW)};
+        switch (s) {
+        case 1:
+            maxpool_bwd_staged_kernel<1><<<grid, kPoolThreads, smem, st>>>(dy, idx, dx, NC, H, W, k, P, Q, ppb, stage,
+                                                                           BH, BW, f_blk, f_bw, device_error_word());
+            break;
+        case 2:
+            maxpool_bwd_staged_kernel<2><<<grid, kPoolThreads, smem, st>>>(dy, idx, dx, NC, H, W, k, P, Q, ppb, stage,
+                                                                           BH, BW, f_blk, f_bw, device_error_word());
+            break;
+        default:
+            maxpool_bwd_staged_kernel<3><<<grid, kPoolThreads, smem, st>>>(dy, idx, dx, NC, H, W, k, P, Q, ppb, stage,
+                                                                           BH, BW, f_blk, f_bw, device_error_word());
+            break;
+        }
         note_launch();
         return cudaGetLastError();
     }
@@ -367,37 +522,44 @@ cudaError_t launch_sgd(int64_t count, float lr, float clip, float* p, const floa
 
 // ---------------------------------------------------------------------------
 // Bias gradient: db[k] = sum over (n, oh, ow) of dy[n, k, oh, ow].
-// One 8-CTA cluster per filter k: CTA r sums images n = r, r + 8, ... with a
-// fixed thread/warp order, then CTA 0 adds the 8 partial sums from the
-// cluster's shared memory in rank order.  Deterministic, no atomics.
+// One cluster of CS CTAs per filter k (CS = 1..8, chosen per call from the
+// work per filter).  CTA r of the cluster sums the planes (n, k) of images
+// n = r, r + CS, ...: thread t takes elements t, t + 512, ... of that list of
+// planes, cycling over eight accumulators (eight loads in flight); the
+// position in the list is advanced incrementally, without divisions.  The
+// accumulators, the warp lanes, the warps and finally the cluster's CTAs (read
+// through distributed shared memory by CTA 0) are combined in fixed orders,
+// so the result is deterministic; no atomics.
 
-constexpr int kBiasCluster = 8;
 constexpr int kBiasThreads = 512;
+constexpr int kBiasMaxCluster = 8;
 
-__global__ void __cluster_dims__(kBiasCluster, 1, 1) __launch_bounds__(kBiasThreads)
-    bias_grad_kernel(const float* __restrict__ dy, float* __restrict__ db, int N, int K, int PQ, FastDiv f_pq)
+__global__ void __launch_bounds__(kBiasThreads, 4)
+    bias_grad_kernel(const float* __restrict__ dy, float* __restrict__ db, int N, int K, int PQ)
 {
     cg::cluster_group cluster = cg::this_cluster();
     __shared__ float warp_part[kBiasThreads / 32];
     __shared__ float cta_part;
-    const int k = blockIdx.x / kBiasCluster;
+    const int cs = int(cluster.num_blocks());
     const int rank = int(cluster.block_rank());
-    // This CTA sums images n = rank, rank + 8, ...: element e of that list is
-    // (image rank + 8 * (e / PQ), pixel e % PQ).  Eight independent partial
-    // sums per thread keep eight loads in flight; they are combined in a
-    // fixed order, so the result is deterministic.
-    const int images = (N - rank + kBiasCluster - 1) / kBiasCluster;
-    const int total = images * PQ;
+    const int k = blockIdx.x / cs;
+    const int images = (N - rank + cs - 1) / cs;          // planes this CTA sums
+    const int img_stride = cs * K * PQ;                   // elements between its consecutive planes
+    const int step_n = kBiasThreads / PQ, step_e = kBiasThreads % PQ;
+    int nl = int(threadIdx.x) / PQ, e = int(threadIdx.x) % PQ;
+    unsigned off = unsigned((rank * K + k) * PQ + nl * img_stride + e);   // may run past the end once nl >= images: never loaded
     float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int e0 = threadIdx.x; e0 < total; e0 += 8 * kBiasThreads) {
+    while (nl < images) {
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            const int e = e0 + u * kBiasThreads;
-            if (e < total) {
-                uint32_t nl, pq;
-                f_pq.divmod(uint32_t(e), nl, pq);
-                const int n = rank + kBiasCluster * int(nl);
-                part[u] += __ldg(dy + (size_t(n) * K + k) * PQ + pq);
+            if (nl < images) part[u] += __ldg(dy + off);
+            nl += step_n;
+            e += step_e;
+            off += unsigned(step_n * img_stride + step_e);
+            if (e >= PQ) {
+                e -= PQ;
+                ++nl;
+                off += unsigned(img_stride - PQ);
             }
         }
     }
@@ -414,7 +576,7 @@ __global__ void __cluster_dims__(kBiasCluster, 1, 1) __launch_bounds__(kBiasThre
     cluster.sync();
     if (rank == 0 && threadIdx.x == 0) {
         float t = 0.f;
-        for (int r = 0; r < kBiasCluster; ++r) t += *cluster.map_shared_rank(&cta_part, r);
+        for (int r = 0; r < cs; ++r) t += *cluster.map_shared_rank(&cta_part, r);
         db[k] = t;
     }
     cluster.sync();   // keep every CTA's shared memory alive until rank 0 has read it
@@ -422,10 +584,27 @@ __global__ void __cluster_dims__(kBiasCluster, 1, 1) __launch_bounds__(kBiasThre
 
 cudaError_t launch_bias_grad(const ConvDims& d, const float* dy, float* db, cudaStream_t st)
 {
-    bias_grad_kernel<<<d.K * kBiasCluster, kBiasThreads, 0, st>>>(dy, db, d.N, d.K, d.P * d.Q,
-                                                                  FastDiv(d.P * d.Q));
+    // about 16 elements per thread per CTA, at most 8 CTAs per filter
+    const long long per_k = (long long)d.N * d.P * d.Q;
+    long long cs = (per_k + 16LL * kBiasThreads - 1) / (16LL * kBiasThreads);
+    if (cs > kBiasMaxCluster) cs = kBiasMaxCluster;
+    if (cs > d.N) cs = d.N;
+    if (cs < 1) cs = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(d.K * cs));
+    cfg.blockDim = dim3(kBiasThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(cs);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, bias_grad_kernel, dy, db, d.N, d.K, d.P * d.Q);
     note_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace cb200

@@ -223,7 +223,11 @@ def test_col2im(cb, orc, shape):
 # max pooling and SGD (bit-exact)
 
 POOL_CASES = [((4, 6, 28, 28), 2, 2), ((4, 16, 10, 10), 2, 2), ((2, 64, 55, 55), 3, 2), ((2, 192, 27, 27), 3, 2),
-              ((1, 3, 9, 8), 2, 3), ((1, 2, 5, 5), 5, 1), ((3, 1, 7, 7), 1, 1)]
+              ((1, 3, 9, 8), 2, 3), ((1, 2, 5, 5), 5, 1), ((3, 1, 7, 7), 1, 1),
+              # backward owner blocks: S = 3 with k = S, odd widths whose last block runs past the row end,
+              # windows wider than stride + 1, a 2-wide grid, stride 1, and stride 4 (plain gather kernel)
+              ((2, 5, 11, 13), 3, 3), ((2, 4, 7, 9), 4, 2), ((1, 3, 4, 5), 3, 2), ((2, 3, 6, 6), 2, 1),
+              ((1, 2, 13, 13), 3, 4)]
 
 
 @pytest.mark.parametrize("shape,k,s", POOL_CASES)
