@@ -92,9 +92,14 @@ struct ConvGatherProb {
     OutGeom o;
     const float* bimg;
     int m_tiles, n_tiles, k_stages;
+    // Tail split (see plan_tail): units [0, full_units) are whole tiles; each
+    // later tile is cut along K into tail_split pieces whose partial sums go
+    // to part_buf [piece][kBM][BN] and are added by tail_reduce_kernel.
+    int full_units = 0, tail_split = 1;
+    float* part_buf = nullptr;
 
-    __device__ int num_tiles() const { return m_tiles * n_tiles; }
-    __device__ Tile tile(int t) const
+    __device__ int num_tiles() const { return full_units + (m_tiles * n_tiles - full_units) * tail_split; }
+    __device__ Tile whole_tile(int t) const
     {
         Tile r;
         r.n0 = (t % n_tiles) * BN;
@@ -102,6 +107,17 @@ struct ConvGatherProb {
         r.ks0 = 0;
         r.ks1 = k_stages;
         r.grp = t % n_tiles;
+        return r;
+    }
+    __device__ Tile tile(int t) const
+    {
+        if (t < full_units) return whole_tile(t);
+        const int u = t - full_units;
+        const int j = u % tail_split;
+        Tile r = whole_tile(full_units + u / tail_split);
+        r.ks0 = int((long long)j * k_stages / tail_split);
+        r.ks1 = int((long long)(j + 1) * k_stages / tail_split);
+        r.part = u;
         return r;
     }
 
@@ -222,8 +238,16 @@ struct ConvGatherProb {
         return e;
     }
 
-    __device__ void store(const EState& e, const Tile& tl, int, int c0, const uint32_t (&r)[32]) const
+    __device__ void store(const EState& e, const Tile& tl, int row, int c0, const uint32_t (&r)[32]) const
     {
+        if (tl.part >= 0) {
+            float4* d = reinterpret_cast<float4*>(part_buf + (size_t(tl.part) * kBM + row) * BN + c0);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                d[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                   __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+            return;
+        }
         if (!e.valid) return;
         if (o.so == 1) {
 #pragma unroll
@@ -422,25 +446,69 @@ static int k_extent(int ci, int T)
     return T * T * ((ci + 31) / 32 * 32);
 }
 
-size_t conv_fwd_ws(const ConvDims& d)
-{
-    int n_tiles;
-    const int bn = pick_conv_bn(d.K, &n_tiles);
-    return bimage_floats(d.K, k_extent(d.C, d.R), bn) * sizeof(float);
-}
-
 static int dgrad_cols(const ConvDims& d) { return d.C * d.S * d.S; }
 
-size_t conv_dgrad_ws(const ConvDims& d)
+// Tail split.  A persistent grid of P CTAs takes tiles t, t + P, ...; with
+// T = q*P + r tiles (0 < r < P) the last round keeps only r SMs busy for a
+// whole tile time.  Instead, the q*P leading tiles run whole and each of the
+// r trailing tiles is cut along K into `split` pieces (split*r <= P, at least
+// four K stages each), so the last round takes about 1/split of a tile time.
+// The pieces write fp32 partial tiles; tail_reduce_kernel adds them in piece
+// order (deterministic) and applies the normal epilogue.
+struct TailPlan {
+    int full_units, split, tail_tiles;
+    size_t part_floats;
+};
+
+static TailPlan plan_tail(int tiles, int k_stages, int bn)
 {
-    int d_lo, T, n_tiles;
-    dgrad_window(d, &d_lo, &T);
-    const int bn = pick_conv_bn(dgrad_cols(d), &n_tiles);
-    return bimage_floats(dgrad_cols(d), k_extent(d.K, T), bn) * sizeof(float);
+    TailPlan p{tiles, 1, 0, 0};
+    const int P = sm_count();
+    if (tiles <= P || tiles % P == 0) return p;
+    const int rem = tiles % P;
+    int split = P / rem;
+    if (split > k_stages / 4) split = k_stages / 4;
+    if (split < 2) return p;
+    p.full_units = tiles - rem;
+    p.split = split;
+    p.tail_tiles = rem;
+    p.part_floats = size_t(rem) * split * kBM * bn;
+    return p;
 }
 
+// One CTA per (trailing tile, 32-column slice); thread = accumulator row.
 template <int BN>
-static cudaError_t run_gather(const GatherGeom& g, const OutGeom& o, float* img, cudaStream_t st)
+__global__ void __launch_bounds__(kBM) tail_reduce_kernel(const __grid_constant__ ConvGatherProb<BN> prob)
+{
+    const int u0 = blockIdx.x * prob.tail_split;
+    const int row = threadIdx.x;
+    const int c0 = blockIdx.y * 32;
+    float acc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+    for (int j = 0; j < prob.tail_split; ++j) {
+        const float4* src = reinterpret_cast<const float4*>(prob.part_buf + (size_t(u0 + j) * kBM + row) * BN + c0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 v = __ldg(src + i);
+            acc[4 * i] += v.x;
+            acc[4 * i + 1] += v.y;
+            acc[4 * i + 2] += v.z;
+            acc[4 * i + 3] += v.w;
+        }
+    }
+    uint32_t r[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(acc[i]);
+    const Tile tl = prob.whole_tile(prob.full_units + blockIdx.x);
+    const typename ConvGatherProb<BN>::EState e = prob.e_setup(tl, row);
+    prob.store(e, tl, row, c0, r);
+}
+
+static size_t round_up_256(size_t b) { return (b + 255) & ~size_t(255); }
+
+template <int BN>
+static cudaError_t run_gather(const GatherGeom& g, const OutGeom& o, float* img, float* part, cudaStream_t st)
 {
     ConvGatherProb<BN> p;
     p.g = g;
@@ -449,17 +517,27 @@ static cudaError_t run_gather(const GatherGeom& g, const OutGeom& o, float* img,
     p.m_tiles = (g.M + kBM - 1) / kBM;
     p.n_tiles = (o.ncols + BN - 1) / BN;
     p.k_stages = (g.K + kBK - 1) / kBK;
-    return launch_tc_gemm<ConvGatherProb<BN>, BN>(p, p.m_tiles * p.n_tiles, device_error_word(), st);
+    const TailPlan tp = plan_tail(p.m_tiles * p.n_tiles, p.k_stages, BN);
+    p.full_units = tp.full_units;
+    p.tail_split = tp.split;
+    p.part_buf = part;
+    const int units = tp.full_units + tp.tail_tiles * tp.split;
+    cudaError_t e = launch_tc_gemm<ConvGatherProb<BN>, BN>(p, units, device_error_word(), st);
+    if (e != cudaSuccess || tp.tail_tiles == 0) return e;
+    tail_reduce_kernel<BN><<<dim3(unsigned(tp.tail_tiles), unsigned(BN / 32)), kBM, 0, st>>>(p);
+    note_launch();
+    return cudaGetLastError();
 }
 
-static cudaError_t dispatch_gather(int bn, const GatherGeom& g, const OutGeom& o, float* img, cudaStream_t st)
+static cudaError_t dispatch_gather(int bn, const GatherGeom& g, const OutGeom& o, float* img, float* part,
+                                   cudaStream_t st)
 {
     switch (bn) {
-    case 32: return run_gather<32>(g, o, img, st);
-    case 64: return run_gather<64>(g, o, img, st);
-    case 128: return run_gather<128>(g, o, img, st);
-    case 192: return run_gather<192>(g, o, img, st);
-    default: return run_gather<256>(g, o, img, st);
+    case 32: return run_gather<32>(g, o, img, part, st);
+    case 64: return run_gather<64>(g, o, img, part, st);
+    case 128: return run_gather<128>(g, o, img, part, st);
+    case 192: return run_gather<192>(g, o, img, part, st);
+    default: return run_gather<256>(g, o, img, part, st);
     }
 }
 
@@ -525,37 +603,80 @@ static cudaError_t run_patch(const PatchGeom& pg, const OutGeom& o, float* img, 
     return launch_tc_patch<ConvPatchProb<BN>, BN>(p, pg.Nb * pg.tpi * p.n_tiles, device_error_word(), st);
 }
 
+// Which kernel a convolution-window GEMM runs on, and the workspace it needs:
+// the patch-staged kernel when the output tile is at most 128 wide and every
+// tile's patch fits its shared-memory buffer, otherwise the register-gather
+// kernel (which may add a tail split's partial tiles).  Workspace layout:
+// [B image, 256-byte aligned][partial tiles].
+struct WindowPlan {
+    int bn;
+    bool patch;
+    size_t img_bytes, part_bytes;
+};
+
+static WindowPlan plan_window(int Nb, int Ci, int Hi, int Wi, int Gp, int Gq, int sp, int o, int T, int ncols)
+{
+    WindowPlan w{};
+    int n_tiles;
+    w.bn = pick_conv_bn(ncols, &n_tiles);
+    w.patch = false;
+    if (w.bn <= 128) {
+        const PatchGeom pg = make_patch(nullptr, Nb, Ci, Hi, Wi, Gp, Gq, sp, o, T);
+        w.patch = max_patch_floats(pg) <= patch_capacity(w.bn);
+    }
+    w.img_bytes = round_up_256(bimage_floats(ncols, k_extent(Ci, T), w.bn) * sizeof(float));
+    w.part_bytes = 0;
+    if (!w.patch) {
+        const GatherGeom g = make_gather(nullptr, Nb, Ci, Hi, Wi, Gp, Gq, sp, o, T);
+        const TailPlan tp = plan_tail(((g.M + kBM - 1) / kBM) * n_tiles, (g.K + kBK - 1) / kBK, w.bn);
+        w.part_bytes = tp.part_floats * sizeof(float);
+    }
+    return w;
+}
+
 // One convolution-window GEMM over the gathered tensor `in` [Nb][Ci][Hi][Wi]:
-// rows = the (Gp x Gq) grid of each image, window h = p*sp + o + tap.  The
-// patch-staged kernel is used when the output tile is at most 128 wide and
-// every tile's patch fits its shared-memory buffer; otherwise the
-// register-gather kernel.  MakeGen(KDecode) builds the B-operand generator in
-// the matching K order.
+// rows = the (Gp x Gq) grid of each image, window h = p*sp + o + tap.
+// MakeGen(KDecode) builds the B-operand generator in the matching K order.
 template <class MakeGen>
 static cudaError_t run_window_gemm(const float* in, int Nb, int Ci, int Hi, int Wi, int Gp, int Gq, int sp, int o,
-                                   int T, const OutGeom& og, float* img, MakeGen make_gen, cudaStream_t st)
+                                   int T, const OutGeom& og, void* ws, MakeGen make_gen, cudaStream_t st)
 {
-    int n_tiles;
-    const int bn = pick_conv_bn(og.ncols, &n_tiles);
-    if (bn <= 128) {
+    const WindowPlan wp = plan_window(Nb, Ci, Hi, Wi, Gp, Gq, sp, o, T, og.ncols);
+    float* img = static_cast<float*>(ws);
+    const int bn = wp.bn;
+    if (wp.patch) {
         const PatchGeom pg = make_patch(in, Nb, Ci, Hi, Wi, Gp, Gq, sp, o, T);
-        if (max_patch_floats(pg) <= patch_capacity(bn)) {
-            const KDecode dec = make_kdecode(pg.mode == 0 ? 1 : 0, pg.Cp, T);
-            const int k_total = pg.mode == 0 ? pg.nch * T * T * kBK : T * T * pg.Cp;   // padded taps excluded
-            cudaError_t e = build_bimage(make_gen(dec), og.ncols, k_total, bn, img, st);
-            if (e != cudaSuccess) return e;
-            switch (bn) {
-            case 32: return run_patch<32>(pg, og, img, st);
-            case 64: return run_patch<64>(pg, og, img, st);
-            default: return run_patch<128>(pg, og, img, st);
-            }
+        const KDecode dec = make_kdecode(pg.mode == 0 ? 1 : 0, pg.Cp, T);
+        const int k_total = pg.mode == 0 ? pg.nch * T * T * kBK : T * T * pg.Cp;   // padded taps excluded
+        cudaError_t e = build_bimage(make_gen(dec), og.ncols, k_total, bn, img, st);
+        if (e != cudaSuccess) return e;
+        switch (bn) {
+        case 32: return run_patch<32>(pg, og, img, st);
+        case 64: return run_patch<64>(pg, og, img, st);
+        default: return run_patch<128>(pg, og, img, st);
         }
     }
     const GatherGeom g = make_gather(in, Nb, Ci, Hi, Wi, Gp, Gq, sp, o, T);
     const KDecode dec = make_kdecode(g.mode == 2 ? 2 : 0, g.Cp, T);
     cudaError_t e = build_bimage(make_gen(dec), og.ncols, g.K, bn, img, st);
     if (e != cudaSuccess) return e;
-    return dispatch_gather(bn, g, og, img, st);
+    float* part = reinterpret_cast<float*>(static_cast<char*>(ws) + wp.img_bytes);
+    return dispatch_gather(bn, g, og, img, part, st);
+}
+
+size_t conv_fwd_ws(const ConvDims& d)
+{
+    const WindowPlan wp = plan_window(d.N, d.C, d.H, d.W, d.P, d.Q, d.S, -d.pad, d.R, d.K);
+    return wp.img_bytes + wp.part_bytes;
+}
+
+size_t conv_dgrad_ws(const ConvDims& d)
+{
+    int d_lo, T;
+    dgrad_window(d, &d_lo, &T);
+    const int Hs = (d.H + d.S - 1) / d.S, Ws = (d.W + d.S - 1) / d.S;
+    const WindowPlan wp = plan_window(d.N, d.K, d.P, d.Q, Hs, Ws, 1, d_lo, T, dgrad_cols(d));
+    return wp.img_bytes + wp.part_bytes;
 }
 
 cudaError_t launch_conv_fwd(const ConvDims& d, const float* x, const float* w, const float* b, float* y, void* ws,
@@ -571,8 +692,7 @@ cudaError_t launch_conv_fwd(const ConvDims& d, const float* x, const float* w, c
     o.so = 1;
     o.ncols = d.K;
     auto make_gen = [&](const KDecode& dec) { return FwdFilterGen{w, d.C, d.R, dec, FastDiv(uint32_t(d.R))}; };
-    return run_window_gemm(x, d.N, d.C, d.H, d.W, d.P, d.Q, d.S, -d.pad, d.R, o, static_cast<float*>(ws), make_gen,
-                           st);
+    return run_window_gemm(x, d.N, d.C, d.H, d.W, d.P, d.Q, d.S, -d.pad, d.R, o, ws, make_gen, st);
 }
 
 cudaError_t launch_conv_dgrad(const ConvDims& d, const float* w, const float* dy, float* dx, void* ws,
@@ -594,7 +714,7 @@ cudaError_t launch_conv_dgrad(const ConvDims& d, const float* w, const float* dy
         return DgradFilterGen{w,   d.C, d.K, d.R, d.S, d.pad, d_lo, dec, FastDiv(uint32_t(T)),
                               FastDiv(uint32_t(d.S * d.S)), FastDiv(uint32_t(d.S))};
     };
-    return run_window_gemm(dy, d.N, d.K, d.P, d.Q, Hs, Ws, 1, d_lo, T, o, static_cast<float*>(ws), make_gen, st);
+    return run_window_gemm(dy, d.N, d.K, d.P, d.Q, Hs, Ws, 1, d_lo, T, o, ws, make_gen, st);
 }
 
 }  // namespace cb200

@@ -46,6 +46,7 @@ struct Tile {
     int m0, n0;     // first row of A / of B (output row / column)
     int ks0, ks1;   // K stages [ks0, ks1)
     int grp;        // problem-defined: sub-problem (stride phase) or split index
+    int part = -1;  // >= 0: this unit is one K piece of a split tile (its partial-sum slot)
 };
 
 // Tile configuration.  With ATMEM the A operand does not use shared memory:

@@ -86,6 +86,10 @@ CONV_SHAPES = [
     (2, 16, 9, 9, 40, 3, 2, 1),        # 16 channels (one 16-wide tap group), 40 filters
     (1, 48, 7, 7, 24, 3, 1, 1),        # 48 channels (per-element order), 24 filters
     (1, 96, 8, 8, 17, 2, 2, 0),        # three 32-channel chunks, 17 filters
+    # 16 x 35 x 35 = 19600 rows: 154 row tiles, more than one wave on any GB300, so the trailing tiles of the
+    # 192-column GEMMs are split along K and their partial tiles added by the reduce kernel
+    (16, 64, 35, 35, 192, 3, 1, 1),    # forward: 192 filters
+    (16, 192, 35, 35, 64, 3, 1, 1),    # input gradient: 192 columns
 ]
 
 
