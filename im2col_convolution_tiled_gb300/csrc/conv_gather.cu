@@ -591,7 +591,7 @@ static int patch_capacity(int bn)
     }
 }
 
-template <int BN>
+template <int BN, bool TMA>
 static cudaError_t run_patch(const PatchGeom& pg, const OutGeom& o, float* img, cudaStream_t st)
 {
     ConvPatchProb<BN> p;
@@ -600,18 +600,137 @@ static cudaError_t run_patch(const PatchGeom& pg, const OutGeom& o, float* img, 
     p.bimg = img;
     p.n_tiles = (o.ncols + BN - 1) / BN;
     p.k_stages = pg.nch * pg.spc;
-    return launch_tc_patch<ConvPatchProb<BN>, BN>(p, pg.Nb * pg.tpi * p.n_tiles, device_error_word(), st);
+    return launch_tc_patch<ConvPatchProb<BN>, BN, TMA>(p, pg.Nb * pg.tpi * p.n_tiles, device_error_word(), st);
+}
+
+template <bool TMA>
+static cudaError_t dispatch_patch(int bn, const PatchGeom& pg, const OutGeom& o, float* img, cudaStream_t st)
+{
+    switch (bn) {
+    case 32: return run_patch<32, TMA>(pg, o, img, st);
+    case 64: return run_patch<64, TMA>(pg, o, img, st);
+    default: return run_patch<128, TMA>(pg, o, img, st);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Tensor-map form of the patch kernel (32-channel chunks).
+
+// Box of one (tile, chunk): rows spanned by any tile's window, full window width.
+static void patch_box(PatchGeom& pg)
+{
+    int span = 0;
+    for (int ti = 0; ti < pg.tpi; ++ti) {
+        const int first = ti * kBM;
+        const int last = (first + kBM < pg.GpGq ? first + kBM : pg.GpGq) - 1;
+        const int d = last / pg.Gq - first / pg.Gq;
+        if (d > span) span = d;
+    }
+    pg.rowsT = span * pg.sp + pg.T;
+    pg.Wt = (pg.Gq - 1) * pg.sp + pg.T;
+    pg.Cb = (pg.Ci + 31) / 32;
+    pg.tbox = uint32_t(pg.rowsT) * uint32_t(pg.Wt) * 128u;
+    pg.tbytes = (pg.tbox + 1023u) & ~1023u;
+}
+
+static bool patch_tma_fits(const PatchGeom& pg, int bn)
+{
+    if (pg.mode != 0 || pg.rowsT > 256 || pg.Wt > 256) return false;
+    const size_t cap = PatchCfg<32>::kMaxSmem;
+    switch (bn) {
+    case 32: return patch_tma_smem<32>(pg.tbytes) <= cap;
+    case 64: return patch_tma_smem<64>(pg.tbytes) <= cap;
+    case 128: return patch_tma_smem<128>(pg.tbytes) <= cap;
+    default: return false;
+    }
+}
+
+static size_t blocked_bytes(const PatchGeom& pg)
+{
+    return size_t(pg.Nb) * pg.Cb * pg.Hi * pg.Wi * 32 * sizeof(float);
+}
+
+// dst[n][c / 32][h][w][c % 32] = src[n][c][h][w], zero for c >= C.  One block
+// per (n, c / 32, h): 32 x 32 (channel x column) tiles through shared memory,
+// coalesced 128-byte reads along w and writes along the pixel.
+__global__ void __launch_bounds__(256) to_blocked32_kernel(const float* __restrict__ src, float* __restrict__ dst,
+                                                           int C, int Cb, int H, int W)
+{
+    __shared__ float tile[32][33];
+    const int h = blockIdx.x % H;
+    const int ncb = blockIdx.x / H;   // n * Cb + cb
+    const int n = ncb / Cb, cb = ncb % Cb;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    float* drow = dst + (size_t(ncb) * H + h) * size_t(W) * 32;
+    for (int w0 = 0; w0 < W; w0 += 32) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int c = ty + 8 * i, ch = cb * 32 + c, w = w0 + tx;
+            tile[c][tx] = (ch < C && w < W) ? __ldg(src + ((size_t(n) * C + ch) * H + h) * W + w) : 0.f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int pw = ty + 8 * i, w = w0 + pw;
+            if (w < W) drow[size_t(w) * 32 + tx] = tile[tx][pw];
+        }
+        __syncthreads();
+    }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled()
+{
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            cudaGetLastError();
+    }
+    return fn;
+}
+
+// Lays the gathered tensor out channel-blocked in `blocked` and describes it
+// with the box the kernel loads.  Fails (and the caller reports a CUDA error)
+// if the driver cannot encode the tensor map.
+static cudaError_t setup_patch_tma(PatchGeom& pg, float* blocked, cudaStream_t st)
+{
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return cudaErrorNotSupported;
+    to_blocked32_kernel<<<unsigned(pg.Nb * pg.Cb * pg.Hi), 256, 0, st>>>(pg.in, blocked, pg.Ci, pg.Cb, pg.Hi, pg.Wi);
+    note_launch();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const cuuint64_t dims[4] = {32, cuuint64_t(pg.Wi), cuuint64_t(pg.Hi), cuuint64_t(pg.Nb) * pg.Cb};
+    const cuuint64_t strides[3] = {128, cuuint64_t(pg.Wi) * 128, cuuint64_t(pg.Hi) * pg.Wi * 128};
+    const cuuint32_t box[4] = {32, cuuint32_t(pg.Wt), cuuint32_t(pg.rowsT), 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = enc(&pg.tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, blocked, dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 // Which kernel a convolution-window GEMM runs on, and the workspace it needs:
 // the patch-staged kernel when the output tile is at most 128 wide and every
 // tile's patch fits its shared-memory buffer, otherwise the register-gather
-// kernel (which may add a tail split's partial tiles).  Workspace layout:
-// [B image, 256-byte aligned][partial tiles].
+// kernel (which may add a tail split's partial tiles).  A patch GEMM over
+// 32-channel chunks whose box fits takes the tensor-map form.  Workspace
+// layout: [B image, 256-byte aligned][partial tiles | channel-blocked copy].
 struct WindowPlan {
     int bn;
-    bool patch;
-    size_t img_bytes, part_bytes;
+    bool patch, tma;
+    size_t img_bytes, part_bytes, blocked_bytes;
 };
 
 static WindowPlan plan_window(int Nb, int Ci, int Hi, int Wi, int Gp, int Gq, int sp, int o, int T, int ncols)
@@ -619,10 +738,14 @@ static WindowPlan plan_window(int Nb, int Ci, int Hi, int Wi, int Gp, int Gq, in
     WindowPlan w{};
     int n_tiles;
     w.bn = pick_conv_bn(ncols, &n_tiles);
-    w.patch = false;
+    w.patch = w.tma = false;
+    w.blocked_bytes = 0;
     if (w.bn <= 128) {
-        const PatchGeom pg = make_patch(nullptr, Nb, Ci, Hi, Wi, Gp, Gq, sp, o, T);
-        w.patch = max_patch_floats(pg) <= patch_capacity(w.bn);
+        PatchGeom pg = make_patch(nullptr, Nb, Ci, Hi, Wi, Gp, Gq, sp, o, T);
+        patch_box(pg);
+        w.tma = patch_tma_fits(pg, w.bn);
+        w.patch = w.tma || max_patch_floats(pg) <= patch_capacity(w.bn);
+        if (w.tma) w.blocked_bytes = blocked_bytes(pg);
     }
     w.img_bytes = round_up_256(bimage_floats(ncols, k_extent(Ci, T), w.bn) * sizeof(float));
     w.part_bytes = 0;
@@ -645,16 +768,18 @@ static cudaError_t run_window_gemm(const float* in, int Nb, int Ci, int Hi, int 
     float* img = static_cast<float*>(ws);
     const int bn = wp.bn;
     if (wp.patch) {
-        const PatchGeom pg = make_patch(in, Nb, Ci, Hi, Wi, Gp, Gq, sp, o, T);
+        PatchGeom pg = make_patch(in, Nb, Ci, Hi, Wi, Gp, Gq, sp, o, T);
         const KDecode dec = make_kdecode(pg.mode == 0 ? 1 : 0, pg.Cp, T);
         const int k_total = pg.mode == 0 ? pg.nch * T * T * kBK : T * T * pg.Cp;   // padded taps excluded
         cudaError_t e = build_bimage(make_gen(dec), og.ncols, k_total, bn, img, st);
         if (e != cudaSuccess) return e;
-        switch (bn) {
-        case 32: return run_patch<32>(pg, og, img, st);
-        case 64: return run_patch<64>(pg, og, img, st);
-        default: return run_patch<128>(pg, og, img, st);
+        if (wp.tma) {
+            patch_box(pg);
+            e = setup_patch_tma(pg, reinterpret_cast<float*>(static_cast<char*>(ws) + wp.img_bytes), st);
+            if (e != cudaSuccess) return e;
+            return dispatch_patch<true>(bn, pg, og, img, st);
         }
+        return dispatch_patch<false>(bn, pg, og, img, st);
     }
     const GatherGeom g = make_gather(in, Nb, Ci, Hi, Wi, Gp, Gq, sp, o, T);
     const KDecode dec = make_kdecode(g.mode == 2 ? 2 : 0, g.Cp, T);
@@ -667,7 +792,7 @@ static cudaError_t run_window_gemm(const float* in, int Nb, int Ci, int Hi, int 
 size_t conv_fwd_ws(const ConvDims& d)
 {
     const WindowPlan wp = plan_window(d.N, d.C, d.H, d.W, d.P, d.Q, d.S, -d.pad, d.R, d.K);
-    return wp.img_bytes + wp.part_bytes;
+    return wp.img_bytes + wp.part_bytes + wp.blocked_bytes;
 }
 
 size_t conv_dgrad_ws(const ConvDims& d)
@@ -676,7 +801,7 @@ size_t conv_dgrad_ws(const ConvDims& d)
     dgrad_window(d, &d_lo, &T);
     const int Hs = (d.H + d.S - 1) / d.S, Ws = (d.W + d.S - 1) / d.S;
     const WindowPlan wp = plan_window(d.N, d.K, d.P, d.Q, Hs, Ws, 1, d_lo, T, dgrad_cols(d));
-    return wp.img_bytes + wp.part_bytes;
+    return wp.img_bytes + wp.part_bytes + wp.blocked_bytes;
 }
 
 cudaError_t launch_conv_fwd(const ConvDims& d, const float* x, const float* w, const float* b, float* y, void* ws,

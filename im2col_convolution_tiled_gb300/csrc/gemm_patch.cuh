@@ -41,6 +41,8 @@
 // converter warp waits on every chunk's "patch loaded" barrier and signals its
 // "patch read" barrier.  All waits are bounded (ptx.cuh).
 #pragma once
+#include <cuda.h>   // CUtensorMap (the type only; encoding is done on the host through the runtime's driver entry point)
+
 #include "gemm_tc.cuh"
 
 namespace cb200 {
@@ -58,6 +60,15 @@ struct PatchGeom {
     int spc;           // stages per chunk
     int pc;            // channels one patch holds (mode 0: 32, mode 1: Ci)
     FastDiv f_gq, f_t;
+    // Tensor-map form (mode 0 only): the gathered tensor re-laid as
+    // [Nb][Ci/32][Hi][Wi][32] (channels innermost, zero-padded to 32) and one
+    // 4-D TMA box per (tile, chunk): rows [p_lo*sp + o, + rowsT), columns
+    // [o, o + Wt), 32 channels -- pixel-major, 128 bytes per pixel, 128-byte
+    // swizzled, and zero wherever the window leaves the image.
+    int Wt, rowsT, Cb;
+    uint32_t tbytes;   // shared-memory bytes of one box buffer (multiple of 1024)
+    uint32_t tbox;     // bytes one box delivers
+    alignas(64) CUtensorMap tmap;
 };
 
 // Floats between consecutive channels of a staged patch holding `run`
@@ -133,6 +144,15 @@ struct PatchCfg {
     static constexpr uint32_t kIdesc = idesc_tf32(kBM, BN);
 };
 
+// Dynamic shared memory of the tensor-map form: alignment slack, B stages, two
+// box buffers of `tbytes` each, control block.
+template <int BN>
+constexpr size_t patch_tma_smem(uint32_t tbytes)
+{
+    return 1024 + size_t(PatchCfg<BN>::kStages) * PatchCfg<BN>::kStage + 2 * size_t(tbytes) +
+           PatchCfg<BN>::kCtlBytes;
+}
+
 struct PatchCtl {
     uint64_t full[8];
     uint64_t empty[8];
@@ -148,7 +168,13 @@ struct PatchCtl {
 // The problem supplies the B image location and the epilogue (same interface
 // as ConvGatherProb: b_image, EState, e_setup, store).  Tile decode is fixed:
 // t -> (n_tile = t % n_tiles, image, tile in image).
-template <class Prob, int BN>
+//
+// TMA selects how a chunk's patch arrives: per-channel bulk copies of the
+// NCHW tensor (channel-major patch, any channel count), or one 4-D tensor-map
+// box of the channel-blocked copy (pixel-major swizzled patch, mode 0): there
+// a converter thread reads its 32 channels with eight conflict-free 16-byte
+// loads and needs no bounds tests, since the box is zero outside the image.
+template <class Prob, int BN, bool TMA>
 __global__ void __launch_bounds__(PatchCfg<BN>::kThreads, 1) tc_patch_kernel(const __grid_constant__ Prob prob, int* err_word)
 {
     using Cfg = PatchCfg<BN>;
@@ -157,9 +183,10 @@ __global__ void __launch_bounds__(PatchCfg<BN>::kThreads, 1) tc_patch_kernel(con
     const PatchGeom& g = prob.pg;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const size_t pbytes = TMA ? size_t(g.tbytes) : Cfg::kPatchBytes;
     float* patch[2] = {reinterpret_cast<float*>(smem + size_t(S) * Cfg::kStage),
-                       reinterpret_cast<float*>(smem + size_t(S) * Cfg::kStage + Cfg::kPatchBytes)};
-    PatchCtl* ctl = reinterpret_cast<PatchCtl*>(smem + size_t(S) * Cfg::kStage + 2 * Cfg::kPatchBytes);
+                       reinterpret_cast<float*>(smem + size_t(S) * Cfg::kStage + pbytes)};
+    PatchCtl* ctl = reinterpret_cast<PatchCtl*>(smem + size_t(S) * Cfg::kStage + 2 * pbytes);
     volatile int* abort_flag = &ctl->abort_flag;
 
     const int warp = threadIdx.x >> 5;
@@ -199,7 +226,7 @@ __global__ void __launch_bounds__(PatchCfg<BN>::kThreads, 1) tc_patch_kernel(con
     // Patch geometry of tile t: image, tile in image, first/last output
     // position, and the clamped input-row range every tap of the tile touches.
     struct TileGeo {
-        int n, first, last, h_lo, rows;
+        int n, first, last, h_lo, rows, p_lo;
     };
     auto tile_geo = [&](int t) {
         TileGeo q;
@@ -207,7 +234,8 @@ __global__ void __launch_bounds__(PatchCfg<BN>::kThreads, 1) tc_patch_kernel(con
         q.n = mt / g.tpi;
         q.first = (mt % g.tpi) * kBM;
         q.last = (q.first + kBM < g.GpGq ? q.first + kBM : g.GpGq) - 1;
-        int h_lo = (q.first / g.Gq) * g.sp + g.o;
+        q.p_lo = q.first / g.Gq;
+        int h_lo = q.p_lo * g.sp + g.o;
         int h_hi = (q.last / g.Gq) * g.sp + g.o + g.T - 1;
         if (h_lo < 0) h_lo = 0;
         if (h_hi > g.Hi - 1) h_hi = g.Hi - 1;
@@ -230,14 +258,18 @@ __global__ void __launch_bounds__(PatchCfg<BN>::kThreads, 1) tc_patch_kernel(con
             const int pix = q.first + tid;
             const bool pvalid = pix <= q.last;
             uint32_t pp = 0, pq = 0;
-            if (pvalid) g.f_gq.divmod(uint32_t(pix), pp, pq);
+            // tensor-map form: a row past the tile's last position reads the
+            // last position's pixels (any in-box address will do: the
+            // epilogue drops the row)
+            if (pvalid || TMA) g.f_gq.divmod(uint32_t(pvalid ? pix : q.last), pp, pq);
             const int hp0 = int(pp) * g.sp + g.o;  // input row of tap 0
             const int wp0 = int(pq) * g.sp + g.o;  // input column of tap 0
+            const int tpix0 = (int(pp) - q.p_lo) * g.sp * g.Wt + int(pq) * g.sp;   // box pixel of tap 0
             for (int cc = 0; cc < g.nch && ok; ++cc, ++u) {
                 const int pb = int(u & 1u);
                 // every channel run of this chunk starts s0 floats into its block
                 const long long x0 = (long long)q.n * g.CiHiWi + (long long)(cc * 32) * g.HiWi + (long long)q.h_lo * g.Wi;
-                const float* pbuf = patch[pb] + int(x0 & 3);
+                const float* pbuf = patch[pb] + (TMA ? 0 : int(x0 & 3));
                 if (!mbar_wait_warp(&ctl->pfull[pb], (u >> 1) & 1u, abort_flag)) { ok = false; break; }
                 const uint32_t c_first = u * uint32_t(g.spc);
                 const int j0 = int((uint32_t(grp) + 2u - (c_first & 1u)) & 1u);   // first stage of this group
@@ -247,7 +279,20 @@ __global__ void __launch_bounds__(PatchCfg<BN>::kThreads, 1) tc_patch_kernel(con
                     const uint32_t phase = (c / uint32_t(S)) & 1u;
                     const int ks = cc * g.spc + j;
                     float va[32];
-                    if (g.mode == 0) {
+                    if constexpr (TMA) {
+                        uint32_t tr, tq;
+                        g.f_t.divmod(uint32_t(j), tr, tq);
+                        const int P = tpix0 + int(tr) * g.Wt + int(tq);
+                        const uint8_t* rowp = reinterpret_cast<const uint8_t*>(pbuf) + size_t(P) * 128;
+#pragma unroll
+                        for (int c4 = 0; c4 < 8; ++c4) {
+                            const float4 v = *reinterpret_cast<const float4*>(rowp + ((c4 ^ (P & 7)) << 4));
+                            va[4 * c4] = v.x;
+                            va[4 * c4 + 1] = v.y;
+                            va[4 * c4 + 2] = v.z;
+                            va[4 * c4 + 3] = v.w;
+                        }
+                    } else if (g.mode == 0) {
                         uint32_t tr, tq;
                         g.f_t.divmod(uint32_t(j), tr, tq);
                         const int h = hp0 + int(tr), w = wp0 + int(tq);
@@ -316,6 +361,16 @@ __global__ void __launch_bounds__(PatchCfg<BN>::kThreads, 1) tc_patch_kernel(con
                     ok = false;
                     break;
                 }
+                if constexpr (TMA) {
+                    // one box: 32 channels x Wt columns x rowsT rows of image n
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&ctl->pfull[pb], g.tbox);
+                        tma_load_4d(patch[pb], &prob.pg.tmap, 0, g.o, q.p_lo * g.sp + g.o, q.n * g.Cb + cc,
+                                    &ctl->pfull[pb]);
+                    }
+                    __syncwarp();
+                    continue;
+                }
                 // lane c copies channel cc*32 + c: its run of rows*Wi floats, widened
                 // to 16-byte boundaries, with one bulk copy into block c of the buffer;
                 // a tail that would reach past the tensor's last 16-byte boundary
@@ -346,7 +401,6 @@ __global__ void __launch_bounds__(PatchCfg<BN>::kThreads, 1) tc_patch_kernel(con
                 if (lane == 0) mbar_arrive_expect_tx(&ctl->pfull[pb], total_bytes);
                 __syncwarp();
                 if (bytes) bulk_g2s(patch[pb] + dst_f, g.in + a0, bytes, &ctl->pfull[pb]);
-
             }
         }
         if (!ok) fail();
@@ -447,20 +501,21 @@ __global__ void __launch_bounds__(PatchCfg<BN>::kThreads, 1) tc_patch_kernel(con
     }
 }
 
-template <class Prob, int BN>
+template <class Prob, int BN, bool TMA>
 cudaError_t launch_tc_patch(const Prob& prob, int num_tiles, int* err_word, cudaStream_t stream)
 {
     using Cfg = PatchCfg<BN>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(tc_patch_kernel<Prob, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             int(Cfg::kSmemBytes));
+        cudaError_t e = cudaFuncSetAttribute(tc_patch_kernel<Prob, BN, TMA>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cfg::kMaxSmem));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     if (num_tiles <= 0) return cudaSuccess;
+    const size_t smem = TMA ? patch_tma_smem<BN>(prob.pg.tbytes) : Cfg::kSmemBytes;
     int grid = num_tiles < sm_count() ? num_tiles : sm_count();
-    tc_patch_kernel<Prob, BN><<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(prob, err_word);
+    tc_patch_kernel<Prob, BN, TMA><<<grid, Cfg::kThreads, smem, stream>>>(prob, err_word);
     note_launch();
     return cudaGetLastError();
 }

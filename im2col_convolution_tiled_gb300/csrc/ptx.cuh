@@ -129,6 +129,22 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, u
         : "memory");
 }
 
+// Tiled 4-D tensor load (TMA) of one box into shared memory, completing on an
+// mbarrier with the box's byte count.  Coordinates are element indices,
+// innermost first; boxes may start outside the tensor (the outside reads as
+// zero) as long as the innermost coordinate times the element size is a
+// multiple of 16 bytes.  `tmap` is the generic address of a CUtensorMap held
+// in kernel-parameter (grid-constant) or global memory.
+__device__ __forceinline__ void tma_load_4d(void* smem_dst, const void* tmap, int c0, int c1, int c2, int c3,
+                                            uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+        "[%6];" ::"r"(smem_u32(smem_dst)),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // fences
 
