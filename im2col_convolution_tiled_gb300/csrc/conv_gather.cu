@@ -651,28 +651,44 @@ static size_t blocked_bytes(const PatchGeom& pg)
 }
 
 // dst[n][c / 32][h][w][c % 32] = src[n][c][h][w], zero for c >= C.  One block
-// per (n, c / 32, h): 32 x 32 (channel x column) tiles through shared memory,
-// coalesced 128-byte reads along w and writes along the pixel.
-__global__ void __launch_bounds__(256) to_blocked32_kernel(const float* __restrict__ src, float* __restrict__ dst,
-                                                           int C, int Cb, int H, int W)
+// per (n, c / 32, group of kBlkRows rows): 32 x 32 (channel x column) tiles of
+// every row of the group go through shared memory together, so each thread
+// keeps 4 * kBlkRows loads in flight; reads are 128-byte rows along w, writes
+// are whole 128-byte pixels (16-byte stores).
+constexpr int kBlkRows = 4;
+
+__global__ void __launch_bounds__(256, 4) to_blocked32_kernel(const float* __restrict__ src, float* __restrict__ dst,
+                                                           int C, int Cb, int H, int W, int hgroups)
 {
-    __shared__ float tile[32][33];
-    const int h = blockIdx.x % H;
-    const int ncb = blockIdx.x / H;   // n * Cb + cb
+    __shared__ float tile[kBlkRows][32][33];
+    const int hg = blockIdx.x % hgroups;
+    const int ncb = blockIdx.x / hgroups;   // n * Cb + cb
     const int n = ncb / Cb, cb = ncb % Cb;
+    const int h0 = hg * kBlkRows;
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    float* drow = dst + (size_t(ncb) * H + h) * size_t(W) * 32;
     for (int w0 = 0; w0 < W; w0 += 32) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int c = ty + 8 * i, ch = cb * 32 + c, w = w0 + tx;
-            tile[c][tx] = (ch < C && w < W) ? __ldg(src + ((size_t(n) * C + ch) * H + h) * W + w) : 0.f;
+        for (int rr = 0; rr < kBlkRows; ++rr) {
+            const int h = h0 + rr;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int c = ty + 8 * i, ch = cb * 32 + c, w = w0 + tx;
+                tile[rr][c][tx] =
+                    (h < H && ch < C && w < W) ? __ldg(src + ((size_t(n) * C + ch) * H + h) * W + w) : 0.f;
+            }
         }
         __syncthreads();
+        // 8 lanes write one pixel's 32 channels as 16-byte chunks: the block
+        // covers the tile's 32 pixels in one pass per row
+        const int chunk = threadIdx.x & 7, pw = threadIdx.x >> 3, w = w0 + pw;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int pw = ty + 8 * i, w = w0 + pw;
-            if (w < W) drow[size_t(w) * 32 + tx] = tile[tx][pw];
+        for (int rr = 0; rr < kBlkRows; ++rr) {
+            const int h = h0 + rr;
+            if (h < H && w < W) {
+                float* dpix = dst + ((size_t(ncb) * H + h) * size_t(W) + w) * 32 + 4 * chunk;
+                *reinterpret_cast<float4*>(dpix) = make_float4(tile[rr][4 * chunk][pw], tile[rr][4 * chunk + 1][pw],
+                                                               tile[rr][4 * chunk + 2][pw], tile[rr][4 * chunk + 3][pw]);
+            }
         }
         __syncthreads();
     }
@@ -703,14 +719,10 @@ static EncodeTiledFn encode_tiled()
 // Lays the gathered tensor out channel-blocked in `blocked` and describes it
 // with the box the kernel loads.  Fails (and the caller reports a CUDA error)
 // if the driver cannot encode the tensor map.
-static cudaError_t setup_patch_tma(PatchGeom& pg, float* blocked, cudaStream_t st)
+static cudaError_t encode_patch_tmap(PatchGeom& pg, float* blocked)
 {
     EncodeTiledFn enc = encode_tiled();
     if (!enc) return cudaErrorNotSupported;
-    to_blocked32_kernel<<<unsigned(pg.Nb * pg.Cb * pg.Hi), 256, 0, st>>>(pg.in, blocked, pg.Ci, pg.Cb, pg.Hi, pg.Wi);
-    note_launch();
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
     const cuuint64_t dims[4] = {32, cuuint64_t(pg.Wi), cuuint64_t(pg.Hi), cuuint64_t(pg.Nb) * pg.Cb};
     const cuuint64_t strides[3] = {128, cuuint64_t(pg.Wi) * 128, cuuint64_t(pg.Hi) * pg.Wi * 128};
     const cuuint32_t box[4] = {32, cuuint32_t(pg.Wt), cuuint32_t(pg.rowsT), 1};
@@ -719,6 +731,121 @@ static cudaError_t setup_patch_tma(PatchGeom& pg, float* blocked, cudaStream_t s
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+static cudaError_t setup_patch_tma(PatchGeom& pg, float* blocked, cudaStream_t st)
+{
+    const int hgroups = (pg.Hi + kBlkRows - 1) / kBlkRows;
+    to_blocked32_kernel<<<unsigned(pg.Nb * pg.Cb * hgroups), 256, 0, st>>>(pg.in, blocked, pg.Ci, pg.Cb, pg.Hi, pg.Wi,
+                                                                         hgroups);
+    note_launch();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return encode_patch_tmap(pg, blocked);
+}
+
+// ---------------------------------------------------------------------------
+// Forward convolution with stride S > 1 and few channels, as a stride-1
+// convolution over S x S super-pixels (space to depth):
+//   y[n, k, p, q] = sum_(c', tr, tq) X'[n, c', p + tr, q + tq] * W'[k, c', tr, tq]
+// with c' = (c, a, b) = c*S*S + a*S + b, X'[n, c', hh, ww] = x[n, c, S*hh + a - pad, S*ww + b - pad]
+// (zero outside the image) and W'[k, c', tr, tq] = W[k, c, S*tr + a, S*tq + b] (zero past the filter):
+// tap r = S*tr + a of output row p reads padded input row S*p + r = S*(p + tr) + a.  The window is
+// T = ceil(R / S) super-pixels wide, and C*S*S channels fill 32-channel chunks: the form the
+// tensor-map patch kernel runs best (AlexNet conv1: 3 channels, 11 x 11, stride 4 -> 48 channels, 3 x 3).
+
+// Row pitch (floats) of the staged input rows of the space-to-depth copy: 4 mod 32.
+__host__ __device__ inline int s2d_pitch(int W) { return W + ((4 - W) % 32 + 32) % 32; }
+
+constexpr int kS2dMaxRowBytes = 64 * 1024;   // shared memory of the staged input rows of one super-row
+
+struct S2dPlan {
+    bool use;
+    int bn, T, Ci;
+    PatchGeom pg;
+};
+
+static S2dPlan plan_fwd_s2d(const ConvDims& d)
+{
+    S2dPlan sp{};
+    sp.use = false;
+    if (d.S < 2 || d.C > 16) return sp;
+    sp.T = (d.R + d.S - 1) / d.S;
+    sp.Ci = d.C * d.S * d.S;
+    if (sp.Ci < 17 || sp.Ci > 128) return sp;
+    int n_tiles;
+    sp.bn = pick_conv_bn(d.K, &n_tiles);
+    if (sp.bn > 128) return sp;
+    if (size_t(d.C) * d.S * s2d_pitch(d.W) * sizeof(float) > size_t(kS2dMaxRowBytes)) return sp;   // staged rows
+    sp.pg = make_patch(nullptr, d.N, sp.Ci, d.P + sp.T - 1, d.Q + sp.T - 1, d.P, d.Q, 1, 0, sp.T);
+    if (sp.pg.mode != 0) return sp;
+    patch_box(sp.pg);
+    sp.use = patch_tma_fits(sp.pg, sp.bn);
+    return sp;
+}
+
+struct FwdS2dFilterGen {   // B[k, kk] = W'[k, c', tr, tq] in the chunk-major K order
+    const float* w;
+    int C, R, S;
+    KDecode dec;
+    FastDiv f_t, f_ss, f_s;
+    __device__ float operator()(int k, int kk) const
+    {
+        int cp, tap;
+        dec(kk, cp, tap);
+        uint32_t c, ab, a, b, tr, tq;
+        f_ss.divmod(uint32_t(cp), c, ab);
+        f_s.divmod(ab, a, b);
+        f_t.divmod(uint32_t(tap), tr, tq);
+        if (int(c) >= C || int(tr) >= int(f_t.d)) return 0.f;
+        const int r = S * int(tr) + int(a), q = S * int(tq) + int(b);
+        if (r >= R || q >= R) return 0.f;
+        return __ldg(w + ((size_t(k) * C + c) * R + r) * R + q);
+    }
+};
+
+// dst[n][c' / 32][hh][ww][c' % 32] = X'[n, c', hh, ww].  One block per
+// (n, hh): the C*S input rows h = S*hh + a - pad (all channels c, phases a)
+// are staged in shared memory with coalesced reads, then the block writes the
+// super-row's pixels of every 32-channel block, 32 consecutive floats (one
+// pixel) per warp store.  A thread keeps one channel c' per block cb, so its
+// (c, a, b) decode is done once per cb.  Rows are loaded eight at a time into
+// registers (eight loads in flight per thread) and stored at a pitch of 4 mod
+// 32 floats, so the lanes of a warp (consecutive b, then a, then c) read
+// distinct banks.
+__global__ void __launch_bounds__(256) to_blocked_s2d_kernel(const float* __restrict__ x, float* __restrict__ dst,
+                                                             int C, int H, int W, int S, int pad, int Cb, int Hs,
+                                                             int Ws)
+{
+    extern __shared__ float rows[];   // [c * S + a][pitch]
+    const int hh = blockIdx.x % Hs, n = blockIdx.x / Hs;
+    const int CS = C * S, pitch = s2d_pitch(W);
+    for (int w = threadIdx.x; w < W; w += blockDim.x) {
+        for (int ca0 = 0; ca0 < CS; ca0 += 8) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int ca = ca0 + u, c = ca / S, h = S * hh + ca % S - pad;
+                v[u] = (ca < CS && unsigned(h) < unsigned(H)) ? __ldg(x + ((size_t(n) * C + c) * H + h) * W + w) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (ca0 + u < CS) rows[(ca0 + u) * pitch + w] = v[u];
+        }
+    }
+    __syncthreads();
+    const int j = threadIdx.x & 31;
+    for (int cb = 0; cb < Cb; ++cb) {
+        const int cp = cb * 32 + j;
+        const int c = cp / (S * S), a = (cp / S) % S, b = cp % S;
+        const bool live = c < C;
+        const float* row = rows + (live ? (c * S + a) * s2d_pitch(W) : 0);
+        float* out = dst + ((size_t(n) * Cb + cb) * Hs + hh) * size_t(Ws) * 32;
+        for (int t = threadIdx.x; t < Ws * 32; t += blockDim.x) {
+            const int w = S * (t >> 5) + b - pad;
+            out[t] = (live && unsigned(w) < unsigned(W)) ? row[w] : 0.f;
+        }
+    }
 }
 
 // Which kernel a convolution-window GEMM runs on, and the workspace it needs:
@@ -791,6 +918,10 @@ static cudaError_t run_window_gemm(const float* in, int Nb, int Ci, int Hi, int 
 
 size_t conv_fwd_ws(const ConvDims& d)
 {
+    const S2dPlan sp = plan_fwd_s2d(d);
+    if (sp.use)
+        return round_up_256(bimage_floats(d.K, sp.pg.nch * sp.T * sp.T * kBK, sp.bn) * sizeof(float)) +
+               blocked_bytes(sp.pg);
     const WindowPlan wp = plan_window(d.N, d.C, d.H, d.W, d.P, d.Q, d.S, -d.pad, d.R, d.K);
     return wp.img_bytes + wp.part_bytes + wp.blocked_bytes;
 }
@@ -816,6 +947,32 @@ cudaError_t launch_conv_fwd(const ConvDims& d, const float* x, const float* w, c
     o.HoWo = d.P * d.Q;
     o.so = 1;
     o.ncols = d.K;
+    S2dPlan sp = plan_fwd_s2d(d);
+    if (sp.use) {
+        PatchGeom& pg = sp.pg;
+        const int k_total = pg.nch * sp.T * sp.T * kBK;
+        const FwdS2dFilterGen gen{w,   d.C, d.R, d.S, make_kdecode(1, pg.Cp, sp.T), FastDiv(uint32_t(sp.T)),
+                                  FastDiv(uint32_t(d.S * d.S)), FastDiv(uint32_t(d.S))};
+        float* img = static_cast<float*>(ws);
+        cudaError_t e = build_bimage(gen, d.K, k_total, sp.bn, img, st);
+        if (e != cudaSuccess) return e;
+        float* blocked = reinterpret_cast<float*>(static_cast<char*>(ws) +
+                                                  round_up_256(bimage_floats(d.K, k_total, sp.bn) * sizeof(float)));
+        static bool attr_set = false;
+        if (!attr_set) {
+            e = cudaFuncSetAttribute(to_blocked_s2d_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kS2dMaxRowBytes);
+            if (e != cudaSuccess) return e;
+            attr_set = true;
+        }
+        const size_t smem = size_t(d.C) * d.S * s2d_pitch(d.W) * sizeof(float);
+        to_blocked_s2d_kernel<<<unsigned(pg.Nb * pg.Hi), 256, smem, st>>>(x, blocked, d.C, d.H, d.W, d.S, d.pad,
+                                                                         pg.Cb, pg.Hi, pg.Wi);
+        note_launch();
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = encode_patch_tmap(pg, blocked)) != cudaSuccess) return e;
+        return dispatch_patch<true>(sp.bn, pg, o, img, st);
+    }
     auto make_gen = [&](const KDecode& dec) { return FwdFilterGen{w, d.C, d.R, dec, FastDiv(uint32_t(d.R))}; };
     return run_window_gemm(x, d.N, d.C, d.H, d.W, d.P, d.Q, d.S, -d.pad, d.R, o, ws, make_gen, st);
 }

@@ -18,10 +18,19 @@
 //                     every value into hi/lo and stores both into the stage's
 //                     tiles (128-byte swizzled, K-major)
 //   warp 4G           allocates tensor memory; lane 0 issues the MMAs
-//   warps 4G+1..4G+4  epilogue: tcgen05.ld the accumulator, hand rows to the
+//   warp 4G+1         (tiles at most 64 wide, A in shared memory) lane 0 is a
+//                     second MMA issuer: one thread cannot issue tcgen05.mma
+//                     fast enough to keep the tensor core busy on such narrow
+//                     tiles (about one MMA per 25 ns whatever N is, plus the
+//                     stage handshakes).  Stage c of the CTA-wide stage count
+//                     is then consumed by issuer c % 2 into its own
+//                     accumulator (S even, so slot c % S has the parity of its
+//                     producer group and of its issuer) and the epilogue adds
+//                     the two accumulators in a fixed order.
+//   last 4 warps      epilogue: tcgen05.ld the accumulator, hand rows to the
 //                     problem's store (bias, NCHW reshape, split-K partials ...)
-// Two accumulators (2 x BN TMEM columns) let the epilogue of tile i overlap
-// the main loop of tile i+1.
+// Two accumulators per issuer (2 x BN TMEM columns) let the epilogue of tile i
+// overlap the main loop of tile i+1.
 //
 // Every wait is bounded (ptx.cuh); on give-up the kernel raises its abort
 // flag, records kDevErrTimeout in the device error word, waits for what it
@@ -35,10 +44,11 @@ constexpr int kBM = 128;       // UMMA M: rows of a tile (TMEM lanes)
 constexpr int kBK = 32;        // K depth of one pipeline stage (one 128-byte swizzle row)
 constexpr size_t kSmemBudget = 200 * 1024;
 
-template <int G>
+template <int G, int NI>
 struct Roles {
-    static constexpr int kWarpMma = 4 * G;
-    static constexpr int kThreads = (4 * G + 5) * 32;
+    static constexpr int kWarpMma = 4 * G;               // first issuer warp
+    static constexpr int kWarpEpi = 4 * G + NI;          // first epilogue warp
+    static constexpr int kThreads = (4 * G + NI + 4) * 32;
 };
 
 
@@ -61,13 +71,17 @@ struct TileCfg {
     // accumulators: two (epilogue of tile i overlaps tile i+1) unless tensor
     // memory is needed for A stages
     static constexpr int kDBuf = (ATMEM && BN > 128) ? 1 : 2;
+    static constexpr int kIssuers = (!ATMEM && BN <= 64) ? 2 : 1;
     static constexpr int kSmemStages = int(kSmemBudget / kStage);
     static constexpr int kTmemStages = ATMEM ? (512 - kDBuf * BN) / 64 : 8;
     static constexpr int kStages0 = kSmemStages < kTmemStages ? kSmemStages : kTmemStages;
-    static constexpr int kStages = kStages0 > (ATMEM ? 8 : 6) ? (ATMEM ? 8 : 6) : kStages0;
+    static constexpr int kStages1 = kStages0 > (ATMEM ? 8 : 6) ? (ATMEM ? 8 : 6) : kStages0;
+    static constexpr int kStages = kIssuers == 2 ? (kStages1 & ~1) : kStages1;   // two issuers: S even
+    static_assert(kIssuers == 1 || kStages >= 2, "two issuers need an even number of stages");
     static constexpr uint32_t kACol = uint32_t(kDBuf * BN);   // first TMEM column of the A stages
+    static constexpr int kAccCols = kIssuers * kDBuf * BN;    // accumulators: [buffer][issuer]
     static constexpr uint32_t kTmemCols =
-        ATMEM ? 512 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
+        ATMEM ? 512 : (kAccCols <= 64) ? 64 : (kAccCols <= 128) ? 128 : (kAccCols <= 256) ? 256 : 512;
     static constexpr size_t kSmemBytes = size_t(kStages) * kStage + 1024 /*align*/ + 256 /*barriers*/;
     static constexpr uint32_t kIdesc = idesc_tf32(kBM, BN);
 };
@@ -126,13 +140,19 @@ struct SharedCtl {
     uint64_t empty[8];
     uint64_t accf[2];
     uint64_t acce[2];
-    uint64_t drain;
+    uint64_t drain[2];
     uint32_t tmem_base;
     int abort_flag;
 };
 
 template <class Prob, int BN>
-__global__ void __launch_bounds__(Roles<Groups<Prob, BN>::value>::kThreads, 1)
+struct EngineRoles {
+    using Cfg = TileCfg<BN, UsesTmemA<Prob>::value>;
+    using R = Roles<Groups<Prob, BN>::value, Cfg::kIssuers>;
+};
+
+template <class Prob, int BN>
+__global__ void __launch_bounds__(EngineRoles<Prob, BN>::R::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ Prob prob, int* err_word)
 {
     constexpr bool ATMEM = UsesTmemA<Prob>::value;
@@ -140,8 +160,11 @@ __global__ void __launch_bounds__(Roles<Groups<Prob, BN>::value>::kThreads, 1)
     constexpr int S = Cfg::kStages;
     constexpr int G = Groups<Prob, BN>::value;
     constexpr int DB = Cfg::kDBuf;
+    constexpr int NI = Cfg::kIssuers;
     static_assert(G >= 1 && G <= S, "producer groups must not outnumber pipeline stages");
-    constexpr int kWarpMma = Roles<G>::kWarpMma;
+    static_assert(NI == 1 || G == 2, "two issuers pair with two producer groups (stage parity)");
+    constexpr int kWarpMma = Roles<G, NI>::kWarpMma;
+    constexpr int kWarpEpi = Roles<G, NI>::kWarpEpi;
     constexpr int kBPasses = BN > 128 ? 2 : 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -164,10 +187,10 @@ __global__ void __launch_bounds__(Roles<Groups<Prob, BN>::value>::kThreads, 1)
             mbar_init(&ctl->empty[s], 1);
         }
         for (int b = 0; b < DB; ++b) {
-            mbar_init(&ctl->accf[b], 1);
+            mbar_init(&ctl->accf[b], NI);   // one commit per issuer
             mbar_init(&ctl->acce[b], 4);
         }
-        mbar_init(&ctl->drain, 1);
+        for (int i = 0; i < NI; ++i) mbar_init(&ctl->drain[i], 1);
         ctl->abort_flag = 0;
         mbar_fence_init();
     }
@@ -284,23 +307,28 @@ __global__ void __launch_bounds__(Roles<Groups<Prob, BN>::value>::kThreads, 1)
                 }
             }
         }
-    } else if (warp == kWarpMma) {
-        // ---------------- MMA issuer ----------------
+    } else if (warp < kWarpEpi) {
+        // ---------------- MMA issuer(s) ----------------
+        const uint32_t me = uint32_t(warp - kWarpMma);
         if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
+            uint32_t cnt = 0;   // CTA-wide stage counter (as the producers count)
             int local = 0;
             bool ok = true;
             bool issued_any = false;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
                 const Tile tile = prob.tile(t);
+                const int nks = tile.ks1 - tile.ks0;
                 const int acc = local % DB;
                 const uint32_t acc_phase = uint32_t(local / DB) & 1u;
                 if (!mbar_wait(&ctl->acce[acc], acc_phase ^ 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
+                const uint32_t d_tmem = tmem_base + uint32_t((acc * NI + int(me)) * BN);
                 uint32_t accumulate = 0;
-                for (int ks = tile.ks0; ks < tile.ks1; ++ks) {
+                const int i0 = NI == 1 ? 0 : int(me ^ (cnt & 1u));   // this issuer's first stage of the tile
+                for (int i = i0; i < nks; i += NI) {
+                    const uint32_t c = cnt + uint32_t(i);
+                    const int stage = int(c % uint32_t(S));
+                    const uint32_t phase = (c / uint32_t(S)) & 1u;
                     if (!mbar_wait(&ctl->full[stage], phase, abort_flag)) { ok = false; break; }
                     tc_fence_after();
 #pragma unroll
@@ -325,18 +353,19 @@ __global__ void __launch_bounds__(Roles<Groups<Prob, BN>::value>::kThreads, 1)
                     }
                     issued_any = true;
                     mma_commit(&ctl->empty[stage]);
-                    if (++stage == S) { stage = 0; phase ^= 1; }
                 }
                 if (!ok) break;
+                cnt += uint32_t(nks);
+                // arrives once this issuer's MMAs of the tile are done (at once if it had none)
                 mma_commit(&ctl->accf[acc]);
             }
             if (!ok) {
                 fail();
                 if (issued_any) {
                     // Let the MMAs in flight finish before the memory goes away.
-                    mma_commit(&ctl->drain);
+                    mma_commit(&ctl->drain[me]);
                     uint64_t t0 = globaltimer_ns();
-                    while (!mbar_try_wait(&ctl->drain, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
+                    while (!mbar_try_wait(&ctl->drain[me], 0) && globaltimer_ns() - t0 < kWaitLimitNs) {}
                 }
             }
         }
@@ -345,21 +374,41 @@ __global__ void __launch_bounds__(Roles<Groups<Prob, BN>::value>::kThreads, 1)
         // ---------------- epilogue ----------------
         const int q = warp & 3;               // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;        // accumulator row of this thread
+        uint32_t cnt = 0;                     // CTA-wide stage counter at the tile's start
         int local = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
             const Tile tile = prob.tile(t);
+            const int nks = tile.ks1 - tile.ks0;
             const int acc = local % DB;
             const uint32_t acc_phase = uint32_t(local / DB) & 1u;
             if (!mbar_wait_warp(&ctl->accf[acc], acc_phase, abort_flag)) { ok = false; break; }
             tc_fence_after();
             typename Prob::EState es = prob.e_setup(tile, row);
+            const uint32_t lane_base = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * NI * BN);
+            if constexpr (NI == 1) {
 #pragma unroll 1
-            for (int c = 0; c < BN; c += 32) {
-                uint32_t r[32];
-                tmem_ld32(tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * BN + c), r);
-                prob.store(es, tile, row, c, r);
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_base + uint32_t(c), r);
+                    prob.store(es, tile, row, c, r);
+                }
+            } else {
+                // an issuer with no stage in the tile left its accumulator untouched
+                const bool use0 = nks >= 2 || (nks == 1 && (cnt & 1u) == 0);
+                const bool use1 = nks >= 2 || (nks == 1 && (cnt & 1u) == 1);
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t r0[32], r1[32];
+                    tmem_ld32x2(lane_base + uint32_t(c), lane_base + uint32_t(BN + c), r0, r1);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        r0[i] = __float_as_uint((use0 ? __uint_as_float(r0[i]) : 0.f) +
+                                                (use1 ? __uint_as_float(r1[i]) : 0.f));
+                    prob.store(es, tile, row, c, r0);
+                }
             }
+            cnt += uint32_t(nks);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctl->acce[acc]);
@@ -380,6 +429,7 @@ template <class Prob, int BN>
 cudaError_t launch_tc_gemm(const Prob& prob, int num_tiles, int* err_word, cudaStream_t stream)
 {
     using Cfg = TileCfg<BN, UsesTmemA<Prob>::value>;
+    constexpr int kThreads = EngineRoles<Prob, BN>::R::kThreads;
     static bool attr_set = false;   // per process; the attribute is per function
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<Prob, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -389,8 +439,7 @@ cudaError_t launch_tc_gemm(const Prob& prob, int num_tiles, int* err_word, cudaS
     }
     if (num_tiles <= 0) return cudaSuccess;
     int grid = num_tiles < sm_count() ? num_tiles : sm_count();
-    tc_gemm_kernel<Prob, BN><<<grid, Roles<Groups<Prob, BN>::value>::kThreads, Cfg::kSmemBytes, stream>>>(prob,
-                                                                                                    err_word);
+    tc_gemm_kernel<Prob, BN><<<grid, kThreads, Cfg::kSmemBytes, stream>>>(prob, err_word);
     note_launch();
     return cudaGetLastError();
 }
