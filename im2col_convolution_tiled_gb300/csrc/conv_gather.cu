@@ -591,6 +591,8 @@ static int patch_capacity(int bn)
     }
 }
 
+constexpr int kShortTileStages = 48;   // K stages per tile at or below which 64-wide tiles double-buffer
+
 template <int BN, bool TMA>
 static cudaError_t run_patch(const PatchGeom& pg, const OutGeom& o, float* img, cudaStream_t st)
 {
@@ -600,7 +602,13 @@ static cudaError_t run_patch(const PatchGeom& pg, const OutGeom& o, float* img, 
     p.bimg = img;
     p.n_tiles = (o.ncols + BN - 1) / BN;
     p.k_stages = pg.nch * pg.spc;
-    return launch_tc_patch<ConvPatchProb<BN>, BN, TMA>(p, pg.Nb * pg.tpi * p.n_tiles, device_error_word(), st);
+    const int tiles = pg.Nb * pg.tpi * p.n_tiles;
+    // short tiles: double-buffer the accumulators (fewer A stages) so the
+    // epilogue overlaps the next tile's MMAs
+    if constexpr (BN == 64)
+        if (p.k_stages <= kShortTileStages)
+            return launch_tc_patch<ConvPatchProb<BN>, BN, TMA, true>(p, tiles, device_error_word(), st);
+    return launch_tc_patch<ConvPatchProb<BN>, BN, TMA, false>(p, tiles, device_error_word(), st);
 }
 
 template <bool TMA>

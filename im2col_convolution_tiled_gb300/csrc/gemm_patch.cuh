@@ -120,14 +120,19 @@ __device__ __forceinline__ void patch_taps(const PatchGeom& g, const float* pbuf
     }
 }
 
-template <int BN>
+// DB2 asks for two accumulator buffers per issuer even where that leaves only
+// four A stages (64-wide tiles): worth it when tiles have few K stages, so that
+// the epilogue of one tile would otherwise stall the next tile's MMAs.
+template <int BN, bool DB2 = false>
 struct PatchCfg {
     static_assert(BN <= 128, "the patch kernel keeps an accumulator per issuer and at least four A stages in "
                              "tensor memory");
+    static_assert(!DB2 || BN <= 64, "two buffers per issuer and four A stages need tiles at most 64 wide");
     static constexpr int kThreads = 480;
     // accumulator buffers per issuer: two (the epilogue of tile i overlaps the
-    // main loop of tile i+1) when six A stages still fit beside them, else one
-    static constexpr int kDBuf = (512 - 4 * BN) / 64 >= 6 ? 2 : 1;
+    // main loop of tile i+1) when six A stages still fit beside them (or DB2),
+    // else one
+    static constexpr int kDBuf = (DB2 || (512 - 4 * BN) / 64 >= 6) ? 2 : 1;
     static constexpr int kTmemStages0 = (512 - 2 * kDBuf * BN) / 64;
     static constexpr int kStages = (kTmemStages0 > 6 ? 6 : kTmemStages0) & ~1;   // even: slot parity = issuer
     static_assert(kStages >= 4, "too few A stages fit in tensor memory");
@@ -146,11 +151,11 @@ struct PatchCfg {
 
 // Dynamic shared memory of the tensor-map form: alignment slack, B stages, two
 // box buffers of `tbytes` each, control block.
-template <int BN>
+template <int BN, bool DB2 = false>
 constexpr size_t patch_tma_smem(uint32_t tbytes)
 {
-    return 1024 + size_t(PatchCfg<BN>::kStages) * PatchCfg<BN>::kStage + 2 * size_t(tbytes) +
-           PatchCfg<BN>::kCtlBytes;
+    using C = PatchCfg<BN, DB2>;
+    return 1024 + size_t(C::kStages) * C::kStage + 2 * size_t(tbytes) + C::kCtlBytes;
 }
 
 struct PatchCtl {
@@ -174,10 +179,10 @@ struct PatchCtl {
 // box of the channel-blocked copy (pixel-major swizzled patch, mode 0): there
 // a converter thread reads its 32 channels with eight conflict-free 16-byte
 // loads and needs no bounds tests, since the box is zero outside the image.
-template <class Prob, int BN, bool TMA>
-__global__ void __launch_bounds__(PatchCfg<BN>::kThreads, 1) tc_patch_kernel(const __grid_constant__ Prob prob, int* err_word)
+template <class Prob, int BN, bool TMA, bool DB2>
+__global__ void __launch_bounds__(PatchCfg<BN, DB2>::kThreads, 1) tc_patch_kernel(const __grid_constant__ Prob prob, int* err_word)
 {
-    using Cfg = PatchCfg<BN>;
+    using Cfg = PatchCfg<BN, DB2>;
     constexpr int S = Cfg::kStages;
     constexpr int DB = Cfg::kDBuf;
     const PatchGeom& g = prob.pg;
@@ -501,21 +506,21 @@ __global__ void __launch_bounds__(PatchCfg<BN>::kThreads, 1) tc_patch_kernel(con
     }
 }
 
-template <class Prob, int BN, bool TMA>
+template <class Prob, int BN, bool TMA, bool DB2>
 cudaError_t launch_tc_patch(const Prob& prob, int num_tiles, int* err_word, cudaStream_t stream)
 {
-    using Cfg = PatchCfg<BN>;
+    using Cfg = PatchCfg<BN, DB2>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(tc_patch_kernel<Prob, BN, TMA>,
+        cudaError_t e = cudaFuncSetAttribute(tc_patch_kernel<Prob, BN, TMA, DB2>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cfg::kMaxSmem));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     if (num_tiles <= 0) return cudaSuccess;
-    const size_t smem = TMA ? patch_tma_smem<BN>(prob.pg.tbytes) : Cfg::kSmemBytes;
+    const size_t smem = TMA ? patch_tma_smem<BN, DB2>(prob.pg.tbytes) : Cfg::kSmemBytes;
     int grid = num_tiles < sm_count() ? num_tiles : sm_count();
-    tc_patch_kernel<Prob, BN, TMA><<<grid, Cfg::kThreads, smem, stream>>>(prob, err_word);
+    tc_patch_kernel<Prob, BN, TMA, DB2><<<grid, Cfg::kThreads, smem, stream>>>(prob, err_word);
     note_launch();
     return cudaGetLastError();
 }

@@ -43,6 +43,7 @@ namespace cb200 {
 constexpr int kBM = 128;       // UMMA M: rows of a tile (TMEM lanes)
 constexpr int kBK = 32;        // K depth of one pipeline stage (one 128-byte swizzle row)
 constexpr size_t kSmemBudget = 200 * 1024;
+constexpr int kBPrefetch = 4;  // stages ahead at which a bulk-fed B block is prefetched into L2
 
 template <int G, int NI>
 struct Roles {
@@ -238,6 +239,11 @@ __global__ void __launch_bounds__(EngineRoles<Prob, BN>::R::kThreads, 1)
                             bulk_g2s(smem + (b_hi(slot) - smem_base), prob.b_image(tile, ks), 2 * Cfg::kBTile,
                                      &ctl->full[slot]);
                             last_issued = int(c);
+                            // the B image may stream from HBM (the filter gradient's dy
+                            // image is larger than L2): pull a later stage's block into L2
+                            // now, so that its copy finds it there
+                            if (ks + kBPrefetch < tile.ks1)
+                                prefetch_l2_bulk(prob.b_image(tile, ks + kBPrefetch), 2 * Cfg::kBTile);
                         }
                     }
                     if constexpr (ATMEM) {

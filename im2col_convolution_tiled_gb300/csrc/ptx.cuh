@@ -129,6 +129,14 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, u
         : "memory");
 }
 
+// Bulk prefetch of a global range into L2 (no shared memory, no completion):
+// a later bulk copy of the range then reads L2 instead of HBM.  Address and
+// size must be multiples of 16 bytes.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* gmem_src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gmem_src), "r"(bytes) : "memory");
+}
+
 // Tiled 4-D tensor load (TMA) of one box into shared memory, completing on an
 // mbarrier with the box's byte count.  Coordinates are element indices,
 // innermost first; boxes may start outside the tensor (the outside reads as
