@@ -71,4 +71,184 @@ cudaError_t build_bimage(const Gen& gen, int n_rows, int k_total, int bn, float*
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Space-to-depth copy for strided convolutions with few channels: for stride
+// S, X'[n, c', hh, ww] = x[n, c, S*hh + a - pad, S*ww + b - pad] with
+// c' = c*S*S + a*S + b (zero outside the image), over an Hs x Ws super-pixel
+// grid.  BLOCKED writes the channel-blocked layout [n][c'/32][hh][ww][32]
+// (zero for c' >= C*S*S) that the tensor-map patch kernel loads; otherwise
+// NCHW [n][c'][hh][ww] for the filter gradient's column gather.
+//
+// Persistent blocks take super-rows (n, hh) in turn.  The C*S input rows of a
+// super-row are staged in shared memory, kS2dBufs super-rows deep, so that the
+// reads of the next ones are in flight while one is written out: with one bulk
+// copy per row (the copy engine, completion on a per-buffer mbarrier) when rows
+// start on 16-byte boundaries (W a multiple of 4), else with 4-byte cp.async.
+// Shared rows have a pitch of 4 mod 32 floats, so the lanes of a warp reading
+// (b, a, c) neighbours hit distinct banks.  Waits are bounded; on give-up the
+// block records the error and leaves after its copies have landed.
+__host__ __device__ inline int s2d_pitch(int W) { return W + ((4 - W) % 32 + 32) % 32; }
+
+constexpr int kS2dThreads = 256;
+constexpr int kS2dBufs = 3;
+
+template <bool BLOCKED>
+__global__ void __launch_bounds__(kS2dThreads, 4)
+    s2d_copy_kernel(const float* __restrict__ x, float* __restrict__ dst, int C, int H, int W, int S, int pad, int Cs,
+                    int Cb, int Hs, int Ws, int items, FastDiv f_s, FastDiv f_ss, FastDiv f_hs, int* err)
+{
+    extern __shared__ __align__(16) float s2d_rows[];   // kS2dBufs buffers of [c * S + a][pitch]
+    __shared__ uint64_t bar[kS2dBufs];
+    __shared__ int abort_flag;
+    const int CS = C * S, pitch = s2d_pitch(W);
+    const int buf_floats = CS * pitch;
+    const bool bulk = (W & 3) == 0;
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < kS2dBufs; ++b) mbar_init(&bar[b], 1);
+        abort_flag = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+    // stage super-row `item` into buffer b
+    auto stage = [&](int item, int b) {
+        uint32_t n, hh;
+        f_hs.divmod(uint32_t(item), n, hh);
+        float* buf = s2d_rows + b * buf_floats;
+        int live = 0;
+        if (bulk && threadIdx.x == 0) fence_proxy_async_smem();   // the buffer's last readers are done
+        int c = 0, a = 0;   // (c, a) of row ca, advanced without divisions
+        for (int ca = 0; ca < CS; ++ca) {
+            const int h = S * int(hh) + a - pad;
+            float* row = buf + ca * pitch;
+            if (unsigned(h) < unsigned(H)) {
+                const float* src = x + ((size_t(n) * C + c) * H + h) * W;
+                if (!bulk)
+                    for (int w = threadIdx.x; w < W; w += kS2dThreads) cp_async4(smem_u32(row + w), src + w);
+                ++live;
+            } else {
+                for (int w = threadIdx.x; w < W; w += kS2dThreads) row[w] = 0.f;
+            }
+            if (++a == S) { a = 0; ++c; }
+        }
+        if (bulk && threadIdx.x == 0) {
+            mbar_arrive_expect_tx(&bar[b], uint32_t(live) * uint32_t(W) * 4u);
+            c = 0, a = 0;
+            for (int ca = 0; ca < CS; ++ca) {
+                const int h = S * int(hh) + a - pad;
+                if (unsigned(h) < unsigned(H))
+                    bulk_g2s(buf + ca * pitch, x + ((size_t(n) * C + c) * H + h) * W, uint32_t(W) * 4u, &bar[b]);
+                if (++a == S) { a = 0; ++c; }
+            }
+        }
+        if (!bulk) cp_async_commit();
+    };
+    int it = 0, item = blockIdx.x;
+    for (int i = 0; i < kS2dBufs - 1; ++i) {
+        const int pre = item + i * int(gridDim.x);
+        if (pre < items) stage(pre, i);
+        else if (!bulk) cp_async_commit();   // keep one group per buffer slot
+    }
+    for (; item < items; item += gridDim.x, ++it) {
+        const int ahead = item + (kS2dBufs - 1) * int(gridDim.x);
+        if (ahead < items) stage(ahead, (it + kS2dBufs - 1) % kS2dBufs);
+        else if (!bulk) cp_async_commit();
+        bool got = true;
+        if (bulk) got = mbar_wait(&bar[it % kS2dBufs], uint32_t(it / kS2dBufs) & 1u, &abort_flag);
+        else cp_async_wait_group<kS2dBufs - 1>();   // this thread's copies of the current super-row landed
+        if (!__syncthreads_and(got ? 1 : 0)) {      // ... and everybody else's
+            if (threadIdx.x == 0) {
+                abort_flag = 1;
+                atomicOr(err, kDevErrTimeout);
+            }
+            break;
+        }
+        const float* buf = s2d_rows + (it % kS2dBufs) * buf_floats;
+        uint32_t n, hh;
+        f_hs.divmod(uint32_t(item), n, hh);
+        // A thread owns four consecutive channels c' = 4g .. 4g + 3 of a 32-channel
+        // block: their rows and column offsets are decoded once per block, then
+        // each pixel costs four shared loads.  Blocked: g = thread % 8 and eight
+        // threads write a pixel; NCHW: g = warp and the lanes run along ww.
+        const int g4 = BLOCKED ? (threadIdx.x & 7) : (threadIdx.x >> 5);
+        const int ww0 = BLOCKED ? (threadIdx.x >> 3) : (threadIdx.x & 31);
+        for (int cb = 0; cb < Cb; ++cb) {
+            const float* row[4];
+            int boff[4];
+            bool live[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                uint32_t c, ab, a, b;
+                f_ss.divmod(uint32_t(cb * 32 + 4 * g4 + e), c, ab);
+                f_s.divmod(ab, a, b);
+                live[e] = int(c) < C;
+                row[e] = buf + (live[e] ? (int(c) * S + int(a)) * pitch : 0);
+                boff[e] = int(b) - pad;
+            }
+            if constexpr (BLOCKED) {
+                // eight threads write one 128-byte pixel with 16-byte stores
+                float4* out = reinterpret_cast<float4*>(dst + ((size_t(n) * Cb + cb) * Hs + hh) * size_t(Ws) * 32);
+                for (int ww = ww0; ww < Ws; ww += 32) {
+                    float v[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int w = S * ww + boff[e];
+                        v[e] = (live[e] && unsigned(w) < unsigned(W)) ? row[e][w] : 0.f;
+                    }
+                    out[ww * 8 + g4] = make_float4(v[0], v[1], v[2], v[3]);
+                }
+            } else {
+                // channels of the block past Cs do not exist in NCHW
+                const int cp0 = cb * 32 + 4 * g4;
+                for (int ww = ww0; ww < Ws; ww += 32) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if (cp0 + e >= Cs) break;
+                        const int w = S * ww + boff[e];
+                        dst[((size_t(n) * Cs + cp0 + e) * Hs + hh) * size_t(Ws) + ww] =
+                            (live[e] && unsigned(w) < unsigned(W)) ? row[e][w] : 0.f;
+                    }
+                }
+            }
+        }
+        __syncthreads();   // the buffer is restaged next iteration
+    }
+    if (!bulk) cp_async_wait_group<0>();
+    if (bulk && abort_flag && threadIdx.x == 0) {
+        // copies still in flight land before the block's shared memory goes away
+        for (int j = 0; j < kS2dBufs; ++j) {
+            const int pending = item + j * int(gridDim.x);
+            if (pending >= items) break;
+            uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(&bar[(it + j) % kS2dBufs], uint32_t((it + j) / kS2dBufs) & 1u) &&
+                   globaltimer_ns() - t0 < kWaitLimitNs) {
+            }
+        }
+    }
+}
+
+// Shared memory of s2d_copy_kernel (kS2dBufs buffers of staged rows).
+inline size_t s2d_copy_smem(int C, int S, int W) { return kS2dBufs * size_t(C) * S * s2d_pitch(W) * sizeof(float); }
+constexpr size_t kS2dMaxSmem = 96 * 1024;
+
+template <bool BLOCKED>
+cudaError_t launch_s2d_copy(const float* x, float* dst, int N, int C, int H, int W, int S, int pad, int Hs, int Ws,
+                            cudaStream_t st)
+{
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(s2d_copy_kernel<BLOCKED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             int(kS2dMaxSmem));
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int Cs = C * S * S, Cb = (Cs + 31) / 32;
+    const int items = N * Hs;
+    const int grid = items < 4 * sm_count() ? items : 4 * sm_count();
+    s2d_copy_kernel<BLOCKED><<<grid, kS2dThreads, s2d_copy_smem(C, S, W), st>>>(
+        x, dst, C, H, W, S, pad, Cs, Cb, Hs, Ws, items, FastDiv(uint32_t(S)), FastDiv(uint32_t(S * S)),
+        FastDiv(uint32_t(Hs)), device_error_word());
+    note_launch();
+    return cudaGetLastError();
+}
+
 }  // namespace cb200

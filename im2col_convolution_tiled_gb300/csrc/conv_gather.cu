@@ -762,11 +762,6 @@ static cudaError_t setup_patch_tma(PatchGeom& pg, float* blocked, cudaStream_t s
 // T = ceil(R / S) super-pixels wide, and C*S*S channels fill 32-channel chunks: the form the
 // tensor-map patch kernel runs best (AlexNet conv1: 3 channels, 11 x 11, stride 4 -> 48 channels, 3 x 3).
 
-// Row pitch (floats) of the staged input rows of the space-to-depth copy: 4 mod 32.
-__host__ __device__ inline int s2d_pitch(int W) { return W + ((4 - W) % 32 + 32) % 32; }
-
-constexpr int kS2dMaxRowBytes = 64 * 1024;   // shared memory of the staged input rows of one super-row
-
 struct S2dPlan {
     bool use;
     int bn, T, Ci;
@@ -784,7 +779,7 @@ static S2dPlan plan_fwd_s2d(const ConvDims& d)
     int n_tiles;
     sp.bn = pick_conv_bn(d.K, &n_tiles);
     if (sp.bn > 128) return sp;
-    if (size_t(d.C) * d.S * s2d_pitch(d.W) * sizeof(float) > size_t(kS2dMaxRowBytes)) return sp;   // staged rows
+    if (s2d_copy_smem(d.C, d.S, d.W) > kS2dMaxSmem) return sp;   // staged input rows
     sp.pg = make_patch(nullptr, d.N, sp.Ci, d.P + sp.T - 1, d.Q + sp.T - 1, d.P, d.Q, 1, 0, sp.T);
     if (sp.pg.mode != 0) return sp;
     patch_box(sp.pg);
@@ -811,50 +806,6 @@ struct FwdS2dFilterGen {   // B[k, kk] = W'[k, c', tr, tq] in the chunk-major K 
         return __ldg(w + ((size_t(k) * C + c) * R + r) * R + q);
     }
 };
-
-// dst[n][c' / 32][hh][ww][c' % 32] = X'[n, c', hh, ww].  One block per
-// (n, hh): the C*S input rows h = S*hh + a - pad (all channels c, phases a)
-// are staged in shared memory with coalesced reads, then the block writes the
-// super-row's pixels of every 32-channel block, 32 consecutive floats (one
-// pixel) per warp store.  A thread keeps one channel c' per block cb, so its
-// (c, a, b) decode is done once per cb.  Rows are loaded eight at a time into
-// registers (eight loads in flight per thread) and stored at a pitch of 4 mod
-// 32 floats, so the lanes of a warp (consecutive b, then a, then c) read
-// distinct banks.
-__global__ void __launch_bounds__(256) to_blocked_s2d_kernel(const float* __restrict__ x, float* __restrict__ dst,
-                                                             int C, int H, int W, int S, int pad, int Cb, int Hs,
-                                                             int Ws)
-{
-    extern __shared__ float rows[];   // [c * S + a][pitch]
-    const int hh = blockIdx.x % Hs, n = blockIdx.x / Hs;
-    const int CS = C * S, pitch = s2d_pitch(W);
-    for (int w = threadIdx.x; w < W; w += blockDim.x) {
-        for (int ca0 = 0; ca0 < CS; ca0 += 8) {
-            float v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int ca = ca0 + u, c = ca / S, h = S * hh + ca % S - pad;
-                v[u] = (ca < CS && unsigned(h) < unsigned(H)) ? __ldg(x + ((size_t(n) * C + c) * H + h) * W + w) : 0.f;
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (ca0 + u < CS) rows[(ca0 + u) * pitch + w] = v[u];
-        }
-    }
-    __syncthreads();
-    const int j = threadIdx.x & 31;
-    for (int cb = 0; cb < Cb; ++cb) {
-        const int cp = cb * 32 + j;
-        const int c = cp / (S * S), a = (cp / S) % S, b = cp % S;
-        const bool live = c < C;
-        const float* row = rows + (live ? (c * S + a) * s2d_pitch(W) : 0);
-        float* out = dst + ((size_t(n) * Cb + cb) * Hs + hh) * size_t(Ws) * 32;
-        for (int t = threadIdx.x; t < Ws * 32; t += blockDim.x) {
-            const int w = S * (t >> 5) + b - pad;
-            out[t] = (live && unsigned(w) < unsigned(W)) ? row[w] : 0.f;
-        }
-    }
-}
 
 // Which kernel a convolution-window GEMM runs on, and the workspace it needs:
 // the patch-staged kernel when the output tile is at most 128 wide and every
@@ -966,17 +917,8 @@ cudaError_t launch_conv_fwd(const ConvDims& d, const float* x, const float* w, c
         if (e != cudaSuccess) return e;
         float* blocked = reinterpret_cast<float*>(static_cast<char*>(ws) +
                                                   round_up_256(bimage_floats(d.K, k_total, sp.bn) * sizeof(float)));
-        static bool attr_set = false;
-        if (!attr_set) {
-            e = cudaFuncSetAttribute(to_blocked_s2d_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kS2dMaxRowBytes);
-            if (e != cudaSuccess) return e;
-            attr_set = true;
-        }
-        const size_t smem = size_t(d.C) * d.S * s2d_pitch(d.W) * sizeof(float);
-        to_blocked_s2d_kernel<<<unsigned(pg.Nb * pg.Hi), 256, smem, st>>>(x, blocked, d.C, d.H, d.W, d.S, d.pad,
-                                                                         pg.Cb, pg.Hi, pg.Wi);
-        note_launch();
+        e = launch_s2d_copy<true>(x, blocked, d.N, d.C, d.H, d.W, d.S, d.pad, pg.Hi, pg.Wi, st);
+        if (e != cudaSuccess) return e;
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if ((e = encode_patch_tmap(pg, blocked)) != cudaSuccess) return e;
         return dispatch_patch<true>(sp.bn, pg, o, img, st);

@@ -170,6 +170,59 @@ __global__ void wgrad_reduce_kernel(const float* __restrict__ part, int splits, 
     }
 }
 
+// Space-to-depth form (stride S > 1, at most 16 channels): the filter
+// gradient of the stride-1 convolution over S x S super-pixels
+//   X'[n, c', hh, ww] = x[n, c, S*hh + a - pad, S*ww + b - pad],  c' = c*S*S + a*S + b
+// with T = ceil(R / S) taps (see the forward's space-to-depth form), whose
+// column-matrix gather reads X' with unit stride instead of x with stride S;
+// then dW[k, c, r, s] = dW'[k, (c, r % S, s % S), r / S, s / S].
+// X' is written NCHW (rows of ww contiguous) for the gather.
+struct WgradS2d {
+    bool use;
+    int T, Cs, Hs, Ws;
+    ConvDims d2;   // the derived stride-1 convolution over X'
+};
+
+static WgradS2d plan_wgrad_s2d(const ConvDims& d)
+{
+    WgradS2d w{};
+    w.use = false;
+    if (d.S < 2 || d.C > 16) return w;
+    w.T = (d.R + d.S - 1) / d.S;
+    w.Cs = d.C * d.S * d.S;
+    if (w.Cs < 17 || w.Cs > 128) return w;
+    if (s2d_copy_smem(d.C, d.S, d.W) > kS2dMaxSmem) return w;   // staged input rows
+    w.Hs = d.P + w.T - 1;
+    w.Ws = d.Q + w.T - 1;
+    if ((long long)d.N * w.Cs * w.Hs * w.Ws >= (1LL << 31)) return w;
+    w.d2 = d;
+    w.d2.C = w.Cs;
+    w.d2.H = w.Hs;
+    w.d2.W = w.Ws;
+    w.d2.R = w.T;
+    w.d2.S = 1;
+    w.d2.pad = 0;
+    w.use = true;
+    return w;
+}
+
+// dW[k, c, r, s] = sum over split (ascending) of part[split][k, (c, r % S, s % S), r / S, s / S].
+__global__ void wgrad_reduce_s2d_kernel(const float* __restrict__ part, int splits, int K, int C, int R, int S, int T,
+                                        float* __restrict__ dw)
+{
+    const int count = K * C * R * R;
+    const int Cs = C * S * S;
+    const long long pcount = (long long)K * Cs * T * T;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < count; i += gridDim.x * blockDim.x) {
+        const int s = i % R, r = (i / R) % R, c = (i / (R * R)) % C, k = i / (R * R * C);
+        const int cp = c * S * S + (r % S) * S + (s % S);
+        const long long j = (((long long)k * Cs + cp) * T + r / S) * T + s / S;
+        float acc = 0.f;
+        for (int sp = 0; sp < splits; ++sp) acc += __ldg(part + sp * pcount + j);
+        dw[i] = acc;
+    }
+}
+
 struct WgradPlan {
     int bn, m_tiles, n_tiles, k_stages, splits, ks_per_split;
 };
@@ -198,23 +251,35 @@ static size_t wgrad_image_floats(const ConvDims& d, const WgradPlan& pl)
     return bimage_floats(d.K, d.N * d.P * d.Q, pl.bn);
 }
 
-size_t conv_wgrad_ws(const ConvDims& d)
+static size_t xs2d_floats(const ConvDims& d, const WgradS2d& w)
 {
-    WgradPlan pl = plan_wgrad(d);
-    const size_t part = pl.splits > 1 ? size_t(pl.splits) * d.K * d.C * d.R * d.R : 0;
-    return (wgrad_image_floats(d, pl) + part) * sizeof(float);
+    return w.use ? (size_t(d.N) * w.Cs * w.Hs * w.Ws + 63) & ~size_t(63) : 0;
 }
 
+// Workspace: [X' (space-to-depth form)] [the G image] [partial tiles: split-K,
+// or always in the space-to-depth form (remapped by its reduce)].
+size_t conv_wgrad_ws(const ConvDims& d)
+{
+    const WgradS2d w = plan_wgrad_s2d(d);
+    const ConvDims& g = w.use ? w.d2 : d;
+    WgradPlan pl = plan_wgrad(g);
+    const size_t part = (pl.splits > 1 || w.use) ? size_t(pl.splits) * g.K * g.C * g.R * g.R : 0;
+    return (xs2d_floats(d, w) + wgrad_image_floats(g, pl) + part) * sizeof(float);
+}
+
+// d: the convolution the GEMM runs (the derived one in the space-to-depth
+// form); ws: its image and partials.  With remap, the partials always go to
+// the workspace and wgrad_reduce_s2d_kernel writes dW of `orig`.
 template <int BN>
 static cudaError_t run_wgrad(const ConvDims& d, const WgradPlan& pl, const float* x, const float* dy, float* dw,
-                             void* ws, cudaStream_t st)
+                             void* ws, cudaStream_t st, const ConvDims* orig = nullptr)
 {
     ConvWgradProb<BN> p;
     float* img = static_cast<float*>(ws);
     float* part = img + wgrad_image_floats(d, pl);
     p.x = x;
     p.bimg = img;
-    p.out = pl.splits > 1 ? part : dw;
+    p.out = (pl.splits > 1 || orig) ? part : dw;
     p.C = d.C; p.H = d.H; p.W = d.W; p.K = d.K; p.R = d.R; p.S = d.S; p.pad = d.pad; p.P = d.P; p.Q = d.Q;
     p.PQ = d.P * d.Q;
     p.NPQ = d.N * p.PQ;
@@ -233,7 +298,15 @@ static cudaError_t run_wgrad(const ConvDims& d, const WgradPlan& pl, const float
     cudaError_t e = build_bimage(GradGen{dy, d.K, p.PQ, FastDiv(uint32_t(p.PQ))}, d.K, p.NPQ, BN, img, st);
     if (e != cudaSuccess) return e;
     e = launch_tc_gemm<ConvWgradProb<BN>, BN>(p, p.m_tiles * p.n_tiles * p.splits, device_error_word(), st);
-    if (e != cudaSuccess || pl.splits == 1) return e;
+    if (e != cudaSuccess) return e;
+    if (orig) {
+        const int count = orig->K * orig->C * orig->R * orig->R;
+        const int blocks = (count + 255) / 256 < 8 * sm_count() ? (count + 255) / 256 : 8 * sm_count();
+        wgrad_reduce_s2d_kernel<<<blocks, 256, 0, st>>>(part, pl.splits, orig->K, orig->C, orig->R, orig->S, d.R, dw);
+        note_launch();
+        return cudaGetLastError();
+    }
+    if (pl.splits == 1) return e;
     const long long count = (long long)d.K * p.CRS;
     long long blocks = (count + 255) / 256;
     if (blocks > 8LL * sm_count()) blocks = 8LL * sm_count();
@@ -245,13 +318,25 @@ static cudaError_t run_wgrad(const ConvDims& d, const WgradPlan& pl, const float
 cudaError_t launch_conv_wgrad(const ConvDims& d, const float* x, const float* dy, float* dw, void* ws,
                               cudaStream_t st)
 {
-    WgradPlan pl = plan_wgrad(d);
+    const WgradS2d w = plan_wgrad_s2d(d);
+    const ConvDims& g = w.use ? w.d2 : d;
+    const ConvDims* orig = w.use ? &d : nullptr;
+    WgradPlan pl = plan_wgrad(g);
+    const float* xg = x;
+    void* gws = ws;
+    if (w.use) {
+        float* xs = static_cast<float*>(ws);
+        cudaError_t e = launch_s2d_copy<false>(x, xs, d.N, d.C, d.H, d.W, d.S, d.pad, w.Hs, w.Ws, st);
+        if (e != cudaSuccess) return e;
+        xg = xs;
+        gws = xs + xs2d_floats(d, w);
+    }
     switch (pl.bn) {
-    case 32: return run_wgrad<32>(d, pl, x, dy, dw, ws, st);
-    case 64: return run_wgrad<64>(d, pl, x, dy, dw, ws, st);
-    case 128: return run_wgrad<128>(d, pl, x, dy, dw, ws, st);
-    case 192: return run_wgrad<192>(d, pl, x, dy, dw, ws, st);
-    default: return run_wgrad<256>(d, pl, x, dy, dw, ws, st);
+    case 32: return run_wgrad<32>(g, pl, xg, dy, dw, gws, st, orig);
+    case 64: return run_wgrad<64>(g, pl, xg, dy, dw, gws, st, orig);
+    case 128: return run_wgrad<128>(g, pl, xg, dy, dw, gws, st, orig);
+    case 192: return run_wgrad<192>(g, pl, xg, dy, dw, gws, st, orig);
+    default: return run_wgrad<256>(g, pl, xg, dy, dw, gws, st, orig);
     }
 }
 
