@@ -60,10 +60,12 @@ def oracle_sample_run(layers, batch):
     import oracle
     orc = oracle.get()
     flops = 0
-    t0 = time.perf_counter()
-    for L in layers:
+    inputs = []
+    for L in layers:   # input generation is not part of the timed work
         l = L.with_batch(batch)
-        x, w, b, dy = l.make()
+        inputs.append((l, l.make()))
+    t0 = time.perf_counter()
+    for l, (x, w, b, dy) in inputs:
         orc.conv_fwd(x, w, b, l.stride, l.pad)
         orc.conv_bwd_data(w, dy, x.shape, l.stride, l.pad)
         orc.conv_bwd_filter(x, dy, w.shape, l.stride, l.pad)
@@ -213,7 +215,7 @@ def run_ours(args):
     ws = torch.empty(max(b.ws_bytes for b in bufs) + 16, dtype=torch.uint8, device="cuda")
     lr, clip = synthetic.SGD_LR_CLIP
     stream = torch.cuda.current_stream()
-    ops = ["fwd", "pool", "dgrad", "wgrad", "bias", "sgd"]
+    ops = ["fwd", "pool", "dgrad", "wgrad", "sgd"]   # wgrad includes the bias gradient
     rec = {}   # (layer, op) -> list of (start_event, end_event)
 
     def timed(key, fn):
@@ -227,21 +229,24 @@ def run_ours(args):
         e1.record(stream)
         rec.setdefault(key, []).append((e0, e1))
 
+    def run_layer(b, record):
+        L = b.L
+        key = (lambda op: (L.name, op)) if record else (lambda op: None)
+        timed(key("fwd"), lambda: cb.conv_fwd(b.x, b.w, b.b, L.stride, L.pad, y=b.y, workspace=ws))
+        if b.pool:
+            k, s = b.pool
+            timed(key("pool"), lambda: (cb.maxpool2d_fwd(b.y, k, s, y=b.yp, idx=b.idx),
+                                        cb.maxpool2d_bwd(b.dyp, b.idx, L.y_shape, k, s, dx=b.dxp)))
+        timed(key("dgrad"), lambda: cb.conv_bwd_data(b.w, b.dy, L.x_shape, L.stride, L.pad, dx=b.dx,
+                                                     workspace=ws))
+        # filter and bias gradients from one pass over dy (conv_bwd_filter_bias)
+        timed(key("wgrad"), lambda: cb.conv_bwd_filter_bias(b.x, b.dy, L.w_shape, L.stride, L.pad, dw=b.dw,
+                                                            db=b.db, workspace=ws))
+        timed(key("sgd"), lambda: (cb.sgd_step(b.w, b.dw, lr, clip), cb.sgd_step(b.b, b.db, lr, clip)))
+
     def step(record):
         for b in bufs:
-            L = b.L
-            key = (lambda op: (L.name, op)) if record else (lambda op: None)
-            timed(key("fwd"), lambda: cb.conv_fwd(b.x, b.w, b.b, L.stride, L.pad, y=b.y, workspace=ws))
-            if b.pool:
-                k, s = b.pool
-                timed(key("pool"), lambda: (cb.maxpool2d_fwd(b.y, k, s, y=b.yp, idx=b.idx),
-                                            cb.maxpool2d_bwd(b.dyp, b.idx, L.y_shape, k, s, dx=b.dxp)))
-            timed(key("dgrad"), lambda: cb.conv_bwd_data(b.w, b.dy, L.x_shape, L.stride, L.pad, dx=b.dx,
-                                                         workspace=ws))
-            timed(key("wgrad"), lambda: cb.conv_bwd_filter(b.x, b.dy, L.w_shape, L.stride, L.pad, dw=b.dw,
-                                                           workspace=ws))
-            timed(key("bias"), lambda: cb.conv_bwd_bias(b.dy, db=b.db))
-            timed(key("sgd"), lambda: (cb.sgd_step(b.w, b.dw, lr, clip), cb.sgd_step(b.b, b.db, lr, clip)))
+            run_layer(b, record)
 
     def barrier():
         torch.cuda.synchronize()
@@ -309,23 +314,38 @@ def run_ours(args):
     h2d = sum(b.bytes_in() for b in bufs)
     d2h = sum(b.bytes_out() for b in bufs)
 
+    # Per-layer pipelining: layer i's host->device copies run on their own
+    # stream ahead of its compute, and its results go back on a third stream
+    # while the next layers compute; every step ends with all copies done.
+    s_h2d, s_d2h = torch.cuda.Stream(), torch.cuda.Stream()
+
     def e2e_step():
-        for b, hi in zip(bufs, host_in):
-            b.x.copy_(hi["x"], non_blocking=True)
-            b.w.copy_(hi["w"], non_blocking=True)
-            b.b.copy_(hi["b"], non_blocking=True)
-            b.dy.copy_(hi["dy"], non_blocking=True)
-            if b.pool:
-                b.dyp.copy_(hi["dyp"], non_blocking=True)
-        step(False)
-        for b, ho in zip(bufs, host_out):
-            ho["y"].copy_(b.y, non_blocking=True)
-            ho["dx"].copy_(b.dx, non_blocking=True)
-            ho["dw"].copy_(b.dw, non_blocking=True)
-            ho["db"].copy_(b.db, non_blocking=True)
-            if b.pool:
-                ho["dxp"].copy_(b.dxp, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+        ev_in = [torch.cuda.Event() for _ in bufs]
+        ev_out = [torch.cuda.Event() for _ in bufs]
+        with torch.cuda.stream(s_h2d):
+            for i, (b, hi) in enumerate(zip(bufs, host_in)):
+                b.x.copy_(hi["x"], non_blocking=True)
+                b.w.copy_(hi["w"], non_blocking=True)
+                b.b.copy_(hi["b"], non_blocking=True)
+                b.dy.copy_(hi["dy"], non_blocking=True)
+                if b.pool:
+                    b.dyp.copy_(hi["dyp"], non_blocking=True)
+                ev_in[i].record(s_h2d)
+        for i, b in enumerate(bufs):
+            stream.wait_event(ev_in[i])
+            run_layer(b, None)
+            ev_out[i].record(stream)
+            with torch.cuda.stream(s_d2h):
+                s_d2h.wait_event(ev_out[i])
+                ho = host_out[i]
+                ho["y"].copy_(b.y, non_blocking=True)
+                ho["dx"].copy_(b.dx, non_blocking=True)
+                ho["dw"].copy_(b.dw, non_blocking=True)
+                ho["db"].copy_(b.db, non_blocking=True)
+                if b.pool:
+                    ho["dxp"].copy_(b.dxp, non_blocking=True)
+        s_d2h.synchronize()
+        stream.synchronize()
 
     e2e_steps = max(3, args.steps // 4)
     e2e_step()
@@ -384,7 +404,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-batch", type=int, default=12)
+    ap.add_argument("--cpu-batch", type=int, default=64)
     ap.add_argument("--ref-batch", type=int, default=1)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps, always

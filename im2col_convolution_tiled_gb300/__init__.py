@@ -19,7 +19,8 @@ import ctypes
 import os
 
 __all__ = [
-    "ConvShape", "lib", "load", "conv_fwd", "conv_bwd_data", "conv_bwd_filter", "conv_bwd_bias",
+    "ConvShape", "lib", "load", "conv_fwd", "conv_bwd_data", "conv_bwd_filter", "conv_bwd_filter_bias",
+    "conv_bwd_bias",
     "im2col", "col2im", "matmul", "maxpool2d_fwd", "maxpool2d_bwd", "sgd_step", "workspace_bytes",
     "check", "ConvError", "out_size", "LIB_PATH", "launch_count",
 ]
@@ -49,6 +50,7 @@ _SIGS = {
     "conv_fwd": ([_SHAPE, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
     "conv_bwd_data": ([_SHAPE, _P, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
     "conv_bwd_filter": ([_SHAPE, _P, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
+    "conv_bwd_filter_bias": ([_SHAPE, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
     "conv_bwd_bias": ([_SHAPE, _P, _P, _P], ctypes.c_int),
     "conv_b200_workspace_bytes": ([ctypes.c_int, _SHAPE], ctypes.c_size_t),
     "im2col": ([_SHAPE, _P, _P, _P], ctypes.c_int),
@@ -190,6 +192,22 @@ def conv_bwd_filter(x, dy, w_shape, stride=1, padding=0, dw=None, workspace=None
     ws, nbytes = _workspace(CONV_OP_BWD_FILTER, s, workspace)
     _call("conv_bwd_filter", ctypes.byref(s), _ptr(x), _ptr(dy), _ptr(dw), _ptr(ws), nbytes, _stream(stream))
     return dw
+
+
+def conv_bwd_filter_bias(x, dy, w_shape, stride=1, padding=0, dw=None, db=None, workspace=None, stream=None):
+    """(dw, db): filter and bias gradients from one pass over dy."""
+    torch = _torch()
+    _want(x, "x"), _want(dy, "dy")
+    s = shape_of(x.shape, tuple(w_shape), stride, padding)
+    if dw is None:
+        dw = torch.empty(tuple(w_shape), dtype=torch.float32, device=x.device)
+    if db is None:
+        db = torch.empty((w_shape[0],), dtype=torch.float32, device=x.device)
+    _want(dw, "dw"), _want(db, "db")
+    ws, nbytes = _workspace(CONV_OP_BWD_FILTER, s, workspace)
+    _call("conv_bwd_filter_bias", ctypes.byref(s), _ptr(x), _ptr(dy), _ptr(dw), _ptr(db), _ptr(ws), nbytes,
+          _stream(stream))
+    return dw, db
 
 
 def conv_bwd_bias(dy, db=None, stream=None):

@@ -186,6 +186,18 @@ int conv_bwd_filter(const conv_shape_t* s, const float* x, const float* dy, floa
     return status_of(launch_conv_wgrad(d, x, dy, dw, workspace, as_cuda(stream)));
 }
 
+int conv_bwd_filter_bias(const conv_shape_t* s, const float* x, const float* dy, float* dw, float* db,
+                         void* workspace, size_t workspace_bytes, conv_stream_t stream)
+{
+    ConvDims d;
+    int rc = check_shape(s, &d);
+    if (rc != CONV_OK) return rc;
+    if ((rc = check_ptrs({x, dy, dw, db})) != CONV_OK) return rc;
+    if ((rc = check_workspace(conv_wgrad_ws(d), workspace, workspace_bytes)) != CONV_OK) return rc;
+    if (!device_ok()) return CONV_ERR_DEVICE;
+    return status_of(launch_conv_wgrad(d, x, dy, dw, workspace, as_cuda(stream), db));
+}
+
 int conv_bwd_bias(const conv_shape_t* s, const float* dy, float* db, conv_stream_t stream)
 {
     ConvDims d;

@@ -44,8 +44,9 @@ cudaError_t launch_conv_dgrad(const ConvDims& d, const float* w, const float* dy
                               cudaStream_t st);
 size_t conv_dgrad_ws(const ConvDims& d);
 
+// db non-null: also the bias gradient, summed in the same pass over dy.
 cudaError_t launch_conv_wgrad(const ConvDims& d, const float* x, const float* dy, float* dw, void* ws,
-                              cudaStream_t st);
+                              cudaStream_t st, float* db = nullptr);
 size_t conv_wgrad_ws(const ConvDims& d);
 
 cudaError_t launch_matmul(int M, int K, int N, unsigned flags, const float* A, const float* B, float* C,

@@ -35,18 +35,28 @@ inline size_t bimage_floats(int n_rows, int k_total, int bn)
 // Gen(row, k) returns the (unsplit) B element.  One thread builds one 16-byte
 // chunk (4 consecutive k of one row) of the hi and of the lo tile; blockIdx.y
 // is the row, so consecutive threads read consecutive k.
+// With rowsum non-null the kernel also sums each row's unsplit values: every
+// block writes rowsum[row * gridDim.x + blockIdx.x] (its threads' values in a
+// fixed order, then lanes, then warps), and rowsum_final_kernel adds a row's
+// block partials in block order -- a deterministic row sum from the same pass
+// (the filter gradient's dy image gives the bias gradient this way).
+constexpr int kBimageThreads = 256;
+
 template <class Gen>
-__global__ void build_bimage_kernel(Gen gen, int n_rows, int k_total, int bn, int k_stages, float* img)
+__global__ void __launch_bounds__(kBimageThreads) build_bimage_kernel(Gen gen, int n_rows, int k_total, int bn,
+                                                                      int k_stages, float* img, float* rowsum)
 {
     const int row = blockIdx.y;
     const int chunks = k_stages * (kBK / 4);
     const int nt = row / bn, r = row % bn;
+    float part = 0.f;
     for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < chunks; t += gridDim.x * blockDim.x) {
         const int k0 = t * 4;
         uint32_t hi[4], lo[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const float v = (row < n_rows && k0 + e < k_total) ? gen(row, k0 + e) : 0.f;
+            part += v;
             split_tf32(v, hi[e], lo[e]);
         }
         const int ks = t / (kBK / 4), c = t % (kBK / 4);
@@ -55,18 +65,36 @@ __global__ void build_bimage_kernel(Gen gen, int n_rows, int k_total, int bn, in
         *reinterpret_cast<uint4*>(blk + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4*>(blk + size_t(bn) * kBK + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
+    if (rowsum == nullptr || row >= n_rows) return;   // uniform over the block
+    __shared__ float warp_part[kBimageThreads / 32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+    if ((threadIdx.x & 31) == 0) warp_part[threadIdx.x >> 5] = part;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float t = 0.f;
+        for (int i = 0; i < kBimageThreads / 32; ++i) t += warp_part[i];
+        rowsum[size_t(row) * gridDim.x + blockIdx.x] = t;
+    }
+}
+
+// Blocks per row of build_bimage (so callers can size the row-sum partials).
+inline int bimage_grid_x(int k_total)
+{
+    const int k_stages = (k_total + kBK - 1) / kBK;
+    const int chunks = k_stages * (kBK / 4);
+    int bx = (chunks + kBimageThreads - 1) / kBimageThreads;
+    return bx > 1024 ? 1024 : bx;
 }
 
 template <class Gen>
-cudaError_t build_bimage(const Gen& gen, int n_rows, int k_total, int bn, float* img, cudaStream_t st)
+cudaError_t build_bimage(const Gen& gen, int n_rows, int k_total, int bn, float* img, cudaStream_t st,
+                         float* rowsum = nullptr)
 {
     const int n_tiles = (n_rows + bn - 1) / bn;
     const int k_stages = (k_total + kBK - 1) / kBK;
-    const int chunks = k_stages * (kBK / 4);
-    int bx = (chunks + 255) / 256;
-    if (bx > 1024) bx = 1024;
-    dim3 grid(bx, n_tiles * bn);
-    build_bimage_kernel<Gen><<<grid, 256, 0, st>>>(gen, n_rows, k_total, bn, k_stages, img);
+    dim3 grid(bimage_grid_x(k_total), n_tiles * bn);
+    build_bimage_kernel<Gen><<<grid, kBimageThreads, 0, st>>>(gen, n_rows, k_total, bn, k_stages, img, rowsum);
     note_launch();
     return cudaGetLastError();
 }

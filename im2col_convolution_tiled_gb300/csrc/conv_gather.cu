@@ -476,33 +476,59 @@ static TailPlan plan_tail(int tiles, int k_stages, int bn)
     return p;
 }
 
-// One CTA per (trailing tile, 32-column slice); thread = accumulator row.
+// One CTA per (trailing tile, 32-column slice), 1024 threads: thread (row,
+// g) adds, in piece order, the 16-byte column group g of its row over the
+// pieces (eight threads read one row's 128 bytes: coalesced, and eight times
+// the loads in flight of a thread-per-row layout).  The sums meet in shared
+// memory, and the 128 row threads hand them to the problem's epilogue.
+constexpr int kTailThreads = 1024;
+
 template <int BN>
-__global__ void __launch_bounds__(kBM) tail_reduce_kernel(const __grid_constant__ ConvGatherProb<BN> prob)
+__global__ void __launch_bounds__(kTailThreads) tail_reduce_kernel(const __grid_constant__ ConvGatherProb<BN> prob)
 {
+    __shared__ float sums[kBM][33];
     const int u0 = blockIdx.x * prob.tail_split;
-    const int row = threadIdx.x;
     const int c0 = blockIdx.y * 32;
-    float acc[32];
+    {
+        const int row = threadIdx.x >> 3, g = threadIdx.x & 7;
+        const float4* src = reinterpret_cast<const float4*>(prob.part_buf + (size_t(u0) * kBM + row) * BN + c0) + g;
+        const size_t piece = size_t(kBM) * BN / 4;   // float4s between consecutive pieces
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        int j = 0;
+        for (; j + 4 <= prob.tail_split; j += 4) {
+            float4 v[4];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-    for (int j = 0; j < prob.tail_split; ++j) {
-        const float4* src = reinterpret_cast<const float4*>(prob.part_buf + (size_t(u0 + j) * kBM + row) * BN + c0);
+            for (int q = 0; q < 4; ++q) v[q] = __ldg(src + (j + q) * piece);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float4 v = __ldg(src + i);
-            acc[4 * i] += v.x;
-            acc[4 * i + 1] += v.y;
-            acc[4 * i + 2] += v.z;
-            acc[4 * i + 3] += v.w;
+            for (int q = 0; q < 4; ++q) {
+                acc.x += v[q].x;
+                acc.y += v[q].y;
+                acc.z += v[q].z;
+                acc.w += v[q].w;
+            }
         }
+        for (; j < prob.tail_split; ++j) {
+            const float4 v = __ldg(src + j * piece);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        sums[row][4 * g] = acc.x;
+        sums[row][4 * g + 1] = acc.y;
+        sums[row][4 * g + 2] = acc.z;
+        sums[row][4 * g + 3] = acc.w;
     }
-    uint32_t r[32];
+    __syncthreads();
+    if (threadIdx.x < kBM) {
+        const int row = threadIdx.x;
+        uint32_t r[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(acc[i]);
-    const Tile tl = prob.whole_tile(prob.full_units + blockIdx.x);
-    const typename ConvGatherProb<BN>::EState e = prob.e_setup(tl, row);
-    prob.store(e, tl, row, c0, r);
+        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(sums[row][i]);
+        const Tile tl = prob.whole_tile(prob.full_units + blockIdx.x);
+        const typename ConvGatherProb<BN>::EState e = prob.e_setup(tl, row);
+        prob.store(e, tl, row, c0, r);
+    }
 }
 
 static size_t round_up_256(size_t b) { return (b + 255) & ~size_t(255); }
@@ -524,7 +550,7 @@ static cudaError_t run_gather(const GatherGeom& g, const OutGeom& o, float* img,
     const int units = tp.full_units + tp.tail_tiles * tp.split;
     cudaError_t e = launch_tc_gemm<ConvGatherProb<BN>, BN>(p, units, device_error_word(), st);
     if (e != cudaSuccess || tp.tail_tiles == 0) return e;
-    tail_reduce_kernel<BN><<<dim3(unsigned(tp.tail_tiles), unsigned(BN / 32)), kBM, 0, st>>>(p);
+    tail_reduce_kernel<BN><<<dim3(unsigned(tp.tail_tiles), unsigned(BN / 32)), kTailThreads, 0, st>>>(p);
     note_launch();
     return cudaGetLastError();
 }

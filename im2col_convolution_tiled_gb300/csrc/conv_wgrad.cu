@@ -159,6 +159,16 @@ struct GradGen {
     }
 };
 
+// out[row] = sum over block i (ascending) of rowsum[row * blocks + i].
+__global__ void rowsum_final_kernel(const float* __restrict__ rowsum, int blocks, int rows, float* __restrict__ out)
+{
+    const int row = blockIdx.x * blockDim.x + threadIdx.x;
+    if (row >= rows) return;
+    float acc = 0.f;
+    for (int i = 0; i < blocks; ++i) acc += __ldg(rowsum + size_t(row) * blocks + i);
+    out[row] = acc;
+}
+
 // dW[i] = sum over split s (ascending) of part[s][i].
 __global__ void wgrad_reduce_kernel(const float* __restrict__ part, int splits, long long count, float* __restrict__ dw)
 {
@@ -256,27 +266,43 @@ static size_t xs2d_floats(const ConvDims& d, const WgradS2d& w)
     return w.use ? (size_t(d.N) * w.Cs * w.Hs * w.Ws + 63) & ~size_t(63) : 0;
 }
 
+static size_t wgrad_part_floats(const ConvDims& g, const WgradPlan& pl, bool s2d)
+{
+    return (pl.splits > 1 || s2d) ? size_t(pl.splits) * g.K * g.C * g.R * g.R : 0;
+}
+
+// Row-sum partials of the G image (the bias gradient of conv_bwd_filter_bias).
+static size_t wgrad_rowsum_floats(const ConvDims& d)
+{
+    return size_t(d.K) * bimage_grid_x(d.N * d.P * d.Q);
+}
+
 // Workspace: [X' (space-to-depth form)] [the G image] [partial tiles: split-K,
-// or always in the space-to-depth form (remapped by its reduce)].
+// or always in the space-to-depth form (remapped by its reduce)] [row-sum
+// partials for the bias gradient].
 size_t conv_wgrad_ws(const ConvDims& d)
 {
     const WgradS2d w = plan_wgrad_s2d(d);
     const ConvDims& g = w.use ? w.d2 : d;
     WgradPlan pl = plan_wgrad(g);
-    const size_t part = (pl.splits > 1 || w.use) ? size_t(pl.splits) * g.K * g.C * g.R * g.R : 0;
-    return (xs2d_floats(d, w) + wgrad_image_floats(g, pl) + part) * sizeof(float);
+    return (xs2d_floats(d, w) + wgrad_image_floats(g, pl) + wgrad_part_floats(g, pl, w.use) +
+            wgrad_rowsum_floats(d)) *
+           sizeof(float);
 }
 
 // d: the convolution the GEMM runs (the derived one in the space-to-depth
 // form); ws: its image and partials.  With remap, the partials always go to
 // the workspace and wgrad_reduce_s2d_kernel writes dW of `orig`.
+// With db non-null the G image pass also sums each row of G (the bias
+// gradient) into row-sum partials, added in block order by rowsum_final_kernel.
 template <int BN>
 static cudaError_t run_wgrad(const ConvDims& d, const WgradPlan& pl, const float* x, const float* dy, float* dw,
-                             void* ws, cudaStream_t st, const ConvDims* orig = nullptr)
+                             void* ws, cudaStream_t st, const ConvDims* orig, float* db)
 {
     ConvWgradProb<BN> p;
     float* img = static_cast<float*>(ws);
     float* part = img + wgrad_image_floats(d, pl);
+    float* rowsum = part + wgrad_part_floats(d, pl, orig != nullptr);
     p.x = x;
     p.bimg = img;
     p.out = (pl.splits > 1 || orig) ? part : dw;
@@ -295,8 +321,14 @@ static cudaError_t run_wgrad(const ConvDims& d, const WgradPlan& pl, const float
     p.k_stages = pl.k_stages;
     p.splits = pl.splits;
     p.ks_per_split = pl.ks_per_split;
-    cudaError_t e = build_bimage(GradGen{dy, d.K, p.PQ, FastDiv(uint32_t(p.PQ))}, d.K, p.NPQ, BN, img, st);
+    cudaError_t e = build_bimage(GradGen{dy, d.K, p.PQ, FastDiv(uint32_t(p.PQ))}, d.K, p.NPQ, BN, img, st,
+                                 db ? rowsum : nullptr);
     if (e != cudaSuccess) return e;
+    if (db) {
+        rowsum_final_kernel<<<(d.K + 127) / 128, 128, 0, st>>>(rowsum, bimage_grid_x(p.NPQ), d.K, db);
+        note_launch();
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
     e = launch_tc_gemm<ConvWgradProb<BN>, BN>(p, p.m_tiles * p.n_tiles * p.splits, device_error_word(), st);
     if (e != cudaSuccess) return e;
     if (orig) {
@@ -316,7 +348,7 @@ static cudaError_t run_wgrad(const ConvDims& d, const WgradPlan& pl, const float
 }
 
 cudaError_t launch_conv_wgrad(const ConvDims& d, const float* x, const float* dy, float* dw, void* ws,
-                              cudaStream_t st)
+                              cudaStream_t st, float* db)
 {
     const WgradS2d w = plan_wgrad_s2d(d);
     const ConvDims& g = w.use ? w.d2 : d;
@@ -332,11 +364,11 @@ cudaError_t launch_conv_wgrad(const ConvDims& d, const float* x, const float* dy
         gws = xs + xs2d_floats(d, w);
     }
     switch (pl.bn) {
-    case 32: return run_wgrad<32>(g, pl, xg, dy, dw, gws, st, orig);
-    case 64: return run_wgrad<64>(g, pl, xg, dy, dw, gws, st, orig);
-    case 128: return run_wgrad<128>(g, pl, xg, dy, dw, gws, st, orig);
-    case 192: return run_wgrad<192>(g, pl, xg, dy, dw, gws, st, orig);
-    default: return run_wgrad<256>(g, pl, xg, dy, dw, gws, st, orig);
+    case 32: return run_wgrad<32>(g, pl, xg, dy, dw, gws, st, orig, db);
+    case 64: return run_wgrad<64>(g, pl, xg, dy, dw, gws, st, orig, db);
+    case 128: return run_wgrad<128>(g, pl, xg, dy, dw, gws, st, orig, db);
+    case 192: return run_wgrad<192>(g, pl, xg, dy, dw, gws, st, orig, db);
+    default: return run_wgrad<256>(g, pl, xg, dy, dw, gws, st, orig, db);
     }
 }
 

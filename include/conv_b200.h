@@ -101,6 +101,16 @@ int conv_bwd_data(const conv_shape_t *s, const float *w, const float *dy, float 
 int conv_bwd_filter(const conv_shape_t *s, const float *x, const float *dy, float *dw, void *workspace,
                     size_t workspace_bytes, conv_stream_t stream);
 
+/* Filter and bias gradients from one pass over dy: conv_bwd_filter plus the
+ * bias gradient of conv_bwd_bias, the latter summed while dy is re-laid for
+ * the filter-gradient GEMM (so dy is read once for both).  Same layouts as
+ * conv_bwd_filter and conv_bwd_bias; db [outC] (overwritten).  The bias sums
+ * run in a fixed order (deterministic) that differs from conv_bwd_bias's, so
+ * the two may differ in the last bits.
+ *   workspace: conv_b200_workspace_bytes(CONV_OP_BWD_FILTER, s) bytes. */
+int conv_bwd_filter_bias(const conv_shape_t *s, const float *x, const float *dy, float *dw, float *db,
+                         void *workspace, size_t workspace_bytes, conv_stream_t stream);
+
 /* Bias gradient.  Page section "Convolution: The im2col Approach", backward:
  * the sum of grad_reshaped over its columns, i.e. over batch, outH and outW.
  * Fixed-order reduction (deterministic).

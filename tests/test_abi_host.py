@@ -35,7 +35,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ["conv_fwd", "conv_bwd_data", "conv_bwd_filter", "conv_bwd_bias", "im2col", "col2im", "matmul",
+    for n in ["conv_fwd", "conv_bwd_data", "conv_bwd_filter", "conv_bwd_filter_bias", "conv_bwd_bias", "im2col",
+              "col2im", "matmul",
               "maxpool2d_fwd", "maxpool2d_bwd", "sgd_step", "conv_b200_strerror", "conv_b200_check",
               "conv_b200_workspace_bytes"]:
         assert n in names
@@ -80,6 +81,8 @@ def test_pointer_validation(lib):
     assert lib.conv_fwd(ctypes.byref(s), FAKE, FAKE, MIS, FAKE, FAKE, 1 << 20, NULL) == ERR_ALIGN
     assert lib.conv_bwd_filter(ctypes.byref(s), FAKE, NULL, FAKE, FAKE, 1 << 20, NULL) == ERR_NULL
     assert lib.conv_bwd_bias(ctypes.byref(s), FAKE, NULL, NULL) == ERR_NULL
+    assert lib.conv_bwd_filter_bias(ctypes.byref(s), FAKE, FAKE, FAKE, NULL, FAKE, 1 << 20, NULL) == ERR_NULL
+    assert lib.conv_bwd_filter_bias(ctypes.byref(s), FAKE, FAKE, FAKE, MIS, FAKE, 1 << 20, NULL) == ERR_ALIGN
     assert lib.col2im(ctypes.byref(s), FAKE, MIS, NULL) == ERR_ALIGN
     assert lib.matmul(4, 4, 4, 0, FAKE, NULL, FAKE, NULL) == ERR_NULL
     assert lib.maxpool2d_fwd(1, 1, 4, 4, 2, 2, 2, 2, FAKE, FAKE, MIS, NULL) == ERR_ALIGN

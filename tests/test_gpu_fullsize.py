@@ -48,8 +48,9 @@ def test_alexnet_layer_sampled(cb, orc, L):
     dx = cb.conv_bwd_data(wt, dyt, L.x_shape, L.stride, L.pad)
     dw = cb.conv_bwd_filter(xt, dyt, L.w_shape, L.stride, L.pad)
     db = cb.conv_bwd_bias(dyt)
+    dw2, db2 = cb.conv_bwd_filter_bias(xt, dyt, L.w_shape, L.stride, L.pad)   # the bench's fused call
     cb.check()
-    y, dx, dw, db = (t.cpu().numpy() for t in (y, dx, dw, db))
+    y, dx, dw, db, dw2, db2 = (t.cpu().numpy() for t in (y, dx, dw, db, dw2, db2))
 
     f = sample_idx(y.size, 1)
     ref, ref_abs = orc.conv_fwd_at(x, w, b, L.stride, L.pad, f)
@@ -60,9 +61,11 @@ def test_alexnet_layer_sampled(cb, orc, L):
     f = sample_idx(dw.size, 3)[:160]
     ref, ref_abs = orc.conv_bwd_filter_at(x, dy, L.w_shape, L.stride, L.pad, f)
     assert_within_tol(dw.ravel()[f], ref, ref_abs, L.name + " bwd_filter")
+    assert_within_tol(dw2.ravel()[f], ref, ref_abs, L.name + " bwd_filter (fused with bias)")
     ref, ref_abs = orc.conv_bwd_bias(dy)
     assert_within_tol(db, ref, ref_abs, L.name + " bwd_bias")
-    for a in (y, dx, dw):
+    assert_within_tol(db2, ref, ref_abs, L.name + " bwd_bias (fused with filter)")
+    for a in (y, dx, dw, dw2, db2):
         assert np.isfinite(a).all()
 
 

@@ -148,6 +148,21 @@ def test_conv_bwd_filter(cb, orc, shape):
     assert_within_tol(dw.numpy(), ref, ref_abs, "conv_bwd_filter %s" % (shape,))
 
 
+@pytest.mark.parametrize("shape", CONV_SHAPES)
+def test_conv_bwd_filter_bias(cb, orc, shape):
+    """The fused entry point: dw as conv_bwd_filter, db summed in the same pass over dy."""
+    x, w, _, dy = conv_inputs(shape, 350)
+    st, pad = shape[6], shape[7]
+    ref_w, ref_w_abs = orc.conv_bwd_filter(x, dy, w.shape, st, pad)
+    ref_b, ref_b_abs = orc.conv_bwd_bias(dy)
+    dw, db = dev_out(w.shape), dev_out(ref_b.shape)
+    cb.conv_bwd_filter_bias(dev_in(x).t, dev_in(dy).t, w.shape, st, pad, dw=dw.t, db=db.t)
+    sync_check(cb)
+    assert dw.guards_intact() and db.guards_intact()
+    assert_within_tol(dw.numpy(), ref_w, ref_w_abs, "conv_bwd_filter_bias dw %s" % (shape,))
+    assert_within_tol(db.numpy(), ref_b, ref_b_abs, "conv_bwd_filter_bias db %s" % (shape,))
+
+
 @pytest.mark.parametrize("shape", CONV_SHAPES[:4])
 def test_conv_bwd_bias(cb, orc, shape):
     _, _, _, dy = conv_inputs(shape, 400)
