@@ -16,6 +16,7 @@ bounded sample of the same workload instead (host cores only).
 from __future__ import annotations
 
 import argparse
+import re
 import json
 import os
 import statistics
@@ -299,11 +300,16 @@ def run_ours(args):
     bf16, hbm, peak_kind = peaks()
     peak = bf16 * TF32_OVER_BF16 / SPLIT_PRODUCTS
     achieved = flops / (gemm_ms * 1e-3) / 1e12
+    # DRAM bytes (read + write) of the GEMM kernels in one step, from the ncu
+    # launch list summarised in profiles/ (a "conv_gemm_dram_bytes_per_step = N"
+    # line); absent -> null
     traffic = None
-    prof = os.path.join(ROOT, "profiles", "traffic.json")
+    prof = os.path.join(ROOT, "profiles", "launch_list_alexnet_b128_step.md")
     if os.path.exists(prof):
         with open(prof) as f:
-            traffic = json.load(f).get("conv_gemm_bytes_per_step")
+            m = re.search(r"conv_gemm_dram_bytes_per_step = (\d+)", f.read())
+        if m:
+            traffic = int(m.group(1))
 
     # --- end to end through the public API with host buffers ---------------
     pin = lambda a: torch.from_numpy(a).pin_memory()

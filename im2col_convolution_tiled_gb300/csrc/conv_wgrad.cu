@@ -159,14 +159,20 @@ struct GradGen {
     }
 };
 
-// out[row] = sum over block i (ascending) of rowsum[row * blocks + i].
+// out[row] = sum of rowsum[row * blocks + i] over the blocks i: one warp per
+// row, lane l adding blocks l, l + 32, ... in order, then a fixed shuffle tree
+// (deterministic).
 __global__ void rowsum_final_kernel(const float* __restrict__ rowsum, int blocks, int rows, float* __restrict__ out)
 {
-    const int row = blockIdx.x * blockDim.x + threadIdx.x;
-    if (row >= rows) return;
+    const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;   // whole warps leave together
+    const float* src = rowsum + size_t(row) * blocks;
     float acc = 0.f;
-    for (int i = 0; i < blocks; ++i) acc += __ldg(rowsum + size_t(row) * blocks + i);
-    out[row] = acc;
+    for (int i = lane; i < blocks; i += 32) acc += __ldg(src + i);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) out[row] = acc;
 }
 
 // dW[i] = sum over split s (ascending) of part[s][i].
@@ -325,7 +331,7 @@ static cudaError_t run_wgrad(const ConvDims& d, const WgradPlan& pl, const float
                                  db ? rowsum : nullptr);
     if (e != cudaSuccess) return e;
     if (db) {
-        rowsum_final_kernel<<<(d.K + 127) / 128, 128, 0, st>>>(rowsum, bimage_grid_x(p.NPQ), d.K, db);
+        rowsum_final_kernel<<<(d.K + 7) / 8, 256, 0, st>>>(rowsum, bimage_grid_x(p.NPQ), d.K, db);
         note_launch();
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
