@@ -90,6 +90,7 @@ CONV_SHAPES = [
     # 192-column GEMMs are split along K and their partial tiles added by the reduce kernel
     (16, 64, 35, 35, 192, 3, 1, 1),    # forward: 192 filters
     (16, 192, 35, 35, 64, 3, 1, 1),    # input gradient: 192 columns
+    (2, 24, 11, 11, 100, 3, 1, 1),     # 100 filters: 128-wide filter-gradient tiles (A in tensor memory)
 ]
 
 
