@@ -382,6 +382,113 @@ __global__ void __launch_bounds__(kPoolThreads, 4) maxpool_bwd_staged_kernel(
     }
 }
 
+// Column walker for the common window shapes (K x K, stride S, K and S
+// compile-time).  A work item is (plane, output column ow, segment
+// of output rows); the thread walks down its rows keeping the maxima of the
+// last K input rows (each the first maximum of its K columns, strict >) in
+// registers.  Window oh combines the maxima of rows oh*S .. oh*S + K - 1 in
+// row order (first strictly greater wins), which is exactly the first
+// maximum of the window in row-major order; the next window reuses K - S of
+// them, so a window costs S*K shared loads instead of K*K.
+template <int K, int S>
+__global__ void __launch_bounds__(kPoolThreads, 3) maxpool_fwd_cols_kernel(
+    const float* __restrict__ x, float* __restrict__ y, int32_t* __restrict__ idx, int NC, int H, int W, int P,
+    int Q, int ppb, int stage_floats, int nseg, int seglen, FastDiv f_seg, FastDiv f_q, int* err)
+{
+    static_assert(S <= K, "windows must overlap or touch");
+    extern __shared__ __align__(16) float pool_smem[];
+    __shared__ uint64_t bar[2];
+    __shared__ int abort_flag;
+    const int HW = H * W, PQ = P * Q;
+    const long long total = (long long)NC * HW;
+    const int groups = (NC + ppb - 1) / ppb;
+    auto issue = [&](int g, int b) {
+        const int nc0 = g * ppb, np = min(ppb, NC - nc0);
+        const long long start = (long long)nc0 * HW;
+        mbar_arrive_expect_tx(&bar[b], stage_range_bytes(start, np * HW, total));
+        stage_range(pool_smem + b * stage_floats, x, start, np * HW, total, &bar[b]);
+    };
+    if (threadIdx.x == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        abort_flag = 0;
+        mbar_fence_init();
+        for (int i = 0; i < 2; ++i)
+            if (int(blockIdx.x) + i * int(gridDim.x) < groups) issue(blockIdx.x + i * gridDim.x, i);
+    }
+    __syncthreads();
+    int i = 0, g = blockIdx.x;
+    for (; g < groups; g += gridDim.x, ++i) {
+        const int b = i & 1;
+        if (!stage_wait(&bar[b], uint32_t(i >> 1) & 1u, &abort_flag, err)) break;
+        const int nc0 = g * ppb, np = min(ppb, NC - nc0);
+        const float* sx = pool_smem + b * stage_floats + ((long long)nc0 * HW & 3);
+        const int items = np * Q * nseg;
+        for (int it = threadIdx.x; it < items; it += kPoolThreads) {
+            uint32_t rest, seg, pl, ow;
+            f_q.divmod(uint32_t(it), rest, ow);   // it = (pl * nseg + seg) * Q + ow: a warp stores along ow
+            f_seg.divmod(rest, pl, seg);
+            const int oh0 = int(seg) * seglen;
+            const int oh1 = min(oh0 + seglen, P);
+            const int plane = int(pl) * HW;
+            const int c0 = int(ow) * S;
+            float rm[K];
+            int ri[K];
+            auto row_max = [&](int h, float& m, int& at) {
+                const int base = plane + h * W + c0;
+                m = sx[base];
+                at = base;
+#pragma unroll
+                for (int c = 1; c < K; ++c) {
+                    const float v = sx[base + c];
+                    if (v > m) {
+                        m = v;
+                        at = base + c;
+                    }
+                }
+            };
+            for (int oh = oh0; oh < oh1; ++oh) {
+                if (oh == oh0) {
+#pragma unroll
+                    for (int r = 0; r < K; ++r) row_max(oh * S + r, rm[r], ri[r]);
+                } else {
+#pragma unroll
+                    for (int r = 0; r < K - S; ++r) {
+                        rm[r] = rm[r + S];
+                        ri[r] = ri[r + S];
+                    }
+#pragma unroll
+                    for (int r = K - S; r < K; ++r) row_max(oh * S + r, rm[r], ri[r]);
+                }
+                float m = rm[0];
+                int at = ri[0];
+#pragma unroll
+                for (int r = 1; r < K; ++r)
+                    if (rm[r] > m) {
+                        m = rm[r];
+                        at = ri[r];
+                    }
+                const size_t o = size_t(nc0) * PQ + size_t(pl) * PQ + size_t(oh) * Q + ow;
+                y[o] = m;
+                idx[o] = nc0 * HW + at;
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x == 0 && g + 2 * int(gridDim.x) < groups) {
+            fence_proxy_async_smem();
+            issue(g + 2 * gridDim.x, b);
+        }
+    }
+    if (abort_flag && threadIdx.x == 0) {
+        for (int j = 0; j < 2 && g + j * int(gridDim.x) < groups; ++j) {
+            uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(&bar[(i + j) & 1], uint32_t((i + j) >> 1) & 1u) &&
+                   globaltimer_ns() - t0 < kWaitLimitNs) {
+            }
+        }
+    }
+}
+
 // Blocks per SM for a staged kernel using `smem` bytes of dynamic shared memory.
 static int staged_grid(int groups, size_t smem)
 {
@@ -400,12 +507,49 @@ static int staged_grid(int groups, size_t smem)
     return groups < cap ? groups : cap;
 }
 
+// Segment length (in output rows) that gives about kPoolThreads work items
+// for `cols` columns per staged group, so every thread walks a few rows.
+static int pool_seglen(int rows, int cols)
+{
+    int nseg = (kPoolThreads + cols - 1) / cols;
+    if (nseg > rows) nseg = rows;
+    if (nseg < 1) nseg = 1;
+    return (rows + nseg - 1) / nseg;
+}
+
+template <int K, int S>
+static cudaError_t launch_pool_fwd_cols(int NC, int H, int W, int P, int Q, const float* x, float* y, int32_t* idx,
+                                        cudaStream_t st)
+{
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(maxpool_fwd_cols_kernel<K, S>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int HW = H * W;
+    const int ppb = (kPoolStageFloats - 4) / HW < 64 ? (kPoolStageFloats - 4) / HW : 64;
+    const int stage = (ppb * HW + 4 + 3) & ~3;
+    const size_t smem = 2 * size_t(stage) * sizeof(float);
+    const int groups = (NC + ppb - 1) / ppb;
+    const int seglen = pool_seglen(P, ppb * Q);
+    const int nseg = (P + seglen - 1) / seglen;
+    maxpool_fwd_cols_kernel<K, S><<<staged_grid(groups, smem), kPoolThreads, smem, st>>>(
+        x, y, idx, NC, H, W, P, Q, ppb, stage, nseg, seglen, FastDiv(uint32_t(nseg)), FastDiv(uint32_t(Q)),
+        device_error_word());
+    note_launch();
+    return cudaGetLastError();
+}
+
 cudaError_t launch_maxpool_fwd(int N, int C, int H, int W, int k, int s, int P, int Q, const float* x, float* y,
                                int32_t* idx, cudaStream_t st)
 {
     const int NC = N * C;
     const int HW = H * W;
     if (HW + 4 <= kPoolStageFloats) {
+        if (k == 3 && s == 2) return launch_pool_fwd_cols<3, 2>(NC, H, W, P, Q, x, y, idx, st);
+        if (k == 2 && s == 2) return launch_pool_fwd_cols<2, 2>(NC, H, W, P, Q, x, y, idx, st);
         const int ppb = (kPoolStageFloats - 4) / HW < 64 ? (kPoolStageFloats - 4) / HW : 64;
         const int stage = (ppb * HW + 4 + 3) & ~3;   // floats per buffer (room for the 16-byte shift)
         const size_t smem = 2 * size_t(stage) * sizeof(float);

@@ -247,7 +247,9 @@ POOL_CASES = [((4, 6, 28, 28), 2, 2), ((4, 16, 10, 10), 2, 2), ((2, 64, 55, 55),
               # backward owner blocks: S = 3 with k = S, odd widths whose last block runs past the row end,
               # windows wider than stride + 1, a 2-wide grid, stride 1, and stride 4 (plain gather kernel)
               ((2, 5, 11, 13), 3, 3), ((2, 4, 7, 9), 4, 2), ((1, 3, 4, 5), 3, 2), ((2, 3, 6, 6), 2, 1),
-              ((1, 2, 13, 13), 3, 4)]
+              ((1, 2, 13, 13), 3, 4),
+              # forward column walker (3x3 and 2x2, stride 2): rows below the last window (H = 8), a narrow width
+              ((2, 3, 8, 9), 3, 2), ((1, 2, 7, 4), 3, 2)]
 
 
 @pytest.mark.parametrize("shape,k,s", POOL_CASES)
