@@ -27,7 +27,167 @@ static int grid_for(long long work, int per_block)
 }
 
 // ---------------------------------------------------------------------------
+// Staging of a contiguous element range into shared memory by the bulk-copy
+// engine (used by the band col2im and the staged pooling kernels).
+
+// Thread 0: copy elements [start, start + count) of a tensor of `total`
+// elements into dst so that element start + i lands at dst[(start & 3) + i].
+// The tensor base is 16-byte aligned, so the bulk copy covers whole 16-byte
+// blocks; up to 3 elements past the tensor's last 16-byte boundary are
+// loaded with plain loads.  Returns the bulk-copied bytes.
+__device__ __forceinline__ uint32_t stage_range_bytes(long long start, int count, long long total)
+{
+    const long long a0 = start & ~3LL;
+    long long a1 = (start + count + 3) & ~3LL;
+    const long long lim = total & ~3LL;
+    if (a1 > lim) a1 = lim;
+    return a1 > a0 ? uint32_t((a1 - a0) * 4) : 0u;
+}
+
+__device__ __forceinline__ void stage_range(float* dst, const float* base, long long start, int count, long long total,
+                                            uint64_t* bar)
+{
+    const long long a0 = start & ~3LL;
+    const uint32_t bytes = stage_range_bytes(start, count, total);
+    const long long a1 = a0 + bytes / 4;
+    for (long long e = a1 > start ? a1 : start; e < start + count; ++e) dst[e - a0] = __ldg(base + e);
+    if (bytes) bulk_g2s(dst, base + a0, bytes, bar);
+}
+
+// Bounded wait by every thread of the block on a staging barrier.  The
+// outcome is agreed block-wide (a barrier every thread reaches), so either all
+// threads go on or all leave the loop together; on give-up the device error
+// word is set.
+__device__ __forceinline__ bool stage_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err)
+{
+    const bool got = mbar_wait(bar, parity, abort_flag);
+    if (__syncthreads_and(got ? 1 : 0)) return true;
+    if (threadIdx.x == 0) {
+        *abort_flag = 1;
+        atomicOr(err, kDevErrTimeout);
+    }
+    return false;
+}
+
+// ---------------------------------------------------------------------------
 // im2col: col[(c, r, q)][(n, oh, ow)] = x[n, c, oh*s + r - pad, ow*s + q - pad].
+//
+// Staged form.  A block owns one (n, c) plane and a band of Pb output rows
+// oh0 .. oh0+Pb-1.  It copies the input rows that band reads -- (Pb-1)*s + R
+// of them, Wn = (Q-1)*s + R padded columns each, zeros outside the image -- to
+// shared memory once, then writes, for each of the R*R filter taps (r, q), the
+// contiguous run of Pb*Q columns of col row (c, r, q) that belong to the band:
+// every global store is coalesced and every input element is read from HBM
+// once per band.  Each staged row is split by column phase (padded column
+// u goes to phase u % s, slot u / s), so the stride-s reads of one tap are
+// consecutive shared addresses for any s.  A thread owns up to kIm2colPer
+// fixed positions j = tid + k*blockDim of the band, whose shared offsets are
+// the same for every tap up to a tap constant.
+
+constexpr int kIm2colThreads = 256;
+constexpr int kIm2colPer = 4;
+constexpr size_t kIm2colSmem = 32 * 1024;
+
+// Band of pb output rows of one image, or (pb == P) whole images, nb of them
+// per block, when a plane is small: the nb images' columns of one col row
+// are contiguous too, and a block then has enough positions to amortise its
+// set-up.
+struct Im2colBand {
+    int pb = 0, nband = 0, nb = 0, rows = 0, wph = 0;
+    size_t smem = 0;
+};
+
+static Im2colBand plan_im2col(const ConvDims& d)
+{
+    Im2colBand b;
+    const int wn = (d.Q - 1) * d.S + d.R;
+    b.wph = (wn + d.S - 1) / d.S;
+    auto smem_of = [&](int p) { return size_t((p - 1) * d.S + d.R) * d.S * b.wph * sizeof(float); };
+    const int cap = kIm2colThreads * kIm2colPer;
+    if ((long long)d.P * d.Q <= cap && smem_of(d.P) <= kIm2colSmem) {
+        int nb = 1;
+        while (nb < d.N && (long long)(nb + 1) * d.P * d.Q <= cap && (nb + 1) * smem_of(d.P) <= kIm2colSmem) ++nb;
+        b.nb = nb;
+        b.pb = d.P;
+        b.nband = 1;
+    } else {
+        int pb = std::min(d.P, cap / std::max(d.Q, 1));
+        while (pb > 1 && smem_of(pb) > kIm2colSmem) --pb;
+        if (pb < 1 || smem_of(pb) > 160 * 1024) return b;  // pb == 0: no staged form
+        b.nband = (d.P + pb - 1) / pb;
+        b.pb = (d.P + b.nband - 1) / b.nband;
+        b.nb = 1;
+    }
+    b.rows = (b.pb - 1) * d.S + d.R;
+    b.smem = b.nb * smem_of(b.pb);
+    return b;
+}
+
+__global__ void __launch_bounds__(kIm2colThreads) im2col_band_kernel(const float* __restrict__ x,
+                                                                     float* __restrict__ col, int N, int C, int H,
+                                                                     int W, int S, int R, int pad, int P, int Q,
+                                                                     int pb, int nband, int nb, int rows, int wph,
+                                                                     FastDiv f_s, FastDiv f_q, FastDiv f_iq,
+                                                                     long long npq)
+{
+    extern __shared__ float tile[];
+    // block = (group * C + c) * nband + band
+    const int band = blockIdx.x % nband;
+    const int rest = blockIdx.x / nband;
+    const int c = rest % C;
+    const int n0 = (rest / C) * nb;
+    const int nbi = min(nb, N - n0);
+    const int oh0 = band * pb;
+    const int nrow = min(pb, P - oh0);
+    const int h0 = oh0 * S - pad;
+    const int wn = (Q - 1) * S + R;
+    const int rowf = S * wph;          // floats per staged row
+    const int imgf = rows * rowf;      // floats per staged image
+
+    // stage rows h0 .. h0+rows-1 of each image, padded columns 0 .. wn-1 (w = u - pad)
+    for (int ra = threadIdx.x >> 5; ra < nbi * rows; ra += kIm2colThreads / 32) {
+        const int img = ra / rows, hl = ra - img * rows;
+        const int h = h0 + hl;
+        const bool hin = unsigned(h) < unsigned(H);
+        const float* xr = x + ((size_t(n0) + img) * C + c) * size_t(H) * W + size_t(h) * W;
+        float* trow = tile + size_t(img) * imgf + size_t(hl) * rowf;
+        for (int u = threadIdx.x & 31; u < wn; u += 32) {
+            const int w = u - pad;
+            const float v = (hin && unsigned(w) < unsigned(W)) ? __ldg(xr + w) : 0.f;
+            uint32_t slot, ph;
+            f_s.divmod(uint32_t(u), slot, ph);
+            trow[ph * wph + slot] = v;
+        }
+    }
+    __syncthreads();
+
+    // position j = (img, oh_l, ow); tap (r, q) reads slot
+    // img*imgf + (oh_l*s + r)*rowf + (q % s)*wph + ow + q / s
+    const int nj = (nbi - 1) * P * Q + nrow * Q;
+    int base[kIm2colPer];
+#pragma unroll
+    for (int k = 0; k < kIm2colPer; ++k) {
+        const int j = threadIdx.x + k * kIm2colThreads;
+        uint32_t img, rem, ohl, ow;
+        f_iq.divmod(uint32_t(j < nj ? j : 0), img, rem);
+        f_q.divmod(rem, ohl, ow);
+        base[k] = j < nj ? int(img) * imgf + int(ohl) * S * rowf + int(ow) : -1;
+    }
+    float* dst = col + size_t(c) * R * R * npq + size_t(n0) * P * Q + size_t(oh0) * Q;
+    for (int r = 0; r < R; ++r) {
+        for (int q = 0; q < R; ++q) {
+            uint32_t qs, qp;
+            f_s.divmod(uint32_t(q), qs, qp);
+            const int toff = r * rowf + int(qp) * wph + int(qs);
+#pragma unroll
+            for (int k = 0; k < kIm2colPer; ++k)
+                if (base[k] >= 0) dst[threadIdx.x + k * kIm2colThreads] = tile[base[k] + toff];
+            dst += npq;
+        }
+    }
+}
+
+// Unstaged form, for shapes whose band does not fit shared memory.
 // One thread writes 4 consecutive columns of one row (a 16-byte store when
 // the row length NPQ is a multiple of 4); its (n, oh, ow) is decoded once and
 // advanced incrementally.
@@ -89,6 +249,20 @@ cudaError_t launch_im2col(const ConvDims& d, const float* x, float* col, cudaStr
     const int NPQ = d.N * d.P * d.Q;
     const int CRS = d.C * d.R * d.R;
     const FastDiv f_pq(d.P * d.Q), f_q(d.Q), f_rr(d.R * d.R), f_r(d.R);
+    const Im2colBand b = plan_im2col(d);
+    const long long blocks = (long long)((d.N + std::max(b.nb, 1) - 1) / std::max(b.nb, 1)) * d.C * b.nband;
+    if (b.pb > 0 && blocks <= INT32_MAX) {
+        if (b.smem > 48 * 1024) {
+            const cudaError_t e = cudaFuncSetAttribute(im2col_band_kernel,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, int(b.smem));
+            if (e != cudaSuccess) return e;
+        }
+        im2col_band_kernel<<<unsigned(blocks), kIm2colThreads, b.smem, st>>>(
+            x, col, d.N, d.C, d.H, d.W, d.S, d.R, d.pad, d.P, d.Q, b.pb, b.nband, b.nb, b.rows, b.wph,
+            FastDiv(d.S), FastDiv(d.Q), FastDiv(b.pb * d.Q), NPQ);
+        note_launch();
+        return cudaGetLastError();
+    }
     if (NPQ % 4 == 0) {
         const long long total4 = (long long)CRS * (NPQ / 4);
         im2col_kernel<<<grid_for(total4, 256), 256, 0, st>>>(x, col, d.C, d.H, d.W, d.S, d.pad, d.P, d.Q, f_pq,
@@ -104,38 +278,287 @@ cudaError_t launch_im2col(const ConvDims& d, const float* x, float* col, cudaStr
 }
 
 // ---------------------------------------------------------------------------
-// col2im as a gather: dx[n, c, h, w] = sum over taps r == (h + pad) mod s
-// (ascending), q likewise, of col[(c, r, q)][(n, (h + pad - r)/s, (w + pad - q)/s)]
-// where that output position exists.  One thread per dx element, fixed order.
+// col2im as a gather: dx[n, c, h, w] = sum of col[(c, r, q)][(n, oh, ow)] over
+// the taps with oh*s + r - pad = h and ow*s + q - pad = w.  With hp = h + pad
+// those are r = hp % s + i*s, oh = hp / s - i (and q, ow alike from wp = w +
+// pad) for i, j < ceil(R/s), kept when r, q < R and oh, ow fall inside the
+// output.  Every thread walks the same (i, j) schedule, masked at the edges,
+// so in each step the lanes of a warp that share wp % s read consecutive ow
+// of one col row: the reads are coalesced for any stride.  The terms arrive
+// in ascending (r, q) order -- a fixed order, so the result is deterministic
+// -- and eight loads are issued before the first add.
 
 __global__ void col2im_kernel(const float* __restrict__ col, float* __restrict__ dx, int R, int S, int pad, int P,
-                              int Q, int NPQ, FastDiv f_w, FastDiv f_h, FastDiv f_c, int total)
+                              int Q, long long npq, FastDiv f_s, FastDiv f_w, FastDiv f_h, FastDiv f_c, int total)
 {
+    const int steps = (R + S - 1) / S;
+    const int taps = steps * steps;
     for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < total; t += gridDim.x * blockDim.x) {
         uint32_t r1, w, r2, h, n, c;
         f_w.divmod(uint32_t(t), r1, w);
         f_h.divmod(r1, r2, h);
         f_c.divmod(r2, n, c);
-        const int hp = int(h) + pad, wp = int(w) + pad;
+        uint32_t ohb, r0, owb, q0;
+        f_s.divmod(h + uint32_t(pad), ohb, r0);
+        f_s.divmod(w + uint32_t(pad), owb, q0);
+        // element (i, j): col row (c*R + r0 + i*s)*R + q0 + j*s, column (n*P + ohb - i)*Q + owb - j
+        const float* base = col + (size_t(c) * R * R + size_t(r0) * R + q0) * npq + (size_t(n) * P + ohb) * Q + owb;
         float acc = 0.f;
-        // taps with r <= h + pad only: oh = (h + pad - r) / S must be >= 0
-        for (int r = hp % S; r < R && r <= hp; r += S) {
-            const int oh = (hp - r) / S;
-            if (oh >= P) continue;
-            for (int q = wp % S; q < R && q <= wp; q += S) {
-                const int ow = (wp - q) / S;
-                if (ow >= Q) continue;
-                acc += __ldg(col + size_t((int(c) * R + r) * R + q) * NPQ + (int(n) * P + oh) * Q + ow);
+        int i = 0, j = 0;
+        for (int k0 = 0; k0 < taps; k0 += 8) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                v[u] = 0.f;
+                if (k0 + u < taps) {
+                    const int r = int(r0) + i * S, q = int(q0) + j * S;
+                    const int oh = int(ohb) - i, ow = int(owb) - j;
+                    if (r < R && q < R && oh >= 0 && oh < P && ow >= 0 && ow < Q)
+                        v[u] = __ldg(base + (size_t(i) * S * R + size_t(j) * S) * npq - size_t(i) * Q - j);
+                    if (++j == steps) {
+                        j = 0;
+                        ++i;
+                    }
+                }
             }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) acc += v[u];
         }
         dx[t] = acc;
     }
 }
 
+// Staged col2im by residue class.  The taps that reach a dx element (h, w)
+// all have r = (h + pad) % s (mod s) and q = (w + pad) % s (mod s), so the
+// taps split into s*s classes (r0, q0), each of which is a stride-1 problem:
+// with a = (h + pad) / s and b = (w + pad) / s, the element sums
+// col[(c, r0 + i*s, q0 + j*s)][(n, a - i, b - j)] over i, j < ceil((R - r0)/s)
+// (and ceil((R - q0)/s)) wherever a - i, b - j fall inside the output.  Every
+// col row belongs to exactly one class.  A block owns one class of one
+// channel c for a band of A sub-rows a of one image, or for all sub-rows of
+// nb consecutive images; for each of its taps it needs one contiguous run of
+// the col row (output rows oa .. ob-1 with a halo of ceil(R/s) - 1 rows, or
+// whole images), which one lane of warp 0 stages with a bulk copy.  After
+// one bounded wait every thread sums its dx elements from shared memory, taps in
+// ascending (r, q) order -- a fixed order, so the result is deterministic --
+// and writes them once.
+
+// One item per block: a block stages its item with bulk copies, waits once,
+// sums, and exits; three blocks share an SM, so one block's copies overlap
+// the others' sums.  (A persistent form with two stages and one block per SM
+// measured 1.6x slower: every item then ends in a block-wide barrier that the
+// whole SM waits at.)
+constexpr int kCol2imThreads = 256;
+constexpr size_t kCol2imStage = 74 * 1024;  // three blocks per SM
+constexpr int kCol2imMaxPix = 2048;         // dx elements per item when whole images are grouped
+
+struct Col2imPlan {
+    int steps = 0, U = 0, V = 0, A = 0, nband = 0, nb = 0, seg = 0, items = 0;
+    size_t smem = 0;
+};
+
+static Col2imPlan plan_col2im(const ConvDims& d)
+{
+    Col2imPlan p;
+    p.steps = (d.R + d.S - 1) / d.S;
+    p.U = (d.H + d.pad + d.S - 1) / d.S;
+    p.V = (d.W + d.pad + d.S - 1) / d.S;
+    const size_t taps = size_t(p.steps) * p.steps;
+    if (taps > 25) return p;  // nb == 0: the taps no longer fit in registers
+    const long long PQ = (long long)d.P * d.Q;
+    auto seg_of = [](long long count) { return (count + 8 + 3) & ~3LL; };
+    // one stage: the staged runs of every tap plus the table of their offsets
+    auto bytes_of = [&](long long count) { return taps * (size_t(seg_of(count)) * sizeof(float) + sizeof(int)); };
+    if (bytes_of(PQ) <= kCol2imStage) {
+        int nb = 1;
+        while (nb < d.N && bytes_of((nb + 1) * PQ) <= kCol2imStage &&
+               (long long)(nb + 1) * p.U * p.V <= kCol2imMaxPix)
+            ++nb;
+        p.nb = nb;
+        p.A = p.U;
+        p.nband = 1;
+        p.seg = int(seg_of(nb * PQ));
+    } else {
+        int A = p.U;
+        while (A > 1 && bytes_of((long long)std::min(d.P, A + p.steps - 1) * d.Q) > kCol2imStage) --A;
+        if (bytes_of((long long)std::min(d.P, A + p.steps - 1) * d.Q) > kCol2imStage) return p;  // nb == 0: none
+        p.nband = (p.U + A - 1) / A;
+        p.A = (p.U + p.nband - 1) / p.nband;
+        p.nb = 1;
+        p.seg = int(seg_of((long long)std::min(d.P, p.A + p.steps - 1) * d.Q));
+    }
+    const long long items = (long long)((d.N + p.nb - 1) / p.nb) * d.C * p.nband * d.S * d.S;
+    if (items > INT32_MAX) {
+        p.nb = 0;
+        return p;
+    }
+    p.items = int(items);
+    p.smem = taps * (size_t(p.seg) * sizeof(float) + sizeof(int));
+    return p;
+}
+
+struct Col2imArgs {
+    const float* col;
+    float* dx;
+    int N, C, H, W, S, R, pad, P, Q;
+    long long npq, total;
+    int steps, A, nband, nb, seg, items;
+    FastDiv f_v, f_av;
+    int* err;
+};
+
+// One work item: class cls of channel c, sub-row band `band`, images n0 .. n0+nbi-1.
+struct Col2imItem {
+    int n0, nbi, c, r0, q0, ni, nj, a0, oa, ob, count;
+    long long start;
+    __device__ Col2imItem(const Col2imArgs& g, int item)
+    {
+        const int SS = g.S * g.S;
+        const int cls = item % SS;
+        int rest = item / SS;
+        const int band = rest % g.nband;
+        rest /= g.nband;
+        c = rest % g.C;
+        n0 = (rest / g.C) * g.nb;
+        nbi = min(g.nb, g.N - n0);
+        r0 = cls / g.S;
+        q0 = cls - r0 * g.S;
+        ni = (g.R - r0 + g.S - 1) / g.S;
+        nj = (g.R - q0 + g.S - 1) / g.S;
+        a0 = band * g.A;
+        oa = max(0, a0 - g.steps + 1);
+        ob = min(g.P, a0 + g.A);
+        start = (long long)n0 * g.P * g.Q + (long long)oa * g.Q;
+        count = (nbi - 1) * g.P * g.Q + max(ob - oa, 0) * g.Q;
+    }
+    __device__ long long tap_start(const Col2imArgs& g, int i, int j) const
+    {
+        return (((long long)c * g.R + r0 + i * g.S) * g.R + q0 + j * g.S) * g.npq + start;
+    }
+};
+
+// Sum the dx elements of one staged item whose class has NI x NJ taps.  The
+// tap offsets live in registers.  Every element takes the same predicated
+// sequence -- a tap counts when its output row a - i and column b - j lie
+// inside the output -- so the lanes of a warp never diverge between an
+// interior and an edge path.  Terms are added in ascending (i, j), i.e.
+// ascending (r, q), order.
+template <int NI, int NJ>
+__device__ __forceinline__ void col2im_sum_item(const Col2imArgs& g, const Col2imItem& it, const float* buf,
+                                                const int* tadj)
+{
+    constexpr int NT = NI * NJ > 0 ? NI * NJ : 1;
+    int tr[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) tr[t] = t < NI * NJ ? tadj[t] : 0;
+    const int PQ = g.P * g.Q, HW = g.H * g.W, CHW = g.C * HW;
+    float* out = g.dx + (size_t(it.n0) * g.C + it.c) * size_t(HW);
+    const int npix = it.nbi * g.A * int(g.f_v.d);
+    for (int px = threadIdx.x; px < npix; px += kCol2imThreads) {
+        uint32_t img, rem, al, bb;
+        g.f_av.divmod(uint32_t(px), img, rem);
+        g.f_v.divmod(rem, al, bb);
+        const int a = it.a0 + int(al), b = int(bb);
+        const int h = a * g.S + it.r0 - g.pad, w = b * g.S + it.q0 - g.pad;
+        if (a >= it.a0 + g.A || h < 0 || h >= g.H || w < 0 || w >= g.W) continue;
+        const float* e = buf + (int(img) * PQ + (a - it.oa) * g.Q + b);
+        bool vi[NI > 0 ? NI : 1], vj[NJ > 0 ? NJ : 1];
+#pragma unroll
+        for (int i = 0; i < NI; ++i) vi[i] = unsigned(a - i) < unsigned(g.P);
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) vj[j] = unsigned(b - j) < unsigned(g.Q);
+        float acc = 0.f;
+#pragma unroll
+        for (int i = 0; i < NI; ++i)
+#pragma unroll
+            for (int j = 0; j < NJ; ++j)
+                if (vi[i] && vj[j]) acc += e[tr[i * NJ + j]];
+        out[int(img) * CHW + h * g.W + w] = acc;
+    }
+}
+
+// Block = one item.  The 32 lanes of warp 0 issue the item's copies, one tap
+// per lane; every thread then waits (bounded) for them and sums.  Shared
+// memory holds three blocks per SM; telling the compiler so (rather than
+// letting it aim at more blocks with fewer registers) lets it schedule the
+// shared loads of a dx element further ahead: 1.4x faster as measured.
+// ST = ceil(R/s): the taps of a class are ST or ST - 1 along each axis.
+template <int ST>
+__global__ void __launch_bounds__(kCol2imThreads, 3) col2im_class_kernel(const __grid_constant__ Col2imArgs g)
+{
+    extern __shared__ __align__(16) float c2i_smem[];
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    const int taps_max = g.steps * g.steps;
+    float* buf = c2i_smem;
+    // tadj[t] for tap t = i*nj + j is the buffer offset of (image 0, output row
+    // oa, column 0) minus i*Q + j, so that the element a dx position (img, a, b)
+    // takes from tap t sits at tadj[t] + img*PQ + (a - oa)*Q + b.
+    int* tadj = reinterpret_cast<int*>(c2i_smem + size_t(taps_max) * g.seg);
+    const Col2imItem it(g, blockIdx.x);
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        const int nt = it.ni * it.nj;
+        uint32_t bytes = 0;
+        for (int t = lane; t < nt; t += 32)
+            bytes += stage_range_bytes(it.tap_start(g, t / it.nj, t % it.nj), it.count, g.total);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+        if (lane == 0) mbar_arrive_expect_tx(&bar, bytes);
+        __syncwarp();
+        for (int t = lane; t < nt; t += 32) {
+            const int i = t / it.nj, j = t % it.nj;
+            const long long st = it.tap_start(g, i, j);
+            tadj[t] = t * g.seg + int(st & 3) - i * g.Q - j;
+            if (it.count > 0) stage_range(buf + size_t(t) * g.seg, g.col, st, it.count, g.total, &bar);
+        }
+    }
+    if (!stage_wait(&bar, 0, &abort_flag, g.err)) return;
+    // a class has ST or ST - 1 taps along each axis
+    if (it.ni == ST && it.nj == ST)
+        col2im_sum_item<ST, ST>(g, it, buf, tadj);
+    else if (it.ni == ST)
+        col2im_sum_item<ST, ST - 1>(g, it, buf, tadj);
+    else if (it.nj == ST)
+        col2im_sum_item<ST - 1, ST>(g, it, buf, tadj);
+    else
+        col2im_sum_item<ST - 1, ST - 1>(g, it, buf, tadj);
+}
+
 cudaError_t launch_col2im(const ConvDims& d, const float* col, float* dx, cudaStream_t st)
 {
+    const long long NPQ = (long long)d.N * d.P * d.Q;
+    const Col2imPlan p = plan_col2im(d);
+    if (p.nb > 0 && (reinterpret_cast<uintptr_t>(col) & 15) == 0) {
+        Col2imArgs g{col, dx, d.N, d.C, d.H, d.W, d.S, d.R, d.pad, d.P, d.Q, NPQ, NPQ * d.C * d.R * d.R,
+                     p.steps, p.A, p.nband, p.nb, p.seg, p.items, FastDiv(p.V), FastDiv(p.A * p.V),
+                     device_error_word()};
+        auto run = [&](auto kern) {
+            if (p.smem > 48 * 1024) {
+                const cudaError_t e =
+                    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(p.smem));
+                if (e != cudaSuccess) return e;
+            }
+            kern<<<p.items, kCol2imThreads, p.smem, st>>>(g);
+            return cudaSuccess;
+        };
+        const cudaError_t e = p.steps == 1   ? run(col2im_class_kernel<1>)
+                              : p.steps == 2 ? run(col2im_class_kernel<2>)
+                              : p.steps == 3 ? run(col2im_class_kernel<3>)
+                              : p.steps == 4 ? run(col2im_class_kernel<4>)
+                                             : run(col2im_class_kernel<5>);
+        if (e != cudaSuccess) return e;
+        note_launch();
+        return cudaGetLastError();
+    }
     const long long total = (long long)d.N * d.C * d.H * d.W;
-    col2im_kernel<<<grid_for(total, 256), 256, 0, st>>>(col, dx, d.R, d.S, d.pad, d.P, d.Q, d.N * d.P * d.Q,
+    col2im_kernel<<<grid_for(total, 256), 256, 0, st>>>(col, dx, d.R, d.S, d.pad, d.P, d.Q, NPQ, FastDiv(d.S),
                                                         FastDiv(d.W), FastDiv(d.H), FastDiv(d.C), int(total));
     note_launch();
     return cudaGetLastError();
@@ -176,45 +599,6 @@ __global__ void maxpool_fwd_kernel(const float* __restrict__ x, float* __restric
 // few per SM) and take groups blockIdx.x, blockIdx.x + gridDim.x, ...
 constexpr int kPoolThreads = 512;
 constexpr int kPoolStageFloats = 6144;   // 24 KB per staged range
-
-// Thread 0: copy elements [start, start + count) of a tensor of `total`
-// elements into dst so that element start + i lands at dst[(start & 3) + i].
-// The tensor base is 16-byte aligned, so the bulk copy covers whole 16-byte
-// blocks; up to 3 elements past the tensor's last 16-byte boundary are
-// loaded with plain loads.  Returns the bulk-copied bytes.
-__device__ __forceinline__ uint32_t stage_range_bytes(long long start, int count, long long total)
-{
-    const long long a0 = start & ~3LL;
-    long long a1 = (start + count + 3) & ~3LL;
-    const long long lim = total & ~3LL;
-    if (a1 > lim) a1 = lim;
-    return a1 > a0 ? uint32_t((a1 - a0) * 4) : 0u;
-}
-
-__device__ __forceinline__ void stage_range(float* dst, const float* base, long long start, int count, long long total,
-                                            uint64_t* bar)
-{
-    const long long a0 = start & ~3LL;
-    const uint32_t bytes = stage_range_bytes(start, count, total);
-    const long long a1 = a0 + bytes / 4;
-    for (long long e = a1 > start ? a1 : start; e < start + count; ++e) dst[e - a0] = __ldg(base + e);
-    if (bytes) bulk_g2s(dst, base + a0, bytes, bar);
-}
-
-// Bounded wait by every thread of the block on a staging barrier.  The
-// outcome is agreed block-wide (a barrier every thread reaches), so either all
-// threads go on or all leave the loop together; on give-up the device error
-// word is set.
-__device__ __forceinline__ bool stage_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err)
-{
-    const bool got = mbar_wait(bar, parity, abort_flag);
-    if (__syncthreads_and(got ? 1 : 0)) return true;
-    if (threadIdx.x == 0) {
-        *abort_flag = 1;
-        atomicOr(err, kDevErrTimeout);
-    }
-    return false;
-}
 
 __global__ void __launch_bounds__(kPoolThreads, 4) maxpool_fwd_staged_kernel(
     const float* __restrict__ x, float* __restrict__ y, int32_t* __restrict__ idx, int NC, int H, int W, int k, int S,

@@ -209,7 +209,18 @@ def test_bwd_filter_and_bias_deterministic(cb):
 # ---------------------------------------------------------------------------
 # standalone im2col / col2im
 
-@pytest.mark.parametrize("shape", CONV_SHAPES[:4] + [(2, 2, 5, 7, 1, 3, 1, 1)])
+IM2COL_SHAPES = CONV_SHAPES[:4] + [
+    (2, 2, 5, 7, 1, 3, 1, 1),
+    (1, 2, 40, 300, 1, 3, 1, 1),       # 300 columns: output-row bands of 3, the last one short
+    (1, 1, 20, 500, 1, 5, 2, 2),       # stride 2, bands of 4 rows over 10
+    (1, 2, 50, 400, 1, 11, 4, 2),      # conv1-like stride 4, bands of 3 rows over 11
+    (3, 2, 19, 21, 1, 7, 2, 3),        # 7x7 stride 2: 4x4 taps per residue class, images grouped
+    (1, 1, 11, 4000, 1, 11, 1, 0),     # staged band too wide for shared memory, odd row length
+    (1, 1, 12, 4002, 1, 11, 1, 0),     # the same with a row length divisible by 4
+]
+
+
+@pytest.mark.parametrize("shape", IM2COL_SHAPES)
 def test_im2col_bit_exact(cb, orc, shape):
     N, C, H, W, K, R, st, pad = shape
     x = synthetic.normal((N, C, H, W), 600)
@@ -221,7 +232,7 @@ def test_im2col_bit_exact(cb, orc, shape):
     assert np.array_equal(col.numpy(), ref)
 
 
-@pytest.mark.parametrize("shape", CONV_SHAPES[:4] + [(2, 2, 5, 7, 1, 3, 1, 1)])
+@pytest.mark.parametrize("shape", IM2COL_SHAPES)
 def test_col2im(cb, orc, shape):
     N, C, H, W, K, R, st, pad = shape
     P, Q = out_size(H, R, st, pad), out_size(W, R, st, pad)
