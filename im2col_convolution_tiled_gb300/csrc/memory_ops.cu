@@ -86,7 +86,7 @@ __device__ __forceinline__ bool stage_wait(uint64_t* bar, uint32_t parity, volat
 
 constexpr int kIm2colThreads = 256;
 constexpr int kIm2colPer = 4;
-constexpr size_t kIm2colSmem = 32 * 1024;
+constexpr size_t kIm2colSmem = 72 * 1024;  // three blocks per SM
 
 // Band of pb output rows of one image, or (pb == P) whole images, nb of them
 // per block, when a plane is small: the nb images' columns of one col row
@@ -114,8 +114,22 @@ static Im2colBand plan_im2col(const ConvDims& d)
         int pb = std::min(d.P, cap / std::max(d.Q, 1));
         while (pb > 1 && smem_of(pb) > kIm2colSmem) --pb;
         if (pb < 1 || smem_of(pb) > 160 * 1024) return b;  // pb == 0: no staged form
-        b.nband = (d.P + pb - 1) / pb;
-        b.pb = (d.P + b.nband - 1) / b.nband;
+        // among the band heights that fit, take the one whose bands leave the
+        // fewest idle thread slots over the whole image (each band of nrow rows
+        // takes ceil(nrow*Q / threads) passes); ties go to the taller band
+        auto use = [&](int h) {
+            long long slots = 0;
+            for (int oh0 = 0; oh0 < d.P; oh0 += h) {
+                const long long pos = (long long)std::min(h, d.P - oh0) * d.Q;
+                slots += (pos + kIm2colThreads - 1) / kIm2colThreads * kIm2colThreads;
+            }
+            return double(d.P) * d.Q / double(slots);
+        };
+        int best = pb;
+        for (int h = pb - 1; h >= std::max(1, pb / 2); --h)
+            if (use(h) > use(best) + 0.01) best = h;
+        b.pb = best;
+        b.nband = (d.P + best - 1) / best;
         b.nb = 1;
     }
     b.rows = (b.pb - 1) * d.S + d.R;
@@ -123,14 +137,12 @@ static Im2colBand plan_im2col(const ConvDims& d)
     return b;
 }
 
-__global__ void __launch_bounds__(kIm2colThreads) im2col_band_kernel(const float* __restrict__ x,
-                                                                     float* __restrict__ col, int N, int C, int H,
-                                                                     int W, int S, int R, int pad, int P, int Q,
-                                                                     int pb, int nband, int nb, int rows, int wph,
-                                                                     FastDiv f_s, FastDiv f_q, FastDiv f_iq,
-                                                                     long long npq)
+__global__ void __launch_bounds__(kIm2colThreads, 6) im2col_band_kernel(
+    const float* __restrict__ x, float* __restrict__ col, int N, int C, int H, int W, int S, int R, int pad, int P,
+    int Q, int pb, int nband, int nb, int rows, int wph, FastDiv f_s, FastDiv f_q, FastDiv f_iq, FastDiv f_wn,
+    FastDiv f_rows, long long npq)
 {
-    extern __shared__ float tile[];
+    extern __shared__ __align__(16) float tile[];
     // block = (group * C + c) * nband + band
     const int band = blockIdx.x % nband;
     const int rest = blockIdx.x / nband;
@@ -140,25 +152,27 @@ __global__ void __launch_bounds__(kIm2colThreads) im2col_band_kernel(const float
     const int oh0 = band * pb;
     const int nrow = min(pb, P - oh0);
     const int h0 = oh0 * S - pad;
-    const int wn = (Q - 1) * S + R;
+    const int wn = int(f_wn.d);
     const int rowf = S * wph;          // floats per staged row
     const int imgf = rows * rowf;      // floats per staged image
 
-    // stage rows h0 .. h0+rows-1 of each image, padded columns 0 .. wn-1 (w = u - pad)
-    for (int ra = threadIdx.x >> 5; ra < nbi * rows; ra += kIm2colThreads / 32) {
-        const int img = ra / rows, hl = ra - img * rows;
-        const int h = h0 + hl;
-        const bool hin = unsigned(h) < unsigned(H);
-        const float* xr = x + ((size_t(n0) + img) * C + c) * size_t(H) * W + size_t(h) * W;
-        float* trow = tile + size_t(img) * imgf + size_t(hl) * rowf;
-        for (int u = threadIdx.x & 31; u < wn; u += 32) {
-            const int w = u - pad;
-            const float v = (hin && unsigned(w) < unsigned(W)) ? __ldg(xr + w) : 0.f;
-            uint32_t slot, ph;
-            f_s.divmod(uint32_t(u), slot, ph);
-            trow[ph * wph + slot] = v;
-        }
+    // stage rows h0 .. h0+rows-1 of each image, padded columns u = 0 .. wn-1
+    // (w = u - pad), zeros outside the image: element e = (img*rows + hl)*wn + u,
+    // one asynchronous 4-byte copy each
+    const size_t plane = size_t(H) * W;
+    const float* xc = x + (size_t(n0) * C + c) * plane;
+    const int ne = nbi * rows * wn;
+    for (int e = threadIdx.x; e < ne; e += kIm2colThreads) {
+        uint32_t ra, u, img, hl, slot, ph;
+        f_wn.divmod(uint32_t(e), ra, u);
+        f_rows.divmod(ra, img, hl);
+        f_s.divmod(u, slot, ph);
+        const int h = h0 + int(hl), w = int(u) - pad;
+        const bool in = unsigned(h) < unsigned(H) && unsigned(w) < unsigned(W);
+        const float* src = in ? xc + size_t(img) * C * plane + size_t(h) * W + w : x;
+        cp_async4_zfill(smem_u32(tile + int(img) * imgf + int(hl) * rowf + int(ph) * wph + int(slot)), src, in);
     }
+    cp_async_wait_all();
     __syncthreads();
 
     // position j = (img, oh_l, ow); tap (r, q) reads slot
@@ -173,16 +187,21 @@ __global__ void __launch_bounds__(kIm2colThreads) im2col_band_kernel(const float
         f_q.divmod(rem, ohl, ow);
         base[k] = j < nj ? int(img) * imgf + int(ohl) * S * rowf + int(ow) : -1;
     }
-    float* dst = col + size_t(c) * R * R * npq + size_t(n0) * P * Q + size_t(oh0) * Q;
+    float* dst = col + size_t(c) * R * R * npq + size_t(n0) * P * Q + size_t(oh0) * Q + threadIdx.x;
     for (int r = 0; r < R; ++r) {
+        int toff = r * rowf;  // r*rowf + (q % s)*wph + q / s, advanced with q
+        int qp = 0;
         for (int q = 0; q < R; ++q) {
-            uint32_t qs, qp;
-            f_s.divmod(uint32_t(q), qs, qp);
-            const int toff = r * rowf + int(qp) * wph + int(qs);
 #pragma unroll
             for (int k = 0; k < kIm2colPer; ++k)
-                if (base[k] >= 0) dst[threadIdx.x + k * kIm2colThreads] = tile[base[k] + toff];
+                if (base[k] >= 0) dst[k * kIm2colThreads] = tile[base[k] + toff];
             dst += npq;
+            if (++qp == S) {
+                qp = 0;
+                toff += 1 - (S - 1) * wph;
+            } else {
+                toff += wph;
+            }
         }
     }
 }
@@ -259,7 +278,7 @@ cudaError_t launch_im2col(const ConvDims& d, const float* x, float* col, cudaStr
         }
         im2col_band_kernel<<<unsigned(blocks), kIm2colThreads, b.smem, st>>>(
             x, col, d.N, d.C, d.H, d.W, d.S, d.R, d.pad, d.P, d.Q, b.pb, b.nband, b.nb, b.rows, b.wph,
-            FastDiv(d.S), FastDiv(d.Q), FastDiv(b.pb * d.Q), NPQ);
+            FastDiv(d.S), FastDiv(d.Q), FastDiv(b.pb * d.Q), FastDiv((d.Q - 1) * d.S + d.R), FastDiv(b.rows), NPQ);
         note_launch();
         return cudaGetLastError();
     }

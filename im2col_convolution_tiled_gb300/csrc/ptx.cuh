@@ -111,6 +111,15 @@ __device__ __forceinline__ void cp_async4(uint32_t smem_dst, const float* gmem_s
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_dst), "l"(gmem_src) : "memory");
 }
 
+// The same with zero fill: when `valid` is false nothing is read and the
+// destination word is written with 0 (the source pointer is then not used).
+__device__ __forceinline__ void cp_async4_zfill(uint32_t smem_dst, const float* gmem_src, bool valid)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_dst), "l"(gmem_src),
+                 "r"(valid ? 4 : 0)
+                 : "memory");
+}
+
 __device__ __forceinline__ void cp_async_wait_all()
 {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
