@@ -698,7 +698,7 @@ __global__ void __launch_bounds__(kPoolThreads, 4) maxpool_fwd_staged_kernel(
 // oracle's order) with a handful of compares per window and no per-pixel
 // division; the S*S results are written with coalesced stores.
 template <int S>
-__global__ void __launch_bounds__(kPoolThreads, 4) maxpool_bwd_staged_kernel(
+__global__ void __launch_bounds__(kPoolThreads, 3) maxpool_bwd_staged_kernel(
     const float* __restrict__ dy, const int32_t* __restrict__ idx, float* __restrict__ dx, int NC, int H, int W,
     int k, int P, int Q, int ppb, int stage_floats, int BH, int BW, FastDiv f_blk, FastDiv f_bw, int* err)
 {
@@ -893,18 +893,15 @@ __global__ void __launch_bounds__(kPoolThreads, 3) maxpool_fwd_cols_kernel(
 }
 
 // Blocks per SM for a staged kernel using `smem` bytes of dynamic shared memory.
-static int staged_grid(int groups, size_t smem)
+static int staged_grid(int groups, size_t smem, int max_per_sm = 4)
 {
     static bool attr_set = false;
     if (!attr_set) {
         cudaFuncSetAttribute(maxpool_fwd_staged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
-        cudaFuncSetAttribute(maxpool_bwd_staged_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
-        cudaFuncSetAttribute(maxpool_bwd_staged_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
-        cudaFuncSetAttribute(maxpool_bwd_staged_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
         attr_set = true;
     }
     int per_sm = int((200 * 1024) / (smem + 1024));
-    if (per_sm > 4) per_sm = 4;
+    if (per_sm > max_per_sm) per_sm = max_per_sm;
     if (per_sm < 1) per_sm = 1;
     const int cap = per_sm * sm_count();
     return groups < cap ? groups : cap;
@@ -1006,21 +1003,16 @@ cudaError_t launch_maxpool_bwd(int N, int C, int H, int W, int k, int s, int P, 
         const size_t smem = 4 * size_t(stage) * sizeof(float);
         const int groups = (NC + ppb - 1) / ppb;
         const int BH = (H + s - 1) / s, BW = (W + s - 1) / s;
-        const int grid = staged_grid(groups, smem);
+        const int grid = staged_grid(groups, smem, 3);  // three blocks per SM (register bound)
         const FastDiv f_blk{uint32_t(BH * BW)}, f_bw{uint32_t(BW)};
+        auto run = [&](auto kern) {
+            kern<<<grid, kPoolThreads, smem, st>>>(dy, idx, dx, NC, H, W, k, P, Q, ppb, stage, BH, BW, f_blk, f_bw,
+                                                   device_error_word());
+        };
         switch (s) {
-        case 1:
-            maxpool_bwd_staged_kernel<1><<<grid, kPoolThreads, smem, st>>>(dy, idx, dx, NC, H, W, k, P, Q, ppb, stage,
-                                                                           BH, BW, f_blk, f_bw, device_error_word());
-            break;
-        case 2:
-            maxpool_bwd_staged_kernel<2><<<grid, kPoolThreads, smem, st>>>(dy, idx, dx, NC, H, W, k, P, Q, ppb, stage,
-                                                                           BH, BW, f_blk, f_bw, device_error_word());
-            break;
-        default:
-            maxpool_bwd_staged_kernel<3><<<grid, kPoolThreads, smem, st>>>(dy, idx, dx, NC, H, W, k, P, Q, ppb, stage,
-                                                                           BH, BW, f_blk, f_bw, device_error_word());
-            break;
+        case 1: run(maxpool_bwd_staged_kernel<1>); break;
+        case 2: run(maxpool_bwd_staged_kernel<2>); break;
+        default: run(maxpool_bwd_staged_kernel<3>); break;
         }
         note_launch();
         return cudaGetLastError();
