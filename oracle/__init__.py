@@ -70,6 +70,13 @@ def _declare(lib):
         "oracle_maxpool_fwd": [_I64] * 8 + [_FP, _FP, _IP],
         "oracle_maxpool_bwd": [_I64] * 6 + [_FP, _IP, _FP],
         "oracle_sgd": [_I64, ctypes.c_float, ctypes.c_float, _FP, _FP],
+        "oracle_relu": [_I64, _FP, _FP],
+        "oracle_relu_grad": [_I64, _FP, _FP, _FP],
+        "oracle_add_bias": [_I64, _I64, _FP, _FP, _FP],
+        "oracle_bias_grad_rows": [_I64, _I64, _DP, _DP, _DP],
+        "oracle_softmax": [_I64, _I64, _DP, _DP],
+        "oracle_softmax_ce": [_I64, _I64, _DP, _IP, _DP, _DP],
+        "oracle_grad_accum": [_I64, _FP, _FP],
         "oracle_threads": [],
     }
     for name, args in sig.items():
@@ -277,6 +284,64 @@ class Oracle:
         assert p.shape == g.shape
         self.lib.oracle_sgd(p.size, lr, clip, _p(p, _FP), _p(g, _FP))
         return p
+
+    # -- training-step pieces (LeNet-5 step) -------------------------------------
+    def relu(self, x):
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        y = np.empty_like(x)
+        self.lib.oracle_relu(x.size, _p(x, _FP), _p(y, _FP))
+        return y
+
+    def relu_grad(self, grad, x):
+        g = np.ascontiguousarray(grad, dtype=np.float32)
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        assert g.shape == x.shape
+        dx = np.empty_like(g)
+        self.lib.oracle_relu_grad(g.size, _p(g, _FP), _p(x, _FP), _p(dx, _FP))
+        return dx
+
+    def add_bias(self, A, b):
+        A = np.ascontiguousarray(A, dtype=np.float32)
+        b = np.ascontiguousarray(b, dtype=np.float32)
+        rows, cols = A.shape
+        assert b.shape == (cols,)
+        out = np.empty_like(A)
+        self.lib.oracle_add_bias(rows, cols, _p(A, _FP), _p(b, _FP), _p(out, _FP))
+        return out
+
+    def bias_grad_rows(self, G, exact=False):
+        G = _d(G)
+        rows, cols = G.shape
+        db = np.empty(cols, np.float64)
+        db_abs = np.empty_like(db)
+        self.lib.oracle_bias_grad_rows(rows, cols, _p(G), _p(db), _p(db_abs))
+        return (db, db_abs) if exact else (_f32(db), db_abs)
+
+    def softmax(self, z):
+        z = _d(z)
+        rows, cols = z.shape
+        p = np.empty_like(z)
+        self.lib.oracle_softmax(rows, cols, _p(z), _p(p))
+        return p
+
+    def softmax_ce(self, z, labels):
+        """(grad, per-row losses), both in double: grad = softmax(z) - one_hot,
+        loss_i = -log softmax(z)_i[label_i]."""
+        z = _d(z)
+        rows, cols = z.shape
+        lab = np.ascontiguousarray(labels, dtype=np.int32)
+        assert lab.shape == (rows,) and lab.min() >= 0 and lab.max() < cols
+        grad = np.empty_like(z)
+        loss = np.empty(rows, np.float64)
+        self.lib.oracle_softmax_ce(rows, cols, _p(z), _p(lab, _IP), _p(grad), _p(loss))
+        return grad, loss
+
+    def grad_accum(self, accum, grad):
+        acc = np.array(accum, dtype=np.float32, copy=True)
+        g = np.ascontiguousarray(grad, dtype=np.float32)
+        assert acc.shape == g.shape
+        self.lib.oracle_grad_accum(acc.size, _p(g, _FP), _p(acc, _FP))
+        return acc
 
 
 _default = None

@@ -395,6 +395,91 @@ void oracle_sgd(i64 count, float lr, float clip, float *param, const float *grad
     }
 }
 
+/* ------------------------------------------------------------------------- */
+/* Training-step pieces around the convolutions (LeNet-5 step), page shader
+ * tables "Activation / Loss Shaders" and "Utility Shaders".                  */
+
+/* nn_relu: y = max(0, x), fp32; the result for x <= 0 is +0.                */
+void oracle_relu(i64 count, const float *x, float *y)
+{
+#pragma omp parallel for schedule(static)
+    for (i64 i = 0; i < count; ++i)
+        y[i] = x[i] > 0.0f ? x[i] : 0.0f;
+}
+
+/* nn_relu_grad: dx = grad * (x > 0), an fp32 product with 1 or 0.  x may be
+ * the ReLU's input or its output: both are > 0 at the same positions.       */
+void oracle_relu_grad(i64 count, const float *grad, const float *x, float *dx)
+{
+#pragma omp parallel for schedule(static)
+    for (i64 i = 0; i < count; ++i)
+        dx[i] = grad[i] * (x[i] > 0.0f ? 1.0f : 0.0f);
+}
+
+/* nn_add_bias: out[i] = A[i] + B[i % cols] over a row-major rows x cols
+ * matrix, one fp32 addition per element.                                    */
+void oracle_add_bias(i64 rows, i64 cols, const float *A, const float *b, float *out)
+{
+#pragma omp parallel for schedule(static)
+    for (i64 i = 0; i < rows * cols; ++i)
+        out[i] = A[i] + b[i % cols];
+}
+
+/* nn_bias_grad for a linear layer: the sum of the rows of the (batch x out)
+ * gradient, db[j] = sum_i G[i][j], in double, with sum_i |G[i][j]|.         */
+void oracle_bias_grad_rows(i64 rows, i64 cols, const double *G, double *db, double *db_abs)
+{
+    for (i64 j = 0; j < cols; ++j) {
+        double acc = 0.0, acc_abs = 0.0;
+        for (i64 i = 0; i < rows; ++i) {
+            acc += G[i * cols + j];
+            acc_abs += fabs(G[i * cols + j]);
+        }
+        db[j] = acc;
+        db_abs[j] = acc_abs;
+    }
+}
+
+/* nn_softmax: per row, subtract the row maximum, exponentiate, divide by the
+ * sum (the numerically stable form the page names), in double.              */
+void oracle_softmax(i64 rows, i64 cols, const double *z, double *p)
+{
+    for (i64 i = 0; i < rows; ++i) {
+        const double *zr = z + i * cols;
+        double m = zr[0];
+        for (i64 j = 1; j < cols; ++j)
+            if (zr[j] > m) m = zr[j];
+        double s = 0.0;
+        for (i64 j = 0; j < cols; ++j) {
+            p[i * cols + j] = exp(zr[j] - m);
+            s += p[i * cols + j];
+        }
+        for (i64 j = 0; j < cols; ++j) p[i * cols + j] /= s;
+    }
+}
+
+/* nn_softmax_ce_grad and nn_loss: with p = softmax(z) per row and the row's
+ * label l, grad = p - one_hot(l) and loss_i = -log p[l], in double.  The
+ * gradient is that of the batch sum of the row losses (no 1/batch factor).   */
+void oracle_softmax_ce(i64 rows, i64 cols, const double *z, const int32_t *labels, double *grad,
+                       double *loss)
+{
+    oracle_softmax(rows, cols, z, grad);
+    for (i64 i = 0; i < rows; ++i) {
+        const i64 l = labels[i];
+        loss[i] = -log(grad[i * cols + l]);
+        grad[i * cols + l] -= 1.0;
+    }
+}
+
+/* nn_grad_accum: accum += grad in place, one fp32 addition per element.     */
+void oracle_grad_accum(i64 count, const float *grad, float *accum)
+{
+#pragma omp parallel for schedule(static)
+    for (i64 i = 0; i < count; ++i)
+        accum[i] = accum[i] + grad[i];
+}
+
 /* Number of threads the parallel loops use (for reporting). */
 int oracle_threads(void)
 {

@@ -123,6 +123,30 @@ LENET = (
 )
 LENET_FC = ((400, 120), (120, 84), (84, 10))
 LENET_SGD = (0.01, 1.0)   # lr, clip
+LENET_CLASSES = 10
+
+# Parameter order of the LeNet-5 step: conv filters are (outC, inC, k, k);
+# linear weights are stored in x out (Y = X W), biases per output.
+LENET_PARAMS = ("conv1_w", "conv1_b", "conv2_w", "conv2_b",
+                "fc1_w", "fc1_b", "fc2_w", "fc2_b", "fc3_w", "fc3_b")
+
+
+def lenet_params(seed_base=2200):
+    """He-normal weights (std sqrt(2 / fan_in)), zero biases: 61,706 fp32 values."""
+    c1, c2 = LENET
+    p = {"conv1_w": he_normal(c1.w_shape, seed_base + 1), "conv1_b": np.zeros((c1.outC,), np.float32),
+         "conv2_w": he_normal(c2.w_shape, seed_base + 2), "conv2_b": np.zeros((c2.outC,), np.float32)}
+    for i, (fin, fout) in enumerate(LENET_FC):
+        p["fc%d_w" % (i + 1)] = normal((fin, fout), seed_base + 3 + i, std=math.sqrt(2.0 / fin))
+        p["fc%d_b" % (i + 1)] = np.zeros((fout,), np.float32)
+    return p
+
+
+def lenet_batch(batch=64, seed=2300):
+    """(x, labels): x (batch, 1, 28, 28) U[0,1); labels int32 uniform over the 10 classes."""
+    x = uniform01((batch, 1, 28, 28), seed)
+    labels = rng(seed + 1).integers(0, LENET_CLASSES, size=(batch,)).astype(np.int32)
+    return x, labels
 
 # Workload 3: AlexNet conv1, batch 128.
 ALEXNET_CONV1 = ConvLayer("alexnet_conv1_b128", 128, 3, 224, 224, 64, 11, 4, 2, 55, 55,
