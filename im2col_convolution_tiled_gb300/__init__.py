@@ -63,6 +63,12 @@ _SIGS = {
     "conv_b200_check": ([_P], ctypes.c_int),
     "conv_b200_launch_count": ([], ctypes.c_uint64),
     "conv_fwd_noalloc": ([_SHAPE, _P, _P, _P, _P, _P], ctypes.c_int),
+    "relu_fwd": ([ctypes.c_int64, _P, _P, _P], ctypes.c_int),
+    "relu_bwd": ([ctypes.c_int64, _P, _P, _P, _P], ctypes.c_int),
+    "grad_accum": ([ctypes.c_int64, _P, _P, _P], ctypes.c_int),
+    "add_bias": ([ctypes.c_int32, ctypes.c_int32, _P, _P, _P, ctypes.c_int32, _P], ctypes.c_int),
+    "bias_grad_rows": ([ctypes.c_int32, ctypes.c_int32, _P, _P, _P], ctypes.c_int),
+    "softmax_ce": ([ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P, _P, _P], ctypes.c_int),
 }
 
 
@@ -302,6 +308,81 @@ def sgd_step(param, grad, lr, clip, stream=None):
         raise ValueError("param and grad sizes differ")
     _call("sgd_step", param.numel(), lr, clip, _ptr(param), _ptr(grad), _stream(stream))
     return param
+
+
+def relu_fwd(x, y=None, stream=None):
+    """y = max(0, x) (y may be x)."""
+    torch = _torch()
+    _want(x, "x")
+    y = torch.empty_like(x) if y is None else y
+    _want(y, "y")
+    if y.numel() != x.numel():
+        raise ValueError("x and y sizes differ")
+    _call("relu_fwd", x.numel(), _ptr(x), _ptr(y), _stream(stream))
+    return y
+
+
+def relu_bwd(dy, x, dx=None, stream=None):
+    """dx = dy * (x > 0); x is the ReLU's input or output (dx may be dy)."""
+    torch = _torch()
+    _want(dy, "dy"), _want(x, "x")
+    dx = torch.empty_like(dy) if dx is None else dx
+    _want(dx, "dx")
+    if not (dy.numel() == x.numel() == dx.numel()):
+        raise ValueError("dy, x and dx sizes differ")
+    _call("relu_bwd", dy.numel(), _ptr(dy), _ptr(x), _ptr(dx), _stream(stream))
+    return dx
+
+
+def grad_accum(accum, grad, stream=None):
+    """accum += grad, in place."""
+    _want(accum, "accum"), _want(grad, "grad")
+    if accum.numel() != grad.numel():
+        raise ValueError("accum and grad sizes differ")
+    _call("grad_accum", accum.numel(), _ptr(grad), _ptr(accum), _stream(stream))
+    return accum
+
+
+def add_bias(a, b, out=None, relu=False, stream=None):
+    """out[i, j] = a[i, j] + b[j] (then max(0, .) when relu); out may be a."""
+    torch = _torch()
+    _want(a, "a"), _want(b, "b")
+    rows, cols = a.shape
+    if b.numel() != cols:
+        raise ValueError("bias length must equal the number of columns")
+    out = torch.empty_like(a) if out is None else out
+    _want(out, "out")
+    _call("add_bias", rows, cols, _ptr(a), _ptr(b), _ptr(out), 1 if relu else 0, _stream(stream))
+    return out
+
+
+def bias_grad_rows(grad, db=None, stream=None):
+    """db[j] = sum_i grad[i, j] (a linear layer's bias gradient)."""
+    torch = _torch()
+    _want(grad, "grad")
+    rows, cols = grad.shape
+    db = torch.empty(cols, dtype=torch.float32, device=grad.device) if db is None else db
+    _want(db, "db")
+    _call("bias_grad_rows", rows, cols, _ptr(grad), _ptr(db), _stream(stream))
+    return db
+
+
+def softmax_ce(logits, labels, dlogits=None, loss=None, probs=None, stream=None):
+    """(dlogits, loss): dlogits = softmax(logits) - one_hot(labels) per row and
+    loss (a 1-element tensor) = sum over rows of -log softmax(logits)[label]."""
+    torch = _torch()
+    _want(logits, "logits"), _want(labels, "labels", torch.int32)
+    rows, cols = logits.shape
+    if labels.numel() != rows:
+        raise ValueError("one label per row")
+    dlogits = torch.empty_like(logits) if dlogits is None else dlogits
+    loss = torch.empty(1, dtype=torch.float32, device=logits.device) if loss is None else loss
+    _want(dlogits, "dlogits"), _want(loss, "loss")
+    if probs is not None:
+        _want(probs, "probs")
+    _call("softmax_ce", rows, cols, _ptr(logits), _ptr(labels), _ptr(probs), _ptr(dlogits), _ptr(loss),
+          _stream(stream))
+    return dlogits, loss
 
 
 def launch_count() -> int:

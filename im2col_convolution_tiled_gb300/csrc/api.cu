@@ -280,6 +280,72 @@ int sgd_step(int64_t count, float lr, float clip, float* param, const float* gra
     return status_of(launch_sgd(count, lr, clip, param, grad, as_cuda(stream)));
 }
 
+// ---------------------------------------------------------------------------
+// training-step pieces
+
+int relu_fwd(int64_t count, const float* x, float* y, conv_stream_t stream)
+{
+    if (count < 0) return CONV_ERR_SHAPE;
+    if (count == 0) return CONV_OK;
+    int rc = check_ptrs({x, y});
+    if (rc != CONV_OK) return rc;
+    if (!device_ok()) return CONV_ERR_DEVICE;
+    return status_of(launch_relu_fwd(count, x, y, as_cuda(stream)));
+}
+
+int relu_bwd(int64_t count, const float* dy, const float* x, float* dx, conv_stream_t stream)
+{
+    if (count < 0) return CONV_ERR_SHAPE;
+    if (count == 0) return CONV_OK;
+    int rc = check_ptrs({dy, x, dx});
+    if (rc != CONV_OK) return rc;
+    if (!device_ok()) return CONV_ERR_DEVICE;
+    return status_of(launch_relu_bwd(count, dy, x, dx, as_cuda(stream)));
+}
+
+int grad_accum(int64_t count, const float* grad, float* accum, conv_stream_t stream)
+{
+    if (count < 0) return CONV_ERR_SHAPE;
+    if (count == 0) return CONV_OK;
+    int rc = check_ptrs({grad, accum});
+    if (rc != CONV_OK) return rc;
+    if (!device_ok()) return CONV_ERR_DEVICE;
+    return status_of(launch_grad_accum(count, grad, accum, as_cuda(stream)));
+}
+
+int add_bias(int32_t rows, int32_t cols, const float* a, const float* b, float* out, int32_t relu,
+             conv_stream_t stream)
+{
+    if (rows <= 0 || cols <= 0) return CONV_ERR_SHAPE;
+    if ((long long)rows * cols > kMaxElems) return CONV_ERR_OVERFLOW;
+    int rc = check_ptrs({a, b, out});
+    if (rc != CONV_OK) return rc;
+    if (!device_ok()) return CONV_ERR_DEVICE;
+    return status_of(launch_add_bias(rows, cols, a, b, out, relu, as_cuda(stream)));
+}
+
+int bias_grad_rows(int32_t rows, int32_t cols, const float* grad, float* db, conv_stream_t stream)
+{
+    if (rows <= 0 || cols <= 0) return CONV_ERR_SHAPE;
+    if ((long long)rows * cols > kMaxElems) return CONV_ERR_OVERFLOW;
+    int rc = check_ptrs({grad, db});
+    if (rc != CONV_OK) return rc;
+    if (!device_ok()) return CONV_ERR_DEVICE;
+    return status_of(launch_bias_grad_rows(rows, cols, grad, db, as_cuda(stream)));
+}
+
+int softmax_ce(int32_t rows, int32_t cols, const float* logits, const int32_t* labels, float* probs,
+               float* dlogits, float* loss, conv_stream_t stream)
+{
+    if (rows <= 0 || cols <= 0) return CONV_ERR_SHAPE;
+    if ((long long)rows * cols > kMaxElems) return CONV_ERR_OVERFLOW;
+    int rc = check_ptrs({logits, labels, dlogits, loss});
+    if (rc != CONV_OK) return rc;
+    if (probs && !aligned16(probs)) return CONV_ERR_ALIGN;
+    if (!device_ok()) return CONV_ERR_DEVICE;
+    return status_of(launch_softmax_ce(rows, cols, logits, labels, probs, dlogits, loss, as_cuda(stream)));
+}
+
 uint64_t conv_b200_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char* conv_b200_strerror(int code)
@@ -295,6 +361,7 @@ const char* conv_b200_strerror(int code)
     case CONV_ERR_DEVICE_TIMEOUT: return "a kernel gave up on a bounded wait";
     case CONV_ERR_DEVICE: return "no usable sm_103 device";
     case CONV_ERR_SCRATCH_LIMIT: return "shape needs more scratch than the built-in array holds";
+    case CONV_ERR_RANGE: return "a class label lies outside [0, cols)";
     default: return "unknown error";
     }
 }
@@ -313,7 +380,8 @@ int conv_b200_check(conv_stream_t stream)
     if (word != 0) {
         const int zero = 0;
         cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int));
-        return (word & kDevErrTimeout) ? CONV_ERR_DEVICE_TIMEOUT : CONV_ERR_CUDA;
+        if (word & kDevErrTimeout) return CONV_ERR_DEVICE_TIMEOUT;
+        return (word & kDevErrRange) ? CONV_ERR_RANGE : CONV_ERR_CUDA;
     }
     return CONV_OK;
 }

@@ -12,6 +12,7 @@ namespace cb200 {
 
 // Bits of the device error word.
 constexpr int kDevErrTimeout = 1;
+constexpr int kDevErrRange = 2;   // a class label outside [0, cols)
 
 // The device error word lives in device memory (one per device, file scope in
 // api.cu); kernels receive its address.
@@ -60,5 +61,14 @@ cudaError_t launch_maxpool_fwd(int N, int C, int H, int W, int k, int s, int P, 
 cudaError_t launch_maxpool_bwd(int N, int C, int H, int W, int k, int s, int P, int Q, const float* dy,
                                const int32_t* idx, float* dx, cudaStream_t st);
 cudaError_t launch_sgd(int64_t count, float lr, float clip, float* p, const float* g, cudaStream_t st);
+
+cudaError_t launch_relu_fwd(int64_t n, const float* x, float* y, cudaStream_t st);
+cudaError_t launch_relu_bwd(int64_t n, const float* dy, const float* x, float* dx, cudaStream_t st);
+cudaError_t launch_grad_accum(int64_t n, const float* g, float* acc, cudaStream_t st);
+cudaError_t launch_add_bias(int rows, int cols, const float* A, const float* b, float* out, int relu,
+                            cudaStream_t st);
+cudaError_t launch_bias_grad_rows(int rows, int cols, const float* G, float* db, cudaStream_t st);
+cudaError_t launch_softmax_ce(int rows, int cols, const float* z, const int32_t* labels, float* probs, float* dz,
+                              float* loss, cudaStream_t st);
 
 }  // namespace cb200

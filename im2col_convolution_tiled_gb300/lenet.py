@@ -1,0 +1,179 @@
+"""LeNet-5 training step on the GPU, composed from the library's entry points.
+
+Page "DirectCompute Neural Network Engine", section "LeNet on MNIST" (the
+trainer) with the convolution of section "Convolution: The im2col Approach"
+and the activation/loss and utility shaders:
+
+    x (B,1,28,28) -> conv 6@5x5 pad 2 -> ReLU -> maxpool 2/2
+                  -> conv 16@5x5       -> ReLU -> maxpool 2/2 -> flatten 400
+                  -> linear 400->120 -> ReLU -> linear 120->84 -> ReLU
+                  -> linear 84->10 -> softmax + cross-entropy against labels
+    backward through the same operations, then SGD with clip on every parameter.
+
+Every operation is one call into libconv_b200 on one stream; nothing is
+computed in Python or by torch (torch only owns the buffers).  All buffers are
+allocated once, so the whole step can be captured into one CUDA graph and
+replayed: the counterpart of the page's dispatch pipelining
+(section "Performance Notes"), without its per-dispatch host round trips.
+
+Conventions (as the page's shaders give them):
+  * linear: Y = X W + b with W stored in x out; dW = X^T dY (matmul flag 1),
+    dX = dY W^T (matmul flag 2), db = row sums of dY; bias and ReLU are one
+    add_bias call (relu flag);
+  * the ReLU gradient is masked by the ReLU's output (> 0 exactly where its
+    input is);
+  * the loss gradient is softmax - one_hot, the gradient of the batch SUM of
+    the row cross-entropies, which is what `loss` holds;
+  * the first layer's input gradient is not formed (x is the network input).
+"""
+from __future__ import annotations
+
+from collections import namedtuple
+
+from . import (CONV_OP_BWD_DATA, CONV_OP_BWD_FILTER, CONV_OP_FWD, add_bias, bias_grad_rows, conv_bwd_data,
+               conv_bwd_filter_bias, conv_fwd, matmul, maxpool2d_bwd, maxpool2d_fwd, relu_bwd, relu_fwd,
+               sgd_step, shape_of, softmax_ce, workspace_bytes)
+
+# The network.  Conv: outC filters k x k, stride, padding, then a k_pool/s_pool
+# max pool; linear layers (in, out); SGD learning rate and clip.
+Conv = namedtuple("Conv", "inC outC k stride pad pool")
+CONVS = (Conv(1, 6, 5, 1, 2, (2, 2)), Conv(6, 16, 5, 1, 0, (2, 2)))
+FCS = ((400, 120), (120, 84), (84, 10))
+IMAGE = (1, 28, 28)
+LR, CLIP = 0.01, 1.0
+PARAMS = ("conv1_w", "conv1_b", "conv2_w", "conv2_b", "fc1_w", "fc1_b", "fc2_w", "fc2_b", "fc3_w", "fc3_b")
+
+
+def _out(n, k, stride, pad):
+    return (n + 2 * pad - k) // stride + 1
+
+
+class LeNet5:
+    """Parameters, gradients and every activation of one LeNet-5 step, resident
+    on the GPU.  ``params`` maps the names in PARAMS to fp32 arrays (numpy or
+    torch): conv filters (outC, inC, k, k), linear weights (in, out), biases (out,)."""
+
+    def __init__(self, params, batch=64, lr=LR, clip=CLIP, device="cuda"):
+        import torch
+
+        self.torch = torch
+        self.B = batch
+        self.lr, self.clip = lr, clip
+        c1, c2 = CONVS
+        f32 = dict(dtype=torch.float32, device=device)
+        self.P = {k: torch.as_tensor(params[k]).to(device=device, dtype=torch.float32).contiguous().clone()
+                  for k in PARAMS}
+        self.G = {k: torch.empty_like(v) for k, v in self.P.items()}
+        B = batch
+        e = torch.empty
+        t = {}
+        t["x"] = e((B,) + IMAGE, **f32)
+        t["labels"] = e((B,), dtype=torch.int32, device=device)
+        H = IMAGE[1]
+        H1 = _out(H, c1.k, c1.stride, c1.pad)
+        H1p = _out(H1, c1.pool[0], c1.pool[1], 0)
+        H2 = _out(H1p, c2.k, c2.stride, c2.pad)
+        H2p = _out(H2, c2.pool[0], c2.pool[1], 0)
+        t["y1"] = e((B, c1.outC, H1, H1), **f32)        # conv1 + bias
+        t["a1"] = torch.empty_like(t["y1"])             # ReLU
+        t["p1"] = e((B, c1.outC, H1p, H1p), **f32)      # max pool
+        t["i1"] = torch.empty_like(t["p1"], dtype=torch.int32)
+        t["y2"] = e((B, c2.outC, H2, H2), **f32)
+        t["a2"] = torch.empty_like(t["y2"])
+        t["p2"] = e((B, c2.outC, H2p, H2p), **f32)
+        t["i2"] = torch.empty_like(t["p2"], dtype=torch.int32)
+        t["f"] = t["p2"].view(B, -1)                    # flatten (a view: no copy)
+        for i, (fin, fout) in enumerate(FCS, 1):
+            t["m%d" % i] = e((B, fout), **f32)          # X W
+            t["dz%d" % i] = e((B, fout), **f32)         # gradient at X W + b
+            t["df" if i == 1 else "dh%d" % (i - 1)] = e((B, fin), **f32)
+        t["h1"] = e((B, FCS[0][1]), **f32)              # ReLU(X W + b), layers 1 and 2
+        t["h2"] = e((B, FCS[1][1]), **f32)
+        t["z3"] = e((B, FCS[2][1]), **f32)              # logits
+        t["loss"] = e((1,), **f32)
+        t["dp2"] = t["df"].view(t["p2"].shape)
+        t["da2"] = torch.empty_like(t["a2"])
+        t["dy2"] = torch.empty_like(t["y2"])
+        t["dp1"] = torch.empty_like(t["p1"])
+        t["da1"] = torch.empty_like(t["a1"])
+        t["dy1"] = torch.empty_like(t["y1"])
+        self.t = t
+        s1 = shape_of(t["x"].shape, self.P["conv1_w"].shape, c1.stride, c1.pad)
+        s2 = shape_of(t["p1"].shape, self.P["conv2_w"].shape, c2.stride, c2.pad)
+        need = max(workspace_bytes(CONV_OP_FWD, s1), workspace_bytes(CONV_OP_BWD_FILTER, s1),
+                   workspace_bytes(CONV_OP_FWD, s2), workspace_bytes(CONV_OP_BWD_DATA, s2),
+                   workspace_bytes(CONV_OP_BWD_FILTER, s2), 16)
+        self.ws = e((need,), dtype=torch.uint8, device=device)
+        self.graph = None
+
+    # -- the step --------------------------------------------------------------
+    def load_batch(self, x, labels):
+        """Copy a batch into the step's input buffers (host or device arrays)."""
+        torch = self.torch
+        self.t["x"].copy_(torch.as_tensor(x), non_blocking=True)
+        self.t["labels"].copy_(torch.as_tensor(labels).to(torch.int32), non_blocking=True)
+
+    def run(self, stream=None):
+        """Issue the whole step on `stream` (torch's current stream by default)."""
+        t, P, G, ws, st = self.t, self.P, self.G, self.ws, stream
+        c1, c2 = CONVS
+        # forward
+        conv_fwd(t["x"], P["conv1_w"], P["conv1_b"], c1.stride, c1.pad, y=t["y1"], workspace=ws, stream=st)
+        relu_fwd(t["y1"], t["a1"], stream=st)
+        maxpool2d_fwd(t["a1"], *c1.pool, y=t["p1"], idx=t["i1"], stream=st)
+        conv_fwd(t["p1"], P["conv2_w"], P["conv2_b"], c2.stride, c2.pad, y=t["y2"], workspace=ws, stream=st)
+        relu_fwd(t["y2"], t["a2"], stream=st)
+        maxpool2d_fwd(t["a2"], *c2.pool, y=t["p2"], idx=t["i2"], stream=st)
+        h = t["f"]
+        for i, out in ((1, "h1"), (2, "h2"), (3, "z3")):
+            matmul(h, P["fc%d_w" % i], 0, C=t["m%d" % i], stream=st)
+            add_bias(t["m%d" % i], P["fc%d_b" % i], out=t[out], relu=i < 3, stream=st)
+            h = t[out]
+        softmax_ce(t["z3"], t["labels"], dlogits=t["dz3"], loss=t["loss"], stream=st)
+        # backward: linear layers
+        for i in (3, 2, 1):
+            hin = t["h%d" % (i - 1)] if i > 1 else t["f"]
+            dz = t["dz%d" % i]
+            dh = t["dh%d" % (i - 1)] if i > 1 else t["df"]
+            matmul(hin, dz, 1, C=G["fc%d_w" % i], stream=st)
+            bias_grad_rows(dz, db=G["fc%d_b" % i], stream=st)
+            matmul(dz, P["fc%d_w" % i], 2, C=dh, stream=st)
+            if i > 1:
+                relu_bwd(dh, t["h%d" % (i - 1)], dx=t["dz%d" % (i - 1)], stream=st)
+        # conv2 block
+        maxpool2d_bwd(t["dp2"], t["i2"], t["a2"].shape, *c2.pool, dx=t["da2"], stream=st)
+        relu_bwd(t["da2"], t["a2"], dx=t["dy2"], stream=st)
+        conv_bwd_filter_bias(t["p1"], t["dy2"], P["conv2_w"].shape, c2.stride, c2.pad, dw=G["conv2_w"],
+                             db=G["conv2_b"], workspace=ws, stream=st)
+        conv_bwd_data(P["conv2_w"], t["dy2"], t["p1"].shape, c2.stride, c2.pad, dx=t["dp1"], workspace=ws,
+                      stream=st)
+        # conv1 block
+        maxpool2d_bwd(t["dp1"], t["i1"], t["a1"].shape, *c1.pool, dx=t["da1"], stream=st)
+        relu_bwd(t["da1"], t["a1"], dx=t["dy1"], stream=st)
+        conv_bwd_filter_bias(t["x"], t["dy1"], P["conv1_w"].shape, c1.stride, c1.pad, dw=G["conv1_w"],
+                             db=G["conv1_b"], workspace=ws, stream=st)
+        # SGD
+        for k in PARAMS:
+            sgd_step(P[k], G[k], self.lr, self.clip, stream=st)
+
+    # -- CUDA graph --------------------------------------------------------------
+    def capture(self):
+        """Capture run() into a CUDA graph (after one eager warm-up step, which
+        also sets every kernel attribute outside the capture).  Note: the
+        warm-up step updates the parameters like any other step."""
+        torch = self.torch
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self.run()
+        torch.cuda.current_stream().wait_stream(side)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.run()
+        return self.graph
+
+    def replay(self):
+        self.graph.replay()
+
+    def params_numpy(self):
+        return {k: v.detach().cpu().numpy() for k, v in self.P.items()}

@@ -62,6 +62,7 @@ typedef struct {
 #define CONV_ERR_DEVICE_TIMEOUT (-7) /* a kernel's bounded wait gave up             */
 #define CONV_ERR_DEVICE (-8)         /* no usable sm_103 device                     */
 #define CONV_ERR_SCRATCH_LIMIT (-9)  /* shape needs more than the built-in scratch  */
+#define CONV_ERR_RANGE (-10)         /* a class label outside [0, cols) (device)    */
 
 /* Operation ids for conv_b200_workspace_bytes. */
 #define CONV_OP_FWD 0
@@ -164,6 +165,51 @@ int maxpool2d_bwd(int32_t batch, int32_t C, int32_t H, int32_t W, int32_t k, int
  * each operation rounded to fp32, no fused multiply-add.  count >= 0. */
 int sgd_step(int64_t count, float lr, float clip, float *param, const float *grad, conv_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Training-step pieces around the convolutions (shader tables "Activation /
+ * Loss Shaders" and "Utility Shaders"; the page's LeNet trainer, section
+ * "LeNet on MNIST", chains them with conv, pooling, flagged matmul and SGD).
+ * Element counts: count >= 0 (0 is a no-op); rows, cols >= 1.  Unlike the
+ * rest of the library these allow the in-place forms named below.
+ * ------------------------------------------------------------------------- */
+
+/* ReLU forward (nn_relu): y[i] = max(0, x[i]) (+0 for x <= 0).  y may be x. */
+int relu_fwd(int64_t count, const float *x, float *y, conv_stream_t stream);
+
+/* ReLU backward (nn_relu_grad): dx[i] = dy[i] * (x[i] > 0), an fp32 product
+ * with 1 or 0.  x may be the ReLU's input or its output (both are > 0 at the
+ * same positions).  dx may be dy. */
+int relu_bwd(int64_t count, const float *dy, const float *x, float *dx, conv_stream_t stream);
+
+/* Gradient accumulation (nn_grad_accum): accum[i] = accum[i] + grad[i], one
+ * fp32 addition each, in place. */
+int grad_accum(int64_t count, const float *grad, float *accum, conv_stream_t stream);
+
+/* Bias add (nn_add_bias): out[i][j] = a[i][j] + b[j] over a row-major
+ * rows x cols matrix (a linear layer's bias broadcast over the batch rows),
+ * one fp32 addition each; relu != 0 then applies max(0, .) (nn_relu fused).
+ * out may be a.   a, out [rows][cols]   b [cols] */
+int add_bias(int32_t rows, int32_t cols, const float *a, const float *b, float *out, int32_t relu,
+             conv_stream_t stream);
+
+/* Bias gradient of a linear layer (nn_bias_grad, "sum-reduces rows"):
+ * db[j] = sum_i grad[i][j] over the rows of a rows x cols gradient.  fp32
+ * sums in a fixed order set by the shape (deterministic).
+ *   grad [rows][cols]   db [cols] (overwritten) */
+int bias_grad_rows(int32_t rows, int32_t cols, const float *grad, float *db, conv_stream_t stream);
+
+/* Softmax + cross-entropy (nn_softmax, nn_softmax_ce_grad, nn_loss), per row
+ * of rows x cols logits with integer labels: p = exp(z - max z) / sum exp(z -
+ * max z) (the numerically stable form), dlogits = p - one_hot(label), and
+ * *loss = sum over rows of -log p[label] -- the batch SUM, whose gradient is
+ * exactly dlogits (the page's softmax_ce_grad has no 1/rows factor).  probs
+ * (nullable) receives p.  A label outside [0, cols) cannot be seen before the
+ * kernel runs: its row gets dlogits = p and no loss, and the next
+ * conv_b200_check() returns CONV_ERR_RANGE.
+ *   logits, probs, dlogits [rows][cols]   labels [rows] (int32)   loss [1] */
+int softmax_ce(int32_t rows, int32_t cols, const float *logits, const int32_t *labels, float *probs,
+               float *dlogits, float *loss, conv_stream_t stream);
+
 /* Number of kernels the library has launched since it was loaded (all
  * devices, all streams).  A diagnostic: callers difference two readings to
  * count the launches of a region of their own code. */
@@ -197,7 +243,7 @@ int conv_fwd_noalloc(const conv_shape_t *s, const float *x, const float *w, cons
 const char *conv_b200_strerror(int code);
 
 /* Synchronise `stream`, then read and clear the device error word: returns
- * CONV_OK, CONV_ERR_DEVICE_TIMEOUT, or CONV_ERR_CUDA. */
+ * CONV_OK, CONV_ERR_DEVICE_TIMEOUT, CONV_ERR_RANGE, or CONV_ERR_CUDA. */
 int conv_b200_check(conv_stream_t stream);
 
 #ifdef __cplusplus

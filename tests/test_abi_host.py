@@ -38,7 +38,8 @@ def test_header_declares_the_entry_points():
     for n in ["conv_fwd", "conv_bwd_data", "conv_bwd_filter", "conv_bwd_filter_bias", "conv_bwd_bias", "im2col",
               "col2im", "matmul",
               "maxpool2d_fwd", "maxpool2d_bwd", "sgd_step", "conv_b200_strerror", "conv_b200_check",
-              "conv_b200_workspace_bytes"]:
+              "conv_b200_workspace_bytes", "relu_fwd", "relu_bwd", "grad_accum", "add_bias", "bias_grad_rows",
+              "softmax_ce"]:
         assert n in names
 
 
@@ -110,8 +111,25 @@ def test_size_validation(lib):
     assert lib.conv_fwd(ctypes.byref(big), FAKE, FAKE, NULL, FAKE, FAKE, 1 << 30, NULL) == ERR_OVERFLOW
 
 
+def test_training_piece_validation(lib):
+    assert lib.relu_fwd(-1, FAKE, FAKE, NULL) == ERR_SHAPE
+    assert lib.relu_fwd(0, NULL, NULL, NULL) == CONV_OK                       # nothing to do
+    assert lib.relu_fwd(8, NULL, FAKE, NULL) == ERR_NULL
+    assert lib.relu_bwd(8, FAKE, MIS, FAKE, NULL) == ERR_ALIGN
+    assert lib.grad_accum(8, FAKE, NULL, NULL) == ERR_NULL
+    assert lib.add_bias(0, 4, FAKE, FAKE, FAKE, 0, NULL) == ERR_SHAPE
+    assert lib.add_bias(4, 4, FAKE, NULL, FAKE, 1, NULL) == ERR_NULL
+    assert lib.add_bias(65536, 65536, FAKE, FAKE, FAKE, 0, NULL) == ERR_OVERFLOW
+    assert lib.bias_grad_rows(4, 0, FAKE, FAKE, NULL) == ERR_SHAPE
+    assert lib.bias_grad_rows(4, 4, FAKE, MIS, NULL) == ERR_ALIGN
+    assert lib.softmax_ce(4, 10, FAKE, NULL, NULL, FAKE, FAKE, NULL) == ERR_NULL     # labels
+    assert lib.softmax_ce(4, 10, FAKE, FAKE, MIS, FAKE, FAKE, NULL) == ERR_ALIGN     # probs (optional)
+    assert lib.softmax_ce(4, 10, FAKE, FAKE, NULL, FAKE, NULL, NULL) == ERR_NULL     # loss
+    assert lib.softmax_ce(-4, 10, FAKE, FAKE, NULL, FAKE, FAKE, NULL) == ERR_SHAPE
+
+
 def test_strerror(lib):
-    for code in [0, -1, -2, -3, -4, -5, -6, -7, -8, -99]:
+    for code in [0, -1, -2, -3, -4, -5, -6, -7, -8, -9, -10, -99]:
         assert isinstance(lib.conv_b200_strerror(code), bytes)
 
 
