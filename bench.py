@@ -8,10 +8,12 @@ conv_bwd_data, conv_bwd_filter, conv_bwd_bias and an SGD step on the filters
 and bias.  The metric is algorithmic TFLOP/s of the three convolution GEMMs
 (2 * outC * inC*k*k * batch*outH*outW each) over the whole step.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload alexnet|lenet]
 
 Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle on a
 bounded sample of the same workload instead (host cores only).
+`--workload lenet` times the LeNet-5 training step (batch 64) instead: the
+whole step captured as one CUDA graph, in training images/s.
 """
 from __future__ import annotations
 
@@ -403,6 +405,166 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------------------
+# LeNet-5 training step (--workload lenet): the whole step -- forward, loss,
+# backward, SGD over 61,706 parameters -- as one CUDA graph
+
+LENET_METRIC = "LeNet-5 training step (fwd + softmax-CE + bwd + SGD), batch 64: training images/s"
+LENET_WORKLOAD = ("LeNet-5, batch 64, 1x28x28 fp32: conv 6@5x5 p2, ReLU, pool 2/2, conv 16@5x5, ReLU, pool 2/2, "
+                  "linear 400-120-84-10 with ReLU, softmax cross-entropy, SGD lr 0.01 clip 1.0")
+
+
+def lenet_step_flops(batch=64) -> int:
+    """Algorithmic FLOPs of the step's contractions: conv1 forward and filter
+    gradient (its input needs no gradient), conv2 forward, input and filter
+    gradients, and three GEMMs per linear layer."""
+    c1, c2 = synthetic.LENET
+    f = 2 * c1.with_batch(batch).gemm_flops + 3 * c2.with_batch(batch).gemm_flops
+    f += sum(3 * 2 * batch * fin * fout for fin, fout in synthetic.LENET_FC)
+    return f
+
+
+def oracle_lenet_run(steps):
+    import oracle.lenet as olenet
+    params = synthetic.lenet_params()
+    x, labels = synthetic.lenet_batch()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        params, _, _ = olenet.step(params, x, labels)
+    return time.perf_counter() - t0
+
+
+def run_lenet_reference(args):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    import oracle
+    oracle_lenet_run(args.warmup)
+    dt = oracle_lenet_run(args.steps)
+    value = args.steps * 64 / dt
+    line = {
+        "impl": "reference", "metric": LENET_METRIC, "value": value, "unit": "images/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": LENET_WORKLOAD},
+        "cpu_baseline": {"value": value, "unit": "images/s", "cores": oracle.get().threads(), "kind": "oracle",
+                         "sample": "the full batch-64 step"},
+        "e2e": {"value": value, "unit": "images/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_lenet(args):
+    import torch
+    import im2col_convolution_tiled_gb300 as cb
+    from im2col_convolution_tiled_gb300.lenet import LeNet5
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    if not os.path.exists(cb.LIB_PATH):
+        from im2col_convolution_tiled_gb300 import build
+        build.build()
+    cb.load()
+
+    B = 64
+    x, labels = synthetic.lenet_batch(B)
+    net = LeNet5(synthetic.lenet_params(), batch=B)
+    net.load_batch(x, labels)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+
+    # eager (one library call per operation from Python), for comparison
+    for _ in range(args.warmup):
+        net.run()
+    barrier()
+    n0 = cb.launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        net.run()
+    e1.record(stream)
+    barrier()
+    launches_per_step = (cb.launch_count() - n0) // args.steps
+    eager_ms = e0.elapsed_time(e1) / args.steps
+
+    # graph: capture once, replay
+    net.capture()
+    for _ in range(args.warmup):
+        net.replay()
+    barrier()
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            net.replay()
+        e1.record(stream)
+        barrier()
+    cb.check()
+    ms = e0.elapsed_time(e1) / args.steps
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * B / (ms * 1e-3)
+
+    # end to end: each step's batch goes up from pinned host memory and its loss comes back
+    hx = torch.from_numpy(x).pin_memory()
+    hl = torch.from_numpy(labels).pin_memory()
+    hloss = torch.empty(1).pin_memory()
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        net.t["x"].copy_(hx, non_blocking=True)
+        net.t["labels"].copy_(hl, non_blocking=True)
+        net.replay()
+        hloss.copy_(net.t["loss"], non_blocking=True)
+    stream.synchronize()
+    barrier()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    cb.check()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n = 20
+        dt = oracle_lenet_run(n)
+        import oracle
+        cpu = {"value": n * B / dt, "unit": "images/s", "cores": oracle.get().threads(), "kind": "oracle",
+               "sample": "%d full batch-64 steps, %.1f s" % (n, dt)}
+    flops = lenet_step_flops(B)
+    line = {
+        "metric": LENET_METRIC, "value": round(value, 1), "unit": "images/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": LENET_WORKLOAD, "batch": B, "params": 61706,
+                   "step_gflop": round(flops / 1e9, 4), "l2": "no flush: the whole step (about 10 MB) is L2-resident",
+                   "eager_ms_per_step": round(eager_ms, 4),
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "latency", "launches_per_step": launches_per_step,
+                     "us_per_launch": round(1e3 * ms / launches_per_step, 2),
+                     "achieved": round(flops / (ms * 1e-3) / 1e12, 4), "unit": "TFLOP/s", "peak": None,
+                     "frac": None, "traffic": None,
+                     "note": "dependent launches of small kernels; the graph removes the host issue cost"},
+        "e2e": {"value": round(world * B / (e2e_ms * 1e-3), 1), "unit": "images/s",
+                "h2d_bytes_per_step": int(x.nbytes + labels.nbytes), "d2h_bytes_per_step": 4,
+                "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -412,9 +574,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-batch", type=int, default=64)
     ap.add_argument("--ref-batch", type=int, default=1)
+    ap.add_argument("--workload", choices=["alexnet", "lenet"], default="alexnet")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps, always
-    if args.impl == "reference":
+    if args.workload == "lenet":
+        (run_lenet_reference if args.impl == "reference" else run_lenet)(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

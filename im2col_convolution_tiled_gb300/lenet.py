@@ -61,9 +61,28 @@ class LeNet5:
         self.lr, self.clip = lr, clip
         c1, c2 = CONVS
         f32 = dict(dtype=torch.float32, device=device)
-        self.P = {k: torch.as_tensor(params[k]).to(device=device, dtype=torch.float32).contiguous().clone()
-                  for k in PARAMS}
-        self.G = {k: torch.empty_like(v) for k, v in self.P.items()}
+        # Parameters and gradients each live in one flat buffer (every tensor a
+        # view starting on a 16-byte boundary), so the SGD step over all of them
+        # is one launch.  The few padding slots between views hold 0 in both
+        # buffers and stay 0: SGD leaves p unchanged where g = 0.
+        shapes = {k: tuple(torch.as_tensor(params[k]).shape) for k in PARAMS}
+        offs, n = {}, 0
+        for k in PARAMS:
+            offs[k] = n
+            size = 1
+            for d in shapes[k]:
+                size *= d
+            n += (size + 3) // 4 * 4
+        self.flat_p = torch.zeros(n, **f32)
+        self.flat_g = torch.zeros(n, **f32)
+        self.P, self.G = {}, {}
+        for k in PARAMS:
+            size = 1
+            for d in shapes[k]:
+                size *= d
+            self.P[k] = self.flat_p[offs[k]:offs[k] + size].view(shapes[k])
+            self.G[k] = self.flat_g[offs[k]:offs[k] + size].view(shapes[k])
+            self.P[k].copy_(torch.as_tensor(params[k]).to(device=device, dtype=torch.float32))
         B = batch
         e = torch.empty
         t = {}
@@ -152,9 +171,8 @@ class LeNet5:
         relu_bwd(t["da1"], t["a1"], dx=t["dy1"], stream=st)
         conv_bwd_filter_bias(t["x"], t["dy1"], P["conv1_w"].shape, c1.stride, c1.pad, dw=G["conv1_w"],
                              db=G["conv1_b"], workspace=ws, stream=st)
-        # SGD
-        for k in PARAMS:
-            sgd_step(P[k], G[k], self.lr, self.clip, stream=st)
+        # SGD over every parameter at once
+        sgd_step(self.flat_p, self.flat_g, self.lr, self.clip, stream=st)
 
     # -- CUDA graph --------------------------------------------------------------
     def capture(self):
