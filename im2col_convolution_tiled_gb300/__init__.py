@@ -22,7 +22,8 @@ __all__ = [
     "ConvShape", "lib", "load", "conv_fwd", "conv_bwd_data", "conv_bwd_filter", "conv_bwd_filter_bias",
     "conv_bwd_bias",
     "im2col", "col2im", "matmul", "maxpool2d_fwd", "maxpool2d_bwd", "sgd_step", "workspace_bytes",
-    "check", "ConvError", "out_size", "LIB_PATH", "launch_count",
+    "check", "ConvError", "out_size", "LIB_PATH", "launch_count", "relu_fwd", "relu_bwd", "grad_accum", "add_bias",
+    "bias_grad_rows", "softmax_ce", "set_math_mode", "math_mode", "math", "CONV_MATH_FP32", "CONV_MATH_TF32",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libconv_b200.so")
@@ -69,6 +70,8 @@ _SIGS = {
     "add_bias": ([ctypes.c_int32, ctypes.c_int32, _P, _P, _P, ctypes.c_int32, _P], ctypes.c_int),
     "bias_grad_rows": ([ctypes.c_int32, ctypes.c_int32, _P, _P, _P], ctypes.c_int),
     "softmax_ce": ([ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P, _P, _P], ctypes.c_int),
+    "conv_b200_set_math_mode": ([ctypes.c_int], ctypes.c_int),
+    "conv_b200_math_mode": ([], ctypes.c_int),
 }
 
 
@@ -383,6 +386,36 @@ def softmax_ce(logits, labels, dlogits=None, loss=None, probs=None, stream=None)
     _call("softmax_ce", rows, cols, _ptr(logits), _ptr(labels), _ptr(probs), _ptr(dlogits), _ptr(loss),
           _stream(stream))
     return dlogits, loss
+
+
+CONV_MATH_FP32, CONV_MATH_TF32 = 0, 1
+
+
+def set_math_mode(mode) -> int:
+    """Select the contractions' arithmetic (process-wide): CONV_MATH_FP32 (3xTF32,
+    the default) or CONV_MATH_TF32 (one TF32 product).  Returns the previous mode."""
+    prev = int(lib().conv_b200_set_math_mode(int(mode)))
+    if prev < 0:
+        raise ConvError("conv_b200_set_math_mode", prev)
+    return prev
+
+
+def math_mode() -> int:
+    return int(lib().conv_b200_math_mode())
+
+
+class math:
+    """Context manager: ``with math(CONV_MATH_TF32): ...`` restores the previous mode on exit."""
+
+    def __init__(self, mode):
+        self.mode = mode
+
+    def __enter__(self):
+        self.prev = set_math_mode(self.mode)
+        return self
+
+    def __exit__(self, *exc):
+        set_math_mode(self.prev)
 
 
 def launch_count() -> int:

@@ -40,6 +40,9 @@ void init_device(int dev)
 static std::atomic<unsigned long long> g_launches{0};
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+static std::atomic<int> g_math_mode{CONV_MATH_FP32};
+int math_terms() { return g_math_mode.load(std::memory_order_relaxed) == CONV_MATH_TF32 ? 1 : 3; }
+
 int* device_error_word()
 {
     const int dev = current_device();
@@ -347,6 +350,14 @@ int softmax_ce(int32_t rows, int32_t cols, const float* logits, const int32_t* l
 }
 
 uint64_t conv_b200_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int conv_b200_set_math_mode(int mode)
+{
+    if (mode != CONV_MATH_FP32 && mode != CONV_MATH_TF32) return CONV_ERR_SHAPE;
+    return g_math_mode.exchange(mode, std::memory_order_relaxed);
+}
+
+int conv_b200_math_mode(void) { return g_math_mode.load(std::memory_order_relaxed); }
 
 const char* conv_b200_strerror(int code)
 {

@@ -21,6 +21,11 @@ int* device_error_word();
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Tensor-core products per 8-deep K step of every contraction launched now:
+// 3 (3xTF32, fp32-faithful; the default) or 1 (one TF32 product), from the
+// process-wide mode set by conv_b200_set_math_mode().
+int math_terms();
+
 // Count of kernels this library has launched since it was loaded (every
 // <<<>>> launch calls note_launch()); exported as conv_b200_launch_count().
 void note_launch();

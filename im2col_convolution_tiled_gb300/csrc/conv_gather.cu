@@ -83,6 +83,7 @@ struct OutGeom {
 template <int BN>
 struct ConvGatherProb {
     static constexpr bool kBBulk = true;
+    int terms = 3;                                // tensor-core products per K step: 3 (3xTF32) or 1 (TF32)
     static constexpr bool kATmem = BN <= 128;     // A stages in tensor memory (keeps 2 accumulators)
     static constexpr int kGroups = 2;
     static constexpr Map kAMap = Map::RowFast;
@@ -275,6 +276,7 @@ struct ConvGatherProb {
 // groups when the gathered tensor has at most 16 channels).
 template <int BN>
 struct ConvPatchProb {
+    int terms = 3;   // tensor-core products per K step: 3 (3xTF32) or 1 (TF32)
     PatchGeom pg;
     OutGeom o;
     const float* bimg;
@@ -537,6 +539,7 @@ template <int BN>
 static cudaError_t run_gather(const GatherGeom& g, const OutGeom& o, float* img, float* part, cudaStream_t st)
 {
     ConvGatherProb<BN> p;
+    p.terms = math_terms();
     p.g = g;
     p.o = o;
     p.bimg = img;
@@ -623,6 +626,7 @@ template <int BN, bool TMA>
 static cudaError_t run_patch(const PatchGeom& pg, const OutGeom& o, float* img, cudaStream_t st)
 {
     ConvPatchProb<BN> p;
+    p.terms = math_terms();
     p.pg = pg;
     p.o = o;
     p.bimg = img;

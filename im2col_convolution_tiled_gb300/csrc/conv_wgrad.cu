@@ -25,6 +25,7 @@ namespace cb200 {
 template <int BN>
 struct ConvWgradProb {
     static constexpr bool kBBulk = true;
+    int terms = 3;   // tensor-core products per K step: 3 (3xTF32) or 1 (TF32)
     static constexpr int kGroups = 2;
     static constexpr Map kAMap = Map::ChunkFast;
     static constexpr Map kBMap = Map::ChunkFast;   // unused (bulk)
@@ -306,6 +307,7 @@ static cudaError_t run_wgrad(const ConvDims& d, const WgradPlan& pl, const float
                              void* ws, cudaStream_t st, const ConvDims* orig, float* db)
 {
     ConvWgradProb<BN> p;
+    p.terms = math_terms();
     float* img = static_cast<float*>(ws);
     float* part = img + wgrad_image_floats(d, pl);
     float* rowsum = part + wgrad_part_floats(d, pl, orig != nullptr);

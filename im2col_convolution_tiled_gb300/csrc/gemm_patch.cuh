@@ -179,7 +179,7 @@ struct PatchCtl {
 // box of the channel-blocked copy (pixel-major swizzled patch, mode 0): there
 // a converter thread reads its 32 channels with eight conflict-free 16-byte
 // loads and needs no bounds tests, since the box is zero outside the image.
-template <class Prob, int BN, bool TMA, bool DB2>
+template <class Prob, int BN, bool TMA, bool DB2, int TERMS>
 __global__ void __launch_bounds__(PatchCfg<BN, DB2>::kThreads, 1) tc_patch_kernel(const __grid_constant__ Prob prob, int* err_word)
 {
     using Cfg = PatchCfg<BN, DB2>;
@@ -223,6 +223,9 @@ __global__ void __launch_bounds__(PatchCfg<BN, DB2>::kThreads, 1) tc_patch_kerne
     const uint32_t tmem_base = ctl->tmem_base;
 
     const int num_tiles = prob.num_tiles();
+    // TERMS == 3: hi*hi + hi*lo + lo*hi (fp32-faithful); TERMS == 1: hi*hi only
+    constexpr bool three = TERMS == 3;
+    constexpr uint32_t b_bytes = (three ? 2u : 1u) * Cfg::kBTile;
     auto fail = [&]() {
         ctl->abort_flag = 1;
         atomicOr(err_word, kDevErrTimeout);
@@ -317,8 +320,8 @@ __global__ void __launch_bounds__(PatchCfg<BN, DB2>::kThreads, 1) tc_patch_kerne
                     }
                     if (!mbar_wait_warp(&ctl->empty[slot], phase ^ 1u, abort_flag)) { ok = false; break; }
                     if (tid == 0) {
-                        mbar_arrive_expect_tx(&ctl->full[slot], 2 * Cfg::kBTile);
-                        bulk_g2s(smem + (b_hi(slot) - smem_base), prob.b_image_t(t, ks), 2 * Cfg::kBTile,
+                        mbar_arrive_expect_tx(&ctl->full[slot], b_bytes);
+                        bulk_g2s(smem + (b_hi(slot) - smem_base), prob.b_image_t(t, ks), b_bytes,
                                  &ctl->full[slot]);
                         last_issued = int(c);
                     }
@@ -329,7 +332,7 @@ __global__ void __launch_bounds__(PatchCfg<BN, DB2>::kThreads, 1) tc_patch_kerne
 #pragma unroll
                         for (int i = 0; i < 8; ++i) split_tf32(va[8 * h4 + i], hi[i], lo[i]);
                         tmem_st8(tbase + a_col(slot) + 8 * h4, hi);
-                        tmem_st8(tbase + a_col(slot) + 32 + 8 * h4, lo);
+                        if (three) tmem_st8(tbase + a_col(slot) + 32 + 8 * h4, lo);
                     }
                     tmem_wait_st();
                     tc_fence_before();
@@ -436,10 +439,14 @@ __global__ void __launch_bounds__(PatchCfg<BN, DB2>::kThreads, 1) tc_patch_kerne
                         const uint64_t bl = sdesc_k_sw128(b_lo(slot) + kk * 32);
                         const uint32_t ah = tmem_base + a_col(slot) + uint32_t(kk * 8);
                         const uint32_t al = ah + 32;
-                        mma_tf32_ts(d_tmem, al, bh, Cfg::kIdesc, accumulate);
+                        if (three) {
+                            mma_tf32_ts(d_tmem, al, bh, Cfg::kIdesc, accumulate);
+                            mma_tf32_ts(d_tmem, ah, bl, Cfg::kIdesc, 1);
+                            mma_tf32_ts(d_tmem, ah, bh, Cfg::kIdesc, 1);
+                        } else {
+                            mma_tf32_ts(d_tmem, ah, bh, Cfg::kIdesc, accumulate);
+                        }
                         accumulate = 1;
-                        mma_tf32_ts(d_tmem, ah, bl, Cfg::kIdesc, 1);
-                        mma_tf32_ts(d_tmem, ah, bh, Cfg::kIdesc, 1);
                     }
                     issued_any = true;
                     mma_commit(&ctl->empty[slot]);
@@ -506,13 +513,13 @@ __global__ void __launch_bounds__(PatchCfg<BN, DB2>::kThreads, 1) tc_patch_kerne
     }
 }
 
-template <class Prob, int BN, bool TMA, bool DB2>
-cudaError_t launch_tc_patch(const Prob& prob, int num_tiles, int* err_word, cudaStream_t stream)
+template <class Prob, int BN, bool TMA, bool DB2, int TERMS>
+cudaError_t launch_tc_patch_terms(const Prob& prob, int num_tiles, int* err_word, cudaStream_t stream)
 {
     using Cfg = PatchCfg<BN, DB2>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(tc_patch_kernel<Prob, BN, TMA, DB2>,
+        cudaError_t e = cudaFuncSetAttribute(tc_patch_kernel<Prob, BN, TMA, DB2, TERMS>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cfg::kMaxSmem));
         if (e != cudaSuccess) return e;
         attr_set = true;
@@ -520,9 +527,17 @@ cudaError_t launch_tc_patch(const Prob& prob, int num_tiles, int* err_word, cuda
     if (num_tiles <= 0) return cudaSuccess;
     const size_t smem = TMA ? patch_tma_smem<BN, DB2>(prob.pg.tbytes) : Cfg::kSmemBytes;
     int grid = num_tiles < sm_count() ? num_tiles : sm_count();
-    tc_patch_kernel<Prob, BN, TMA, DB2><<<grid, Cfg::kThreads, smem, stream>>>(prob, err_word);
+    tc_patch_kernel<Prob, BN, TMA, DB2, TERMS><<<grid, Cfg::kThreads, smem, stream>>>(prob, err_word);
     note_launch();
     return cudaGetLastError();
+}
+
+// prob.terms (3 or 1) selects the kernel instantiation.
+template <class Prob, int BN, bool TMA, bool DB2>
+cudaError_t launch_tc_patch(const Prob& prob, int num_tiles, int* err_word, cudaStream_t stream)
+{
+    return prob.terms == 1 ? launch_tc_patch_terms<Prob, BN, TMA, DB2, 1>(prob, num_tiles, err_word, stream)
+                           : launch_tc_patch_terms<Prob, BN, TMA, DB2, 3>(prob, num_tiles, err_word, stream);
 }
 
 }  // namespace cb200

@@ -115,14 +115,15 @@ enum class Map { RowFast, ChunkFast };
 
 template <Map M>
 __device__ __forceinline__ void store_slice(uint32_t hi_tile, uint32_t lo_tile, int row_base, int rows, int tid,
-                                            const float (&v)[32])
+                                            const float (&v)[32], bool with_lo = true)
 {
     if constexpr (M == Map::RowFast) {
         int row = row_base + tid;
         if (row - row_base < rows) {
 #pragma unroll
             for (int c = 0; c < 8; ++c)
-                store_split_chunk(hi_tile, lo_tile, row, c, v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+                store_split_chunk(hi_tile, lo_tile, row, c, v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3],
+                                  with_lo);
         }
     } else {
         int chunk = tid & 7;
@@ -131,7 +132,7 @@ __device__ __forceinline__ void store_slice(uint32_t hi_tile, uint32_t lo_tile, 
             int r = (tid >> 3) + 16 * p;
             if (r < rows)
                 store_split_chunk(hi_tile, lo_tile, row_base + r, chunk, v[4 * p], v[4 * p + 1], v[4 * p + 2],
-                                  v[4 * p + 3]);
+                                  v[4 * p + 3], with_lo);
         }
     }
 }
@@ -152,7 +153,7 @@ struct EngineRoles {
     using R = Roles<Groups<Prob, BN>::value, Cfg::kIssuers>;
 };
 
-template <class Prob, int BN>
+template <class Prob, int BN, int TERMS>
 __global__ void __launch_bounds__(EngineRoles<Prob, BN>::R::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ Prob prob, int* err_word)
 {
@@ -202,6 +203,12 @@ __global__ void __launch_bounds__(EngineRoles<Prob, BN>::R::kThreads, 1)
     const uint32_t tmem_base = ctl->tmem_base;
 
     const int num_tiles = prob.num_tiles();
+    // TERMS == 3: hi*hi + hi*lo + lo*hi (fp32-faithful); TERMS == 1: hi*hi only
+    // (one TF32 product: no lo halves are stored, copied or multiplied).  A
+    // template parameter, so that the 3xTF32 kernel carries no trace of the
+    // other mode (a runtime switch measured 7% slower).
+    constexpr bool three = TERMS == 3;
+    constexpr uint32_t b_bytes = (three ? 2u : 1u) * Cfg::kBTile;
     auto fail = [&]() {
         ctl->abort_flag = 1;
         atomicOr(err_word, kDevErrTimeout);
@@ -235,15 +242,15 @@ __global__ void __launch_bounds__(EngineRoles<Prob, BN>::R::kThreads, 1)
                     if (!mbar_wait_warp(&ctl->empty[slot], phase ^ 1u, abort_flag)) return false;
                     if constexpr (Prob::kBBulk) {
                         if (tid == 0) {
-                            mbar_arrive_expect_tx(&ctl->full[slot], 2 * Cfg::kBTile);
-                            bulk_g2s(smem + (b_hi(slot) - smem_base), prob.b_image(tile, ks), 2 * Cfg::kBTile,
+                            mbar_arrive_expect_tx(&ctl->full[slot], b_bytes);
+                            bulk_g2s(smem + (b_hi(slot) - smem_base), prob.b_image(tile, ks), b_bytes,
                                      &ctl->full[slot]);
                             last_issued = int(c);
                             // the B image may stream from HBM (the filter gradient's dy
                             // image is larger than L2): pull a later stage's block into L2
                             // now, so that its copy finds it there
                             if (ks + kBPrefetch < tile.ks1)
-                                prefetch_l2_bulk(prob.b_image(tile, ks + kBPrefetch), 2 * Cfg::kBTile);
+                                prefetch_l2_bulk(prob.b_image(tile, ks + kBPrefetch), b_bytes);
                         }
                     }
                     if constexpr (ATMEM) {
@@ -258,18 +265,19 @@ __global__ void __launch_bounds__(EngineRoles<Prob, BN>::R::kThreads, 1)
 #pragma unroll
                             for (int i = 0; i < 8; ++i) split_tf32(va[8 * h + i], hi[i], lo[i]);
                             tmem_st8(tbase + 8 * h, hi);
-                            tmem_st8(tbase + 32 + 8 * h, lo);
+                            if (three) tmem_st8(tbase + 32 + 8 * h, lo);
                         }
                         tmem_wait_st();
                         tc_fence_before();
                     } else {
-                        store_slice<Prob::kAMap>(a_hi(slot), a_lo(slot), 0, kBM, tid, va);
+                        store_slice<Prob::kAMap>(a_hi(slot), a_lo(slot), 0, kBM, tid, va, three);
                     }
                     if constexpr (!Prob::kBBulk) {
 #pragma unroll
                         for (int pass = 0; pass < kBPasses; ++pass) {
                             const int rows = BN - 128 * pass < 128 ? BN - 128 * pass : 128;
-                            store_slice<Prob::kBMap>(b_hi(slot), b_lo(slot), 128 * pass, rows, tid, vb[pass]);
+                            store_slice<Prob::kBMap>(b_hi(slot), b_lo(slot), 128 * pass, rows, tid, vb[pass],
+                                                     three);
                         }
                     }
                     fence_proxy_async_smem();
@@ -344,17 +352,25 @@ __global__ void __launch_bounds__(EngineRoles<Prob, BN>::R::kThreads, 1)
                         if constexpr (ATMEM) {
                             const uint32_t ah = tmem_base + a_col(stage) + uint32_t(kk * 8);
                             const uint32_t al = ah + 32;
-                            mma_tf32_ts(d_tmem, al, bh, Cfg::kIdesc, accumulate);
+                            if (three) {
+                                mma_tf32_ts(d_tmem, al, bh, Cfg::kIdesc, accumulate);
+                                mma_tf32_ts(d_tmem, ah, bl, Cfg::kIdesc, 1);
+                                mma_tf32_ts(d_tmem, ah, bh, Cfg::kIdesc, 1);
+                            } else {
+                                mma_tf32_ts(d_tmem, ah, bh, Cfg::kIdesc, accumulate);
+                            }
                             accumulate = 1;
-                            mma_tf32_ts(d_tmem, ah, bl, Cfg::kIdesc, 1);
-                            mma_tf32_ts(d_tmem, ah, bh, Cfg::kIdesc, 1);
                         } else {
                             const uint64_t ah = sdesc_k_sw128(a_hi(stage) + kk * 32);
                             const uint64_t al = sdesc_k_sw128(a_lo(stage) + kk * 32);
-                            mma_tf32_ss(d_tmem, al, bh, Cfg::kIdesc, accumulate);
+                            if (three) {
+                                mma_tf32_ss(d_tmem, al, bh, Cfg::kIdesc, accumulate);
+                                mma_tf32_ss(d_tmem, ah, bl, Cfg::kIdesc, 1);
+                                mma_tf32_ss(d_tmem, ah, bh, Cfg::kIdesc, 1);
+                            } else {
+                                mma_tf32_ss(d_tmem, ah, bh, Cfg::kIdesc, accumulate);
+                            }
                             accumulate = 1;
-                            mma_tf32_ss(d_tmem, ah, bl, Cfg::kIdesc, 1);
-                            mma_tf32_ss(d_tmem, ah, bh, Cfg::kIdesc, 1);
                         }
                     }
                     issued_any = true;
@@ -431,23 +447,31 @@ __global__ void __launch_bounds__(EngineRoles<Prob, BN>::R::kThreads, 1)
 }
 
 // Host-side launch: persistent grid of min(tiles, SMs) CTAs.
-template <class Prob, int BN>
-cudaError_t launch_tc_gemm(const Prob& prob, int num_tiles, int* err_word, cudaStream_t stream)
+template <class Prob, int BN, int TERMS>
+cudaError_t launch_tc_gemm_terms(const Prob& prob, int num_tiles, int* err_word, cudaStream_t stream)
 {
     using Cfg = TileCfg<BN, UsesTmemA<Prob>::value>;
     constexpr int kThreads = EngineRoles<Prob, BN>::R::kThreads;
     static bool attr_set = false;   // per process; the attribute is per function
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<Prob, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             int(Cfg::kSmemBytes));
+        cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<Prob, BN, TERMS>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cfg::kSmemBytes));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     if (num_tiles <= 0) return cudaSuccess;
     int grid = num_tiles < sm_count() ? num_tiles : sm_count();
-    tc_gemm_kernel<Prob, BN><<<grid, kThreads, Cfg::kSmemBytes, stream>>>(prob, err_word);
+    tc_gemm_kernel<Prob, BN, TERMS><<<grid, kThreads, Cfg::kSmemBytes, stream>>>(prob, err_word);
     note_launch();
     return cudaGetLastError();
+}
+
+// prob.terms (3 or 1) selects the kernel instantiation.
+template <class Prob, int BN>
+cudaError_t launch_tc_gemm(const Prob& prob, int num_tiles, int* err_word, cudaStream_t stream)
+{
+    return prob.terms == 1 ? launch_tc_gemm_terms<Prob, BN, 1>(prob, num_tiles, err_word, stream)
+                           : launch_tc_gemm_terms<Prob, BN, 3>(prob, num_tiles, err_word, stream);
 }
 
 // ---------------------------------------------------------------------------

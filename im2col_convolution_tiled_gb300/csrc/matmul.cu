@@ -15,6 +15,7 @@ namespace cb200 {
 template <unsigned FLAGS, int BN>
 struct MatmulProb {
     static constexpr bool kBBulk = false;
+    int terms = 3;   // tensor-core products per K step: 3 (3xTF32) or 1 (TF32)
     static constexpr int kGroups = 2;
     static constexpr Map kAMap = (FLAGS & 1u) ? Map::RowFast : Map::ChunkFast;
     static constexpr Map kBMap = (FLAGS & 2u) ? Map::ChunkFast : Map::RowFast;
@@ -142,6 +143,7 @@ template <unsigned FLAGS, int BN>
 static cudaError_t run_matmul(int M, int K, int N, const float* A, const float* B, float* C, cudaStream_t st)
 {
     MatmulProb<FLAGS, BN> p;
+    p.terms = math_terms();
     p.A = A;
     p.B = B;
     p.C = C;

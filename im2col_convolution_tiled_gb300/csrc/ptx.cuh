@@ -365,7 +365,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t saddr, uint32_t a, uint32_
 // Split four consecutive-k values and store them as one 16-byte chunk into the
 // hi tile and the lo tile.
 __device__ __forceinline__ void store_split_chunk(uint32_t hi_tile, uint32_t lo_tile, uint32_t row, uint32_t chunk,
-                                                  float v0, float v1, float v2, float v3)
+                                                  float v0, float v1, float v2, float v3, bool with_lo = true)
 {
     uint32_t h0, h1, h2, h3, l0, l1, l2, l3;
     split_tf32(v0, h0, l0);
@@ -374,7 +374,7 @@ __device__ __forceinline__ void store_split_chunk(uint32_t hi_tile, uint32_t lo_
     split_tf32(v3, h3, l3);
     uint32_t off = sw128_offset(row, chunk);
     st_shared_v4(hi_tile + off, h0, h1, h2, h3);
-    st_shared_v4(lo_tile + off, l0, l1, l2, l3);
+    if (with_lo) st_shared_v4(lo_tile + off, l0, l1, l2, l3);
 }
 
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }

@@ -28,7 +28,7 @@
  *  - Contractions (conv_fwd, conv_bwd_data, conv_bwd_filter, matmul) run on
  *    the tcgen05 tensor cores in an fp32-faithful 3xTF32 mode with fp32
  *    accumulation: each result is within 1e-4 * sum_k |a_k b_k| + 1e-6 of the
- *    exact sum.
+ *    exact sum (a one-product TF32 mode is selectable: conv_b200_set_math_mode).
  */
 #ifndef CONV_B200_H
 #define CONV_B200_H
@@ -209,6 +209,26 @@ int bias_grad_rows(int32_t rows, int32_t cols, const float *grad, float *db, con
  *   logits, probs, dlogits [rows][cols]   labels [rows] (int32)   loss [1] */
 int softmax_ce(int32_t rows, int32_t cols, const float *logits, const int32_t *labels, float *probs,
                float *dlogits, float *loss, conv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Arithmetic of the contractions (conv_fwd, conv_bwd_data, conv_bwd_filter,
+ * conv_bwd_filter_bias, conv_fwd_noalloc, matmul).
+ *   CONV_MATH_FP32 (default): fp32-faithful 3xTF32 -- each operand split into a
+ *     TF32 high part and a TF32 remainder, three tensor-core products per
+ *     product (hi*hi + hi*lo + lo*hi), fp32 accumulation; within
+ *     1e-4 * sum_k |a_k b_k| + 1e-6 of the exact sum.
+ *   CONV_MATH_TF32: one tensor-core product of the operands truncated to TF32
+ *     (10 explicit mantissa bits), fp32 accumulation: within
+ *     2.5e-3 * sum_k |a_k b_k| + 1e-6; the "fast precision" mode, about three
+ *     times fewer tensor-core instructions and half the operand traffic.
+ * The mode is process-wide and read when a call launches its kernels (a CUDA
+ * graph keeps the mode it was captured with).  conv_b200_set_math_mode returns
+ * the previous mode, or CONV_ERR_SHAPE for an unknown mode (nothing changes).
+ * ------------------------------------------------------------------------- */
+#define CONV_MATH_FP32 0
+#define CONV_MATH_TF32 1
+int conv_b200_set_math_mode(int mode);
+int conv_b200_math_mode(void);
 
 /* Number of kernels the library has launched since it was loaded (all
  * devices, all streams).  A diagnostic: callers difference two readings to

@@ -39,7 +39,7 @@ def test_header_declares_the_entry_points():
               "col2im", "matmul",
               "maxpool2d_fwd", "maxpool2d_bwd", "sgd_step", "conv_b200_strerror", "conv_b200_check",
               "conv_b200_workspace_bytes", "relu_fwd", "relu_bwd", "grad_accum", "add_bias", "bias_grad_rows",
-              "softmax_ce"]:
+              "softmax_ce", "conv_b200_set_math_mode", "conv_b200_math_mode"]:
         assert n in names
 
 
@@ -126,6 +126,18 @@ def test_training_piece_validation(lib):
     assert lib.softmax_ce(4, 10, FAKE, FAKE, MIS, FAKE, FAKE, NULL) == ERR_ALIGN     # probs (optional)
     assert lib.softmax_ce(4, 10, FAKE, FAKE, NULL, FAKE, NULL, NULL) == ERR_NULL     # loss
     assert lib.softmax_ce(-4, 10, FAKE, FAKE, NULL, FAKE, FAKE, NULL) == ERR_SHAPE
+
+
+def test_math_mode_switch(lib):
+    assert lib.conv_b200_math_mode() == 0                        # 3xTF32 by default
+    assert lib.conv_b200_set_math_mode(2) == ERR_SHAPE           # unknown: rejected, nothing changes
+    assert lib.conv_b200_math_mode() == 0
+    assert lib.conv_b200_set_math_mode(1) == 0                   # returns the previous mode
+    assert lib.conv_b200_math_mode() == 1
+    assert lib.conv_b200_set_math_mode(0) == 1
+    with cb.math(cb.CONV_MATH_TF32):
+        assert cb.math_mode() == cb.CONV_MATH_TF32
+    assert cb.math_mode() == cb.CONV_MATH_FP32
 
 
 def test_strerror(lib):
