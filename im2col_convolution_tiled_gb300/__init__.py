@@ -49,6 +49,7 @@ _P = ctypes.c_void_p
 _SHAPE = ctypes.POINTER(ConvShape)
 _SIGS = {
     "conv_fwd": ([_SHAPE, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
+    "conv_fwd_relu": ([_SHAPE, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
     "conv_bwd_data": ([_SHAPE, _P, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
     "conv_bwd_filter": ([_SHAPE, _P, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
     "conv_bwd_filter_bias": ([_SHAPE, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
@@ -162,8 +163,9 @@ def _workspace(op, s, workspace):
 # ---------------------------------------------------------------------------
 # entry points (same names as the C ABI)
 
-def conv_fwd(x, w, b, stride=1, padding=0, y=None, workspace=None, stream=None):
-    """y = conv(x, w) + b, NCHW fp32 (b may be None)."""
+def conv_fwd(x, w, b, stride=1, padding=0, y=None, workspace=None, stream=None, relu=False):
+    """y = conv(x, w) + b, NCHW fp32 (b may be None); relu=True: max(0, .) fused
+    into the epilogue (conv_fwd_relu)."""
     torch = _torch()
     _want(x, "x"), _want(w, "w")
     if b is not None:
@@ -173,7 +175,8 @@ def conv_fwd(x, w, b, stride=1, padding=0, y=None, workspace=None, stream=None):
         y = torch.empty((s.batch, s.outC, s.outH, s.outW), dtype=torch.float32, device=x.device)
     _want(y, "y")
     ws, nbytes = _workspace(CONV_OP_FWD, s, workspace)
-    _call("conv_fwd", ctypes.byref(s), _ptr(x), _ptr(w), _ptr(b), _ptr(y), _ptr(ws), nbytes, _stream(stream))
+    _call("conv_fwd_relu" if relu else "conv_fwd", ctypes.byref(s), _ptr(x), _ptr(w), _ptr(b), _ptr(y), _ptr(ws),
+          nbytes, _stream(stream))
     return y
 
 

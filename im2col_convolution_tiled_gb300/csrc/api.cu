@@ -165,6 +165,19 @@ int conv_fwd(const conv_shape_t* s, const float* x, const float* w, const float*
     return status_of(launch_conv_fwd(d, x, w, b, y, workspace, as_cuda(stream)));
 }
 
+int conv_fwd_relu(const conv_shape_t* s, const float* x, const float* w, const float* b, float* y, void* workspace,
+                  size_t workspace_bytes, conv_stream_t stream)
+{
+    ConvDims d;
+    int rc = check_shape(s, &d);
+    if (rc != CONV_OK) return rc;
+    if ((rc = check_ptrs({x, w, y})) != CONV_OK) return rc;
+    if (b && !aligned16(b)) return CONV_ERR_ALIGN;
+    if ((rc = check_workspace(conv_fwd_ws(d), workspace, workspace_bytes)) != CONV_OK) return rc;
+    if (!device_ok()) return CONV_ERR_DEVICE;
+    return status_of(launch_conv_fwd(d, x, w, b, y, workspace, as_cuda(stream), true));
+}
+
 int conv_bwd_data(const conv_shape_t* s, const float* w, const float* dy, float* dx, void* workspace,
                   size_t workspace_bytes, conv_stream_t stream)
 {

@@ -42,8 +42,9 @@ struct ConvDims {
     int pad;
 };
 
+// relu: apply max(0, .) after the bias in the epilogue (conv_fwd_relu).
 cudaError_t launch_conv_fwd(const ConvDims& d, const float* x, const float* w, const float* b, float* y,
-                            void* ws, cudaStream_t st);
+                            void* ws, cudaStream_t st, bool relu = false);
 size_t conv_fwd_ws(const ConvDims& d);
 
 cudaError_t launch_conv_dgrad(const ConvDims& d, const float* w, const float* dy, float* dx, void* ws,

@@ -75,6 +75,7 @@ static inline void k_order(int ci, int* mode, int* cp, int* lcp)
 struct OutGeom {
     float* out;              // [Nb][Co][Ho][Wo]
     const float* bias;       // [Co] or null
+    int relu;                // forward only: max(0, .) after the bias (nn_relu fused into the epilogue)
     int Co, Ho, Wo, HoWo;
     int so;                  // output phase stride (1: plain NCHW)
     int ncols;               // Co * so * so
@@ -254,8 +255,10 @@ struct ConvGatherProb {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const int ch = tl.n0 + c0 + i;
-                if (ch < o.Co)
-                    e.opix[size_t(ch) * o.HoWo] = __uint_as_float(r[i]) + (o.bias ? __ldg(o.bias + ch) : 0.f);
+                if (ch < o.Co) {
+                    const float v = __uint_as_float(r[i]) + (o.bias ? __ldg(o.bias + ch) : 0.f);
+                    e.opix[size_t(ch) * o.HoWo] = o.relu && !(v > 0.f) ? 0.f : v;
+                }
             }
         } else {
             const int ss = o.so * o.so;
@@ -925,11 +928,12 @@ size_t conv_dgrad_ws(const ConvDims& d)
 }
 
 cudaError_t launch_conv_fwd(const ConvDims& d, const float* x, const float* w, const float* b, float* y, void* ws,
-                            cudaStream_t st)
+                            cudaStream_t st, bool relu)
 {
     OutGeom o{};
     o.out = y;
     o.bias = b;
+    o.relu = relu ? 1 : 0;
     o.Co = d.K;
     o.Ho = d.P;
     o.Wo = d.Q;

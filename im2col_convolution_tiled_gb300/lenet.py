@@ -20,8 +20,10 @@ Conventions (as the page's shaders give them):
   * linear: Y = X W + b with W stored in x out; dW = X^T dY (matmul flag 1),
     dX = dY W^T (matmul flag 2), db = row sums of dY; bias and ReLU are one
     add_bias call (relu flag);
+  * the convolutions' ReLU runs in their epilogue (conv_fwd_relu);
   * the ReLU gradient is masked by the ReLU's output (> 0 exactly where its
-    input is);
+    input is); behind a max pool the mask is applied to the pooled gradient,
+    by the pooled value, before routing;
   * the loss gradient is softmax - one_hot, the gradient of the batch SUM of
     the row cross-entropies, which is what `loss` holds;
   * the first layer's input gradient is not formed (x is the network input).
@@ -31,8 +33,8 @@ from __future__ import annotations
 from collections import namedtuple
 
 from . import (CONV_OP_BWD_DATA, CONV_OP_BWD_FILTER, CONV_OP_FWD, add_bias, bias_grad_rows, conv_bwd_data,
-               conv_bwd_filter_bias, conv_fwd, matmul, maxpool2d_bwd, maxpool2d_fwd, relu_bwd, relu_fwd,
-               sgd_step, shape_of, softmax_ce, workspace_bytes)
+               conv_bwd_filter_bias, conv_fwd, matmul, maxpool2d_bwd, maxpool2d_fwd, relu_bwd, sgd_step, shape_of,
+               softmax_ce, workspace_bytes)
 
 # The network.  Conv: outC filters k x k, stride, padding, then a k_pool/s_pool
 # max pool; linear layers (in, out); SGD learning rate and clip.
@@ -93,12 +95,10 @@ class LeNet5:
         H1p = _out(H1, c1.pool[0], c1.pool[1], 0)
         H2 = _out(H1p, c2.k, c2.stride, c2.pad)
         H2p = _out(H2, c2.pool[0], c2.pool[1], 0)
-        t["y1"] = e((B, c1.outC, H1, H1), **f32)        # conv1 + bias
-        t["a1"] = torch.empty_like(t["y1"])             # ReLU
+        t["a1"] = e((B, c1.outC, H1, H1), **f32)        # ReLU(conv1 + bias), one fused pass
         t["p1"] = e((B, c1.outC, H1p, H1p), **f32)      # max pool
         t["i1"] = torch.empty_like(t["p1"], dtype=torch.int32)
-        t["y2"] = e((B, c2.outC, H2, H2), **f32)
-        t["a2"] = torch.empty_like(t["y2"])
+        t["a2"] = e((B, c2.outC, H2, H2), **f32)
         t["p2"] = e((B, c2.outC, H2p, H2p), **f32)
         t["i2"] = torch.empty_like(t["p2"], dtype=torch.int32)
         t["f"] = t["p2"].view(B, -1)                    # flatten (a view: no copy)
@@ -111,11 +111,11 @@ class LeNet5:
         t["z3"] = e((B, FCS[2][1]), **f32)              # logits
         t["loss"] = e((1,), **f32)
         t["dp2"] = t["df"].view(t["p2"].shape)
-        t["da2"] = torch.empty_like(t["a2"])
-        t["dy2"] = torch.empty_like(t["y2"])
+        t["dq2"] = torch.empty_like(t["p2"])            # dp2 masked by p2 > 0
+        t["dy2"] = torch.empty_like(t["a2"])
         t["dp1"] = torch.empty_like(t["p1"])
-        t["da1"] = torch.empty_like(t["a1"])
-        t["dy1"] = torch.empty_like(t["y1"])
+        t["dq1"] = torch.empty_like(t["p1"])
+        t["dy1"] = torch.empty_like(t["a1"])
         self.t = t
         s1 = shape_of(t["x"].shape, self.P["conv1_w"].shape, c1.stride, c1.pad)
         s2 = shape_of(t["p1"].shape, self.P["conv2_w"].shape, c2.stride, c2.pad)
@@ -137,11 +137,11 @@ class LeNet5:
         t, P, G, ws, st = self.t, self.P, self.G, self.ws, stream
         c1, c2 = CONVS
         # forward
-        conv_fwd(t["x"], P["conv1_w"], P["conv1_b"], c1.stride, c1.pad, y=t["y1"], workspace=ws, stream=st)
-        relu_fwd(t["y1"], t["a1"], stream=st)
+        conv_fwd(t["x"], P["conv1_w"], P["conv1_b"], c1.stride, c1.pad, y=t["a1"], workspace=ws, stream=st,
+                 relu=True)
         maxpool2d_fwd(t["a1"], *c1.pool, y=t["p1"], idx=t["i1"], stream=st)
-        conv_fwd(t["p1"], P["conv2_w"], P["conv2_b"], c2.stride, c2.pad, y=t["y2"], workspace=ws, stream=st)
-        relu_fwd(t["y2"], t["a2"], stream=st)
+        conv_fwd(t["p1"], P["conv2_w"], P["conv2_b"], c2.stride, c2.pad, y=t["a2"], workspace=ws, stream=st,
+                 relu=True)
         maxpool2d_fwd(t["a2"], *c2.pool, y=t["p2"], idx=t["i2"], stream=st)
         h = t["f"]
         for i, out in ((1, "h1"), (2, "h2"), (3, "z3")):
@@ -159,16 +159,20 @@ class LeNet5:
             matmul(dz, P["fc%d_w" % i], 2, C=dh, stream=st)
             if i > 1:
                 relu_bwd(dh, t["h%d" % (i - 1)], dx=t["dz%d" % (i - 1)], stream=st)
-        # conv2 block
-        maxpool2d_bwd(t["dp2"], t["i2"], t["a2"].shape, *c2.pool, dx=t["da2"], stream=st)
-        relu_bwd(t["da2"], t["a2"], dx=t["dy2"], stream=st)
+        # conv2 block.  The ReLU mask is applied to the pooled gradient before it
+        # is routed: a window's pooled value is the ReLU output at its argmax, so
+        # masking by p > 0 keeps exactly the terms that reach positions with
+        # a > 0 and zeroes the rest (the same values as masking after the
+        # routing, up to the sign of a zero), over a tensor four times smaller.
+        relu_bwd(t["dp2"], t["p2"], dx=t["dq2"], stream=st)
+        maxpool2d_bwd(t["dq2"], t["i2"], t["a2"].shape, *c2.pool, dx=t["dy2"], stream=st)
         conv_bwd_filter_bias(t["p1"], t["dy2"], P["conv2_w"].shape, c2.stride, c2.pad, dw=G["conv2_w"],
                              db=G["conv2_b"], workspace=ws, stream=st)
         conv_bwd_data(P["conv2_w"], t["dy2"], t["p1"].shape, c2.stride, c2.pad, dx=t["dp1"], workspace=ws,
                       stream=st)
         # conv1 block
-        maxpool2d_bwd(t["dp1"], t["i1"], t["a1"].shape, *c1.pool, dx=t["da1"], stream=st)
-        relu_bwd(t["da1"], t["a1"], dx=t["dy1"], stream=st)
+        relu_bwd(t["dp1"], t["p1"], dx=t["dq1"], stream=st)
+        maxpool2d_bwd(t["dq1"], t["i1"], t["a1"].shape, *c1.pool, dx=t["dy1"], stream=st)
         conv_bwd_filter_bias(t["x"], t["dy1"], P["conv1_w"].shape, c1.stride, c1.pad, dw=G["conv1_w"],
                              db=G["conv1_b"], workspace=ws, stream=st)
         # SGD over every parameter at once

@@ -81,6 +81,13 @@ typedef struct {
 int conv_fwd(const conv_shape_t *s, const float *x, const float *w, const float *b, float *y, void *workspace,
              size_t workspace_bytes, conv_stream_t stream);
 
+/* Forward convolution with ReLU (nn_relu) fused into the epilogue: exactly
+ * max(0, conv_fwd(...)) -- the same sums and the same fp32 bias add, then +0
+ * wherever the result is not > 0 -- in one pass over y instead of two.
+ * Arguments, workspace (CONV_OP_FWD) and errors as conv_fwd. */
+int conv_fwd_relu(const conv_shape_t *s, const float *x, const float *w, const float *b, float *y, void *workspace,
+                  size_t workspace_bytes, conv_stream_t stream);
+
 /* Input gradient.  Page section "Convolution: The im2col Approach", backward:
  * filters^T x grad_reshaped -> col2im -> grad_input.  Computed as one implicit
  * GEMM per stride phase that gathers grad_output directly, so the col2im sum

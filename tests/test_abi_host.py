@@ -35,7 +35,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ["conv_fwd", "conv_bwd_data", "conv_bwd_filter", "conv_bwd_filter_bias", "conv_bwd_bias", "im2col",
+    for n in ["conv_fwd", "conv_fwd_relu", "conv_bwd_data", "conv_bwd_filter", "conv_bwd_filter_bias", "conv_bwd_bias", "im2col",
               "col2im", "matmul",
               "maxpool2d_fwd", "maxpool2d_bwd", "sgd_step", "conv_b200_strerror", "conv_b200_check",
               "conv_b200_workspace_bytes", "relu_fwd", "relu_bwd", "grad_accum", "add_bias", "bias_grad_rows",

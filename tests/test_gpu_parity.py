@@ -116,6 +116,25 @@ def test_conv_fwd(cb, orc, shape):
     assert_within_tol(y.numpy(), ref, ref_abs, "conv_fwd %s" % (shape,))
 
 
+@pytest.mark.parametrize("shape", CONV_SHAPES)
+def test_conv_fwd_relu(cb, orc, shape):
+    """conv_fwd_relu: within tolerance of max(0, oracle) (ReLU is 1-Lipschitz),
+    and bit-for-bit max(0, .) of conv_fwd's own output (same kernels, same
+    sums: the ReLU is only applied in the epilogue)."""
+    x, w, b, _ = conv_inputs(shape, 120)
+    st, pad = shape[6], shape[7]
+    ref, ref_abs = orc.conv_fwd(x, w, b, st, pad)
+    yr = dev_out(ref.shape)
+    xd, wd, bd = dev_in(x), dev_in(w), dev_in(b)
+    cb.conv_fwd(xd.t, wd.t, bd.t, st, pad, y=yr.t, relu=True)
+    y = cb.conv_fwd(xd.t, wd.t, bd.t, st, pad)
+    sync_check(cb)
+    assert yr.guards_intact()
+    got = yr.numpy()
+    assert_within_tol(got, orc.relu(ref), ref_abs, "conv_fwd_relu %s" % (shape,))
+    assert np.array_equal(got, orc.relu(y.cpu().numpy()))
+
+
 def test_conv_fwd_without_bias(cb, orc):
     shape = CONV_SHAPES[2]
     x, w, _, _ = conv_inputs(shape, 110)
