@@ -15,7 +15,8 @@ bounded sample of the same workload instead (host cores only).
 `--workload lenet` times the LeNet-5 training step (batch 64) instead: the
 whole step captured as one CUDA graph, in training images/s.  `--math tf32`
 runs the contractions as one TF32 product (the fast mode) and reports them
-against the TF32 roofline.
+against the TF32 roofline.  `--workload direct` times the direct (CUDA-core)
+convolution kernels against the implicit-GEMM path (an ablation).
 """
 from __future__ import annotations
 
@@ -571,6 +572,73 @@ def run_lenet(args):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------------------
+# direct convolution vs implicit GEMM (--workload direct): the page's legacy
+# direct kernels as an ablation on small-channel and large layers
+
+DIRECT_METRIC = "direct (CUDA-core) vs implicit-GEMM (tcgen05) convolution time, fwd + input grad + filter grad"
+
+
+def run_direct(args):
+    import torch
+    import im2col_convolution_tiled_gb300 as cb
+
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    if not os.path.exists(cb.LIB_PATH):
+        from im2col_convolution_tiled_gb300 import build
+        build.build()
+    cb.load()
+    layers = [synthetic.SINGLE] + list(synthetic.LENET) + [synthetic.ALEXNET_CONV1]
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, reps):
+        for _ in range(args.warmup):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    rows = []
+    total = {"gemm": 0.0, "direct": 0.0}
+    with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
+        for L in layers:
+            x, w, b, dy = (torch.from_numpy(a).cuda() for a in L.make())
+            s = cb.shape_of(L.x_shape, L.w_shape, L.stride, L.pad)
+            ws = torch.empty(max(cb.workspace_bytes(op, s) for op in range(3)) + 16, dtype=torch.uint8, device="cuda")
+            y, dx, dw = torch.empty(L.y_shape, device="cuda"), torch.empty(L.x_shape, device="cuda"), \
+                torch.empty(L.w_shape, device="cuda")
+            gemm = lambda: (cb.conv_fwd(x, w, b, L.stride, L.pad, y=y, workspace=ws),
+                            cb.conv_bwd_data(w, dy, L.x_shape, L.stride, L.pad, dx=dx, workspace=ws),
+                            cb.conv_bwd_filter(x, dy, L.w_shape, L.stride, L.pad, dw=dw, workspace=ws))
+            direct = lambda: (cb.conv_fwd_direct(x, w, b, L.stride, L.pad, y=y),
+                              cb.conv_bwd_data_direct(w, dy, L.x_shape, L.stride, L.pad, dx=dx),
+                              cb.conv_bwd_filter_direct(x, dy, L.w_shape, L.stride, L.pad, dw=dw))
+            reps = max(2, args.steps if L.batch < 128 else args.steps // 10)
+            tg, td = timed(gemm, reps), timed(direct, reps)
+            total["gemm"] += tg
+            total["direct"] += td
+            rows.append({"layer": L.name, "gemm_ms": round(tg, 4), "direct_ms": round(td, 4),
+                         "direct_over_gemm": round(td / tg, 3),
+                         "gemm_tflops": round(3 * L.gemm_flops / (tg * 1e-3) / 1e12, 3),
+                         "direct_tflops": round(3 * L.gemm_flops / (td * 1e-3) / 1e12, 3)})
+    cb.check()
+    line = {
+        "metric": DIRECT_METRIC, "value": round(total["direct"] / total["gemm"], 3), "unit": "time ratio",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "single conv b4, LeNet conv1/conv2 b64, AlexNet conv1 b128; each layer's three "
+                               "convolution calls", "layers": rows},
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -580,13 +648,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-batch", type=int, default=64)
     ap.add_argument("--ref-batch", type=int, default=1)
-    ap.add_argument("--workload", choices=["alexnet", "lenet"], default="alexnet")
+    ap.add_argument("--workload", choices=["alexnet", "lenet", "direct"], default="alexnet")
     ap.add_argument("--math", choices=["fp32", "tf32"], default="fp32",
                     help="contractions in fp32-faithful 3xTF32 (default) or one TF32 product")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps, always
     if args.workload == "lenet":
         (run_lenet_reference if args.impl == "reference" else run_lenet)(args)
+    elif args.workload == "direct":
+        run_direct(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

@@ -24,6 +24,7 @@ __all__ = [
     "im2col", "col2im", "matmul", "maxpool2d_fwd", "maxpool2d_bwd", "sgd_step", "workspace_bytes",
     "check", "ConvError", "out_size", "LIB_PATH", "launch_count", "relu_fwd", "relu_bwd", "grad_accum", "add_bias",
     "bias_grad_rows", "softmax_ce", "set_math_mode", "math_mode", "math", "CONV_MATH_FP32", "CONV_MATH_TF32",
+    "conv_fwd_direct", "conv_bwd_data_direct", "conv_bwd_filter_direct",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libconv_b200.so")
@@ -71,6 +72,9 @@ _SIGS = {
     "add_bias": ([ctypes.c_int32, ctypes.c_int32, _P, _P, _P, ctypes.c_int32, _P], ctypes.c_int),
     "bias_grad_rows": ([ctypes.c_int32, ctypes.c_int32, _P, _P, _P], ctypes.c_int),
     "softmax_ce": ([ctypes.c_int32, ctypes.c_int32, _P, _P, _P, _P, _P, _P], ctypes.c_int),
+    "conv_fwd_direct": ([_SHAPE, _P, _P, _P, _P, _P], ctypes.c_int),
+    "conv_bwd_data_direct": ([_SHAPE, _P, _P, _P, _P], ctypes.c_int),
+    "conv_bwd_filter_direct": ([_SHAPE, _P, _P, _P, _P], ctypes.c_int),
     "conv_b200_set_math_mode": ([ctypes.c_int], ctypes.c_int),
     "conv_b200_math_mode": ([], ctypes.c_int),
 }
@@ -389,6 +393,42 @@ def softmax_ce(logits, labels, dlogits=None, loss=None, probs=None, stream=None)
     _call("softmax_ce", rows, cols, _ptr(logits), _ptr(labels), _ptr(probs), _ptr(dlogits), _ptr(loss),
           _stream(stream))
     return dlogits, loss
+
+
+def conv_fwd_direct(x, w, b, stride=1, padding=0, y=None, stream=None):
+    """Direct (CUDA-core) forward convolution; same result definition as conv_fwd."""
+    torch = _torch()
+    _want(x, "x"), _want(w, "w")
+    if b is not None:
+        _want(b, "b")
+    s = shape_of(x.shape, w.shape, stride, padding)
+    if y is None:
+        y = torch.empty((s.batch, s.outC, s.outH, s.outW), dtype=torch.float32, device=x.device)
+    _want(y, "y")
+    _call("conv_fwd_direct", ctypes.byref(s), _ptr(x), _ptr(w), _ptr(b), _ptr(y), _stream(stream))
+    return y
+
+
+def conv_bwd_data_direct(w, dy, x_shape, stride=1, padding=0, dx=None, stream=None):
+    torch = _torch()
+    _want(w, "w"), _want(dy, "dy")
+    s = shape_of(tuple(x_shape), w.shape, stride, padding)
+    if dx is None:
+        dx = torch.empty(tuple(x_shape), dtype=torch.float32, device=dy.device)
+    _want(dx, "dx")
+    _call("conv_bwd_data_direct", ctypes.byref(s), _ptr(w), _ptr(dy), _ptr(dx), _stream(stream))
+    return dx
+
+
+def conv_bwd_filter_direct(x, dy, w_shape, stride=1, padding=0, dw=None, stream=None):
+    torch = _torch()
+    _want(x, "x"), _want(dy, "dy")
+    s = shape_of(x.shape, tuple(w_shape), stride, padding)
+    if dw is None:
+        dw = torch.empty(tuple(w_shape), dtype=torch.float32, device=x.device)
+    _want(dw, "dw")
+    _call("conv_bwd_filter_direct", ctypes.byref(s), _ptr(x), _ptr(dy), _ptr(dw), _stream(stream))
+    return dw
 
 
 CONV_MATH_FP32, CONV_MATH_TF32 = 0, 1

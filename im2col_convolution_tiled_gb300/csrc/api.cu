@@ -297,6 +297,52 @@ int sgd_step(int64_t count, float lr, float clip, float* param, const float* gra
 }
 
 // ---------------------------------------------------------------------------
+// direct convolution (legacy shaders; cross-check and small-channel ablation)
+
+static int check_direct(const conv_shape_t* s, ConvDims* d)
+{
+    int rc = check_shape(s, d);
+    if (rc != CONV_OK) return rc;
+    // grid limits (batch and 8-wide filter/channel groups on y/z) and the forward patch
+    const long long ph = 15LL * d->S + d->R;
+    if (d->N > 65535 || (d->K + 7) / 8 > 65535 || (d->C + 7) / 8 > 65535) return CONV_ERR_SHAPE;
+    if ((ph * ph + 8LL * d->R * d->R) * 4 > 200 * 1024) return CONV_ERR_SHAPE;
+    return CONV_OK;
+}
+
+int conv_fwd_direct(const conv_shape_t* s, const float* x, const float* w, const float* b, float* y,
+                    conv_stream_t stream)
+{
+    ConvDims d;
+    int rc = check_direct(s, &d);
+    if (rc != CONV_OK) return rc;
+    if ((rc = check_ptrs({x, w, y})) != CONV_OK) return rc;
+    if (b && !aligned16(b)) return CONV_ERR_ALIGN;
+    if (!device_ok()) return CONV_ERR_DEVICE;
+    return status_of(launch_conv_fwd_direct(d, x, w, b, y, as_cuda(stream)));
+}
+
+int conv_bwd_data_direct(const conv_shape_t* s, const float* w, const float* dy, float* dx, conv_stream_t stream)
+{
+    ConvDims d;
+    int rc = check_direct(s, &d);
+    if (rc != CONV_OK) return rc;
+    if ((rc = check_ptrs({w, dy, dx})) != CONV_OK) return rc;
+    if (!device_ok()) return CONV_ERR_DEVICE;
+    return status_of(launch_conv_dgrad_direct(d, w, dy, dx, as_cuda(stream)));
+}
+
+int conv_bwd_filter_direct(const conv_shape_t* s, const float* x, const float* dy, float* dw, conv_stream_t stream)
+{
+    ConvDims d;
+    int rc = check_direct(s, &d);
+    if (rc != CONV_OK) return rc;
+    if ((rc = check_ptrs({x, dy, dw})) != CONV_OK) return rc;
+    if (!device_ok()) return CONV_ERR_DEVICE;
+    return status_of(launch_conv_wgrad_direct(d, x, dy, dw, as_cuda(stream)));
+}
+
+// ---------------------------------------------------------------------------
 // training-step pieces
 
 int relu_fwd(int64_t count, const float* x, float* y, conv_stream_t stream)

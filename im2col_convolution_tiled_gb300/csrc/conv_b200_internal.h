@@ -68,6 +68,11 @@ cudaError_t launch_maxpool_bwd(int N, int C, int H, int W, int k, int s, int P, 
                                const int32_t* idx, float* dx, cudaStream_t st);
 cudaError_t launch_sgd(int64_t count, float lr, float clip, float* p, const float* g, cudaStream_t st);
 
+cudaError_t launch_conv_fwd_direct(const ConvDims& d, const float* x, const float* w, const float* b, float* y,
+                                   cudaStream_t st);
+cudaError_t launch_conv_dgrad_direct(const ConvDims& d, const float* w, const float* dy, float* dx, cudaStream_t st);
+cudaError_t launch_conv_wgrad_direct(const ConvDims& d, const float* x, const float* dy, float* dw, cudaStream_t st);
+
 cudaError_t launch_relu_fwd(int64_t n, const float* x, float* y, cudaStream_t st);
 cudaError_t launch_relu_bwd(int64_t n, const float* dy, const float* x, float* dx, cudaStream_t st);
 cudaError_t launch_grad_accum(int64_t n, const float* g, float* acc, cudaStream_t st);

@@ -173,6 +173,25 @@ int maxpool2d_bwd(int32_t batch, int32_t C, int32_t H, int32_t W, int32_t k, int
 int sgd_step(int64_t count, float lr, float clip, float *param, const float *grad, conv_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * Direct convolution: the page's legacy shaders (table "Legacy / Unused
+ * Shaders": nn_conv_forward[_tiled], nn_conv_backprop_input[_fused],
+ * nn_conv_backprop_filters[_tiled] with nn_conv_reduce_filters), which the
+ * im2col pipeline replaced.  Same definitions, layouts and overwrite rule as
+ * conv_fwd / conv_bwd_data / conv_bwd_filter, computed with fp32 fused
+ * multiply-adds on the CUDA cores (no workspace, no tensor cores), each
+ * output summed in a fixed order: a cross-check of the implicit-GEMM path and
+ * an ablation for layers with few input channels.  Each result is within
+ * n * 2^-24 * sum |a_k b_k| of the exact sum for its n terms.  Extra limits
+ * (CONV_ERR_SHAPE): batch <= 65535, and the forward's input patch for a 16x16
+ * output tile with 8 filter slices, ((15 * stride + kH)^2 + 8 * kH^2) floats,
+ * within 200 KB.
+ * ------------------------------------------------------------------------- */
+int conv_fwd_direct(const conv_shape_t *s, const float *x, const float *w, const float *b, float *y,
+                    conv_stream_t stream);
+int conv_bwd_data_direct(const conv_shape_t *s, const float *w, const float *dy, float *dx, conv_stream_t stream);
+int conv_bwd_filter_direct(const conv_shape_t *s, const float *x, const float *dy, float *dw, conv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * Training-step pieces around the convolutions (shader tables "Activation /
  * Loss Shaders" and "Utility Shaders"; the page's LeNet trainer, section
  * "LeNet on MNIST", chains them with conv, pooling, flagged matmul and SGD).

@@ -39,7 +39,8 @@ def test_header_declares_the_entry_points():
               "col2im", "matmul",
               "maxpool2d_fwd", "maxpool2d_bwd", "sgd_step", "conv_b200_strerror", "conv_b200_check",
               "conv_b200_workspace_bytes", "relu_fwd", "relu_bwd", "grad_accum", "add_bias", "bias_grad_rows",
-              "softmax_ce", "conv_b200_set_math_mode", "conv_b200_math_mode"]:
+              "softmax_ce", "conv_b200_set_math_mode", "conv_b200_math_mode", "conv_fwd_direct",
+              "conv_bwd_data_direct", "conv_bwd_filter_direct"]:
         assert n in names
 
 
