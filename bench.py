@@ -320,6 +320,13 @@ def run_ours(args):
             traffic = int(m.group(1))
 
     # --- end to end through the public API with host buffers ---------------
+    # Every step uploads its inputs (x, w, b, dy and the pool gradients) from
+    # pinned host memory and reads all its results back (y, dx, dw, db and the
+    # pool input gradients).  Two sets of device buffers alternate between
+    # steps, as a training loop double-buffers its batches: step i + 1's
+    # uploads run on one copy stream and step i - 1's read-backs on another
+    # while step i computes.  Within a step, layer i's compute waits only for
+    # layer i's uploads, and its results go back as soon as it is done.
     pin = lambda a: torch.from_numpy(a).pin_memory()
     host_in = [{k: pin(v) for k, v in b.host.items()} for b in bufs]
     host_out = [{"y": torch.empty(b.L.y_shape).pin_memory(), "dx": torch.empty(b.L.x_shape).pin_memory(),
@@ -327,46 +334,56 @@ def run_ours(args):
                  "dxp": torch.empty(b.L.y_shape).pin_memory() if b.pool else None} for b in bufs]
     h2d = sum(b.bytes_in() for b in bufs)
     d2h = sum(b.bytes_out() for b in bufs)
-
-    # Per-layer pipelining: layer i's host->device copies run on their own
-    # stream ahead of its compute, and its results go back on a third stream
-    # while the next layers compute; every step ends with all copies done.
+    sets = [bufs, [LayerBufs(L, torch, cb) for L in LAYERS]]
     s_h2d, s_d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_free_in = [torch.cuda.Event() for _ in sets]     # compute of the set's last step is done
+    ev_free_out = [torch.cuda.Event() for _ in sets]    # read-back of the set's last step is done
+    for e_ in ev_free_in + ev_free_out:
+        e_.record(stream)
 
-    def e2e_step():
-        ev_in = [torch.cuda.Event() for _ in bufs]
-        ev_out = [torch.cuda.Event() for _ in bufs]
+    def e2e_step(i):
+        cur = sets[i % 2]
+        ev_in = [torch.cuda.Event() for _ in cur]
+        ev_out = [torch.cuda.Event() for _ in cur]
         with torch.cuda.stream(s_h2d):
-            for i, (b, hi) in enumerate(zip(bufs, host_in)):
+            s_h2d.wait_event(ev_free_in[i % 2])
+            for j, (b, hi) in enumerate(zip(cur, host_in)):
                 b.x.copy_(hi["x"], non_blocking=True)
                 b.w.copy_(hi["w"], non_blocking=True)
                 b.b.copy_(hi["b"], non_blocking=True)
                 b.dy.copy_(hi["dy"], non_blocking=True)
                 if b.pool:
                     b.dyp.copy_(hi["dyp"], non_blocking=True)
-                ev_in[i].record(s_h2d)
-        for i, b in enumerate(bufs):
-            stream.wait_event(ev_in[i])
+                ev_in[j].record(s_h2d)
+        stream.wait_event(ev_free_out[i % 2])
+        for j, b in enumerate(cur):
+            stream.wait_event(ev_in[j])
             run_layer(b, None)
-            ev_out[i].record(stream)
+            ev_out[j].record(stream)
             with torch.cuda.stream(s_d2h):
-                s_d2h.wait_event(ev_out[i])
-                ho = host_out[i]
+                s_d2h.wait_event(ev_out[j])
+                ho = host_out[j]
                 ho["y"].copy_(b.y, non_blocking=True)
                 ho["dx"].copy_(b.dx, non_blocking=True)
                 ho["dw"].copy_(b.dw, non_blocking=True)
                 ho["db"].copy_(b.db, non_blocking=True)
                 if b.pool:
                     ho["dxp"].copy_(b.dxp, non_blocking=True)
+        ev_free_in[i % 2].record(stream)
+        ev_free_out[i % 2].record(s_d2h)
+
+    def e2e_run(n):
+        for i in range(n):
+            e2e_step(i)
+        s_h2d.synchronize()
         s_d2h.synchronize()
         stream.synchronize()
 
     e2e_steps = max(3, args.steps // 4)
-    e2e_step()
+    e2e_run(2)
     barrier()
     t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
+    e2e_run(e2e_steps)
     barrier()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
     if dist is not None:
