@@ -55,6 +55,25 @@ def peaks():
     return 1900.0, 6800.0, "fallback"
 
 
+def max_over_ranks(x, dist=None) -> float:
+    """The largest value of x over all ranks (x itself on one process): every
+    rank's timed region must be done before the job's is."""
+    if dist is None:
+        return float(x)
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank, ms_max, world) -> float:
+    """Whole-job throughput of independent replicas (weak scaling): every rank
+    processes units_per_rank per step, the job's step takes the slowest rank's
+    time.  Units per second."""
+    return world * units_per_rank / (ms_max * 1e-3)
+
+
 def step_flops(layers) -> int:
     return sum(3 * L.gemm_flops for L in layers)
 
@@ -279,13 +298,10 @@ def run_ours(args):
     launches = cb.launch_count() - n0
     cb.check()
     ms_total = t_start.elapsed_time(t_end)
-    if dist is not None:
-        t = torch.tensor([ms_total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dist)
     ms_step = ms_total / args.steps
     flops = step_flops(LAYERS)
-    value = world * flops / (ms_step * 1e-3) / 1e12
+    value = job_rate(flops, ms_step, world) / 1e12
 
     avg = {k: sum(a.elapsed_time(b) for a, b in v) / len(v) for k, v in rec.items()}
     per_layer = []
@@ -386,10 +402,7 @@ def run_ours(args):
     e2e_run(e2e_steps)
     barrier()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist)
     cb.check()
 
     cpu = None
@@ -417,7 +430,7 @@ def run_ours(args):
                      "peak_basis": ("%s bf16 %.1f TFLOP/s x %.3f (TF32/BF16)" % (peak_kind, bf16, TF32_OVER_BF16) +
                                     ("" if fast else " / 3 (3xTF32)"))},
         "per_layer": per_layer,
-        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": UNIT,
+        "e2e": {"value": round(job_rate(flops, e2e_ms, world) / 1e12, 3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
         "gpu_launches": launches,
         "clocks": clk.summary(),
@@ -533,11 +546,8 @@ def run_lenet(args):
         barrier()
     cb.check()
     ms = e0.elapsed_time(e1) / args.steps
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * B / (ms * 1e-3)
+    ms = max_over_ranks(ms, dist)
+    value = job_rate(B, ms, world)
 
     # end to end: each step's batch goes up from pinned host memory and its loss comes back
     hx = torch.from_numpy(x).pin_memory()
@@ -552,7 +562,7 @@ def run_lenet(args):
         hloss.copy_(net.t["loss"], non_blocking=True)
     stream.synchronize()
     barrier()
-    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / args.steps, dist)
     cb.check()
 
     cpu = None
@@ -576,7 +586,7 @@ def run_lenet(args):
                      "achieved": round(flops / (ms * 1e-3) / 1e12, 4), "unit": "TFLOP/s", "peak": None,
                      "frac": None, "traffic": None,
                      "note": "dependent launches of small kernels; the graph removes the host issue cost"},
-        "e2e": {"value": round(world * B / (e2e_ms * 1e-3), 1), "unit": "images/s",
+        "e2e": {"value": round(job_rate(B, e2e_ms, world), 1), "unit": "images/s",
                 "h2d_bytes_per_step": int(x.nbytes + labels.nbytes), "d2h_bytes_per_step": 4,
                 "ms_per_step": round(e2e_ms, 4)},
         "gpu_launches": launches_per_step * args.steps,
