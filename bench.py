@@ -303,7 +303,8 @@ def run_ours(args):
     flops = step_flops(LAYERS)
     value = job_rate(flops, ms_step, world) / 1e12
 
-    avg = {k: sum(a.elapsed_time(b) for a, b in v) / len(v) for k, v in rec.items()}
+    times = {k: sorted(a.elapsed_time(b) for a, b in v) for k, v in rec.items()}
+    avg = {k: sum(v) / len(v) for k, v in times.items()}
     per_layer = []
     gemm_ms = 0.0
     for b in bufs:
@@ -312,7 +313,9 @@ def run_ours(args):
         d = {"layer": L.name}
         for op in ops:
             if (L.name, op) in avg:
+                v = times[(L.name, op)]
                 d[op + "_ms"] = round(avg[(L.name, op)], 4)
+                d[op + "_ms_median_min_max"] = [round(statistics.median(v), 4), round(v[0], 4), round(v[-1], 4)]
         for op in ("fwd", "dgrad", "wgrad"):
             d[op + "_tflops"] = round(g / (avg[(L.name, op)] * 1e-3) / 1e12, 2)
             gemm_ms += avg[(L.name, op)]
