@@ -184,17 +184,40 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # our arm
 
+class ParamStore:
+    """Every layer's filters and bias in one flat device buffer and their
+    gradients in another (each tensor a view starting on a 16-byte boundary),
+    so that one SGD call updates all parameters of the step.  The padding slots
+    between views hold 0 in both buffers, so SGD leaves them unchanged."""
+
+    def __init__(self, layers, torch):
+        shapes = []
+        for L in layers:
+            shapes += [L.w_shape, (L.outC,)]
+        sizes = [int(np.prod(sh)) for sh in shapes]
+        offs, n = [], 0
+        for sz in sizes:
+            offs.append(n)
+            n += (sz + 3) // 4 * 4
+        self.p = torch.zeros(n, device="cuda")
+        self.g = torch.zeros(n, device="cuda")
+        self.views = [(self.p[o:o + sz].view(sh), self.g[o:o + sz].view(sh))
+                      for o, sz, sh in zip(offs, sizes, shapes)]
+
+
 class LayerBufs:
-    def __init__(self, L, torch, cb):
+    def __init__(self, L, torch, cb, params):
+        """params: (w, dw, b, db) views of a ParamStore."""
         self.L = L
         x, w, b, dy = L.make()
         self.host = {"x": x, "w": w, "b": b, "dy": dy}
         dev = lambda a: torch.from_numpy(a).cuda()
-        self.x, self.w, self.b, self.dy = dev(x), dev(w), dev(b), dev(dy)
+        self.x, self.dy = dev(x), dev(dy)
+        self.w, self.dw, self.b, self.db = params
+        self.w.copy_(torch.from_numpy(w))
+        self.b.copy_(torch.from_numpy(b))
         self.y = torch.empty(L.y_shape, device="cuda")
         self.dx = torch.empty(L.x_shape, device="cuda")
-        self.dw = torch.empty(L.w_shape, device="cuda")
-        self.db = torch.empty((L.outC,), device="cuda")
         self.pool = None
         if L.pool:
             k, s = L.pool
@@ -238,11 +261,17 @@ def run_ours(args):
     fast = args.math == "tf32"
     cb.set_math_mode(cb.CONV_MATH_TF32 if fast else cb.CONV_MATH_FP32)
 
-    bufs = [LayerBufs(L, torch, cb) for L in LAYERS]
+    def make_set():
+        store = ParamStore(LAYERS, torch)
+        v = store.views
+        return store, [LayerBufs(L, torch, cb, (v[2 * i][0], v[2 * i][1], v[2 * i + 1][0], v[2 * i + 1][1]))
+                       for i, L in enumerate(LAYERS)]
+
+    store, bufs = make_set()
     ws = torch.empty(max(b.ws_bytes for b in bufs) + 16, dtype=torch.uint8, device="cuda")
     lr, clip = synthetic.SGD_LR_CLIP
     stream = torch.cuda.current_stream()
-    ops = ["fwd", "pool", "dgrad", "wgrad", "sgd"]   # wgrad includes the bias gradient
+    ops = ["fwd", "pool", "dgrad", "wgrad"]   # wgrad includes the bias gradient; SGD runs once per step
     rec = {}   # (layer, op) -> list of (start_event, end_event)
 
     def timed(key, fn):
@@ -269,11 +298,15 @@ def run_ours(args):
         # filter and bias gradients from one pass over dy (conv_bwd_filter_bias)
         timed(key("wgrad"), lambda: cb.conv_bwd_filter_bias(b.x, b.dy, L.w_shape, L.stride, L.pad, dw=b.dw,
                                                             db=b.db, workspace=ws))
-        timed(key("sgd"), lambda: (cb.sgd_step(b.w, b.dw, lr, clip), cb.sgd_step(b.b, b.db, lr, clip)))
+
+    def sgd(st_, record):
+        # SGD on every filter and bias of the step, one launch over the flat store
+        timed(("step", "sgd") if record else None, lambda: cb.sgd_step(st_.p, st_.g, lr, clip))
 
     def step(record):
         for b in bufs:
             run_layer(b, record)
+        sgd(store, record)
 
     def barrier():
         torch.cuda.synchronize()
@@ -353,7 +386,7 @@ def run_ours(args):
                  "dxp": torch.empty(b.L.y_shape).pin_memory() if b.pool else None} for b in bufs]
     h2d = sum(b.bytes_in() for b in bufs)
     d2h = sum(b.bytes_out() for b in bufs)
-    sets = [bufs, [LayerBufs(L, torch, cb) for L in LAYERS]]
+    sets = [(store, bufs), make_set()]
     s_h2d, s_d2h = torch.cuda.Stream(), torch.cuda.Stream()
     ev_free_in = [torch.cuda.Event() for _ in sets]     # compute of the set's last step is done
     ev_free_out = [torch.cuda.Event() for _ in sets]    # read-back of the set's last step is done
@@ -361,7 +394,7 @@ def run_ours(args):
         e_.record(stream)
 
     def e2e_step(i):
-        cur = sets[i % 2]
+        cur_store, cur = sets[i % 2]
         ev_in = [torch.cuda.Event() for _ in cur]
         ev_out = [torch.cuda.Event() for _ in cur]
         with torch.cuda.stream(s_h2d):
@@ -378,6 +411,8 @@ def run_ours(args):
         for j, b in enumerate(cur):
             stream.wait_event(ev_in[j])
             run_layer(b, None)
+            if j == len(cur) - 1:
+                sgd(cur_store, False)
             ev_out[j].record(stream)
             with torch.cuda.stream(s_d2h):
                 s_d2h.wait_event(ev_out[j])
@@ -433,6 +468,7 @@ def run_ours(args):
                      "peak_basis": ("%s bf16 %.1f TFLOP/s x %.3f (TF32/BF16)" % (peak_kind, bf16, TF32_OVER_BF16) +
                                     ("" if fast else " / 3 (3xTF32)"))},
         "per_layer": per_layer,
+        "sgd_ms_per_step": round(avg[("step", "sgd")], 4),
         "e2e": {"value": round(job_rate(flops, e2e_ms, world) / 1e12, 3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
         "gpu_launches": launches,
