@@ -137,35 +137,45 @@ __global__ void __launch_bounds__(kS2dThreads, 4)
         mbar_fence_init();
     }
     __syncthreads();
-    // stage super-row `item` into buffer b
+    // stage super-row `item` into buffer b.  Rows outside the image are
+    // zero-filled by every thread; with bulk copies the lanes of warp 0 issue
+    // one input row each (the byte count of the stage summed over the warp
+    // first), so no single thread walks all C * S rows.
     auto stage = [&](int item, int b) {
         uint32_t n, hh;
         f_hs.divmod(uint32_t(item), n, hh);
         float* buf = s2d_rows + b * buf_floats;
-        int live = 0;
-        if (bulk && threadIdx.x == 0) fence_proxy_async_smem();   // the buffer's last readers are done
         int c = 0, a = 0;   // (c, a) of row ca, advanced without divisions
         for (int ca = 0; ca < CS; ++ca) {
             const int h = S * int(hh) + a - pad;
             float* row = buf + ca * pitch;
             if (unsigned(h) < unsigned(H)) {
-                const float* src = x + ((size_t(n) * C + c) * H + h) * W;
-                if (!bulk)
+                if (!bulk) {
+                    const float* src = x + ((size_t(n) * C + c) * H + h) * W;
                     for (int w = threadIdx.x; w < W; w += kS2dThreads) cp_async4(smem_u32(row + w), src + w);
-                ++live;
+                }
             } else {
                 for (int w = threadIdx.x; w < W; w += kS2dThreads) row[w] = 0.f;
             }
             if (++a == S) { a = 0; ++c; }
         }
-        if (bulk && threadIdx.x == 0) {
-            mbar_arrive_expect_tx(&bar[b], uint32_t(live) * uint32_t(W) * 4u);
-            c = 0, a = 0;
-            for (int ca = 0; ca < CS; ++ca) {
-                const int h = S * int(hh) + a - pad;
+        if (bulk && threadIdx.x < 32) {
+            const int lane = threadIdx.x;
+            fence_proxy_async_smem();   // the buffer's last readers are done (they passed the barrier)
+            uint32_t live = 0;
+            for (int ca = lane; ca < CS; ca += 32) {
+                const int h = S * int(hh) + ca % S - pad;
+                live += unsigned(h) < unsigned(H) ? 1u : 0u;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) live += __shfl_xor_sync(0xffffffffu, live, o);
+            if (lane == 0) mbar_arrive_expect_tx(&bar[b], live * uint32_t(W) * 4u);
+            __syncwarp();
+            for (int ca = lane; ca < CS; ca += 32) {
+                const int cc = ca / S, aa = ca - cc * S;
+                const int h = S * int(hh) + aa - pad;
                 if (unsigned(h) < unsigned(H))
-                    bulk_g2s(buf + ca * pitch, x + ((size_t(n) * C + c) * H + h) * W, uint32_t(W) * 4u, &bar[b]);
-                if (++a == S) { a = 0; ++c; }
+                    bulk_g2s(buf + ca * pitch, x + ((size_t(n) * C + cc) * H + h) * W, uint32_t(W) * 4u, &bar[b]);
             }
         }
         if (!bulk) cp_async_commit();
@@ -177,12 +187,9 @@ __global__ void __launch_bounds__(kS2dThreads, 4)
         else if (!bulk) cp_async_commit();   // keep one group per buffer slot
     }
     for (; item < items; item += gridDim.x, ++it) {
-        const int ahead = item + (kS2dBufs - 1) * int(gridDim.x);
-        if (ahead < items) stage(ahead, (it + kS2dBufs - 1) % kS2dBufs);
-        else if (!bulk) cp_async_commit();
         bool got = true;
         if (bulk) got = mbar_wait(&bar[it % kS2dBufs], uint32_t(it / kS2dBufs) & 1u, &abort_flag);
-        else cp_async_wait_group<kS2dBufs - 1>();   // this thread's copies of the current super-row landed
+        else cp_async_wait_group<kS2dBufs - 2>();   // this thread's copies of the current super-row landed
         if (!__syncthreads_and(got ? 1 : 0)) {      // ... and everybody else's
             if (threadIdx.x == 0) {
                 abort_flag = 1;
@@ -190,6 +197,11 @@ __global__ void __launch_bounds__(kS2dThreads, 4)
             }
             break;
         }
+        // Every thread is past this barrier, hence done reading the buffer of
+        // the previous super-row: refill that one with the super-row two ahead.
+        const int ahead = item + (kS2dBufs - 1) * int(gridDim.x);
+        if (ahead < items) stage(ahead, (it + kS2dBufs - 1) % kS2dBufs);
+        else if (!bulk) cp_async_commit();
         const float* buf = s2d_rows + (it % kS2dBufs) * buf_floats;
         uint32_t n, hh;
         f_hs.divmod(uint32_t(item), n, hh);
@@ -238,12 +250,13 @@ __global__ void __launch_bounds__(kS2dThreads, 4)
                 }
             }
         }
-        __syncthreads();   // the buffer is restaged next iteration
     }
     if (!bulk) cp_async_wait_group<0>();
     if (bulk && abort_flag && threadIdx.x == 0) {
-        // copies still in flight land before the block's shared memory goes away
-        for (int j = 0; j < kS2dBufs; ++j) {
+        // copies still in flight (the failed super-row's and the next one's:
+        // refills happen only after a passed barrier) land before the block's
+        // shared memory goes away
+        for (int j = 0; j < kS2dBufs - 1; ++j) {
             const int pending = item + j * int(gridDim.x);
             if (pending >= items) break;
             uint64_t t0 = globaltimer_ns();
