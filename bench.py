@@ -16,7 +16,8 @@ bounded sample of the same workload instead (host cores only).
 whole step captured as one CUDA graph, in training images/s.  `--math tf32`
 runs the contractions as one TF32 product (the fast mode) and reports them
 against the TF32 roofline.  `--workload direct` times the direct (CUDA-core)
-convolution kernels against the implicit-GEMM path (an ablation).
+convolution kernels against the implicit-GEMM path (an ablation);
+`--workload matmul` times the flagged matmul on shapes of its sweep.
 """
 from __future__ import annotations
 
@@ -705,6 +706,71 @@ def run_direct(args):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# flagged matmul (--workload matmul): shapes of the matmul sweep, every flag
+
+MATMUL_METRIC = "flagged fp32 matmul C = op(A) op(B): TFLOP/s (3xTF32 on tcgen05) and % of tensor roofline"
+MATMUL_SHAPES = [(9216, 9216, 4096), (4096, 4096, 4096), (9216, 9216, 363), (1024, 1024, 1600), (128, 9216, 2304),
+                 (16, 4096, 4096), (127, 127, 150)]
+
+
+def run_matmul(args):
+    import torch
+    import im2col_convolution_tiled_gb300 as cb
+
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    if not os.path.exists(cb.LIB_PATH):
+        from im2col_convolution_tiled_gb300 import build
+        build.build()
+    cb.load()
+    bf16, _, peak_kind = peaks()
+    peak = bf16 * TF32_OVER_BF16 / SPLIT_PRODUCTS
+    stream = torch.cuda.current_stream()
+    rows = []
+    flops_all, ms_all = 0, 0.0
+    with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
+        for M, N, K in MATMUL_SHAPES:
+            for flags in range(4):
+                A, B = synthetic.matmul_case(M, K, N, flags)
+                a, b = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+                c = torch.empty((M, N), device="cuda")
+                reps = args.steps if M * N * K < 2 ** 32 else max(3, args.steps // 5)
+                for _ in range(args.warmup):
+                    cb.matmul(a, b, flags, C=c)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize()
+                e0.record(stream)
+                for _ in range(reps):
+                    cb.matmul(a, b, flags, C=c)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ms = e0.elapsed_time(e1) / reps
+                f = 2 * M * N * K
+                flops_all += f
+                ms_all += ms
+                rows.append({"M": M, "N": N, "K": K, "flags": flags, "ms": round(ms, 4),
+                             "tflops": round(f / (ms * 1e-3) / 1e12, 2), "frac": round(f / (ms * 1e-3) / 1e12 / peak, 4)})
+    cb.check()
+    big = [r for r in rows if (r["M"], r["N"], r["K"]) == MATMUL_SHAPES[0]]
+    value = sum(2 * r["M"] * r["N"] * r["K"] for r in big) / (sum(r["ms"] for r in big) * 1e-3) / 1e12
+    line = {
+        "metric": MATMUL_METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "largest sweep shape M=N=9216, K=4096, all four flags (value); the table covers "
+                               "further sweep shapes", "shapes": rows,
+                   "all_shapes_tflops": round(flops_all / (ms_all * 1e-3) / 1e12, 2),
+                   "l2": "no flush: operands of the value's shape are 0.6 GB (> 126 MB L2)"},
+        "roofline": {"bound": "tensor", "achieved": round(value, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
+                     "frac": round(value / peak, 4), "traffic": None,
+                     "peak_basis": "%s bf16 %.1f TFLOP/s x %.3f (TF32/BF16) / 3 (3xTF32)"
+                                   % (peak_kind, bf16, TF32_OVER_BF16)},
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -714,7 +780,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-batch", type=int, default=64)
     ap.add_argument("--ref-batch", type=int, default=1)
-    ap.add_argument("--workload", choices=["alexnet", "lenet", "direct"], default="alexnet")
+    ap.add_argument("--workload", choices=["alexnet", "lenet", "direct", "matmul"], default="alexnet")
     ap.add_argument("--math", choices=["fp32", "tf32"], default="fp32",
                     help="contractions in fp32-faithful 3xTF32 (default) or one TF32 product")
     args = ap.parse_args()
@@ -723,6 +789,8 @@ def main():
         (run_lenet_reference if args.impl == "reference" else run_lenet)(args)
     elif args.workload == "direct":
         run_direct(args)
+    elif args.workload == "matmul":
+        run_matmul(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
