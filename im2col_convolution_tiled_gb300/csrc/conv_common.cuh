@@ -107,187 +107,95 @@ cudaError_t build_bimage(const Gen& gen, int n_rows, int k_total, int bn, float*
 // (zero for c' >= C*S*S) that the tensor-map patch kernel loads; otherwise
 // NCHW [n][c'][hh][ww] for the filter gradient's column gather.
 //
-// Persistent blocks take super-rows (n, hh) in turn.  The C*S input rows of a
-// super-row are staged in shared memory, kS2dBufs super-rows deep, so that the
-// reads of the next ones are in flight while one is written out: with one bulk
-// copy per row (the copy engine, completion on a per-buffer mbarrier) when rows
-// start on 16-byte boundaries (W a multiple of 4), else with 4-byte cp.async.
-// Shared rows have a pitch of 4 mod 32 floats, so the lanes of a warp reading
-// (b, a, c) neighbours hit distinct banks.  Waits are bounded; on give-up the
-// block records the error and leaves after its copies have landed.
-__host__ __device__ inline int s2d_pitch(int W) { return W + ((4 - W) % 32 + 32) % 32; }
-
-constexpr int kS2dThreads = 256;
-constexpr int kS2dBufs = 3;
+// A gather with no shared memory and no barriers: one output vector per
+// thread, every load it needs issued up front.  (A persistent form that staged
+// each super-row's input rows in shared memory through bulk copies ran at a
+// third of the copy bandwidth: one block-wide barrier per 15 KB super-row.)
+//   BLOCKED: thread t writes float4 t of [n][c'/32][hh][ww][32], i.e. channels
+//            c' = 32*cb + 4*g .. + 3 of one super-pixel (g = t % 8): eight
+//            threads fill a 128-byte pixel, a warp four whole pixels.
+//   NCHW:    thread t = (((n*C + c)*S + a)*Hs + hh)*Ws + ww reads the S
+//            consecutive inputs x[n, c, S*hh + a - pad, S*ww - pad ..] and
+//            writes them to planes c' = (c*S + a)*S + b, b < S; lanes run
+//            along ww, so loads and stores are contiguous per warp.
+constexpr int kS2dGatherThreads = 256;
+constexpr int kS2dLoads = 8;   // NCHW form: loads issued together
 
 template <bool BLOCKED>
-__global__ void __launch_bounds__(kS2dThreads, 4)
-    s2d_copy_kernel(const float* __restrict__ x, float* __restrict__ dst, int C, int H, int W, int S, int pad, int Cs,
-                    int Cb, int Hs, int Ws, int items, FastDiv f_s, FastDiv f_ss, FastDiv f_hs, int* err)
+__global__ void __launch_bounds__(kS2dGatherThreads)
+    s2d_gather_kernel(const float* __restrict__ x, float* __restrict__ dst, int C, int H, int W, int S, int pad,
+                      int Cs, long long total, FastDiv f_ws, FastDiv f_hs, FastDiv f_mid, FastDiv f_s, FastDiv f_ss)
 {
-    extern __shared__ __align__(16) float s2d_rows[];   // kS2dBufs buffers of [c * S + a][pitch]
-    __shared__ uint64_t bar[kS2dBufs];
-    __shared__ int abort_flag;
-    const int CS = C * S, pitch = s2d_pitch(W);
-    const int buf_floats = CS * pitch;
-    const bool bulk = (W & 3) == 0;
-    if (threadIdx.x == 0) {
-        for (int b = 0; b < kS2dBufs; ++b) mbar_init(&bar[b], 1);
-        abort_flag = 0;
-        mbar_fence_init();
-    }
-    __syncthreads();
-    // stage super-row `item` into buffer b.  Rows outside the image are
-    // zero-filled by every thread; with bulk copies the lanes of warp 0 issue
-    // one input row each (the byte count of the stage summed over the warp
-    // first), so no single thread walks all C * S rows.
-    auto stage = [&](int item, int b) {
-        uint32_t n, hh;
-        f_hs.divmod(uint32_t(item), n, hh);
-        float* buf = s2d_rows + b * buf_floats;
-        int c = 0, a = 0;   // (c, a) of row ca, advanced without divisions
-        for (int ca = 0; ca < CS; ++ca) {
-            const int h = S * int(hh) + a - pad;
-            float* row = buf + ca * pitch;
-            if (unsigned(h) < unsigned(H)) {
-                if (!bulk) {
-                    const float* src = x + ((size_t(n) * C + c) * H + h) * W;
-                    for (int w = threadIdx.x; w < W; w += kS2dThreads) cp_async4(smem_u32(row + w), src + w);
-                }
-            } else {
-                for (int w = threadIdx.x; w < W; w += kS2dThreads) row[w] = 0.f;
-            }
-            if (++a == S) { a = 0; ++c; }
+    const long long t = (long long)blockIdx.x * kS2dGatherThreads + threadIdx.x;
+    if (t >= total) return;
+    if constexpr (BLOCKED) {
+        // t = (((n * Cb + cb) * Hs + hh) * Ws + ww) * 8 + g; f_mid divides by Cb
+        const uint32_t g = uint32_t(t) & 7u;
+        uint32_t r, ww, hh, cb, n;
+        f_ws.divmod(uint32_t(t >> 3), r, ww);
+        f_hs.divmod(r, r, hh);
+        f_mid.divmod(r, n, cb);
+        float v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int cp = int(cb) * 32 + 4 * int(g) + e;
+            uint32_t c, ab, a, b;
+            f_ss.divmod(uint32_t(cp), c, ab);
+            f_s.divmod(ab, a, b);
+            const int h = S * int(hh) + int(a) - pad, w = S * int(ww) + int(b) - pad;
+            const bool in = cp < Cs && unsigned(h) < unsigned(H) && unsigned(w) < unsigned(W);
+            v[e] = in ? __ldg(x + ((size_t(n) * C + c) * H + h) * W + w) : 0.f;
         }
-        if (bulk && threadIdx.x < 32) {
-            const int lane = threadIdx.x;
-            fence_proxy_async_smem();   // the buffer's last readers are done (they passed the barrier)
-            uint32_t live = 0;
-            for (int ca = lane; ca < CS; ca += 32) {
-                const int h = S * int(hh) + ca % S - pad;
-                live += unsigned(h) < unsigned(H) ? 1u : 0u;
+        reinterpret_cast<float4*>(dst)[t] = make_float4(v[0], v[1], v[2], v[3]);
+    } else {
+        // t = (((n * C + c) * S + a) * Hs + hh) * Ws + ww; f_mid divides by C
+        uint32_t r, ww, hh, a, c, n;
+        f_ws.divmod(uint32_t(t), r, ww);
+        f_hs.divmod(r, r, hh);
+        f_s.divmod(r, r, a);
+        f_mid.divmod(r, n, c);
+        const int Hs = int(f_hs.d), Ws = int(f_ws.d);
+        const int h = S * int(hh) + int(a) - pad;
+        const bool row_in = unsigned(h) < unsigned(H);
+        const float* src = x + ((size_t(n) * C + c) * H + (row_in ? h : 0)) * W;
+        float* out = dst + ((size_t(n) * Cs + (int(c) * S + int(a)) * S) * Hs + hh) * Ws + ww;
+        if (S <= kS2dLoads) {
+            // one pass, fully unrolled (a loop around it measured 6% slower on AlexNet conv1)
+            float v[kS2dLoads];
+#pragma unroll
+            for (int b = 0; b < kS2dLoads; ++b) {
+                const int w = S * int(ww) + b - pad;
+                v[b] = (b < S && row_in && unsigned(w) < unsigned(W)) ? __ldg(src + w) : 0.f;
             }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) live += __shfl_xor_sync(0xffffffffu, live, o);
-            if (lane == 0) mbar_arrive_expect_tx(&bar[b], live * uint32_t(W) * 4u);
-            __syncwarp();
-            for (int ca = lane; ca < CS; ca += 32) {
-                const int cc = ca / S, aa = ca - cc * S;
-                const int h = S * int(hh) + aa - pad;
-                if (unsigned(h) < unsigned(H))
-                    bulk_g2s(buf + ca * pitch, x + ((size_t(n) * C + cc) * H + h) * W, uint32_t(W) * 4u, &bar[b]);
-            }
+            for (int b = 0; b < kS2dLoads; ++b)
+                if (b < S) out[size_t(b) * Hs * Ws] = v[b];
+            return;
         }
-        if (!bulk) cp_async_commit();
-    };
-    int it = 0, item = blockIdx.x;
-    for (int i = 0; i < kS2dBufs - 1; ++i) {
-        const int pre = item + i * int(gridDim.x);
-        if (pre < items) stage(pre, i);
-        else if (!bulk) cp_async_commit();   // keep one group per buffer slot
-    }
-    for (; item < items; item += gridDim.x, ++it) {
-        bool got = true;
-        if (bulk) got = mbar_wait(&bar[it % kS2dBufs], uint32_t(it / kS2dBufs) & 1u, &abort_flag);
-        else cp_async_wait_group<kS2dBufs - 2>();   // this thread's copies of the current super-row landed
-        if (!__syncthreads_and(got ? 1 : 0)) {      // ... and everybody else's
-            if (threadIdx.x == 0) {
-                abort_flag = 1;
-                atomicOr(err, kDevErrTimeout);
-            }
-            break;
-        }
-        // Every thread is past this barrier, hence done reading the buffer of
-        // the previous super-row: refill that one with the super-row two ahead.
-        const int ahead = item + (kS2dBufs - 1) * int(gridDim.x);
-        if (ahead < items) stage(ahead, (it + kS2dBufs - 1) % kS2dBufs);
-        else if (!bulk) cp_async_commit();
-        const float* buf = s2d_rows + (it % kS2dBufs) * buf_floats;
-        uint32_t n, hh;
-        f_hs.divmod(uint32_t(item), n, hh);
-        // A thread owns four consecutive channels c' = 4g .. 4g + 3 of a 32-channel
-        // block: their rows and column offsets are decoded once per block, then
-        // each pixel costs four shared loads.  Blocked: g = thread % 8 and eight
-        // threads write a pixel; NCHW: g = warp and the lanes run along ww.
-        const int g4 = BLOCKED ? (threadIdx.x & 7) : (threadIdx.x >> 5);
-        const int ww0 = BLOCKED ? (threadIdx.x >> 3) : (threadIdx.x & 31);
-        for (int cb = 0; cb < Cb; ++cb) {
-            const float* row[4];
-            int boff[4];
-            bool live[4];
+        for (int b0 = 0; b0 < S; b0 += kS2dLoads) {
+            float v[kS2dLoads];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                uint32_t c, ab, a, b;
-                f_ss.divmod(uint32_t(cb * 32 + 4 * g4 + e), c, ab);
-                f_s.divmod(ab, a, b);
-                live[e] = int(c) < C;
-                row[e] = buf + (live[e] ? (int(c) * S + int(a)) * pitch : 0);
-                boff[e] = int(b) - pad;
+            for (int i = 0; i < kS2dLoads; ++i) {
+                const int w = S * int(ww) + b0 + i - pad;
+                v[i] = (b0 + i < S && row_in && unsigned(w) < unsigned(W)) ? __ldg(src + w) : 0.f;
             }
-            if constexpr (BLOCKED) {
-                // eight threads write one 128-byte pixel with 16-byte stores
-                float4* out = reinterpret_cast<float4*>(dst + ((size_t(n) * Cb + cb) * Hs + hh) * size_t(Ws) * 32);
-                for (int ww = ww0; ww < Ws; ww += 32) {
-                    float v[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int w = S * ww + boff[e];
-                        v[e] = (live[e] && unsigned(w) < unsigned(W)) ? row[e][w] : 0.f;
-                    }
-                    out[ww * 8 + g4] = make_float4(v[0], v[1], v[2], v[3]);
-                }
-            } else {
-                // channels of the block past Cs do not exist in NCHW
-                const int cp0 = cb * 32 + 4 * g4;
-                for (int ww = ww0; ww < Ws; ww += 32) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        if (cp0 + e >= Cs) break;
-                        const int w = S * ww + boff[e];
-                        dst[((size_t(n) * Cs + cp0 + e) * Hs + hh) * size_t(Ws) + ww] =
-                            (live[e] && unsigned(w) < unsigned(W)) ? row[e][w] : 0.f;
-                    }
-                }
-            }
-        }
-    }
-    if (!bulk) cp_async_wait_group<0>();
-    if (bulk && abort_flag && threadIdx.x == 0) {
-        // copies still in flight (the failed super-row's and the next one's:
-        // refills happen only after a passed barrier) land before the block's
-        // shared memory goes away
-        for (int j = 0; j < kS2dBufs - 1; ++j) {
-            const int pending = item + j * int(gridDim.x);
-            if (pending >= items) break;
-            uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(&bar[(it + j) % kS2dBufs], uint32_t((it + j) / kS2dBufs) & 1u) &&
-                   globaltimer_ns() - t0 < kWaitLimitNs) {
-            }
+            for (int i = 0; i < kS2dLoads; ++i)
+                if (b0 + i < S) out[size_t(b0 + i) * Hs * Ws] = v[i];
         }
     }
 }
-
-// Shared memory of s2d_copy_kernel (kS2dBufs buffers of staged rows).
-inline size_t s2d_copy_smem(int C, int S, int W) { return kS2dBufs * size_t(C) * S * s2d_pitch(W) * sizeof(float); }
-constexpr size_t kS2dMaxSmem = 96 * 1024;
 
 template <bool BLOCKED>
 cudaError_t launch_s2d_copy(const float* x, float* dst, int N, int C, int H, int W, int S, int pad, int Hs, int Ws,
                             cudaStream_t st)
 {
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(s2d_copy_kernel<BLOCKED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             int(kS2dMaxSmem));
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
     const int Cs = C * S * S, Cb = (Cs + 31) / 32;
-    const int items = N * Hs;
-    const int grid = items < 4 * sm_count() ? items : 4 * sm_count();
-    s2d_copy_kernel<BLOCKED><<<grid, kS2dThreads, s2d_copy_smem(C, S, W), st>>>(
-        x, dst, C, H, W, S, pad, Cs, Cb, Hs, Ws, items, FastDiv(uint32_t(S)), FastDiv(uint32_t(S * S)),
-        FastDiv(uint32_t(Hs)), device_error_word());
+    const long long total = BLOCKED ? (long long)N * Cb * Hs * Ws * 8 : (long long)N * C * S * Hs * Ws;
+    const unsigned blocks = unsigned((total + kS2dGatherThreads - 1) / kS2dGatherThreads);
+    s2d_gather_kernel<BLOCKED><<<blocks, kS2dGatherThreads, 0, st>>>(
+        x, dst, C, H, W, S, pad, Cs, total, FastDiv(uint32_t(Ws)), FastDiv(uint32_t(Hs)),
+        FastDiv(uint32_t(BLOCKED ? Cb : C)), FastDiv(uint32_t(S)), FastDiv(uint32_t(S * S)));
     note_launch();
     return cudaGetLastError();
 }

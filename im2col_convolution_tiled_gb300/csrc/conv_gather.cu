@@ -79,6 +79,8 @@ struct OutGeom {
     int Co, Ho, Wo, HoWo;
     int so;                  // output phase stride (1: plain NCHW)
     int ncols;               // Co * so * so
+    int vec;                 // so = 2 or 4 with Wo % so == 0 and out 16-byte aligned: each (ch, a) row of so
+                             // phases is one float2 / float4 store
 };
 
 template <int BN>
@@ -258,6 +260,30 @@ struct ConvGatherProb {
                 if (ch < o.Co) {
                     const float v = __uint_as_float(r[i]) + (o.bias ? __ldg(o.bias + ch) : 0.f);
                     e.opix[size_t(ch) * o.HoWo] = o.relu && !(v > 0.f) ? 0.f : v;
+                }
+            }
+        } else if (o.vec) {
+            // columns (ch, a, b) with b fastest: the so phases b of one (ch, a)
+            // are so adjacent columns and so adjacent floats of output row
+            // h + a (w = so * q is a multiple of so, so wrem >= so)
+            if (o.so == 4) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    const int col = tl.n0 + c0 + i;
+                    const int ch = col >> 4, a = (col >> 2) & 3;
+                    if (ch < o.Co && a < e.hrem)
+                        *reinterpret_cast<float4*>(e.opix + size_t(ch) * o.HoWo + a * o.Wo) =
+                            make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]), __uint_as_float(r[i + 2]),
+                                        __uint_as_float(r[i + 3]));
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const int col = tl.n0 + c0 + i;
+                    const int ch = col >> 2, a = (col >> 1) & 1;
+                    if (ch < o.Co && a < e.hrem)
+                        *reinterpret_cast<float2*>(e.opix + size_t(ch) * o.HoWo + a * o.Wo) =
+                            make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1]));
                 }
             }
         } else {
@@ -812,7 +838,8 @@ static S2dPlan plan_fwd_s2d(const ConvDims& d)
     int n_tiles;
     sp.bn = pick_conv_bn(d.K, &n_tiles);
     if (sp.bn > 128) return sp;
-    if (s2d_copy_smem(d.C, d.S, d.W) > kS2dMaxSmem) return sp;   // staged input rows
+    if ((long long)d.N * ((sp.Ci + 31) / 32) * 32 * (d.P + sp.T - 1) * (d.Q + sp.T - 1) >= (1LL << 31))
+        return sp;   // the channel-blocked copy is indexed with 32-bit element offsets
     sp.pg = make_patch(nullptr, d.N, sp.Ci, d.P + sp.T - 1, d.Q + sp.T - 1, d.P, d.Q, 1, 0, sp.T);
     if (sp.pg.mode != 0) return sp;
     patch_box(sp.pg);
@@ -976,6 +1003,7 @@ cudaError_t launch_conv_dgrad(const ConvDims& d, const float* w, const float* dy
     o.HoWo = d.H * d.W;
     o.so = d.S;
     o.ncols = dgrad_cols(d);
+    o.vec = (d.S == 4 || d.S == 2) && d.W % d.S == 0 && (reinterpret_cast<uintptr_t>(dx) & 15) == 0 ? 1 : 0;
     auto make_gen = [&](const KDecode& dec) {
         return DgradFilterGen{w,   d.C, d.K, d.R, d.S, d.pad, d_lo, dec, FastDiv(uint32_t(T)),
                               FastDiv(uint32_t(d.S * d.S)), FastDiv(uint32_t(d.S))};

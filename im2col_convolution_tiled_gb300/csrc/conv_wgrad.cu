@@ -208,7 +208,6 @@ static WgradS2d plan_wgrad_s2d(const ConvDims& d)
     w.T = (d.R + d.S - 1) / d.S;
     w.Cs = d.C * d.S * d.S;
     if (w.Cs < 17 || w.Cs > 128) return w;
-    if (s2d_copy_smem(d.C, d.S, d.W) > kS2dMaxSmem) return w;   // staged input rows
     w.Hs = d.P + w.T - 1;
     w.Ws = d.Q + w.T - 1;
     if ((long long)d.N * w.Cs * w.Hs * w.Ws >= (1LL << 31)) return w;
@@ -253,12 +252,29 @@ static WgradPlan plan_wgrad(const ConvDims& d)
     pl.m_tiles = (CRS + kBM - 1) / kBM;
     pl.k_stages = int((NPQ + kBK - 1) / kBK);
     const int mn = pl.m_tiles * pl.n_tiles;
-    int splits = (sm_count() + mn / 2) / mn;       // about one tile per SM
+    // The persistent grid runs ceil(tiles / SMs) rounds of tiles; a round
+    // costs its range length plus a fixed per-tile overhead (pipeline fill,
+    // last epilogue).  Pick the split count with the least total, fewest
+    // splits on a tie: a 13-tile GEMM on 152 SMs takes 11 splits (one round
+    // of 143 tiles), not 12 (156 tiles: a second round for 4 of them).
     const int min_stages = 16;                     // keep each range worth a tile
-    if (splits > pl.k_stages / min_stages) splits = pl.k_stages / min_stages;
-    if (splits < 1) splits = 1;
-    pl.ks_per_split = (pl.k_stages + splits - 1) / splits;
-    pl.splits = (pl.k_stages + pl.ks_per_split - 1) / pl.ks_per_split;   // no empty range
+    const int tile_overhead = 16;                  // in stages
+    const long long P = sm_count();
+    const int max_splits = pl.k_stages / min_stages > 1 ? pl.k_stages / min_stages : 1;
+    long long best = -1;
+    pl.splits = 1;
+    pl.ks_per_split = pl.k_stages;
+    for (int s = 1; s <= max_splits; ++s) {
+        const int per = (pl.k_stages + s - 1) / s;
+        const int ns = (pl.k_stages + per - 1) / per;   // no empty range
+        const long long rounds = ((long long)mn * ns + P - 1) / P;
+        const long long cost = rounds * (per + tile_overhead);
+        if (best < 0 || cost < best) {
+            best = cost;
+            pl.splits = ns;
+            pl.ks_per_split = per;
+        }
+    }
     return pl;
 }
 

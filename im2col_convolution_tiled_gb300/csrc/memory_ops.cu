@@ -785,111 +785,261 @@ __global__ void __launch_bounds__(kPoolThreads, 3) maxpool_bwd_staged_kernel(
     }
 }
 
-// Column walker for the common window shapes (K x K, stride S, K and S
-// compile-time).  A work item is (plane, output column ow, segment
-// of output rows); the thread walks down its rows keeping the maxima of the
-// last K input rows (each the first maximum of its K columns, strict >) in
-// registers.  Window oh combines the maxima of rows oh*S .. oh*S + K - 1 in
-// row order (first strictly greater wins), which is exactly the first
-// maximum of the window in row-major order; the next window reuses K - S of
-// them, so a window costs S*K shared loads instead of K*K.
+// ---------------------------------------------------------------------------
+// Register walkers for K x K windows with stride S and K <= 2S (the 3x3/2 and
+// 2x2/2 pools).  No shared memory and no barriers: a thread walks down one
+// column of windows (forward) or one column of S-wide pixel blocks
+// (backward) and keeps what neighbouring rows share in registers.  Loads for
+// kWalkChunk rows of windows are issued before any of them is used, so each
+// thread has a few dozen independent loads in flight.  Work item = (plane,
+// row segment, column), column fastest, so a warp's loads and stores run
+// along a row.
+constexpr int kWalkThreads = 256;
+constexpr int kWalkChunk = 4;
+
+// Forward: window oh combines the first maxima of its K input rows
+// (rows oh*S .. oh*S + K - 1, each the first maximum over its K columns);
+// taking rows in order with a strict > gives the first maximum of the window
+// in row-major order.  Rows shared with the previous window (K - S of them)
+// are carried.
 template <int K, int S>
-__global__ void __launch_bounds__(kPoolThreads, 3) maxpool_fwd_cols_kernel(
-    const float* __restrict__ x, float* __restrict__ y, int32_t* __restrict__ idx, int NC, int H, int W, int P,
-    int Q, int ppb, int stage_floats, int nseg, int seglen, FastDiv f_seg, FastDiv f_q, int* err)
+__global__ void __launch_bounds__(kWalkThreads) maxpool_fwd_walk_kernel(
+    const float* __restrict__ x, float* __restrict__ y, int32_t* __restrict__ idx, int H, int W, int P, int Q,
+    int seglen, FastDiv f_q, FastDiv f_seg, int items)
 {
-    static_assert(S <= K, "windows must overlap or touch");
-    extern __shared__ __align__(16) float pool_smem[];
-    __shared__ uint64_t bar[2];
-    __shared__ int abort_flag;
-    const int HW = H * W, PQ = P * Q;
-    const long long total = (long long)NC * HW;
-    const int groups = (NC + ppb - 1) / ppb;
-    auto issue = [&](int g, int b) {
-        const int nc0 = g * ppb, np = min(ppb, NC - nc0);
-        const long long start = (long long)nc0 * HW;
-        mbar_arrive_expect_tx(&bar[b], stage_range_bytes(start, np * HW, total));
-        stage_range(pool_smem + b * stage_floats, x, start, np * HW, total, &bar[b]);
+    static_assert(S <= K && K <= 2 * S, "walker covers windows at most two strides wide");
+    const int t = int(blockIdx.x) * kWalkThreads + int(threadIdx.x);
+    if (t >= items) return;
+    uint32_t rest, ow, plane, seg;
+    f_q.divmod(uint32_t(t), rest, ow);
+    f_seg.divmod(rest, plane, seg);
+    const int oh0 = int(seg) * seglen;
+    const int oh1 = min(oh0 + seglen, P);
+    const int col0 = int(plane) * H * W + int(ow) * S;   // flat index of the column's first window corner
+    float rm[K];
+    int ri[K];
+    // the K - S rows the segment's first window shares with the window above it
+#pragma unroll
+    for (int r = 0; r < K - S; ++r) {
+        const int at = col0 + (oh0 * S + r) * W;
+        rm[r] = __ldg(x + at);
+        ri[r] = at;
+#pragma unroll
+        for (int c = 1; c < K; ++c) {
+            const float v = __ldg(x + at + c);
+            if (v > rm[r]) {
+                rm[r] = v;
+                ri[r] = at + c;
+            }
+        }
+    }
+    float* yo = y + size_t(plane) * P * Q + ow;
+    int32_t* io = idx + size_t(plane) * P * Q + ow;
+    for (int oh = oh0; oh < oh1; oh += kWalkChunk) {
+        // rows oh*S + K - S + u, u < kWalkChunk*S: the S new rows of each window of the chunk
+        float v[kWalkChunk * S][K];
+#pragma unroll
+        for (int u = 0; u < kWalkChunk * S; ++u)
+            if (oh + u / S < oh1) {
+                const int at = col0 + (oh * S + K - S + u) * W;
+#pragma unroll
+                for (int c = 0; c < K; ++c) v[u][c] = __ldg(x + at + c);
+            }
+#pragma unroll
+        for (int i = 0; i < kWalkChunk; ++i) {
+            if (oh + i >= oh1) break;
+#pragma unroll
+            for (int r = 0; r < S; ++r) {
+                const float* row = v[i * S + r];
+                const int at = col0 + ((oh + i) * S + K - S + r) * W;
+                float m = row[0];
+                int a = at;
+#pragma unroll
+                for (int c = 1; c < K; ++c)
+                    if (row[c] > m) {
+                        m = row[c];
+                        a = at + c;
+                    }
+                rm[K - S + r] = m;
+                ri[K - S + r] = a;
+            }
+            float m = rm[0];
+            int a = ri[0];
+#pragma unroll
+            for (int r = 1; r < K; ++r)
+                if (rm[r] > m) {
+                    m = rm[r];
+                    a = ri[r];
+                }
+            yo[size_t(oh + i) * Q] = m;
+            io[size_t(oh + i) * Q] = a;
+            // the next window's first K - S rows are this window's last ones
+#pragma unroll
+            for (int r = 0; r < K - S; ++r) {
+                rm[r] = rm[r + S];
+                ri[r] = ri[r + S];
+            }
+        }
+    }
+}
+
+// Backward: a thread owns the column of S x S pixel blocks j (pixel columns
+// S*j .. S*j + S - 1) and walks down its block rows b.  With K <= 2S only the
+// windows (b, j - 1) and (b, j) of window row b reach block (b, j), and
+// window row b reaches block row b (its first S rows) and block row b + 1
+// (its last K - S rows, carried to the next step).  A pixel of block (b, j)
+// therefore receives, in this order, (b-1, j-1) and (b-1, j) through the
+// carry, then (b, j-1) and (b, j): ascending window order, each added in
+// fp32 to a sum that starts at zero -- bit-for-bit the ClearBuffer-then-
+// scatter result.  A saved index outside its window routes nothing.
+template <int K, int S>
+__global__ void __launch_bounds__(kWalkThreads) maxpool_bwd_walk_kernel(
+    const float* __restrict__ dy, const int32_t* __restrict__ idx, float* __restrict__ dx, int H, int W, int P,
+    int Q, int BH, int seglen, FastDiv f_bw, FastDiv f_seg, int items)
+{
+    static_assert(S <= K && K <= 2 * S, "walker covers windows at most two strides wide");
+    constexpr int KC = K - S > 0 ? K - S : 1;   // carried rows (at least one slot)
+    const int t = int(blockIdx.x) * kWalkThreads + int(threadIdx.x);
+    if (t >= items) return;
+    uint32_t rest, j, plane, seg;
+    f_bw.divmod(uint32_t(t), rest, j);
+    f_seg.divmod(rest, plane, seg);
+    const int b0 = int(seg) * seglen;
+    const int b1 = min(b0 + seglen, BH);
+    const int pbase = int(plane) * H * W;
+    const float* dyp = dy + size_t(plane) * P * Q;
+    const int32_t* ip = idx + size_t(plane) * P * Q;
+    const bool has_l = j >= 1 && int(j) - 1 < Q;   // window column j - 1 exists
+    const bool has_r = int(j) < Q;                 // window column j exists
+
+    // Add gradient v of window (oh, ow) to the pixel its saved index iv names,
+    // if that pixel lies in this thread's blocks: window column j - 1 (own =
+    // false) reaches block columns dc >= S, window column j (own) dc < S.
+    auto route = [&](float v, int iv, int oh, int ow, bool own, float (&acc)[S][S], float (&nxt)[KC][S]) {
+        const int d = iv - (pbase + (oh * W + ow) * S);
+        int dr = 0;
+#pragma unroll
+        for (int r = 1; r < K; ++r) dr += d >= r * W ? 1 : 0;
+        const int dc = d - dr * W;
+        const bool ok = d >= 0 && dc < K && (own ? dc < S : dc >= S);
+        const int c = own ? dc : dc - S;
+#pragma unroll
+        for (int r = 0; r < K; ++r)
+#pragma unroll
+            for (int cc = 0; cc < S; ++cc)
+                if (ok && dr == r && c == cc) {
+                    if (r < S)
+                        acc[r][cc] += v;
+                    else
+                        nxt[r - S < KC ? r - S : 0][cc] += v;
+                }
     };
-    if (threadIdx.x == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
-        abort_flag = 0;
-        mbar_fence_init();
-        for (int i = 0; i < 2; ++i)
-            if (int(blockIdx.x) + i * int(gridDim.x) < groups) issue(blockIdx.x + i * gridDim.x, i);
-    }
-    __syncthreads();
-    int i = 0, g = blockIdx.x;
-    for (; g < groups; g += gridDim.x, ++i) {
-        const int b = i & 1;
-        if (!stage_wait(&bar[b], uint32_t(i >> 1) & 1u, &abort_flag, err)) break;
-        const int nc0 = g * ppb, np = min(ppb, NC - nc0);
-        const float* sx = pool_smem + b * stage_floats + ((long long)nc0 * HW & 3);
-        const int items = np * Q * nseg;
-        for (int it = threadIdx.x; it < items; it += kPoolThreads) {
-            uint32_t rest, seg, pl, ow;
-            f_q.divmod(uint32_t(it), rest, ow);   // it = (pl * nseg + seg) * Q + ow: a warp stores along ow
-            f_seg.divmod(rest, pl, seg);
-            const int oh0 = int(seg) * seglen;
-            const int oh1 = min(oh0 + seglen, P);
-            const int plane = int(pl) * HW;
-            const int c0 = int(ow) * S;
-            float rm[K];
-            int ri[K];
-            auto row_max = [&](int h, float& m, int& at) {
-                const int base = plane + h * W + c0;
-                m = sx[base];
-                at = base;
+
+    float carry[KC][S];
 #pragma unroll
-                for (int c = 1; c < K; ++c) {
-                    const float v = sx[base + c];
-                    if (v > m) {
-                        m = v;
-                        at = base + c;
-                    }
+    for (int r = 0; r < KC; ++r)
+#pragma unroll
+        for (int c = 0; c < S; ++c) carry[r][c] = 0.f;
+    if (K > S && b0 >= 1 && b0 - 1 < P) {
+        // the segment starts mid-plane: window row b0 - 1's contributions to block row b0
+        float unused[S][S] = {};
+        const int oh = b0 - 1;
+        if (has_l) route(__ldg(dyp + oh * Q + j - 1), __ldg(ip + oh * Q + j - 1), oh, int(j) - 1, false, unused, carry);
+        if (has_r) route(__ldg(dyp + oh * Q + j), __ldg(ip + oh * Q + j), oh, int(j), true, unused, carry);
+    }
+    const int wend = min(b1, P);   // window rows this segment reads: [b0, wend)
+    float* out = dx + pbase + int(j) * S;
+    for (int b = b0; b < b1; b += kWalkChunk) {
+        float vl[kWalkChunk], vr[kWalkChunk];
+        int il[kWalkChunk], ir[kWalkChunk];
+#pragma unroll
+        for (int u = 0; u < kWalkChunk; ++u)
+            if (b + u < wend) {
+                const int o = (b + u) * Q + int(j);
+                if (has_l) {
+                    vl[u] = __ldg(dyp + o - 1);
+                    il[u] = __ldg(ip + o - 1);
                 }
-            };
-            for (int oh = oh0; oh < oh1; ++oh) {
-                if (oh == oh0) {
-#pragma unroll
-                    for (int r = 0; r < K; ++r) row_max(oh * S + r, rm[r], ri[r]);
-                } else {
-#pragma unroll
-                    for (int r = 0; r < K - S; ++r) {
-                        rm[r] = rm[r + S];
-                        ri[r] = ri[r + S];
-                    }
-#pragma unroll
-                    for (int r = K - S; r < K; ++r) row_max(oh * S + r, rm[r], ri[r]);
+                if (has_r) {
+                    vr[u] = __ldg(dyp + o);
+                    ir[u] = __ldg(ip + o);
                 }
-                float m = rm[0];
-                int at = ri[0];
+            }
 #pragma unroll
-                for (int r = 1; r < K; ++r)
-                    if (rm[r] > m) {
-                        m = rm[r];
-                        at = ri[r];
-                    }
-                const size_t o = size_t(nc0) * PQ + size_t(pl) * PQ + size_t(oh) * Q + ow;
-                y[o] = m;
-                idx[o] = nc0 * HW + at;
+        for (int u = 0; u < kWalkChunk; ++u) {
+            const int bb = b + u;
+            if (bb >= b1) break;
+            float acc[S][S], nxt[KC][S];
+#pragma unroll
+            for (int r = 0; r < S; ++r)
+#pragma unroll
+                for (int c = 0; c < S; ++c) acc[r][c] = (K > S && r < K - S) ? carry[r < KC ? r : 0][c] : 0.f;
+#pragma unroll
+            for (int r = 0; r < KC; ++r)
+#pragma unroll
+                for (int c = 0; c < S; ++c) nxt[r][c] = 0.f;
+            if (bb < wend) {
+                if (has_l) route(vl[u], il[u], bb, int(j) - 1, false, acc, nxt);
+                if (has_r) route(vr[u], ir[u], bb, int(j), true, acc, nxt);
             }
-        }
-        __syncthreads();
-        if (threadIdx.x == 0 && g + 2 * int(gridDim.x) < groups) {
-            fence_proxy_async_smem();
-            issue(g + 2 * gridDim.x, b);
+#pragma unroll
+            for (int r = 0; r < S; ++r) {
+                const int h = bb * S + r;
+                if (h < H) {
+#pragma unroll
+                    for (int c = 0; c < S; ++c)
+                        if (int(j) * S + c < W) out[h * W + c] = acc[r][c];
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < KC; ++r)
+#pragma unroll
+                for (int c = 0; c < S; ++c) carry[r][c] = nxt[r][c];
         }
     }
-    if (abort_flag && threadIdx.x == 0) {
-        for (int j = 0; j < 2 && g + j * int(gridDim.x) < groups; ++j) {
-            uint64_t t0 = globaltimer_ns();
-            while (!mbar_try_wait(&bar[(i + j) & 1], uint32_t((i + j) >> 1) & 1u) &&
-                   globaltimer_ns() - t0 < kWaitLimitNs) {
-            }
-        }
-    }
+}
+
+// Rows per segment for a walker with `per_seg_items` threads per segment:
+// split planes into row segments only until about one wave of threads is
+// resident (1024 per SM at the walkers' register use), and keep at least one
+// load chunk of rows per segment.  Measured on the AlexNet pools, whole-plane
+// walks beat four waves of shorter segments (pool2 backward 0.57 -> 0.61 of
+// the copy bandwidth).
+static int walk_seglen(int rows, long long per_seg_items)
+{
+    const long long want = 1LL * sm_count() * 1024;
+    long long nseg = (want + per_seg_items - 1) / per_seg_items;
+    const long long max_seg = rows / kWalkChunk > 1 ? rows / kWalkChunk : 1;
+    if (nseg > max_seg) nseg = max_seg;
+    if (nseg < 1) nseg = 1;
+    return int((rows + nseg - 1) / nseg);
+}
+
+template <int K, int S>
+static cudaError_t launch_pool_fwd_walk(int NC, int H, int W, int P, int Q, const float* x, float* y, int32_t* idx,
+                                        cudaStream_t st)
+{
+    const int seglen = walk_seglen(P, (long long)NC * Q);
+    const int nseg = (P + seglen - 1) / seglen;
+    const long long items = (long long)NC * nseg * Q;
+    maxpool_fwd_walk_kernel<K, S><<<unsigned((items + kWalkThreads - 1) / kWalkThreads), kWalkThreads, 0, st>>>(
+        x, y, idx, H, W, P, Q, seglen, FastDiv(uint32_t(Q)), FastDiv(uint32_t(nseg)), int(items));
+    note_launch();
+    return cudaGetLastError();
+}
+
+template <int K, int S>
+static cudaError_t launch_pool_bwd_walk(int NC, int H, int W, int P, int Q, const float* dy, const int32_t* idx,
+                                        float* dx, cudaStream_t st)
+{
+    const int BH = (H + S - 1) / S, BW = (W + S - 1) / S;
+    const int seglen = walk_seglen(BH, (long long)NC * BW);
+    const int nseg = (BH + seglen - 1) / seglen;
+    const long long items = (long long)NC * nseg * BW;
+    maxpool_bwd_walk_kernel<K, S><<<unsigned((items + kWalkThreads - 1) / kWalkThreads), kWalkThreads, 0, st>>>(
+        dy, idx, dx, H, W, P, Q, BH, seglen, FastDiv(uint32_t(BW)), FastDiv(uint32_t(nseg)), int(items));
+    note_launch();
+    return cudaGetLastError();
 }
 
 // Blocks per SM for a staged kernel using `smem` bytes of dynamic shared memory.
@@ -907,49 +1057,14 @@ static int staged_grid(int groups, size_t smem, int max_per_sm = 4)
     return groups < cap ? groups : cap;
 }
 
-// Segment length (in output rows) that gives about kPoolThreads work items
-// for `cols` columns per staged group, so every thread walks a few rows.
-static int pool_seglen(int rows, int cols)
-{
-    int nseg = (kPoolThreads + cols - 1) / cols;
-    if (nseg > rows) nseg = rows;
-    if (nseg < 1) nseg = 1;
-    return (rows + nseg - 1) / nseg;
-}
-
-template <int K, int S>
-static cudaError_t launch_pool_fwd_cols(int NC, int H, int W, int P, int Q, const float* x, float* y, int32_t* idx,
-                                        cudaStream_t st)
-{
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(maxpool_fwd_cols_kernel<K, S>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    const int HW = H * W;
-    const int ppb = (kPoolStageFloats - 4) / HW < 64 ? (kPoolStageFloats - 4) / HW : 64;
-    const int stage = (ppb * HW + 4 + 3) & ~3;
-    const size_t smem = 2 * size_t(stage) * sizeof(float);
-    const int groups = (NC + ppb - 1) / ppb;
-    const int seglen = pool_seglen(P, ppb * Q);
-    const int nseg = (P + seglen - 1) / seglen;
-    maxpool_fwd_cols_kernel<K, S><<<staged_grid(groups, smem), kPoolThreads, smem, st>>>(
-        x, y, idx, NC, H, W, P, Q, ppb, stage, nseg, seglen, FastDiv(uint32_t(nseg)), FastDiv(uint32_t(Q)),
-        device_error_word());
-    note_launch();
-    return cudaGetLastError();
-}
-
 cudaError_t launch_maxpool_fwd(int N, int C, int H, int W, int k, int s, int P, int Q, const float* x, float* y,
                                int32_t* idx, cudaStream_t st)
 {
     const int NC = N * C;
     const int HW = H * W;
+    if (k == 3 && s == 2) return launch_pool_fwd_walk<3, 2>(NC, H, W, P, Q, x, y, idx, st);
+    if (k == 2 && s == 2) return launch_pool_fwd_walk<2, 2>(NC, H, W, P, Q, x, y, idx, st);
     if (HW + 4 <= kPoolStageFloats) {
-        if (k == 3 && s == 2) return launch_pool_fwd_cols<3, 2>(NC, H, W, P, Q, x, y, idx, st);
-        if (k == 2 && s == 2) return launch_pool_fwd_cols<2, 2>(NC, H, W, P, Q, x, y, idx, st);
         const int ppb = (kPoolStageFloats - 4) / HW < 64 ? (kPoolStageFloats - 4) / HW : 64;
         const int stage = (ppb * HW + 4 + 3) & ~3;   // floats per buffer (room for the 16-byte shift)
         const size_t smem = 2 * size_t(stage) * sizeof(float);
@@ -997,6 +1112,8 @@ cudaError_t launch_maxpool_bwd(int N, int C, int H, int W, int k, int s, int P, 
 {
     const int NC = N * C;
     const int PQ = P * Q;
+    if (k == 3 && s == 2) return launch_pool_bwd_walk<3, 2>(NC, H, W, P, Q, dy, idx, dx, st);
+    if (k == 2 && s == 2) return launch_pool_bwd_walk<2, 2>(NC, H, W, P, Q, dy, idx, dx, st);
     if (PQ + 4 <= kPoolStageFloats / 2 && s >= 1 && s <= 3) {
         const int ppb = (kPoolStageFloats / 2 - 4) / PQ < 64 ? (kPoolStageFloats / 2 - 4) / PQ : 64;
         const int stage = (ppb * PQ + 4 + 3) & ~3;

@@ -91,6 +91,10 @@ CONV_SHAPES = [
     (16, 64, 35, 35, 192, 3, 1, 1),    # forward: 192 filters
     (16, 192, 35, 35, 64, 3, 1, 1),    # input gradient: 192 columns
     (2, 24, 11, 11, 100, 3, 1, 1),     # 100 filters: 128-wide filter-gradient tiles (A in tensor memory)
+    # input gradient stored as one float4 (stride 4) / float2 (stride 2) per (channel, row phase), with a
+    # last super-row cut by the image's bottom edge (H % stride != 0)
+    (2, 3, 30, 28, 8, 5, 4, 1),
+    (1, 5, 11, 10, 6, 3, 2, 1),
 ]
 
 
@@ -279,7 +283,10 @@ POOL_CASES = [((4, 6, 28, 28), 2, 2), ((4, 16, 10, 10), 2, 2), ((2, 64, 55, 55),
               ((2, 5, 11, 13), 3, 3), ((2, 4, 7, 9), 4, 2), ((1, 3, 4, 5), 3, 2), ((2, 3, 6, 6), 2, 1),
               ((1, 2, 13, 13), 3, 4),
               # forward column walker (3x3 and 2x2, stride 2): rows below the last window (H = 8), a narrow width
-              ((2, 3, 8, 9), 3, 2), ((1, 2, 7, 4), 3, 2)]
+              ((2, 3, 8, 9), 3, 2), ((1, 2, 7, 4), 3, 2),
+              # register walkers: odd sizes leave a row and a column outside every 2x2 window; a plane
+              # whose single window row spans it all; a batch large enough for several row segments
+              ((1, 3, 9, 11), 2, 2), ((3, 2, 3, 17), 3, 2), ((16, 64, 55, 55), 3, 2)]
 
 
 @pytest.mark.parametrize("shape,k,s", POOL_CASES)
