@@ -146,10 +146,17 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
-        time.sleep(0.3)
+        # nvidia-smi's start-up queries the driver; let it finish (first sample
+        # written, at most 5 s) before the timed launches begin
+        t0 = time.time()
+        while self.proc is not None and time.time() - t0 < 5.0 and self.proc.poll() is None:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.05)
+        time.sleep(0.25)
         return self
 
     def __exit__(self, *exc):
