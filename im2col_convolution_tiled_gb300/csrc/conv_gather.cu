@@ -78,16 +78,21 @@ struct OutGeom {
     int relu;                // forward only: max(0, .) after the bias (nn_relu fused into the epilogue)
     int Co, Ho, Wo, HoWo;
     int so;                  // output phase stride (1: plain NCHW)
+    int oo;                  // phase offset: row p's phase block starts at output row p * so - oo (0 <= oo < so)
     int ncols;               // Co * so * so
-    int vec;                 // so = 2 or 4 with Wo % so == 0 and out 16-byte aligned: each (ch, a) row of so
-                             // phases is one float2 / float4 store
+    int vec;                 // 1: so = 2 or 4, oo = 0, Wo % so == 0, out 16-byte aligned: each (ch, a) row of
+                             //    so phases is one float2 / float4 store
+                             // 2: so = 4, oo = 2, Wo even, out 8-byte aligned: two float2 stores per (ch, a)
 };
 
 template <int BN>
 struct ConvGatherProb {
     static constexpr bool kBBulk = true;
     int terms = 3;                                // tensor-core products per K step: 3 (3xTF32) or 1 (TF32)
-    static constexpr bool kATmem = BN <= 128;     // A stages in tensor memory (keeps 2 accumulators)
+    // A stages in tensor memory up to 128 columns (two accumulators still fit).
+    // Wider tiles keep A in shared memory: with A in tensor memory they would
+    // keep a single accumulator, and measured 5-20% slower on the AlexNet layers.
+    static constexpr bool kATmem = BN <= 128;
     static constexpr int kGroups = 2;
     static constexpr Map kAMap = Map::RowFast;
     static constexpr Map kBMap = Map::RowFast;   // unused (bulk)
@@ -221,9 +226,10 @@ struct ConvGatherProb {
     }
 
     struct EState {
-        float* opix;   // out[n][0][p*so][q*so]
+        float* opix;   // out[n][0][h][w], (h, w) = (p*so - oo, q*so - oo): may lie before the row/image
         bool valid;
         int hrem, wrem;   // rows/cols of the output left below/right of this pixel's phase block
+        int hmin, wmin;   // phases a < hmin (b < wmin) fall above (left of) the output: -h, -w
     };
     __device__ EState e_setup(const Tile& tl, int row) const
     {
@@ -235,10 +241,12 @@ struct ConvGatherProb {
             g.f_gpq.divmod(uint32_t(m), n, pq);
             g.f_gq.divmod(pq, p, q);
         }
-        const int h = int(p) * o.so, w = int(q) * o.so;
+        const int h = int(p) * o.so - o.oo, w = int(q) * o.so - o.oo;
         e.hrem = o.Ho - h;
         e.wrem = o.Wo - w;
-        e.opix = o.out + size_t(n) * o.Co * o.HoWo + size_t(h) * o.Wo + w;
+        e.hmin = -h;
+        e.wmin = -w;
+        e.opix = o.out + (ptrdiff_t(n) * o.Co * o.HoWo + ptrdiff_t(h) * o.Wo + w);
         return e;
     }
 
@@ -262,10 +270,28 @@ struct ConvGatherProb {
                     e.opix[size_t(ch) * o.HoWo] = o.relu && !(v > 0.f) ? 0.f : v;
                 }
             }
+        } else if (o.vec == 2) {
+            // so = 4, oo = 2: the four phases b of one (ch, a) are output
+            // columns w .. w + 3 with w = 4q - 2 (even): two 8-byte-aligned
+            // pairs, the first left of the image when q = 0, the second right
+            // of it when w + 2 = Wo
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+                const int col = tl.n0 + c0 + i;
+                const int ch = col >> 4, a = (col >> 2) & 3;
+                if (ch < o.Co && a < e.hrem && a >= e.hmin) {
+                    float* rowp = e.opix + (size_t(ch) * o.HoWo + a * o.Wo);
+                    if (e.wmin <= 0)
+                        *reinterpret_cast<float2*>(rowp) = make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+                    if (e.wrem > 2)
+                        *reinterpret_cast<float2*>(rowp + 2) =
+                            make_float2(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+                }
+            }
         } else if (o.vec) {
             // columns (ch, a, b) with b fastest: the so phases b of one (ch, a)
             // are so adjacent columns and so adjacent floats of output row
-            // h + a (w = so * q is a multiple of so, so wrem >= so)
+            // h + a (oo = 0 and w = so * q is a multiple of so, so wrem >= so)
             if (o.so == 4) {
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
@@ -293,7 +319,7 @@ struct ConvGatherProb {
                 const int col = tl.n0 + c0 + i;
                 const int ch = col / ss, ab = col - ch * ss;
                 const int a = ab / o.so, b = ab - a * o.so;
-                if (ch < o.Co && a < e.hrem && b < e.wrem)
+                if (ch < o.Co && a < e.hrem && b < e.wrem && a >= e.hmin && b >= e.wmin)
                     e.opix[size_t(ch) * o.HoWo + a * o.Wo + b] = __uint_as_float(r[i]);
             }
         }
@@ -337,10 +363,12 @@ struct ConvPatchProb {
         e.valid = pix < pg.GpGq;
         uint32_t p = 0, q = 0;
         if (e.valid) pg.f_gq.divmod(uint32_t(pix), p, q);
-        const int h = int(p) * o.so, w = int(q) * o.so;
+        const int h = int(p) * o.so - o.oo, w = int(q) * o.so - o.oo;
         e.hrem = o.Ho - h;
         e.wrem = o.Wo - w;
-        e.opix = o.out + size_t(n) * o.Co * o.HoWo + size_t(h) * o.Wo + w;
+        e.hmin = -h;
+        e.wmin = -w;
+        e.opix = o.out + (ptrdiff_t(n) * o.Co * o.HoWo + ptrdiff_t(h) * o.Wo + w);
         return e;
     }
     __device__ void store(const EState& e, const Tile& tl, int row, int c0, const uint32_t (&r)[32]) const
@@ -406,9 +434,9 @@ struct FwdFilterGen {   // B[k, kk] = W[k, c, r, q] (0 for padded channels)
     }
 };
 
-struct DgradFilterGen {   // B[(c, a, b), (d, e, kc)] = W[kc, c, a + pad - s*d, b + pad - s*e]
+struct DgradFilterGen {   // B[(c, a, b), (d, e, kc)] = W[kc, c, a + pad' - s*d, b + pad' - s*e], pad' = pad - oo
     const float* w;
-    int C, K, R, S, pad, d_lo;
+    int C, K, R, S, pad, d_lo;   // pad: pad' (the padding less the grid's phase offset)
     KDecode dec;
     FastDiv f_t, f_ss, f_s;
     __device__ float operator()(int col, int kk) const
@@ -428,15 +456,20 @@ struct DgradFilterGen {   // B[(c, a, b), (d, e, kc)] = W[kc, c, a + pad - s*d, 
     }
 };
 
-// Window of dy rows a phase can reach: d = (a + pad - r) / s over taps r and
-// phases a, i.e. d in [ceil((pad - R + 1) / s), floor((s - 1 + pad) / s)].
-static void dgrad_window(const ConvDims& d, int* d_lo, int* T)
+// The input-gradient GEMM's super-pixel grid.  Input row h is written as
+// h = s*hh + a - oo with phase a in [0, s) and oo = pad mod s: the grid is
+// aligned with the padding rather than with row 0.  Output row oh reaches h
+// through tap r = h + pad - s*oh = s*(hh - oh + pad div s) + a, so with
+// d = oh - hh every phase's taps r = a, a + s, ... < R sit at
+// d = pad div s - tr, tr in [0, ceil(R / s)): one window of T = ceil(R / s)
+// dy rows [d_lo, d_lo + T) serves all phases (a grid aligned with row 0
+// needs up to T + 1: 4 instead of 3 for an 11-wide filter at stride 4, pad 2).
+// The grid has ceil((H + oo) / s) rows.
+static void dgrad_window(const ConvDims& d, int* d_lo, int* T, int* oo)
 {
-    const int lo_num = d.pad - d.R + 1;   // may be negative
-    const int lo = lo_num >= 0 ? (lo_num + d.S - 1) / d.S : -((-lo_num) / d.S);
-    const int hi = (d.S - 1 + d.pad) / d.S;
-    *d_lo = lo;
-    *T = hi - lo + 1;
+    *oo = d.pad % d.S;
+    *T = (d.R + d.S - 1) / d.S;
+    *d_lo = d.pad / d.S - *T + 1;
 }
 
 static GatherGeom make_gather(const float* in, int Nb, int Ci, int Hi, int Wi, int Gp, int Gq, int sp, int o, int T)
@@ -947,9 +980,9 @@ size_t conv_fwd_ws(const ConvDims& d)
 
 size_t conv_dgrad_ws(const ConvDims& d)
 {
-    int d_lo, T;
-    dgrad_window(d, &d_lo, &T);
-    const int Hs = (d.H + d.S - 1) / d.S, Ws = (d.W + d.S - 1) / d.S;
+    int d_lo, T, oo;
+    dgrad_window(d, &d_lo, &T, &oo);
+    const int Hs = (d.H + oo + d.S - 1) / d.S, Ws = (d.W + oo + d.S - 1) / d.S;
     const WindowPlan wp = plan_window(d.N, d.K, d.P, d.Q, Hs, Ws, 1, d_lo, T, dgrad_cols(d));
     return wp.img_bytes + wp.part_bytes + wp.blocked_bytes;
 }
@@ -991,9 +1024,9 @@ cudaError_t launch_conv_fwd(const ConvDims& d, const float* x, const float* w, c
 cudaError_t launch_conv_dgrad(const ConvDims& d, const float* w, const float* dy, float* dx, void* ws,
                               cudaStream_t st)
 {
-    int d_lo, T;
-    dgrad_window(d, &d_lo, &T);
-    const int Hs = (d.H + d.S - 1) / d.S, Ws = (d.W + d.S - 1) / d.S;
+    int d_lo, T, oo;
+    dgrad_window(d, &d_lo, &T, &oo);
+    const int Hs = (d.H + oo + d.S - 1) / d.S, Ws = (d.W + oo + d.S - 1) / d.S;
     OutGeom o{};
     o.out = dx;
     o.bias = nullptr;
@@ -1002,10 +1035,14 @@ cudaError_t launch_conv_dgrad(const ConvDims& d, const float* w, const float* dy
     o.Wo = d.W;
     o.HoWo = d.H * d.W;
     o.so = d.S;
+    o.oo = oo;
     o.ncols = dgrad_cols(d);
-    o.vec = (d.S == 4 || d.S == 2) && d.W % d.S == 0 && (reinterpret_cast<uintptr_t>(dx) & 15) == 0 ? 1 : 0;
+    const uintptr_t ax = reinterpret_cast<uintptr_t>(dx);
+    o.vec = (d.S == 4 || d.S == 2) && oo == 0 && d.W % d.S == 0 && (ax & 15) == 0 ? 1
+            : (d.S == 4 && oo == 2 && d.W % 2 == 0 && (ax & 7) == 0)           ? 2
+                                                                               : 0;
     auto make_gen = [&](const KDecode& dec) {
-        return DgradFilterGen{w,   d.C, d.K, d.R, d.S, d.pad, d_lo, dec, FastDiv(uint32_t(T)),
+        return DgradFilterGen{w,   d.C, d.K, d.R, d.S, d.pad - oo, d_lo, dec, FastDiv(uint32_t(T)),
                               FastDiv(uint32_t(d.S * d.S)), FastDiv(uint32_t(d.S))};
     };
     return run_window_gemm(dy, d.N, d.K, d.P, d.Q, Hs, Ws, 1, d_lo, T, o, ws, make_gen, st);

@@ -95,6 +95,13 @@ CONV_SHAPES = [
     # last super-row cut by the image's bottom edge (H % stride != 0)
     (2, 3, 30, 28, 8, 5, 4, 1),
     (1, 5, 11, 10, 6, 3, 2, 1),
+    # strided input gradients on the padding-aligned super-pixel grid (phase offset pad mod stride): two float2
+    # stores per (channel, row phase) with the image's left and right edges cutting a pair (W % 4 = 0 and 2),
+    # and pads of at least the stride
+    (2, 3, 28, 28, 16, 11, 4, 2),
+    (2, 3, 26, 30, 8, 11, 4, 2),
+    (1, 4, 17, 17, 5, 7, 2, 3),
+    (1, 3, 20, 20, 8, 11, 4, 6),
 ]
 
 
