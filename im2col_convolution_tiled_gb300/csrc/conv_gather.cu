@@ -250,6 +250,9 @@ struct ConvGatherProb {
         return e;
     }
 
+    // epilogue of split trailing tile b, once its pieces are summed
+    __device__ void reduce_store(int b, int row, int c0, const uint32_t (&r)[32]) const;
+
     __device__ void store(const EState& e, const Tile& tl, int row, int c0, const uint32_t (&r)[32]) const
     {
         if (tl.part >= 0) {
@@ -326,6 +329,13 @@ struct ConvGatherProb {
     }
 };
 
+template <int BN>
+__device__ void ConvGatherProb<BN>::reduce_store(int b, int row, int c0, const uint32_t (&r)[32]) const
+{
+    const Tile tl = whole_tile(full_units + b);
+    store(e_setup(tl, row), tl, row, c0, r);
+}
+
 // The same GEMMs on the patch-staged kernel (gemm_patch.cuh): tiles never
 // straddle images, and the K order is chunk-major in 32-channel chunks (or tap
 // groups when the gathered tensor has at most 16 channels).
@@ -336,8 +346,30 @@ struct ConvPatchProb {
     OutGeom o;
     const float* bimg;
     int n_tiles, k_stages;
+    // Tail split (see plan_patch_tail): units [0, full_units) are whole tiles;
+    // each later tile is cut into tail_split pieces along its channel chunks,
+    // whose partial tiles go to part_buf [piece][kBM][BN] and are added by
+    // tail_reduce_kernel.
+    int full_units = 0, tail_split = 1;
+    float* part_buf = nullptr;
 
-    __device__ int num_tiles() const { return pg.Nb * pg.tpi * n_tiles; }
+    __device__ int num_tiles() const
+    {
+        return full_units + (pg.Nb * pg.tpi * n_tiles - full_units) * tail_split;
+    }
+    __device__ PatchUnit unit(int t) const
+    {
+        PatchUnit u{t, 0, pg.nch, -1};
+        if (t >= full_units) {
+            const int v = t - full_units;
+            const int j = v % tail_split;
+            u.tt = full_units + v / tail_split;
+            u.cc0 = j * pg.nch / tail_split;
+            u.cc1 = (j + 1) * pg.nch / tail_split;
+            u.part = v;
+        }
+        return u;
+    }
     __device__ Tile tile_t(int t) const
     {
         Tile r;
@@ -375,7 +407,15 @@ struct ConvPatchProb {
     {
         ConvGatherProb<BN> helper;
         helper.o = o;
+        helper.part_buf = part_buf;
         helper.store(e, tl, row, c0, r);
+    }
+    // epilogue of split trailing tile b, once its pieces are summed
+    __device__ void reduce_store(int b, int row, int c0, const uint32_t (&r)[32]) const
+    {
+        const int tt = full_units + b;
+        const Tile tl = tile_t(tt);
+        store(e_setup_t(tt, row), tl, row, c0, r);
     }
 };
 
@@ -547,8 +587,8 @@ static TailPlan plan_tail(int tiles, int k_stages, int bn)
 // memory, and the 128 row threads hand them to the problem's epilogue.
 constexpr int kTailThreads = 1024;
 
-template <int BN>
-__global__ void __launch_bounds__(kTailThreads) tail_reduce_kernel(const __grid_constant__ ConvGatherProb<BN> prob)
+template <class Prob, int BN>
+__global__ void __launch_bounds__(kTailThreads) tail_reduce_kernel(const __grid_constant__ Prob prob)
 {
     __shared__ float sums[kBM][33];
     const int u0 = blockIdx.x * prob.tail_split;
@@ -589,9 +629,7 @@ __global__ void __launch_bounds__(kTailThreads) tail_reduce_kernel(const __grid_
         uint32_t r[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(sums[row][i]);
-        const Tile tl = prob.whole_tile(prob.full_units + blockIdx.x);
-        const typename ConvGatherProb<BN>::EState e = prob.e_setup(tl, row);
-        prob.store(e, tl, row, c0, r);
+        prob.reduce_store(int(blockIdx.x), row, c0, r);
     }
 }
 
@@ -615,7 +653,8 @@ static cudaError_t run_gather(const GatherGeom& g, const OutGeom& o, float* img,
     const int units = tp.full_units + tp.tail_tiles * tp.split;
     cudaError_t e = launch_tc_gemm<ConvGatherProb<BN>, BN>(p, units, device_error_word(), st);
     if (e != cudaSuccess || tp.tail_tiles == 0) return e;
-    tail_reduce_kernel<BN><<<dim3(unsigned(tp.tail_tiles), unsigned(BN / 32)), kTailThreads, 0, st>>>(p);
+    tail_reduce_kernel<ConvGatherProb<BN>, BN>
+        <<<dim3(unsigned(tp.tail_tiles), unsigned(BN / 32)), kTailThreads, 0, st>>>(p);
     note_launch();
     return cudaGetLastError();
 }
@@ -684,8 +723,33 @@ static int patch_capacity(int bn)
 
 constexpr int kShortTileStages = 48;   // K stages per tile at or below which 64-wide tiles double-buffer
 
+// Tail split of the patch kernel, by channel chunks.  Worth a reduce launch
+// only when the grid runs few rounds of tiles (a round is then a large share
+// of the time): AlexNet conv2's input gradient has 768 tiles, five rounds on
+// 152 SMs plus 8 tiles, whose round the split cuts to a sixth.
+constexpr int kPatchTailMaxRounds = 8;
+
+static TailPlan plan_patch_tail(const PatchGeom& pg, int ncols, int bn)
+{
+    const int n_tiles = (ncols + bn - 1) / bn;
+    const int tiles = pg.Nb * pg.tpi * n_tiles;
+    TailPlan p{tiles, 1, 0, 0};
+    const int P = sm_count();
+    if (tiles <= P || tiles % P == 0 || tiles / P >= kPatchTailMaxRounds) return p;
+    const int rem = tiles % P;
+    int split = P / rem;
+    if (split > pg.nch) split = pg.nch;
+    if (split < 2) return p;
+    p.full_units = tiles - rem;
+    p.split = split;
+    p.tail_tiles = rem;
+    p.part_floats = size_t(rem) * split * kBM * bn;
+    return p;
+}
+
+// part: room for plan_patch_tail's partial tiles, or null (no split)
 template <int BN, bool TMA>
-static cudaError_t run_patch(const PatchGeom& pg, const OutGeom& o, float* img, cudaStream_t st)
+static cudaError_t run_patch(const PatchGeom& pg, const OutGeom& o, float* img, float* part, cudaStream_t st)
 {
     ConvPatchProb<BN> p;
     p.terms = math_terms();
@@ -694,22 +758,36 @@ static cudaError_t run_patch(const PatchGeom& pg, const OutGeom& o, float* img, 
     p.bimg = img;
     p.n_tiles = (o.ncols + BN - 1) / BN;
     p.k_stages = pg.nch * pg.spc;
-    const int tiles = pg.Nb * pg.tpi * p.n_tiles;
+    TailPlan tp{pg.Nb * pg.tpi * p.n_tiles, 1, 0, 0};
+    if (part) tp = plan_patch_tail(pg, o.ncols, BN);
+    p.full_units = tp.full_units;
+    p.tail_split = tp.split;
+    p.part_buf = part;
+    const int units = tp.full_units + tp.tail_tiles * tp.split;
+    cudaError_t e;
     // short tiles: double-buffer the accumulators (fewer A stages) so the
     // epilogue overlaps the next tile's MMAs
-    if constexpr (BN == 64)
-        if (p.k_stages <= kShortTileStages)
-            return launch_tc_patch<ConvPatchProb<BN>, BN, TMA, true>(p, tiles, device_error_word(), st);
-    return launch_tc_patch<ConvPatchProb<BN>, BN, TMA, false>(p, tiles, device_error_word(), st);
+    bool db2 = false;
+    if constexpr (BN == 64) db2 = p.k_stages <= kShortTileStages;
+    if (db2)
+        e = launch_tc_patch<ConvPatchProb<BN>, BN, TMA, BN <= 64>(p, units, device_error_word(), st);
+    else
+        e = launch_tc_patch<ConvPatchProb<BN>, BN, TMA, false>(p, units, device_error_word(), st);
+    if (e != cudaSuccess || tp.tail_tiles == 0) return e;
+    tail_reduce_kernel<ConvPatchProb<BN>, BN>
+        <<<dim3(unsigned(tp.tail_tiles), unsigned(BN / 32)), kTailThreads, 0, st>>>(p);
+    note_launch();
+    return cudaGetLastError();
 }
 
 template <bool TMA>
-static cudaError_t dispatch_patch(int bn, const PatchGeom& pg, const OutGeom& o, float* img, cudaStream_t st)
+static cudaError_t dispatch_patch(int bn, const PatchGeom& pg, const OutGeom& o, float* img, float* part,
+                                  cudaStream_t st)
 {
     switch (bn) {
-    case 32: return run_patch<32, TMA>(pg, o, img, st);
-    case 64: return run_patch<64, TMA>(pg, o, img, st);
-    default: return run_patch<128, TMA>(pg, o, img, st);
+    case 32: return run_patch<32, TMA>(pg, o, img, part, st);
+    case 64: return run_patch<64, TMA>(pg, o, img, part, st);
+    default: return run_patch<128, TMA>(pg, o, img, part, st);
     }
 }
 
@@ -925,9 +1003,9 @@ static WindowPlan plan_window(int Nb, int Ci, int Hi, int Wi, int Gp, int Gq, in
         w.tma = patch_tma_fits(pg, w.bn);
         w.patch = w.tma || max_patch_floats(pg) <= patch_capacity(w.bn);
         if (w.tma) w.blocked_bytes = blocked_bytes(pg);
+        if (w.patch) w.part_bytes = round_up_256(plan_patch_tail(pg, ncols, w.bn).part_floats * sizeof(float));
     }
     w.img_bytes = round_up_256(bimage_floats(ncols, k_extent(Ci, T), w.bn) * sizeof(float));
-    w.part_bytes = 0;
     if (!w.patch) {
         const GatherGeom g = make_gather(nullptr, Nb, Ci, Hi, Wi, Gp, Gq, sp, o, T);
         const TailPlan tp = plan_tail(((g.M + kBM - 1) / kBM) * n_tiles, (g.K + kBK - 1) / kBK, w.bn);
@@ -952,13 +1030,17 @@ static cudaError_t run_window_gemm(const float* in, int Nb, int Ci, int Hi, int 
         const int k_total = pg.mode == 0 ? pg.nch * T * T * kBK : T * T * pg.Cp;   // padded taps excluded
         cudaError_t e = build_bimage(make_gen(dec), og.ncols, k_total, bn, img, st);
         if (e != cudaSuccess) return e;
+        // workspace: [B image][channel-blocked copy (tensor-map form)][tail partial tiles]
+        float* part = wp.part_bytes ? reinterpret_cast<float*>(static_cast<char*>(ws) + wp.img_bytes +
+                                                               wp.blocked_bytes)
+                                    : nullptr;
         if (wp.tma) {
             patch_box(pg);
             e = setup_patch_tma(pg, reinterpret_cast<float*>(static_cast<char*>(ws) + wp.img_bytes), st);
             if (e != cudaSuccess) return e;
-            return dispatch_patch<true>(bn, pg, og, img, st);
+            return dispatch_patch<true>(bn, pg, og, img, part, st);
         }
-        return dispatch_patch<false>(bn, pg, og, img, st);
+        return dispatch_patch<false>(bn, pg, og, img, part, st);
     }
     const GatherGeom g = make_gather(in, Nb, Ci, Hi, Wi, Gp, Gq, sp, o, T);
     const KDecode dec = make_kdecode(g.mode == 2 ? 2 : 0, g.Cp, T);
@@ -1015,7 +1097,7 @@ cudaError_t launch_conv_fwd(const ConvDims& d, const float* x, const float* w, c
         if (e != cudaSuccess) return e;
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if ((e = encode_patch_tmap(pg, blocked)) != cudaSuccess) return e;
-        return dispatch_patch<true>(sp.bn, pg, o, img, st);
+        return dispatch_patch<true>(sp.bn, pg, o, img, nullptr, st);
     }
     auto make_gen = [&](const KDecode& dec) { return FwdFilterGen{w, d.C, d.R, dec, FastDiv(uint32_t(d.R))}; };
     return run_window_gemm(x, d.N, d.C, d.H, d.W, d.P, d.Q, d.S, -d.pad, d.R, o, ws, make_gen, st);

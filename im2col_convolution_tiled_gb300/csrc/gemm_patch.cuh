@@ -158,6 +158,13 @@ constexpr size_t patch_tma_smem(uint32_t tbytes)
     return 1024 + size_t(C::kStages) * C::kStage + 2 * size_t(tbytes) + C::kCtlBytes;
 }
 
+// One work unit of the patch kernel (see the problem interface below).
+struct PatchUnit {
+    int tt;         // whole tile
+    int cc0, cc1;   // channel chunks [cc0, cc1)
+    int part;       // >= 0: partial-tile slot of a K piece of a split trailing tile
+};
+
 struct PatchCtl {
     uint64_t full[8];
     uint64_t empty[8];
@@ -171,8 +178,12 @@ struct PatchCtl {
 };
 
 // The problem supplies the B image location and the epilogue (same interface
-// as ConvGatherProb: b_image, EState, e_setup, store).  Tile decode is fixed:
-// t -> (n_tile = t % n_tiles, image, tile in image).
+// as ConvGatherProb: b_image, EState, e_setup, store).  Work units: unit(t)
+// gives the whole tile tt it belongs to (decoded as n_tile = tt % n_tiles,
+// image, tile in image), its chunk range [cc0, cc1) and, for one K piece of a
+// split trailing tile, the slot of its partial tile (part >= 0).  Units can
+// differ in stage count, so every role keeps the CTA-wide stage counter as a
+// running sum.
 //
 // TMA selects how a chunk's patch arrives: per-channel bulk copies of the
 // NCHW tensor (channel-major patch, any channel count), or one 4-D tensor-map
@@ -261,7 +272,8 @@ __global__ void __launch_bounds__(PatchCfg<BN, DB2>::kThreads, 1) tc_patch_kerne
         bool ok = true;
         const uint32_t tbase = tmem_base + (uint32_t((warp & 3) * 32) << 16);
         for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-            const TileGeo q = tile_geo(t);
+            const PatchUnit un = prob.unit(t);
+            const TileGeo q = tile_geo(un.tt);
             const int cstride = patch_cstride(q.rows * g.Wi, g.HiWi);   // floats per channel in the patch
             const int pix = q.first + tid;
             const bool pvalid = pix <= q.last;
@@ -273,7 +285,7 @@ __global__ void __launch_bounds__(PatchCfg<BN, DB2>::kThreads, 1) tc_patch_kerne
             const int hp0 = int(pp) * g.sp + g.o;  // input row of tap 0
             const int wp0 = int(pq) * g.sp + g.o;  // input column of tap 0
             const int tpix0 = (int(pp) - q.p_lo) * g.sp * g.Wt + int(pq) * g.sp;   // box pixel of tap 0
-            for (int cc = 0; cc < g.nch && ok; ++cc, ++u) {
+            for (int cc = un.cc0; cc < un.cc1 && ok; ++cc, ++u) {
                 const int pb = int(u & 1u);
                 // every channel run of this chunk starts s0 floats into its block
                 const long long x0 = (long long)q.n * g.CiHiWi + (long long)(cc * 32) * g.HiWi + (long long)q.h_lo * g.Wi;
@@ -321,7 +333,7 @@ __global__ void __launch_bounds__(PatchCfg<BN, DB2>::kThreads, 1) tc_patch_kerne
                     if (!mbar_wait_warp(&ctl->empty[slot], phase ^ 1u, abort_flag)) { ok = false; break; }
                     if (tid == 0) {
                         mbar_arrive_expect_tx(&ctl->full[slot], b_bytes);
-                        bulk_g2s(smem + (b_hi(slot) - smem_base), prob.b_image_t(t, ks), b_bytes,
+                        bulk_g2s(smem + (b_hi(slot) - smem_base), prob.b_image_t(un.tt, ks), b_bytes,
                                  &ctl->full[slot]);
                         last_issued = int(c);
                     }
@@ -360,9 +372,10 @@ __global__ void __launch_bounds__(PatchCfg<BN, DB2>::kThreads, 1) tc_patch_kerne
         uint32_t u = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-            const TileGeo q = tile_geo(t);
+            const PatchUnit un = prob.unit(t);
+            const TileGeo q = tile_geo(un.tt);
             const int cstride = patch_cstride(q.rows * g.Wi, g.HiWi);
-            for (int cc = 0; cc < g.nch && ok; ++cc, ++u) {
+            for (int cc = un.cc0; cc < un.cc1 && ok; ++cc, ++u) {
                 const int pb = int(u & 1u);
                 // chunk u - 2 (same buffer) must be fully read
                 if (u >= 2 && !mbar_wait_warp(&ctl->pempty[pb], ((u >> 1) - 1) & 1u, abort_flag)) {
@@ -419,14 +432,15 @@ __global__ void __launch_bounds__(PatchCfg<BN, DB2>::kThreads, 1) tc_patch_kerne
             int local = 0;
             bool ok = true;
             bool issued_any = false;
-            const uint32_t k_stages = uint32_t(g.nch * g.spc);
+            uint32_t c0 = 0;   // CTA-wide counter of the unit's first stage
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
+                const PatchUnit un = prob.unit(t);
+                const uint32_t k_stages = uint32_t((un.cc1 - un.cc0) * g.spc);
                 const int buf = local % DB;
                 const uint32_t acc_phase = uint32_t(local / DB) & 1u;
                 if (!mbar_wait(&ctl->acce[buf], acc_phase ^ 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + uint32_t((2 * buf + int(me)) * BN);
-                const uint32_t c0 = uint32_t(local) * k_stages;   // CTA-wide counter of the tile's first stage
                 uint32_t accumulate = 0;
                 for (uint32_t ks = me ^ (c0 & 1u); ks < k_stages; ks += 2) {
                     const uint32_t c = c0 + ks;
@@ -452,6 +466,7 @@ __global__ void __launch_bounds__(PatchCfg<BN, DB2>::kThreads, 1) tc_patch_kerne
                     mma_commit(&ctl->empty[slot]);
                 }
                 if (!ok) break;
+                c0 += k_stages;
                 // arrives once this issuer's MMAs of the tile are done (at once
                 // if it had none: a one-stage tile)
                 mma_commit(&ctl->accf[buf]);
@@ -470,20 +485,23 @@ __global__ void __launch_bounds__(PatchCfg<BN, DB2>::kThreads, 1) tc_patch_kerne
         // ---------------- epilogue ----------------
         const int q = warp & 3;
         const int row = q * 32 + lane;
-        const uint32_t k_stages = uint32_t(g.nch * g.spc);
+        uint32_t c0 = 0;   // CTA-wide counter of the unit's first stage
         int local = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
+            const PatchUnit un = prob.unit(t);
+            const uint32_t k_stages = uint32_t((un.cc1 - un.cc0) * g.spc);
             const int buf = local % DB;
             const uint32_t acc_phase = uint32_t(local / DB) & 1u;
             if (!mbar_wait_warp(&ctl->accf[buf], acc_phase, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            // a one-stage tile leaves the other issuer's accumulator untouched
-            const uint32_t c0 = uint32_t(local) * k_stages;
+            // a one-stage unit leaves the other issuer's accumulator untouched
             const bool use0 = k_stages >= 2 || (c0 & 1u) == 0;
             const bool use1 = k_stages >= 2 || (c0 & 1u) == 1;
-            const Tile tile = prob.tile_t(t);
-            typename Prob::EState es = prob.e_setup_t(t, row);
+            c0 += k_stages;
+            Tile tile = prob.tile_t(un.tt);
+            tile.part = un.part;
+            typename Prob::EState es = prob.e_setup_t(un.tt, row);
             const uint32_t lane_base = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(2 * buf * BN);
 #pragma unroll 1
             for (int c = 0; c < BN; c += 32) {
