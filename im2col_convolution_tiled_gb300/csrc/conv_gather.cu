@@ -769,10 +769,14 @@ static cudaError_t run_patch(const PatchGeom& pg, const OutGeom& o, float* img, 
     // epilogue overlaps the next tile's MMAs
     bool db2 = false;
     if constexpr (BN == 64) db2 = p.k_stages <= kShortTileStages;
+    // Long tiles stack the B tiles (two MMAs per K step instead of three; one
+    // accumulator buffer per issuer then): AlexNet conv2's input gradient
+    // 0.329 -> 0.298 ms.  Short tiles keep the second buffer instead, which
+    // stacking would cost them (conv1's forward measured 13% slower stacked).
     if (db2)
-        e = launch_tc_patch<ConvPatchProb<BN>, BN, TMA, BN <= 64>(p, units, device_error_word(), st);
+        e = launch_tc_patch<ConvPatchProb<BN>, BN, TMA, BN <= 64>(p, units, device_error_word(), st, false);
     else
-        e = launch_tc_patch<ConvPatchProb<BN>, BN, TMA, false>(p, units, device_error_word(), st);
+        e = launch_tc_patch<ConvPatchProb<BN>, BN, TMA, false>(p, units, device_error_word(), st, true);
     if (e != cudaSuccess || tp.tail_tiles == 0) return e;
     tail_reduce_kernel<ConvPatchProb<BN>, BN>
         <<<dim3(unsigned(tp.tail_tiles), unsigned(BN / 32)), kTailThreads, 0, st>>>(p);

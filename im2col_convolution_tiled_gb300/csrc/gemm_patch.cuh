@@ -123,22 +123,31 @@ __device__ __forceinline__ void patch_taps(const PatchGeom& g, const float* pbuf
 // DB2 asks for two accumulator buffers per issuer even where that leaves only
 // four A stages (64-wide tiles): worth it when tiles have few K stages, so that
 // the epilogue of one tile would otherwise stall the next tile's MMAs.
-template <int BN, bool DB2 = false>
+//
+// STACK (tiles at most 64 wide, 3xTF32): per 8-deep K step two MMAs instead of
+// three.  The stage's B tiles lie back to back in shared memory (hi rows, then
+// lo rows), so one MMA with N = 2*BN multiplies A_hi by both: hi*hi into the
+// accumulator's first BN columns, hi*lo into the next BN; a second MMA (N = BN)
+// adds lo*hi to the first BN.  The epilogue adds the two halves.  Each A column
+// block is then read from tensor memory twice per K step instead of three times.
+template <int BN, bool DB2 = false, bool STACK = false>
 struct PatchCfg {
     static_assert(BN <= 128, "the patch kernel keeps an accumulator per issuer and at least four A stages in "
                              "tensor memory");
     static_assert(!DB2 || BN <= 64, "two buffers per issuer and four A stages need tiles at most 64 wide");
+    static_assert(!STACK || BN <= 64, "stacked B tiles need 2*BN <= 128 accumulator columns");
     static constexpr int kThreads = 480;
+    static constexpr int kAccW = STACK ? 2 * BN : BN;   // accumulator columns per issuer and buffer
     // accumulator buffers per issuer: two (the epilogue of tile i overlaps the
-    // main loop of tile i+1) when six A stages still fit beside them (or DB2),
-    // else one
-    static constexpr int kDBuf = (DB2 || (512 - 4 * BN) / 64 >= 6) ? 2 : 1;
-    static constexpr int kTmemStages0 = (512 - 2 * kDBuf * BN) / 64;
+    // main loop of tile i+1) when six A stages still fit beside them (or DB2
+    // and four still fit), else one
+    static constexpr int kDBuf = ((DB2 && 512 - 4 * kAccW >= 4 * 64) || (512 - 4 * kAccW) / 64 >= 6) ? 2 : 1;
+    static constexpr int kTmemStages0 = (512 - 2 * kDBuf * kAccW) / 64;
     static constexpr int kStages = (kTmemStages0 > 6 ? 6 : kTmemStages0) & ~1;   // even: slot parity = issuer
     static_assert(kStages >= 4, "too few A stages fit in tensor memory");
     static constexpr uint32_t kBTile = BN * kBK * 4;
     static constexpr uint32_t kStage = 2 * kBTile;
-    static constexpr uint32_t kACol = uint32_t(2 * kDBuf * BN);   // accumulators: [buffer][issuer]
+    static constexpr uint32_t kACol = uint32_t(2 * kDBuf * kAccW);   // accumulators: [buffer][issuer]
     static constexpr size_t kCtlBytes = 512;
     static constexpr size_t kMaxSmem = 227 * 1024;
     // two patch buffers share what the B stages leave
@@ -147,14 +156,15 @@ struct PatchCfg {
     static constexpr int kPatchFloats = int(kPatchBytes / 4);
     static constexpr size_t kSmemBytes = 1024 + size_t(kStages) * kStage + 2 * kPatchBytes + kCtlBytes;
     static constexpr uint32_t kIdesc = idesc_tf32(kBM, BN);
+    static constexpr uint32_t kIdesc2 = idesc_tf32(kBM, STACK ? 2 * BN : BN);   // the stacked hi*[hi; lo] MMA
 };
 
 // Dynamic shared memory of the tensor-map form: alignment slack, B stages, two
 // box buffers of `tbytes` each, control block.
-template <int BN, bool DB2 = false>
+template <int BN, bool DB2 = false, bool STACK = false>
 constexpr size_t patch_tma_smem(uint32_t tbytes)
 {
-    using C = PatchCfg<BN, DB2>;
+    using C = PatchCfg<BN, DB2, STACK>;
     return 1024 + size_t(C::kStages) * C::kStage + 2 * size_t(tbytes) + C::kCtlBytes;
 }
 
@@ -190,10 +200,12 @@ struct PatchCtl {
 // box of the channel-blocked copy (pixel-major swizzled patch, mode 0): there
 // a converter thread reads its 32 channels with eight conflict-free 16-byte
 // loads and needs no bounds tests, since the box is zero outside the image.
-template <class Prob, int BN, bool TMA, bool DB2, int TERMS>
-__global__ void __launch_bounds__(PatchCfg<BN, DB2>::kThreads, 1) tc_patch_kernel(const __grid_constant__ Prob prob, int* err_word)
+template <class Prob, int BN, bool TMA, bool DB2, int TERMS, bool STACK>
+__global__ void __launch_bounds__(PatchCfg<BN, DB2, STACK>::kThreads, 1) tc_patch_kernel(const __grid_constant__ Prob prob, int* err_word)
 {
-    using Cfg = PatchCfg<BN, DB2>;
+    static_assert(!STACK || TERMS == 3, "stacking pairs the hi and lo B tiles of 3xTF32");
+    using Cfg = PatchCfg<BN, DB2, STACK>;
+    constexpr int AW = Cfg::kAccW;
     constexpr int S = Cfg::kStages;
     constexpr int DB = Cfg::kDBuf;
     const PatchGeom& g = prob.pg;
@@ -440,7 +452,7 @@ __global__ void __launch_bounds__(PatchCfg<BN, DB2>::kThreads, 1) tc_patch_kerne
                 const uint32_t acc_phase = uint32_t(local / DB) & 1u;
                 if (!mbar_wait(&ctl->acce[buf], acc_phase ^ 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + uint32_t((2 * buf + int(me)) * BN);
+                const uint32_t d_tmem = tmem_base + uint32_t((2 * buf + int(me)) * AW);
                 uint32_t accumulate = 0;
                 for (uint32_t ks = me ^ (c0 & 1u); ks < k_stages; ks += 2) {
                     const uint32_t c = c0 + ks;
@@ -453,7 +465,11 @@ __global__ void __launch_bounds__(PatchCfg<BN, DB2>::kThreads, 1) tc_patch_kerne
                         const uint64_t bl = sdesc_k_sw128(b_lo(slot) + kk * 32);
                         const uint32_t ah = tmem_base + a_col(slot) + uint32_t(kk * 8);
                         const uint32_t al = ah + 32;
-                        if (three) {
+                        if (STACK) {
+                            // columns [0, BN): hi*hi (+ lo*hi below); [BN, 2BN): hi*lo
+                            mma_tf32_ts(d_tmem, ah, bh, Cfg::kIdesc2, accumulate);
+                            mma_tf32_ts(d_tmem, al, bh, Cfg::kIdesc, 1);
+                        } else if (three) {
                             mma_tf32_ts(d_tmem, al, bh, Cfg::kIdesc, accumulate);
                             mma_tf32_ts(d_tmem, ah, bl, Cfg::kIdesc, 1);
                             mma_tf32_ts(d_tmem, ah, bh, Cfg::kIdesc, 1);
@@ -502,11 +518,23 @@ __global__ void __launch_bounds__(PatchCfg<BN, DB2>::kThreads, 1) tc_patch_kerne
             Tile tile = prob.tile_t(un.tt);
             tile.part = un.part;
             typename Prob::EState es = prob.e_setup_t(un.tt, row);
-            const uint32_t lane_base = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(2 * buf * BN);
+            const uint32_t lane_base = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(2 * buf * AW);
 #pragma unroll 1
             for (int c = 0; c < BN; c += 32) {
                 uint32_t r0[32], r1[32];
-                tmem_ld32x2(lane_base + uint32_t(c), lane_base + uint32_t(BN + c), r0, r1);
+                if constexpr (STACK) {
+                    // each issuer's hi*lo half added to its first half, one
+                    // issuer at a time (keeps two register blocks live)
+                    tmem_ld32x2(lane_base + uint32_t(c), lane_base + uint32_t(BN + c), r0, r1);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r0[i] = __float_as_uint(__uint_as_float(r0[i]) + __uint_as_float(r1[i]));
+                    uint32_t h[32];
+                    tmem_ld32x2(lane_base + uint32_t(AW + c), lane_base + uint32_t(AW + BN + c), r1, h);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r1[i] = __float_as_uint(__uint_as_float(r1[i]) + __uint_as_float(h[i]));
+                } else {
+                    tmem_ld32x2(lane_base + uint32_t(c), lane_base + uint32_t(AW + c), r0, r1);
+                }
                 if (c + 32 >= BN) {
                     // the accumulators are free once the last columns are in registers
                     tc_fence_before();
@@ -531,31 +559,34 @@ __global__ void __launch_bounds__(PatchCfg<BN, DB2>::kThreads, 1) tc_patch_kerne
     }
 }
 
-template <class Prob, int BN, bool TMA, bool DB2, int TERMS>
+template <class Prob, int BN, bool TMA, bool DB2, int TERMS, bool STACK>
 cudaError_t launch_tc_patch_terms(const Prob& prob, int num_tiles, int* err_word, cudaStream_t stream)
 {
-    using Cfg = PatchCfg<BN, DB2>;
+    using Cfg = PatchCfg<BN, DB2, STACK>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(tc_patch_kernel<Prob, BN, TMA, DB2, TERMS>,
+        cudaError_t e = cudaFuncSetAttribute(tc_patch_kernel<Prob, BN, TMA, DB2, TERMS, STACK>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cfg::kMaxSmem));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     if (num_tiles <= 0) return cudaSuccess;
-    const size_t smem = TMA ? patch_tma_smem<BN, DB2>(prob.pg.tbytes) : Cfg::kSmemBytes;
+    const size_t smem = TMA ? patch_tma_smem<BN, DB2, STACK>(prob.pg.tbytes) : Cfg::kSmemBytes;
     int grid = num_tiles < sm_count() ? num_tiles : sm_count();
-    tc_patch_kernel<Prob, BN, TMA, DB2, TERMS><<<grid, Cfg::kThreads, smem, stream>>>(prob, err_word);
+    tc_patch_kernel<Prob, BN, TMA, DB2, TERMS, STACK><<<grid, Cfg::kThreads, smem, stream>>>(prob, err_word);
     note_launch();
     return cudaGetLastError();
 }
 
-// prob.terms (3 or 1) selects the kernel instantiation.
+// prob.terms (3 or 1) selects the kernel instantiation; 3xTF32 tiles at most
+// 64 wide stack their B tiles when `stack` is set.
 template <class Prob, int BN, bool TMA, bool DB2>
-cudaError_t launch_tc_patch(const Prob& prob, int num_tiles, int* err_word, cudaStream_t stream)
+cudaError_t launch_tc_patch(const Prob& prob, int num_tiles, int* err_word, cudaStream_t stream, bool stack)
 {
-    return prob.terms == 1 ? launch_tc_patch_terms<Prob, BN, TMA, DB2, 1>(prob, num_tiles, err_word, stream)
-                           : launch_tc_patch_terms<Prob, BN, TMA, DB2, 3>(prob, num_tiles, err_word, stream);
+    if (prob.terms == 1) return launch_tc_patch_terms<Prob, BN, TMA, DB2, 1, false>(prob, num_tiles, err_word, stream);
+    if constexpr (BN <= 64)
+        if (stack) return launch_tc_patch_terms<Prob, BN, TMA, DB2, 3, true>(prob, num_tiles, err_word, stream);
+    return launch_tc_patch_terms<Prob, BN, TMA, DB2, 3, false>(prob, num_tiles, err_word, stream);
 }
 
 }  // namespace cb200
