@@ -37,6 +37,12 @@ struct ConvWgradProb {
     int PQ, NPQ, CRS, HW, CHW;
     FastDiv f_pq, f_q, f_rr, f_r;
     int m_tiles, n_tiles, k_stages, splits, ks_per_split;
+    // Space-to-depth form (s2dS > 1): x is X', the geometry above is the
+    // derived stride-1 convolution, and the rows are the ORIGINAL taps
+    // (c, r, q), CRS = C_orig * R_orig^2, decoded by f_rr / f_r over R_orig and
+    // read from X' channel (c*s2dS + r % s2dS)*s2dS + q % s2dS, tap
+    // (r / s2dS, q / s2dS).
+    int s2dS = 0;
 
     __device__ int num_tiles() const { return m_tiles * n_tiles * splits; }
     __device__ Tile tile(int t) const
@@ -68,6 +74,12 @@ struct ConvWgradProb {
                 uint32_t c, rem, r, q;
                 f_rr.divmod(uint32_t(crs), c, rem);
                 f_r.divmod(rem, r, q);
+                if (s2dS > 1) {
+                    const uint32_t S2 = uint32_t(s2dS);
+                    c = (c * S2 + r % S2) * S2 + q % S2;
+                    r /= S2;
+                    q /= S2;
+                }
                 s.rowoff[p] = int(c) * HW + int(r) * W + int(q);
                 s.rq[p] = int((r << 16) | q);
             } else {
@@ -192,7 +204,10 @@ __global__ void wgrad_reduce_kernel(const float* __restrict__ part, int splits, 
 //   X'[n, c', hh, ww] = x[n, c, S*hh + a - pad, S*ww + b - pad],  c' = c*S*S + a*S + b
 // with T = ceil(R / S) taps (see the forward's space-to-depth form), whose
 // column-matrix gather reads X' with unit stride instead of x with stride S;
-// then dW[k, c, r, s] = dW'[k, (c, r % S, s % S), r / S, s / S].
+// then dW[k, c, r, s] = dW'[k, (c, r % S, s % S), r / S, s / S].  The GEMM's
+// rows are the original taps (c, r, s), each gathering its X' channel and tap:
+// the taps past the filter (S*tr + a >= R), zero in W', are not computed
+// (AlexNet conv1: 363 rows, three tiles, instead of 48 * 3 * 3 = 432, four).
 // X' is written NCHW (rows of ww contiguous) for the gather.
 struct WgradS2d {
     bool use;
@@ -222,32 +237,16 @@ static WgradS2d plan_wgrad_s2d(const ConvDims& d)
     return w;
 }
 
-// dW[k, c, r, s] = sum over split (ascending) of part[split][k, (c, r % S, s % S), r / S, s / S].
-__global__ void wgrad_reduce_s2d_kernel(const float* __restrict__ part, int splits, int K, int C, int R, int S, int T,
-                                        float* __restrict__ dw)
-{
-    const int count = K * C * R * R;
-    const int Cs = C * S * S;
-    const long long pcount = (long long)K * Cs * T * T;
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < count; i += gridDim.x * blockDim.x) {
-        const int s = i % R, r = (i / R) % R, c = (i / (R * R)) % C, k = i / (R * R * C);
-        const int cp = c * S * S + (r % S) * S + (s % S);
-        const long long j = (((long long)k * Cs + cp) * T + r / S) * T + s / S;
-        float acc = 0.f;
-        for (int sp = 0; sp < splits; ++sp) acc += __ldg(part + sp * pcount + j);
-        dw[i] = acc;
-    }
-}
-
 struct WgradPlan {
     int bn, m_tiles, n_tiles, k_stages, splits, ks_per_split;
 };
 
-static WgradPlan plan_wgrad(const ConvDims& d)
+// rows: the GEMM's row count (taps of the original convolution)
+static WgradPlan plan_wgrad(const ConvDims& d, int rows)
 {
     WgradPlan pl;
     pl.bn = pick_conv_bn(d.K, &pl.n_tiles);
-    const int CRS = d.C * d.R * d.R;
+    const int CRS = rows;
     const long long NPQ = (long long)d.N * d.P * d.Q;
     pl.m_tiles = (CRS + kBM - 1) / kBM;
     pl.k_stages = int((NPQ + kBK - 1) / kBK);
@@ -289,9 +288,9 @@ static size_t xs2d_floats(const ConvDims& d, const WgradS2d& w)
     return w.use ? (size_t(d.N) * w.Cs * w.Hs * w.Ws + 63) & ~size_t(63) : 0;
 }
 
-static size_t wgrad_part_floats(const ConvDims& g, const WgradPlan& pl, bool s2d)
+static size_t wgrad_part_floats(const ConvDims& d, const WgradPlan& pl)
 {
-    return (pl.splits > 1 || s2d) ? size_t(pl.splits) * g.K * g.C * g.R * g.R : 0;
+    return pl.splits > 1 ? size_t(pl.splits) * d.K * d.C * d.R * d.R : 0;
 }
 
 // Row-sum partials of the G image (the bias gradient of conv_bwd_filter_bias).
@@ -300,22 +299,19 @@ static size_t wgrad_rowsum_floats(const ConvDims& d)
     return size_t(d.K) * bimage_grid_x(d.N * d.P * d.Q);
 }
 
-// Workspace: [X' (space-to-depth form)] [the G image] [partial tiles: split-K,
-// or always in the space-to-depth form (remapped by its reduce)] [row-sum
-// partials for the bias gradient].
+// Workspace: [X' (space-to-depth form)] [the G image] [split-K partial tiles]
+// [row-sum partials for the bias gradient].
 size_t conv_wgrad_ws(const ConvDims& d)
 {
     const WgradS2d w = plan_wgrad_s2d(d);
     const ConvDims& g = w.use ? w.d2 : d;
-    WgradPlan pl = plan_wgrad(g);
-    return (xs2d_floats(d, w) + wgrad_image_floats(g, pl) + wgrad_part_floats(g, pl, w.use) +
-            wgrad_rowsum_floats(d)) *
+    WgradPlan pl = plan_wgrad(g, d.C * d.R * d.R);
+    return (xs2d_floats(d, w) + wgrad_image_floats(g, pl) + wgrad_part_floats(d, pl) + wgrad_rowsum_floats(d)) *
            sizeof(float);
 }
 
 // d: the convolution the GEMM runs (the derived one in the space-to-depth
-// form); ws: its image and partials.  With remap, the partials always go to
-// the workspace and wgrad_reduce_s2d_kernel writes dW of `orig`.
+// form, whose rows are then orig's taps); ws: its image and partials.
 // With db non-null the G image pass also sums each row of G (the bias
 // gradient) into row-sum partials, added in block order by rowsum_final_kernel.
 template <int BN>
@@ -324,22 +320,24 @@ static cudaError_t run_wgrad(const ConvDims& d, const WgradPlan& pl, const float
 {
     ConvWgradProb<BN> p;
     p.terms = math_terms();
+    const ConvDims& o = orig ? *orig : d;   // the convolution whose filter gradient is written
     float* img = static_cast<float*>(ws);
     float* part = img + wgrad_image_floats(d, pl);
-    float* rowsum = part + wgrad_part_floats(d, pl, orig != nullptr);
+    float* rowsum = part + wgrad_part_floats(o, pl);
     p.x = x;
     p.bimg = img;
-    p.out = (pl.splits > 1 || orig) ? part : dw;
+    p.out = pl.splits > 1 ? part : dw;
     p.C = d.C; p.H = d.H; p.W = d.W; p.K = d.K; p.R = d.R; p.S = d.S; p.pad = d.pad; p.P = d.P; p.Q = d.Q;
     p.PQ = d.P * d.Q;
     p.NPQ = d.N * p.PQ;
-    p.CRS = d.C * d.R * d.R;
+    p.CRS = o.C * o.R * o.R;
     p.HW = d.H * d.W;
     p.CHW = d.C * p.HW;
     p.f_pq = FastDiv(p.PQ);
     p.f_q = FastDiv(d.Q);
-    p.f_rr = FastDiv(d.R * d.R);
-    p.f_r = FastDiv(d.R);
+    p.f_rr = FastDiv(o.R * o.R);
+    p.f_r = FastDiv(o.R);
+    p.s2dS = orig ? orig->S : 0;
     p.m_tiles = pl.m_tiles;
     p.n_tiles = pl.n_tiles;
     p.k_stages = pl.k_stages;
@@ -355,13 +353,6 @@ static cudaError_t run_wgrad(const ConvDims& d, const WgradPlan& pl, const float
     }
     e = launch_tc_gemm<ConvWgradProb<BN>, BN>(p, p.m_tiles * p.n_tiles * p.splits, device_error_word(), st);
     if (e != cudaSuccess) return e;
-    if (orig) {
-        const int count = orig->K * orig->C * orig->R * orig->R;
-        const int blocks = (count + 255) / 256 < 8 * sm_count() ? (count + 255) / 256 : 8 * sm_count();
-        wgrad_reduce_s2d_kernel<<<blocks, 256, 0, st>>>(part, pl.splits, orig->K, orig->C, orig->R, orig->S, d.R, dw);
-        note_launch();
-        return cudaGetLastError();
-    }
     if (pl.splits == 1) return e;
     const long long count = (long long)d.K * p.CRS;
     long long blocks = (count + 255) / 256;
@@ -377,7 +368,7 @@ cudaError_t launch_conv_wgrad(const ConvDims& d, const float* x, const float* dy
     const WgradS2d w = plan_wgrad_s2d(d);
     const ConvDims& g = w.use ? w.d2 : d;
     const ConvDims* orig = w.use ? &d : nullptr;
-    WgradPlan pl = plan_wgrad(g);
+    WgradPlan pl = plan_wgrad(g, d.C * d.R * d.R);
     const float* xg = x;
     void* gws = ws;
     if (w.use) {
