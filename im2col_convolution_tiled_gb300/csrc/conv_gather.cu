@@ -429,10 +429,18 @@ struct KDecode {
     FastDiv f_cp;      // order 0: Cp
     FastDiv f_chunk;   // order 1: T*T*32
     FastDiv f_tt;      // order 2: T*T
+    // order 1 with a half last chunk (the patch kernel's two-tap stages): from
+    // K index half_k0 on, stage j holds taps 2j and 2j + 1, channels
+    // half_c0 + 0..15 of each (half_k0 = INT32_MAX: none)
+    int half_k0 = 0x7FFFFFFF, half_c0 = 0;
     __device__ __forceinline__ void operator()(int kk, int& c, int& tap) const
     {
         uint32_t a, b;
-        if (order == 0) {
+        if (kk >= half_k0) {
+            const int rel = kk - half_k0;
+            tap = 2 * (rel >> 5) + ((rel >> 4) & 1);
+            c = half_c0 + (rel & 15);
+        } else if (order == 0) {
             f_cp.divmod(uint32_t(kk), a, b);
             tap = int(a);
             c = int(b);
@@ -706,10 +714,37 @@ static PatchGeom make_patch(const float* in, int Nb, int Ci, int Hi, int Wi, int
         pg.spc = T * T;
         pg.pc = 32;
     }
+    pg.half = 0;
+    pg.spch = pg.spc;
     pg.f_gq = FastDiv(uint32_t(Gq));
     pg.f_t = FastDiv(uint32_t(T));
     return pg;
 }
+
+// Tensor-map form: a last chunk of at most 16 channels takes two taps per
+// stage (AlexNet conv1's space-to-depth forward: 48 channels, 2 chunks of 9
+// taps -> 9 + 5 stages instead of 18).
+static void set_half_chunk(PatchGeom& pg)
+{
+    const int last = pg.Ci - 32 * (pg.nch - 1);
+    if (pg.mode == 0 && last <= 16 && pg.T * pg.T >= 2) {
+        pg.half = 1;
+        pg.spch = (pg.T * pg.T + 1) / 2;
+    }
+}
+
+// The patch kernel's K order decode (matching set_half_chunk).
+static KDecode patch_kdecode(const PatchGeom& pg)
+{
+    KDecode dec = make_kdecode(pg.mode == 0 ? 1 : 0, pg.Cp, pg.T);
+    if (pg.half) {
+        dec.half_k0 = (pg.nch - 1) * pg.spc * kBK;
+        dec.half_c0 = (pg.nch - 1) * 32;
+    }
+    return dec;
+}
+
+static int patch_kstages(const PatchGeom& pg) { return pg.stages_range(0, pg.nch); }
 
 static int patch_capacity(int bn)
 {
@@ -757,7 +792,7 @@ static cudaError_t run_patch(const PatchGeom& pg, const OutGeom& o, float* img, 
     p.o = o;
     p.bimg = img;
     p.n_tiles = (o.ncols + BN - 1) / BN;
-    p.k_stages = pg.nch * pg.spc;
+    p.k_stages = patch_kstages(pg);
     TailPlan tp{pg.Nb * pg.tpi * p.n_tiles, 1, 0, 0};
     if (part) tp = plan_patch_tail(pg, o.ncols, BN);
     p.full_units = tp.full_units;
@@ -958,6 +993,7 @@ static S2dPlan plan_fwd_s2d(const ConvDims& d)
     sp.pg = make_patch(nullptr, d.N, sp.Ci, d.P + sp.T - 1, d.Q + sp.T - 1, d.P, d.Q, 1, 0, sp.T);
     if (sp.pg.mode != 0) return sp;
     patch_box(sp.pg);
+    set_half_chunk(sp.pg);
     sp.use = patch_tma_fits(sp.pg, sp.bn);
     return sp;
 }
@@ -1030,8 +1066,9 @@ static cudaError_t run_window_gemm(const float* in, int Nb, int Ci, int Hi, int 
     const int bn = wp.bn;
     if (wp.patch) {
         PatchGeom pg = make_patch(in, Nb, Ci, Hi, Wi, Gp, Gq, sp, o, T);
-        const KDecode dec = make_kdecode(pg.mode == 0 ? 1 : 0, pg.Cp, T);
-        const int k_total = pg.mode == 0 ? pg.nch * T * T * kBK : T * T * pg.Cp;   // padded taps excluded
+        if (wp.tma) set_half_chunk(pg);
+        const KDecode dec = patch_kdecode(pg);
+        const int k_total = pg.mode == 0 ? patch_kstages(pg) * kBK : T * T * pg.Cp;   // padded taps excluded
         cudaError_t e = build_bimage(make_gen(dec), og.ncols, k_total, bn, img, st);
         if (e != cudaSuccess) return e;
         // workspace: [B image][channel-blocked copy (tensor-map form)][tail partial tiles]
@@ -1058,7 +1095,7 @@ size_t conv_fwd_ws(const ConvDims& d)
 {
     const S2dPlan sp = plan_fwd_s2d(d);
     if (sp.use)
-        return round_up_256(bimage_floats(d.K, sp.pg.nch * sp.T * sp.T * kBK, sp.bn) * sizeof(float)) +
+        return round_up_256(bimage_floats(d.K, patch_kstages(sp.pg) * kBK, sp.bn) * sizeof(float)) +
                blocked_bytes(sp.pg);
     const WindowPlan wp = plan_window(d.N, d.C, d.H, d.W, d.P, d.Q, d.S, -d.pad, d.R, d.K);
     return wp.img_bytes + wp.part_bytes + wp.blocked_bytes;
@@ -1089,8 +1126,8 @@ cudaError_t launch_conv_fwd(const ConvDims& d, const float* x, const float* w, c
     S2dPlan sp = plan_fwd_s2d(d);
     if (sp.use) {
         PatchGeom& pg = sp.pg;
-        const int k_total = pg.nch * sp.T * sp.T * kBK;
-        const FwdS2dFilterGen gen{w,   d.C, d.R, d.S, make_kdecode(1, pg.Cp, sp.T), FastDiv(uint32_t(sp.T)),
+        const int k_total = patch_kstages(pg) * kBK;
+        const FwdS2dFilterGen gen{w,   d.C, d.R, d.S, patch_kdecode(pg), FastDiv(uint32_t(sp.T)),
                                   FastDiv(uint32_t(d.S * d.S)), FastDiv(uint32_t(d.S))};
         float* img = static_cast<float*>(ws);
         cudaError_t e = build_bimage(gen, d.K, k_total, sp.bn, img, st);

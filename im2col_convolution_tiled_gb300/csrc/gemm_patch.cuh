@@ -58,8 +58,18 @@ struct PatchGeom {
     int Cp, lcp;       // mode 1: channels padded to Cp = 2^lcp
     int nch;           // channel chunks per tile (mode 1: 1)
     int spc;           // stages per chunk
+    // Tensor-map form with at most 16 channels in the last chunk: its stages
+    // take two taps of 16 channels each (half), spch = ceil(T*T / 2) of them
+    // instead of spc (otherwise half = 0, spch = spc).
+    int half, spch;
     int pc;            // channels one patch holds (mode 0: 32, mode 1: Ci)
     FastDiv f_gq, f_t;
+    __host__ __device__ int stages_of(int cc) const { return cc == nch - 1 ? spch : spc; }
+    // K stages of chunks [cc0, cc1), cc0 < cc1
+    __host__ __device__ int stages_range(int cc0, int cc1) const
+    {
+        return (cc1 - cc0) * spc - (cc1 == nch ? spc - spch : 0);
+    }
     // Tensor-map form (mode 0 only): the gathered tensor re-laid as
     // [Nb][Ci/32][Hi][Wi][32] (channels innermost, zero-padded to 32) and one
     // 4-D TMA box per (tile, chunk): rows [p_lo*sp + o, + rowsT), columns
@@ -280,6 +290,7 @@ __global__ void __launch_bounds__(PatchCfg<BN, DB2, STACK>::kThreads, 1) tc_patc
         const int grp = warp >> 2;
         const int tid = threadIdx.x - 128 * grp;   // 0..127: the A row this thread owns
         uint32_t u = 0;                            // chunk counter of this CTA
+        uint32_t cst = 0;                          // stage counter of this CTA
         int last_issued = -1;
         bool ok = true;
         const uint32_t tbase = tmem_base + (uint32_t((warp & 3) * 32) << 16);
@@ -303,15 +314,41 @@ __global__ void __launch_bounds__(PatchCfg<BN, DB2, STACK>::kThreads, 1) tc_patc
                 const long long x0 = (long long)q.n * g.CiHiWi + (long long)(cc * 32) * g.HiWi + (long long)q.h_lo * g.Wi;
                 const float* pbuf = patch[pb] + (TMA ? 0 : int(x0 & 3));
                 if (!mbar_wait_warp(&ctl->pfull[pb], (u >> 1) & 1u, abort_flag)) { ok = false; break; }
-                const uint32_t c_first = u * uint32_t(g.spc);
+                const uint32_t c_first = cst;   // CTA-wide counter of the chunk's first stage
+                const int nst = g.stages_of(cc);
+                cst += uint32_t(nst);
+                const bool halfc = TMA && g.half && cc == g.nch - 1;
                 const int j0 = int((uint32_t(grp) + 2u - (c_first & 1u)) & 1u);   // first stage of this group
-                for (int j = j0; j < g.spc; j += 2) {
+                for (int j = j0; j < nst; j += 2) {
                     const uint32_t c = c_first + uint32_t(j);
                     const int slot = int(c % uint32_t(S));
                     const uint32_t phase = (c / uint32_t(S)) & 1u;
                     const int ks = cc * g.spc + j;
                     float va[32];
-                    if constexpr (TMA) {
+                    if (halfc) {
+                        // taps 2j and 2j + 1, channels 0..15 of the chunk each
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int tap = 2 * j + h;
+                            if (tap < g.T * g.T) {
+                                uint32_t tr, tq;
+                                g.f_t.divmod(uint32_t(tap), tr, tq);
+                                const int P = tpix0 + int(tr) * g.Wt + int(tq);
+                                const uint8_t* rowp = reinterpret_cast<const uint8_t*>(pbuf) + size_t(P) * 128;
+#pragma unroll
+                                for (int c4 = 0; c4 < 4; ++c4) {
+                                    const float4 v = *reinterpret_cast<const float4*>(rowp + ((c4 ^ (P & 7)) << 4));
+                                    va[16 * h + 4 * c4] = v.x;
+                                    va[16 * h + 4 * c4 + 1] = v.y;
+                                    va[16 * h + 4 * c4 + 2] = v.z;
+                                    va[16 * h + 4 * c4 + 3] = v.w;
+                                }
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) va[16 * h + i] = 0.f;
+                            }
+                        }
+                    } else if constexpr (TMA) {
                         uint32_t tr, tq;
                         g.f_t.divmod(uint32_t(j), tr, tq);
                         const int P = tpix0 + int(tr) * g.Wt + int(tq);
@@ -447,7 +484,7 @@ __global__ void __launch_bounds__(PatchCfg<BN, DB2, STACK>::kThreads, 1) tc_patc
             uint32_t c0 = 0;   // CTA-wide counter of the unit's first stage
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
                 const PatchUnit un = prob.unit(t);
-                const uint32_t k_stages = uint32_t((un.cc1 - un.cc0) * g.spc);
+                const uint32_t k_stages = uint32_t(g.stages_range(un.cc0, un.cc1));
                 const int buf = local % DB;
                 const uint32_t acc_phase = uint32_t(local / DB) & 1u;
                 if (!mbar_wait(&ctl->acce[buf], acc_phase ^ 1, abort_flag)) { ok = false; break; }
@@ -506,7 +543,7 @@ __global__ void __launch_bounds__(PatchCfg<BN, DB2, STACK>::kThreads, 1) tc_patc
         bool ok = true;
         for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
             const PatchUnit un = prob.unit(t);
-            const uint32_t k_stages = uint32_t((un.cc1 - un.cc0) * g.spc);
+            const uint32_t k_stages = uint32_t(g.stages_range(un.cc0, un.cc1));
             const int buf = local % DB;
             const uint32_t acc_phase = uint32_t(local / DB) & 1u;
             if (!mbar_wait_warp(&ctl->accf[buf], acc_phase, abort_flag)) { ok = false; break; }

@@ -107,6 +107,9 @@ CONV_SHAPES = [
     (80, 96, 16, 16, 64, 3, 1, 1),
     # input gradient with 5 chunks of dy on 32 columns: the trailing tiles split into five pieces
     (80, 32, 16, 16, 160, 3, 1, 1),
+    # 40 channels: a last chunk of 8 channels whose stages take two taps each (forward), split from the full
+    # chunk in the trailing tiles (pieces of 9 and 5 stages)
+    (80, 40, 16, 16, 64, 3, 1, 1),
 ]
 
 
