@@ -46,6 +46,8 @@ template <class Gen>
 __global__ void __launch_bounds__(kBimageThreads) build_bimage_kernel(Gen gen, int n_rows, int k_total, int bn,
                                                                       int k_stages, float* img, float* rowsum)
 {
+    griddep_wait();
+    griddep_launch();
     const int row = blockIdx.y;
     const int chunks = k_stages * (kBK / 4);
     const int nt = row / bn, r = row % bn;
@@ -94,7 +96,9 @@ cudaError_t build_bimage(const Gen& gen, int n_rows, int k_total, int bn, float*
     const int n_tiles = (n_rows + bn - 1) / bn;
     const int k_stages = (k_total + kBK - 1) / kBK;
     dim3 grid(bimage_grid_x(k_total), n_tiles * bn);
-    build_bimage_kernel<Gen><<<grid, kBimageThreads, 0, st>>>(gen, n_rows, k_total, bn, k_stages, img, rowsum);
+    cudaError_t le = launch_pdl(build_bimage_kernel<Gen>, grid, dim3(kBimageThreads), 0, st, gen, n_rows, k_total, bn,
+                                k_stages, img, rowsum);
+    if (le != cudaSuccess) return le;
     note_launch();
     return cudaGetLastError();
 }
@@ -126,6 +130,8 @@ __global__ void __launch_bounds__(kS2dGatherThreads)
     s2d_gather_kernel(const float* __restrict__ x, float* __restrict__ dst, int C, int H, int W, int S, int pad,
                       int Cs, long long total, FastDiv f_ws, FastDiv f_hs, FastDiv f_mid, FastDiv f_s, FastDiv f_ss)
 {
+    griddep_wait();
+    griddep_launch();
     const long long t = (long long)blockIdx.x * kS2dGatherThreads + threadIdx.x;
     if (t >= total) return;
     if constexpr (BLOCKED) {
@@ -193,9 +199,10 @@ cudaError_t launch_s2d_copy(const float* x, float* dst, int N, int C, int H, int
     const int Cs = C * S * S, Cb = (Cs + 31) / 32;
     const long long total = BLOCKED ? (long long)N * Cb * Hs * Ws * 8 : (long long)N * C * S * Hs * Ws;
     const unsigned blocks = unsigned((total + kS2dGatherThreads - 1) / kS2dGatherThreads);
-    s2d_gather_kernel<BLOCKED><<<blocks, kS2dGatherThreads, 0, st>>>(
-        x, dst, C, H, W, S, pad, Cs, total, FastDiv(uint32_t(Ws)), FastDiv(uint32_t(Hs)),
-        FastDiv(uint32_t(BLOCKED ? Cb : C)), FastDiv(uint32_t(S)), FastDiv(uint32_t(S * S)));
+    cudaError_t le = launch_pdl(s2d_gather_kernel<BLOCKED>, dim3(blocks), dim3(kS2dGatherThreads), 0, st, x, dst, C,
+                                H, W, S, pad, Cs, total, FastDiv(uint32_t(Ws)), FastDiv(uint32_t(Hs)),
+                                FastDiv(uint32_t(BLOCKED ? Cb : C)), FastDiv(uint32_t(S)), FastDiv(uint32_t(S * S)));
+    if (le != cudaSuccess) return le;
     note_launch();
     return cudaGetLastError();
 }

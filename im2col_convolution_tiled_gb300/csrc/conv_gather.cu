@@ -598,6 +598,8 @@ constexpr int kTailThreads = 1024;
 template <class Prob, int BN>
 __global__ void __launch_bounds__(kTailThreads) tail_reduce_kernel(const __grid_constant__ Prob prob)
 {
+    griddep_wait();
+    griddep_launch();
     __shared__ float sums[kBM][33];
     const int u0 = blockIdx.x * prob.tail_split;
     const int c0 = blockIdx.y * 32;
@@ -661,8 +663,9 @@ static cudaError_t run_gather(const GatherGeom& g, const OutGeom& o, float* img,
     const int units = tp.full_units + tp.tail_tiles * tp.split;
     cudaError_t e = launch_tc_gemm<ConvGatherProb<BN>, BN>(p, units, device_error_word(), st);
     if (e != cudaSuccess || tp.tail_tiles == 0) return e;
-    tail_reduce_kernel<ConvGatherProb<BN>, BN>
-        <<<dim3(unsigned(tp.tail_tiles), unsigned(BN / 32)), kTailThreads, 0, st>>>(p);
+    e = launch_pdl(tail_reduce_kernel<ConvGatherProb<BN>, BN>, dim3(unsigned(tp.tail_tiles), unsigned(BN / 32)),
+                   dim3(kTailThreads), 0, st, p);
+    if (e != cudaSuccess) return e;
     note_launch();
     return cudaGetLastError();
 }
@@ -813,8 +816,9 @@ static cudaError_t run_patch(const PatchGeom& pg, const OutGeom& o, float* img, 
     else
         e = launch_tc_patch<ConvPatchProb<BN>, BN, TMA, false>(p, units, device_error_word(), st, true);
     if (e != cudaSuccess || tp.tail_tiles == 0) return e;
-    tail_reduce_kernel<ConvPatchProb<BN>, BN>
-        <<<dim3(unsigned(tp.tail_tiles), unsigned(BN / 32)), kTailThreads, 0, st>>>(p);
+    e = launch_pdl(tail_reduce_kernel<ConvPatchProb<BN>, BN>, dim3(unsigned(tp.tail_tiles), unsigned(BN / 32)),
+                   dim3(kTailThreads), 0, st, p);
+    if (e != cudaSuccess) return e;
     note_launch();
     return cudaGetLastError();
 }
@@ -877,6 +881,8 @@ constexpr int kBlkRows = 4;
 __global__ void __launch_bounds__(256, 4) to_blocked32_kernel(const float* __restrict__ src, float* __restrict__ dst,
                                                            int C, int Cb, int H, int W, int hgroups)
 {
+    griddep_wait();
+    griddep_launch();
     __shared__ float tile[kBlkRows][32][33];
     const int hg = blockIdx.x % hgroups;
     const int ncb = blockIdx.x / hgroups;   // n * Cb + cb
@@ -953,10 +959,11 @@ static cudaError_t encode_patch_tmap(PatchGeom& pg, float* blocked)
 static cudaError_t setup_patch_tma(PatchGeom& pg, float* blocked, cudaStream_t st)
 {
     const int hgroups = (pg.Hi + kBlkRows - 1) / kBlkRows;
-    to_blocked32_kernel<<<unsigned(pg.Nb * pg.Cb * hgroups), 256, 0, st>>>(pg.in, blocked, pg.Ci, pg.Cb, pg.Hi, pg.Wi,
-                                                                         hgroups);
+    cudaError_t e = launch_pdl(to_blocked32_kernel, dim3(unsigned(pg.Nb * pg.Cb * hgroups)), dim3(256), 0, st, pg.in,
+                               blocked, pg.Ci, pg.Cb, pg.Hi, pg.Wi, hgroups);
+    if (e != cudaSuccess) return e;
     note_launch();
-    cudaError_t e = cudaGetLastError();
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return encode_patch_tmap(pg, blocked);
 }

@@ -177,6 +177,8 @@ struct GradGen {
 // (deterministic).
 __global__ void rowsum_final_kernel(const float* __restrict__ rowsum, int blocks, int rows, float* __restrict__ out)
 {
+    griddep_wait();
+    griddep_launch();
     const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;   // whole warps leave together
@@ -191,6 +193,8 @@ __global__ void rowsum_final_kernel(const float* __restrict__ rowsum, int blocks
 // dW[i] = sum over split s (ascending) of part[s][i].
 __global__ void wgrad_reduce_kernel(const float* __restrict__ part, int splits, long long count, float* __restrict__ dw)
 {
+    griddep_wait();
+    griddep_launch();
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < count;
          i += (long long)gridDim.x * blockDim.x) {
         float acc = 0.f;
@@ -347,7 +351,8 @@ static cudaError_t run_wgrad(const ConvDims& d, const WgradPlan& pl, const float
                                  db ? rowsum : nullptr);
     if (e != cudaSuccess) return e;
     if (db) {
-        rowsum_final_kernel<<<(d.K + 7) / 8, 256, 0, st>>>(rowsum, bimage_grid_x(p.NPQ), d.K, db);
+        e = launch_pdl(rowsum_final_kernel, dim3((d.K + 7) / 8), dim3(256), 0, st, rowsum, bimage_grid_x(p.NPQ), d.K, db);
+        if (e != cudaSuccess) return e;
         note_launch();
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
@@ -357,7 +362,8 @@ static cudaError_t run_wgrad(const ConvDims& d, const WgradPlan& pl, const float
     const long long count = (long long)d.K * p.CRS;
     long long blocks = (count + 255) / 256;
     if (blocks > 8LL * sm_count()) blocks = 8LL * sm_count();
-    wgrad_reduce_kernel<<<int(blocks), 256, 0, st>>>(part, pl.splits, count, dw);
+    e = launch_pdl(wgrad_reduce_kernel, dim3(unsigned(blocks)), dim3(256), 0, st, part, pl.splits, count, dw);
+    if (e != cudaSuccess) return e;
     note_launch();
     return cudaGetLastError();
 }

@@ -254,6 +254,9 @@ __global__ void __launch_bounds__(PatchCfg<BN, DB2, STACK>::kThreads, 1) tc_patc
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
+    // set-up above overlaps the previous kernel when launched with PDL
+    griddep_wait();
+    griddep_launch();
 
     const int num_tiles = prob.num_tiles();
     // TERMS == 3: hi*hi + hi*lo + lo*hi (fp32-faithful); TERMS == 1: hi*hi only
@@ -610,7 +613,9 @@ cudaError_t launch_tc_patch_terms(const Prob& prob, int num_tiles, int* err_word
     if (num_tiles <= 0) return cudaSuccess;
     const size_t smem = TMA ? patch_tma_smem<BN, DB2, STACK>(prob.pg.tbytes) : Cfg::kSmemBytes;
     int grid = num_tiles < sm_count() ? num_tiles : sm_count();
-    tc_patch_kernel<Prob, BN, TMA, DB2, TERMS, STACK><<<grid, Cfg::kThreads, smem, stream>>>(prob, err_word);
+    cudaError_t e = launch_pdl(tc_patch_kernel<Prob, BN, TMA, DB2, TERMS, STACK>, dim3(grid), dim3(Cfg::kThreads), smem,
+                               stream, prob, err_word);
+    if (e != cudaSuccess) return e;
     note_launch();
     return cudaGetLastError();
 }

@@ -201,6 +201,9 @@ __global__ void __launch_bounds__(EngineRoles<Prob, BN>::R::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
+    // set-up above overlaps the previous kernel when launched with PDL
+    griddep_wait();
+    griddep_launch();
 
     const int num_tiles = prob.num_tiles();
     // TERMS == 3: hi*hi + hi*lo + lo*hi (fp32-faithful); TERMS == 1: hi*hi only
@@ -461,7 +464,9 @@ cudaError_t launch_tc_gemm_terms(const Prob& prob, int num_tiles, int* err_word,
     }
     if (num_tiles <= 0) return cudaSuccess;
     int grid = num_tiles < sm_count() ? num_tiles : sm_count();
-    tc_gemm_kernel<Prob, BN, TERMS><<<grid, kThreads, Cfg::kSmemBytes, stream>>>(prob, err_word);
+    cudaError_t e = launch_pdl(tc_gemm_kernel<Prob, BN, TERMS>, dim3(grid), dim3(kThreads), Cfg::kSmemBytes, stream, prob,
+                               err_word);
+    if (e != cudaSuccess) return e;
     note_launch();
     return cudaGetLastError();
 }

@@ -3,6 +3,7 @@
 // the proxy/ordering fences that go with them.
 #pragma once
 #include <cstdint>
+#include <utility>
 
 #include "conv_b200_internal.h"
 
@@ -379,4 +380,34 @@ __device__ __forceinline__ void store_split_chunk(uint32_t hi_tile, uint32_t lo_
 
 __device__ __forceinline__ int lane_id() { return threadIdx.x & 31; }
 
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  A kernel launched with launch_pdl may start
+// while the kernel before it in the stream is still running: it must call
+// griddep_wait() -- in every CTA, before touching memory that kernel writes --
+// which returns once that kernel has completed and its writes are visible.
+// griddep_launch() lets the next PDL-launched kernel start early.  Both are
+// no-ops for a kernel launched the ordinary way.  Every kernel that calls
+// griddep_wait() does so unconditionally at its start, so its completion
+// implies its predecessor's: the ordering stays transitive along a chain.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 }  // namespace cb200
+
