@@ -808,6 +808,8 @@ __global__ void __launch_bounds__(kWalkThreads) maxpool_fwd_walk_kernel(
     int seglen, FastDiv f_q, FastDiv f_seg, int items)
 {
     static_assert(S <= K && K <= 2 * S, "walker covers windows at most two strides wide");
+    griddep_wait();
+    griddep_launch();
     const int t = int(blockIdx.x) * kWalkThreads + int(threadIdx.x);
     if (t >= items) return;
     uint32_t rest, ow, plane, seg;
@@ -898,6 +900,8 @@ __global__ void __launch_bounds__(kWalkThreads) maxpool_bwd_walk_kernel(
     int Q, int BH, int seglen, FastDiv f_bw, FastDiv f_seg, int items)
 {
     static_assert(S <= K && K <= 2 * S, "walker covers windows at most two strides wide");
+    griddep_wait();
+    griddep_launch();
     constexpr int KC = K - S > 0 ? K - S : 1;   // carried rows (at least one slot)
     const int t = int(blockIdx.x) * kWalkThreads + int(threadIdx.x);
     if (t >= items) return;
@@ -1022,8 +1026,10 @@ static cudaError_t launch_pool_fwd_walk(int NC, int H, int W, int P, int Q, cons
     const int seglen = walk_seglen(P, (long long)NC * Q);
     const int nseg = (P + seglen - 1) / seglen;
     const long long items = (long long)NC * nseg * Q;
-    maxpool_fwd_walk_kernel<K, S><<<unsigned((items + kWalkThreads - 1) / kWalkThreads), kWalkThreads, 0, st>>>(
-        x, y, idx, H, W, P, Q, seglen, FastDiv(uint32_t(Q)), FastDiv(uint32_t(nseg)), int(items));
+    cudaError_t e = launch_pdl(maxpool_fwd_walk_kernel<K, S>, dim3(unsigned((items + kWalkThreads - 1) / kWalkThreads)),
+                               dim3(kWalkThreads), 0, st, x, y, idx, H, W, P, Q, seglen, FastDiv(uint32_t(Q)),
+                               FastDiv(uint32_t(nseg)), int(items));
+    if (e != cudaSuccess) return e;
     note_launch();
     return cudaGetLastError();
 }
@@ -1036,8 +1042,10 @@ static cudaError_t launch_pool_bwd_walk(int NC, int H, int W, int P, int Q, cons
     const int seglen = walk_seglen(BH, (long long)NC * BW);
     const int nseg = (BH + seglen - 1) / seglen;
     const long long items = (long long)NC * nseg * BW;
-    maxpool_bwd_walk_kernel<K, S><<<unsigned((items + kWalkThreads - 1) / kWalkThreads), kWalkThreads, 0, st>>>(
-        dy, idx, dx, H, W, P, Q, BH, seglen, FastDiv(uint32_t(BW)), FastDiv(uint32_t(nseg)), int(items));
+    cudaError_t e = launch_pdl(maxpool_bwd_walk_kernel<K, S>, dim3(unsigned((items + kWalkThreads - 1) / kWalkThreads)),
+                               dim3(kWalkThreads), 0, st, dy, idx, dx, H, W, P, Q, BH, seglen, FastDiv(uint32_t(BW)),
+                               FastDiv(uint32_t(nseg)), int(items));
+    if (e != cudaSuccess) return e;
     note_launch();
     return cudaGetLastError();
 }
@@ -1153,6 +1161,8 @@ __device__ __forceinline__ float sgd_one(float p, float g, float lr, float clip)
 __global__ void sgd_kernel(float* __restrict__ p, const float* __restrict__ g, long long n4, long long count, float lr,
                            float clip)
 {
+    griddep_wait();
+    griddep_launch();
     const long long stride = (long long)gridDim.x * blockDim.x;
     const long long tid = blockIdx.x * (long long)blockDim.x + threadIdx.x;
     for (long long i = tid; i < n4; i += stride) {
@@ -1171,7 +1181,9 @@ cudaError_t launch_sgd(int64_t count, float lr, float clip, float* p, const floa
 {
     if (count == 0) return cudaSuccess;
     const long long n4 = count / 4;
-    sgd_kernel<<<grid_for(n4 > 0 ? n4 : 1, 256), 256, 0, st>>>(p, g, n4, count, lr, clip);
+    cudaError_t e = launch_pdl(sgd_kernel, dim3(grid_for(n4 > 0 ? n4 : 1, 256)), dim3(256), 0, st, p, g, n4, count, lr,
+                               clip);
+    if (e != cudaSuccess) return e;
     note_launch();
     return cudaGetLastError();
 }
