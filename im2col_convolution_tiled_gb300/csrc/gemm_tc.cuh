@@ -111,7 +111,11 @@ struct Groups {
 //   RowFast:   thread t owns row t of a 128-row block; v[i] is k = ks*32 + i.
 //   ChunkFast: thread t owns 16-byte chunk (t % 8) of rows (t / 8) + 16 p,
 //              p = 0..7; v[4p + e] is k = ks*32 + 4 (t % 8) + e.
-enum class Map { RowFast, ChunkFast };
+//   QuadRow:   thread t owns rows 4 (t / 4) + j, j = 0..3, and K values
+//              8 (t % 4) + kk, kk = 0..7: v[4 kk + j] is (row 4 (t / 4) + j,
+//              k = ks*32 + 8 (t % 4) + kk).  For an operand stored with the
+//              ROWS contiguous: one 16-byte load covers four rows of one k.
+enum class Map { RowFast, ChunkFast, QuadRow };
 
 template <Map M>
 __device__ __forceinline__ void store_slice(uint32_t hi_tile, uint32_t lo_tile, int row_base, int rows, int tid,
@@ -125,7 +129,7 @@ __device__ __forceinline__ void store_slice(uint32_t hi_tile, uint32_t lo_tile, 
                 store_split_chunk(hi_tile, lo_tile, row, c, v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3],
                                   with_lo);
         }
-    } else {
+    } else if constexpr (M == Map::ChunkFast) {
         int chunk = tid & 7;
 #pragma unroll
         for (int p = 0; p < 8; ++p) {
@@ -133,6 +137,29 @@ __device__ __forceinline__ void store_slice(uint32_t hi_tile, uint32_t lo_tile, 
             if (r < rows)
                 store_split_chunk(hi_tile, lo_tile, row_base + r, chunk, v[4 * p], v[4 * p + 1], v[4 * p + 2],
                                   v[4 * p + 3], with_lo);
+        }
+    } else {
+        // Thread t writes chunks 2 (t % 4) and 2 (t % 4) + 1 of its four rows,
+        // odd quads of lanes the two chunks in the other order: a quarter-warp
+        // then covers all eight 16-byte bank groups of the swizzled rows.
+        const int kg = tid & 3, rq = tid >> 2;
+        const bool swap = (rq & 1) != 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int r = 4 * rq + j;
+            if (r < rows) {
+#pragma unroll
+                for (int s = 0; s < 2; ++s) {
+                    float a[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float first = v[4 * (4 * s + e) + j], second = v[4 * (4 * (1 - s) + e) + j];
+                        a[e] = swap ? second : first;
+                    }
+                    const int h = swap ? 1 - s : s;
+                    store_split_chunk(hi_tile, lo_tile, row_base + r, 2 * kg + h, a[0], a[1], a[2], a[3], with_lo);
+                }
+            }
         }
     }
 }

@@ -3,11 +3,11 @@
 // row-major, flags bit 0 = A stored K x M, bit 1 = B stored N x K.
 //
 // Mapped onto the tcgen05 GEMM with A rows = rows of C and B rows = columns of
-// C.  The gathers read each operand in the order that keeps a warp's loads
-// contiguous: a K-contiguous operand is read 16 bytes per thread along K
-// (ChunkFast), an M/N-contiguous one 4 bytes per thread along M/N (RowFast).
-// Either way the producer writes K-major swizzled hi/lo tiles, so all four flag
-// combinations feed the same MMA.
+// C.  The gathers keep a warp's loads contiguous: a K-contiguous operand is
+// read 16 bytes per thread along K (ChunkFast); A stored K x M 16 bytes per
+// thread along M, four rows of one k (QuadRow); B stored K x N 4 bytes per
+// thread along N (RowFast).  Either way the producer writes K-major swizzled
+// hi/lo tiles, so all four flag combinations feed the same MMA.
 #include "gemm_tc.cuh"
 
 namespace cb200 {
@@ -17,7 +17,9 @@ struct MatmulProb {
     static constexpr bool kBBulk = false;
     int terms = 3;   // tensor-core products per K step: 3 (3xTF32) or 1 (TF32)
     static constexpr int kGroups = 2;
-    static constexpr Map kAMap = (FLAGS & 1u) ? Map::RowFast : Map::ChunkFast;
+    static constexpr Map kAMap = (FLAGS & 1u) ? Map::QuadRow : Map::ChunkFast;
+    // B stored K x N stays one row per thread: measured faster than QuadRow
+    // for it (flag 0: 0.69 vs 0.61 of the roofline on 9216 x 9216 x 4096)
     static constexpr Map kBMap = (FLAGS & 2u) ? Map::ChunkFast : Map::RowFast;
 
     const float* A;
@@ -26,6 +28,7 @@ struct MatmulProb {
     int M, K, N;
     int m_tiles, n_tiles, k_stages;
     int vec_a, vec_b, vec_c;   // 16-byte accesses allowed along K (A, B) / along N (C)
+    int vec_am;                // 16-byte accesses allowed along M (A stored K x M)
 
     __device__ int num_tiles() const { return m_tiles * n_tiles; }
 
@@ -52,6 +55,27 @@ struct MatmulProb {
         }
     }
 
+    // QuadRow gather of an operand stored K x R (rows contiguous): rows
+    // r0 + 4 (tid / 4) + j, K values k0 + 8 (tid % 4) + kk (zero past R or K).
+    __device__ __forceinline__ static void load_quad(const float* X, int R, int K, bool vec, int r0, int k0, int tid,
+                                                     float (&v)[32])
+    {
+        const int r = r0 + 4 * (tid >> 2);
+        const int kb = k0 + 8 * (tid & 3);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const int k = kb + kk;
+            const float* src = X + size_t(k) * R + r;
+            if (k < K && vec && r + 3 < R) {
+                const float4 f = __ldg(reinterpret_cast<const float4*>(src));
+                v[4 * kk] = f.x; v[4 * kk + 1] = f.y; v[4 * kk + 2] = f.z; v[4 * kk + 3] = f.w;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) v[4 * kk + j] = (k < K && r + j < R) ? __ldg(src + j) : 0.f;
+            }
+        }
+    }
+
     struct AState {};
     __device__ AState a_setup(const Tile&, int) const { return {}; }
 
@@ -59,13 +83,7 @@ struct MatmulProb {
     {
         const int k0 = ks * kBK;
         if constexpr (FLAGS & 1u) {   // A stored K x M: (m, k) at k*M + m
-            const int m = tl.m0 + tid;
-            const bool mv = m < M;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int k = k0 + i;
-                v[i] = (mv && k < K) ? __ldg(A + size_t(k) * M + m) : 0.f;
-            }
+            load_quad(A, M, K, vec_am != 0, tl.m0, k0, tid, v);
         } else {                      // A stored M x K: (m, k) at m*K + k
             const int kc = k0 + 4 * (tid & 7);
 #pragma unroll
@@ -156,6 +174,7 @@ static cudaError_t run_matmul(int M, int K, int N, const float* A, const float* 
     p.vec_a = (K % 4 == 0) && aligned16(A);
     p.vec_b = (K % 4 == 0) && aligned16(B);
     p.vec_c = (N % 4 == 0) && aligned16(C);
+    p.vec_am = (M % 4 == 0) && aligned16(A);
     return launch_tc_gemm<MatmulProb<FLAGS, BN>, BN>(p, p.m_tiles * p.n_tiles, device_error_word(), st);
 }
 
