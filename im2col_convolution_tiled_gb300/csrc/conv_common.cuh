@@ -192,11 +192,98 @@ __global__ void __launch_bounds__(kS2dGatherThreads)
     }
 }
 
+// The same copy for S = 4, W % 4 == 0 and x 16-byte aligned: the four inputs
+// of a (c, a, hh, ww) row segment, x[n, c, 4hh + a - pad, 4ww - pad .. + 3],
+// lie in two aligned float4 of the row (each wholly inside or outside the
+// image, since W % 4 == 0), at offset OFF = (-pad) mod 4 -- the same for every
+// thread, so it is a template parameter.  Lanes run along ww: each load
+// instruction reads 512 contiguous bytes.
+//   BLOCKED: thread t = ((n*Cb + cb)*Hs + hh)*Ws + ww writes the whole 128-byte
+//            pixel of chunk cb (eight (c, a) segments of four channels b).
+//   NCHW:    thread t = (((n*C + c)*4 + a)*Hs + hh)*Ws + ww writes its segment
+//            to the four planes b.
+template <int OFF>
+__device__ __forceinline__ float4 s2d_segment(const float* __restrict__ rowp, int a0, int W)
+{
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 lo = unsigned(a0) < unsigned(W) ? __ldg(reinterpret_cast<const float4*>(rowp + a0)) : z;
+    if constexpr (OFF == 0) return lo;
+    const float4 hi = unsigned(a0 + 4) < unsigned(W) ? __ldg(reinterpret_cast<const float4*>(rowp + a0 + 4)) : z;
+    if constexpr (OFF == 1) return make_float4(lo.y, lo.z, lo.w, hi.x);
+    if constexpr (OFF == 2) return make_float4(lo.z, lo.w, hi.x, hi.y);
+    return make_float4(lo.w, hi.x, hi.y, hi.z);
+}
+
+template <bool BLOCKED, int OFF>
+__global__ void __launch_bounds__(kS2dGatherThreads)
+    s2d_gather4_kernel(const float* __restrict__ x, float* __restrict__ dst, int C, int H, int W, int pad, int Cs,
+                       long long total, FastDiv f_ws, FastDiv f_hs, FastDiv f_mid)
+{
+    griddep_wait();
+    griddep_launch();
+    const long long t = (long long)blockIdx.x * kS2dGatherThreads + threadIdx.x;
+    if (t >= total) return;
+    const int Hs = int(f_hs.d), Ws = int(f_ws.d);
+    if constexpr (BLOCKED) {
+        uint32_t r, ww, hh, cb, n;
+        f_ws.divmod(uint32_t(t), r, ww);
+        f_hs.divmod(r, r, hh);
+        f_mid.divmod(r, n, cb);
+        const int a0 = 4 * int(ww) - pad - OFF;   // aligned start of the segment's first float4
+        float4 out[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int cp0 = int(cb) * 32 + 4 * j;   // channels cp0 .. cp0 + 3: b = 0..3 of one (c, a)
+            const int c = cp0 >> 4, a = (cp0 >> 2) & 3;
+            const int h = 4 * int(hh) + a - pad;
+            out[j] = (cp0 < Cs && unsigned(h) < unsigned(H))
+                         ? s2d_segment<OFF>(x + ((size_t(n) * C + c) * H + h) * W, a0, W)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        float4* d = reinterpret_cast<float4*>(dst) + size_t(t) * 8;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) d[j] = out[j];
+    } else {
+        uint32_t r, ww, hh, a, c, n;
+        f_ws.divmod(uint32_t(t), r, ww);
+        f_hs.divmod(r, r, hh);
+        a = r & 3u;
+        r >>= 2;
+        f_mid.divmod(r, n, c);
+        const int h = 4 * int(hh) + int(a) - pad;
+        const float4 v = unsigned(h) < unsigned(H)
+                             ? s2d_segment<OFF>(x + ((size_t(n) * C + c) * H + h) * W, 4 * int(ww) - pad - OFF, W)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        float* out = dst + ((size_t(n) * Cs + (int(c) * 4 + int(a)) * 4) * Hs + hh) * Ws + ww;
+        const size_t plane = size_t(Hs) * Ws;
+        out[0] = v.x;
+        out[plane] = v.y;
+        out[2 * plane] = v.z;
+        out[3 * plane] = v.w;
+    }
+}
+
 template <bool BLOCKED>
 cudaError_t launch_s2d_copy(const float* x, float* dst, int N, int C, int H, int W, int S, int pad, int Hs, int Ws,
                             cudaStream_t st)
 {
     const int Cs = C * S * S, Cb = (Cs + 31) / 32;
+    if (S == 4 && W % 4 == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0) {
+        const long long total4 = BLOCKED ? (long long)N * Cb * Hs * Ws : (long long)N * C * 4 * Hs * Ws;
+        const unsigned blocks4 = unsigned((total4 + kS2dGatherThreads - 1) / kS2dGatherThreads);
+        const int off = ((-pad) % 4 + 4) % 4;
+        auto run = [&](auto kern) {
+            return launch_pdl(kern, dim3(blocks4), dim3(kS2dGatherThreads), 0, st, x, dst, C, H, W, pad, Cs, total4,
+                              FastDiv(uint32_t(Ws)), FastDiv(uint32_t(Hs)), FastDiv(uint32_t(BLOCKED ? Cb : C)));
+        };
+        cudaError_t le = off == 0   ? run(s2d_gather4_kernel<BLOCKED, 0>)
+                         : off == 1 ? run(s2d_gather4_kernel<BLOCKED, 1>)
+                         : off == 2 ? run(s2d_gather4_kernel<BLOCKED, 2>)
+                                    : run(s2d_gather4_kernel<BLOCKED, 3>);
+        if (le != cudaSuccess) return le;
+        note_launch();
+        return cudaGetLastError();
+    }
     const long long total = BLOCKED ? (long long)N * Cb * Hs * Ws * 8 : (long long)N * C * S * Hs * Ws;
     const unsigned blocks = unsigned((total + kS2dGatherThreads - 1) / kS2dGatherThreads);
     cudaError_t le = launch_pdl(s2d_gather_kernel<BLOCKED>, dim3(blocks), dim3(kS2dGatherThreads), 0, st, x, dst, C,

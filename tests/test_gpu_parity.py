@@ -102,6 +102,7 @@ CONV_SHAPES = [
     (2, 3, 26, 30, 8, 11, 4, 2),
     (1, 4, 17, 17, 5, 7, 2, 3),
     (1, 3, 20, 20, 8, 11, 4, 6),
+    (1, 3, 24, 24, 8, 7, 4, 3),        # stride 4, pad 3: the vector space-to-depth copy at offset 1
     # 160 patch-kernel tiles: a round on 152 SMs plus 8 tiles, which are split along their channel chunks and
     # summed by the reduce kernel (forward: 3 chunks of x, 64 columns; input gradient: 2 chunks of dy, 96 columns)
     (80, 96, 16, 16, 64, 3, 1, 1),
