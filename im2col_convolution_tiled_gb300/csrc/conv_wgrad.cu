@@ -173,15 +173,12 @@ struct GradGen {
 };
 
 // out[row] = sum of rowsum[row * blocks + i] over the blocks i: one warp per
-// row, lane l adding blocks l, l + 32, ... in order, then a fixed shuffle tree
-// (deterministic).
-__global__ void rowsum_final_kernel(const float* __restrict__ rowsum, int blocks, int rows, float* __restrict__ out)
+// row (warp `wid` of the grid), lane l adding blocks l, l + 32, ... in order,
+// then a fixed shuffle tree (deterministic).
+__device__ __forceinline__ void rowsum_final_warp(const float* __restrict__ rowsum, int blocks, int row,
+                                                  float* __restrict__ out)
 {
-    griddep_wait();
-    griddep_launch();
-    const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (row >= rows) return;   // whole warps leave together
     const float* src = rowsum + size_t(row) * blocks;
     float acc = 0.f;
     for (int i = lane; i < blocks; i += 32) acc += __ldg(src + i);
@@ -190,11 +187,28 @@ __global__ void rowsum_final_kernel(const float* __restrict__ rowsum, int blocks
     if (lane == 0) out[row] = acc;
 }
 
-// dW[i] = sum over split s (ascending) of part[s][i].
-__global__ void wgrad_reduce_kernel(const float* __restrict__ part, int splits, long long count, float* __restrict__ dw)
+__global__ void rowsum_final_kernel(const float* __restrict__ rowsum, int blocks, int rows, float* __restrict__ out)
 {
     griddep_wait();
     griddep_launch();
+    const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (row >= rows) return;   // whole warps leave together
+    rowsum_final_warp(rowsum, blocks, row, out);
+}
+
+// dW[i] = sum over split s (ascending) of part[s][i].  With db non-null the
+// grid's first warps also finish the bias gradient (rowsum_final's work, one
+// warp per filter row), saving that launch.
+__global__ void wgrad_reduce_kernel(const float* __restrict__ part, int splits, long long count, float* __restrict__ dw,
+                                    const float* __restrict__ rowsum, int rs_blocks, int rows, float* __restrict__ db)
+{
+    griddep_wait();
+    griddep_launch();
+    if (db) {
+        const int wid = int(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+        const int nw = int(gridDim.x) * (blockDim.x >> 5);
+        for (int row = wid; row < rows; row += nw) rowsum_final_warp(rowsum, rs_blocks, row, db);
+    }
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < count;
          i += (long long)gridDim.x * blockDim.x) {
         float acc = 0.f;
@@ -350,7 +364,7 @@ static cudaError_t run_wgrad(const ConvDims& d, const WgradPlan& pl, const float
     cudaError_t e = build_bimage(GradGen{dy, d.K, p.PQ, FastDiv(uint32_t(p.PQ))}, d.K, p.NPQ, BN, img, st,
                                  db ? rowsum : nullptr);
     if (e != cudaSuccess) return e;
-    if (db) {
+    if (db && pl.splits == 1) {   // with split partials the reduce kernel finishes db
         e = launch_pdl(rowsum_final_kernel, dim3((d.K + 7) / 8), dim3(256), 0, st, rowsum, bimage_grid_x(p.NPQ), d.K, db);
         if (e != cudaSuccess) return e;
         note_launch();
@@ -362,7 +376,8 @@ static cudaError_t run_wgrad(const ConvDims& d, const WgradPlan& pl, const float
     const long long count = (long long)d.K * p.CRS;
     long long blocks = (count + 255) / 256;
     if (blocks > 8LL * sm_count()) blocks = 8LL * sm_count();
-    e = launch_pdl(wgrad_reduce_kernel, dim3(unsigned(blocks)), dim3(256), 0, st, part, pl.splits, count, dw);
+    e = launch_pdl(wgrad_reduce_kernel, dim3(unsigned(blocks)), dim3(256), 0, st, part, pl.splits, count, dw,
+                   static_cast<const float*>(rowsum), bimage_grid_x(p.NPQ), d.K, db);
     if (e != cudaSuccess) return e;
     note_launch();
     return cudaGetLastError();
