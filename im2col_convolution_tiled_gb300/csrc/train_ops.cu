@@ -9,7 +9,7 @@
 // is produced by one thread in a fixed order, sums use fixed shuffle trees,
 // and fp32 additions/products are explicit (__fadd_rn / __fmul_rn) so no
 // multiply-add is formed.  The element-wise kernels use 16-byte accesses.
-#include "conv_b200_internal.h"
+#include "ptx.cuh"
 
 namespace cb200 {
 
@@ -32,6 +32,8 @@ __device__ __forceinline__ float relu_grad1(float g, float x) { return __fmul_rn
 // y = max(0, x) (nn_relu); +0 for x <= 0.  y may be x (in place).
 __global__ void relu_fwd_kernel(const float* x, float* y, long long n)
 {
+    griddep_wait();
+    griddep_launch();
     const long long n4 = n / 4;
     const long long stride = (long long)gridDim.x * blockDim.x;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += stride) {
@@ -46,6 +48,8 @@ __global__ void relu_fwd_kernel(const float* x, float* y, long long n)
 // be dy (in place).
 __global__ void relu_bwd_kernel(const float* dy, const float* __restrict__ x, float* dx, long long n)
 {
+    griddep_wait();
+    griddep_launch();
     const long long n4 = n / 4;
     const long long stride = (long long)gridDim.x * blockDim.x;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += stride) {
@@ -61,6 +65,8 @@ __global__ void relu_bwd_kernel(const float* dy, const float* __restrict__ x, fl
 // acc = acc + g (nn_grad_accum), in place.
 __global__ void grad_accum_kernel(const float* __restrict__ g, float* __restrict__ acc, long long n)
 {
+    griddep_wait();
+    griddep_launch();
     const long long n4 = n / 4;
     const long long stride = (long long)gridDim.x * blockDim.x;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += stride) {
@@ -79,6 +85,8 @@ __global__ void grad_accum_kernel(const float* __restrict__ g, float* __restrict
 __global__ void add_bias_kernel(const float* A, const float* __restrict__ b, float* out, int rows,
                                 int cols, int relu)
 {
+    griddep_wait();
+    griddep_launch();
     const long long n = (long long)rows * cols;
     const long long stride = (long long)gridDim.x * blockDim.x;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += stride) {
@@ -96,6 +104,8 @@ constexpr int kBgSlices = 8;
 __global__ void __launch_bounds__(32 * kBgSlices) bias_grad_rows_kernel(const float* __restrict__ G,
                                                                        float* __restrict__ db, int rows, int cols)
 {
+    griddep_wait();
+    griddep_launch();
     __shared__ float part[kBgSlices][32];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int j = blockIdx.x * 32 + lane;
@@ -127,6 +137,8 @@ __global__ void __launch_bounds__(kCeThreads) softmax_ce_kernel(const float* __r
                                                                 float* __restrict__ loss, int rows, int cols,
                                                                 int* err)
 {
+    griddep_wait();
+    griddep_launch();
     __shared__ float warp_loss[kCeThreads / 32];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     float my_loss = 0.f;
@@ -164,21 +176,24 @@ __global__ void __launch_bounds__(kCeThreads) softmax_ce_kernel(const float* __r
 
 cudaError_t launch_relu_fwd(int64_t n, const float* x, float* y, cudaStream_t st)
 {
-    relu_fwd_kernel<<<ew_grid(n / 4 + 1), kEwThreads, 0, st>>>(x, y, n);
+    cudaError_t e = launch_pdl(relu_fwd_kernel, dim3(ew_grid(n / 4 + 1)), dim3(kEwThreads), 0, st, x, y, n);
+    if (e != cudaSuccess) return e;
     note_launch();
     return cudaGetLastError();
 }
 
 cudaError_t launch_relu_bwd(int64_t n, const float* dy, const float* x, float* dx, cudaStream_t st)
 {
-    relu_bwd_kernel<<<ew_grid(n / 4 + 1), kEwThreads, 0, st>>>(dy, x, dx, n);
+    cudaError_t e = launch_pdl(relu_bwd_kernel, dim3(ew_grid(n / 4 + 1)), dim3(kEwThreads), 0, st, dy, x, dx, n);
+    if (e != cudaSuccess) return e;
     note_launch();
     return cudaGetLastError();
 }
 
 cudaError_t launch_grad_accum(int64_t n, const float* g, float* acc, cudaStream_t st)
 {
-    grad_accum_kernel<<<ew_grid(n / 4 + 1), kEwThreads, 0, st>>>(g, acc, n);
+    cudaError_t e = launch_pdl(grad_accum_kernel, dim3(ew_grid(n / 4 + 1)), dim3(kEwThreads), 0, st, g, acc, n);
+    if (e != cudaSuccess) return e;
     note_launch();
     return cudaGetLastError();
 }
@@ -186,14 +201,18 @@ cudaError_t launch_grad_accum(int64_t n, const float* g, float* acc, cudaStream_
 cudaError_t launch_add_bias(int rows, int cols, const float* A, const float* b, float* out, int relu,
                             cudaStream_t st)
 {
-    add_bias_kernel<<<ew_grid((long long)rows * cols), kEwThreads, 0, st>>>(A, b, out, rows, cols, relu ? 1 : 0);
+    cudaError_t e = launch_pdl(add_bias_kernel, dim3(ew_grid((long long)rows * cols)), dim3(kEwThreads), 0, st, A, b, out,
+                               rows, cols, relu ? 1 : 0);
+    if (e != cudaSuccess) return e;
     note_launch();
     return cudaGetLastError();
 }
 
 cudaError_t launch_bias_grad_rows(int rows, int cols, const float* G, float* db, cudaStream_t st)
 {
-    bias_grad_rows_kernel<<<(cols + 31) / 32, 32 * kBgSlices, 0, st>>>(G, db, rows, cols);
+    cudaError_t e = launch_pdl(bias_grad_rows_kernel, dim3((cols + 31) / 32), dim3(32 * kBgSlices), 0, st, G, db, rows,
+                               cols);
+    if (e != cudaSuccess) return e;
     note_launch();
     return cudaGetLastError();
 }
@@ -201,7 +220,9 @@ cudaError_t launch_bias_grad_rows(int rows, int cols, const float* G, float* db,
 cudaError_t launch_softmax_ce(int rows, int cols, const float* z, const int32_t* labels, float* probs, float* dz,
                               float* loss, cudaStream_t st)
 {
-    softmax_ce_kernel<<<1, kCeThreads, 0, st>>>(z, labels, probs, dz, loss, rows, cols, device_error_word());
+    cudaError_t e = launch_pdl(softmax_ce_kernel, dim3(1), dim3(kCeThreads), 0, st, z, labels, probs, dz, loss, rows, cols,
+                               device_error_word());
+    if (e != cudaSuccess) return e;
     note_launch();
     return cudaGetLastError();
 }
