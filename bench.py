@@ -392,28 +392,36 @@ def run_ours(args):
             traffic = int(m.group(1))
 
     # --- end to end through the public API with host buffers ---------------
-    # Every step uploads its inputs (x, w, b, dy and the pool gradients) from
-    # pinned host memory and reads all its results back (y, dx, dw, db and the
-    # pool input gradients).  Two sets of device buffers alternate between
-    # steps, as a training loop double-buffers its batches: step i + 1's
+    # As a training loop runs it: every step uploads its batch -- each layer's
+    # input x, its upstream gradient dy and the pool gradients -- from pinned
+    # host memory, and reads the step's result back: the parameters (every
+    # filter and bias) after the SGD update, one flat buffer.  Parameters stay
+    # resident on the device between steps.  `e2e_full_readback` additionally
+    # uploads the parameters and reads every output of every call back (y, dx,
+    # dw, db, pool input gradients).  Two sets of device buffers alternate
+    # between steps, as a training loop double-buffers its batches: step i + 1's
     # uploads run on one copy stream and step i - 1's read-backs on another
     # while step i computes.  Within a step, layer i's compute waits only for
-    # layer i's uploads, and its results go back as soon as it is done.
+    # layer i's uploads.
     pin = lambda a: torch.from_numpy(a).pin_memory()
     host_in = [{k: pin(v) for k, v in b.host.items()} for b in bufs]
     host_out = [{"y": torch.empty(b.L.y_shape).pin_memory(), "dx": torch.empty(b.L.x_shape).pin_memory(),
                  "dw": torch.empty(b.L.w_shape).pin_memory(), "db": torch.empty((b.L.outC,)).pin_memory(),
                  "dxp": torch.empty(b.L.y_shape).pin_memory() if b.pool else None} for b in bufs]
-    h2d = sum(b.bytes_in() for b in bufs)
-    d2h = sum(b.bytes_out() for b in bufs)
     sets = [(store, bufs), make_set()]
+    host_params = torch.empty(store.p.shape).pin_memory()
+    batch_keys = ("x", "dy", "dyp")
+    h2d_full = sum(b.bytes_in() for b in bufs)
+    d2h_full = sum(b.bytes_out() for b in bufs)
+    h2d_batch = sum(a.nbytes for b in bufs for k, a in b.host.items() if k in batch_keys)
+    d2h_result = host_params.numel() * 4
     s_h2d, s_d2h = torch.cuda.Stream(), torch.cuda.Stream()
     ev_free_in = [torch.cuda.Event() for _ in sets]     # compute of the set's last step is done
     ev_free_out = [torch.cuda.Event() for _ in sets]    # read-back of the set's last step is done
     for e_ in ev_free_in + ev_free_out:
         e_.record(stream)
 
-    def e2e_step(i):
+    def e2e_step(i, full):
         cur_store, cur = sets[i % 2]
         ev_in = [torch.cuda.Event() for _ in cur]
         ev_out = [torch.cuda.Event() for _ in cur]
@@ -421,8 +429,9 @@ def run_ours(args):
             s_h2d.wait_event(ev_free_in[i % 2])
             for j, (b, hi) in enumerate(zip(cur, host_in)):
                 b.x.copy_(hi["x"], non_blocking=True)
-                b.w.copy_(hi["w"], non_blocking=True)
-                b.b.copy_(hi["b"], non_blocking=True)
+                if full:
+                    b.w.copy_(hi["w"], non_blocking=True)
+                    b.b.copy_(hi["b"], non_blocking=True)
                 b.dy.copy_(hi["dy"], non_blocking=True)
                 if b.pool:
                     b.dyp.copy_(hi["dyp"], non_blocking=True)
@@ -436,31 +445,37 @@ def run_ours(args):
             ev_out[j].record(stream)
             with torch.cuda.stream(s_d2h):
                 s_d2h.wait_event(ev_out[j])
-                ho = host_out[j]
-                ho["y"].copy_(b.y, non_blocking=True)
-                ho["dx"].copy_(b.dx, non_blocking=True)
-                ho["dw"].copy_(b.dw, non_blocking=True)
-                ho["db"].copy_(b.db, non_blocking=True)
-                if b.pool:
-                    ho["dxp"].copy_(b.dxp, non_blocking=True)
+                if full:
+                    ho = host_out[j]
+                    ho["y"].copy_(b.y, non_blocking=True)
+                    ho["dx"].copy_(b.dx, non_blocking=True)
+                    ho["dw"].copy_(b.dw, non_blocking=True)
+                    ho["db"].copy_(b.db, non_blocking=True)
+                    if b.pool:
+                        ho["dxp"].copy_(b.dxp, non_blocking=True)
+                elif j == len(cur) - 1:
+                    host_params.copy_(cur_store.p, non_blocking=True)
         ev_free_in[i % 2].record(stream)
         ev_free_out[i % 2].record(s_d2h)
 
-    def e2e_run(n):
+    def e2e_run(n, full):
         for i in range(n):
-            e2e_step(i)
+            e2e_step(i, full)
         s_h2d.synchronize()
         s_d2h.synchronize()
         stream.synchronize()
 
-    e2e_steps = max(3, args.steps // 4)
-    e2e_run(2)
-    barrier()
-    t0 = time.perf_counter()
-    e2e_run(e2e_steps)
-    barrier()
-    e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
-    e2e_ms = max_over_ranks(e2e_ms, dist)
+    def e2e_time(full):
+        steps = max(3, args.steps // 4)
+        e2e_run(2, full)
+        barrier()
+        t0 = time.perf_counter()
+        e2e_run(steps, full)
+        barrier()
+        return max_over_ranks((time.perf_counter() - t0) * 1e3 / steps, dist)
+
+    e2e_ms = e2e_time(False)
+    e2e_full_ms = e2e_time(True)
     cb.check()
 
     cpu = None
@@ -490,7 +505,12 @@ def run_ours(args):
         "per_layer": per_layer,
         "sgd_ms_per_step": round(avg[("step", "sgd")], 4),
         "e2e": {"value": round(job_rate(flops, e2e_ms, world) / 1e12, 3), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
+                "h2d_bytes_per_step": h2d_batch, "d2h_bytes_per_step": d2h_result, "ms_per_step": round(e2e_ms, 3),
+                "copies": "up: every layer's x and dy and the pool gradients; back: the parameters after SGD"},
+        "e2e_full_readback": {"value": round(job_rate(flops, e2e_full_ms, world) / 1e12, 3), "unit": UNIT,
+                              "h2d_bytes_per_step": h2d_full, "d2h_bytes_per_step": d2h_full,
+                              "ms_per_step": round(e2e_full_ms, 3),
+                              "copies": "up: also the parameters; back: every output of every call"},
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "cpu_baseline": cpu,
