@@ -263,17 +263,24 @@ struct ConvGatherProb {
                                    __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
             return;
         }
-        if (!e.valid) return;
         if (o.so == 1) {
+            // the 32 columns' biases: lane i loads column c0 + i once and the
+            // warp shares them (every epilogue lane calls store, valid row or not)
+            const int chl = tl.n0 + c0 + int(threadIdx.x & 31);
+            const float bl = (o.bias && chl < o.Co) ? __ldg(o.bias + chl) : 0.f;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
+                const float bias = __shfl_sync(0xffffffffu, bl, i);
                 const int ch = tl.n0 + c0 + i;
-                if (ch < o.Co) {
-                    const float v = __uint_as_float(r[i]) + (o.bias ? __ldg(o.bias + ch) : 0.f);
+                if (e.valid && ch < o.Co) {
+                    const float v = __uint_as_float(r[i]) + bias;
                     e.opix[size_t(ch) * o.HoWo] = o.relu && !(v > 0.f) ? 0.f : v;
                 }
             }
-        } else if (o.vec == 2) {
+            return;
+        }
+        if (!e.valid) return;
+        if (o.vec == 2) {
             // so = 4, oo = 2: the four phases b of one (ch, a) are output
             // columns w .. w + 3 with w = 4q - 2 (even): two 8-byte-aligned
             // pairs, the first left of the image when q = 0, the second right
