@@ -17,6 +17,12 @@
  *    reported before anything is launched.  A device-side failure (a bounded
  *    wait that gave up) is latched in a device error word and reported by the
  *    next conv_b200_check().
+ *  - Kernels are launched with programmatic stream serialization: each one
+ *    waits (griddepcontrol.wait) for the kernel before it in the stream before
+ *    touching memory, and lets the next one be scheduled early.  Stream order
+ *    is kept for everything else (events, copies, ordinary kernels); a
+ *    caller's own kernel launched the same way right after a call must itself
+ *    wait before reading the call's outputs, as that launch mode requires.
  *  - Operands must not alias outputs.  Pointers must be 16-byte aligned
  *    (CONV_ERR_ALIGN otherwise); element counts of every tensor must stay
  *    below 2^31 (CONV_ERR_OVERFLOW otherwise).
