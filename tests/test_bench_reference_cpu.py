@@ -28,3 +28,14 @@ def test_reference_arm_prints_one_contract_line():
     assert cpu["kind"] == "oracle" and cpu["cores"] >= 1 and cpu["value"] == d["value"]
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_step_profile_states_gemm_traffic():
+    """bench.py reads the GEMM kernels' DRAM bytes per step (its roofline
+    `traffic`) from the committed launch-list summary; the line must be there
+    and plausible: about the sum of the GEMMs' own inputs and outputs (1.26 GB)."""
+    import re
+    with open(os.path.join(ROOT, "profiles", "launch_list_alexnet_b128_step.md")) as f:
+        m = re.search(r"conv_gemm_dram_bytes_per_step = (\d+)", f.read())
+    assert m, "launch-list summary lacks the conv_gemm_dram_bytes_per_step line"
+    assert 1.0e9 < int(m.group(1)) < 1.6e9
