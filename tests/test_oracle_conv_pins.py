@@ -186,6 +186,51 @@ def test_bwd_matches_torch_autograd(orc, shape):
     np.testing.assert_allclose(db, bt.grad.numpy(), rtol=0, atol=1e-12 * (1 + db_abs.max()))
 
 
+def abs_grads(x, w, dy, st, pad):
+    """Torch float64 autograd of conv2d on |x| and |w| with upstream |dy|.
+
+    Every term of the input gradient dx[i] = sum w*dy and of the filter
+    gradient dw[j] = sum dy*x is a product of two such factors, so the
+    per-element scale sum |a_k b_k| the tolerance uses is exactly the gradient
+    of the convolution of the absolute values (padding taps read zero and
+    contribute nothing, as in the page's col2im, which drops them).
+    """
+    xa = torch.from_numpy(np.abs(x)).double().requires_grad_()
+    wa = torch.from_numpy(np.abs(w)).double().requires_grad_()
+    F.conv2d(xa, wa, stride=st, padding=pad).backward(torch.from_numpy(np.abs(dy)).double())
+    return xa.grad.numpy(), wa.grad.numpy()
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_bwd_abs_scales_match_torch(orc, shape):
+    """The tolerance scales of both gradients (full and sampled forms) against
+    torch's float64 autograd on absolute values."""
+    x, w, b, dy = make(shape, 18)
+    st, pad = shape[6], shape[7]
+    dx_abs_ref, dw_abs_ref = abs_grads(x, w, dy, st, pad)
+    _, dx_abs = orc.conv_bwd_data(w, dy, x.shape, st, pad, exact=True)
+    _, dw_abs = orc.conv_bwd_filter(x, dy, w.shape, st, pad, exact=True)
+    np.testing.assert_allclose(dx_abs, dx_abs_ref, rtol=1e-12, atol=1e-300)
+    np.testing.assert_allclose(dw_abs, dw_abs_ref, rtol=1e-12, atol=1e-300)
+    fx = np.arange(x.size, dtype=np.int64)
+    fw = np.arange(w.size, dtype=np.int64)
+    _, dx_abs_at = orc.conv_bwd_data_at(w, dy, x.shape, st, pad, fx, exact=True)
+    _, dw_abs_at = orc.conv_bwd_filter_at(x, dy, w.shape, st, pad, fw, exact=True)
+    np.testing.assert_allclose(dx_abs_at, dx_abs_ref.ravel(), rtol=1e-12, atol=1e-300)
+    np.testing.assert_allclose(dw_abs_at, dw_abs_ref.ravel(), rtol=1e-12, atol=1e-300)
+
+
+def test_bwd_abs_scale_hand_case(orc):
+    """One input channel, one filter of ones, 3x3 image, k 2, stride 1, no pad:
+    dx_abs is the tap-count map weighted by |dy| (closed form)."""
+    x = np.zeros((1, 1, 3, 3), np.float32)
+    w = np.ones((1, 1, 2, 2), np.float32)
+    dy = np.array([[[[1, -2], [-3, 4]]]], np.float32)
+    _, dx_abs = orc.conv_bwd_data(w, dy, x.shape, 1, 0, exact=True)
+    expect = np.array([[1, 3, 2], [4, 10, 6], [3, 7, 4]], np.float64)
+    assert np.array_equal(dx_abs[0, 0], expect)
+
+
 @pytest.mark.parametrize("shape", [SHAPES[1], SHAPES[3], SHAPES[5]])
 def test_bwd_central_differences(orc, shape):
     """L(x, W, b) = sum(conv(x, W, b) * R) is linear in each argument, so the

@@ -37,6 +37,21 @@ MUTATIONS = {
     "maxpool_last_max": ("if (x[at] > m)", "if (x[at] >= m)"),
     "maxpool_bwd_overwrites": ("dx[idx[t]] = dx[idx[t]] + dy[t];", "dx[idx[t]] = dy[t];"),
     "sgd_clip_sign": ("float c = g < -clip ? -clip : g;", "float c = g < -clip ? clip : g;"),
+    "col2im_abs_twice": ("col_abs ? col_abs[row * cols + j] : fabs(col[row * cols + j]);",
+                         "col_abs ? 2.0 * col_abs[row * cols + j] : fabs(col[row * cols + j]);"),
+    "col2im_abs_pad_taps": ("if (h < 0 || h >= H || w < 0 || w >= W)\n                            continue;",
+                            "if (h < 0 || h >= H || w < 0 || w >= W) {\n"
+                            "                            if (plane_abs && col_abs)\n"
+                            "                                plane_abs[(h < 0 ? 0 : h >= H ? H - 1 : h) * W +\n"
+                            "                                          (w < 0 ? 0 : w >= W ? W - 1 : w)] +=\n"
+                            "                                    col_abs[row * cols + (n * P + oh) * Q + ow];\n"
+                            "                            continue;\n"
+                            "                        }"),
+    "dgrad_at_abs_signed": ("acc_abs += fabs(p);\n                        }\n                    }",
+                            "acc_abs += p;\n                        }\n                    }"),
+    "wgrad_at_abs_from_x": ("acc_abs += fabs(p);\n        }\n        out[t] = acc;\n        out_abs[t] = acc_abs;\n    }\n}\n\n/* Step A8",
+                            "acc_abs += fabs(dy[(n * Ko + k) * PQ + pq]);\n        }\n        out[t] = acc;\n"
+                            "        out_abs[t] = acc_abs;\n    }\n}\n\n/* Step A8"),
     "abs_scale_signed": ("acc_abs += fabs(p);\n    }\n    *out = acc;", "acc_abs += p;\n    }\n    *out = acc;"),
 }
 
@@ -67,6 +82,21 @@ def pin_failures(orc):
             bad.append("dgrad_vs_torch")
         if not np.allclose(dw, wt.grad.numpy(), rtol=0, atol=1e-10):
             bad.append("wgrad_vs_torch")
+        xa = torch.from_numpy(np.abs(x)).double().requires_grad_()
+        wa = torch.from_numpy(np.abs(w)).double().requires_grad_()
+        F.conv2d(xa, wa, stride=st, padding=pad).backward(torch.from_numpy(np.abs(dy)).double())
+        _, dx_abs = orc.conv_bwd_data(w, dy, x.shape, st, pad, exact=True)
+        _, dw_abs = orc.conv_bwd_filter(x, dy, w.shape, st, pad, exact=True)
+        if not np.allclose(dx_abs, xa.grad.numpy(), rtol=1e-12, atol=0):
+            bad.append("dgrad_abs_scale")
+        if not np.allclose(dw_abs, wa.grad.numpy(), rtol=1e-12, atol=0):
+            bad.append("wgrad_abs_scale")
+        _, dxa_at = orc.conv_bwd_data_at(w, dy, x.shape, st, pad, np.arange(x.size, dtype=np.int64), exact=True)
+        _, dwa_at = orc.conv_bwd_filter_at(x, dy, w.shape, st, pad, np.arange(w.size, dtype=np.int64), exact=True)
+        if not np.allclose(dxa_at, xa.grad.numpy().ravel(), rtol=1e-12, atol=0):
+            bad.append("dgrad_at_abs_scale")
+        if not np.allclose(dwa_at, wa.grad.numpy().ravel(), rtol=1e-12, atol=0):
+            bad.append("wgrad_at_abs_scale")
         col = orc.im2col(np.ones_like(x), R, st, pad)
         d1, _ = orc.col2im(col, x.shape, R, st, pad)
         cnt = np.zeros((H, W))
