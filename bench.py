@@ -810,6 +810,100 @@ def run_matmul(args):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# the whole flagged-matmul sweep (--workload matmul_sweep): every one of the
+# 1176 (M, N, K, flags) cases timed on its own
+
+def attainable_tflops(M, N, K, peak_tflops, hbm_gbs):
+    """Roofline of one case: the tensor peak, or the HBM bandwidth times the
+    arithmetic intensity at minimal traffic (read A and B once, write C once),
+    whichever is lower."""
+    ai = 2.0 * M * N * K / (4.0 * (M * K + K * N + M * N))
+    return min(peak_tflops, ai * hbm_gbs * 1e-3)
+
+
+def run_matmul_sweep(args):
+    import torch
+    import im2col_convolution_tiled_gb300 as cb
+
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    if not os.path.exists(cb.LIB_PATH):
+        from im2col_convolution_tiled_gb300 import build
+        build.build()
+    cb.load()
+    bf16, hbm, peak_kind = peaks()
+    tf32 = args.math == "tf32"
+    cb.set_math_mode(cb.CONV_MATH_TF32 if tf32 else cb.CONV_MATH_FP32)
+    peak = bf16 * TF32_OVER_BF16 / (1 if tf32 else SPLIT_PRODUCTS)
+    stream = torch.cuda.current_stream()
+    pools = [torch.from_numpy(synthetic.matmul_pool(i)).cuda() for i in (0, 1)]
+    big = max(synthetic.MATMUL_MN)
+    cbuf = torch.empty(big * big, dtype=torch.float32, device="cuda")
+    rows = []
+    flops_all, ms_all = 0, 0.0
+    n0 = cb.launch_count()
+    with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
+        for M, K, N, flags in synthetic.matmul_sweep():
+            oa, ob = synthetic.matmul_sweep_offsets(M, K, N, flags)
+            a = pools[0][oa:oa + M * K].view(*((K, M) if flags & 1 else (M, K)))
+            b = pools[1][ob:ob + K * N].view(*((N, K) if flags & 2 else (K, N)))
+            c = cbuf[:M * N].view(M, N)
+            f = 2 * M * N * K
+            est_ms = f / 150e12 * 1e3 + 0.005
+            reps = int(min(50, max(3, 1.0 / est_ms)))
+            cb.matmul(a, b, flags, C=c)   # warm-up
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                cb.matmul(a, b, flags, C=c)
+            e1.record(stream)
+            e1.synchronize()
+            ms = e0.elapsed_time(e1) / reps
+            flops_all += f
+            ms_all += ms
+            att = attainable_tflops(M, N, K, peak, hbm)
+            tfl = f / (ms * 1e-3) / 1e12
+            rows.append({"M": M, "N": N, "K": K, "flags": flags, "ms": round(ms, 5), "tflops": round(tfl, 2),
+                         "frac": round(tfl / peak, 4), "frac_attainable": round(tfl / att, 4)})
+    cb.check()
+    launches = cb.launch_count() - n0
+    small = [r for r in rows if min(r["M"], r["N"]) < 128]
+    large = [r for r in rows if min(r["M"], r["N"]) >= 128]
+
+    def agg(rs):
+        fl = sum(2 * r["M"] * r["N"] * r["K"] for r in rs)
+        ms = sum(r["ms"] for r in rs)
+        return {"cases": len(rs), "tflops": round(fl / (ms * 1e-3) / 1e12, 2),
+                "median_frac_attainable": round(statistics.median(r["frac_attainable"] for r in rs), 4),
+                "min_frac_attainable": min(r["frac_attainable"] for r in rs)}
+
+    value = flops_all / (ms_all * 1e-3) / 1e12
+    worst = sorted(rows, key=lambda r: r["frac_attainable"])[:12]
+    if args.table:
+        with open(args.table, "w") as fh:
+            json.dump(rows, fh)
+    line = {
+        "metric": MATMUL_METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": 1, "steps": 1,
+        "warmup": 1, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "tf32" if tf32 else "f32", "data": "synthetic",
+        "config": {"workload": "the whole flagged-matmul sweep: M, N in %s, K in %s, flags 0-3 (1176 cases); "
+                               "value = total sweep FLOP / summed per-case time"
+                               % (list(synthetic.MATMUL_MN), list(synthetic.MATMUL_K)),
+                   "math": args.math, "small_regime": agg(small), "large_regime": agg(large),
+                   "worst_cases": worst, "table": args.table,
+                   "l2": "no flush; each case repeated on the same operands (small cases run from L2)"},
+        "roofline": {"bound": "tensor", "achieved": round(value, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
+                     "frac": round(value / peak, 4), "traffic": None,
+                     "peak_basis": "%s bf16 %.1f TFLOP/s x %.3f (TF32/BF16)%s; frac_attainable per case uses "
+                                   "min(peak, intensity x %.1f GB/s)"
+                                   % (peak_kind, bf16, TF32_OVER_BF16, "" if tf32 else " / 3 (3xTF32)", hbm)},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -819,7 +913,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-batch", type=int, default=64)
     ap.add_argument("--ref-batch", type=int, default=1)
-    ap.add_argument("--workload", choices=["alexnet", "lenet", "direct", "matmul"], default="alexnet")
+    ap.add_argument("--workload", choices=["alexnet", "lenet", "direct", "matmul", "matmul_sweep"],
+                    default="alexnet")
+    ap.add_argument("--table", default=None, help="matmul_sweep: write the per-case table (JSON) here")
     ap.add_argument("--math", choices=["fp32", "tf32"], default="fp32",
                     help="contractions in fp32-faithful 3xTF32 (default) or one TF32 product")
     args = ap.parse_args()
@@ -830,6 +926,8 @@ def main():
         run_direct(args)
     elif args.workload == "matmul":
         run_matmul(args)
+    elif args.workload == "matmul_sweep":
+        run_matmul_sweep(args)
     elif args.impl == "reference":
         run_reference(args)
     else:

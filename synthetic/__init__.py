@@ -190,6 +190,40 @@ def matmul_sweep():
                     yield M, K, N, flags
 
 
+# The sweep's 1176 cases would need 7e9 fresh N(0,1) draws; instead every case
+# reads its operands out of two fixed N(0,1) pools (one for A, one for B), at a
+# case-dependent offset (a multiple of 4 floats, so views stay 16-byte aligned).
+# Any such window of i.i.d. N(0,1) draws is itself i.i.d. N(0,1).
+MATMUL_POOL_FLOATS = max(MATMUL_MN) * max(MATMUL_K) + 4096
+_MATMUL_POOLS = {}
+
+
+def matmul_pool(which):
+    """Pool 0 (A operands) or 1 (B operands): MATMUL_POOL_FLOATS N(0,1) fp32 draws."""
+    if which not in _MATMUL_POOLS:
+        _MATMUL_POOLS[which] = normal((MATMUL_POOL_FLOATS,), 5900 + which)
+    return _MATMUL_POOLS[which]
+
+
+def matmul_sweep_offsets(M, K, N, flags):
+    """(offset of A in pool 0, offset of B in pool 1), in floats, for one sweep case."""
+    tag = ((M * 31 + K) * 31 + N) * 4 + flags
+    offs = []
+    for i, size in enumerate((M * K, K * N)):
+        room = (MATMUL_POOL_FLOATS - size) // 4
+        offs.append(4 * int(rng(7000 + 2 * tag + i).integers(0, room + 1)))
+    return tuple(offs)
+
+
+def matmul_sweep_case(M, K, N, flags):
+    """A (M x K, or K x M when flags bit 0) and B (K x N, or N x K when bit 1) of
+    one sweep case: contiguous views into the two pools."""
+    oa, ob = matmul_sweep_offsets(M, K, N, flags)
+    a_shape = (K, M) if flags & 1 else (M, K)
+    b_shape = (N, K) if flags & 2 else (K, N)
+    return (matmul_pool(0)[oa:oa + M * K].reshape(a_shape), matmul_pool(1)[ob:ob + K * N].reshape(b_shape))
+
+
 def pool_input(layer: ConvLayer, seed_offset=10):
     """Input of the max-pool after ``layer``: post-ReLU activations of the layer's
     output shape (about half zeros, so ties are frequent)."""
