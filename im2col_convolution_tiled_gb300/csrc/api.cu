@@ -18,6 +18,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 int* g_err_ptr[kMaxDevices];
 int g_sms[kMaxDevices];
+bool g_sm103[kMaxDevices];   // an sm_103 part this library was compiled for
 std::once_flag g_once[kMaxDevices];
 
 int current_device()
@@ -34,6 +35,13 @@ void init_device(int dev)
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) sms = 148;
     g_sms[dev] = sms;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        cudaGetLastError();
+        major = minor = 0;
+    }
+    g_sm103[dev] = major == 10 && minor == 3;
 }
 }  // namespace
 
@@ -58,20 +66,13 @@ int sm_count()
 }
 
 // Is the current device an sm_103 part this library was compiled for?
+// (Looked up once per device, under the same once-flag as the rest of the
+// per-device state, so concurrent host threads see one consistent answer.)
 static bool device_ok()
 {
-    static int ok[kMaxDevices];   // 0 unknown, 1 yes, -1 no
     const int dev = current_device();
-    if (ok[dev] == 0) {
-        int major = 0, minor = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
-            cudaGetLastError();
-            return false;
-        }
-        ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
-    }
-    return ok[dev] == 1;
+    std::call_once(g_once[dev], init_device, dev);
+    return g_sm103[dev];
 }
 
 static constexpr long long kMaxElems = (1LL << 31) - 1;

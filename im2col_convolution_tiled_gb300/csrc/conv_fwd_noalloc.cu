@@ -1,7 +1,11 @@
 // conv_fwd_noalloc.cu -- conv_fwd for callers that must not allocate device
-// memory: the scratch conv_fwd needs (the filters re-laid as pre-split
-// tensor-core tiles) comes from a fixed array compiled into this library
-// instead of from a caller-provided workspace.
+// memory: the scratch conv_fwd needs comes from a fixed array compiled into
+// this library instead of from a caller-provided workspace.  That scratch has
+// up to three regions, laid out as conv_fwd lays out its workspace: the
+// filters re-laid as pre-split tensor-core tiles (the B image); for the patch
+// and space-to-depth forms, the channel-blocked or space-to-depth copy of x,
+// whose size grows with the batch; and the partial tiles of a split last
+// round of tiles.  Shapes whose total exceeds the array are refused.
 //
 // Who needs this: code that runs under a device-memory manager owning the
 // whole heap (a host framework, an embedded runtime with a fixed budget), or
@@ -44,9 +48,9 @@ extern "C" int conv_fwd_noalloc(const conv_shape_t* s, const float* x, const flo
                                 conv_stream_t stream)
 {
     using namespace cb200;
-    // Shapes whose filter image does not fit are refused before anything is
-    // launched.  (An invalid shape needs 0 bytes here and is reported by
-    // conv_fwd's own validation below.)
+    // Shapes whose scratch (B image + staged copy of x + split partials) does
+    // not fit are refused before anything is launched.  (An invalid shape
+    // needs 0 bytes here and is reported by conv_fwd's own validation below.)
     const size_t need = conv_b200_workspace_bytes(CONV_OP_FWD, s);
     if (need > size_t(CONV_FWD_NOALLOC_SCRATCH_BYTES)) return CONV_ERR_SCRATCH_LIMIT;
     int dev = 0;
@@ -56,7 +60,10 @@ extern "C" int conv_fwd_noalloc(const conv_shape_t* s, const float* x, const flo
     }
     std::call_once(g_scratch_once[dev], resolve_scratch, dev);
     if (g_scratch_err[dev] != cudaSuccess || g_scratch_addr[dev] == nullptr) return CONV_ERR_CUDA;
-    // The filter image is rewritten in full by every call (padding included),
-    // so nothing left in the array by an earlier call needs clearing.
+    // Every region is written in full by this call before it is read: the B
+    // image (padding included) by its builder, the copy of x by its gather
+    // kernel, and each partial tile by the GEMM piece that owns it before the
+    // reduce adds them.  So nothing an earlier call left in the array needs
+    // clearing.
     return conv_fwd(s, x, w, b, y, g_scratch_addr[dev], size_t(CONV_FWD_NOALLOC_SCRATCH_BYTES), stream);
 }

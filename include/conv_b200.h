@@ -276,14 +276,22 @@ uint64_t conv_b200_launch_count(void);
  * of CONV_FWD_NOALLOC_SCRATCH_BYTES inside the library instead.  The library
  * allocates nothing for it: the array is part of the loaded module, and every
  * device that loads the library keeps one until the process exits.
- *  - Shapes with conv_b200_workspace_bytes(CONV_OP_FWD, s) larger than the
- *    array (filters with more than about a million entries) are rejected
- *    with CONV_ERR_SCRATCH_LIMIT before anything is launched.  Every other
- *    argument is validated exactly as by conv_fwd, with the same codes.
+ *  - The array must hold the whole scratch conv_fwd would take for the shape,
+ *    conv_b200_workspace_bytes(CONV_OP_FWD, s): the filters as pre-split
+ *    tensor-core tiles, plus -- for the forms that stage the input through a
+ *    copy -- the channel-blocked or space-to-depth copy of x (its size grows
+ *    with the batch) and the partial tiles of a split last round of tiles.
+ *    Shapes that need more are rejected with CONV_ERR_SCRATCH_LIMIT before
+ *    anything is launched; check in advance with conv_b200_workspace_bytes.
+ *    Of the AlexNet layers at batch 128 only conv2 fits (2.3 MiB); conv1
+ *    (101.8 MiB), conv3 (16.9), conv4 (25.1) and conv5 (22.9) are refused,
+ *    while all five fit at batch 2.  Every other argument is validated
+ *    exactly as by conv_fwd, with the same codes.
  *  - The first call on each device resolves the array's device address
  *    (cudaGetSymbolAddress, with that device current); make that first call
  *    before capturing a stream.
- *  - All calls share the one array and each rewrites it in full.  Two calls
+ *  - All calls share the one array.  Each call writes every byte of it that
+ *    it later reads, so nothing needs clearing between calls.  Two calls
  *    whose kernels may overlap on the GPU (different streams with no ordering
  *    between them) race on it and can both return garbage: order them.
  *  - The result is identical to conv_fwd's for the same inputs. */
