@@ -22,7 +22,6 @@ convolution kernels against the implicit-GEMM path (an ablation);
 from __future__ import annotations
 
 import argparse
-import re
 import json
 import os
 import statistics
@@ -73,6 +72,33 @@ def job_rate(units_per_rank, ms_max, world) -> float:
     processes units_per_rank per step, the job's step takes the slowest rank's
     time.  Units per second."""
     return world * units_per_rank / (ms_max * 1e-3)
+
+
+STEP_TRAFFIC = os.path.join(ROOT, "profiles", "step_traffic_alexnet_b128.json")
+
+
+def gemm_sources_digest(names) -> str:
+    """sha256 over the named GEMM kernel sources (name, then bytes, in order)."""
+    import hashlib
+    h = hashlib.sha256()
+    for n in names:
+        h.update(n.encode())
+        with open(os.path.join(ROOT, "im2col_convolution_tiled_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def gemm_traffic_per_step():
+    """DRAM bytes (read + write) of the conv GEMM kernels in one step, from the
+    ncu counters stored in profiles/ -- or None when they are absent or were
+    taken on GEMM sources other than the ones built now (stale)."""
+    if not os.path.exists(STEP_TRAFFIC):
+        return None
+    with open(STEP_TRAFFIC) as f:
+        rec = json.load(f)
+    if gemm_sources_digest(rec["gemm_sources"]) != rec["gemm_sources_sha256"]:
+        return None
+    return int(rec["conv_gemm_dram_bytes_per_step"])
 
 
 def step_flops(layers) -> int:
@@ -380,16 +406,7 @@ def run_ours(args):
     products = 1 if fast else SPLIT_PRODUCTS
     peak = bf16 * TF32_OVER_BF16 / products
     achieved = flops / (gemm_ms * 1e-3) / 1e12
-    # DRAM bytes (read + write) of the GEMM kernels in one step, from the ncu
-    # launch list summarised in profiles/ (a "conv_gemm_dram_bytes_per_step = N"
-    # line); absent -> null
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "launch_list_alexnet_b128_step.md")
-    if os.path.exists(prof) and not fast:
-        with open(prof) as f:
-            m = re.search(r"conv_gemm_dram_bytes_per_step = (\d+)", f.read())
-        if m:
-            traffic = int(m.group(1))
+    traffic = None if fast else gemm_traffic_per_step()
 
     # --- end to end through the public API with host buffers ---------------
     # As a training loop runs it: every step uploads its batch -- each layer's

@@ -10,6 +10,14 @@ import sys
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
+def _bench():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
 def test_reference_arm_prints_one_contract_line():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
                         "--warmup", "1", "--ref-batch", "1"],
@@ -30,12 +38,17 @@ def test_reference_arm_prints_one_contract_line():
     assert e2e["value"] == d["value"] and e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
 
 
-def test_step_profile_states_gemm_traffic():
-    """bench.py reads the GEMM kernels' DRAM bytes per step (its roofline
-    `traffic`) from the committed launch-list summary; the line must be there
-    and plausible: about the sum of the GEMMs' own inputs and outputs (1.26 GB)."""
-    import re
-    with open(os.path.join(ROOT, "profiles", "launch_list_alexnet_b128_step.md")) as f:
-        m = re.search(r"conv_gemm_dram_bytes_per_step = (\d+)", f.read())
-    assert m, "launch-list summary lacks the conv_gemm_dram_bytes_per_step line"
-    assert 1.0e9 < int(m.group(1)) < 1.6e9
+def test_step_traffic_record():
+    """bench.py reports the GEMM kernels' DRAM bytes per step (its roofline
+    `traffic`) from the stored ncu counters, and only while the GEMM sources
+    are the ones they were taken on.  The record must be plausible (about the
+    sum of the GEMMs' own inputs and outputs, 1.26 GB), and a changed source
+    must make the figure null."""
+    import json
+    bench = _bench()
+    with open(bench.STEP_TRAFFIC) as f:
+        rec = json.load(f)
+    assert 1.0e9 < rec["conv_gemm_dram_bytes_per_step"] < 1.6e9
+    t = bench.gemm_traffic_per_step()
+    assert t is None or t == rec["conv_gemm_dram_bytes_per_step"]
+    assert bench.gemm_sources_digest(rec["gemm_sources"][:-1]) != rec["gemm_sources_sha256"]
