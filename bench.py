@@ -828,6 +828,278 @@ def run_matmul(args):
 
 
 # ---------------------------------------------------------------------------
+# helpers shared by the per-kernel workloads below
+
+def _load_lib():
+    import im2col_convolution_tiled_gb300 as cb
+    if not os.path.exists(cb.LIB_PATH):
+        from im2col_convolution_tiled_gb300 import build
+        build.build()
+    cb.load()
+    return cb
+
+
+def graph_time_ms(run, reps, warmup=3):
+    """Mean device time of one run() over `reps` calls captured once into a
+    CUDA graph and replayed between CUDA events on the launching stream (host
+    issue cost cannot hide short kernels).  run() must allocate nothing."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(warmup):
+            run()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            run()
+    g.replay()   # one untimed replay
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def layer_tensors(cb, L):
+    """Device tensors of one layer workload plus preallocated outputs and one
+    workspace large enough for its three convolution calls."""
+    import torch
+    x, w, b, dy = (torch.from_numpy(a).cuda() for a in L.make())
+    s = cb.shape_of(L.x_shape, L.w_shape, L.stride, L.pad)
+    ws = torch.empty(max(cb.workspace_bytes(op, s) for op in range(3)) + 16, dtype=torch.uint8, device="cuda")
+    return {"x": x, "w": w, "b": b, "dy": dy, "ws": ws, "y": torch.empty(L.y_shape, device="cuda"),
+            "dx": torch.empty(L.x_shape, device="cuda"), "dw": torch.empty(L.w_shape, device="cuda"),
+            "db": torch.empty(L.outC, device="cuda")}
+
+
+# ---------------------------------------------------------------------------
+# the single convolution layer (--workload single): batch 4, 1x28x28, six 5x5
+# filters -- the forward and the three gradients of one ConvLayer
+
+SINGLE_METRIC = "single conv layer fwd+bwd (batch 4, 1x28x28 -> 6@5x5): TFLOP/s of the three GEMMs"
+
+
+def run_single(args):
+    import torch
+    cb = _load_lib()
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    L = synthetic.SINGLE
+    t = layer_tensors(cb, L)
+
+    def step():
+        cb.conv_fwd(t["x"], t["w"], t["b"], L.stride, L.pad, y=t["y"], workspace=t["ws"])
+        cb.conv_bwd_data(t["w"], t["dy"], L.x_shape, L.stride, L.pad, dx=t["dx"], workspace=t["ws"])
+        cb.conv_bwd_filter_bias(t["x"], t["dy"], L.w_shape, L.stride, L.pad, dw=t["dw"], db=t["db"],
+                                workspace=t["ws"])
+
+    n0 = cb.launch_count()
+    step()
+    launches = cb.launch_count() - n0
+    with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
+        ms = graph_time_ms(step, args.steps, args.warmup)
+    cb.check()
+    flops = 3 * L.gemm_flops
+    value = flops / (ms * 1e-3) / 1e12
+
+    # end to end: x and dy up from pinned host memory, y, dx, dw, db back, per step
+    hx, hdy = (torch.from_numpy(a).pin_memory() for a in L.make()[0:4:3])
+    outs = {k: torch.empty(t[k].shape).pin_memory() for k in ("y", "dx", "dw", "db")}
+    stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        t["x"].copy_(hx, non_blocking=True)
+        t["dy"].copy_(hdy, non_blocking=True)
+        step()
+        for k, v in outs.items():
+            v.copy_(t[k], non_blocking=True)
+    stream.synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    cb.check()
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        orc = oracle.get()
+        x, w, b, dy = L.make()
+        n = 200
+        t0 = time.perf_counter()
+        for _ in range(n):
+            orc.conv_fwd(x, w, b, L.stride, L.pad)
+            orc.conv_bwd_data(w, dy, x.shape, L.stride, L.pad)
+            orc.conv_bwd_filter(x, dy, w.shape, L.stride, L.pad)
+            orc.conv_bwd_bias(dy)
+        dt = time.perf_counter() - t0
+        cpu = {"value": n * flops / dt / 1e12, "unit": "TFLOP/s", "cores": orc.threads(), "kind": "oracle",
+               "sample": "the whole layer (forward and the three gradients) %d times, %.2f s" % (n, dt)}
+    line = {
+        "metric": SINGLE_METRIC, "value": round(value, 4), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "single conv layer, batch 4, 1x28x28 U[0,1) -> 6 filters 5x5, stride 1, pad 0: "
+                               "conv_fwd, conv_bwd_data, conv_bwd_filter_bias, one CUDA graph",
+                   "gflop_per_step": round(flops / 1e9, 5), "l2": "no flush: the layer is 0.1 MB, L2-resident"},
+        "roofline": {"bound": "latency", "launches_per_step": launches,
+                     "us_per_launch": round(1e3 * ms / max(launches, 1), 2), "achieved": round(value, 4),
+                     "unit": "TFLOP/s", "peak": None, "frac": None, "traffic": None,
+                     "note": "2.1 MFLOP over dependent launches: far below any throughput roofline"},
+        "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12, 4), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(hx.numel() * 4 + hdy.numel() * 4),
+                "d2h_bytes_per_step": int(sum(v.numel() * 4 for v in outs.values())),
+                "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": launches * args.steps,
+        "clocks": clk.summary(),
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# HBM-bound kernels (--workload hbm): im2col, col2im, max pooling, the
+# standalone bias gradient and SGD on the AlexNet batch-128 shapes, each
+# timed alone (graph-replayed) against the measured copy bandwidth
+
+HBM_METRIC = "HBM-bound kernels on AlexNet batch-128 shapes: GB/s of algorithmic bytes and fraction of copy bandwidth"
+
+
+def hbm_cases(cb, torch):
+    """(name, algorithmic bytes, run) for every HBM-bound kernel measured."""
+    cases = []
+    for L in synthetic.ALEXNET:
+        x = torch.from_numpy(L.make()[0]).cuda()
+        ncol = L.inC * L.k * L.k * L.batch * L.outH * L.outW
+        col = torch.empty(ncol, device="cuda").view(L.inC * L.k * L.k, -1)
+        dx = torch.empty(L.x_shape, device="cuda")
+        nb = 4 * (x.numel() + ncol)
+        cases.append(("im2col " + L.name, nb, lambda x=x, col=col, L=L: cb.im2col(x, L.k, L.stride, L.pad, col=col)))
+        cases.append(("col2im " + L.name, nb, lambda col=col, dx=dx, L=L:
+                      cb.col2im(col, L.x_shape, L.k, L.stride, L.pad, dx=dx)))
+        dy = torch.from_numpy(synthetic.normal(L.y_shape, L.seed_base + 4)).cuda()
+        db = torch.empty(L.outC, device="cuda")
+        cases.append(("bias_grad " + L.name, 4 * dy.numel(), lambda dy=dy, db=db: cb.conv_bwd_bias(dy, db=db)))
+        if L.pool:
+            k, st = L.pool
+            xp = torch.from_numpy(synthetic.pool_input(L)).cuda()
+            yp, idx = cb.maxpool2d_fwd(xp, k, st)
+            dyp = torch.from_numpy(synthetic.pool_grad(tuple(yp.shape), 5)).cuda()
+            dxp = torch.empty(L.y_shape, device="cuda")
+            fwd_b = 4 * (xp.numel() + 2 * yp.numel())
+            bwd_b = 4 * (2 * yp.numel() + xp.numel())
+            cases.append(("maxpool_fwd %dx%d/%d after %s" % (k, k, st, L.name), fwd_b,
+                          lambda xp=xp, yp=yp, idx=idx, k=k, st=st: cb.maxpool2d_fwd(xp, k, st, y=yp, idx=idx)))
+            cases.append(("maxpool_bwd %dx%d/%d after %s" % (k, k, st, L.name), bwd_b,
+                          lambda dyp=dyp, idx=idx, dxp=dxp, k=k, st=st, L=L:
+                          cb.maxpool2d_bwd(dyp, idx, L.y_shape, k, st, dx=dxp)))
+    n = sum(L.outC * L.inC * L.k * L.k + L.outC for L in synthetic.ALEXNET)
+    for count, what in ((n, "AlexNet conv1-5 filters and biases"), (1 << 26, "64 M parameters")):
+        p = torch.from_numpy(synthetic.normal((count,), 71)).cuda()
+        g = torch.from_numpy(synthetic.normal((count,), 72)).cuda()
+        cases.append(("sgd_step " + what, 12 * count, lambda p=p, g=g: cb.sgd_step(p, g, 0.01, 1.0)))
+    return cases
+
+
+def run_hbm(args):
+    import torch
+    cb = _load_lib()
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    _, hbm, peak_kind = peaks()
+    rows = []
+    n0 = cb.launch_count()
+    with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
+        for name, nbytes, run in hbm_cases(cb, torch):
+            reps = max(5, min(args.steps, 50))
+            ms = graph_time_ms(run, reps, args.warmup)
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            rows.append({"kernel": name, "mb": round(nbytes / 1e6, 2), "us": round(ms * 1e3, 2),
+                         "gbs": round(gbs, 1), "frac": round(gbs / hbm, 4)})
+            torch.cuda.empty_cache()
+    cb.check()
+    launches = cb.launch_count() - n0
+    big = [r for r in rows if r["mb"] >= 100]
+    tot_b = sum(r["mb"] for r in big) * 1e6
+    tot_s = sum(r["us"] for r in big) * 1e-6
+    value = tot_b / tot_s / 1e9
+    dom = max(rows, key=lambda r: r["us"])
+    line = {
+        "metric": HBM_METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "im2col, col2im, bias gradient (AlexNet conv1-5, batch 128), max pool fwd / bwd "
+                               "(3x3 stride 2 after conv1 and conv2), SGD; value = algorithmic bytes / time over "
+                               "the kernels moving >= 100 MB per call",
+                   "kernels": rows,
+                   "l2": "no flush: every kernel of >= 100 MB streams more than L2; smaller ones are listed "
+                         "but left out of the value"},
+        "roofline": {"bound": "hbm", "kernel": dom["kernel"], "achieved": dom["gbs"], "peak": round(hbm, 1),
+                     "unit": "GB/s", "frac": dom["frac"], "traffic": None,
+                     "peak_basis": "%s copy bandwidth" % peak_kind},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# one entry point on one workload (--workload case): a small fixed command for
+# a profiler to attach to; nothing is timed or checked
+
+def run_case(args):
+    import torch
+    cb = _load_lib()
+    layers = {L.name: L for L in synthetic.ALEXNET + synthetic.LENET + (synthetic.SINGLE,)}
+    if args.op == "matmul":
+        M, N, K = (int(v) for v in args.mnk.split(","))
+        A, B = synthetic.matmul_case(M, K, N, args.flags)
+        At, Bt = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+        C = torch.empty((M, N), device="cuda")
+        run = lambda: cb.matmul(At, Bt, args.flags, C=C)
+    else:
+        L = layers[args.layer]
+        t = layer_tensors(cb, L)
+        if args.op == "fwd":
+            run = lambda: cb.conv_fwd(t["x"], t["w"], t["b"], L.stride, L.pad, y=t["y"], workspace=t["ws"])
+        elif args.op == "dgrad":
+            run = lambda: cb.conv_bwd_data(t["w"], t["dy"], L.x_shape, L.stride, L.pad, dx=t["dx"], workspace=t["ws"])
+        elif args.op == "wgrad":
+            run = lambda: cb.conv_bwd_filter_bias(t["x"], t["dy"], L.w_shape, L.stride, L.pad, dw=t["dw"],
+                                                  db=t["db"], workspace=t["ws"])
+        elif args.op == "bias":
+            run = lambda: cb.conv_bwd_bias(t["dy"], db=t["db"])
+        elif args.op in ("pool", "poolfwd", "poolbwd"):
+            k, st = L.pool or (2, 2)
+            xp = torch.from_numpy(synthetic.pool_input(L)).cuda()
+            yp, idx = cb.maxpool2d_fwd(xp, k, st)
+            dyp = torch.from_numpy(synthetic.pool_grad(tuple(yp.shape), 5)).cuda()
+            dxp = torch.empty(L.y_shape, device="cuda")
+            f = lambda: cb.maxpool2d_fwd(xp, k, st, y=yp, idx=idx)
+            bw = lambda: cb.maxpool2d_bwd(dyp, idx, L.y_shape, k, st, dx=dxp)
+            run = {"pool": lambda: (f(), bw()), "poolfwd": f, "poolbwd": bw}[args.op]
+        elif args.op == "im2col":
+            col = torch.empty((L.inC * L.k * L.k, L.batch * L.outH * L.outW), device="cuda")
+            run = lambda: cb.im2col(t["x"], L.k, L.stride, L.pad, col=col)
+        elif args.op == "col2im":
+            col = torch.from_numpy(synthetic.normal((L.inC * L.k * L.k, L.batch * L.outH * L.outW), 6)).cuda()
+            run = lambda: cb.col2im(col, L.x_shape, L.k, L.stride, L.pad, dx=t["dx"])
+        elif args.op == "sgd":
+            p = torch.from_numpy(synthetic.normal((1 << 26,), 71)).cuda()
+            g = torch.from_numpy(synthetic.normal((1 << 26,), 72)).cuda()
+            run = lambda: cb.sgd_step(p, g, 0.01, 1.0)
+        else:
+            raise SystemExit("unknown --op %s" % args.op)
+    for _ in range(args.steps):
+        run()
+    cb.check()
+    print("case done: %s %s x%d" % (args.mnk if args.op == "matmul" else args.layer, args.op, args.steps))
+
+
+# ---------------------------------------------------------------------------
 # the whole flagged-matmul sweep (--workload matmul_sweep): every one of the
 # 1176 (M, N, K, flags) cases timed on its own
 
@@ -930,8 +1202,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-batch", type=int, default=64)
     ap.add_argument("--ref-batch", type=int, default=1)
-    ap.add_argument("--workload", choices=["alexnet", "lenet", "direct", "matmul", "matmul_sweep"],
-                    default="alexnet")
+    ap.add_argument("--workload", choices=["alexnet", "lenet", "single", "direct", "matmul", "matmul_sweep",
+                                           "hbm", "case"], default="alexnet")
+    ap.add_argument("--layer", default="alexnet_conv2_b128", help="case: the layer workload")
+    ap.add_argument("--op", default="fwd", help="case: fwd, dgrad, wgrad, bias, pool, poolfwd, poolbwd, im2col, "
+                                                "col2im, sgd or matmul")
+    ap.add_argument("--mnk", default="4096,4096,4096", help="case --op matmul: M,N,K")
+    ap.add_argument("--flags", type=int, default=0, help="case --op matmul: transpose flags")
     ap.add_argument("--table", default=None, help="matmul_sweep: write the per-case table (JSON) here")
     ap.add_argument("--math", choices=["fp32", "tf32"], default="fp32",
                     help="contractions in fp32-faithful 3xTF32 (default) or one TF32 product")
@@ -945,6 +1222,12 @@ def main():
         run_matmul(args)
     elif args.workload == "matmul_sweep":
         run_matmul_sweep(args)
+    elif args.workload == "single":
+        run_single(args)
+    elif args.workload == "hbm":
+        run_hbm(args)
+    elif args.workload == "case":
+        run_case(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
