@@ -55,6 +55,8 @@ _SIGS = {
     "conv_bwd_filter": ([_SHAPE, _P, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
     "conv_bwd_filter_bias": ([_SHAPE, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
     "conv_bwd_bias": ([_SHAPE, _P, _P, _P], ctypes.c_int),
+    "conv_bwd_data_relu": ([_SHAPE, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
+    "conv_bwd_filter_bias_relu": ([_SHAPE, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P], ctypes.c_int),
     "conv_b200_workspace_bytes": ([ctypes.c_int, _SHAPE], ctypes.c_size_t),
     "im2col": ([_SHAPE, _P, _P, _P], ctypes.c_int),
     "col2im": ([_SHAPE, _P, _P, _P], ctypes.c_int),
@@ -184,16 +186,25 @@ def conv_fwd(x, w, b, stride=1, padding=0, y=None, workspace=None, stream=None, 
     return y
 
 
-def conv_bwd_data(w, dy, x_shape, stride=1, padding=0, dx=None, workspace=None, stream=None):
-    """dx = gradient of the convolution with respect to its input."""
+def conv_bwd_data(w, dy, x_shape, stride=1, padding=0, dx=None, workspace=None, stream=None, relu_mask=None):
+    """dx = gradient of the convolution with respect to its input.  With
+    relu_mask (the ReLU output that followed the convolution, shaped like dy)
+    the convolution's gradient is dy * (relu_mask > 0), formed as dy is read
+    (conv_bwd_data_relu)."""
     torch = _torch()
     _want(w, "w"), _want(dy, "dy")
+    if relu_mask is not None:
+        _want(relu_mask, "relu_mask")
     s = shape_of(tuple(x_shape), w.shape, stride, padding)
     if dx is None:
         dx = torch.empty(tuple(x_shape), dtype=torch.float32, device=dy.device)
     _want(dx, "dx")
     ws, nbytes = _workspace(CONV_OP_BWD_DATA, s, workspace)
-    _call("conv_bwd_data", ctypes.byref(s), _ptr(w), _ptr(dy), _ptr(dx), _ptr(ws), nbytes, _stream(stream))
+    if relu_mask is not None:
+        _call("conv_bwd_data_relu", ctypes.byref(s), _ptr(w), _ptr(dy), _ptr(relu_mask), _ptr(dx), _ptr(ws), nbytes,
+              _stream(stream))
+    else:
+        _call("conv_bwd_data", ctypes.byref(s), _ptr(w), _ptr(dy), _ptr(dx), _ptr(ws), nbytes, _stream(stream))
     return dx
 
 
@@ -210,10 +221,15 @@ def conv_bwd_filter(x, dy, w_shape, stride=1, padding=0, dw=None, workspace=None
     return dw
 
 
-def conv_bwd_filter_bias(x, dy, w_shape, stride=1, padding=0, dw=None, db=None, workspace=None, stream=None):
-    """(dw, db): filter and bias gradients from one pass over dy."""
+def conv_bwd_filter_bias(x, dy, w_shape, stride=1, padding=0, dw=None, db=None, workspace=None, stream=None,
+                         relu_mask=None):
+    """(dw, db): filter and bias gradients from one pass over dy.  With
+    relu_mask the convolution's gradient is dy * (relu_mask > 0), formed as dy
+    is read (conv_bwd_filter_bias_relu)."""
     torch = _torch()
     _want(x, "x"), _want(dy, "dy")
+    if relu_mask is not None:
+        _want(relu_mask, "relu_mask")
     s = shape_of(x.shape, tuple(w_shape), stride, padding)
     if dw is None:
         dw = torch.empty(tuple(w_shape), dtype=torch.float32, device=x.device)
@@ -221,8 +237,12 @@ def conv_bwd_filter_bias(x, dy, w_shape, stride=1, padding=0, dw=None, db=None, 
         db = torch.empty((w_shape[0],), dtype=torch.float32, device=x.device)
     _want(dw, "dw"), _want(db, "db")
     ws, nbytes = _workspace(CONV_OP_BWD_FILTER, s, workspace)
-    _call("conv_bwd_filter_bias", ctypes.byref(s), _ptr(x), _ptr(dy), _ptr(dw), _ptr(db), _ptr(ws), nbytes,
-          _stream(stream))
+    if relu_mask is not None:
+        _call("conv_bwd_filter_bias_relu", ctypes.byref(s), _ptr(x), _ptr(dy), _ptr(relu_mask), _ptr(dw), _ptr(db),
+              _ptr(ws), nbytes, _stream(stream))
+    else:
+        _call("conv_bwd_filter_bias", ctypes.byref(s), _ptr(x), _ptr(dy), _ptr(dw), _ptr(db), _ptr(ws), nbytes,
+              _stream(stream))
     return dw, db
 
 

@@ -215,6 +215,31 @@ int conv_bwd_filter_bias(const conv_shape_t* s, const float* x, const float* dy,
     return status_of(launch_conv_wgrad(d, x, dy, dw, workspace, as_cuda(stream), db));
 }
 
+int conv_bwd_data_relu(const conv_shape_t* s, const float* w, const float* dy, const float* a, float* dx,
+                       void* workspace, size_t workspace_bytes, conv_stream_t stream)
+{
+    ConvDims d;
+    int rc = check_shape(s, &d);
+    if (rc != CONV_OK) return rc;
+    if ((rc = check_ptrs({w, dy, a, dx})) != CONV_OK) return rc;
+    if ((rc = check_workspace(conv_dgrad_ws(d), workspace, workspace_bytes)) != CONV_OK) return rc;
+    if (!device_ok()) return CONV_ERR_DEVICE;
+    return status_of(launch_conv_dgrad(d, w, dy, dx, workspace, as_cuda(stream), a));
+}
+
+int conv_bwd_filter_bias_relu(const conv_shape_t* s, const float* x, const float* dy, const float* a, float* dw,
+                              float* db, void* workspace, size_t workspace_bytes, conv_stream_t stream)
+{
+    ConvDims d;
+    int rc = check_shape(s, &d);
+    if (rc != CONV_OK) return rc;
+    if ((rc = check_ptrs({x, dy, a, dw})) != CONV_OK) return rc;
+    if (db && !aligned16(db)) return CONV_ERR_ALIGN;
+    if ((rc = check_workspace(conv_wgrad_ws(d), workspace, workspace_bytes)) != CONV_OK) return rc;
+    if (!device_ok()) return CONV_ERR_DEVICE;
+    return status_of(launch_conv_wgrad(d, x, dy, dw, workspace, as_cuda(stream), db, a));
+}
+
 int conv_bwd_bias(const conv_shape_t* s, const float* dy, float* db, conv_stream_t stream)
 {
     ConvDims d;

@@ -47,13 +47,15 @@ cudaError_t launch_conv_fwd(const ConvDims& d, const float* x, const float* w, c
                             void* ws, cudaStream_t st, bool relu = false);
 size_t conv_fwd_ws(const ConvDims& d);
 
+// mask non-null: G = dy * (mask > 0) (nn_relu_grad fused where dy is read).
 cudaError_t launch_conv_dgrad(const ConvDims& d, const float* w, const float* dy, float* dx, void* ws,
-                              cudaStream_t st);
+                              cudaStream_t st, const float* mask = nullptr);
 size_t conv_dgrad_ws(const ConvDims& d);
 
 // db non-null: also the bias gradient, summed in the same pass over dy.
+// mask non-null: G = dy * (mask > 0) (nn_relu_grad fused where dy is read).
 cudaError_t launch_conv_wgrad(const ConvDims& d, const float* x, const float* dy, float* dw, void* ws,
-                              cudaStream_t st, float* db = nullptr);
+                              cudaStream_t st, float* db = nullptr, const float* mask = nullptr);
 size_t conv_wgrad_ws(const ConvDims& d);
 
 cudaError_t launch_matmul(int M, int K, int N, unsigned flags, const float* A, const float* B, float* C,

@@ -39,6 +39,8 @@ namespace cb200 {
 
 struct GatherGeom {
     const float* in;         // gathered tensor [Nb][Ci][Hi][Wi]
+    const float* mask;       // null, or a tensor shaped like `in`: each gathered value is multiplied by
+                             // (mask > 0) as it is loaded (nn_relu_grad fused into the input gradient)
     int Ci, Hi, Wi, HiWi, CiHiWi;
     int Gp, Gq, M;           // row grid per image and rows in all (Nb * Gp * Gq)
     int sp;                  // window stride on the input
@@ -167,9 +169,18 @@ struct ConvGatherProb {
             const int h = s.h0 + int(tr);
             const int w = s.w0 + int(tq);
             const bool ok = tap < TT && unsigned(h) < unsigned(g.Hi) && unsigned(w) < unsigned(g.Wi);
-            const float* p = g.in + (s.base + int(tr) * g.Wi + int(tq));
+            const int off = s.base + int(tr) * g.Wi + int(tq);
+            const float* p = g.in + off;
+            if (g.mask == nullptr) {
 #pragma unroll
-            for (int c = 0; c < CP; ++c) v[t * CP + c] = ldg_keep_if(p + c * g.HiWi, ok && c < g.Ci);
+                for (int c = 0; c < CP; ++c) v[t * CP + c] = ldg_keep_if(p + c * g.HiWi, ok && c < g.Ci);
+            } else {
+                const float* mp = g.mask + off;
+#pragma unroll
+                for (int c = 0; c < CP; ++c)
+                    v[t * CP + c] = ldg_keep_if(p + c * g.HiWi, ok && c < g.Ci) *
+                                    relu_gate(ldg_keep_if(mp + c * g.HiWi, ok && c < g.Ci));
+            }
         }
     }
 
@@ -184,9 +195,18 @@ struct ConvGatherProb {
             const int w = s.w0 + int(tq);
             const bool ok = unsigned(h) < unsigned(g.Hi) && unsigned(w) < unsigned(g.Wi);
             const int cleft = g.Ci - int(chunk) * 32;   // channels of this chunk that exist
-            const float* p = g.in + (s.base + int(chunk) * 32 * g.HiWi + int(tr) * g.Wi + int(tq));
+            const int off = s.base + int(chunk) * 32 * g.HiWi + int(tr) * g.Wi + int(tq);
+            const float* p = g.in + off;
+            if (g.mask == nullptr) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = ldg_keep_if(p + i * g.HiWi, ok && i < cleft);
+                for (int i = 0; i < 32; ++i) v[i] = ldg_keep_if(p + i * g.HiWi, ok && i < cleft);
+            } else {
+                const float* mp = g.mask + off;
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    v[i] = ldg_keep_if(p + i * g.HiWi, ok && i < cleft) *
+                           relu_gate(ldg_keep_if(mp + i * g.HiWi, ok && i < cleft));
+            }
         } else if (g.mode == 1) {
             switch (g.lcp) {
             case 0: load_taps<0>(s, ks, v); break;
@@ -212,7 +232,9 @@ struct ConvGatherProb {
                 const int rs = __shfl_sync(0xffffffffu, krs, i);
                 const int h = s.h0 + (rs >> 16);
                 const int w = s.w0 + (rs & 0xFFFF);
-                v[i] = ldg_keep_if(g.in + (s.base + off), unsigned(h) < unsigned(g.Hi) && unsigned(w) < unsigned(g.Wi));
+                const bool in = unsigned(h) < unsigned(g.Hi) && unsigned(w) < unsigned(g.Wi);
+                v[i] = ldg_keep_if(g.in + (s.base + off), in);
+                if (g.mask != nullptr) v[i] *= relu_gate(ldg_keep_if(g.mask + (s.base + off), in));
             }
         }
     }
@@ -885,8 +907,12 @@ static size_t blocked_bytes(const PatchGeom& pg)
 // are whole 128-byte pixels (16-byte stores).
 constexpr int kBlkRows = 4;
 
+// MASK: each value is multiplied by (mask > 0), mask shaped like src (the
+// ReLU gradient fused into the copy the input gradient reads).
+template <bool MASK>
 __global__ void __launch_bounds__(256, 4) to_blocked32_kernel(const float* __restrict__ src, float* __restrict__ dst,
-                                                           int C, int Cb, int H, int W, int hgroups)
+                                                           int C, int Cb, int H, int W, int hgroups,
+                                                           const float* __restrict__ mask)
 {
     griddep_wait();
     griddep_launch();
@@ -903,8 +929,11 @@ __global__ void __launch_bounds__(256, 4) to_blocked32_kernel(const float* __res
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int c = ty + 8 * i, ch = cb * 32 + c, w = w0 + tx;
-                tile[rr][c][tx] =
-                    (h < H && ch < C && w < W) ? __ldg(src + ((size_t(n) * C + ch) * H + h) * W + w) : 0.f;
+                const bool in = h < H && ch < C && w < W;
+                const size_t at = ((size_t(n) * C + ch) * H + h) * W + w;
+                float v = in ? __ldg(src + at) : 0.f;
+                if constexpr (MASK) v *= relu_gate(in ? __ldg(mask + at) : 0.f);
+                tile[rr][c][tx] = v;
             }
         }
         __syncthreads();
@@ -963,11 +992,14 @@ static cudaError_t encode_patch_tmap(PatchGeom& pg, float* blocked)
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-static cudaError_t setup_patch_tma(PatchGeom& pg, float* blocked, cudaStream_t st)
+static cudaError_t setup_patch_tma(PatchGeom& pg, float* blocked, cudaStream_t st, const float* mask = nullptr)
 {
     const int hgroups = (pg.Hi + kBlkRows - 1) / kBlkRows;
-    cudaError_t e = launch_pdl(to_blocked32_kernel, dim3(unsigned(pg.Nb * pg.Cb * hgroups)), dim3(256), 0, st, pg.in,
-                               blocked, pg.Ci, pg.Cb, pg.Hi, pg.Wi, hgroups);
+    const dim3 grid(unsigned(pg.Nb * pg.Cb * hgroups));
+    cudaError_t e = mask ? launch_pdl(to_blocked32_kernel<true>, grid, dim3(256), 0, st, pg.in, blocked, pg.Ci, pg.Cb,
+                                      pg.Hi, pg.Wi, hgroups, mask)
+                         : launch_pdl(to_blocked32_kernel<false>, grid, dim3(256), 0, st, pg.in, blocked, pg.Ci,
+                                      pg.Cb, pg.Hi, pg.Wi, hgroups, mask);
     if (e != cudaSuccess) return e;
     note_launch();
     e = cudaGetLastError();
@@ -1044,7 +1076,12 @@ struct WindowPlan {
     size_t img_bytes, part_bytes, blocked_bytes;
 };
 
-static WindowPlan plan_window(int Nb, int Ci, int Hi, int Wi, int Gp, int Gq, int sp, int o, int T, int ncols)
+// masked: the gathered tensor is multiplied by a ReLU mask where it is first
+// read -- in the channel-blocked copy of the tensor-map form, or in the
+// register gather -- so the per-channel bulk-copied patch form (which reads
+// the tensor straight into shared memory) is not used.
+static WindowPlan plan_window(int Nb, int Ci, int Hi, int Wi, int Gp, int Gq, int sp, int o, int T, int ncols,
+                              bool masked = false)
 {
     WindowPlan w{};
     int n_tiles;
@@ -1055,7 +1092,7 @@ static WindowPlan plan_window(int Nb, int Ci, int Hi, int Wi, int Gp, int Gq, in
         PatchGeom pg = make_patch(nullptr, Nb, Ci, Hi, Wi, Gp, Gq, sp, o, T);
         patch_box(pg);
         w.tma = patch_tma_fits(pg, w.bn);
-        w.patch = w.tma || max_patch_floats(pg) <= patch_capacity(w.bn);
+        w.patch = w.tma || (!masked && max_patch_floats(pg) <= patch_capacity(w.bn));
         if (w.tma) w.blocked_bytes = blocked_bytes(pg);
         if (w.patch) w.part_bytes = round_up_256(plan_patch_tail(pg, ncols, w.bn).part_floats * sizeof(float));
     }
@@ -1071,11 +1108,13 @@ static WindowPlan plan_window(int Nb, int Ci, int Hi, int Wi, int Gp, int Gq, in
 // One convolution-window GEMM over the gathered tensor `in` [Nb][Ci][Hi][Wi]:
 // rows = the (Gp x Gq) grid of each image, window h = p*sp + o + tap.
 // MakeGen(KDecode) builds the B-operand generator in the matching K order.
+// mask (nullable): multiply the gathered tensor by (mask > 0) as it is read.
 template <class MakeGen>
 static cudaError_t run_window_gemm(const float* in, int Nb, int Ci, int Hi, int Wi, int Gp, int Gq, int sp, int o,
-                                   int T, const OutGeom& og, void* ws, MakeGen make_gen, cudaStream_t st)
+                                   int T, const OutGeom& og, void* ws, MakeGen make_gen, cudaStream_t st,
+                                   const float* mask = nullptr)
 {
-    const WindowPlan wp = plan_window(Nb, Ci, Hi, Wi, Gp, Gq, sp, o, T, og.ncols);
+    const WindowPlan wp = plan_window(Nb, Ci, Hi, Wi, Gp, Gq, sp, o, T, og.ncols, mask != nullptr);
     float* img = static_cast<float*>(ws);
     const int bn = wp.bn;
     if (wp.patch) {
@@ -1091,13 +1130,14 @@ static cudaError_t run_window_gemm(const float* in, int Nb, int Ci, int Hi, int 
                                     : nullptr;
         if (wp.tma) {
             patch_box(pg);
-            e = setup_patch_tma(pg, reinterpret_cast<float*>(static_cast<char*>(ws) + wp.img_bytes), st);
+            e = setup_patch_tma(pg, reinterpret_cast<float*>(static_cast<char*>(ws) + wp.img_bytes), st, mask);
             if (e != cudaSuccess) return e;
             return dispatch_patch<true>(bn, pg, og, img, part, st);
         }
         return dispatch_patch<false>(bn, pg, og, img, part, st);
     }
-    const GatherGeom g = make_gather(in, Nb, Ci, Hi, Wi, Gp, Gq, sp, o, T);
+    GatherGeom g = make_gather(in, Nb, Ci, Hi, Wi, Gp, Gq, sp, o, T);
+    g.mask = mask;
     const KDecode dec = make_kdecode(g.mode == 2 ? 2 : 0, g.Cp, T);
     cudaError_t e = build_bimage(make_gen(dec), og.ncols, g.K, bn, img, st);
     if (e != cudaSuccess) return e;
@@ -1120,8 +1160,12 @@ size_t conv_dgrad_ws(const ConvDims& d)
     int d_lo, T, oo;
     dgrad_window(d, &d_lo, &T, &oo);
     const int Hs = (d.H + oo + d.S - 1) / d.S, Ws = (d.W + oo + d.S - 1) / d.S;
+    // room for either plan: the masked one (conv_bwd_data_relu) may take the
+    // register-gather form where the plain one takes the per-channel patch form
     const WindowPlan wp = plan_window(d.N, d.K, d.P, d.Q, Hs, Ws, 1, d_lo, T, dgrad_cols(d));
-    return wp.img_bytes + wp.part_bytes + wp.blocked_bytes;
+    const WindowPlan wm = plan_window(d.N, d.K, d.P, d.Q, Hs, Ws, 1, d_lo, T, dgrad_cols(d), true);
+    const size_t a = wp.img_bytes + wp.part_bytes + wp.blocked_bytes, b = wm.img_bytes + wm.part_bytes + wm.blocked_bytes;
+    return a > b ? a : b;
 }
 
 cudaError_t launch_conv_fwd(const ConvDims& d, const float* x, const float* w, const float* b, float* y, void* ws,
@@ -1159,7 +1203,7 @@ cudaError_t launch_conv_fwd(const ConvDims& d, const float* x, const float* w, c
 }
 
 cudaError_t launch_conv_dgrad(const ConvDims& d, const float* w, const float* dy, float* dx, void* ws,
-                              cudaStream_t st)
+                              cudaStream_t st, const float* mask)
 {
     int d_lo, T, oo;
     dgrad_window(d, &d_lo, &T, &oo);
@@ -1182,7 +1226,7 @@ cudaError_t launch_conv_dgrad(const ConvDims& d, const float* w, const float* dy
         return DgradFilterGen{w,   d.C, d.K, d.R, d.S, d.pad - oo, d_lo, dec, FastDiv(uint32_t(T)),
                               FastDiv(uint32_t(d.S * d.S)), FastDiv(uint32_t(d.S))};
     };
-    return run_window_gemm(dy, d.N, d.K, d.P, d.Q, Hs, Ws, 1, d_lo, T, o, ws, make_gen, st);
+    return run_window_gemm(dy, d.N, d.K, d.P, d.Q, Hs, Ws, 1, d_lo, T, o, ws, make_gen, st, mask);
 }
 
 }  // namespace cb200

@@ -172,6 +172,22 @@ struct GradGen {
     }
 };
 
+// The same with the ReLU gradient applied as dy is read (nn_relu_grad):
+// G[k, j] = dy[n, k, pq] * (mask[n, k, pq] > 0), mask shaped like dy.
+struct GradMaskGen {
+    const float* dy;
+    const float* mask;
+    int K, PQ;
+    FastDiv f_pq;
+    __device__ float operator()(int k, int j) const
+    {
+        uint32_t n, pq;
+        f_pq.divmod(uint32_t(j), n, pq);
+        const size_t at = (size_t(n) * K + k) * PQ + pq;
+        return __ldg(dy + at) * relu_gate(__ldg(mask + at));
+    }
+};
+
 // out[row] = sum of rowsum[row * blocks + i] over the blocks i: one warp per
 // row (warp `wid` of the grid), lane l adding blocks l, l + 32, ... in order,
 // then a fixed shuffle tree (deterministic).
@@ -334,7 +350,7 @@ size_t conv_wgrad_ws(const ConvDims& d)
 // gradient) into row-sum partials, added in block order by rowsum_final_kernel.
 template <int BN>
 static cudaError_t run_wgrad(const ConvDims& d, const WgradPlan& pl, const float* x, const float* dy, float* dw,
-                             void* ws, cudaStream_t st, const ConvDims* orig, float* db)
+                             void* ws, cudaStream_t st, const ConvDims* orig, float* db, const float* mask)
 {
     ConvWgradProb<BN> p;
     p.terms = math_terms();
@@ -361,8 +377,10 @@ static cudaError_t run_wgrad(const ConvDims& d, const WgradPlan& pl, const float
     p.k_stages = pl.k_stages;
     p.splits = pl.splits;
     p.ks_per_split = pl.ks_per_split;
-    cudaError_t e = build_bimage(GradGen{dy, d.K, p.PQ, FastDiv(uint32_t(p.PQ))}, d.K, p.NPQ, BN, img, st,
-                                 db ? rowsum : nullptr);
+    cudaError_t e = mask ? build_bimage(GradMaskGen{dy, mask, d.K, p.PQ, FastDiv(uint32_t(p.PQ))}, d.K, p.NPQ, BN,
+                                        img, st, db ? rowsum : nullptr)
+                         : build_bimage(GradGen{dy, d.K, p.PQ, FastDiv(uint32_t(p.PQ))}, d.K, p.NPQ, BN, img, st,
+                                        db ? rowsum : nullptr);
     if (e != cudaSuccess) return e;
     if (db && pl.splits == 1) {   // with split partials the reduce kernel finishes db
         e = launch_pdl(rowsum_final_kernel, dim3((d.K + 7) / 8), dim3(256), 0, st, rowsum, bimage_grid_x(p.NPQ), d.K, db);
@@ -384,7 +402,7 @@ static cudaError_t run_wgrad(const ConvDims& d, const WgradPlan& pl, const float
 }
 
 cudaError_t launch_conv_wgrad(const ConvDims& d, const float* x, const float* dy, float* dw, void* ws,
-                              cudaStream_t st, float* db)
+                              cudaStream_t st, float* db, const float* mask)
 {
     const WgradS2d w = plan_wgrad_s2d(d);
     const ConvDims& g = w.use ? w.d2 : d;
@@ -400,11 +418,11 @@ cudaError_t launch_conv_wgrad(const ConvDims& d, const float* x, const float* dy
         gws = xs + xs2d_floats(d, w);
     }
     switch (pl.bn) {
-    case 32: return run_wgrad<32>(g, pl, xg, dy, dw, gws, st, orig, db);
-    case 64: return run_wgrad<64>(g, pl, xg, dy, dw, gws, st, orig, db);
-    case 128: return run_wgrad<128>(g, pl, xg, dy, dw, gws, st, orig, db);
-    case 192: return run_wgrad<192>(g, pl, xg, dy, dw, gws, st, orig, db);
-    default: return run_wgrad<256>(g, pl, xg, dy, dw, gws, st, orig, db);
+    case 32: return run_wgrad<32>(g, pl, xg, dy, dw, gws, st, orig, db, mask);
+    case 64: return run_wgrad<64>(g, pl, xg, dy, dw, gws, st, orig, db, mask);
+    case 128: return run_wgrad<128>(g, pl, xg, dy, dw, gws, st, orig, db, mask);
+    case 192: return run_wgrad<192>(g, pl, xg, dy, dw, gws, st, orig, db, mask);
+    default: return run_wgrad<256>(g, pl, xg, dy, dw, gws, st, orig, db, mask);
     }
 }
 

@@ -103,6 +103,11 @@ __device__ __forceinline__ float ldg_keep_if(const float* p, bool pred)
     return pred ? __ldg(p) : 0.f;
 }
 
+// ReLU gradient gate (nn_relu_grad): 1 where the ReLU's input (or output) is
+// > 0, else 0; a gradient g is gated as g * relu_gate(a), an fp32 product
+// with 1 or 0, exactly as relu_bwd computes it.
+__device__ __forceinline__ float relu_gate(float a) { return a > 0.f ? 1.f : 0.f; }
+
 // ---------------------------------------------------------------------------
 // 4-byte asynchronous copy global -> shared (no register staging); completion
 // is awaited per thread with cp_async_wait_all().

@@ -22,8 +22,9 @@ Conventions (as the page's shaders give them):
     add_bias call (relu flag);
   * the convolutions' ReLU runs in their epilogue (conv_fwd_relu);
   * the ReLU gradient is masked by the ReLU's output (> 0 exactly where its
-    input is); behind a max pool the mask is applied to the pooled gradient,
-    by the pooled value, before routing;
+    input is); behind a convolution the mask is applied inside the
+    convolution's gradient calls, where they first read the routed gradient
+    (conv_bwd_data_relu, conv_bwd_filter_bias_relu), so it costs no pass;
   * the loss gradient is softmax - one_hot, the gradient of the batch SUM of
     the row cross-entropies, which is what `loss` holds;
   * the first layer's input gradient is not formed (x is the network input).
@@ -111,11 +112,9 @@ class LeNet5:
         t["z3"] = e((B, FCS[2][1]), **f32)              # logits
         t["loss"] = e((1,), **f32)
         t["dp2"] = t["df"].view(t["p2"].shape)
-        t["dq2"] = torch.empty_like(t["p2"])            # dp2 masked by p2 > 0
-        t["dy2"] = torch.empty_like(t["a2"])
+        t["da2"] = torch.empty_like(t["a2"])            # gradient at the ReLU output a2 (routed by the pool)
         t["dp1"] = torch.empty_like(t["p1"])
-        t["dq1"] = torch.empty_like(t["p1"])
-        t["dy1"] = torch.empty_like(t["a1"])
+        t["da1"] = torch.empty_like(t["a1"])
         self.t = t
         s1 = shape_of(t["x"].shape, self.P["conv1_w"].shape, c1.stride, c1.pad)
         s2 = shape_of(t["p1"].shape, self.P["conv2_w"].shape, c2.stride, c2.pad)
@@ -159,22 +158,19 @@ class LeNet5:
             matmul(dz, P["fc%d_w" % i], 2, C=dh, stream=st)
             if i > 1:
                 relu_bwd(dh, t["h%d" % (i - 1)], dx=t["dz%d" % (i - 1)], stream=st)
-        # conv2 block.  The ReLU mask is applied to the pooled gradient before it
-        # is routed: a window's pooled value is the ReLU output at its argmax, so
-        # masking by p > 0 keeps exactly the terms that reach positions with
-        # a > 0 and zeroes the rest (the same values as masking after the
-        # routing, up to the sign of a zero), over a tensor four times smaller.
-        relu_bwd(t["dp2"], t["p2"], dx=t["dq2"], stream=st)
-        maxpool2d_bwd(t["dq2"], t["i2"], t["a2"].shape, *c2.pool, dx=t["dy2"], stream=st)
-        conv_bwd_filter_bias(t["p1"], t["dy2"], P["conv2_w"].shape, c2.stride, c2.pad, dw=G["conv2_w"],
-                             db=G["conv2_b"], workspace=ws, stream=st)
-        conv_bwd_data(P["conv2_w"], t["dy2"], t["p1"].shape, c2.stride, c2.pad, dx=t["dp1"], workspace=ws,
-                      stream=st)
+        # conv2 block: route the pooled gradient to the ReLU output, then the
+        # convolution's gradients with the ReLU mask (a2 > 0) applied as they
+        # read it -- the page's order (pool backward, relu_grad, conv backward)
+        # with the relu_grad pass fused away
+        maxpool2d_bwd(t["dp2"], t["i2"], t["a2"].shape, *c2.pool, dx=t["da2"], stream=st)
+        conv_bwd_filter_bias(t["p1"], t["da2"], P["conv2_w"].shape, c2.stride, c2.pad, dw=G["conv2_w"],
+                             db=G["conv2_b"], workspace=ws, stream=st, relu_mask=t["a2"])
+        conv_bwd_data(P["conv2_w"], t["da2"], t["p1"].shape, c2.stride, c2.pad, dx=t["dp1"], workspace=ws,
+                      stream=st, relu_mask=t["a2"])
         # conv1 block
-        relu_bwd(t["dp1"], t["p1"], dx=t["dq1"], stream=st)
-        maxpool2d_bwd(t["dq1"], t["i1"], t["a1"].shape, *c1.pool, dx=t["dy1"], stream=st)
-        conv_bwd_filter_bias(t["x"], t["dy1"], P["conv1_w"].shape, c1.stride, c1.pad, dw=G["conv1_w"],
-                             db=G["conv1_b"], workspace=ws, stream=st)
+        maxpool2d_bwd(t["dp1"], t["i1"], t["a1"].shape, *c1.pool, dx=t["da1"], stream=st)
+        conv_bwd_filter_bias(t["x"], t["da1"], P["conv1_w"].shape, c1.stride, c1.pad, dw=G["conv1_w"],
+                             db=G["conv1_b"], workspace=ws, stream=st, relu_mask=t["a1"])
         # SGD over every parameter at once
         sgd_step(self.flat_p, self.flat_g, self.lr, self.clip, stream=st)
 

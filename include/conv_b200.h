@@ -125,6 +125,25 @@ int conv_bwd_filter(const conv_shape_t *s, const float *x, const float *dy, floa
 int conv_bwd_filter_bias(const conv_shape_t *s, const float *x, const float *dy, float *dw, float *db,
                          void *workspace, size_t workspace_bytes, conv_stream_t stream);
 
+/* The two gradient calls above with the ReLU gradient that precedes them fused
+ * in (shader table "Activation / Loss Shaders": nn_relu_grad, grad * (x > 0)).
+ * For a layer followed by a ReLU, a = the ReLU's output (or its input: both
+ * are > 0 at the same positions) and dy = the gradient at the ReLU's output;
+ * the convolution's own output gradient is G = dy * (a > 0), an fp32 product
+ * with 1 or 0 -- exactly relu_bwd(dy, a) -- and it is formed where dy is
+ * first read (the gather of the input gradient, or the re-layout of dy that
+ * the filter gradient and the bias sums read), so no separate pass over dy
+ * runs.  Results equal conv_bwd_data / conv_bwd_filter_bias on relu_bwd's
+ * output.
+ *   a [batch][outC][outH][outW] (same shape as dy; read only)
+ *   conv_bwd_filter_bias_relu: db may be NULL (filter gradient only).
+ *   workspace: conv_b200_workspace_bytes(CONV_OP_BWD_DATA or CONV_OP_BWD_FILTER, s),
+ *   the same sizes as the unfused calls.  Errors as the unfused calls. */
+int conv_bwd_data_relu(const conv_shape_t *s, const float *w, const float *dy, const float *a, float *dx,
+                       void *workspace, size_t workspace_bytes, conv_stream_t stream);
+int conv_bwd_filter_bias_relu(const conv_shape_t *s, const float *x, const float *dy, const float *a, float *dw,
+                              float *db, void *workspace, size_t workspace_bytes, conv_stream_t stream);
+
 /* Bias gradient.  Page section "Convolution: The im2col Approach", backward:
  * the sum of grad_reshaped over its columns, i.e. over batch, outH and outW.
  * Fixed-order reduction (deterministic).

@@ -190,20 +190,19 @@ def test_lenet_step_operation_by_operation(cb, orc, lenet_run):
         tol(dh, *orc.matmul(dz, P0["fc%d_w" % i], 2), "dX fc%d" % i)
         if i > 1:
             assert np.array_equal(t["dz%d" % (i - 1)], orc.relu_grad(dh, t["h%d" % (i - 1)])), i
-    # conv blocks: the ReLU mask on the pooled gradient, then routing; equal (up
-    # to the sign of a zero, which == ignores) to routing, then the page's mask
+    # conv blocks: the pooled gradient routed to the ReLU output (bit-exact),
+    # then the convolution gradients with the ReLU mask fused in, against the
+    # oracle's relu_grad followed by its backward convolution
     dp2 = t["df"].reshape(t["p2"].shape)
-    assert np.array_equal(t["dq2"], orc.relu_grad(dp2, t["p2"]))
-    assert np.array_equal(t["dy2"], orc.maxpool_bwd(t["dq2"], t["i2"], t["a2"].shape))
-    assert np.array_equal(t["dy2"], orc.relu_grad(orc.maxpool_bwd(dp2, t["i2"], t["a2"].shape), t["a2"]))
-    tol(G["conv2_w"], *orc.conv_bwd_filter(t["p1"], t["dy2"], P0["conv2_w"].shape, c2.stride, c2.pad), "dW conv2")
-    tol(G["conv2_b"], *orc.conv_bwd_bias(t["dy2"]), "db conv2")
-    tol(t["dp1"], *orc.conv_bwd_data(P0["conv2_w"], t["dy2"], t["p1"].shape, c2.stride, c2.pad), "dX conv2")
-    assert np.array_equal(t["dq1"], orc.relu_grad(t["dp1"], t["p1"]))
-    assert np.array_equal(t["dy1"], orc.maxpool_bwd(t["dq1"], t["i1"], t["a1"].shape))
-    assert np.array_equal(t["dy1"], orc.relu_grad(orc.maxpool_bwd(t["dp1"], t["i1"], t["a1"].shape), t["a1"]))
-    tol(G["conv1_w"], *orc.conv_bwd_filter(x, t["dy1"], P0["conv1_w"].shape, c1.stride, c1.pad), "dW conv1")
-    tol(G["conv1_b"], *orc.conv_bwd_bias(t["dy1"]), "db conv1")
+    assert np.array_equal(t["da2"], orc.maxpool_bwd(dp2, t["i2"], t["a2"].shape))
+    dy2 = orc.relu_grad(t["da2"], t["a2"])
+    tol(G["conv2_w"], *orc.conv_bwd_filter(t["p1"], dy2, P0["conv2_w"].shape, c2.stride, c2.pad), "dW conv2")
+    tol(G["conv2_b"], *orc.conv_bwd_bias(dy2), "db conv2")
+    tol(t["dp1"], *orc.conv_bwd_data(P0["conv2_w"], dy2, t["p1"].shape, c2.stride, c2.pad), "dX conv2")
+    assert np.array_equal(t["da1"], orc.maxpool_bwd(t["dp1"], t["i1"], t["a1"].shape))
+    dy1 = orc.relu_grad(t["da1"], t["a1"])
+    tol(G["conv1_w"], *orc.conv_bwd_filter(x, dy1, P0["conv1_w"].shape, c1.stride, c1.pad), "dW conv1")
+    tol(G["conv1_b"], *orc.conv_bwd_bias(dy1), "db conv1")
 
     # SGD, bit-exact on the GPU's own gradients
     lr, clip = synthetic.LENET_SGD

@@ -203,6 +203,34 @@ def test_conv_bwd_filter_bias(cb, orc, shape):
     assert_within_tol(db.numpy(), ref_b, ref_b_abs, "conv_bwd_filter_bias db %s" % (shape,))
 
 
+@pytest.mark.parametrize("shape", CONV_SHAPES)
+def test_conv_bwd_relu_fused(cb, orc, shape):
+    """conv_bwd_data_relu and conv_bwd_filter_bias_relu: the ReLU gradient
+    (nn_relu_grad) applied where dy is read.  Against the oracle's relu_grad
+    followed by its backward convolution, within the contraction tolerance;
+    the filter and bias gradients also bit for bit equal to the unfused call
+    on relu_bwd's output (same kernels, same sums)."""
+    x, w, _, dy = conv_inputs(shape, 500)
+    st, pad = shape[6], shape[7]
+    a = synthetic.relu_normal(dy.shape, 501)          # a ReLU output: about half exact zeros
+    g = orc.relu_grad(dy, a)
+    ref_x, ref_x_abs = orc.conv_bwd_data(w, g, x.shape, st, pad)
+    ref_w, ref_w_abs = orc.conv_bwd_filter(x, g, w.shape, st, pad)
+    ref_b, ref_b_abs = orc.conv_bwd_bias(g)
+    xd, wd, dyd, ad = dev_in(x), dev_in(w), dev_in(dy), dev_in(a)
+    dx, dw, db = dev_out(x.shape), dev_out(w.shape), dev_out(ref_b.shape)
+    cb.conv_bwd_data(wd.t, dyd.t, x.shape, st, pad, dx=dx.t, relu_mask=ad.t)
+    cb.conv_bwd_filter_bias(xd.t, dyd.t, w.shape, st, pad, dw=dw.t, db=db.t, relu_mask=ad.t)
+    gd = cb.relu_bwd(dyd.t, ad.t)
+    dw0, db0 = cb.conv_bwd_filter_bias(xd.t, gd, w.shape, st, pad)
+    sync_check(cb)
+    assert dx.guards_intact() and dw.guards_intact() and db.guards_intact()
+    assert_within_tol(dx.numpy(), ref_x, ref_x_abs, "conv_bwd_data_relu %s" % (shape,))
+    assert_within_tol(dw.numpy(), ref_w, ref_w_abs, "conv_bwd_filter_bias_relu dw %s" % (shape,))
+    assert_within_tol(db.numpy(), ref_b, ref_b_abs, "conv_bwd_filter_bias_relu db %s" % (shape,))
+    assert np.array_equal(dw.numpy(), dw0.cpu().numpy()) and np.array_equal(db.numpy(), db0.cpu().numpy())
+
+
 @pytest.mark.parametrize("shape", CONV_SHAPES[:4])
 def test_conv_bwd_bias(cb, orc, shape):
     _, _, _, dy = conv_inputs(shape, 400)
