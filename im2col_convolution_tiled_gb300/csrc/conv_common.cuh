@@ -80,6 +80,57 @@ __global__ void __launch_bounds__(kBimageThreads) build_bimage_kernel(Gen gen, i
     }
 }
 
+// The same image in 16-deep blocks with 64-byte rows (the flat kernel's B
+// operand, gemm_flat.cuh): img[n_tile][block][2 * bn rows][16] -- the hi rows
+// 0..bn-1 then the lo rows bn..2bn-1 of the block, each row one 64-byte
+// swizzled K-major row (16-byte chunk j of row r at (j ^ ((r >> 1) & 3)) * 16).
+// A flat K stage is two consecutive blocks (two taps).
+template <class Gen>
+__global__ void __launch_bounds__(kBimageThreads) build_bimage16_kernel(Gen gen, int n_rows, int k_total, int bn,
+                                                                        int k_stages, float* img)
+{
+    griddep_wait();
+    griddep_launch();
+    const int row = blockIdx.y;
+    const int nt = row / bn, r = row % bn;
+    const int chunks = k_stages * 4;   // 4-value chunks of one row
+    for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < chunks; t += gridDim.x * blockDim.x) {
+        const int k0 = t * 4;
+        uint32_t hi[4], lo[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float v = (row < n_rows && k0 + e < k_total) ? gen(row, k0 + e) : 0.f;
+            split_tf32(v, hi[e], lo[e]);
+        }
+        const int ks = t >> 2, c = t & 3;
+        float* blk = img + (size_t(nt) * k_stages + ks) * 2 * size_t(bn) * 16;
+        const uint32_t oh = (uint32_t(r) * 64u + ((uint32_t(c) ^ ((uint32_t(r) >> 1) & 3u)) << 4)) / 4u;
+        const uint32_t ol = (uint32_t(r + bn) * 64u + ((uint32_t(c) ^ ((uint32_t(r + bn) >> 1) & 3u)) << 4)) / 4u;
+        *reinterpret_cast<uint4*>(blk + oh) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(blk + ol) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+}
+
+// Floats of build_bimage16's image: n_tiles x k_stages stages of 2 * bn x 16.
+inline size_t bimage16_floats(int n_rows, int k_stages, int bn)
+{
+    return size_t((n_rows + bn - 1) / bn) * size_t(k_stages) * 2 * size_t(bn) * 16;
+}
+
+template <class Gen>
+cudaError_t build_bimage16(const Gen& gen, int n_rows, int k_stages, int bn, float* img, cudaStream_t st)
+{
+    const int n_tiles = (n_rows + bn - 1) / bn;
+    const int chunks = k_stages * 4;
+    int bx = (chunks + kBimageThreads - 1) / kBimageThreads;
+    if (bx > 1024) bx = 1024;
+    cudaError_t le = launch_pdl(build_bimage16_kernel<Gen>, dim3(bx, n_tiles * bn), dim3(kBimageThreads), 0, st, gen,
+                                n_rows, k_stages * 16, bn, k_stages, img);
+    if (le != cudaSuccess) return le;
+    note_launch();
+    return cudaGetLastError();
+}
+
 // Blocks per row of build_bimage (so callers can size the row-sum partials).
 inline int bimage_grid_x(int k_total)
 {

@@ -32,338 +32,10 @@
 // decode shared across the warp.  The B operand (filters, rearranged and
 // zero-padded to the same K order) is laid out once per call as pre-split
 // hi/lo tiles and fed by bulk copies.
-#include "conv_common.cuh"
+#include "conv_window.cuh"
 #include "gemm_patch.cuh"
 
 namespace cb200 {
-
-struct GatherGeom {
-    const float* in;         // gathered tensor [Nb][Ci][Hi][Wi]
-    const float* mask;       // null, or a tensor shaped like `in`: each gathered value is multiplied by
-                             // (mask > 0) as it is loaded (nn_relu_grad fused into the input gradient)
-    int Ci, Hi, Wi, HiWi, CiHiWi;
-    int Gp, Gq, M;           // row grid per image and rows in all (Nb * Gp * Gq)
-    int sp;                  // window stride on the input
-    int o;                   // window origin offset: h = p*sp + o + tap_r
-    int T;                   // taps per axis
-    int mode;                // K order: 0 chunk of one tap, 1 tap group (Ci <= 16), 2 generic
-    int Cp, lcp;             // padded channels (modes 0/1) and log2 Cp (mode 1)
-    int K;                   // reduction length: T*T*Cp (modes 0/1), T*T*Ci (mode 2)
-    FastDiv f_gpq, f_gq;     // row decode
-    FastDiv f_cchunks;       // Cp / 32 (mode 0)
-    FastDiv f_tt, f_t;       // T*T and T
-};
-
-// K order of a gather over a tensor with `ci` channels (see top of file).
-static inline void k_order(int ci, int* mode, int* cp, int* lcp)
-{
-    if (ci % 32 == 0 || (ci > 16 && ci < 32)) {
-        *mode = 0;
-        *cp = (ci + 31) / 32 * 32;
-        *lcp = 0;
-    } else if (ci < 32) {
-        int l = 0;
-        while ((1 << l) < ci) ++l;
-        *mode = 1;
-        *cp = 1 << l;
-        *lcp = l;
-    } else {
-        *mode = 2;
-        *cp = ci;
-        *lcp = 0;
-    }
-}
-
-struct OutGeom {
-    float* out;              // [Nb][Co][Ho][Wo]
-    const float* bias;       // [Co] or null
-    int relu;                // forward only: max(0, .) after the bias (nn_relu fused into the epilogue)
-    int Co, Ho, Wo, HoWo;
-    int so;                  // output phase stride (1: plain NCHW)
-    int oo;                  // phase offset: row p's phase block starts at output row p * so - oo (0 <= oo < so)
-    int ncols;               // Co * so * so
-    int vec;                 // 1: so = 2 or 4, oo = 0, Wo % so == 0, out 16-byte aligned: each (ch, a) row of
-                             //    so phases is one float2 / float4 store
-                             // 2: so = 4, oo = 2, Wo even, out 8-byte aligned: two float2 stores per (ch, a)
-};
-
-template <int BN>
-struct ConvGatherProb {
-    static constexpr bool kBBulk = true;
-    int terms = 3;                                // tensor-core products per K step: 3 (3xTF32) or 1 (TF32)
-    // A stages in tensor memory up to 128 columns (two accumulators still fit).
-    // Wider tiles keep A in shared memory: with A in tensor memory they would
-    // keep a single accumulator, and measured 5-20% slower on the AlexNet layers.
-    static constexpr bool kATmem = BN <= 128;
-    static constexpr int kGroups = 2;
-    static constexpr Map kAMap = Map::RowFast;
-    static constexpr Map kBMap = Map::RowFast;   // unused (bulk)
-
-    GatherGeom g;
-    OutGeom o;
-    const float* bimg;
-    int m_tiles, n_tiles, k_stages;
-    // Tail split (see plan_tail): units [0, full_units) are whole tiles; each
-    // later tile is cut along K into tail_split pieces whose partial sums go
-    // to part_buf [piece][kBM][BN] and are added by tail_reduce_kernel.
-    int full_units = 0, tail_split = 1;
-    float* part_buf = nullptr;
-
-    __device__ int num_tiles() const { return full_units + (m_tiles * n_tiles - full_units) * tail_split; }
-    __device__ Tile whole_tile(int t) const
-    {
-        Tile r;
-        r.n0 = (t % n_tiles) * BN;
-        r.m0 = (t / n_tiles) * kBM;
-        r.ks0 = 0;
-        r.ks1 = k_stages;
-        r.grp = t % n_tiles;
-        return r;
-    }
-    __device__ Tile tile(int t) const
-    {
-        if (t < full_units) return whole_tile(t);
-        const int u = t - full_units;
-        const int j = u % tail_split;
-        Tile r = whole_tile(full_units + u / tail_split);
-        r.ks0 = int((long long)j * k_stages / tail_split);
-        r.ks1 = int((long long)(j + 1) * k_stages / tail_split);
-        r.part = u;
-        return r;
-    }
-
-    struct AState {
-        int base;      // offset of in[n][0][h0][w0]
-        int h0, w0;    // window origin of this row
-    };
-    __device__ AState a_setup(const Tile& tl, int tid) const
-    {
-        AState s;
-        const int m = tl.m0 + tid;
-        if (m < g.M) {
-            uint32_t n, pq, p, q;
-            g.f_gpq.divmod(uint32_t(m), n, pq);
-            g.f_gq.divmod(pq, p, q);
-            s.h0 = int(p) * g.sp + g.o;
-            s.w0 = int(q) * g.sp + g.o;
-            s.base = int(n) * g.CiHiWi + s.h0 * g.Wi + s.w0;
-        } else {
-            s.h0 = -(1 << 24);   // no window position is ever inside
-            s.w0 = 0;
-            s.base = 0;
-        }
-        return s;
-    }
-
-    // Mode 1: 32 / CP taps per stage, CP channels each.
-    template <int LCP>
-    __device__ __forceinline__ void load_taps(const AState& s, int ks, float (&v)[32]) const
-    {
-        constexpr int CP = 1 << LCP, TPS = 32 >> LCP;
-        const int TT = g.T * g.T;
-#pragma unroll
-        for (int t = 0; t < TPS; ++t) {
-            const int tap = ks * TPS + t;
-            uint32_t tr, tq;
-            g.f_t.divmod(uint32_t(tap), tr, tq);
-            const int h = s.h0 + int(tr);
-            const int w = s.w0 + int(tq);
-            const bool ok = tap < TT && unsigned(h) < unsigned(g.Hi) && unsigned(w) < unsigned(g.Wi);
-            const int off = s.base + int(tr) * g.Wi + int(tq);
-            const float* p = g.in + off;
-            if (g.mask == nullptr) {
-#pragma unroll
-                for (int c = 0; c < CP; ++c) v[t * CP + c] = ldg_keep_if(p + c * g.HiWi, ok && c < g.Ci);
-            } else {
-                const float* mp = g.mask + off;
-#pragma unroll
-                for (int c = 0; c < CP; ++c)
-                    v[t * CP + c] = ldg_keep_if(p + c * g.HiWi, ok && c < g.Ci) *
-                                    relu_gate(ldg_keep_if(mp + c * g.HiWi, ok && c < g.Ci));
-            }
-        }
-    }
-
-    __device__ void load_a(const AState& s, const Tile&, int ks, int tid, float (&v)[32]) const
-    {
-        if (g.mode == 0) {
-            // One tap, 32 consecutive channels.
-            uint32_t tap, chunk, tr, tq;
-            g.f_cchunks.divmod(uint32_t(ks), tap, chunk);
-            g.f_t.divmod(tap, tr, tq);
-            const int h = s.h0 + int(tr);
-            const int w = s.w0 + int(tq);
-            const bool ok = unsigned(h) < unsigned(g.Hi) && unsigned(w) < unsigned(g.Wi);
-            const int cleft = g.Ci - int(chunk) * 32;   // channels of this chunk that exist
-            const int off = s.base + int(chunk) * 32 * g.HiWi + int(tr) * g.Wi + int(tq);
-            const float* p = g.in + off;
-            if (g.mask == nullptr) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = ldg_keep_if(p + i * g.HiWi, ok && i < cleft);
-            } else {
-                const float* mp = g.mask + off;
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    v[i] = ldg_keep_if(p + i * g.HiWi, ok && i < cleft) *
-                           relu_gate(ldg_keep_if(mp + i * g.HiWi, ok && i < cleft));
-            }
-        } else if (g.mode == 1) {
-            switch (g.lcp) {
-            case 0: load_taps<0>(s, ks, v); break;
-            case 1: load_taps<1>(s, ks, v); break;
-            case 2: load_taps<2>(s, ks, v); break;
-            case 3: load_taps<3>(s, ks, v); break;
-            default: load_taps<4>(s, ks, v); break;
-            }
-        } else {
-            // Generic order: lane l decodes k = ks*32 + l, the warp shares it.
-            const int k = ks * kBK + (tid & 31);
-            int koff = 0, krs = 0x7FFF0000;   // past K: the tap lands far outside
-            if (k < g.K) {
-                uint32_t c, rem, r, q;
-                g.f_tt.divmod(uint32_t(k), c, rem);
-                g.f_t.divmod(rem, r, q);
-                koff = int(c) * g.HiWi + int(r) * g.Wi + int(q);
-                krs = int((r << 16) | q);
-            }
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int off = __shfl_sync(0xffffffffu, koff, i);
-                const int rs = __shfl_sync(0xffffffffu, krs, i);
-                const int h = s.h0 + (rs >> 16);
-                const int w = s.w0 + (rs & 0xFFFF);
-                const bool in = unsigned(h) < unsigned(g.Hi) && unsigned(w) < unsigned(g.Wi);
-                v[i] = ldg_keep_if(g.in + (s.base + off), in);
-                if (g.mask != nullptr) v[i] *= relu_gate(ldg_keep_if(g.mask + (s.base + off), in));
-            }
-        }
-    }
-
-    struct BState {};
-    __device__ BState b_setup(const Tile&, int) const { return {}; }
-    __device__ void load_b(const BState&, const Tile&, int, int, int, float (&)[32]) const {}
-    __device__ const float* b_image(const Tile& tl, int ks) const
-    {
-        return bimg + (size_t(tl.grp) * k_stages + ks) * 2 * size_t(BN) * kBK;
-    }
-
-    struct EState {
-        float* opix;   // out[n][0][h][w], (h, w) = (p*so - oo, q*so - oo): may lie before the row/image
-        bool valid;
-        int hrem, wrem;   // rows/cols of the output left below/right of this pixel's phase block
-        int hmin, wmin;   // phases a < hmin (b < wmin) fall above (left of) the output: -h, -w
-    };
-    __device__ EState e_setup(const Tile& tl, int row) const
-    {
-        EState e;
-        const int m = tl.m0 + row;
-        e.valid = m < g.M;
-        uint32_t n = 0, pq = 0, p = 0, q = 0;
-        if (e.valid) {
-            g.f_gpq.divmod(uint32_t(m), n, pq);
-            g.f_gq.divmod(pq, p, q);
-        }
-        const int h = int(p) * o.so - o.oo, w = int(q) * o.so - o.oo;
-        e.hrem = o.Ho - h;
-        e.wrem = o.Wo - w;
-        e.hmin = -h;
-        e.wmin = -w;
-        e.opix = o.out + (ptrdiff_t(n) * o.Co * o.HoWo + ptrdiff_t(h) * o.Wo + w);
-        return e;
-    }
-
-    // epilogue of split trailing tile b, once its pieces are summed
-    __device__ void reduce_store(int b, int row, int c0, const uint32_t (&r)[32]) const;
-
-    __device__ void store(const EState& e, const Tile& tl, int row, int c0, const uint32_t (&r)[32]) const
-    {
-        if (tl.part >= 0) {
-            float4* d = reinterpret_cast<float4*>(part_buf + (size_t(tl.part) * kBM + row) * BN + c0);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                d[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                   __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
-            return;
-        }
-        if (o.so == 1) {
-            // the 32 columns' biases: lane i loads column c0 + i once and the
-            // warp shares them (every epilogue lane calls store, valid row or not)
-            const int chl = tl.n0 + c0 + int(threadIdx.x & 31);
-            const float bl = (o.bias && chl < o.Co) ? __ldg(o.bias + chl) : 0.f;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float bias = __shfl_sync(0xffffffffu, bl, i);
-                const int ch = tl.n0 + c0 + i;
-                if (e.valid && ch < o.Co) {
-                    const float v = __uint_as_float(r[i]) + bias;
-                    e.opix[size_t(ch) * o.HoWo] = o.relu && !(v > 0.f) ? 0.f : v;
-                }
-            }
-            return;
-        }
-        if (!e.valid) return;
-        if (o.vec == 2) {
-            // so = 4, oo = 2: the four phases b of one (ch, a) are output
-            // columns w .. w + 3 with w = 4q - 2 (even): two 8-byte-aligned
-            // pairs, the first left of the image when q = 0, the second right
-            // of it when w + 2 = Wo
-#pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-                const int col = tl.n0 + c0 + i;
-                const int ch = col >> 4, a = (col >> 2) & 3;
-                if (ch < o.Co && a < e.hrem && a >= e.hmin) {
-                    float* rowp = e.opix + (size_t(ch) * o.HoWo + a * o.Wo);
-                    if (e.wmin <= 0)
-                        *reinterpret_cast<float2*>(rowp) = make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1]));
-                    if (e.wrem > 2)
-                        *reinterpret_cast<float2*>(rowp + 2) =
-                            make_float2(__uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
-                }
-            }
-        } else if (o.vec) {
-            // columns (ch, a, b) with b fastest: the so phases b of one (ch, a)
-            // are so adjacent columns and so adjacent floats of output row
-            // h + a (oo = 0 and w = so * q is a multiple of so, so wrem >= so)
-            if (o.so == 4) {
-#pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    const int col = tl.n0 + c0 + i;
-                    const int ch = col >> 4, a = (col >> 2) & 3;
-                    if (ch < o.Co && a < e.hrem)
-                        *reinterpret_cast<float4*>(e.opix + size_t(ch) * o.HoWo + a * o.Wo) =
-                            make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]), __uint_as_float(r[i + 2]),
-                                        __uint_as_float(r[i + 3]));
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const int col = tl.n0 + c0 + i;
-                    const int ch = col >> 2, a = (col >> 1) & 1;
-                    if (ch < o.Co && a < e.hrem)
-                        *reinterpret_cast<float2*>(e.opix + size_t(ch) * o.HoWo + a * o.Wo) =
-                            make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1]));
-                }
-            }
-        } else {
-            const int ss = o.so * o.so;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int col = tl.n0 + c0 + i;
-                const int ch = col / ss, ab = col - ch * ss;
-                const int a = ab / o.so, b = ab - a * o.so;
-                if (ch < o.Co && a < e.hrem && b < e.wrem && a >= e.hmin && b >= e.wmin)
-                    e.opix[size_t(ch) * o.HoWo + a * o.Wo + b] = __uint_as_float(r[i]);
-            }
-        }
-    }
-};
-
-template <int BN>
-__device__ void ConvGatherProb<BN>::reduce_store(int b, int row, int c0, const uint32_t (&r)[32]) const
-{
-    const Tile tl = whole_tile(full_units + b);
-    store(e_setup(tl, row), tl, row, c0, r);
-}
 
 // The same GEMMs on the patch-staged kernel (gemm_patch.cuh): tiles never
 // straddle images, and the K order is chunk-major in 32-channel chunks (or tap
@@ -454,9 +126,10 @@ struct ConvPatchProb {
 // K index -> (channel of the gathered tensor, tap index) in one of the three
 // orders the gathers use.
 struct KDecode {
-    int order;         // 0: tap-major, channels padded to Cp fastest; 1: 32-channel chunk, tap, channel; 2: channel, tap
+    int order;         // 0: tap-major, channels padded to Cp fastest; 1: 32-channel chunk, tap, channel; 2: channel, tap;
+                       // 3: 16-channel chunk, tap, channel (the flat kernel)
     FastDiv f_cp;      // order 0: Cp
-    FastDiv f_chunk;   // order 1: T*T*32
+    FastDiv f_chunk;   // order 1: T*T*32; order 3: T*T*16
     FastDiv f_tt;      // order 2: T*T
     // order 1 with a half last chunk (the patch kernel's two-tap stages): from
     // K index half_k0 on, stage j holds taps 2j and 2j + 1, channels
@@ -477,6 +150,10 @@ struct KDecode {
             f_chunk.divmod(uint32_t(kk), a, b);
             tap = int(b) >> 5;
             c = int(a) * 32 + (int(b) & 31);
+        } else if (order == 3) {
+            f_chunk.divmod(uint32_t(kk), a, b);
+            tap = int(b) >> 4;
+            c = int(a) * 16 + (int(b) & 15);
         } else {
             f_tt.divmod(uint32_t(kk), a, b);
             c = int(a);
@@ -490,7 +167,7 @@ static KDecode make_kdecode(int order, int cp, int T)
     KDecode d{};
     d.order = order;
     d.f_cp = FastDiv(uint32_t(cp > 0 ? cp : 1));
-    d.f_chunk = FastDiv(uint32_t(T * T * 32));
+    d.f_chunk = FastDiv(uint32_t(T * T * (order == 3 ? 16 : 32)));
     d.f_tt = FastDiv(uint32_t(T * T));
     return d;
 }
@@ -1008,6 +685,103 @@ static cudaError_t setup_patch_tma(PatchGeom& pg, float* blocked, cudaStream_t s
 }
 
 // ---------------------------------------------------------------------------
+// The flat kernel (gemm_flat.cuh): a stride-1 window of at least 2 x 2 taps
+// over a channel-blocked tensor of at least 16 channels, at most 64 output
+// columns (one column tile, BN = the columns rounded up to 16), box and
+// stages within shared memory.
+
+struct FlatPlan {
+    bool use;
+    int bn;
+    FlatGeom fg;
+};
+
+// The flat kernel runs the forward of a strided few-channel layer in its
+// space-to-depth form (AlexNet conv1: 48 channels, 3 x 3 taps, 64 filters),
+// where it measured faster than the patch kernel (176 vs 184 us per call in
+// 3xTF32, 164 vs 167 us in TF32).  On the input gradients, whose operand
+// traffic the patch kernel splits between tensor and shared memory, it was
+// slower (conv1 204 vs 178 us, conv2 322 vs 271 us), so they stay on the
+// patch kernel.
+static FlatPlan plan_flat(int Nb, int Ci, int Hi, int Wi, int Gp, int Gq, int o, int T, int ncols)
+{
+    FlatPlan f{};
+    f.use = false;
+    if (T < 2 || Ci < 16 || ncols > 64) return f;
+    f.bn = (ncols + 15) / 16 * 16;
+    FlatGeom& g = f.fg;
+    g.Nb = Nb;
+    g.Ci = Ci;
+    g.Hi = Hi;
+    g.Wi = Wi;
+    g.Cb = (Ci + 31) / 32;
+    g.nch = (Ci + 15) / 16;
+    g.Gp = Gp;
+    g.Gq = Gq;
+    g.o = o;
+    g.T = T;
+    g.TT = T * T;
+    g.spc = (g.TT + 1) / 2;
+    g.Wt = Gq + T - 1;
+    g.Rb = flat_box_rows(g.Wt, T);
+    if (g.Wt > 256 || g.Rb > 256) return f;
+    g.vpi = Gp * g.Wt;
+    g.tpi = (g.vpi + kBM - 1) / kBM;
+    g.box_bytes = uint32_t(g.Rb) * uint32_t(g.Wt) * 64u;
+    g.box_stride = (g.box_bytes + 1023u) & ~1023u;
+    size_t smem = 0;
+    switch (f.bn) {
+    case 16: smem = flat_smem<16>(g.box_stride); break;
+    case 32: smem = flat_smem<32>(g.box_stride); break;
+    case 48: smem = flat_smem<48>(g.box_stride); break;
+    default: smem = flat_smem<64>(g.box_stride); break;
+    }
+    if (smem > 227 * 1024) return f;
+    if ((long long)Nb * g.Cb * Hi * Wi * 32 >= (1LL << 31)) return f;   // 32-bit element offsets in the copy
+    g.f_wt = FastDiv(uint32_t(g.Wt));
+    g.f_t = FastDiv(uint32_t(T));
+    g.f_tt = FastDiv(uint32_t(g.TT));
+    f.use = true;
+    return f;
+}
+
+// The B image: 2 * spc taps (the last padded with zeros when T*T is odd) of
+// each 16-channel chunk, one 16-deep block per tap.
+static int flat_kblocks(const FlatGeom& g) { return 2 * flat_kstages(g); }
+
+static size_t flat_img_bytes(const FlatPlan& f, int ncols)
+{
+    return round_up_256(bimage16_floats(ncols, flat_kblocks(f.fg), f.bn) * sizeof(float));
+}
+
+// K decode of the flat image: 16-channel chunk, tap (of 2 * spc), channel.
+static KDecode flat_kdecode(const FlatGeom& g)
+{
+    KDecode d = make_kdecode(3, 1, g.T);
+    d.f_chunk = FastDiv(uint32_t(2 * g.spc * 16));
+    return d;
+}
+
+static size_t flat_blocked_bytes(const FlatGeom& g) { return size_t(g.Nb) * g.Cb * g.Hi * g.Wi * 32 * sizeof(float); }
+
+// The box of one (tile, 16-channel chunk) from the channel-blocked copy:
+// 16 channels (64 bytes, 64-byte swizzle) x Wt columns x Rb rows.
+static cudaError_t encode_flat_tmap(FlatGeom& g, float* blocked)
+{
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[4] = {32, cuuint64_t(g.Wi), cuuint64_t(g.Hi), cuuint64_t(g.Nb) * g.Cb};
+    const cuuint64_t strides[3] = {128, cuuint64_t(g.Wi) * 128, cuuint64_t(g.Hi) * g.Wi * 128};
+    const cuuint32_t box[4] = {16, cuuint32_t(g.Wt), cuuint32_t(g.Rb), 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUresult r = enc(&g.tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, blocked, dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+
+// ---------------------------------------------------------------------------
 // Forward convolution with stride S > 1 and few channels, as a stride-1
 // convolution over S x S super-pixels (space to depth):
 //   y[n, k, p, q] = sum_(c', tr, tq) X'[n, c', p + tr, q + tq] * W'[k, c', tr, tq]
@@ -1021,6 +795,7 @@ struct S2dPlan {
     bool use;
     int bn, T, Ci;
     PatchGeom pg;
+    FlatPlan fp;   // the flat kernel over the same space-to-depth copy, when it applies
 };
 
 static S2dPlan plan_fwd_s2d(const ConvDims& d)
@@ -1037,6 +812,11 @@ static S2dPlan plan_fwd_s2d(const ConvDims& d)
     if ((long long)d.N * ((sp.Ci + 31) / 32) * 32 * (d.P + sp.T - 1) * (d.Q + sp.T - 1) >= (1LL << 31))
         return sp;   // the channel-blocked copy is indexed with 32-bit element offsets
     sp.pg = make_patch(nullptr, d.N, sp.Ci, d.P + sp.T - 1, d.Q + sp.T - 1, d.P, d.Q, 1, 0, sp.T);
+    sp.fp = plan_flat(d.N, sp.Ci, d.P + sp.T - 1, d.Q + sp.T - 1, d.P, d.Q, 0, sp.T, d.K);
+    if (sp.fp.use) {
+        sp.use = true;
+        return sp;
+    }
     if (sp.pg.mode != 0) return sp;
     patch_box(sp.pg);
     set_half_chunk(sp.pg);
@@ -1117,6 +897,7 @@ static cudaError_t run_window_gemm(const float* in, int Nb, int Ci, int Hi, int 
     const WindowPlan wp = plan_window(Nb, Ci, Hi, Wi, Gp, Gq, sp, o, T, og.ncols, mask != nullptr);
     float* img = static_cast<float*>(ws);
     const int bn = wp.bn;
+
     if (wp.patch) {
         PatchGeom pg = make_patch(in, Nb, Ci, Hi, Wi, Gp, Gq, sp, o, T);
         if (wp.tma) set_half_chunk(pg);
@@ -1148,6 +929,7 @@ static cudaError_t run_window_gemm(const float* in, int Nb, int Ci, int Hi, int 
 size_t conv_fwd_ws(const ConvDims& d)
 {
     const S2dPlan sp = plan_fwd_s2d(d);
+    if (sp.use && sp.fp.use) return flat_img_bytes(sp.fp, d.K) + flat_blocked_bytes(sp.fp.fg);
     if (sp.use)
         return round_up_256(bimage_floats(d.K, patch_kstages(sp.pg) * kBK, sp.bn) * sizeof(float)) +
                blocked_bytes(sp.pg);
@@ -1182,6 +964,20 @@ cudaError_t launch_conv_fwd(const ConvDims& d, const float* x, const float* w, c
     o.so = 1;
     o.ncols = d.K;
     S2dPlan sp = plan_fwd_s2d(d);
+    if (sp.use && sp.fp.use) {
+        FlatGeom& fg = sp.fp.fg;
+        const FwdS2dFilterGen gen{w,   d.C, d.R, d.S, flat_kdecode(fg), FastDiv(uint32_t(sp.T)),
+                                  FastDiv(uint32_t(d.S * d.S)), FastDiv(uint32_t(d.S))};
+        float* img = static_cast<float*>(ws);
+        cudaError_t e = build_bimage16(gen, d.K, flat_kblocks(fg), sp.fp.bn, img, st);
+        if (e != cudaSuccess) return e;
+        float* blocked = reinterpret_cast<float*>(static_cast<char*>(ws) + flat_img_bytes(sp.fp, d.K));
+        e = launch_s2d_copy<true>(x, blocked, d.N, d.C, d.H, d.W, d.S, d.pad, fg.Hi, fg.Wi, st);
+        if (e != cudaSuccess) return e;
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = encode_flat_tmap(fg, blocked)) != cudaSuccess) return e;
+        return dispatch_flat(sp.fp.bn, fg, o, img, st);
+    }
     if (sp.use) {
         PatchGeom& pg = sp.pg;
         const int k_total = patch_kstages(pg) * kBK;
