@@ -67,6 +67,7 @@ _SIGS = {
     "conv_b200_strerror": ([ctypes.c_int], ctypes.c_char_p),
     "conv_b200_check": ([_P], ctypes.c_int),
     "conv_b200_launch_count": ([], ctypes.c_uint64),
+    "conv_b200_debug_withhold_stage": ([ctypes.c_int64], ctypes.c_int),
     "conv_fwd_noalloc": ([_SHAPE, _P, _P, _P, _P, _P], ctypes.c_int),
     "relu_fwd": ([ctypes.c_int64, _P, _P, _P], ctypes.c_int),
     "relu_bwd": ([ctypes.c_int64, _P, _P, _P, _P], ctypes.c_int),

@@ -49,6 +49,12 @@ static std::atomic<unsigned long long> g_launches{0};
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 static std::atomic<int> g_math_mode{CONV_MATH_FP32};
+
+// Test hook of the bounded-wait error path (conv_b200_debug_withhold_stage):
+// -1, or the CTA-wide stage whose arrival CTA 0 of the next register-gather
+// GEMM launch withholds.  One-shot: the launch that takes it resets it.
+static std::atomic<long long> g_withhold_stage{-1};
+long long take_withhold_stage() { return g_withhold_stage.exchange(-1, std::memory_order_relaxed); }
 int math_terms() { return g_math_mode.load(std::memory_order_relaxed) == CONV_MATH_TF32 ? 1 : 3; }
 
 int* device_error_word()
@@ -435,6 +441,13 @@ int softmax_ce(int32_t rows, int32_t cols, const float* logits, const int32_t* l
 }
 
 uint64_t conv_b200_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int conv_b200_debug_withhold_stage(int64_t stage)
+{
+    if (stage < -1 || stage > (int64_t(1) << 30)) return CONV_ERR_SHAPE;
+    g_withhold_stage.store(stage, std::memory_order_relaxed);
+    return CONV_OK;
+}
 
 int conv_b200_set_math_mode(int mode)
 {

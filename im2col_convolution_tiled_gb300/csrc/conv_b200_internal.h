@@ -30,6 +30,10 @@ int math_terms();
 // <<<>>> launch calls note_launch()); exported as conv_b200_launch_count().
 void note_launch();
 
+// The stage set by conv_b200_debug_withhold_stage (or -1), taken -- and reset
+// to -1 -- by the next launch of the register-gather GEMM kernel.
+long long take_withhold_stage();
+
 inline cudaStream_t as_cuda(conv_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

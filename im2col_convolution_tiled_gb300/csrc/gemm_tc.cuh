@@ -35,6 +35,9 @@
 // Every wait is bounded (ptx.cuh); on give-up the kernel raises its abort
 // flag, records kDevErrTimeout in the device error word, waits for what it
 // already launched asynchronously, frees its tensor memory and returns.
+// withhold_stage (a test hook, -1 in normal use): CTA 0's producers do not
+// arrive on the "full" barrier of that CTA-wide stage, so the MMA issuer's
+// bounded wait runs out and the kernel takes the path above.
 #pragma once
 #include "ptx.cuh"
 
@@ -182,7 +185,7 @@ struct EngineRoles {
 
 template <class Prob, int BN, int TERMS>
 __global__ void __launch_bounds__(EngineRoles<Prob, BN>::R::kThreads, 1)
-    tc_gemm_kernel(const __grid_constant__ Prob prob, int* err_word)
+    tc_gemm_kernel(const __grid_constant__ Prob prob, int* err_word, int withhold_stage)
 {
     constexpr bool ATMEM = UsesTmemA<Prob>::value;
     using Cfg = TileCfg<BN, ATMEM>;
@@ -312,7 +315,7 @@ __global__ void __launch_bounds__(EngineRoles<Prob, BN>::R::kThreads, 1)
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&ctl->full[slot]);
+                    if (lane == 0 && !(blockIdx.x == 0 && int(c) == withhold_stage)) mbar_arrive(&ctl->full[slot]);
                     return true;
                 };
                 if constexpr (Prob::kBBulk) {
@@ -491,8 +494,9 @@ cudaError_t launch_tc_gemm_terms(const Prob& prob, int num_tiles, int* err_word,
     }
     if (num_tiles <= 0) return cudaSuccess;
     int grid = num_tiles < sm_count() ? num_tiles : sm_count();
+    const int withhold = int(take_withhold_stage());
     cudaError_t e = launch_pdl(tc_gemm_kernel<Prob, BN, TERMS>, dim3(grid), dim3(kThreads), Cfg::kSmemBytes, stream, prob,
-                               err_word);
+                               err_word, withhold);
     if (e != cudaSuccess) return e;
     note_launch();
     return cudaGetLastError();

@@ -318,6 +318,20 @@ uint64_t conv_b200_launch_count(void);
 int conv_fwd_noalloc(const conv_shape_t *s, const float *x, const float *w, const float *b, float *y,
                      conv_stream_t stream);
 
+/* Test hook of the bounded-wait error path; the page has no counterpart (its
+ * D3D11 runtime has no device-side waits).  Off by default.  After
+ * conv_b200_debug_withhold_stage(k) the NEXT launch of the register-gather
+ * tensor-core kernel (flagged matmul, and the convolution GEMMs that run on
+ * it) withholds, in its first CTA, the producers' arrival for CTA-wide
+ * pipeline stage k: that CTA's MMA issuer waits for a stage that never
+ * fills, gives up after its bounded wait (about 2 s), and the kernel unwinds
+ * -- it drains its own MMAs, frees its tensor memory and returns -- so the
+ * next conv_b200_check() returns CONV_ERR_DEVICE_TIMEOUT and the stream stays
+ * usable.  The results of that one launch are undefined.  One-shot: the
+ * launch that takes the setting resets it; k = -1 cancels it.  Returns
+ * CONV_OK, or CONV_ERR_SHAPE for k < -1. */
+int conv_b200_debug_withhold_stage(int64_t stage);
+
 /* Text for a return code. */
 const char *conv_b200_strerror(int code);
 

@@ -141,6 +141,27 @@ def test_math_mode_switch(lib):
     assert cb.math_mode() == cb.CONV_MATH_FP32
 
 
+def test_withhold_hook_validation(lib):
+    """The bounded-wait test hook is off by default, rejects k < -1 and can be
+    cancelled (no launch happens here)."""
+    assert lib.conv_b200_debug_withhold_stage(-2) == ERR_SHAPE
+    assert lib.conv_b200_debug_withhold_stage(3) == CONV_OK
+    assert lib.conv_b200_debug_withhold_stage(-1) == CONV_OK
+
+
+def test_relu_fused_gradient_validation(lib):
+    """conv_bwd_data_relu / conv_bwd_filter_bias_relu validate like the unfused
+    calls, including the mask pointer (db may be NULL in the filter call)."""
+    s = good_shape()
+    ws = ctypes.c_size_t(1 << 30)
+    assert lib.conv_bwd_data_relu(ctypes.byref(s), FAKE, FAKE, NULL, FAKE, FAKE, ws, None) == ERR_NULL
+    assert lib.conv_bwd_data_relu(ctypes.byref(s), FAKE, FAKE, MIS, FAKE, FAKE, ws, None) == ERR_ALIGN
+    assert lib.conv_bwd_filter_bias_relu(ctypes.byref(s), FAKE, FAKE, NULL, FAKE, NULL, FAKE, ws, None) == ERR_NULL
+    assert lib.conv_bwd_filter_bias_relu(ctypes.byref(s), FAKE, FAKE, FAKE, FAKE, MIS, FAKE, ws, None) == ERR_ALIGN
+    bad = ConvShape(2, 3, 9, 9, 4, 3, 2, 1, 6, 5)
+    assert lib.conv_bwd_data_relu(ctypes.byref(bad), FAKE, FAKE, FAKE, FAKE, FAKE, ws, None) == ERR_SHAPE
+
+
 def test_strerror(lib):
     for code in [0, -1, -2, -3, -4, -5, -6, -7, -8, -9, -10, -99]:
         assert isinstance(lib.conv_b200_strerror(code), bytes)
