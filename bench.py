@@ -1053,6 +1053,7 @@ def run_hbm(args):
 def run_case(args):
     import torch
     cb = _load_lib()
+    cb.set_math_mode(cb.CONV_MATH_TF32 if args.math == "tf32" else cb.CONV_MATH_FP32)
     layers = {L.name: L for L in synthetic.ALEXNET + synthetic.LENET + (synthetic.SINGLE,)}
     if args.op == "matmul":
         M, N, K = (int(v) for v in args.mnk.split(","))

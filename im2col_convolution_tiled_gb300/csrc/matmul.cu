@@ -116,8 +116,10 @@ struct MatmulProb {
                 }
             }
         } else {                      // B stored K x N: (n, k) at k*N + n
+            // thread tid loads tile column 128 * pass + tid: only the BN the
+            // tile has (narrower tiles would otherwise fetch columns they drop)
             const int n = tl.n0 + 128 * pass + tid;
-            const bool nv = n < N;
+            const bool nv = n < N && 128 * pass + tid < BN;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const int k = k0 + i;

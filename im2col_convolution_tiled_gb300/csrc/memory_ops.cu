@@ -1003,27 +1003,51 @@ __global__ void __launch_bounds__(kWalkThreads) maxpool_bwd_walk_kernel(
     }
 }
 
-// Rows per segment for a walker with `per_seg_items` threads per segment:
-// split planes into row segments only until about one wave of threads is
-// resident (1024 per SM at the walkers' register use), and keep at least one
-// load chunk of rows per segment.  Measured on the AlexNet pools, whole-plane
-// walks beat four waves of shorter segments (pool2 backward 0.57 -> 0.61 of
-// the copy bandwidth).
-static int walk_seglen(int rows, long long per_seg_items)
+// Rows per segment for a walker with `per_seg_items` threads per segment and
+// `resident` threads resident on the GPU at once.  The walk is latency-bound
+// (long-scoreboard stalls), so it wants every SM full until the end: of the
+// segment counts that keep at least two load chunks of rows per segment (a
+// shorter walk does not amortise its start), take the fewest whose last wave
+// of threads is nearly as full as the best (within 5 points).  AlexNet pool1:
+// one whole-plane walk per column is 1.42 waves (the second 42% full); two
+// half-plane segments are 2.84 waves (forward 0.65 -> 0.68, backward 0.56 ->
+// 0.60 of the copy bandwidth).  Pool2's 13-row planes stay whole (three
+// 5-row segments measured 0.78 -> 0.71).
+static int walk_seglen(int rows, long long per_seg_items, long long resident)
 {
-    const long long want = 1LL * sm_count() * 1024;
-    long long nseg = (want + per_seg_items - 1) / per_seg_items;
-    const long long max_seg = rows / kWalkChunk > 1 ? rows / kWalkChunk : 1;
-    if (nseg > max_seg) nseg = max_seg;
-    if (nseg < 1) nseg = 1;
-    return int((rows + nseg - 1) / nseg);
+    const long long max_seg = rows / (2 * kWalkChunk) > 1 ? rows / (2 * kWalkChunk) : 1;
+    int best = 1;
+    double best_eff = 0.0;
+    for (int nseg = 1; nseg <= max_seg && nseg <= 8; ++nseg) {
+        const double waves = double(per_seg_items) * nseg / double(resident);
+        const double eff = waves / double((long long)(waves + 0.999999));
+        if (eff > best_eff + 0.05) {
+            best_eff = eff;
+            best = nseg;
+        }
+    }
+    return (rows + best - 1) / best;
+}
+
+// Threads of a walker kernel resident on the GPU at once (from the occupancy
+// the compiled kernel allows).
+template <class Kern>
+static long long walk_resident(Kern kern)
+{
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWalkThreads, 0) != cudaSuccess || per_sm < 1) {
+        cudaGetLastError();
+        per_sm = 4;
+    }
+    return (long long)sm_count() * per_sm * kWalkThreads;
 }
 
 template <int K, int S>
 static cudaError_t launch_pool_fwd_walk(int NC, int H, int W, int P, int Q, const float* x, float* y, int32_t* idx,
                                         cudaStream_t st)
 {
-    const int seglen = walk_seglen(P, (long long)NC * Q);
+    static const long long resident = walk_resident(maxpool_fwd_walk_kernel<K, S>);
+    const int seglen = walk_seglen(P, (long long)NC * Q, resident);
     const int nseg = (P + seglen - 1) / seglen;
     const long long items = (long long)NC * nseg * Q;
     cudaError_t e = launch_pdl(maxpool_fwd_walk_kernel<K, S>, dim3(unsigned((items + kWalkThreads - 1) / kWalkThreads)),
@@ -1039,7 +1063,8 @@ static cudaError_t launch_pool_bwd_walk(int NC, int H, int W, int P, int Q, cons
                                         float* dx, cudaStream_t st)
 {
     const int BH = (H + S - 1) / S, BW = (W + S - 1) / S;
-    const int seglen = walk_seglen(BH, (long long)NC * BW);
+    static const long long resident = walk_resident(maxpool_bwd_walk_kernel<K, S>);
+    const int seglen = walk_seglen(BH, (long long)NC * BW, resident);
     const int nseg = (BH + seglen - 1) / seglen;
     const long long items = (long long)NC * nseg * BW;
     cudaError_t e = launch_pdl(maxpool_bwd_walk_kernel<K, S>, dim3(unsigned((items + kWalkThreads - 1) / kWalkThreads)),
