@@ -109,3 +109,24 @@ def test_mode_takes_effect(cb, orc):
     e1 = np.abs(c1 - ref).max()
     assert e1 > 10 * e3, (e1, e3)
     assert (np.abs(c1 - ref) <= TOL * ref_abs + 1e-6).all()
+
+
+# ---------------------------------------------------------------------------
+# flagged matmul: a subset of the 1176-case sweep (small, ragged and the
+# largest sizes, so the 32- to 256-wide tiles all run), sampled entries as in
+# tests/test_gpu_matmul_sweep.py, at the TF32 tolerance
+
+from tests.test_gpu_matmul_sweep import pools, run_case  # noqa: E402,F401  (fixture and checker)
+
+TF32_SWEEP_MN = (127, 1024, 9216)
+TF32_SWEEP_K = (25, 2304, 4096)
+
+
+@pytest.mark.parametrize("flags", [0, 1, 2, 3])
+@pytest.mark.parametrize("M", TF32_SWEEP_MN)
+def test_matmul_sweep_subset_tf32(cb, orc, tf32, pools, M, flags):
+    worst = 0.0
+    for N in TF32_SWEEP_MN:
+        for K in TF32_SWEEP_K:
+            worst = max(worst, run_case(cb, orc, pools, M, K, N, flags, tol_scale=TOL))
+    assert worst <= 1.0
