@@ -32,6 +32,14 @@
 // Two accumulators per issuer (2 x BN TMEM columns) let the epilogue of tile i
 // overlap the main loop of tile i+1.
 //
+// Stacked B tiles (two issuers, 3xTF32): a stage's hi and lo B tiles lie back
+// to back in shared memory, so one MMA with N = 2*BN multiplies A_hi by both
+// (hi*hi into the accumulator's first BN columns, hi*lo into the next BN) and
+// a second MMA (N = BN) adds lo*hi: two MMAs per 8-deep step instead of three,
+// and A is read from shared memory twice instead of three times.  On these
+// narrow tiles the shared-memory operand traffic (producer stores + MMA reads)
+// is what bounds the stage rate.  The epilogue adds the halves.
+//
 // Every wait is bounded (ptx.cuh); on give-up the kernel raises its abort
 // flag, records kDevErrTimeout in the device error word, waits for what it
 // already launched asynchronously, frees its tensor memory and returns.
@@ -83,11 +91,14 @@ struct TileCfg {
     static constexpr int kStages = kIssuers == 2 ? (kStages1 & ~1) : kStages1;   // two issuers: S even
     static_assert(kIssuers == 1 || kStages >= 2, "two issuers need an even number of stages");
     static constexpr uint32_t kACol = uint32_t(kDBuf * BN);   // first TMEM column of the A stages
-    static constexpr int kAccCols = kIssuers * kDBuf * BN;    // accumulators: [buffer][issuer]
+    // accumulators: [buffer][issuer], each 2*BN wide when B tiles are stacked
+    // (two issuers, 3xTF32: the allocation covers that case for both modes)
+    static constexpr int kAccCols = kIssuers * kDBuf * BN * (kIssuers == 2 ? 2 : 1);
     static constexpr uint32_t kTmemCols =
         ATMEM ? 512 : (kAccCols <= 64) ? 64 : (kAccCols <= 128) ? 128 : (kAccCols <= 256) ? 256 : 512;
     static constexpr size_t kSmemBytes = size_t(kStages) * kStage + 1024 /*align*/ + 256 /*barriers*/;
     static constexpr uint32_t kIdesc = idesc_tf32(kBM, BN);
+    static constexpr uint32_t kIdescStack = idesc_tf32(kBM, kIssuers == 2 ? 2 * BN : BN);   // the hi*[hi; lo] MMA
 };
 
 template <class Prob>
@@ -241,6 +252,8 @@ __global__ void __launch_bounds__(EngineRoles<Prob, BN>::R::kThreads, 1)
     // template parameter, so that the 3xTF32 kernel carries no trace of the
     // other mode (a runtime switch measured 7% slower).
     constexpr bool three = TERMS == 3;
+    constexpr bool STACK = three && NI == 2 && !ATMEM;   // stacked hi|lo B tiles (see the top of the file)
+    constexpr int AW = STACK ? 2 * BN : BN;              // accumulator columns per (buffer, issuer)
     constexpr uint32_t b_bytes = (three ? 2u : 1u) * Cfg::kBTile;
     auto fail = [&]() {
         ctl->abort_flag = 1;
@@ -369,7 +382,7 @@ __global__ void __launch_bounds__(EngineRoles<Prob, BN>::R::kThreads, 1)
                 const uint32_t acc_phase = uint32_t(local / DB) & 1u;
                 if (!mbar_wait(&ctl->acce[acc], acc_phase ^ 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + uint32_t((acc * NI + int(me)) * BN);
+                const uint32_t d_tmem = tmem_base + uint32_t((acc * NI + int(me)) * AW);
                 uint32_t accumulate = 0;
                 const int i0 = NI == 1 ? 0 : int(me ^ (cnt & 1u));   // this issuer's first stage of the tile
                 for (int i = i0; i < nks; i += NI) {
@@ -396,7 +409,11 @@ __global__ void __launch_bounds__(EngineRoles<Prob, BN>::R::kThreads, 1)
                         } else {
                             const uint64_t ah = sdesc_k_sw128(a_hi(stage) + kk * 32);
                             const uint64_t al = sdesc_k_sw128(a_lo(stage) + kk * 32);
-                            if (three) {
+                            if constexpr (STACK) {
+                                // [0, BN): hi*hi (+ lo*hi below); [BN, 2BN): hi*lo
+                                mma_tf32_ss(d_tmem, ah, bh, Cfg::kIdescStack, accumulate);
+                                mma_tf32_ss(d_tmem, al, bh, Cfg::kIdesc, 1);
+                            } else if (three) {
                                 mma_tf32_ss(d_tmem, al, bh, Cfg::kIdesc, accumulate);
                                 mma_tf32_ss(d_tmem, ah, bl, Cfg::kIdesc, 1);
                                 mma_tf32_ss(d_tmem, ah, bh, Cfg::kIdesc, 1);
@@ -440,7 +457,7 @@ __global__ void __launch_bounds__(EngineRoles<Prob, BN>::R::kThreads, 1)
             if (!mbar_wait_warp(&ctl->accf[acc], acc_phase, abort_flag)) { ok = false; break; }
             tc_fence_after();
             typename Prob::EState es = prob.e_setup(tile, row);
-            const uint32_t lane_base = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * NI * BN);
+            const uint32_t lane_base = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * NI * AW);
             if constexpr (NI == 1) {
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 32) {
@@ -455,7 +472,20 @@ __global__ void __launch_bounds__(EngineRoles<Prob, BN>::R::kThreads, 1)
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 32) {
                     uint32_t r0[32], r1[32];
-                    tmem_ld32x2(lane_base + uint32_t(c), lane_base + uint32_t(BN + c), r0, r1);
+                    if constexpr (STACK) {
+                        // each issuer's hi*lo half added to its first half
+                        uint32_t h[32];
+                        tmem_ld32x2(lane_base + uint32_t(c), lane_base + uint32_t(BN + c), r0, h);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            r0[i] = __float_as_uint(__uint_as_float(r0[i]) + __uint_as_float(h[i]));
+                        tmem_ld32x2(lane_base + uint32_t(AW + c), lane_base + uint32_t(AW + BN + c), r1, h);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            r1[i] = __float_as_uint(__uint_as_float(r1[i]) + __uint_as_float(h[i]));
+                    } else {
+                        tmem_ld32x2(lane_base + uint32_t(c), lane_base + uint32_t(AW + c), r0, r1);
+                    }
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         r0[i] = __float_as_uint((use0 ? __uint_as_float(r0[i]) : 0.f) +
