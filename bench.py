@@ -780,7 +780,7 @@ def run_matmul(args):
         from im2col_convolution_tiled_gb300 import build
         build.build()
     cb.load()
-    bf16, _, peak_kind = peaks()
+    bf16, hbm, peak_kind = peaks()
     peak = bf16 * TF32_OVER_BF16 / SPLIT_PRODUCTS
     stream = torch.cuda.current_stream()
     rows = []
@@ -805,8 +805,11 @@ def run_matmul(args):
                 f = 2 * M * N * K
                 flops_all += f
                 ms_all += ms
+                bn, pieces = cb.matmul_tiling(M, K, N, flags)
                 rows.append({"M": M, "N": N, "K": K, "flags": flags, "ms": round(ms, 4),
-                             "tflops": round(f / (ms * 1e-3) / 1e12, 2), "frac": round(f / (ms * 1e-3) / 1e12 / peak, 4)})
+                             "tflops": round(f / (ms * 1e-3) / 1e12, 2), "frac": round(f / (ms * 1e-3) / 1e12 / peak, 4),
+                             "frac_attainable": round(f / (ms * 1e-3) / 1e12 / attainable_tflops(M, N, K, peak, hbm), 4),
+                             "tile_cols": bn, "k_pieces": pieces})
     cb.check()
     big = [r for r in rows if (r["M"], r["N"], r["K"]) == MATMUL_SHAPES[0]]
     value = sum(2 * r["M"] * r["N"] * r["K"] for r in big) / (sum(r["ms"] for r in big) * 1e-3) / 1e12
@@ -1154,8 +1157,10 @@ def run_matmul_sweep(args):
             ms_all += ms
             att = attainable_tflops(M, N, K, peak, hbm)
             tfl = f / (ms * 1e-3) / 1e12
+            bn, pieces = cb.matmul_tiling(M, K, N, flags)
             rows.append({"M": M, "N": N, "K": K, "flags": flags, "ms": round(ms, 5), "tflops": round(tfl, 2),
-                         "frac": round(tfl / peak, 4), "frac_attainable": round(tfl / att, 4)})
+                         "frac": round(tfl / peak, 4), "frac_attainable": round(tfl / att, 4),
+                         "tile_cols": bn, "k_pieces": pieces})
     cb.check()
     launches = cb.launch_count() - n0
     small = [r for r in rows if min(r["M"], r["N"]) < 128]

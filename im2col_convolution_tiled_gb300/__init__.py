@@ -21,7 +21,7 @@ import os
 __all__ = [
     "ConvShape", "lib", "load", "conv_fwd", "conv_bwd_data", "conv_bwd_filter", "conv_bwd_filter_bias",
     "conv_bwd_bias",
-    "im2col", "col2im", "matmul", "maxpool2d_fwd", "maxpool2d_bwd", "sgd_step", "workspace_bytes",
+    "im2col", "col2im", "matmul", "matmul_tiling", "maxpool2d_fwd", "maxpool2d_bwd", "sgd_step", "workspace_bytes",
     "check", "ConvError", "out_size", "LIB_PATH", "launch_count", "relu_fwd", "relu_bwd", "grad_accum", "add_bias",
     "bias_grad_rows", "softmax_ce", "set_math_mode", "math_mode", "math", "CONV_MATH_FP32", "CONV_MATH_TF32",
     "conv_fwd_direct", "conv_bwd_data_direct", "conv_bwd_filter_direct",
@@ -61,6 +61,7 @@ _SIGS = {
     "im2col": ([_SHAPE, _P, _P, _P], ctypes.c_int),
     "col2im": ([_SHAPE, _P, _P, _P], ctypes.c_int),
     "matmul": ([ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_uint32, _P, _P, _P, _P], ctypes.c_int),
+    "matmul_tiling": ([ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_uint32, _P, _P], ctypes.c_int),
     "maxpool2d_fwd": ([ctypes.c_int32] * 8 + [_P, _P, _P, _P], ctypes.c_int),
     "maxpool2d_bwd": ([ctypes.c_int32] * 8 + [_P, _P, _P, _P], ctypes.c_int),
     "sgd_step": ([ctypes.c_int64, ctypes.c_float, ctypes.c_float, _P, _P, _P], ctypes.c_int),
@@ -304,6 +305,13 @@ def matmul(A, B, flags=0, C=None, stream=None):
     _want(C, "C")
     _call("matmul", M, K, N, flags, _ptr(A), _ptr(B), _ptr(C), _stream(stream))
     return C
+
+
+def matmul_tiling(M, K, N, flags=0):
+    """(tile columns, K pieces per tile) that matmul uses for this shape."""
+    bn, pieces = ctypes.c_int32(0), ctypes.c_int32(0)
+    _call("matmul_tiling", M, K, N, flags, ctypes.addressof(bn), ctypes.addressof(pieces))
+    return bn.value, pieces.value
 
 
 def maxpool2d_fwd(x, k, stride, y=None, idx=None, stream=None):

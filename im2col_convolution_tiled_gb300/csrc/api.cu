@@ -290,6 +290,18 @@ int matmul(int32_t M, int32_t K, int32_t N, uint32_t flags, const float* A, cons
     return status_of(launch_matmul(M, K, N, flags, A, B, C, as_cuda(stream)));
 }
 
+int matmul_tiling(int32_t M, int32_t K, int32_t N, uint32_t flags, int32_t* tile_cols, int32_t* k_pieces)
+{
+    if (!tile_cols || !k_pieces) return CONV_ERR_NULL;
+    if (M <= 0 || K <= 0 || N <= 0 || flags > 3u) return CONV_ERR_SHAPE;
+    if (!device_ok()) return CONV_ERR_DEVICE;
+    int bn = 0, cs = 0;
+    cb200::matmul_tiling(M, K, N, flags, &bn, &cs);
+    *tile_cols = bn;
+    *k_pieces = cs;
+    return CONV_OK;
+}
+
 static int check_pool(int32_t N, int32_t C, int32_t H, int32_t W, int32_t k, int32_t s, int32_t P, int32_t Q)
 {
     if (N <= 0 || C <= 0 || H <= 0 || W <= 0 || k <= 0 || s <= 0 || k > H || k > W) return CONV_ERR_SHAPE;

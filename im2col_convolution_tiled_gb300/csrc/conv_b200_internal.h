@@ -62,6 +62,8 @@ cudaError_t launch_conv_wgrad(const ConvDims& d, const float* x, const float* dy
                               cudaStream_t st, float* db = nullptr, const float* mask = nullptr);
 size_t conv_wgrad_ws(const ConvDims& d);
 
+// Tile width and K pieces per tile (cluster split) that launch_matmul uses.
+void matmul_tiling(int M, int K, int N, unsigned flags, int* bn, int* csplit);
 cudaError_t launch_matmul(int M, int K, int N, unsigned flags, const float* A, const float* B, float* C,
                           cudaStream_t st);
 

@@ -46,7 +46,18 @@
 // withhold_stage (a test hook, -1 in normal use): CTA 0's producers do not
 // arrive on the "full" barrier of that CTA-wide stage, so the MMA issuer's
 // bounded wait runs out and the kernel takes the path above.
+//
+// Cluster split (problems with kClusterSplit, prob.csplit > 1): when a GEMM
+// has too few output tiles to occupy the SMs, each tile's K range is cut into
+// csplit pieces run by the CTAs of one thread-block cluster (one piece, and
+// so one unit, per CTA).  A piece's epilogue writes its partial tile into the
+// CTA's own shared memory (the pipeline stages are idle by then); after a
+// cluster barrier every CTA adds, for its 128 / csplit rows of the tile, the
+// partials of all pieces in rank order through distributed shared memory and
+// hands the sums to prob.reduce_store.  Deterministic, no global workspace.
 #pragma once
+#include <cooperative_groups.h>
+
 #include "ptx.cuh"
 
 namespace cb200 {
@@ -100,6 +111,21 @@ struct TileCfg {
     static constexpr uint32_t kIdesc = idesc_tf32(kBM, BN);
     static constexpr uint32_t kIdescStack = idesc_tf32(kBM, kIssuers == 2 ? 2 * BN : BN);   // the hi*[hi; lo] MMA
 };
+
+template <class Prob>
+struct UsesClusterSplit {
+    template <class P>
+    static constexpr bool test(decltype(P::kClusterSplit)*) { return P::kClusterSplit; }
+    template <class P>
+    static constexpr bool test(...) { return false; }
+    static constexpr bool value = test<Prob>(nullptr);
+};
+
+// Row pitch (floats) of a cluster-split partial tile in shared memory: 16
+// bytes past a multiple of 128, so eight consecutive rows' 16-byte stores hit
+// eight different bank groups.
+template <int BN>
+__host__ __device__ constexpr int part_pitch() { return BN + 4; }
 
 template <class Prob>
 struct UsesTmemA {
@@ -194,6 +220,38 @@ struct EngineRoles {
     using R = Roles<Groups<Prob, BN>::value, Cfg::kIssuers>;
 };
 
+// The cluster split's reduction (see the top of the file), run by every thread
+// of every CTA of the cluster once its unit is done.  Not inlined: the main
+// kernel keeps its register allocation (inlined, it spilled the wide tiles).
+template <class Prob, int BN>
+__device__ __noinline__ void cluster_split_reduce(const Prob& prob, const uint8_t* smem, bool good)
+{
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();   // every piece's partial tile is in its CTA's shared memory
+    const int pieces = prob.csplit;
+    const int rank = int(cluster.block_rank());
+    const Tile tile = prob.tile(int(blockIdx.x));
+    const int rows = kBM / pieces;
+    constexpr int kC4 = BN / 4;
+    const float* part = reinterpret_cast<const float*>(smem);
+    for (int i = int(threadIdx.x); i < rows * kC4; i += int(blockDim.x)) {
+        const int row = rank * rows + i / kC4;
+        const int c = 4 * (i % kC4);
+        const int off = row * part_pitch<BN>() + c;
+        float4 acc = *reinterpret_cast<const float4*>(cluster.map_shared_rank(part, 0) + off);
+        for (int j = 1; j < pieces; ++j) {
+            const float4 v = *reinterpret_cast<const float4*>(cluster.map_shared_rank(part, j) + off);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        if (good) prob.reduce_store(tile, row, c, acc);
+    }
+    cluster.sync();   // each CTA's shared memory stays alive until its peers have read it
+}
+
 template <class Prob, int BN, int TERMS>
 __global__ void __launch_bounds__(EngineRoles<Prob, BN>::R::kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ Prob prob, int* err_word, int withhold_stage)
@@ -209,6 +267,9 @@ __global__ void __launch_bounds__(EngineRoles<Prob, BN>::R::kThreads, 1)
     constexpr int kWarpMma = Roles<G, NI>::kWarpMma;
     constexpr int kWarpEpi = Roles<G, NI>::kWarpEpi;
     constexpr int kBPasses = BN > 128 ? 2 : 1;
+    constexpr bool CS = UsesClusterSplit<Prob>::value;
+    static_assert(!CS || size_t(kBM) * part_pitch<BN>() * 4 <= size_t(S) * Cfg::kStage,
+                  "a cluster-split partial tile must fit the pipeline stages");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + size_t(S) * Cfg::kStage);
@@ -446,6 +507,20 @@ __global__ void __launch_bounds__(EngineRoles<Prob, BN>::R::kThreads, 1)
         // ---------------- epilogue ----------------
         const int q = warp & 3;               // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;        // accumulator row of this thread
+        // a cluster-split piece keeps its partial row in shared memory
+        auto emit = [&](const typename Prob::EState& es, const Tile& tl, int c, const uint32_t (&r)[32]) {
+            if constexpr (CS) {
+                if (tl.part >= 0) {
+                    float4* d = reinterpret_cast<float4*>(reinterpret_cast<float*>(smem) + row * part_pitch<BN>() + c);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        d[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                           __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+                    return;
+                }
+            }
+            prob.store(es, tl, row, c, r);
+        };
         uint32_t cnt = 0;                     // CTA-wide stage counter at the tile's start
         int local = 0;
         bool ok = true;
@@ -463,7 +538,7 @@ __global__ void __launch_bounds__(EngineRoles<Prob, BN>::R::kThreads, 1)
                 for (int c = 0; c < BN; c += 32) {
                     uint32_t r[32];
                     tmem_ld32(lane_base + uint32_t(c), r);
-                    prob.store(es, tile, row, c, r);
+                    emit(es, tile, c, r);
                 }
             } else {
                 // an issuer with no stage in the tile left its accumulator untouched
@@ -490,7 +565,7 @@ __global__ void __launch_bounds__(EngineRoles<Prob, BN>::R::kThreads, 1)
                     for (int i = 0; i < 32; ++i)
                         r0[i] = __float_as_uint((use0 ? __uint_as_float(r0[i]) : 0.f) +
                                                 (use1 ? __uint_as_float(r1[i]) : 0.f));
-                    prob.store(es, tile, row, c, r0);
+                    emit(es, tile, c, r0);
                 }
             }
             cnt += uint32_t(nks);
@@ -507,6 +582,72 @@ __global__ void __launch_bounds__(EngineRoles<Prob, BN>::R::kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem_base, Cfg::kTmemCols);
     }
+
+    // one unit per CTA when split: blockIdx.x is this CTA's piece
+    if constexpr (CS) {
+        if (prob.csplit > 1) cluster_split_reduce<Prob, BN>(prob, smem, *abort_flag == 0);
+    }
+}
+
+// Largest number of clusters of `cs` CTAs of this kernel that the device runs
+// at once (0 when it cannot launch them).  Cached per instantiation.
+template <class Prob, int BN, int TERMS>
+int max_active_clusters(int cs)
+{
+    using Cfg = TileCfg<BN, UsesTmemA<Prob>::value>;
+    static int cache[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
+    if (cs < 1 || cs > 8) return 0;
+    if (cache[cs] != 0) return cache[cs] > 0 ? cache[cs] : 0;
+    int n = 0;
+    if (cudaFuncSetAttribute(tc_gemm_kernel<Prob, BN, TERMS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(Cfg::kSmemBytes)) == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(unsigned(cs));
+        cfg.blockDim = dim3(EngineRoles<Prob, BN>::R::kThreads);
+        cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = unsigned(cs);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<Prob, BN, TERMS>, &cfg) != cudaSuccess) n = 0;
+    }
+    (void)cudaGetLastError();
+    cache[cs] = n > 0 ? n : -1;
+    return n > 0 ? n : 0;
+}
+
+// Pieces per tile for a cluster split (1 = none): the cut of K into 2, 4 or 8
+// pieces that minimises (rounds of clusters) x (stages per piece + a fixed
+// cost of about two stages for the cluster reduction), against whole tiles on
+// a persistent grid.  Pieces keep at least two K stages each.
+constexpr int kSplitFixedStages = 2;
+
+template <class Prob, int BN, int TERMS>
+int pick_csplit(int tiles, int k_stages)
+{
+    const int P = sm_count();
+    long long best_cost = (long long)((tiles + P - 1) / P) * k_stages;
+    int best = 1;
+    for (int cs = 2; cs <= 8; cs *= 2) {
+        if (k_stages < 2 * cs) break;
+        const int mc = max_active_clusters<Prob, BN, TERMS>(cs);
+        if (mc <= 0) continue;
+        const long long cost = (long long)((tiles + mc - 1) / mc) * ((k_stages + cs - 1) / cs + kSplitFixedStages);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = cs;
+        }
+    }
+    return best;
+}
+
+template <class Prob, int BN>
+int pick_csplit_terms(const Prob& prob, int tiles, int k_stages)
+{
+    return prob.terms == 1 ? pick_csplit<Prob, BN, 1>(tiles, k_stages) : pick_csplit<Prob, BN, 3>(tiles, k_stages);
 }
 
 // Host-side launch: persistent grid of min(tiles, SMs) CTAs.
@@ -524,9 +665,16 @@ cudaError_t launch_tc_gemm_terms(const Prob& prob, int num_tiles, int* err_word,
     }
     if (num_tiles <= 0) return cudaSuccess;
     int grid = num_tiles < sm_count() ? num_tiles : sm_count();
+    int cluster = 1;
+    if constexpr (UsesClusterSplit<Prob>::value) {
+        if (prob.csplit > 1) {   // one unit per CTA, clusters of csplit CTAs
+            grid = num_tiles;
+            cluster = prob.csplit;
+        }
+    }
     const int withhold = int(take_withhold_stage());
-    cudaError_t e = launch_pdl(tc_gemm_kernel<Prob, BN, TERMS>, dim3(grid), dim3(kThreads), Cfg::kSmemBytes, stream, prob,
-                               err_word, withhold);
+    cudaError_t e = launch_pdl_cluster(tc_gemm_kernel<Prob, BN, TERMS>, dim3(grid), dim3(kThreads), Cfg::kSmemBytes,
+                                       stream, cluster, prob, err_word, withhold);
     if (e != cudaSuccess) return e;
     note_launch();
     return cudaGetLastError();

@@ -8,6 +8,11 @@
 // thread along M, four rows of one k (QuadRow); B stored K x N 4 bytes per
 // thread along N (RowFast).  Either way the producer writes K-major swizzled
 // hi/lo tiles, so all four flag combinations feed the same MMA.
+//
+// Shapes with fewer output tiles than SMs (skinny C, or a small C with a long
+// K) cut each tile's K range over a thread-block cluster (the engine's
+// cluster split): csplit CTAs each run one K piece and the pieces are added
+// in a fixed order through distributed shared memory.
 #include "gemm_tc.cuh"
 
 namespace cb200 {
@@ -15,7 +20,10 @@ namespace cb200 {
 template <unsigned FLAGS, int BN>
 struct MatmulProb {
     static constexpr bool kBBulk = false;
-    int terms = 3;   // tensor-core products per K step: 3 (3xTF32) or 1 (TF32)
+    static constexpr bool kClusterSplit = true;
+    int terms = 3;    // tensor-core products per K step: 3 (3xTF32) or 1 (TF32)
+    int csplit = 1;   // K pieces per tile, one per CTA of a cluster (1: whole tiles; a power of two)
+    int lcsplit = 0;  // log2(csplit)
     static constexpr int kGroups = 2;
     static constexpr Map kAMap = (FLAGS & 1u) ? Map::QuadRow : Map::ChunkFast;
     // B stored K x N stays one row per thread: measured faster than QuadRow
@@ -30,16 +38,20 @@ struct MatmulProb {
     int vec_a, vec_b, vec_c;   // 16-byte accesses allowed along K (A, B) / along N (C)
     int vec_am;                // 16-byte accesses allowed along M (A stored K x M)
 
-    __device__ int num_tiles() const { return m_tiles * n_tiles; }
+    __device__ int num_tiles() const { return m_tiles * n_tiles * csplit; }
 
+    // Unit t: tile t / csplit, K piece t % csplit (the CTA's rank in its
+    // cluster when csplit > 1).
     __device__ Tile tile(int t) const
     {
+        const int tt = t >> lcsplit, j = t & (csplit - 1);
         Tile r;
-        r.n0 = (t % n_tiles) * BN;
-        r.m0 = (t / n_tiles) * kBM;
-        r.ks0 = 0;
-        r.ks1 = k_stages;
+        r.n0 = (tt % n_tiles) * BN;
+        r.m0 = (tt / n_tiles) * kBM;
+        r.ks0 = (j * k_stages) >> lcsplit;
+        r.ks1 = ((j + 1) * k_stages) >> lcsplit;
         r.grp = 0;
+        r.part = csplit > 1 ? j : -1;
         return r;
     }
 
@@ -143,6 +155,23 @@ struct MatmulProb {
         return e;
     }
 
+    // Cluster split: the sum of all pieces for columns n0 + c .. + 3 of one row.
+    __device__ void reduce_store(const Tile& tl, int row, int c, float4 v) const
+    {
+        const int m = tl.m0 + row;
+        const int n = tl.n0 + c;
+        if (m >= M || n >= N) return;
+        float* dst = C + size_t(m) * N + n;
+        if (vec_c && n + 3 < N) {
+            *reinterpret_cast<float4*>(dst) = v;
+        } else {
+            dst[0] = v.x;
+            if (n + 1 < N) dst[1] = v.y;
+            if (n + 2 < N) dst[2] = v.z;
+            if (n + 3 < N) dst[3] = v.w;
+        }
+    }
+
     __device__ void store(const EState& e, const Tile& tl, int, int c, const uint32_t (&r)[32]) const
     {
         if (!e.valid) return;
@@ -160,6 +189,16 @@ struct MatmulProb {
         }
     }
 };
+
+// K pieces per tile for an M x K x N product on tiles BN wide (1: whole tiles).
+template <unsigned FLAGS, int BN>
+static int matmul_csplit(int M, int K, int N)
+{
+    MatmulProb<FLAGS, BN> p;
+    p.terms = math_terms();
+    return pick_csplit_terms<MatmulProb<FLAGS, BN>, BN>(p, ((M + kBM - 1) / kBM) * ((N + BN - 1) / BN),
+                                                        (K + kBK - 1) / kBK);
+}
 
 template <unsigned FLAGS, int BN>
 static cudaError_t run_matmul(int M, int K, int N, const float* A, const float* B, float* C, cudaStream_t st)
@@ -179,7 +218,9 @@ static cudaError_t run_matmul(int M, int K, int N, const float* A, const float* 
     p.vec_b = (K % 4 == 0) && aligned16(B);
     p.vec_c = (N % 4 == 0) && aligned16(C);
     p.vec_am = (M % 4 == 0) && aligned16(A);
-    return launch_tc_gemm<MatmulProb<FLAGS, BN>, BN>(p, p.m_tiles * p.n_tiles, device_error_word(), st);
+    p.csplit = matmul_csplit<FLAGS, BN>(M, K, N);
+    while ((1 << p.lcsplit) < p.csplit) ++p.lcsplit;
+    return launch_tc_gemm<MatmulProb<FLAGS, BN>, BN>(p, p.m_tiles * p.n_tiles * p.csplit, device_error_word(), st);
 }
 
 // Tile width: the widest of {256, 128, 64, 32} that still gives every SM a
@@ -201,6 +242,29 @@ static cudaError_t run_flags(int M, int K, int N, const float* A, const float* B
     case 128: return run_matmul<FLAGS, 128>(M, K, N, A, B, C, st);
     case 64: return run_matmul<FLAGS, 64>(M, K, N, A, B, C, st);
     default: return run_matmul<FLAGS, 32>(M, K, N, A, B, C, st);
+    }
+}
+
+template <unsigned FLAGS>
+static int csplit_flags(int M, int K, int N, int bn)
+{
+    switch (bn) {
+    case 256: return matmul_csplit<FLAGS, 256>(M, K, N);
+    case 128: return matmul_csplit<FLAGS, 128>(M, K, N);
+    case 64: return matmul_csplit<FLAGS, 64>(M, K, N);
+    default: return matmul_csplit<FLAGS, 32>(M, K, N);
+    }
+}
+
+void matmul_tiling(int M, int K, int N, unsigned flags, int* bn, int* csplit)
+{
+    const int b = pick_bn(M, N);
+    *bn = b;
+    switch (flags) {
+    case 0: *csplit = csplit_flags<0>(M, K, N, b); break;
+    case 1: *csplit = csplit_flags<1>(M, K, N, b); break;
+    case 2: *csplit = csplit_flags<2>(M, K, N, b); break;
+    default: *csplit = csplit_flags<3>(M, K, N, b); break;
     }
 }
 

@@ -175,6 +175,17 @@ int col2im(const conv_shape_t *s, const float *col, float *dx, conv_stream_t str
 int matmul(int32_t M, int32_t K, int32_t N, uint32_t flags, const float *A, const float *B, float *C,
            conv_stream_t stream);
 
+/* How matmul tiles an M x K x N product on the current device and in the
+ * current math mode (a host-side query, no GPU work): *tile_cols = width of
+ * an output tile (32, 64, 128 or 256 columns; tiles are 128 rows);
+ * *k_pieces = number of pieces each tile's K range is cut into when there are
+ * too few tiles for the SMs (1: whole tiles).  The pieces of a tile run on the
+ * CTAs of one thread-block cluster and are added in a fixed order through
+ * distributed shared memory, so results stay deterministic.  Returns CONV_OK,
+ * CONV_ERR_NULL (an output pointer is NULL), CONV_ERR_SHAPE (as matmul) or
+ * CONV_ERR_DEVICE. */
+int matmul_tiling(int32_t M, int32_t K, int32_t N, uint32_t flags, int32_t *tile_cols, int32_t *k_pieces);
+
 /* Max pooling forward (nn_maxpool_forward, section "Pooling Shaders"):
  * k x k windows, stride `stride`, no padding, outH = (H - k) / stride + 1.
  * y = window maximum; idx = flat offset into the whole NCHW x of the FIRST

@@ -36,7 +36,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ["conv_fwd", "conv_fwd_relu", "conv_bwd_data", "conv_bwd_filter", "conv_bwd_filter_bias", "conv_bwd_bias", "im2col",
-              "col2im", "matmul",
+              "col2im", "matmul", "matmul_tiling",
               "maxpool2d_fwd", "maxpool2d_bwd", "sgd_step", "conv_b200_strerror", "conv_b200_check",
               "conv_b200_workspace_bytes", "relu_fwd", "relu_bwd", "grad_accum", "add_bias", "bias_grad_rows",
               "softmax_ce", "conv_b200_set_math_mode", "conv_b200_math_mode", "conv_fwd_direct",
@@ -127,6 +127,15 @@ def test_training_piece_validation(lib):
     assert lib.softmax_ce(4, 10, FAKE, FAKE, MIS, FAKE, FAKE, NULL) == ERR_ALIGN     # probs (optional)
     assert lib.softmax_ce(4, 10, FAKE, FAKE, NULL, FAKE, NULL, NULL) == ERR_NULL     # loss
     assert lib.softmax_ce(-4, 10, FAKE, FAKE, NULL, FAKE, FAKE, NULL) == ERR_SHAPE
+
+
+def test_matmul_tiling_validation(lib):
+    """The tiling query validates its arguments before it looks for a device."""
+    bn, pieces = ctypes.c_int32(0), ctypes.c_int32(0)
+    assert lib.matmul_tiling(4, 4, 4, 0, NULL, ctypes.byref(pieces)) == ERR_NULL
+    assert lib.matmul_tiling(4, 4, 4, 0, ctypes.byref(bn), NULL) == ERR_NULL
+    assert lib.matmul_tiling(0, 4, 4, 0, ctypes.byref(bn), ctypes.byref(pieces)) == ERR_SHAPE
+    assert lib.matmul_tiling(4, 4, 4, 4, ctypes.byref(bn), ctypes.byref(pieces)) == ERR_SHAPE
 
 
 def test_math_mode_switch(lib):

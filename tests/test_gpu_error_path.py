@@ -38,12 +38,14 @@ def test_withheld_stage_times_out_then_stream_recovers(cb):
     import torch
     import oracle
     orc = oracle.get()
-    M, K, N = 512, 512, 512          # 16 K stages per tile: stage 5 exists in CTA 0
+    # 16 K stages per tile; whether a tile runs whole or its K range is cut
+    # over a cluster (at most 8 pieces of >= 2 stages), CTA 0 runs stage 1
+    M, K, N = 512, 512, 512
     A, B = synthetic.matmul_case(M, K, N, 0)
     a, b = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
     cb.check()                       # nothing pending before the test
     lib = cb.lib()
-    assert lib.conv_b200_debug_withhold_stage(5) == 0
+    assert lib.conv_b200_debug_withhold_stage(1) == 0
     t0 = time.perf_counter()
     cb.matmul(a, b, 0)               # asynchronous: the call itself succeeds
     with pytest.raises(cb.ConvError) as ei:

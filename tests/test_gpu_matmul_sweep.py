@@ -110,3 +110,45 @@ def test_matmul_sweep(cb, orc, pools, M, flags):
         for K in synthetic.MATMUL_K:
             worst = max(worst, run_case(cb, orc, pools, M, K, N, flags))
     assert worst <= 1.0
+
+
+def test_sweep_reaches_every_tiling(cb):
+    """Over the sweep, each flag combination meets every tile width (32 to 256
+    columns) and both whole tiles and K cut over clusters of 2, 4 and 8 CTAs
+    (the cluster split: few tiles, long K)."""
+    for flags in range(4):
+        widths, pieces = set(), set()
+        for M in synthetic.MATMUL_MN:
+            for N in synthetic.MATMUL_MN:
+                for K in synthetic.MATMUL_K:
+                    bn, p = cb.matmul_tiling(M, K, N, flags)
+                    widths.add(bn)
+                    pieces.add(p)
+        assert widths == {32, 64, 128, 256}, (flags, widths)
+        assert {1, 2, 4, 8} <= pieces, (flags, pieces)
+
+
+# Shapes whose tiles are cut over clusters, checked against the full oracle
+# (every entry) and for run-to-run bit-identity (the pieces are added in a
+# fixed order): one tile (16 x 16), ragged tiles (127 x 127, 130 columns) and
+# several tiles (128 x 1024), K from 150 to 4096.
+SPLIT_SHAPES = [(16, 4096, 16), (127, 1600, 127), (64, 2304, 130), (128, 363, 1024), (127, 4096, 200),
+                (16, 150, 64)]
+
+
+@pytest.mark.parametrize("flags", [0, 1, 2, 3])
+def test_cluster_split_full_oracle(cb, orc, flags):
+    import torch
+    seen = set()
+    for M, K, N in SPLIT_SHAPES:
+        A, B = synthetic.matmul_case(M, K, N, flags)
+        a, b = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+        bn, pieces = cb.matmul_tiling(M, K, N, flags)
+        seen.add(pieces)
+        c1 = cb.matmul(a, b, flags)
+        c2 = cb.matmul(a, b, flags)
+        cb.check()
+        ref, ref_abs = orc.matmul(A.astype(np.float64), B.astype(np.float64), flags)
+        assert_within_tol(c1.cpu().numpy(), ref, ref_abs, "matmul %dx%dx%d f%d (%d pieces)" % (M, K, N, flags, pieces))
+        assert torch.equal(c1, c2), "matmul %dx%dx%d f%d: not bit-identical run to run" % (M, K, N, flags)
+    assert len(seen - {1}) >= 2, seen
