@@ -42,6 +42,29 @@ inline size_t bimage_floats(int n_rows, int k_total, int bn)
 // (the filter gradient's dy image gives the bias gradient this way).
 constexpr int kBimageThreads = 256;
 
+// Gen may provide load4(row, k0, k_total, v): the four values k0 .. k0+3 of a
+// row (zero past k_total) in one go, e.g. with one index division instead of
+// four; otherwise they come from gen(row, k) one by one.
+template <class Gen>
+struct HasLoad4 {
+    template <class G>
+    static constexpr bool test(decltype(&G::load4)) { return true; }
+    template <class G>
+    static constexpr bool test(...) { return false; }
+    static constexpr bool value = test<Gen>(nullptr);
+};
+
+template <class Gen>
+__device__ __forceinline__ void bimage_load4(const Gen& gen, int row, int k0, int k_total, float (&v)[4])
+{
+    if constexpr (HasLoad4<Gen>::value) {
+        gen.load4(row, k0, k_total, v);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = k0 + e < k_total ? gen(row, k0 + e) : 0.f;
+    }
+}
+
 template <class Gen>
 __global__ void __launch_bounds__(kBimageThreads) build_bimage_kernel(Gen gen, int n_rows, int k_total, int bn,
                                                                       int k_stages, float* img, float* rowsum)
@@ -51,21 +74,33 @@ __global__ void __launch_bounds__(kBimageThreads) build_bimage_kernel(Gen gen, i
     const int row = blockIdx.y;
     const int chunks = k_stages * (kBK / 4);
     const int nt = row / bn, r = row % bn;
+    const int stride = gridDim.x * blockDim.x;
     float part = 0.f;
-    for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < chunks; t += gridDim.x * blockDim.x) {
-        const int k0 = t * 4;
+    auto put = [&](int t, const float (&v)[4]) {
         uint32_t hi[4], lo[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float v = (row < n_rows && k0 + e < k_total) ? gen(row, k0 + e) : 0.f;
-            part += v;
-            split_tf32(v, hi[e], lo[e]);
-        }
+        for (int e = 0; e < 4; ++e) split_tf32(v[e], hi[e], lo[e]);
         const int ks = t / (kBK / 4), c = t % (kBK / 4);
         float* blk = img + ((size_t(nt) * k_stages + ks) * 2) * size_t(bn) * kBK;
         const uint32_t off = sw128_offset(uint32_t(r), uint32_t(c)) / 4;
         *reinterpret_cast<uint4*>(blk + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4*>(blk + size_t(bn) * kBK + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    };
+    // two chunks per iteration: both chunks' loads are issued before either
+    // is split and stored
+    for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < chunks; t += 2 * stride) {
+        const int t2 = t + stride;
+        float v[4] = {0.f, 0.f, 0.f, 0.f}, w[4] = {0.f, 0.f, 0.f, 0.f};
+        if (row < n_rows) {
+            bimage_load4(gen, row, t * 4, k_total, v);
+            if (t2 < chunks) bimage_load4(gen, row, t2 * 4, k_total, w);
+        }
+        part += (v[0] + v[1]) + (v[2] + v[3]);
+        put(t, v);
+        if (t2 < chunks) {
+            part += (w[0] + w[1]) + (w[2] + w[3]);
+            put(t2, w);
+        }
     }
     if (rowsum == nullptr || row >= n_rows) return;   // uniform over the block
     __shared__ float warp_part[kBimageThreads / 32];

@@ -170,6 +170,24 @@ struct GradGen {
         f_pq.divmod(uint32_t(j), n, pq);
         return __ldg(dy + (size_t(n) * K + k) * PQ + pq);
     }
+    // j0 .. j0+3 with one division: offsets step by one pixel, and by
+    // (K - 1) * PQ more where the run crosses into the next image (dy has
+    // fewer than 2^31 elements, so 32-bit offsets hold)
+    __device__ void load4(int k, int j0, int J, float (&v)[4]) const
+    {
+        uint32_t n, pq;
+        f_pq.divmod(uint32_t(j0 < J ? j0 : 0), n, pq);
+        uint32_t off = (n * uint32_t(K) + uint32_t(k)) * uint32_t(PQ) + pq;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            v[e] = j0 + e < J ? __ldg(dy + off) : 0.f;
+            ++off;
+            if (++pq == uint32_t(PQ)) {
+                pq = 0;
+                off += uint32_t(K - 1) * uint32_t(PQ);
+            }
+        }
+    }
 };
 
 // The same with the ReLU gradient applied as dy is read (nn_relu_grad):
@@ -185,6 +203,21 @@ struct GradMaskGen {
         f_pq.divmod(uint32_t(j), n, pq);
         const size_t at = (size_t(n) * K + k) * PQ + pq;
         return __ldg(dy + at) * relu_gate(__ldg(mask + at));
+    }
+    __device__ void load4(int k, int j0, int J, float (&v)[4]) const
+    {
+        uint32_t n, pq;
+        f_pq.divmod(uint32_t(j0 < J ? j0 : 0), n, pq);
+        uint32_t off = (n * uint32_t(K) + uint32_t(k)) * uint32_t(PQ) + pq;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            v[e] = j0 + e < J ? __ldg(dy + off) * relu_gate(__ldg(mask + off)) : 0.f;
+            ++off;
+            if (++pq == uint32_t(PQ)) {
+                pq = 0;
+                off += uint32_t(K - 1) * uint32_t(PQ);
+            }
+        }
     }
 };
 
