@@ -619,37 +619,6 @@ int max_active_clusters(int cs)
     return n > 0 ? n : 0;
 }
 
-// Pieces per tile for a cluster split (1 = none): the cut of K into 2, 4 or 8
-// pieces that minimises (rounds of clusters) x (stages per piece + a fixed
-// cost of about two stages for the cluster reduction), against whole tiles on
-// a persistent grid.  Pieces keep at least two K stages each.
-constexpr int kSplitFixedStages = 2;
-
-template <class Prob, int BN, int TERMS>
-int pick_csplit(int tiles, int k_stages)
-{
-    const int P = sm_count();
-    long long best_cost = (long long)((tiles + P - 1) / P) * k_stages;
-    int best = 1;
-    for (int cs = 2; cs <= 8; cs *= 2) {
-        if (k_stages < 2 * cs) break;
-        const int mc = max_active_clusters<Prob, BN, TERMS>(cs);
-        if (mc <= 0) continue;
-        const long long cost = (long long)((tiles + mc - 1) / mc) * ((k_stages + cs - 1) / cs + kSplitFixedStages);
-        if (cost < best_cost) {
-            best_cost = cost;
-            best = cs;
-        }
-    }
-    return best;
-}
-
-template <class Prob, int BN>
-int pick_csplit_terms(const Prob& prob, int tiles, int k_stages)
-{
-    return prob.terms == 1 ? pick_csplit<Prob, BN, 1>(tiles, k_stages) : pick_csplit<Prob, BN, 3>(tiles, k_stages);
-}
-
 // Host-side launch: persistent grid of min(tiles, SMs) CTAs.
 template <class Prob, int BN, int TERMS>
 cudaError_t launch_tc_gemm_terms(const Prob& prob, int num_tiles, int* err_word, cudaStream_t stream)

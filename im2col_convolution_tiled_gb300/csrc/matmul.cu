@@ -9,10 +9,10 @@
 // thread along N (RowFast).  Either way the producer writes K-major swizzled
 // hi/lo tiles, so all four flag combinations feed the same MMA.
 //
-// Shapes with fewer output tiles than SMs (skinny C, or a small C with a long
-// K) cut each tile's K range over a thread-block cluster (the engine's
-// cluster split): csplit CTAs each run one K piece and the pieces are added
-// in a fixed order through distributed shared memory.
+// Tile width and K split are planned together (plan_matmul below): where the
+// widest tiles leave SMs idle, each tile's K range is cut over a thread-block
+// cluster (the engine's cluster split): csplit CTAs each run one K piece and
+// the pieces are added in a fixed order through distributed shared memory.
 #include "gemm_tc.cuh"
 
 namespace cb200 {
@@ -190,18 +190,78 @@ struct MatmulProb {
     }
 };
 
-// K pieces per tile for an M x K x N product on tiles BN wide (1: whole tiles).
+// Tiling plan: tile width BN and K pieces per tile (cluster split).
+//
+// The producers gather each stage through registers at a nearly fixed cost
+// per operand row loaded (measured on GB300: about 7 cycles per 32-value row,
+// against which the MMAs of a stage rarely bound it), so a stage costs about
+// (A rows + B rows) -- min(M, 128) for A; min(N, BN) for B stored N x K, but
+// 128 per pass for B stored K x N, whose loader reads a column per thread
+// whatever the tile's width.  Wide tiles therefore do more work per producer
+// cycle, and where they leave SMs idle the cluster split fills them.  The plan
+// minimises rounds x (stages per unit + a fixed cost) x (rows per stage) over
+// BN in {256, 128, 64} (32 when N <= 32) and 1, 2, 4 or 8 pieces per tile.
+struct MatmulPlan {
+    int bn, cs;
+};
+
+constexpr int kTileFixedStages = 1;    // a whole tile's epilogue and hand-over
+constexpr int kClusterFixedStages = 3; // a split tile's partials, cluster barriers and reduction
+
 template <unsigned FLAGS, int BN>
-static int matmul_csplit(int M, int K, int N)
+static int mm_clusters(int cs)
 {
-    MatmulProb<FLAGS, BN> p;
-    p.terms = math_terms();
-    return pick_csplit_terms<MatmulProb<FLAGS, BN>, BN>(p, ((M + kBM - 1) / kBM) * ((N + BN - 1) / BN),
-                                                        (K + kBK - 1) / kBK);
+    return math_terms() == 1 ? max_active_clusters<MatmulProb<FLAGS, BN>, BN, 1>(cs)
+                             : max_active_clusters<MatmulProb<FLAGS, BN>, BN, 3>(cs);
+}
+
+template <unsigned FLAGS>
+static int clusters_for(int bn, int cs)
+{
+    switch (bn) {
+    case 256: return mm_clusters<FLAGS, 256>(cs);
+    case 128: return mm_clusters<FLAGS, 128>(cs);
+    case 64: return mm_clusters<FLAGS, 64>(cs);
+    default: return mm_clusters<FLAGS, 32>(cs);
+    }
+}
+
+template <unsigned FLAGS>
+static MatmulPlan plan_matmul(int M, int K, int N)
+{
+    const int P = sm_count();
+    const long long mt = (M + kBM - 1) / kBM;
+    const int ks = (K + kBK - 1) / kBK;
+    const int bn_max = N <= 32 ? 32 : N <= 64 ? 64 : N <= 128 ? 128 : 256;
+    const int bn_min = bn_max < 64 ? bn_max : 64;
+    MatmulPlan best{bn_max, 1};
+    long long best_cost = -1, best_units = 0;
+    for (int bn = bn_max; bn >= bn_min; bn /= 2) {
+        const long long tiles = mt * ((N + bn - 1) / bn);
+        const long long rows_a = M < kBM ? M : kBM;
+        const long long rows_b = (FLAGS & 2u) ? (N < bn ? N : bn) : 128LL * ((bn + 127) / 128);
+        for (int cs = 1; cs <= 8; cs *= 2) {
+            if (cs > 1 && ks < 2 * cs) break;
+            const int slots = cs == 1 ? P : clusters_for<FLAGS>(bn, cs);
+            if (slots <= 0) continue;
+            const long long rounds = (tiles + slots - 1) / slots;
+            const long long per = (ks + cs - 1) / cs + (cs == 1 ? kTileFixedStages : kClusterFixedStages);
+            const long long cost = rounds * per * (rows_a + rows_b);
+            // on a tie the plan with more CTAs wins: they share the same work
+            // (small shapes are latency-bound)
+            const long long units = tiles * cs;
+            if (best_cost < 0 || cost < best_cost || (cost == best_cost && units > best_units)) {
+                best_cost = cost;
+                best_units = units;
+                best = MatmulPlan{bn, cs};
+            }
+        }
+    }
+    return best;
 }
 
 template <unsigned FLAGS, int BN>
-static cudaError_t run_matmul(int M, int K, int N, const float* A, const float* B, float* C, cudaStream_t st)
+static cudaError_t run_matmul(int M, int K, int N, int cs, const float* A, const float* B, float* C, cudaStream_t st)
 {
     MatmulProb<FLAGS, BN> p;
     p.terms = math_terms();
@@ -218,54 +278,34 @@ static cudaError_t run_matmul(int M, int K, int N, const float* A, const float* 
     p.vec_b = (K % 4 == 0) && aligned16(B);
     p.vec_c = (N % 4 == 0) && aligned16(C);
     p.vec_am = (M % 4 == 0) && aligned16(A);
-    p.csplit = matmul_csplit<FLAGS, BN>(M, K, N);
+    p.csplit = cs;
     while ((1 << p.lcsplit) < p.csplit) ++p.lcsplit;
     return launch_tc_gemm<MatmulProb<FLAGS, BN>, BN>(p, p.m_tiles * p.n_tiles * p.csplit, device_error_word(), st);
-}
-
-// Tile width: the widest of {256, 128, 64, 32} that still gives every SM a
-// tile; narrower C only when there are too few tiles to go round.
-static int pick_bn(int M, int N)
-{
-    const int m_tiles = (M + kBM - 1) / kBM;
-    const int bn_max = N <= 32 ? 32 : N <= 64 ? 64 : N <= 128 ? 128 : 256;
-    for (int bn = bn_max; bn > 64; bn /= 2)
-        if (m_tiles * ((N + bn - 1) / bn) >= sm_count()) return bn;
-    return bn_max < 64 ? bn_max : 64;
 }
 
 template <unsigned FLAGS>
 static cudaError_t run_flags(int M, int K, int N, const float* A, const float* B, float* C, cudaStream_t st)
 {
-    switch (pick_bn(M, N)) {
-    case 256: return run_matmul<FLAGS, 256>(M, K, N, A, B, C, st);
-    case 128: return run_matmul<FLAGS, 128>(M, K, N, A, B, C, st);
-    case 64: return run_matmul<FLAGS, 64>(M, K, N, A, B, C, st);
-    default: return run_matmul<FLAGS, 32>(M, K, N, A, B, C, st);
-    }
-}
-
-template <unsigned FLAGS>
-static int csplit_flags(int M, int K, int N, int bn)
-{
-    switch (bn) {
-    case 256: return matmul_csplit<FLAGS, 256>(M, K, N);
-    case 128: return matmul_csplit<FLAGS, 128>(M, K, N);
-    case 64: return matmul_csplit<FLAGS, 64>(M, K, N);
-    default: return matmul_csplit<FLAGS, 32>(M, K, N);
+    const MatmulPlan pl = plan_matmul<FLAGS>(M, K, N);
+    switch (pl.bn) {
+    case 256: return run_matmul<FLAGS, 256>(M, K, N, pl.cs, A, B, C, st);
+    case 128: return run_matmul<FLAGS, 128>(M, K, N, pl.cs, A, B, C, st);
+    case 64: return run_matmul<FLAGS, 64>(M, K, N, pl.cs, A, B, C, st);
+    default: return run_matmul<FLAGS, 32>(M, K, N, pl.cs, A, B, C, st);
     }
 }
 
 void matmul_tiling(int M, int K, int N, unsigned flags, int* bn, int* csplit)
 {
-    const int b = pick_bn(M, N);
-    *bn = b;
+    MatmulPlan pl;
     switch (flags) {
-    case 0: *csplit = csplit_flags<0>(M, K, N, b); break;
-    case 1: *csplit = csplit_flags<1>(M, K, N, b); break;
-    case 2: *csplit = csplit_flags<2>(M, K, N, b); break;
-    default: *csplit = csplit_flags<3>(M, K, N, b); break;
+    case 0: pl = plan_matmul<0>(M, K, N); break;
+    case 1: pl = plan_matmul<1>(M, K, N); break;
+    case 2: pl = plan_matmul<2>(M, K, N); break;
+    default: pl = plan_matmul<3>(M, K, N); break;
     }
+    *bn = pl.bn;
+    *csplit = pl.cs;
 }
 
 cudaError_t launch_matmul(int M, int K, int N, unsigned flags, const float* A, const float* B, float* C,
