@@ -336,7 +336,7 @@ __global__ void __launch_bounds__(EngineRoles<Prob, BN>::R::kThreads, 1)
                 typename Prob::AState ast = prob.a_setup(tile, tid);
                 typename Prob::BState bst = prob.b_setup(tile, tid);
                 // Everything for stage i except the A gather (already in va).
-                auto produce = [&](int i, const float (&va)[32]) -> bool {
+                auto produce = [&](int i, float (&va)[32]) -> bool {
                     const uint32_t c = cnt + uint32_t(i);
                     const int slot = int(c % uint32_t(S));
                     const uint32_t phase = (c / uint32_t(S)) & 1u;
@@ -345,6 +345,17 @@ __global__ void __launch_bounds__(EngineRoles<Prob, BN>::R::kThreads, 1)
                     if constexpr (!Prob::kBBulk) {
 #pragma unroll
                         for (int pass = 0; pass < kBPasses; ++pass) prob.load_b(bst, tile, ks, pass, tid, vb[pass]);
+                        // Every gathered value lands in its register here, before
+                        // the wait for the slot: all of the stage's loads are then
+                        // in flight together.  Without this the TF32 build (fewer
+                        // stores to schedule against) let loads trail into the
+                        // stores and ran 2.8x slower on B stored K x N.
+#pragma unroll
+                        for (int pass = 0; pass < kBPasses; ++pass)
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) asm volatile("" : "+f"(vb[pass][i]));
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) asm volatile("" : "+f"(va[i]));
                     }
                     if (!mbar_wait_warp(&ctl->empty[slot], phase ^ 1u, abort_flag)) return false;
                     if constexpr (Prob::kBBulk) {
