@@ -885,6 +885,29 @@ __global__ void __launch_bounds__(kWalkThreads) maxpool_fwd_walk_kernel(
     }
 }
 
+// Add gradient v of a window to the pixel its saved index iv names, if that
+// pixel is one of the walking thread's cells: rows r < K below its block
+// origin p00 (rows >= S belong to the next block row and go to the carry),
+// columns c < CM (S for the thread's own window column, K - S for the window
+// column to its left, the part of that window over this block column).  All
+// those cells lie inside the window, so a match is also the window check: the
+// index is compared with each cell's offset instead of being decoded.
+template <int K, int S, int KC, int CM>
+__device__ __forceinline__ void pool_route(float v, int iv, int p00, int W, float (&acc)[S][S], float (&nxt)[KC][S])
+{
+    const int d = iv - p00;
+#pragma unroll
+    for (int r = 0; r < K; ++r)
+#pragma unroll
+        for (int c = 0; c < CM; ++c)
+            if (d == r * W + c) {
+                if (r < S)
+                    acc[r][c] += v;
+                else
+                    nxt[r - S < KC ? r - S : 0][c] += v;
+            }
+}
+
 // Backward: a thread owns the column of S x S pixel blocks j (pixel columns
 // S*j .. S*j + S - 1) and walks down its block rows b.  With K <= 2S only the
 // windows (b, j - 1) and (b, j) of window row b reach block (b, j), and
@@ -916,29 +939,6 @@ __global__ void __launch_bounds__(kWalkThreads) maxpool_bwd_walk_kernel(
     const bool has_l = j >= 1 && int(j) - 1 < Q;   // window column j - 1 exists
     const bool has_r = int(j) < Q;                 // window column j exists
 
-    // Add gradient v of window (oh, ow) to the pixel its saved index iv names,
-    // if that pixel lies in this thread's blocks: window column j - 1 (own =
-    // false) reaches block columns dc >= S, window column j (own) dc < S.
-    auto route = [&](float v, int iv, int oh, int ow, bool own, float (&acc)[S][S], float (&nxt)[KC][S]) {
-        const int d = iv - (pbase + (oh * W + ow) * S);
-        int dr = 0;
-#pragma unroll
-        for (int r = 1; r < K; ++r) dr += d >= r * W ? 1 : 0;
-        const int dc = d - dr * W;
-        const bool ok = d >= 0 && dc < K && (own ? dc < S : dc >= S);
-        const int c = own ? dc : dc - S;
-#pragma unroll
-        for (int r = 0; r < K; ++r)
-#pragma unroll
-            for (int cc = 0; cc < S; ++cc)
-                if (ok && dr == r && c == cc) {
-                    if (r < S)
-                        acc[r][cc] += v;
-                    else
-                        nxt[r - S < KC ? r - S : 0][cc] += v;
-                }
-    };
-
     float carry[KC][S];
 #pragma unroll
     for (int r = 0; r < KC; ++r)
@@ -948,8 +948,9 @@ __global__ void __launch_bounds__(kWalkThreads) maxpool_bwd_walk_kernel(
         // the segment starts mid-plane: window row b0 - 1's contributions to block row b0
         float unused[S][S] = {};
         const int oh = b0 - 1;
-        if (has_l) route(__ldg(dyp + oh * Q + j - 1), __ldg(ip + oh * Q + j - 1), oh, int(j) - 1, false, unused, carry);
-        if (has_r) route(__ldg(dyp + oh * Q + j), __ldg(ip + oh * Q + j), oh, int(j), true, unused, carry);
+        const int p00 = pbase + oh * S * W + int(j) * S;
+        if (has_l) pool_route<K, S, KC, K - S>(__ldg(dyp + oh * Q + j - 1), __ldg(ip + oh * Q + j - 1), p00, W, unused, carry);
+        if (has_r) pool_route<K, S, KC, S>(__ldg(dyp + oh * Q + j), __ldg(ip + oh * Q + j), p00, W, unused, carry);
     }
     const int wend = min(b1, P);   // window rows this segment reads: [b0, wend)
     float* out = dx + pbase + int(j) * S;
@@ -983,8 +984,9 @@ __global__ void __launch_bounds__(kWalkThreads) maxpool_bwd_walk_kernel(
 #pragma unroll
                 for (int c = 0; c < S; ++c) nxt[r][c] = 0.f;
             if (bb < wend) {
-                if (has_l) route(vl[u], il[u], bb, int(j) - 1, false, acc, nxt);
-                if (has_r) route(vr[u], ir[u], bb, int(j), true, acc, nxt);
+                const int p00 = pbase + bb * S * W + int(j) * S;
+                if (has_l) pool_route<K, S, KC, K - S>(vl[u], il[u], p00, W, acc, nxt);
+                if (has_r) pool_route<K, S, KC, S>(vr[u], ir[u], p00, W, acc, nxt);
             }
 #pragma unroll
             for (int r = 0; r < S; ++r) {
