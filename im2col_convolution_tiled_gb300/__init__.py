@@ -62,6 +62,8 @@ _SIGS = {
     "col2im": ([_SHAPE, _P, _P, _P], ctypes.c_int),
     "matmul": ([ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_uint32, _P, _P, _P, _P], ctypes.c_int),
     "matmul_tiling": ([ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_uint32, _P, _P], ctypes.c_int),
+    "matmul_fused": ([ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_uint32, _P, _P, _P, ctypes.c_int32, _P,
+                      _P, _P], ctypes.c_int),
     "maxpool2d_fwd": ([ctypes.c_int32] * 8 + [_P, _P, _P, _P], ctypes.c_int),
     "maxpool2d_bwd": ([ctypes.c_int32] * 8 + [_P, _P, _P, _P], ctypes.c_int),
     "sgd_step": ([ctypes.c_int64, ctypes.c_float, ctypes.c_float, _P, _P, _P], ctypes.c_int),
@@ -286,8 +288,11 @@ def col2im(col, x_shape, k, stride=1, padding=0, dx=None, stream=None):
     return dx
 
 
-def matmul(A, B, flags=0, C=None, stream=None):
-    """C = op(A) op(B); flags bit 0: A stored K x M, bit 1: B stored N x K."""
+def matmul(A, B, flags=0, C=None, stream=None, bias=None, relu=False, gate=None):
+    """C = op(A) op(B); flags bit 0: A stored K x M, bit 1: B stored N x K.
+    With bias ([N]), relu or gate ([M, N]) the epilogue adds the bias per
+    column, applies max(0, .) and multiplies by (gate > 0), in that order, in
+    the same pass (matmul_fused)."""
     torch = _torch()
     _want(A, "A"), _want(B, "B")
     if flags & 1:
@@ -303,7 +308,19 @@ def matmul(A, B, flags=0, C=None, stream=None):
     if C is None:
         C = torch.empty((M, N), dtype=torch.float32, device=A.device)
     _want(C, "C")
-    _call("matmul", M, K, N, flags, _ptr(A), _ptr(B), _ptr(C), _stream(stream))
+    if bias is None and gate is None and not relu:
+        _call("matmul", M, K, N, flags, _ptr(A), _ptr(B), _ptr(C), _stream(stream))
+        return C
+    if bias is not None:
+        _want(bias, "bias")
+        if tuple(bias.shape) != (N,):
+            raise ValueError("bias must have shape (%d,)" % N)
+    if gate is not None:
+        _want(gate, "gate")
+        if tuple(gate.shape) != (M, N):
+            raise ValueError("gate must have shape (%d, %d)" % (M, N))
+    _call("matmul_fused", M, K, N, flags, _ptr(A), _ptr(B), _ptr(bias) if bias is not None else None,
+          1 if relu else 0, _ptr(gate) if gate is not None else None, _ptr(C), _stream(stream))
     return C
 
 

@@ -290,6 +290,22 @@ int matmul(int32_t M, int32_t K, int32_t N, uint32_t flags, const float* A, cons
     return status_of(launch_matmul(M, K, N, flags, A, B, C, as_cuda(stream)));
 }
 
+int matmul_fused(int32_t M, int32_t K, int32_t N, uint32_t flags, const float* A, const float* B, const float* bias,
+                 int32_t relu, const float* gate, float* C, conv_stream_t stream)
+{
+    if (M <= 0 || K <= 0 || N <= 0 || flags > 3u) return CONV_ERR_SHAPE;
+    if ((long long)M * K > kMaxElems || (long long)K * N > kMaxElems || (long long)M * N > kMaxElems)
+        return CONV_ERR_OVERFLOW;
+    int rc = check_ptrs({A, B, C});
+    if (rc != CONV_OK) return rc;
+    if (!device_ok()) return CONV_ERR_DEVICE;
+    MatmulEpi ep;
+    ep.bias = bias;
+    ep.gate = gate;
+    ep.relu = relu ? 1 : 0;
+    return status_of(launch_matmul(M, K, N, flags, A, B, C, as_cuda(stream), ep));
+}
+
 int matmul_tiling(int32_t M, int32_t K, int32_t N, uint32_t flags, int32_t* tile_cols, int32_t* k_pieces)
 {
     if (!tile_cols || !k_pieces) return CONV_ERR_NULL;

@@ -64,8 +64,15 @@ size_t conv_wgrad_ws(const ConvDims& d);
 
 // Tile width and K pieces per tile (cluster split) that launch_matmul uses.
 void matmul_tiling(int M, int K, int N, unsigned flags, int* bn, int* csplit);
+// Optional epilogue of matmul_fused: bias [N] added per column, then ReLU,
+// then the product with (gate[m][n] > 0); all off by default.
+struct MatmulEpi {
+    const float* bias = nullptr;
+    const float* gate = nullptr;
+    int relu = 0;
+};
 cudaError_t launch_matmul(int M, int K, int N, unsigned flags, const float* A, const float* B, float* C,
-                          cudaStream_t st);
+                          cudaStream_t st, const MatmulEpi& ep = MatmulEpi{});
 
 cudaError_t launch_bias_grad(const ConvDims& d, const float* dy, float* db, cudaStream_t st);
 cudaError_t launch_im2col(const ConvDims& d, const float* x, float* col, cudaStream_t st);

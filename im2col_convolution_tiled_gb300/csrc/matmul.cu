@@ -34,6 +34,21 @@ struct MatmulProb {
     const float* B;
     float* C;
     int M, K, N;
+    // Fused epilogue (matmul_fused): c + bias[n], then max(0, .), then
+    // c * (gate[m][n] > 0) -- each an fp32 operation, as add_bias, relu_fwd
+    // and relu_bwd compute them; off when epi == 0.
+    const float* bias = nullptr;
+    const float* gate = nullptr;
+    int relu = 0, epi = 0;
+    int vec_bias = 0, vec_gate = 0;   // 16-byte loads allowed (bias aligned; gate aligned with N % 4 == 0)
+
+    __device__ __forceinline__ float epilogue(float v, int m, int n) const
+    {
+        if (bias) v = __fadd_rn(v, __ldg(bias + n));
+        if (relu) v = v > 0.f ? v : 0.f;
+        if (gate) v = __fmul_rn(v, __ldg(gate + size_t(m) * N + n) > 0.f ? 1.f : 0.f);
+        return v;
+    }
     int m_tiles, n_tiles, k_stages;
     int vec_a, vec_b, vec_c;   // 16-byte accesses allowed along K (A, B) / along N (C)
     int vec_am;                // 16-byte accesses allowed along M (A stored K x M)
@@ -161,6 +176,12 @@ struct MatmulProb {
         const int m = tl.m0 + row;
         const int n = tl.n0 + c;
         if (m >= M || n >= N) return;
+        if (epi) {
+            v.x = epilogue(v.x, m, n);
+            if (n + 1 < N) v.y = epilogue(v.y, m, n + 1);
+            if (n + 2 < N) v.z = epilogue(v.z, m, n + 2);
+            if (n + 3 < N) v.w = epilogue(v.w, m, n + 3);
+        }
         float* dst = C + size_t(m) * N + n;
         if (vec_c && n + 3 < N) {
             *reinterpret_cast<float4*>(dst) = v;
@@ -172,10 +193,60 @@ struct MatmulProb {
         }
     }
 
-    __device__ void store(const EState& e, const Tile& tl, int, int c, const uint32_t (&r)[32]) const
+    __device__ void store(const EState& e, const Tile& tl, int row, int c, const uint32_t (&r)[32]) const
     {
         if (!e.valid) return;
         const int n0 = tl.n0 + c;
+        if (epi) {
+            // eight columns at a time: their bias and gate values are loaded
+            // together (16-byte loads where aligned), then applied in order
+            const int m = tl.m0 + row;
+            const float* grow = gate ? gate + size_t(m) * N : nullptr;
+            const bool full = n0 + 32 <= N;
+            uint32_t q[32];
+#pragma unroll
+            for (int g8 = 0; g8 < 32; g8 += 8) {
+                float bv[8], gv[8];
+                const int n = n0 + g8;
+                if (bias) {
+                    if (full && vec_bias) {
+                        const float4 u = __ldg(reinterpret_cast<const float4*>(bias + n));
+                        const float4 w = __ldg(reinterpret_cast<const float4*>(bias + n + 4));
+                        bv[0] = u.x; bv[1] = u.y; bv[2] = u.z; bv[3] = u.w;
+                        bv[4] = w.x; bv[5] = w.y; bv[6] = w.z; bv[7] = w.w;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) bv[i] = n + i < N ? __ldg(bias + n + i) : 0.f;
+                    }
+                }
+                if (grow) {
+                    if (full && vec_gate) {
+                        const float4 u = __ldg(reinterpret_cast<const float4*>(grow + n));
+                        const float4 w = __ldg(reinterpret_cast<const float4*>(grow + n + 4));
+                        gv[0] = u.x; gv[1] = u.y; gv[2] = u.z; gv[3] = u.w;
+                        gv[4] = w.x; gv[5] = w.y; gv[6] = w.z; gv[7] = w.w;
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) gv[i] = n + i < N ? __ldg(grow + n + i) : 0.f;
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    float v = __uint_as_float(r[g8 + i]);
+                    if (bias) v = __fadd_rn(v, bv[i]);
+                    if (relu) v = v > 0.f ? v : 0.f;
+                    if (grow) v = __fmul_rn(v, gv[i] > 0.f ? 1.f : 0.f);
+                    q[g8 + i] = __float_as_uint(v);
+                }
+            }
+            store_row(e, n0, q);
+            return;
+        }
+        store_row(e, n0, r);
+    }
+
+    __device__ __forceinline__ void store_row(const EState& e, int n0, const uint32_t (&r)[32]) const
+    {
         if (vec_c && n0 + 32 <= N) {
 #pragma unroll
             for (int i = 0; i < 32; i += 4)
@@ -261,10 +332,17 @@ static MatmulPlan plan_matmul(int M, int K, int N)
 }
 
 template <unsigned FLAGS, int BN>
-static cudaError_t run_matmul(int M, int K, int N, int cs, const float* A, const float* B, float* C, cudaStream_t st)
+static cudaError_t run_matmul(int M, int K, int N, int cs, const float* A, const float* B, float* C,
+                              const MatmulEpi& ep, cudaStream_t st)
 {
     MatmulProb<FLAGS, BN> p;
     p.terms = math_terms();
+    p.bias = ep.bias;
+    p.gate = ep.gate;
+    p.relu = ep.relu ? 1 : 0;
+    p.epi = (ep.bias || ep.gate || ep.relu) ? 1 : 0;
+    p.vec_bias = ep.bias && aligned16(ep.bias);
+    p.vec_gate = ep.gate && (N % 4 == 0) && aligned16(ep.gate);
     p.A = A;
     p.B = B;
     p.C = C;
@@ -284,14 +362,15 @@ static cudaError_t run_matmul(int M, int K, int N, int cs, const float* A, const
 }
 
 template <unsigned FLAGS>
-static cudaError_t run_flags(int M, int K, int N, const float* A, const float* B, float* C, cudaStream_t st)
+static cudaError_t run_flags(int M, int K, int N, const float* A, const float* B, float* C, const MatmulEpi& ep,
+                             cudaStream_t st)
 {
     const MatmulPlan pl = plan_matmul<FLAGS>(M, K, N);
     switch (pl.bn) {
-    case 256: return run_matmul<FLAGS, 256>(M, K, N, pl.cs, A, B, C, st);
-    case 128: return run_matmul<FLAGS, 128>(M, K, N, pl.cs, A, B, C, st);
-    case 64: return run_matmul<FLAGS, 64>(M, K, N, pl.cs, A, B, C, st);
-    default: return run_matmul<FLAGS, 32>(M, K, N, pl.cs, A, B, C, st);
+    case 256: return run_matmul<FLAGS, 256>(M, K, N, pl.cs, A, B, C, ep, st);
+    case 128: return run_matmul<FLAGS, 128>(M, K, N, pl.cs, A, B, C, ep, st);
+    case 64: return run_matmul<FLAGS, 64>(M, K, N, pl.cs, A, B, C, ep, st);
+    default: return run_matmul<FLAGS, 32>(M, K, N, pl.cs, A, B, C, ep, st);
     }
 }
 
@@ -309,13 +388,13 @@ void matmul_tiling(int M, int K, int N, unsigned flags, int* bn, int* csplit)
 }
 
 cudaError_t launch_matmul(int M, int K, int N, unsigned flags, const float* A, const float* B, float* C,
-                          cudaStream_t st)
+                          cudaStream_t st, const MatmulEpi& ep)
 {
     switch (flags) {
-    case 0: return run_flags<0>(M, K, N, A, B, C, st);
-    case 1: return run_flags<1>(M, K, N, A, B, C, st);
-    case 2: return run_flags<2>(M, K, N, A, B, C, st);
-    default: return run_flags<3>(M, K, N, A, B, C, st);
+    case 0: return run_flags<0>(M, K, N, A, B, C, ep, st);
+    case 1: return run_flags<1>(M, K, N, A, B, C, ep, st);
+    case 2: return run_flags<2>(M, K, N, A, B, C, ep, st);
+    default: return run_flags<3>(M, K, N, A, B, C, ep, st);
     }
 }
 

@@ -18,8 +18,12 @@ replayed: the counterpart of the page's dispatch pipelining
 
 Conventions (as the page's shaders give them):
   * linear: Y = X W + b with W stored in x out; dW = X^T dY (matmul flag 1),
-    dX = dY W^T (matmul flag 2), db = row sums of dY; bias and ReLU are one
-    add_bias call (relu flag);
+    dX = dY W^T (matmul flag 2), db = row sums of dY; the bias add and the
+    ReLU run in the forward matmul's epilogue (matmul_fused: the same fp32
+    operations as add_bias, bit for bit).  The ReLU gradient behind a linear
+    layer stays a relu_bwd pass: gating the dX matmul's epilogue instead
+    measured 1-12 us slower per graph-replayed step (programmatic dependent
+    launch already hides the separate pass);
   * the convolutions' ReLU runs in their epilogue (conv_fwd_relu);
   * the ReLU gradient is masked by the ReLU's output (> 0 exactly where its
     input is); behind a convolution the mask is applied inside the
@@ -33,7 +37,7 @@ from __future__ import annotations
 
 from collections import namedtuple
 
-from . import (CONV_OP_BWD_DATA, CONV_OP_BWD_FILTER, CONV_OP_FWD, add_bias, bias_grad_rows, conv_bwd_data,
+from . import (CONV_OP_BWD_DATA, CONV_OP_BWD_FILTER, CONV_OP_FWD, bias_grad_rows, conv_bwd_data,
                conv_bwd_filter_bias, conv_fwd, matmul, maxpool2d_bwd, maxpool2d_fwd, relu_bwd, sgd_step, shape_of,
                softmax_ce, workspace_bytes)
 
@@ -104,9 +108,8 @@ class LeNet5:
         t["i2"] = torch.empty_like(t["p2"], dtype=torch.int32)
         t["f"] = t["p2"].view(B, -1)                    # flatten (a view: no copy)
         for i, (fin, fout) in enumerate(FCS, 1):
-            t["m%d" % i] = e((B, fout), **f32)          # X W
             t["dz%d" % i] = e((B, fout), **f32)         # gradient at X W + b
-            t["df" if i == 1 else "dh%d" % (i - 1)] = e((B, fin), **f32)
+            t["df" if i == 1 else "dh%d" % (i - 1)] = e((B, fin), **f32)   # gradient at X
         t["h1"] = e((B, FCS[0][1]), **f32)              # ReLU(X W + b), layers 1 and 2
         t["h2"] = e((B, FCS[1][1]), **f32)
         t["z3"] = e((B, FCS[2][1]), **f32)              # logits
@@ -144,17 +147,16 @@ class LeNet5:
         maxpool2d_fwd(t["a2"], *c2.pool, y=t["p2"], idx=t["i2"], stream=st)
         h = t["f"]
         for i, out in ((1, "h1"), (2, "h2"), (3, "z3")):
-            matmul(h, P["fc%d_w" % i], 0, C=t["m%d" % i], stream=st)
-            add_bias(t["m%d" % i], P["fc%d_b" % i], out=t[out], relu=i < 3, stream=st)
+            matmul(h, P["fc%d_w" % i], 0, C=t[out], bias=P["fc%d_b" % i], relu=i < 3, stream=st)
             h = t[out]
         softmax_ce(t["z3"], t["labels"], dlogits=t["dz3"], loss=t["loss"], stream=st)
         # backward: linear layers
         for i in (3, 2, 1):
             hin = t["h%d" % (i - 1)] if i > 1 else t["f"]
             dz = t["dz%d" % i]
-            dh = t["dh%d" % (i - 1)] if i > 1 else t["df"]
             matmul(hin, dz, 1, C=G["fc%d_w" % i], stream=st)
             bias_grad_rows(dz, db=G["fc%d_b" % i], stream=st)
+            dh = t["dh%d" % (i - 1)] if i > 1 else t["df"]
             matmul(dz, P["fc%d_w" % i], 2, C=dh, stream=st)
             if i > 1:
                 relu_bwd(dh, t["h%d" % (i - 1)], dx=t["dz%d" % (i - 1)], stream=st)

@@ -175,6 +175,20 @@ int col2im(const conv_shape_t *s, const float *col, float *dx, conv_stream_t str
 int matmul(int32_t M, int32_t K, int32_t N, uint32_t flags, const float *A, const float *B, float *C,
            conv_stream_t stream);
 
+/* Flagged matmul with a fused epilogue: the linear layer of the page's LeNet
+ * trainer (section "LeNet on MNIST") without separate element-wise passes.
+ * C = op(A) * op(B) exactly as matmul computes it, then per element (i, j),
+ * in this order:
+ *   bias != NULL:  c = c + bias[j]          one fp32 addition (nn_add_bias, as add_bias)
+ *   relu != 0:     c = max(0, c)            +0 for c <= 0 (nn_relu, as relu_fwd)
+ *   gate != NULL:  c = c * (gate[i][j] > 0) an fp32 product with 1 or 0 (nn_relu_grad, as relu_bwd)
+ * so the result is bit-identical to matmul followed by add_bias and relu_bwd
+ * (the forward Y = relu(X W + b); the input gradient of a ReLU-fed layer,
+ * dX = (dY W^T) * (X > 0)).  bias [N] and gate [M][N] are optional, read only,
+ * and must not overlap C; arguments otherwise as matmul. */
+int matmul_fused(int32_t M, int32_t K, int32_t N, uint32_t flags, const float *A, const float *B, const float *bias,
+                 int32_t relu, const float *gate, float *C, conv_stream_t stream);
+
 /* How matmul tiles an M x K x N product on the current device and in the
  * current math mode (a host-side query, no GPU work): *tile_cols = width of
  * an output tile (32, 64, 128 or 256 columns; tiles are 128 rows);

@@ -36,7 +36,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ["conv_fwd", "conv_fwd_relu", "conv_bwd_data", "conv_bwd_filter", "conv_bwd_filter_bias", "conv_bwd_bias", "im2col",
-              "col2im", "matmul", "matmul_tiling",
+              "col2im", "matmul", "matmul_tiling", "matmul_fused",
               "maxpool2d_fwd", "maxpool2d_bwd", "sgd_step", "conv_b200_strerror", "conv_b200_check",
               "conv_b200_workspace_bytes", "relu_fwd", "relu_bwd", "grad_accum", "add_bias", "bias_grad_rows",
               "softmax_ce", "conv_b200_set_math_mode", "conv_b200_math_mode", "conv_fwd_direct",
@@ -127,6 +127,15 @@ def test_training_piece_validation(lib):
     assert lib.softmax_ce(4, 10, FAKE, FAKE, MIS, FAKE, FAKE, NULL) == ERR_ALIGN     # probs (optional)
     assert lib.softmax_ce(4, 10, FAKE, FAKE, NULL, FAKE, NULL, NULL) == ERR_NULL     # loss
     assert lib.softmax_ce(-4, 10, FAKE, FAKE, NULL, FAKE, FAKE, NULL) == ERR_SHAPE
+
+
+def test_matmul_fused_validation(lib):
+    """matmul_fused validates like matmul; bias and gate are optional."""
+    assert lib.matmul_fused(4, 4, 4, 0, NULL, FAKE, NULL, 1, NULL, FAKE, NULL) == ERR_NULL
+    assert lib.matmul_fused(4, 4, 4, 0, FAKE, FAKE, NULL, 1, NULL, MIS, NULL) == ERR_ALIGN
+    assert lib.matmul_fused(0, 4, 4, 0, FAKE, FAKE, NULL, 0, NULL, FAKE, NULL) == ERR_SHAPE
+    assert lib.matmul_fused(4, 4, 4, 4, FAKE, FAKE, FAKE, 0, FAKE, FAKE, NULL) == ERR_SHAPE
+    assert lib.matmul_fused(65536, 65536, 4, 0, FAKE, FAKE, NULL, 0, NULL, FAKE, NULL) == ERR_OVERFLOW
 
 
 def test_matmul_tiling_validation(lib):
