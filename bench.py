@@ -781,7 +781,9 @@ def run_matmul(args):
         build.build()
     cb.load()
     bf16, hbm, peak_kind = peaks()
-    peak = bf16 * TF32_OVER_BF16 / SPLIT_PRODUCTS
+    tf32 = args.math == "tf32"
+    cb.set_math_mode(cb.CONV_MATH_TF32 if tf32 else cb.CONV_MATH_FP32)
+    peak = bf16 * TF32_OVER_BF16 / (1 if tf32 else SPLIT_PRODUCTS)
     stream = torch.cuda.current_stream()
     rows = []
     flops_all, ms_all = 0, 0.0
@@ -805,8 +807,8 @@ def run_matmul(args):
                 f = 2 * M * N * K
                 flops_all += f
                 ms_all += ms
-                bn, pieces = cb.matmul_tiling(M, K, N, flags)
-                rows.append({"M": M, "N": N, "K": K, "flags": flags, "ms": round(ms, 4),
+                bn, pieces, fed = cb.matmul_tiling(M, K, N, flags, a, b, with_tma=True)
+                rows.append({"M": M, "N": N, "K": K, "flags": flags, "ms": round(ms, 4), "tma_fed": fed,
                              "tflops": round(f / (ms * 1e-3) / 1e12, 2), "frac": round(f / (ms * 1e-3) / 1e12 / peak, 4),
                              "frac_attainable": round(f / (ms * 1e-3) / 1e12 / attainable_tflops(M, N, K, peak, hbm), 4),
                              "tile_cols": bn, "k_pieces": pieces})
@@ -815,16 +817,17 @@ def run_matmul(args):
     value = sum(2 * r["M"] * r["N"] * r["K"] for r in big) / (sum(r["ms"] for r in big) * 1e-3) / 1e12
     line = {
         "metric": MATMUL_METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
-        "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "tf32" if tf32 else "f32",
         "data": "synthetic",
         "config": {"workload": "largest sweep shape M=N=9216, K=4096, all four flags (value); the table covers "
                                "further sweep shapes", "shapes": rows,
-                   "all_shapes_tflops": round(flops_all / (ms_all * 1e-3) / 1e12, 2),
+                   "all_shapes_tflops": round(flops_all / (ms_all * 1e-3) / 1e12, 2), "math": args.math,
                    "l2": "no flush: operands of the value's shape are 0.6 GB (> 126 MB L2)"},
         "roofline": {"bound": "tensor", "achieved": round(value, 2), "peak": round(peak, 1), "unit": "TFLOP/s",
                      "frac": round(value / peak, 4), "traffic": None,
-                     "peak_basis": "%s bf16 %.1f TFLOP/s x %.3f (TF32/BF16) / 3 (3xTF32)"
-                                   % (peak_kind, bf16, TF32_OVER_BF16)},
+                     "peak_basis": "%s bf16 %.1f TFLOP/s x %.3f (TF32/BF16)%s"
+                                   % (peak_kind, bf16, TF32_OVER_BF16, "" if tf32 else " / 3 (3xTF32)")},
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
@@ -1157,10 +1160,10 @@ def run_matmul_sweep(args):
             ms_all += ms
             att = attainable_tflops(M, N, K, peak, hbm)
             tfl = f / (ms * 1e-3) / 1e12
-            bn, pieces = cb.matmul_tiling(M, K, N, flags)
+            bn, pieces, fed = cb.matmul_tiling(M, K, N, flags, a, b, with_tma=True)
             rows.append({"M": M, "N": N, "K": K, "flags": flags, "ms": round(ms, 5), "tflops": round(tfl, 2),
                          "frac": round(tfl / peak, 4), "frac_attainable": round(tfl / att, 4),
-                         "tile_cols": bn, "k_pieces": pieces})
+                         "tile_cols": bn, "k_pieces": pieces, "tma_fed": fed})
     cb.check()
     launches = cb.launch_count() - n0
     small = [r for r in rows if min(r["M"], r["N"]) < 128]

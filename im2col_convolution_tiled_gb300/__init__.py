@@ -61,7 +61,8 @@ _SIGS = {
     "im2col": ([_SHAPE, _P, _P, _P], ctypes.c_int),
     "col2im": ([_SHAPE, _P, _P, _P], ctypes.c_int),
     "matmul": ([ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_uint32, _P, _P, _P, _P], ctypes.c_int),
-    "matmul_tiling": ([ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_uint32, _P, _P], ctypes.c_int),
+    "matmul_tiling": ([ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_uint32, _P, _P, _P, _P, _P],
+                      ctypes.c_int),
     "matmul_fused": ([ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_uint32, _P, _P, _P, ctypes.c_int32, _P,
                       _P, _P], ctypes.c_int),
     "maxpool2d_fwd": ([ctypes.c_int32] * 8 + [_P, _P, _P, _P], ctypes.c_int),
@@ -324,11 +325,16 @@ def matmul(A, B, flags=0, C=None, stream=None, bias=None, relu=False, gate=None)
     return C
 
 
-def matmul_tiling(M, K, N, flags=0):
-    """(tile columns, K pieces per tile) that matmul uses for this shape."""
-    bn, pieces = ctypes.c_int32(0), ctypes.c_int32(0)
-    _call("matmul_tiling", M, K, N, flags, ctypes.addressof(bn), ctypes.addressof(pieces))
-    return bn.value, pieces.value
+def matmul_tiling(M, K, N, flags=0, A=None, B=None, with_tma=False):
+    """(tile columns, K pieces per tile) that matmul uses for this shape, plus
+    whether the operands arrive by TMA when with_tma (A and B: the operand
+    tensors, whose alignment decides; 16-byte aligned when omitted)."""
+    bn, pieces, tma = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)
+    pa = ctypes.c_void_p(A.data_ptr()) if A is not None else ctypes.c_void_p(0)
+    pb = ctypes.c_void_p(B.data_ptr()) if B is not None else ctypes.c_void_p(0)
+    _call("matmul_tiling", M, K, N, flags, pa, pb, ctypes.addressof(bn), ctypes.addressof(pieces),
+          ctypes.addressof(tma))
+    return (bn.value, pieces.value, bool(tma.value)) if with_tma else (bn.value, pieces.value)
 
 
 def maxpool2d_fwd(x, k, stride, y=None, idx=None, stream=None):

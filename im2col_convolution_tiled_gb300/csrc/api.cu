@@ -306,15 +306,17 @@ int matmul_fused(int32_t M, int32_t K, int32_t N, uint32_t flags, const float* A
     return status_of(launch_matmul(M, K, N, flags, A, B, C, as_cuda(stream), ep));
 }
 
-int matmul_tiling(int32_t M, int32_t K, int32_t N, uint32_t flags, int32_t* tile_cols, int32_t* k_pieces)
+int matmul_tiling(int32_t M, int32_t K, int32_t N, uint32_t flags, const float* A, const float* B, int32_t* tile_cols,
+                  int32_t* k_pieces, int32_t* tma_fed)
 {
-    if (!tile_cols || !k_pieces) return CONV_ERR_NULL;
+    if (!tile_cols || !k_pieces || !tma_fed) return CONV_ERR_NULL;
     if (M <= 0 || K <= 0 || N <= 0 || flags > 3u) return CONV_ERR_SHAPE;
     if (!device_ok()) return CONV_ERR_DEVICE;
-    int bn = 0, cs = 0;
-    cb200::matmul_tiling(M, K, N, flags, &bn, &cs);
+    int bn = 0, cs = 0, tma = 0;
+    cb200::matmul_tiling(M, K, N, flags, A, B, &bn, &cs, &tma);
     *tile_cols = bn;
     *k_pieces = cs;
+    *tma_fed = tma;
     return CONV_OK;
 }
 

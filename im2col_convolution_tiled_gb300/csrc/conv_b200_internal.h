@@ -62,8 +62,10 @@ cudaError_t launch_conv_wgrad(const ConvDims& d, const float* x, const float* dy
                               cudaStream_t st, float* db = nullptr, const float* mask = nullptr);
 size_t conv_wgrad_ws(const ConvDims& d);
 
-// Tile width and K pieces per tile (cluster split) that launch_matmul uses.
-void matmul_tiling(int M, int K, int N, unsigned flags, int* bn, int* csplit);
+// Tile width, K pieces per tile (cluster split) and whether the operands
+// arrive by TMA, as launch_matmul plans them for operands at A and B.
+void matmul_tiling(int M, int K, int N, unsigned flags, const float* A, const float* B, int* bn, int* csplit,
+                   int* tma);
 // Optional epilogue of matmul_fused: bias [N] added per column, then ReLU,
 // then the product with (gate[m][n] > 0); all off by default.
 struct MatmulEpi {

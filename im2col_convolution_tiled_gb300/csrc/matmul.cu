@@ -14,6 +14,7 @@
 // cluster (the engine's cluster split): csplit CTAs each run one K piece and
 // the pieces are added in a fixed order through distributed shared memory.
 #include "gemm_tc.cuh"
+#include "gemm_tma.cuh"
 
 namespace cb200 {
 
@@ -274,7 +275,18 @@ struct MatmulProb {
 // BN in {256, 128, 64} (32 when N <= 32) and 1, 2, 4 or 8 pieces per tile.
 struct MatmulPlan {
     int bn, cs;
+    bool tma;   // operands by TMA (gemm_tma.cuh; whole tiles, cs == 1)
 };
+
+// A TMA-fed stage's cost in the same unit (register-gathered rows at about
+// 7 cycles each), per 32 deep, measured on GB300 from its steady-state stage
+// time: 3xTF32 2390 cycles at 256 columns, 2040 at 128 (the tensor core and
+// the shared-memory port, not the loads, set it); TF32 1040-1170 and 1200.
+inline long long tma_rows(int bn, bool tf32)
+{
+    if (tf32) return bn == 256 ? 150 : 165;
+    return bn == 256 ? 332 : 280;
+}
 
 constexpr int kTileFixedStages = 1;    // a whole tile's epilogue and hand-over
 constexpr int kClusterFixedStages = 3; // a split tile's partials, cluster barriers and reduction
@@ -297,16 +309,30 @@ static int clusters_for(int bn, int cs)
     }
 }
 
+// tma_ok: the shape and operands qualify for the TMA-fed kernel (tma_fed).
 template <unsigned FLAGS>
-static MatmulPlan plan_matmul(int M, int K, int N)
+static MatmulPlan plan_matmul(int M, int K, int N, bool tma_ok)
 {
     const int P = sm_count();
+    const bool tf32 = math_terms() == 1;
     const long long mt = (M + kBM - 1) / kBM;
     const int ks = (K + kBK - 1) / kBK;
     const int bn_max = N <= 32 ? 32 : N <= 64 ? 64 : N <= 128 ? 128 : 256;
     const int bn_min = bn_max < 64 ? bn_max : 64;
-    MatmulPlan best{bn_max, 1};
+    MatmulPlan best{bn_max, 1, false};
     long long best_cost = -1, best_units = 0;
+    // the TMA-fed kernel: whole tiles 128 or 256 wide on a persistent grid
+    if (tma_ok) {
+        for (int bn = bn_max; bn >= 128; bn /= 2) {
+            const long long tiles = mt * ((N + bn - 1) / bn);
+            const long long cost = ((tiles + P - 1) / P) * (ks + kTileFixedStages) * tma_rows(bn, tf32) * 4;
+            if (best_cost < 0 || cost < best_cost) {
+                best_cost = cost;
+                best_units = tiles;
+                best = MatmulPlan{bn, 1, true};
+            }
+        }
+    }
     for (int bn = bn_max; bn >= bn_min; bn /= 2) {
         const long long tiles = mt * ((N + bn - 1) / bn);
         const long long rows_a = M < kBM ? M : kBM;
@@ -317,14 +343,15 @@ static MatmulPlan plan_matmul(int M, int K, int N)
             if (slots <= 0) continue;
             const long long rounds = (tiles + slots - 1) / slots;
             const long long per = (ks + cs - 1) / cs + (cs == 1 ? kTileFixedStages : kClusterFixedStages);
-            const long long cost = rounds * per * (rows_a + rows_b);
+            // (a TF32 stage stores no lo tiles: about three quarters of the 3xTF32 cost, measured)
+            const long long cost = rounds * per * (rows_a + rows_b) * (tf32 ? 3 : 4);
             // on a tie the plan with more CTAs wins: they share the same work
             // (small shapes are latency-bound)
             const long long units = tiles * cs;
             if (best_cost < 0 || cost < best_cost || (cost == best_cost && units > best_units)) {
                 best_cost = cost;
                 best_units = units;
-                best = MatmulPlan{bn, cs};
+                best = MatmulPlan{bn, cs, false};
             }
         }
     }
@@ -361,11 +388,54 @@ static cudaError_t run_matmul(int M, int K, int N, int cs, const float* A, const
     return launch_tc_gemm<MatmulProb<FLAGS, BN>, BN>(p, p.m_tiles * p.n_tiles * p.csplit, device_error_word(), st);
 }
 
+// TMA-fed path (gemm_tma.cuh): both operands K-contiguous (flags 2), K a
+// multiple of 4 (the tensor maps' row pitch must be a multiple of 16 bytes),
+// 16-byte aligned operands, no fused epilogue, and a plan of whole tiles at
+// least 128 wide.  Everything else runs on the register-gather engine.
+static bool tma_ok(unsigned flags, int N, int K, const float* A, const float* B, const MatmulEpi& ep)
+{
+    return flags == 2u && N > 64 && K % 4 == 0 && aligned16(A) && aligned16(B) && !ep.bias && !ep.gate && !ep.relu;
+}
+
+static cudaError_t encode_kmajor(CUtensorMap* map, const float* X, int rows, int K, int box_rows)
+{
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(K) * 4};
+    const cuuint32_t box[2] = {cuuint32_t(kTmaBK), cuuint32_t(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(X), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int BN>
+static cudaError_t run_tma(int M, int K, int N, const float* A, const float* B, float* C, cudaStream_t st)
+{
+    TmaGemmArgs args{};
+    cudaError_t e = encode_kmajor(&args.ta, A, M, K, kBM);
+    if (e != cudaSuccess) return e;
+    if ((e = encode_kmajor(&args.tb, B, N, K, BN)) != cudaSuccess) return e;
+    args.C = C;
+    args.M = M;
+    args.N = N;
+    args.K = K;
+    args.m_tiles = (M + kBM - 1) / kBM;
+    args.n_tiles = (N + BN - 1) / BN;
+    args.k_stages = (K + kTmaBK - 1) / kTmaBK;
+    args.vec_c = (N % 4 == 0) && aligned16(C);
+    return math_terms() == 1 ? launch_tma_gemm_terms<BN, 1>(args, device_error_word(), st)
+                             : launch_tma_gemm_terms<BN, 3>(args, device_error_word(), st);
+}
+
 template <unsigned FLAGS>
 static cudaError_t run_flags(int M, int K, int N, const float* A, const float* B, float* C, const MatmulEpi& ep,
                              cudaStream_t st)
 {
-    const MatmulPlan pl = plan_matmul<FLAGS>(M, K, N);
+    const MatmulPlan pl = plan_matmul<FLAGS>(M, K, N, tma_ok(FLAGS, N, K, A, B, ep));
+    if (pl.tma) return pl.bn == 256 ? run_tma<256>(M, K, N, A, B, C, st) : run_tma<128>(M, K, N, A, B, C, st);
     switch (pl.bn) {
     case 256: return run_matmul<FLAGS, 256>(M, K, N, pl.cs, A, B, C, ep, st);
     case 128: return run_matmul<FLAGS, 128>(M, K, N, pl.cs, A, B, C, ep, st);
@@ -374,17 +444,20 @@ static cudaError_t run_flags(int M, int K, int N, const float* A, const float* B
     }
 }
 
-void matmul_tiling(int M, int K, int N, unsigned flags, int* bn, int* csplit)
+void matmul_tiling(int M, int K, int N, unsigned flags, const float* A, const float* B, int* bn, int* csplit,
+                   int* tma)
 {
     MatmulPlan pl;
+    const bool ok = tma_ok(flags, N, K, A, B, MatmulEpi{});
     switch (flags) {
-    case 0: pl = plan_matmul<0>(M, K, N); break;
-    case 1: pl = plan_matmul<1>(M, K, N); break;
-    case 2: pl = plan_matmul<2>(M, K, N); break;
-    default: pl = plan_matmul<3>(M, K, N); break;
+    case 0: pl = plan_matmul<0>(M, K, N, ok); break;
+    case 1: pl = plan_matmul<1>(M, K, N, ok); break;
+    case 2: pl = plan_matmul<2>(M, K, N, ok); break;
+    default: pl = plan_matmul<3>(M, K, N, ok); break;
     }
     *bn = pl.bn;
     *csplit = pl.cs;
+    *tma = pl.tma ? 1 : 0;
 }
 
 cudaError_t launch_matmul(int M, int K, int N, unsigned flags, const float* A, const float* B, float* C,

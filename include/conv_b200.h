@@ -189,16 +189,20 @@ int matmul(int32_t M, int32_t K, int32_t N, uint32_t flags, const float *A, cons
 int matmul_fused(int32_t M, int32_t K, int32_t N, uint32_t flags, const float *A, const float *B, const float *bias,
                  int32_t relu, const float *gate, float *C, conv_stream_t stream);
 
-/* How matmul tiles an M x K x N product on the current device and in the
- * current math mode (a host-side query, no GPU work): *tile_cols = width of
- * an output tile (32, 64, 128 or 256 columns; tiles are 128 rows);
- * *k_pieces = number of pieces each tile's K range is cut into when there are
- * too few tiles for the SMs (1: whole tiles).  The pieces of a tile run on the
- * CTAs of one thread-block cluster and are added in a fixed order through
- * distributed shared memory, so results stay deterministic.  Returns CONV_OK,
- * CONV_ERR_NULL (an output pointer is NULL), CONV_ERR_SHAPE (as matmul) or
- * CONV_ERR_DEVICE. */
-int matmul_tiling(int32_t M, int32_t K, int32_t N, uint32_t flags, int32_t *tile_cols, int32_t *k_pieces);
+/* How matmul runs an M x K x N product with operands at A and B (a
+ * host-side query, no GPU work; only the operands' alignment is looked at,
+ * they may be NULL) on the current device and in the current math mode:
+ * *tile_cols = width of an output tile (32, 64, 128 or 256 columns; tiles are
+ * 128 rows); *k_pieces = number of pieces each tile's K range is cut into when
+ * there are too few tiles for the SMs (1: whole tiles) -- the pieces of a tile
+ * run on the CTAs of one thread-block cluster and are added in a fixed order
+ * through distributed shared memory, so results stay deterministic;
+ * *tma_fed = 1 when both operands arrive by TMA tensor copies (flags 2, K a
+ * multiple of 4, 16-byte aligned operands, whole tiles at least 128 wide),
+ * 0 when the producer warps gather them.  Returns CONV_OK, CONV_ERR_NULL (an
+ * output pointer is NULL), CONV_ERR_SHAPE (as matmul) or CONV_ERR_DEVICE. */
+int matmul_tiling(int32_t M, int32_t K, int32_t N, uint32_t flags, const float *A, const float *B,
+                  int32_t *tile_cols, int32_t *k_pieces, int32_t *tma_fed);
 
 /* Max pooling forward (nn_maxpool_forward, section "Pooling Shaders"):
  * k x k windows, stride `stride`, no padding, outH = (H - k) / stride + 1.

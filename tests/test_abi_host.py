@@ -140,11 +140,14 @@ def test_matmul_fused_validation(lib):
 
 def test_matmul_tiling_validation(lib):
     """The tiling query validates its arguments before it looks for a device."""
-    bn, pieces = ctypes.c_int32(0), ctypes.c_int32(0)
-    assert lib.matmul_tiling(4, 4, 4, 0, NULL, ctypes.byref(pieces)) == ERR_NULL
-    assert lib.matmul_tiling(4, 4, 4, 0, ctypes.byref(bn), NULL) == ERR_NULL
-    assert lib.matmul_tiling(0, 4, 4, 0, ctypes.byref(bn), ctypes.byref(pieces)) == ERR_SHAPE
-    assert lib.matmul_tiling(4, 4, 4, 4, ctypes.byref(bn), ctypes.byref(pieces)) == ERR_SHAPE
+    bn, pieces, tma = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)
+    assert lib.matmul_tiling(4, 4, 4, 0, NULL, NULL, NULL, ctypes.byref(pieces), ctypes.byref(tma)) == ERR_NULL
+    assert lib.matmul_tiling(4, 4, 4, 0, NULL, NULL, ctypes.byref(bn), NULL, ctypes.byref(tma)) == ERR_NULL
+    assert lib.matmul_tiling(4, 4, 4, 0, NULL, NULL, ctypes.byref(bn), ctypes.byref(pieces), NULL) == ERR_NULL
+    assert lib.matmul_tiling(0, 4, 4, 0, NULL, NULL, ctypes.byref(bn), ctypes.byref(pieces),
+                             ctypes.byref(tma)) == ERR_SHAPE
+    assert lib.matmul_tiling(4, 4, 4, 4, NULL, NULL, ctypes.byref(bn), ctypes.byref(pieces),
+                             ctypes.byref(tma)) == ERR_SHAPE
 
 
 def test_math_mode_switch(lib):

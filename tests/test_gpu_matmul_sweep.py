@@ -117,15 +117,34 @@ def test_sweep_reaches_every_tiling(cb):
     columns) and both whole tiles and K cut over clusters of 2, 4 and 8 CTAs
     (the cluster split: few tiles, long K)."""
     for flags in range(4):
-        widths, pieces = set(), set()
+        widths, pieces, tma = set(), set(), set()
         for M in synthetic.MATMUL_MN:
             for N in synthetic.MATMUL_MN:
                 for K in synthetic.MATMUL_K:
-                    bn, p = cb.matmul_tiling(M, K, N, flags)
+                    bn, p, fed = cb.matmul_tiling(M, K, N, flags, with_tma=True)
                     widths.add(bn)
                     pieces.add(p)
+                    tma.add(fed)
         assert widths == {32, 64, 128, 256}, (flags, widths)
         assert {1, 2, 4, 8} <= pieces, (flags, pieces)
+        # both operands K-contiguous (flags 2): the large cases arrive by TMA
+        assert tma == ({False, True} if flags == 2 else {False}), (flags, tma)
+
+
+# The TMA-fed path (flags 2, whole tiles >= 128 wide) on ragged shapes: M and
+# N past the last full tile (the boxes zero-fill, the epilogue drops rows and
+# columns past C), K not a multiple of the 16-deep stage; both math modes.
+TMA_SHAPES = [(5000, 1024, 5000), (2500, 2048, 9000), (4096, 100, 4096)]
+
+
+@pytest.mark.parametrize("M,K,N", TMA_SHAPES)
+def test_tma_fed_ragged(cb, orc, pools, M, K, N):
+    import torch
+    a, b = views(pools[1], M, K, N, 2)
+    assert cb.matmul_tiling(M, K, N, 2, a, b, with_tma=True)[2], "expected the TMA-fed path"
+    run_case(cb, orc, pools, M, K, N, 2)
+    with cb.math(cb.CONV_MATH_TF32):
+        assert run_case(cb, orc, pools, M, K, N, 2, tol_scale=2.5e-3) <= 1.0
 
 
 # Shapes whose tiles are cut over clusters, checked against the full oracle
