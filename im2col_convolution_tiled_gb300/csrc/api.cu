@@ -55,6 +55,10 @@ static std::atomic<int> g_math_mode{CONV_MATH_FP32};
 // GEMM launch withholds.  One-shot: the launch that takes it resets it.
 static std::atomic<long long> g_withhold_stage{-1};
 long long take_withhold_stage() { return g_withhold_stage.exchange(-1, std::memory_order_relaxed); }
+
+// Test hook of the matmul engine choice (conv_b200_debug_matmul_engine).
+static std::atomic<int> g_matmul_engine{-1};
+int matmul_engine_override() { return g_matmul_engine.load(std::memory_order_relaxed); }
 int math_terms() { return g_math_mode.load(std::memory_order_relaxed) == CONV_MATH_TF32 ? 1 : 3; }
 
 int* device_error_word()
@@ -471,6 +475,12 @@ int softmax_ce(int32_t rows, int32_t cols, const float* logits, const int32_t* l
 }
 
 uint64_t conv_b200_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int conv_b200_debug_matmul_engine(int32_t engine)
+{
+    if (engine < -1 || engine > 1) return CONV_ERR_SHAPE;
+    return g_matmul_engine.exchange(engine, std::memory_order_relaxed);
+}
 
 int conv_b200_debug_withhold_stage(int64_t stage)
 {

@@ -33,6 +33,8 @@ void note_launch();
 // The stage set by conv_b200_debug_withhold_stage (or -1), taken -- and reset
 // to -1 -- by the next launch of the register-gather GEMM kernel.
 long long take_withhold_stage();
+// The matmul engine test hook: -1 plan, 0 register gather, 1 TMA where eligible.
+int matmul_engine_override();
 
 inline cudaStream_t as_cuda(conv_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
@@ -75,6 +77,10 @@ struct MatmulEpi {
 };
 cudaError_t launch_matmul(int M, int K, int N, unsigned flags, const float* A, const float* B, float* C,
                           cudaStream_t st, const MatmulEpi& ep = MatmulEpi{});
+// The TMA-fed kernel for a planned matmul (matmul_tma.cu): flags 0..3, tile
+// width bn (128 or 256); the caller has checked the operands qualify.
+cudaError_t launch_matmul_tma(unsigned flags, int bn, int M, int K, int N, const float* A, const float* B, float* C,
+                              cudaStream_t st);
 
 cudaError_t launch_bias_grad(const ConvDims& d, const float* dy, float* db, cudaStream_t st);
 cudaError_t launch_im2col(const ConvDims& d, const float* x, float* col, cudaStream_t st);

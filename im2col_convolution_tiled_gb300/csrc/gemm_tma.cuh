@@ -1,6 +1,5 @@
 // gemm_tma.cuh -- tcgen05 GEMM whose operands arrive by TMA, for the flagged
-// matmul when both operands are K-contiguous (flags 2: A stored M x K, B
-// stored N x K) and the shape is large enough for wide tiles.
+// matmul when the shape is large enough for wide tiles, any flags.
 //
 // D (128 x BN tile, fp32, tensor memory) = sum over K of A(128 x K) B(BN x K)^T.
 // A stage is 16 deep: one 2-D TMA box per operand ({16 fp32, rows}, 64-byte
@@ -15,12 +14,21 @@
 // swizzle is a function of the address, so the same offsets serve both).
 // Each 8-deep step then issues lo*hi, hi*lo and hi*hi -- or, for tiles at
 // most 128 wide, whose B hi and lo rows lie back to back, hi*[hi; lo] as one
-// MMA with N = 2*BN plus lo*hi.  One TF32 product (TERMS == 1) needs no
-// converter at all: the MMAs read what TMA delivered.
+// MMA with N = 2*BN plus lo*hi.  One TF32 product (TERMS == 1) of
+// K-contiguous operands needs no converter at all: the MMAs read what TMA
+// delivered.
+//
+// An operand stored with its rows contiguous (A stored K x M, B stored K x N:
+// AT / BT) lands raw, in [16 k][32 r] boxes with the 128-byte swizzle, in a
+// buffer of its stage; the converters transpose each box into the K-major
+// tile (hi, and lo in 3xTF32): a lane takes a 4 x 4 block, four 16-byte reads
+// down k, four 16-byte writes along r (lane (r4, k4) = (lane % 8,
+// (lane / 8) ^ (lane % 4)): at most two lanes of a quarter-warp share a bank
+// group on either side).
 //
 // Roles (320 threads, one CTA per SM, persistent over tiles, n fastest):
 //   warp 0       TMA producer (lane 0): one A box and one B box per stage
-//   warps 1-4    converters: the stage's lo tiles (3xTF32)
+//   warps 1-4    converters: the stage's lo tiles (3xTF32) and transposes
 //   warp 5       MMA issuer (lane 0); allocates tensor memory
 //   warps 6-9    epilogue: tcgen05.ld, row-major C with 16-byte stores
 // Two accumulator buffers: the epilogue of tile i overlaps tile i+1.  Every
@@ -36,16 +44,19 @@ namespace cb200 {
 
 constexpr int kTmaBK = 16;   // K depth of a stage: one 64-byte swizzle row
 
-template <int BN, int TERMS>
+template <int BN, int TERMS, bool AT = false, bool BT = false>
 struct TmaCfg {
     static_assert(BN == 128 || BN == 256, "TMA-fed tiles are 128 or 256 wide");
     static constexpr bool kThree = TERMS == 3;
     static constexpr bool kStack = kThree && BN <= 128;   // hi|lo B rows back to back: N = 2*BN
+    static constexpr bool kConvert = kThree || AT || BT;  // converters have work
     static constexpr int kThreads = 320;
     static constexpr uint32_t kATile = kBM * kTmaBK * 4;   // 8 KB
     static constexpr uint32_t kBTile = BN * kTmaBK * 4;
-    // stage: A hi, [A lo], B hi, [B lo]
-    static constexpr uint32_t kStage = (kThree ? 2u : 1u) * (kATile + kBTile);
+    static constexpr uint32_t kARaw = AT ? kATile : 0u;    // raw boxes of a rows-contiguous operand
+    static constexpr uint32_t kBRaw = BT ? kBTile : 0u;
+    // stage: A hi, [A lo], B hi, [B lo], [A raw], [B raw]
+    static constexpr uint32_t kStage = (kThree ? 2u : 1u) * (kATile + kBTile) + kARaw + kBRaw;
     static constexpr size_t kCtlBytes = 512;
     static constexpr int kStages0 = int((216u * 1024u) / kStage);
     static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
@@ -60,8 +71,10 @@ struct TmaCfg {
 };
 
 struct TmaGemmArgs {
-    alignas(64) CUtensorMap ta;   // A: dims {K, M}, box {16, 128}, 64-byte swizzle
-    alignas(64) CUtensorMap tb;   // B: dims {K, N}, box {16, BN}
+    // K-contiguous operand: dims {K, rows}, box {16, rows of the tile}, 64-byte swizzle;
+    // rows-contiguous operand: dims {rows, K}, box {32, 16}, 128-byte swizzle
+    alignas(64) CUtensorMap ta;
+    alignas(64) CUtensorMap tb;
     float* C;
     int M, N, K;
     int m_tiles, n_tiles, k_stages;
@@ -88,11 +101,50 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, in
         : "memory");
 }
 
-template <int BN, int TERMS>
-__global__ void __launch_bounds__(TmaCfg<BN, TERMS>::kThreads, 1)
+__device__ __forceinline__ uint32_t u4_at(const uint4& v, int j)
+{
+    return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+}
+
+__device__ __forceinline__ uint4 lo_of(uint4 v)
+{
+    uint32_t h, l0, l1, l2, l3;
+    split_tf32(__uint_as_float(v.x), h, l0);
+    split_tf32(__uint_as_float(v.y), h, l1);
+    split_tf32(__uint_as_float(v.z), h, l2);
+    split_tf32(__uint_as_float(v.w), h, l3);
+    return make_uint4(l0, l1, l2, l3);
+}
+
+// One raw [16 k][32 r] box (128-byte swizzle) -> rows r0 .. r0+31 of a K-major
+// tile with 64-byte rows (64-byte swizzle): the raw values as hi (the tensor
+// core drops their low bits), and with LO their a - trunc(a) parts.
+template <bool LO>
+__device__ __forceinline__ void transpose_box(const uint8_t* raw, uint8_t* hi, uint8_t* lo, int r0, int lane)
+{
+    const int r4 = lane & 7, k4 = (lane >> 3) ^ (lane & 3);
+    uint4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int k = 4 * k4 + i;
+        v[i] = *reinterpret_cast<const uint4*>(raw + k * 128 + ((r4 ^ (k & 7)) << 4));
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int r = r0 + 4 * r4 + j;
+        const uint4 row = make_uint4(u4_at(v[0], j), u4_at(v[1], j), u4_at(v[2], j), u4_at(v[3], j));
+        const int off = r * 64 + ((k4 ^ ((r >> 1) & 3)) << 4);
+        *reinterpret_cast<uint4*>(hi + off) = row;
+        if (LO) *reinterpret_cast<uint4*>(lo + off) = lo_of(row);
+    }
+}
+
+template <int BN, int TERMS, bool AT, bool BT>
+__global__ void __launch_bounds__(TmaCfg<BN, TERMS, AT, BT>::kThreads, 1)
     tc_tma_gemm_kernel(const __grid_constant__ TmaGemmArgs args, int* err_word)
 {
-    using Cfg = TmaCfg<BN, TERMS>;
+    using Cfg = TmaCfg<BN, TERMS, AT, BT>;
+    constexpr bool convert = Cfg::kConvert;
     constexpr int S = Cfg::kStages;
     constexpr bool three = Cfg::kThree;
     constexpr bool STACK = Cfg::kStack;
@@ -109,6 +161,8 @@ __global__ void __launch_bounds__(TmaCfg<BN, TERMS>::kThreads, 1)
     auto a_lo = [&](int s) { return a_hi(s) + Cfg::kATile; };
     auto b_hi = [&](int s) { return a_hi(s) + (three ? 2u : 1u) * Cfg::kATile; };
     auto b_lo = [&](int s) { return b_hi(s) + Cfg::kBTile; };
+    auto a_raw = [&](int s) { return a_hi(s) + (three ? 2u : 1u) * (Cfg::kATile + Cfg::kBTile); };
+    auto b_raw = [&](int s) { return a_raw(s) + Cfg::kARaw; };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -155,8 +209,22 @@ __global__ void __launch_bounds__(TmaCfg<BN, TERMS>::kThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(&ctl->tfull[slot], Cfg::kTxBytes);
-                    tma_load_2d(smem + (a_hi(slot) - base), &args.ta, ks * kTmaBK, m0, &ctl->tfull[slot]);
-                    tma_load_2d(smem + (b_hi(slot) - base), &args.tb, ks * kTmaBK, n0, &ctl->tfull[slot]);
+                    if constexpr (AT) {
+#pragma unroll
+                        for (int j = 0; j < kBM / 32; ++j)
+                            tma_load_2d(smem + (a_raw(slot) - base) + 2048 * j, &args.ta, m0 + 32 * j, ks * kTmaBK,
+                                        &ctl->tfull[slot]);
+                    } else {
+                        tma_load_2d(smem + (a_hi(slot) - base), &args.ta, ks * kTmaBK, m0, &ctl->tfull[slot]);
+                    }
+                    if constexpr (BT) {
+#pragma unroll
+                        for (int j = 0; j < BN / 32; ++j)
+                            tma_load_2d(smem + (b_raw(slot) - base) + 2048 * j, &args.tb, n0 + 32 * j, ks * kTmaBK,
+                                        &ctl->tfull[slot]);
+                    } else {
+                        tma_load_2d(smem + (b_hi(slot) - base), &args.tb, ks * kTmaBK, n0, &ctl->tfull[slot]);
+                    }
                     last = int(c);
                 }
             }
@@ -172,9 +240,10 @@ __global__ void __launch_bounds__(TmaCfg<BN, TERMS>::kThreads, 1)
         }
         __syncwarp();
     } else if (warp < 5) {
-        // ---------------- converters: lo = a - trunc(a), same offsets ----------------
-        if constexpr (three) {
+        // ---------------- converters: lo tiles, transposes ----------------
+        if constexpr (convert) {
             const int tid = threadIdx.x - 32;   // 0..127
+            const int cw = warp - 1;            // converter warp 0..3
             uint32_t c = 0;
             bool ok = true;
             constexpr uint32_t nA = Cfg::kATile / 16u, nB = Cfg::kBTile / 16u;
@@ -185,22 +254,26 @@ __global__ void __launch_bounds__(TmaCfg<BN, TERMS>::kThreads, 1)
                         ok = false;
                         break;
                     }
-                    const uint4* ah = reinterpret_cast<const uint4*>(smem + (a_hi(slot) - base));
-                    uint4* al = reinterpret_cast<uint4*>(smem + (a_lo(slot) - base));
-                    const uint4* bh = reinterpret_cast<const uint4*>(smem + (b_hi(slot) - base));
-                    uint4* bl = reinterpret_cast<uint4*>(smem + (b_lo(slot) - base));
-                    auto lo4 = [](uint4 v) {
-                        uint32_t h, l0, l1, l2, l3;
-                        split_tf32(__uint_as_float(v.x), h, l0);
-                        split_tf32(__uint_as_float(v.y), h, l1);
-                        split_tf32(__uint_as_float(v.z), h, l2);
-                        split_tf32(__uint_as_float(v.w), h, l3);
-                        return make_uint4(l0, l1, l2, l3);
-                    };
+                    uint8_t* ah = smem + (a_hi(slot) - base);
+                    uint8_t* al = smem + (a_lo(slot) - base);
+                    uint8_t* bh = smem + (b_hi(slot) - base);
+                    uint8_t* bl = smem + (b_lo(slot) - base);
+                    if constexpr (AT) {   // four boxes, one per converter warp
+                        transpose_box<three>(smem + (a_raw(slot) - base) + 2048 * cw, ah, al, 32 * cw, lane);
+                    } else if constexpr (three) {
 #pragma unroll
-                    for (uint32_t i = uint32_t(tid); i < nA; i += 128u) al[i] = lo4(ah[i]);
+                        for (uint32_t i = uint32_t(tid); i < nA; i += 128u)
+                            reinterpret_cast<uint4*>(al)[i] = lo_of(reinterpret_cast<const uint4*>(ah)[i]);
+                    }
+                    if constexpr (BT) {
+#pragma unroll
+                        for (int j = cw; j < BN / 32; j += 4)
+                            transpose_box<three>(smem + (b_raw(slot) - base) + 2048 * j, bh, bl, 32 * j, lane);
+                    } else if constexpr (three) {
 #pragma unroll 4
-                    for (uint32_t i = uint32_t(tid); i < nB; i += 128u) bl[i] = lo4(bh[i]);
+                        for (uint32_t i = uint32_t(tid); i < nB; i += 128u)
+                            reinterpret_cast<uint4*>(bl)[i] = lo_of(reinterpret_cast<const uint4*>(bh)[i]);
+                    }
                     fence_proxy_async_smem();   // generic-proxy writes -> visible to the tensor core
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&ctl->cfull[slot]);
@@ -227,7 +300,7 @@ __global__ void __launch_bounds__(TmaCfg<BN, TERMS>::kThreads, 1)
                     const int slot = int(c % uint32_t(S));
                     const uint32_t ph = (c / uint32_t(S)) & 1u;
                     if (!mbar_wait(&ctl->tfull[slot], ph, abort_flag) ||
-                        (three && !mbar_wait(&ctl->cfull[slot], ph, abort_flag))) {
+                        (convert && !mbar_wait(&ctl->cfull[slot], ph, abort_flag))) {
                         ok = false;
                         break;
                     }
@@ -328,22 +401,22 @@ __global__ void __launch_bounds__(TmaCfg<BN, TERMS>::kThreads, 1)
     }
 }
 
-template <int BN, int TERMS>
+template <int BN, int TERMS, bool AT, bool BT>
 cudaError_t launch_tma_gemm_terms(const TmaGemmArgs& args, int* err_word, cudaStream_t stream)
 {
-    using Cfg = TmaCfg<BN, TERMS>;
+    using Cfg = TmaCfg<BN, TERMS, AT, BT>;
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(tc_tma_gemm_kernel<BN, TERMS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             int(Cfg::kSmemBytes));
+        cudaError_t e = cudaFuncSetAttribute(tc_tma_gemm_kernel<BN, TERMS, AT, BT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cfg::kSmemBytes));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
     const int tiles = args.m_tiles * args.n_tiles;
     if (tiles <= 0) return cudaSuccess;
     const int grid = tiles < sm_count() ? tiles : sm_count();
-    cudaError_t e = launch_pdl(tc_tma_gemm_kernel<BN, TERMS>, dim3(grid), dim3(Cfg::kThreads), Cfg::kSmemBytes,
-                               stream, args, err_word);
+    cudaError_t e = launch_pdl(tc_tma_gemm_kernel<BN, TERMS, AT, BT>, dim3(grid), dim3(Cfg::kThreads),
+                               Cfg::kSmemBytes, stream, args, err_word);
     if (e != cudaSuccess) return e;
     note_launch();
     return cudaGetLastError();

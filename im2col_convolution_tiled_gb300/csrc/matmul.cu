@@ -14,7 +14,7 @@
 // cluster (the engine's cluster split): csplit CTAs each run one K piece and
 // the pieces are added in a fixed order through distributed shared memory.
 #include "gemm_tc.cuh"
-#include "gemm_tma.cuh"
+#include "gemm_tma.cuh"   // kTmaBK
 
 namespace cb200 {
 
@@ -271,21 +271,28 @@ struct MatmulProb {
 // 128 per pass for B stored K x N, whose loader reads a column per thread
 // whatever the tile's width.  Wide tiles therefore do more work per producer
 // cycle, and where they leave SMs idle the cluster split fills them.  The plan
-// minimises rounds x (stages per unit + a fixed cost) x (rows per stage) over
-// BN in {256, 128, 64} (32 when N <= 32) and 1, 2, 4 or 8 pieces per tile.
+// minimises rounds x (stages per unit + a fixed cost) x (cost of a stage) over
+// BN in {256, 128, 64} (32 when N <= 32) and 1, 2, 4 or 8 pieces per tile, and,
+// where the operands qualify, the TMA-fed kernel's whole tiles 128 or 256 wide.
 struct MatmulPlan {
     int bn, cs;
     bool tma;   // operands by TMA (gemm_tma.cuh; whole tiles, cs == 1)
 };
 
-// A TMA-fed stage's cost in the same unit (register-gathered rows at about
-// 7 cycles each), per 32 deep, measured on GB300 from its steady-state stage
-// time: 3xTF32 2390 cycles at 256 columns, 2040 at 128 (the tensor core and
-// the shared-memory port, not the loads, set it); TF32 1040-1170 and 1200.
-inline long long tma_rows(int bn, bool tf32)
+// Stage costs, measured on GB300 in cycles x 10 per 32 deep (steady-state
+// stage times of large shapes at 2070 MHz):
+// * register gather: a nearly fixed cost per operand row a producer loads,
+//   7.2 cycles in 3xTF32, 5.4 in TF32 (no lo tiles to store);
+// * TMA-fed: 2390 / 2040 cycles (3xTF32, 256 / 128 columns), 1100 / 1190
+//   (TF32) -- the tensor core and the shared-memory port set it -- plus 3.2
+//   cycles per row of an operand stored rows-contiguous, which the converters
+//   transpose through shared memory (landing, reading and rewriting it).
+constexpr long long kGatherRow10[2] = {72, 54};   // [3xTF32, TF32]
+constexpr long long kTransposeRow10 = 32;
+inline long long tma_stage10(int bn, bool tf32)
 {
-    if (tf32) return bn == 256 ? 150 : 165;
-    return bn == 256 ? 332 : 280;
+    if (tf32) return bn == 256 ? 11000 : 11900;
+    return bn == 256 ? 23900 : 20400;
 }
 
 constexpr int kTileFixedStages = 1;    // a whole tile's epilogue and hand-over
@@ -321,11 +328,15 @@ static MatmulPlan plan_matmul(int M, int K, int N, bool tma_ok)
     const int bn_min = bn_max < 64 ? bn_max : 64;
     MatmulPlan best{bn_max, 1, false};
     long long best_cost = -1, best_units = 0;
+    const int engine = matmul_engine_override();   // test hook: -1 plan, 0 gather, 1 TMA where eligible
+    if (engine == 0) tma_ok = false;
     // the TMA-fed kernel: whole tiles 128 or 256 wide on a persistent grid
     if (tma_ok) {
         for (int bn = bn_max; bn >= 128; bn /= 2) {
             const long long tiles = mt * ((N + bn - 1) / bn);
-            const long long cost = ((tiles + P - 1) / P) * (ks + kTileFixedStages) * tma_rows(bn, tf32) * 4;
+            const long long trows = ((FLAGS & 1u) ? kBM : 0) + ((FLAGS & 2u) ? 0 : bn);   // transposed rows
+            const long long cost =
+                ((tiles + P - 1) / P) * (ks + kTileFixedStages) * (tma_stage10(bn, tf32) + trows * kTransposeRow10);
             if (best_cost < 0 || cost < best_cost) {
                 best_cost = cost;
                 best_units = tiles;
@@ -337,14 +348,14 @@ static MatmulPlan plan_matmul(int M, int K, int N, bool tma_ok)
         const long long tiles = mt * ((N + bn - 1) / bn);
         const long long rows_a = M < kBM ? M : kBM;
         const long long rows_b = (FLAGS & 2u) ? (N < bn ? N : bn) : 128LL * ((bn + 127) / 128);
+        if (engine == 1 && tma_ok) break;   // forced TMA: the register plans are not candidates
         for (int cs = 1; cs <= 8; cs *= 2) {
             if (cs > 1 && ks < 2 * cs) break;
             const int slots = cs == 1 ? P : clusters_for<FLAGS>(bn, cs);
             if (slots <= 0) continue;
             const long long rounds = (tiles + slots - 1) / slots;
             const long long per = (ks + cs - 1) / cs + (cs == 1 ? kTileFixedStages : kClusterFixedStages);
-            // (a TF32 stage stores no lo tiles: about three quarters of the 3xTF32 cost, measured)
-            const long long cost = rounds * per * (rows_a + rows_b) * (tf32 ? 3 : 4);
+            const long long cost = rounds * per * (rows_a + rows_b) * kGatherRow10[tf32 ? 1 : 0];
             // on a tie the plan with more CTAs wins: they share the same work
             // (small shapes are latency-bound)
             const long long units = tiles * cs;
@@ -388,54 +399,24 @@ static cudaError_t run_matmul(int M, int K, int N, int cs, const float* A, const
     return launch_tc_gemm<MatmulProb<FLAGS, BN>, BN>(p, p.m_tiles * p.n_tiles * p.csplit, device_error_word(), st);
 }
 
-// TMA-fed path (gemm_tma.cuh): both operands K-contiguous (flags 2), K a
-// multiple of 4 (the tensor maps' row pitch must be a multiple of 16 bytes),
-// 16-byte aligned operands, no fused epilogue, and a plan of whole tiles at
-// least 128 wide.  Everything else runs on the register-gather engine.
-static bool tma_ok(unsigned flags, int N, int K, const float* A, const float* B, const MatmulEpi& ep)
+// TMA-fed path (gemm_tma.cuh): every operand's row pitch a multiple of 16
+// bytes (K % 4 == 0 for a K-contiguous operand, M or N % 4 == 0 for a
+// rows-contiguous one), 16-byte aligned operands, no fused epilogue, N > 64,
+// and a plan of whole tiles at least 128 wide.  Everything else runs on the
+// register-gather engine.
+static bool tma_ok(unsigned flags, int M, int N, int K, const float* A, const float* B, const MatmulEpi& ep)
 {
-    return flags == 2u && N > 64 && K % 4 == 0 && aligned16(A) && aligned16(B) && !ep.bias && !ep.gate && !ep.relu;
-}
-
-static cudaError_t encode_kmajor(CUtensorMap* map, const float* X, int rows, int K, int box_rows)
-{
-    EncodeTiledFn enc = encode_tiled();
-    if (!enc) return cudaErrorNotSupported;
-    const cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
-    const cuuint64_t strides[1] = {cuuint64_t(K) * 4};
-    const cuuint32_t box[2] = {cuuint32_t(kTmaBK), cuuint32_t(box_rows)};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(X), dims, strides, box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
-template <int BN>
-static cudaError_t run_tma(int M, int K, int N, const float* A, const float* B, float* C, cudaStream_t st)
-{
-    TmaGemmArgs args{};
-    cudaError_t e = encode_kmajor(&args.ta, A, M, K, kBM);
-    if (e != cudaSuccess) return e;
-    if ((e = encode_kmajor(&args.tb, B, N, K, BN)) != cudaSuccess) return e;
-    args.C = C;
-    args.M = M;
-    args.N = N;
-    args.K = K;
-    args.m_tiles = (M + kBM - 1) / kBM;
-    args.n_tiles = (N + BN - 1) / BN;
-    args.k_stages = (K + kTmaBK - 1) / kTmaBK;
-    args.vec_c = (N % 4 == 0) && aligned16(C);
-    return math_terms() == 1 ? launch_tma_gemm_terms<BN, 1>(args, device_error_word(), st)
-                             : launch_tma_gemm_terms<BN, 3>(args, device_error_word(), st);
+    const bool pitch_a = (flags & 1u) ? M % 4 == 0 : K % 4 == 0;
+    const bool pitch_b = (flags & 2u) ? K % 4 == 0 : N % 4 == 0;
+    return pitch_a && pitch_b && N > 64 && aligned16(A) && aligned16(B) && !ep.bias && !ep.gate && !ep.relu;
 }
 
 template <unsigned FLAGS>
 static cudaError_t run_flags(int M, int K, int N, const float* A, const float* B, float* C, const MatmulEpi& ep,
                              cudaStream_t st)
 {
-    const MatmulPlan pl = plan_matmul<FLAGS>(M, K, N, tma_ok(FLAGS, N, K, A, B, ep));
-    if (pl.tma) return pl.bn == 256 ? run_tma<256>(M, K, N, A, B, C, st) : run_tma<128>(M, K, N, A, B, C, st);
+    const MatmulPlan pl = plan_matmul<FLAGS>(M, K, N, tma_ok(FLAGS, M, N, K, A, B, ep));
+    if (pl.tma) return launch_matmul_tma(FLAGS, pl.bn, M, K, N, A, B, C, st);
     switch (pl.bn) {
     case 256: return run_matmul<FLAGS, 256>(M, K, N, pl.cs, A, B, C, ep, st);
     case 128: return run_matmul<FLAGS, 128>(M, K, N, pl.cs, A, B, C, ep, st);
@@ -448,7 +429,7 @@ void matmul_tiling(int M, int K, int N, unsigned flags, const float* A, const fl
                    int* tma)
 {
     MatmulPlan pl;
-    const bool ok = tma_ok(flags, N, K, A, B, MatmulEpi{});
+    const bool ok = tma_ok(flags, M, N, K, A, B, MatmulEpi{});
     switch (flags) {
     case 0: pl = plan_matmul<0>(M, K, N, ok); break;
     case 1: pl = plan_matmul<1>(M, K, N, ok); break;

@@ -361,6 +361,15 @@ int conv_fwd_noalloc(const conv_shape_t *s, const float *x, const float *w, cons
  * CONV_OK, or CONV_ERR_SHAPE for k < -1. */
 int conv_b200_debug_withhold_stage(int64_t stage);
 
+/* Test hook choosing the flagged matmul's engine (process-wide, read at each
+ * matmul call and by matmul_tiling): -1 (default) lets the plan choose from
+ * measured stage costs, 0 always gathers the operands in the producer warps,
+ * 1 feeds them by TMA wherever the operands qualify (see matmul_tiling), so
+ * that tests reach both engines in both math modes.  Results agree within the
+ * matmul's tolerance whichever engine runs.  Returns the previous setting, or
+ * CONV_ERR_SHAPE for a value outside -1..1 (nothing changes). */
+int conv_b200_debug_matmul_engine(int32_t engine);
+
 /* Text for a return code. */
 const char *conv_b200_strerror(int code);
 

@@ -129,6 +129,16 @@ def test_training_piece_validation(lib):
     assert lib.softmax_ce(-4, 10, FAKE, FAKE, NULL, FAKE, FAKE, NULL) == ERR_SHAPE
 
 
+def test_matmul_engine_hook_validation(lib):
+    """The engine test hook defaults to the plan (-1), returns the previous
+    setting and rejects values outside -1..1 (no launch happens here)."""
+    assert lib.conv_b200_debug_matmul_engine(2) == ERR_SHAPE
+    assert lib.conv_b200_debug_matmul_engine(-2) == ERR_SHAPE
+    assert lib.conv_b200_debug_matmul_engine(1) == -1
+    assert lib.conv_b200_debug_matmul_engine(0) == 1
+    assert lib.conv_b200_debug_matmul_engine(-1) == 0
+
+
 def test_matmul_fused_validation(lib):
     """matmul_fused validates like matmul; bias and gate are optional."""
     assert lib.matmul_fused(4, 4, 4, 0, NULL, FAKE, NULL, 1, NULL, FAKE, NULL) == ERR_NULL

@@ -112,11 +112,29 @@ def test_matmul_sweep(cb, orc, pools, M, flags):
     assert worst <= 1.0
 
 
+class engine:
+    """Context manager over the matmul engine test hook: -1 plan, 0 gather,
+    1 TMA wherever the operands qualify."""
+
+    def __init__(self, cb, which):
+        self.lib, self.which = cb.lib(), which
+
+    def __enter__(self):
+        self.prev = self.lib.conv_b200_debug_matmul_engine(self.which)
+        assert self.prev in (-1, 0, 1)
+
+    def __exit__(self, *exc):
+        self.lib.conv_b200_debug_matmul_engine(self.prev)
+
+
 def test_sweep_reaches_every_tiling(cb):
     """Over the sweep, each flag combination meets every tile width (32 to 256
     columns) and both whole tiles and K cut over clusters of 2, 4 and 8 CTAs
-    (the cluster split: few tiles, long K)."""
-    for flags in range(4):
+    (the cluster split: few tiles, long K).  The plan feeds the large
+    K-contiguous cases (flags 2) by TMA in both math modes, and those with one
+    rows-contiguous operand in TF32 mode, where that measured faster; forced,
+    every flag reaches it."""
+    def survey(flags):
         widths, pieces, tma = set(), set(), set()
         for M in synthetic.MATMUL_MN:
             for N in synthetic.MATMUL_MN:
@@ -125,26 +143,41 @@ def test_sweep_reaches_every_tiling(cb):
                     widths.add(bn)
                     pieces.add(p)
                     tma.add(fed)
+        return widths, pieces, tma
+    for flags in range(4):
+        widths, pieces, tma = survey(flags)
         assert widths == {32, 64, 128, 256}, (flags, widths)
         assert {1, 2, 4, 8} <= pieces, (flags, pieces)
-        # both operands K-contiguous (flags 2): the large cases arrive by TMA
-        assert tma == ({False, True} if flags == 2 else {False}), (flags, tma)
+        if flags == 2:
+            assert tma == {False, True}, (flags, tma)
+        with engine(cb, 1):
+            assert survey(flags)[2] == {False, True}, flags   # small or misaligned pitches stay gathered
+        with engine(cb, 0):
+            assert survey(flags)[2] == {False}, flags
+    with cb.math(cb.CONV_MATH_TF32):   # one rows-contiguous operand (A stored K x M)
+        assert True in survey(3)[2]
 
 
-# The TMA-fed path (flags 2, whole tiles >= 128 wide) on ragged shapes: M and
-# N past the last full tile (the boxes zero-fill, the epilogue drops rows and
-# columns past C), K not a multiple of the 16-deep stage; both math modes.
+# The TMA-fed path (whole tiles >= 128 wide; K-contiguous operands land as
+# they are, rows-contiguous ones are transposed by the converters) on ragged
+# shapes: M and N past the last full tile (the boxes zero-fill, the epilogue
+# drops rows and columns past C), K not a multiple of the 16-deep stage; every
+# flag combination, both math modes.
 TMA_SHAPES = [(5000, 1024, 5000), (2500, 2048, 9000), (4096, 100, 4096)]
 
 
+@pytest.mark.parametrize("which", [1, 0])
+@pytest.mark.parametrize("flags", [0, 1, 2, 3])
 @pytest.mark.parametrize("M,K,N", TMA_SHAPES)
-def test_tma_fed_ragged(cb, orc, pools, M, K, N):
-    import torch
-    a, b = views(pools[1], M, K, N, 2)
-    assert cb.matmul_tiling(M, K, N, 2, a, b, with_tma=True)[2], "expected the TMA-fed path"
-    run_case(cb, orc, pools, M, K, N, 2)
-    with cb.math(cb.CONV_MATH_TF32):
-        assert run_case(cb, orc, pools, M, K, N, 2, tol_scale=2.5e-3) <= 1.0
+def test_engines_ragged(cb, orc, pools, M, K, N, flags, which):
+    """Both engines, forced, on the shapes above (which = 1: TMA-fed, 0:
+    register gather), in both math modes."""
+    a, b = views(pools[1], M, K, N, flags)
+    with engine(cb, which):
+        assert cb.matmul_tiling(M, K, N, flags, a, b, with_tma=True)[2] == bool(which)
+        run_case(cb, orc, pools, M, K, N, flags)
+        with cb.math(cb.CONV_MATH_TF32):
+            assert run_case(cb, orc, pools, M, K, N, flags, tol_scale=2.5e-3) <= 1.0
 
 
 # Shapes whose tiles are cut over clusters, checked against the full oracle
