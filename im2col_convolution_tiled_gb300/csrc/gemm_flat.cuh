@@ -42,6 +42,7 @@
 // flag, records the timeout, waits (bounded) for its own copies and MMAs in
 // flight, frees tensor memory and returns.
 #pragma once
+#include <atomic>
 #include <cuda.h>   // CUtensorMap (type only)
 
 #include "gemm_tc.cuh"
@@ -56,19 +57,17 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
 
 inline EncodeTiledFn encode_tiled()
 {
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+    // a function-local static's initialiser runs once, thread-safely
+    static const EncodeTiledFn fn = []() -> EncodeTiledFn {
         void* p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-        else
-            cudaGetLastError();
-    }
+            return reinterpret_cast<EncodeTiledFn>(p);
+        cudaGetLastError();
+        return nullptr;
+    }();
     return fn;
 }
 
@@ -434,7 +433,7 @@ template <class Prob, int BN, int TERMS>
 cudaError_t launch_tc_flat_terms(const Prob& prob, int num_tiles, int* err_word, cudaStream_t stream)
 {
     using Cfg = FlatCfg<BN>;
-    static bool attr_set = false;
+    static std::atomic<bool> attr_set{false};   // set once; racing setters are harmless
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(tc_flat_kernel<Prob, BN, TERMS>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);

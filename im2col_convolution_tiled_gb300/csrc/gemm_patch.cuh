@@ -41,6 +41,7 @@
 // converter warp waits on every chunk's "patch loaded" barrier and signals its
 // "patch read" barrier.  All waits are bounded (ptx.cuh).
 #pragma once
+#include <atomic>
 #include <cuda.h>   // CUtensorMap (the type only; encoding is done on the host through the runtime's driver entry point)
 
 #include "gemm_tc.cuh"
@@ -603,7 +604,7 @@ template <class Prob, int BN, bool TMA, bool DB2, int TERMS, bool STACK>
 cudaError_t launch_tc_patch_terms(const Prob& prob, int num_tiles, int* err_word, cudaStream_t stream)
 {
     using Cfg = PatchCfg<BN, DB2, STACK>;
-    static bool attr_set = false;
+    static std::atomic<bool> attr_set{false};   // set once; racing setters are harmless
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(tc_patch_kernel<Prob, BN, TMA, DB2, TERMS, STACK>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cfg::kMaxSmem));

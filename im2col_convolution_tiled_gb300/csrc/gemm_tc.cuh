@@ -56,6 +56,7 @@
 // partials of all pieces in rank order through distributed shared memory and
 // hands the sums to prob.reduce_store.  Deterministic, no global workspace.
 #pragma once
+#include <atomic>
 #include <cooperative_groups.h>
 
 #include "ptx.cuh"
@@ -606,9 +607,10 @@ template <class Prob, int BN, int TERMS>
 int max_active_clusters(int cs)
 {
     using Cfg = TileCfg<BN, UsesTmemA<Prob>::value>;
-    static int cache[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
+    static std::atomic<int> cache[9];   // 0: not asked yet, -1: none fit (calls from several threads may race)
     if (cs < 1 || cs > 8) return 0;
-    if (cache[cs] != 0) return cache[cs] > 0 ? cache[cs] : 0;
+    const int hit = cache[cs].load(std::memory_order_relaxed);
+    if (hit != 0) return hit > 0 ? hit : 0;
     int n = 0;
     if (cudaFuncSetAttribute(tc_gemm_kernel<Prob, BN, TERMS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(Cfg::kSmemBytes)) == cudaSuccess) {
@@ -626,7 +628,7 @@ int max_active_clusters(int cs)
         if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_kernel<Prob, BN, TERMS>, &cfg) != cudaSuccess) n = 0;
     }
     (void)cudaGetLastError();
-    cache[cs] = n > 0 ? n : -1;
+    cache[cs].store(n > 0 ? n : -1, std::memory_order_relaxed);
     return n > 0 ? n : 0;
 }
 
@@ -636,7 +638,7 @@ cudaError_t launch_tc_gemm_terms(const Prob& prob, int num_tiles, int* err_word,
 {
     using Cfg = TileCfg<BN, UsesTmemA<Prob>::value>;
     constexpr int kThreads = EngineRoles<Prob, BN>::R::kThreads;
-    static bool attr_set = false;   // per process; the attribute is per function
+    static std::atomic<bool> attr_set{false};   // per process; the attribute is per function
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<Prob, BN, TERMS>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cfg::kSmemBytes));

@@ -36,6 +36,7 @@
 // records the timeout, waits (bounded) for its own copies and MMAs in flight,
 // frees tensor memory and returns.
 #pragma once
+#include <atomic>
 #include <cuda.h>   // CUtensorMap (type only)
 
 #include "gemm_flat.cuh"   // sdesc_k_sw64
@@ -405,7 +406,7 @@ template <int BN, int TERMS, bool AT, bool BT>
 cudaError_t launch_tma_gemm_terms(const TmaGemmArgs& args, int* err_word, cudaStream_t stream)
 {
     using Cfg = TmaCfg<BN, TERMS, AT, BT>;
-    static bool attr_set = false;
+    static std::atomic<bool> attr_set{false};   // set once; racing setters are harmless
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(tc_tma_gemm_kernel<BN, TERMS, AT, BT>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cfg::kSmemBytes));

@@ -9,6 +9,7 @@
 // every output element produced by exactly one thread in a fixed order (no
 // atomics; results are deterministic and, for the integer/routing work,
 // bit-exact).
+#include <atomic>
 #include <cooperative_groups.h>
 
 #include "gemm_tc.cuh"
@@ -1080,7 +1081,7 @@ static cudaError_t launch_pool_bwd_walk(int NC, int H, int W, int P, int Q, cons
 // Blocks per SM for a staged kernel using `smem` bytes of dynamic shared memory.
 static int staged_grid(int groups, size_t smem, int max_per_sm = 4)
 {
-    static bool attr_set = false;
+    static std::atomic<bool> attr_set{false};   // set once; racing setters are harmless
     if (!attr_set) {
         cudaFuncSetAttribute(maxpool_fwd_staged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
         attr_set = true;
