@@ -288,6 +288,11 @@ struct MatmulPlan {
 //   cycles per row of an operand stored rows-contiguous, which the converters
 //   transpose through shared memory (landing, reading and rewriting it).
 constexpr long long kGatherRow10[2] = {72, 54};   // [3xTF32, TF32]
+// ... scaled per flag combination (percent), measured at 256 columns on
+// 9216 x 9216 x 4096 against the 384-row model: how each operand is gathered
+// (A: 16 bytes along K or four rows of one k; B: a column per thread or 16
+// bytes along K) shows in the stage time.
+constexpr long long kGatherFlagPct[2][4] = {{89, 99, 107, 109}, {101, 99, 100, 123}};
 constexpr long long kTransposeRow10 = 32;
 inline long long tma_stage10(int bn, bool tf32)
 {
@@ -335,8 +340,8 @@ static MatmulPlan plan_matmul(int M, int K, int N, bool tma_ok)
         for (int bn = bn_max; bn >= 128; bn /= 2) {
             const long long tiles = mt * ((N + bn - 1) / bn);
             const long long trows = ((FLAGS & 1u) ? kBM : 0) + ((FLAGS & 2u) ? 0 : bn);   // transposed rows
-            const long long cost =
-                ((tiles + P - 1) / P) * (ks + kTileFixedStages) * (tma_stage10(bn, tf32) + trows * kTransposeRow10);
+            const long long cost = ((tiles + P - 1) / P) * (ks + kTileFixedStages) *
+                                   (tma_stage10(bn, tf32) + trows * kTransposeRow10);
             if (best_cost < 0 || cost < best_cost) {
                 best_cost = cost;
                 best_units = tiles;
@@ -355,7 +360,8 @@ static MatmulPlan plan_matmul(int M, int K, int N, bool tma_ok)
             if (slots <= 0) continue;
             const long long rounds = (tiles + slots - 1) / slots;
             const long long per = (ks + cs - 1) / cs + (cs == 1 ? kTileFixedStages : kClusterFixedStages);
-            const long long cost = rounds * per * (rows_a + rows_b) * kGatherRow10[tf32 ? 1 : 0];
+            const long long cost =
+                rounds * per * (rows_a + rows_b) * kGatherRow10[tf32 ? 1 : 0] * kGatherFlagPct[tf32 ? 1 : 0][FLAGS] / 100;
             // on a tie the plan with more CTAs wins: they share the same work
             // (small shapes are latency-bound)
             const long long units = tiles * cs;
