@@ -335,9 +335,11 @@ static MatmulPlan plan_matmul(int M, int K, int N, bool tma_ok)
     long long best_cost = -1, best_units = 0;
     const int engine = matmul_engine_override();   // test hook: -1 plan, 0 gather, 1 TMA where eligible
     if (engine == 0) tma_ok = false;
-    // the TMA-fed kernel: whole tiles 128 or 256 wide on a persistent grid
-    if (tma_ok) {
+    // the TMA-fed kernel: whole tiles 128 or 256 wide on a persistent grid,
+    // whose boxes (128 rows of A, bn rows of B) the tensors can fill
+    if (tma_ok && M >= kBM) {
         for (int bn = bn_max; bn >= 128; bn /= 2) {
+            if (N < bn) continue;
             const long long tiles = mt * ((N + bn - 1) / bn);
             const long long trows = ((FLAGS & 1u) ? kBM : 0) + ((FLAGS & 2u) ? 0 : bn);   // transposed rows
             const long long cost = ((tiles + P - 1) / P) * (ks + kTileFixedStages) *
@@ -353,7 +355,7 @@ static MatmulPlan plan_matmul(int M, int K, int N, bool tma_ok)
         const long long tiles = mt * ((N + bn - 1) / bn);
         const long long rows_a = M < kBM ? M : kBM;
         const long long rows_b = (FLAGS & 2u) ? (N < bn ? N : bn) : 128LL * ((bn + 127) / 128);
-        if (engine == 1 && tma_ok) break;   // forced TMA: the register plans are not candidates
+        if (engine == 1 && best.tma) break;   // forced TMA: the register plans are not candidates
         for (int cs = 1; cs <= 8; cs *= 2) {
             if (cs > 1 && ks < 2 * cs) break;
             const int slots = cs == 1 ? P : clusters_for<FLAGS>(bn, cs);
@@ -407,9 +409,9 @@ static cudaError_t run_matmul(int M, int K, int N, int cs, const float* A, const
 
 // TMA-fed path (gemm_tma.cuh): every operand's row pitch a multiple of 16
 // bytes (K % 4 == 0 for a K-contiguous operand, M or N % 4 == 0 for a
-// rows-contiguous one), 16-byte aligned operands, no fused epilogue, N > 64,
-// and a plan of whole tiles at least 128 wide.  Everything else runs on the
-// register-gather engine.
+// rows-contiguous one), 16-byte aligned operands, no fused epilogue; the plan
+// then offers it whole tiles 128 or 256 wide that M and N fill (M >= 128,
+// N >= the tile width).  Everything else runs on the register-gather engine.
 static bool tma_ok(unsigned flags, int M, int N, int K, const float* A, const float* B, const MatmulEpi& ep)
 {
     const bool pitch_a = (flags & 1u) ? M % 4 == 0 : K % 4 == 0;

@@ -197,10 +197,14 @@ int matmul_fused(int32_t M, int32_t K, int32_t N, uint32_t flags, const float *A
  * there are too few tiles for the SMs (1: whole tiles) -- the pieces of a tile
  * run on the CTAs of one thread-block cluster and are added in a fixed order
  * through distributed shared memory, so results stay deterministic;
- * *tma_fed = 1 when both operands arrive by TMA tensor copies (flags 2, K a
- * multiple of 4, 16-byte aligned operands, whole tiles at least 128 wide),
- * 0 when the producer warps gather them.  Returns CONV_OK, CONV_ERR_NULL (an
- * output pointer is NULL), CONV_ERR_SHAPE (as matmul) or CONV_ERR_DEVICE. */
+ * *tma_fed = 1 when the operands arrive by TMA tensor copies, 0 when the
+ * producer warps gather them.  TMA qualifies when every operand's row pitch
+ * is a multiple of 16 bytes (K % 4 == 0 for an operand stored with K
+ * contiguous, M or N % 4 == 0 for one stored K-major), the operands are
+ * 16-byte aligned, M >= 128 and N >= 128; the plan then picks whichever
+ * engine, tile width and split its measured stage costs make fastest.
+ * Returns CONV_OK, CONV_ERR_NULL (an output pointer is NULL), CONV_ERR_SHAPE
+ * (as matmul) or CONV_ERR_DEVICE. */
 int matmul_tiling(int32_t M, int32_t K, int32_t N, uint32_t flags, const float *A, const float *B,
                   int32_t *tile_cols, int32_t *k_pieces, int32_t *tma_fed);
 
