@@ -308,28 +308,45 @@ __global__ void __launch_bounds__(kS2dGatherThreads)
     griddep_wait();
     griddep_launch();
     const long long t = (long long)blockIdx.x * kS2dGatherThreads + threadIdx.x;
-    if (t >= total) return;
     const int Hs = int(f_hs.d), Ws = int(f_ws.d);
     if constexpr (BLOCKED) {
-        uint32_t r, ww, hh, cb, n;
-        f_ws.divmod(uint32_t(t), r, ww);
-        f_hs.divmod(r, r, hh);
-        f_mid.divmod(r, n, cb);
-        const int a0 = 4 * int(ww) - pad - OFF;   // aligned start of the segment's first float4
+        // The warp's 32 pixels pass through shared memory so that each store
+        // instruction writes four whole pixels (512 contiguous bytes) instead
+        // of one 16-byte piece of 32 pixels; the 16-byte slots are XOR-swizzled
+        // by pixel, so neither side has bank conflicts.
+        __shared__ float4 stage[kS2dGatherThreads * 8];
+        const int lane = int(threadIdx.x) & 31;
+        float4* wst = stage + (threadIdx.x - lane) * 8;
         float4 out[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int cp0 = int(cb) * 32 + 4 * j;   // channels cp0 .. cp0 + 3: b = 0..3 of one (c, a)
-            const int c = cp0 >> 4, a = (cp0 >> 2) & 3;
-            const int h = 4 * int(hh) + a - pad;
-            out[j] = (cp0 < Cs && unsigned(h) < unsigned(H))
-                         ? s2d_segment<OFF>(x + ((size_t(n) * C + c) * H + h) * W, a0, W)
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        float4* d = reinterpret_cast<float4*>(dst) + size_t(t) * 8;
+        for (int j = 0; j < 8; ++j) out[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (t < total) {
+            uint32_t r, ww, hh, cb, n;
+            f_ws.divmod(uint32_t(t), r, ww);
+            f_hs.divmod(r, r, hh);
+            f_mid.divmod(r, n, cb);
+            const int a0 = 4 * int(ww) - pad - OFF;   // aligned start of the segment's first float4
 #pragma unroll
-        for (int j = 0; j < 8; ++j) d[j] = out[j];
+            for (int j = 0; j < 8; ++j) {
+                const int cp0 = int(cb) * 32 + 4 * j;   // channels cp0 .. cp0 + 3: b = 0..3 of one (c, a)
+                const int c = cp0 >> 4, a = (cp0 >> 2) & 3;
+                const int h = 4 * int(hh) + a - pad;
+                if (cp0 < Cs && unsigned(h) < unsigned(H))
+                    out[j] = s2d_segment<OFF>(x + ((size_t(n) * C + c) * H + h) * W, a0, W);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) wst[lane * 8 + (j ^ (lane & 7))] = out[j];
+        __syncwarp();
+        const long long t0 = t - lane;   // the warp's first pixel
+        float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int px = 4 * i + (lane >> 3), j = lane & 7;
+            if (t0 + px < total) d[size_t(t0 + px) * 8 + j] = wst[px * 8 + (j ^ (px & 7))];
+        }
     } else {
+        if (t >= total) return;
         uint32_t r, ww, hh, a, c, n;
         f_ws.divmod(uint32_t(t), r, ww);
         f_hs.divmod(r, r, hh);

@@ -22,7 +22,11 @@
 
 namespace cb200 {
 
-template <int BN>
+// INTERIOR: no padding and every window inside the image ((P-1)*S + R <= H,
+// likewise along W), so the gather tests only the end of the reduction -- the
+// space-to-depth form of AlexNet conv1 (X' 57 x 57, 3 x 3 taps, 55 x 55
+// outputs).
+template <int BN, bool INTERIOR = false>
 struct ConvWgradProb {
     static constexpr bool kBBulk = true;
     int terms = 3;   // tensor-core products per K step: 3 (3xTF32) or 1 (TF32)
@@ -95,6 +99,24 @@ struct ConvWgradProb {
         // Pixels j0..j0+3 of this thread's chunk.
         const int j0 = ks * kBK + 4 * (tid & 7);
         int jbase[4], jh[4], jw[4];
+        if constexpr (INTERIOR) {
+            uint32_t n, pq, oh, ow;
+            f_pq.divmod(uint32_t(j0 < NPQ ? j0 : 0), n, pq);
+            f_q.divmod(pq, oh, ow);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                jbase[e] = j0 + e < NPQ ? int(n) * CHW + int(oh) * S * W + int(ow) * S : -1;
+                if (++ow == uint32_t(Q)) {
+                    ow = 0;
+                    if (++oh == uint32_t(P)) { oh = 0; ++n; }
+                }
+            }
+#pragma unroll
+            for (int p = 0; p < 8; ++p)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) v[4 * p + e] = ldg_keep_if(x + (jbase[e] + s.rowoff[p]), jbase[e] >= 0);
+            return;
+        }
         {
             uint32_t n, pq, oh, ow;
             f_pq.divmod(uint32_t(j0 < NPQ ? j0 : 0), n, pq);
@@ -381,11 +403,11 @@ size_t conv_wgrad_ws(const ConvDims& d)
 // form, whose rows are then orig's taps); ws: its image and partials.
 // With db non-null the G image pass also sums each row of G (the bias
 // gradient) into row-sum partials, added in block order by rowsum_final_kernel.
-template <int BN>
+template <int BN, bool INTERIOR = false>
 static cudaError_t run_wgrad(const ConvDims& d, const WgradPlan& pl, const float* x, const float* dy, float* dw,
                              void* ws, cudaStream_t st, const ConvDims* orig, float* db, const float* mask)
 {
-    ConvWgradProb<BN> p;
+    ConvWgradProb<BN, INTERIOR> p;
     p.terms = math_terms();
     const ConvDims& o = orig ? *orig : d;   // the convolution whose filter gradient is written
     float* img = static_cast<float*>(ws);
@@ -421,7 +443,7 @@ static cudaError_t run_wgrad(const ConvDims& d, const WgradPlan& pl, const float
         note_launch();
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    e = launch_tc_gemm<ConvWgradProb<BN>, BN>(p, p.m_tiles * p.n_tiles * p.splits, device_error_word(), st);
+    e = launch_tc_gemm<ConvWgradProb<BN, INTERIOR>, BN>(p, p.m_tiles * p.n_tiles * p.splits, device_error_word(), st);
     if (e != cudaSuccess) return e;
     if (pl.splits == 1) return e;
     const long long count = (long long)d.K * p.CRS;
@@ -450,9 +472,14 @@ cudaError_t launch_conv_wgrad(const ConvDims& d, const float* x, const float* dy
         xg = xs;
         gws = xs + xs2d_floats(d, w);
     }
+    // windows that never leave the image (no padding): the gather tests only
+    // the reduction's end (instantiated for the 64-wide tiles, AlexNet conv1)
+    const bool interior = g.pad == 0 && (g.P - 1) * g.S + g.R <= g.H && (g.Q - 1) * g.S + g.R <= g.W;
     switch (pl.bn) {
     case 32: return run_wgrad<32>(g, pl, xg, dy, dw, gws, st, orig, db, mask);
-    case 64: return run_wgrad<64>(g, pl, xg, dy, dw, gws, st, orig, db, mask);
+    case 64:
+        return interior ? run_wgrad<64, true>(g, pl, xg, dy, dw, gws, st, orig, db, mask)
+                        : run_wgrad<64>(g, pl, xg, dy, dw, gws, st, orig, db, mask);
     case 128: return run_wgrad<128>(g, pl, xg, dy, dw, gws, st, orig, db, mask);
     case 192: return run_wgrad<192>(g, pl, xg, dy, dw, gws, st, orig, db, mask);
     default: return run_wgrad<256>(g, pl, xg, dy, dw, gws, st, orig, db, mask);

@@ -1218,37 +1218,44 @@ cudaError_t launch_sgd(int64_t count, float lr, float clip, float* p, const floa
 
 // ---------------------------------------------------------------------------
 // Bias gradient: db[k] = sum over (n, oh, ow) of dy[n, k, oh, ow].
-// One cluster of CS CTAs per filter k (CS = 1..8, chosen per call from the
-// work per filter).  CTA r of the cluster sums the planes (n, k) of images
-// n = r, r + CS, ...: thread t takes elements t, t + 512, ... of that list of
-// planes, cycling over eight accumulators (eight loads in flight); the
-// position in the list is advanced incrementally, without divisions.  The
-// accumulators, the warp lanes, the warps and finally the cluster's CTAs (read
-// through distributed shared memory by CTA 0) are combined in fixed orders,
-// so the result is deterministic; no atomics.
+// One cluster of CS CTAs (T threads each) per filter k.  CTA r of the cluster
+// sums the planes (n, k) of images n = r, r + CS, ...: thread t takes elements
+// t, t + T, ... of that list of planes, sixteen loads in flight at a time,
+// into four accumulators; the position in the list is advanced incrementally,
+// without divisions.  The accumulators, the warp lanes, the warps and finally
+// the cluster's CTAs (read through distributed shared memory by CTA 0) are
+// combined in fixed orders, so the result is deterministic; no atomics.
+// (T, CS) are chosen per call so that the grid is about one wave of resident
+// CTAs: a call on small planes (13 x 13) moves only 22-33 MB, and a second,
+// partial wave of short CTAs cost as much as the first.
 
-constexpr int kBiasThreads = 512;
+constexpr int kBiasMaxThreads = 512;
 constexpr int kBiasMaxCluster = 8;
+constexpr int kBiasBatch = 16;   // loads in flight per thread
 
-__global__ void __launch_bounds__(kBiasThreads, 4)
+__global__ void __launch_bounds__(kBiasMaxThreads, 3)
     bias_grad_kernel(const float* __restrict__ dy, float* __restrict__ db, int N, int K, int PQ)
 {
     cg::cluster_group cluster = cg::this_cluster();
-    __shared__ float warp_part[kBiasThreads / 32];
+    __shared__ float warp_part[kBiasMaxThreads / 32];
     __shared__ float cta_part;
+    griddep_wait();
+    griddep_launch();
+    const int T = int(blockDim.x);
     const int cs = int(cluster.num_blocks());
     const int rank = int(cluster.block_rank());
     const int k = blockIdx.x / cs;
     const int images = (N - rank + cs - 1) / cs;          // planes this CTA sums
     const int img_stride = cs * K * PQ;                   // elements between its consecutive planes
-    const int step_n = kBiasThreads / PQ, step_e = kBiasThreads % PQ;
+    const int step_n = T / PQ, step_e = T % PQ;
     int nl = int(threadIdx.x) / PQ, e = int(threadIdx.x) % PQ;
     unsigned off = unsigned((rank * K + k) * PQ + nl * img_stride + e);   // may run past the end once nl >= images: never loaded
-    float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float part[4] = {0.f, 0.f, 0.f, 0.f};
     while (nl < images) {
+        float v[kBiasBatch];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            if (nl < images) part[u] += __ldg(dy + off);
+        for (int u = 0; u < kBiasBatch; ++u) {
+            v[u] = nl < images ? __ldg(dy + off) : 0.f;
             nl += step_n;
             e += step_e;
             off += unsigned(step_n * img_stride + step_e);
@@ -1258,17 +1265,21 @@ __global__ void __launch_bounds__(kBiasThreads, 4)
                 off += unsigned(img_stride - PQ);
             }
         }
+#pragma unroll
+        for (int u = 0; u < kBiasBatch; ++u) part[u & 3] += v[u];
     }
-    float acc = ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
+    float acc = (part[0] + part[1]) + (part[2] + part[3]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
     if ((threadIdx.x & 31) == 0) warp_part[threadIdx.x >> 5] = acc;
     __syncthreads();
     if (threadIdx.x == 0) {
         float t = 0.f;
-        for (int i = 0; i < kBiasThreads / 32; ++i) t += warp_part[i];
+        for (int i = 0; i < T / 32; ++i) t += warp_part[i];
         cta_part = t;
+        if (cs == 1) db[k] = t;   // launched without a cluster
     }
+    if (cs == 1) return;
     cluster.sync();
     if (rank == 0 && threadIdx.x == 0) {
         float t = 0.f;
@@ -1278,29 +1289,65 @@ __global__ void __launch_bounds__(kBiasThreads, 4)
     cluster.sync();   // keep every CTA's shared memory alive until rank 0 has read it
 }
 
+// CTAs of `threads` threads of bias_grad_kernel resident on the GPU at once.
+static int bias_resident(int threads)
+{
+    static std::atomic<int> cached[2] = {0, 0};
+    std::atomic<int>& c = cached[threads == kBiasMaxThreads ? 1 : 0];
+    int r = c.load();
+    if (r > 0) return r;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bias_grad_kernel, threads, 0) != cudaSuccess ||
+        per_sm < 1) {
+        cudaGetLastError();
+        per_sm = (2048 / threads) / 2;
+    }
+    r = per_sm * sm_count();
+    c.store(r);
+    return r;
+}
+
+struct BiasPlan {
+    int threads, cluster;
+};
+
+// Of 512- and 256-thread CTAs, the (threads, cluster size) whose grid fills
+// its last wave of resident CTAs best (ties to 512); a cluster is at most 8
+// CTAs, at most one per image, and no larger than gives each thread 8
+// elements.  AlexNet batch 128: conv1 (64 filters, 55 x 55) 512 x 8; conv2
+// (192, 27 x 27) 512 x 3; conv3 (384, 13 x 13) 256 x 3; conv4/5 (256) 512 x 2.
+static BiasPlan plan_bias(const ConvDims& d)
+{
+    const long long per_k = (long long)d.N * d.P * d.Q;
+    BiasPlan best{kBiasMaxThreads, 1};
+    double best_fill = -1.0;
+    for (int threads : {kBiasMaxThreads, kBiasMaxThreads / 2}) {
+        const long long resident = bias_resident(threads);
+        long long cs = resident / d.K;
+        const long long by_work = per_k / (8LL * threads);
+        if (cs > by_work) cs = by_work;
+        if (cs > kBiasMaxCluster) cs = kBiasMaxCluster;
+        if (cs > d.N) cs = d.N;
+        if (cs < 1) cs = 1;
+        const long long ctas = (long long)d.K * cs;
+        const long long waves = (ctas + resident - 1) / resident;
+        const double fill = double(ctas) / double(waves * resident);
+        if (fill > best_fill + 1e-9) {
+            best_fill = fill;
+            best = BiasPlan{threads, int(cs)};
+        }
+    }
+    return best;
+}
+
 cudaError_t launch_bias_grad(const ConvDims& d, const float* dy, float* db, cudaStream_t st)
 {
-    // about 16 elements per thread per CTA, at most 8 CTAs per filter
-    const long long per_k = (long long)d.N * d.P * d.Q;
-    long long cs = (per_k + 16LL * kBiasThreads - 1) / (16LL * kBiasThreads);
-    if (cs > kBiasMaxCluster) cs = kBiasMaxCluster;
-    if (cs > d.N) cs = d.N;
-    if (cs < 1) cs = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(d.K * cs));
-    cfg.blockDim = dim3(kBiasThreads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = unsigned(cs);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, bias_grad_kernel, dy, db, d.N, d.K, d.P * d.Q);
+    const BiasPlan bp = plan_bias(d);
+    cudaError_t e = launch_pdl_cluster(bias_grad_kernel, dim3(unsigned(d.K * bp.cluster)), dim3(unsigned(bp.threads)), 0,
+                                       st, bp.cluster, dy, db, d.N, d.K, d.P * d.Q);
+    if (e != cudaSuccess) return e;
     note_launch();
-    return e;
+    return cudaGetLastError();
 }
 
 }  // namespace cb200
