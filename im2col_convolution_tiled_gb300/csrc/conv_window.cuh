@@ -171,7 +171,11 @@ struct ConvGatherProb {
             const int cleft = g.Ci - int(chunk) * 32;   // channels of this chunk that exist
             const int off = s.base + int(chunk) * 32 * g.HiWi + int(tr) * g.Wi + int(tq);
             const float* p = g.in + off;
-            if (g.mask == nullptr) {
+            if (g.mask == nullptr && cleft >= 32) {
+                // a whole chunk: one predicate for all 32 loads
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = ldg_keep_if(p + i * g.HiWi, ok);
+            } else if (g.mask == nullptr) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = ldg_keep_if(p + i * g.HiWi, ok && i < cleft);
             } else {
