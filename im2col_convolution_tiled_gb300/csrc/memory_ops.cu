@@ -797,6 +797,7 @@ __global__ void __launch_bounds__(kPoolThreads, 3) maxpool_bwd_staged_kernel(
 // along a row.
 constexpr int kWalkThreads = 256;
 constexpr int kWalkChunk = 4;
+constexpr int kFwdWalkChunk = 8;   // the forward walk is load-latency bound: more windows' rows in flight
 
 // Forward: window oh combines the first maxima of its K input rows
 // (rows oh*S .. oh*S + K - 1, each the first maximum over its K columns);
@@ -838,18 +839,18 @@ __global__ void __launch_bounds__(kWalkThreads) maxpool_fwd_walk_kernel(
     }
     float* yo = y + size_t(plane) * P * Q + ow;
     int32_t* io = idx + size_t(plane) * P * Q + ow;
-    for (int oh = oh0; oh < oh1; oh += kWalkChunk) {
-        // rows oh*S + K - S + u, u < kWalkChunk*S: the S new rows of each window of the chunk
-        float v[kWalkChunk * S][K];
+    for (int oh = oh0; oh < oh1; oh += kFwdWalkChunk) {
+        // rows oh*S + K - S + u, u < kFwdWalkChunk*S: the S new rows of each window of the chunk
+        float v[kFwdWalkChunk * S][K];
 #pragma unroll
-        for (int u = 0; u < kWalkChunk * S; ++u)
+        for (int u = 0; u < kFwdWalkChunk * S; ++u)
             if (oh + u / S < oh1) {
                 const int at = col0 + (oh * S + K - S + u) * W;
 #pragma unroll
                 for (int c = 0; c < K; ++c) v[u][c] = __ldg(x + at + c);
             }
 #pragma unroll
-        for (int i = 0; i < kWalkChunk; ++i) {
+        for (int i = 0; i < kFwdWalkChunk; ++i) {
             if (oh + i >= oh1) break;
 #pragma unroll
             for (int r = 0; r < S; ++r) {
